@@ -1,0 +1,244 @@
+/*
+ * v4a.h - C ABI of libv4a, a GB300 (sm_103a) implementation of the
+ * DeepSeek-V4-style compressed sparse attention layer (c4a / c128a) in
+ * decode and chunked prefill.
+ *
+ * Source of the method: "DeepSeek V4 in vLLM: Efficient Long-context
+ * Attention" (vLLM blog, April 2026), sections Background (shared K=V,
+ * compression, sparse attention, sliding window), Method details (single
+ * logical block size, compressor state as a sliding window, kernel fusions)
+ * and Appendix (inverse RoPE, exact position ranges and causality, values of
+ * k, why the short window).  Byte layouts of the fp8 indexer entry follow the
+ * SGLang KV-pool article, section "DSA".
+ *
+ * General rules for every entry point:
+ *  - All pointers inside the argument structs are DEVICE pointers unless a
+ *    field says otherwise; the structs themselves live in host memory and are
+ *    read only during the call.
+ *  - The caller owns and allocates every buffer (caches, rings, block tables,
+ *    inputs, outputs, workspace).  The library never allocates or frees device
+ *    memory, never synchronises, and launches only on the given stream
+ *    (a cudaStream_t passed as void*; NULL = legacy default stream).
+ *  - Calls are ordered by the stream: compress_insert -> index_topk ->
+ *    sparse_attn -> inv_rope_quant.
+ *  - A nonzero return code means nothing was launched, except V4A_ERR_CUDA,
+ *    which reports a launch failure.  Problems that only the device can see
+ *    (an unallocated block, a bad index) are OR-ed into the optional device
+ *    word `status` as V4A_DEV_* bits; the offending read or write is skipped.
+ *    No kernel traps and no kernel waits on another.
+ *  - bf16 tensors are passed as uint16_t bit patterns; fp8 is OCP e4m3fn,
+ *    fp4 is OCP e2m1 (element 2j in the low nibble of byte j).
+ */
+#ifndef V4A_H
+#define V4A_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define V4A_ABI_VERSION 1
+
+/* ---- host return codes ---------------------------------------------------- */
+#define V4A_OK                 0
+#define V4A_ERR_INVALID_ARG    1  /* null pointer, bad size, bad enum */
+#define V4A_ERR_UNSUPPORTED    2  /* valid but not implemented (dim, heads, format pairing) */
+#define V4A_ERR_RING_TOO_SMALL 3  /* ring capacity < window - 1 + max_new_per_seq */
+#define V4A_ERR_WORKSPACE      4  /* workspace missing or smaller than *_workspace_size */
+#define V4A_ERR_CUDA           5  /* a kernel launch failed */
+
+/* ---- device status bits (OR-ed into *status when status != NULL) ---------- */
+#define V4A_DEV_BAD_BLOCK  1  /* a needed block-table entry is < 0 or >= num_blocks */
+#define V4A_DEV_BAD_BATCH  2  /* seq id out of range, positions not consecutive in a
+                                 sequence's run, or a run longer than max_new_per_seq */
+#define V4A_DEV_BAD_INDEX  4  /* a selected entry index is >= the visible count */
+
+/* ---- formats ---------------------------------------------------------------- */
+/* Shared-K=V cache and window ring rows. */
+#define V4A_KV_BF16       0  /* row = dim bf16 */
+#define V4A_KV_FP8_TOKEN  1  /* row = dim e4m3 codes; one fp32 scale per row (amax/448) */
+/* Indexer key cache rows. */
+#define V4A_IX_BF16       0  /* row = dim bf16 */
+#define V4A_IX_FP8_B128   1  /* row = dim e4m3; one fp32 scale per 128 elements (132 B at dim 128) */
+#define V4A_IX_FP4_B32    2  /* row = dim/2 bytes e2m1; one fp32 scale per 32 elements */
+/* Indexer query. */
+#define V4A_Q_BF16        0  /* [T][H_I][dim] bf16 */
+#define V4A_Q_FP8_HEAD    1  /* [T][H_I][dim] e4m3 + [T][H_I] fp32 scale */
+/* Output of the inverse-RoPE stage. */
+#define V4A_OUT_BF16      0
+#define V4A_OUT_FP8_TOKEN 1  /* e4m3 codes + one fp32 scale per token over H*dim (amax/448) */
+
+/*
+ * Ragged batch of new tokens.  Token t belongs to sequence seq_ids[t] and sits
+ * at absolute 0-based position positions[t].  The tokens of one sequence are
+ * contiguous in t and at consecutive increasing positions.  In decode each
+ * sequence has one token; in chunked prefill a sequence has up to
+ * max_new_per_seq tokens.  The same tokens are the queries of the step.
+ */
+typedef struct {
+  int32_t num_tokens;          /* T >= 0 */
+  const int32_t* seq_ids;      /* [T], each in [0, num_seqs) */
+  const int32_t* positions;    /* [T] */
+  int32_t num_seqs;            /* B: rows of every block table and ring */
+  int32_t max_new_per_seq;     /* host-side bound on one sequence's tokens in this call */
+} v4a_batch;
+
+/*
+ * A paged compressed cache ("a single logical block size": every physical
+ * block covers 256 native positions, i.e. 256/ratio entries).  Entry i of
+ * sequence b lives in physical block block_table[b][i / E], slot i % E, with
+ * E = 256/ratio.  Inside a block all data rows come first ([E][row bytes]),
+ * then the fp32 scale words ([E][scales per row]) if the format has any.
+ * Block bytes:  KV_BF16 E*dim*2;  KV_FP8_TOKEN E*(dim+4);
+ *               IX_BF16 64*dim*2;  IX_FP8_B128 64*(dim + 4*dim/128);
+ *               IX_FP4_B32 64*(dim/2 + 4*dim/32).
+ */
+typedef struct {
+  int32_t ratio;               /* 4 (c4a) or 128 (c128a); indexer caches use 4 */
+  int32_t dim;                 /* row length in elements */
+  int32_t rope_dims;           /* the last rope_dims dims are rotated (interleaved pairs) */
+  float rope_theta;            /* base of the rotary frequencies */
+  int32_t format;              /* V4A_KV_* or V4A_IX_* */
+  void* pool;                  /* num_blocks * block bytes */
+  int64_t num_blocks;
+  const int32_t* block_table;  /* [num_seqs][max_blocks]; -1 = unallocated */
+  int32_t max_blocks;
+} v4a_cache;
+
+/*
+ * One compressor (the main KV compressor or the indexer's own).  For token t
+ * at position P with (P+1) % ratio == 0 it emits entry i = (P+1)/ratio - 1 over
+ * the native positions [4i-4, 4i+3] (c4a; positions < 0 take no weight) or
+ * [128i, 128i+127] (c128a):  w = softmax_j(gate[p_j] + bias[j]),
+ * c = sum_j w_j x[p_j], c <- c / sqrt(mean(c^2) + eps) * gamma, RoPE at the
+ * anchor P, encode, store at the entry's slot.  Every new token's (x, gate) is
+ * also stored in the ring at slot P % ring_cap; positions older than the
+ * call's first token of that sequence are read from the ring.
+ */
+typedef struct {
+  v4a_cache cache;             /* destination */
+  const uint16_t* x;           /* [T][cache.dim] bf16 */
+  const float* gate;           /* [T] */
+  const float* bias;           /* [8] (c4a) or [128] (c128a) */
+  const float* gamma;          /* [cache.dim] */
+  float eps;                   /* RMSNorm epsilon (1e-6) */
+  uint16_t* ring_x;            /* [num_seqs][ring_cap][cache.dim] bf16 */
+  float* ring_gate;            /* [num_seqs][ring_cap] */
+  int32_t ring_cap;            /* >= window - 1 + max_new_per_seq (window 8 or 128) */
+} v4a_compressor;
+
+/* Uncompressed sliding-window keys: k[t] rotated at P, encoded, stored at
+ * ring[seq][P % ring_cap]. */
+typedef struct {
+  const uint16_t* k;           /* [T][dim] bf16 (normalised upstream) */
+  int32_t dim, rope_dims;
+  float rope_theta;
+  int32_t format;              /* V4A_KV_BF16 or V4A_KV_FP8_TOKEN */
+  void* ring;                  /* [num_seqs][ring_cap][dim] bf16 or e4m3 */
+  float* ring_scale;           /* [num_seqs][ring_cap] (fp8 only) */
+  int32_t ring_cap;            /* >= 127 + max_new_per_seq */
+} v4a_window;
+
+typedef struct {
+  v4a_batch batch;
+  const v4a_compressor* main;     /* host pointer; may be NULL */
+  const v4a_compressor* indexer;  /* host pointer; may be NULL (c128a layers) */
+  const v4a_window* window;       /* host pointer; may be NULL */
+  int32_t* status;                /* optional device word */
+} v4a_compress_args;
+
+/*
+ * Fused compressor + RMSNorm + RoPE + cache insert for the main and indexer
+ * caches, and RoPE + insert of the window keys (vLLM page, Method details,
+ * fusions (1) and (3); appendix "exact position ranges and causality").
+ * One launch.  Returns V4A_ERR_RING_TOO_SMALL when a ring cannot hold the
+ * call's tokens without overwriting positions a window still reads.
+ */
+int v4a_compress_insert(const v4a_compress_args* args, void* stream);
+
+/*
+ * Indexer scoring and top-k (vLLM page, Background "DeepSeek Sparse
+ * Attention"; appendix "values of k").  For query t at position m:
+ *   score_i = sum_h weights[t][h] * ReLU(q_h . key_i),  i < (m+1)/4,
+ * with q_h = q[t][h] (* q_scale[t][h] for fp8) and key_i the decoded indexer
+ * entry.  out_idx[t] receives the k entries with the largest scores (ties to
+ * the lower index) in ascending order, padded with -1 when fewer than k are
+ * visible.
+ */
+typedef struct {
+  v4a_batch batch;
+  v4a_cache keys;              /* indexer cache, ratio 4 */
+  int32_t num_heads;           /* H_I */
+  int32_t q_format;            /* V4A_Q_BF16 (with IX_BF16 keys) or V4A_Q_FP8_HEAD */
+  const void* q;               /* [T][H_I][keys.dim] */
+  const float* q_scale;        /* [T][H_I] (fp8 query only) */
+  const float* weights;        /* [T][H_I] */
+  int32_t k;                   /* 1 <= k <= 16384 */
+  int32_t* out_idx;            /* [T][k] */
+  int32_t* status;
+} v4a_index_args;
+
+size_t v4a_index_workspace_size(const v4a_index_args* args);
+int v4a_index_topk(const v4a_index_args* args, void* workspace, size_t workspace_bytes,
+                   void* stream);
+
+/*
+ * Sparse attention with shared K=V (vLLM page, Background and appendix "why
+ * inverse RoPE").  For query t at position m and head h, over the keys
+ *   S = {selected compressed entries} U {window tokens max(0,m-W+1) .. m}:
+ *   z_n = softmax_scale * q_h . k_n,  o_h = sum_n softmax(z)_n k_n.
+ * idx == NULL selects every visible entry i < (m+1)/ratio (c128a layers).
+ * Entries of idx that are -1 are skipped.  out is bf16; lse (optional) is the
+ * natural-log sum of exp(z) per (t, h).
+ */
+typedef struct {
+  v4a_batch batch;
+  v4a_cache kv;                /* main compressed cache */
+  const int32_t* idx;          /* [T][k] or NULL */
+  int32_t k;
+  const void* window;          /* [num_seqs][window_cap][kv.dim] */
+  const float* window_scale;   /* [num_seqs][window_cap] (fp8 window only) */
+  int32_t window_cap;
+  int32_t window_format;       /* V4A_KV_* */
+  int32_t window_len;          /* 128 */
+  int32_t num_heads;           /* H */
+  const uint16_t* q;           /* [T][H][kv.dim] bf16, already rotated */
+  float softmax_scale;         /* 1/sqrt(dim) */
+  uint16_t* out;               /* [T][H][kv.dim] bf16 */
+  float* lse;                  /* [T][H] or NULL */
+  int32_t* status;
+} v4a_attn_args;
+
+size_t v4a_attn_workspace_size(const v4a_attn_args* args);
+int v4a_sparse_attn(const v4a_attn_args* args, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
+/*
+ * Inverse RoPE on the attention output, fused with fp8 quantisation (vLLM
+ * page, Method details, fusion (2); appendix "why inverse RoPE"):
+ * out[t][h] = R_{-m} in[t][h] on the last rope_dims dims, m = positions[t];
+ * for V4A_OUT_FP8_TOKEN one scale per token, amax over all heads and dims / 448.
+ */
+typedef struct {
+  int32_t num_tokens;
+  const int32_t* positions;    /* [T] */
+  int32_t num_heads, dim, rope_dims;
+  float rope_theta;
+  const uint16_t* in;          /* [T][H][dim] bf16 */
+  int32_t out_format;          /* V4A_OUT_* */
+  void* out;                   /* [T][H][dim] bf16 or e4m3 */
+  float* out_scale;            /* [T] (fp8 only) */
+} v4a_output_args;
+
+int v4a_inv_rope_quant(const v4a_output_args* args, void* stream);
+
+/* Human-readable text of a V4A_* return code. */
+const char* v4a_status_string(int code);
+int v4a_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* V4A_H */

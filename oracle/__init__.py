@@ -1,0 +1,28 @@
+"""fp64 CPU oracle for the DeepSeek-V4-style compressed sparse attention layer.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path may import this
+package: only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` use it.  It shares
+no code with the CUDA library (no kernels, headers, tables or helpers) and it
+imports nothing from ``compressed_sparse_long_c4a_gb300``.
+
+Every function is a plain, slow, obviously-correct restatement of the method
+described on the page "DeepSeek V4 in vLLM: Efficient Long-context Attention"
+(vLLM blog, April 2026), computed in float64 with numpy.  Each module header
+says which passage it follows and which readings it takes where the page is
+silent.
+
+Pinning status (what each part is checked against, in ``tests/``):
+  formats     - exhaustive codec checks against torch.float8_e4m3fn and the
+                OCP e2m1 value table; bf16 against torch.bfloat16.
+  geometry    - closed forms for counts/windows/causality, brute-force
+                enumeration of slot mapping.
+  compressor  - closed forms (equal logits -> mean, dominant logit -> copy,
+                RMS = 1), RoPE group identities, chunk == step.
+  indexer     - brute-force sort on tiny inputs, all-tie rule.
+  attention   - dense special case against torch fp64 softmax + matmul,
+                SWA coverage, translation invariance after inverse RoPE.
+  kvbytes     - the page's 9.62 GiB / 83.9 GiB / 8.7x figures.
+  Absolute attention values on general inputs: parity unpinned beyond the
+  above (the page prints no worked numerical example).
+"""

@@ -1,0 +1,156 @@
+"""Pins of the oracle's number formats against library casts and the OCP tables."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import formats as F
+
+
+def test_e4m3_decode_matches_torch_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = F.e4m3_decode(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert set(np.nonzero(nan)[0].tolist()) == {0x7F, 0xFF}
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert ours[0x7E] == 448.0 and ours[0x01] == 2.0 ** -9
+
+
+def _e4m3_probe_values():
+    pos = F.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+    mids = (pos[1:] + pos[:-1]) / 2
+    rng = np.random.default_rng(0)
+    rand = rng.standard_normal(20000) * rng.choice([1e-3, 0.1, 1, 30, 200], 20000)
+    v = np.concatenate([pos, mids, mids * (1 + 1e-9), mids * (1 - 1e-9), rand])
+    v = v[np.abs(v) <= 448]
+    return np.concatenate([v, -v])
+
+
+def test_e4m3_encode_matches_torch_cast():
+    v = _e4m3_probe_values().astype(np.float32).astype(np.float64)  # torch casts from fp32
+    ours = F.e4m3_decode(F.e4m3_encode(v))
+    ref = torch.from_numpy(v).to(torch.float32).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(ours, ref)
+
+
+def test_e4m3_saturates_and_roundtrips():
+    assert F.e4m3_decode(F.e4m3_encode(np.array([1e6, -500.0, 470.0])).tolist()).tolist() == [448.0, -448.0, 448.0]
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    back = F.e4m3_encode(F.e4m3_decode(codes))
+    # +0 and -0 both decode to 0; everything else round-trips exactly
+    assert np.array_equal(F.e4m3_decode(back), F.e4m3_decode(codes))
+    assert np.array_equal(back[codes != 0x80], codes[codes != 0x80])
+
+
+OCP_E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e2m1_decode_is_ocp_table():
+    vals = F.e2m1_decode(np.arange(16))
+    assert vals[:8].tolist() == OCP_E2M1
+    assert (-vals[8:]).tolist() == OCP_E2M1
+
+
+def test_e2m1_encode_nearest_even_brute_force():
+    table = np.array(OCP_E2M1)
+    rng = np.random.default_rng(1)
+    mids = (table[1:] + table[:-1]) / 2
+    v = np.concatenate([table, mids, rng.uniform(-7, 7, 5000), [6.5, 100.0]])
+    for x in v:
+        mag = min(abs(x), 6.0)
+        d = np.abs(table - mag)
+        best = np.nonzero(d == d.min())[0]
+        code = best[0] if len(best) == 1 else [c for c in best if c % 2 == 0][0]
+        got = int(F.e2m1_encode(np.array([x]))[0])
+        assert got & 7 == code, (x, got, code)
+        assert (got >> 3) == (1 if np.signbit(x) else 0)
+    # ties printed explicitly: 0.25->0, 0.75->1, 1.25->1, 2.5->2, 5->4
+    assert F.e2m1_decode(F.e2m1_encode(np.array([0.25, 0.75, 1.25, 2.5, 5.0]))).tolist() == [0, 1, 1, 2, 4]
+
+
+def test_bf16_encode_matches_torch_on_fp32_and_brute_force_on_fp64():
+    rng = np.random.default_rng(2)
+    v32 = np.concatenate([rng.standard_normal(20000) * 10 ** rng.uniform(-30, 30, 20000),
+                          [0.0, -0.0, 1.0, 3.0e38, 1e-40]]).astype(np.float32)
+    ours = F.bf16_encode(v32.astype(np.float64))
+    ref = torch.from_numpy(v32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+    v64 = rng.standard_normal(2000) * 10 ** rng.uniform(-5, 5, 2000)
+    for x in v64:
+        b = int(F.bf16_encode(np.array([x]))[0])
+        lo = F.bf16_decode(np.array([b - 1], np.uint16))[0]
+        hi = F.bf16_decode(np.array([b + 1], np.uint16))[0]
+        mid = F.bf16_decode(np.array([b], np.uint16))[0]
+        assert abs(mid - x) <= abs(lo - x) and abs(mid - x) <= abs(hi - x)
+
+
+def test_fp8_token_quant_scale_rule_and_error():
+    rng = np.random.default_rng(3)
+    v = rng.standard_normal(512)
+    codes, s = F.fp8_token_encode(v)
+    assert s == pytest.approx(np.max(np.abs(v)) / 448, rel=1e-7)
+    dq = F.e4m3_decode(codes) * s
+    assert np.all(np.abs(dq - v) <= 0.5 * F.e4m3_ulp(v / s) * s * (1 + 1e-6) + 1e-12)
+    assert np.max(np.abs(F.e4m3_decode(codes))) == 448.0
+    z, s0 = F.fp8_token_encode(np.zeros(8))
+    assert s0 == 1.0 and np.all(z == 0)
+
+
+def test_fp4_blocks_quant_and_nibble_order():
+    rng = np.random.default_rng(4)
+    v = rng.standard_normal(128)
+    packed, sc = F.fp4_blocks_encode(v, 32)
+    assert packed.shape == (64,) and sc.shape == (4,)
+    for b in range(4):
+        assert sc[b] == pytest.approx(np.max(np.abs(v[32 * b:32 * b + 32])) / 6, rel=1e-7)
+    nib = F.unpack_nibbles(packed)
+    assert np.array_equal(nib[0::2], packed & 0xF)   # element 2j in the low nibble
+    assert np.array_equal(F.pack_nibbles(nib), packed)
+    dq = F.e2m1_decode(nib) * np.repeat(sc, 32)
+    assert np.all(np.abs(dq - v) <= 0.5 * F.e2m1_ulp(v / np.repeat(sc, 32)) * np.repeat(sc, 32) + 1e-12)
+
+
+def test_block_layout_bytes_and_decode():
+    assert F.ix_block_bytes(F.IX_FP8_B128, 128) == 64 * 132          # 132 B per entry
+    assert F.ix_block_bytes(F.IX_FP4_B32, 128) == 64 * 80            # 64 B + 4 scales
+    assert F.kv_block_bytes(F.KV_FP8_TOKEN, 64, 512) == 64 * 516
+    assert F.kv_block_bytes(F.KV_BF16, 2, 512) == 2048
+    rng = np.random.default_rng(5)
+    rows = rng.standard_normal((64, 128))
+    raw = np.zeros(F.ix_block_bytes(F.IX_FP8_B128, 128), np.uint8)
+    expect = np.zeros((64, 128))
+    for e in range(64):
+        c, s = F.fp8_blocks_encode(rows[e], 128)
+        raw[e * 128:(e + 1) * 128] = c
+        raw[64 * 128 + 4 * e: 64 * 128 + 4 * e + 4] = np.array(s, np.float32).view(np.uint8)
+        expect[e] = F.e4m3_decode(c) * s[0]
+    assert np.array_equal(F.ix_block_decode(raw, F.IX_FP8_B128, 128), expect)
+
+
+def test_nibble_order_hand_bytes():
+    # byte 0x21 holds element 0 = code 1 (0.5) and element 1 = code 2 (1.0);
+    # byte 0xF8 holds element 2 = code 8 (-0) and element 3 = code 15 (-6)
+    nib = F.unpack_nibbles(np.array([0x21, 0xF8], np.uint8))
+    assert nib.tolist() == [1, 2, 8, 15]
+    assert F.e2m1_decode(nib).tolist() == [0.5, 1.0, -0.0, -6.0]
+
+
+def test_kv_fp8_and_ix_fp4_block_decode_apply_scales():
+    E, D = 64, 512
+    raw = np.zeros(F.kv_block_bytes(F.KV_FP8_TOKEN, E, D), np.uint8)
+    raw[0] = 0x38                      # e4m3 1.0 at entry 0, dim 0
+    raw[D * 5 + 7] = 0xC0              # e4m3 -2.0 at entry 5, dim 7
+    sc = np.ones(E, np.float32)
+    sc[0], sc[5] = 0.25, 3.0
+    raw[E * D:] = sc.view(np.uint8)
+    dec = F.kv_block_decode(raw, F.KV_FP8_TOKEN, E, D)
+    assert dec[0, 0] == 0.25 and dec[5, 7] == -6.0 and dec.sum() == 0.25 - 6.0
+    dI = 128
+    raw = np.zeros(F.ix_block_bytes(F.IX_FP4_B32, dI), np.uint8)
+    raw[3 * 64 + 20] = 0x70            # entry 3: element 40 = 0 (low), element 41 = code 7 (6.0)
+    s4 = np.ones((64, 4), np.float32)
+    s4[3, 1] = 0.5                     # elements 32..63 of entry 3
+    raw[64 * 64:] = s4.reshape(-1).view(np.uint8)
+    dec = F.ix_block_decode(raw, F.IX_FP4_B32, dI)
+    assert dec[3, 41] == 3.0 and np.count_nonzero(dec) == 1
