@@ -1,0 +1,403 @@
+"""Benchmark of one compressed sparse attention layer step on GB300.
+
+Default workload: c4a decode at 1M context, batch 4 (m = 1,048,575; 262,144
+visible entries per query), fp8 attention/window caches, fp4 indexer cache,
+128 heads x 512, k = 2048, window 128, fp8 output.  A step is the whole
+path: compress+insert (main, indexer, window) -> indexer scores -> top-k ->
+sparse attention (+ combine) -> inverse RoPE + fp8 quant.
+
+Prints one JSON line.  `value` = decode tokens/s with inputs resident in HBM,
+timed with CUDA events over K CUDA-graph replays that rotate over enough layer
+replicas (distinct caches) that the bytes a step touches never come from L2;
+`e2e` = the same metric with the step's inputs copied from pinned host memory
+and its output copied back inside the timed region.  `roofline` reports the
+dominant kernel (the indexer scan) against the measured HBM copy bandwidth.
+
+--impl reference times the fp64 CPU oracle on the same workload (a bounded
+sample per step, stated in the line) on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode tokens/s & µs/layer for c4a sparse attention at 1M ctx; % HBM roofline"
+L2_BYTES = 126 * 2 ** 20
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1917.5)), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def algorithmic_bytes(spec):
+    """Indexer-key scan + gathered top-k entries + window tokens, per step."""
+    import compressed_sparse_long_c4a_gb300.inputs as I
+    row = spec.dim * 2 if spec.kv_fmt == I.KV_BF16 else spec.dim + 4
+    wrow = spec.dim * 2 if spec.swa_fmt == I.KV_BF16 else spec.dim + 4
+    ix_row = spec.ix_block_bytes // 64 if spec.ix_heads else 0
+    scan = gather = win = 0
+    for b in range(spec.batch):
+        for j in range(spec.new):
+            m = spec.cached[b] + j
+            n = (m + 1) // spec.ratio
+            scan += n * ix_row if spec.ix_heads else 0
+            gather += (min(spec.topk, n) if spec.topk else n) * row
+            win += min(spec.swa, m + 1) * wrow
+    return scan, gather, win
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"v4a_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if not self.proc or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def oracle_token(case, t, frac=1.0):
+    """Runs the fp64 oracle's full step for query t of `case`; with frac < 1
+    the query is moved back so it sees frac of its entries (same caches)."""
+    import dataclasses
+    import numpy as np
+    from tests import oracle_bridge as OB
+    from compressed_sparse_long_c4a_gb300 import inputs as I
+    c = case
+    if frac < 1.0:
+        n = int((case.positions[t].item() + 1) // case.spec.ratio * frac)
+        m = case.spec.ratio * max(n, 1) - 1
+        pos = case.positions.clone()
+        pos[t] = m
+        c = dataclasses.replace(case, positions=pos)
+    sub = dataclasses.replace(
+        c, seq_ids=c.seq_ids[t:t + 1], positions=c.positions[t:t + 1], x=c.x[t:t + 1],
+        gate=c.gate[t:t + 1], k_swa=c.k_swa[t:t + 1], q=c.q[t:t + 1],
+        x_i=None if c.x_i is None else c.x_i[t:t + 1], gate_i=None if c.gate_i is None else c.gate_i[t:t + 1],
+        q_i=None if c.q_i is None else c.q_i[t:t + 1],
+        q_i_scale=None if c.q_i_scale is None else c.q_i_scale[t:t + 1],
+        w_i=None if c.w_i is None else c.w_i[t:t + 1],
+        spec=dataclasses.replace(c.spec, new=1))
+    main, ix, swa = OB.oracle_compress(sub)
+    kv, ixp, ring, rsc = OB.oracle_state_after_compress(sub, main, ix, swa)
+    idx = None
+    if sub.spec.ix_heads:
+        idx, _ = OB.oracle_index(sub, ixp)
+    att = OB.oracle_attention(sub, kv, ring, rsc, idx)
+    o = np.stack([att[0][0]])
+    from oracle import formats as F
+    OB.oracle_output(sub, F.bf16_encode(o))
+
+
+def cpu_cores():
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(v):
+            return int(os.environ[v])
+    return os.cpu_count() or 1
+
+
+def run_reference(args, spec, case):
+    """The oracle as the reference arm: K timed steps of one sampled query each."""
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return None
+    # size the per-step sample so that W + K steps take about two minutes
+    t0 = time.perf_counter()
+    oracle_token(case, 0, 0.05)
+    probe = max(time.perf_counter() - t0, 1e-3) / 0.05
+    frac = min(1.0, 120.0 / max(1, args.steps + args.warmup) / probe)
+    for i in range(args.warmup):
+        oracle_token(case, i % spec.tokens, frac)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle_token(case, i % spec.tokens, frac)
+    dt = time.perf_counter() - t0
+    tokens = args.steps * frac
+    value = tokens / dt
+    sample = (f"one query per step ({args.steps} steps), each over {frac:.3f} of its "
+              f"{(spec.cached[0] + 1) // spec.ratio} visible entries; value = tokens equivalent / s")
+    return {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "impl": "reference",
+            "config": {"workload": spec.name, "batch": spec.batch, "context": spec.cached[0] + 1,
+                       "heads": spec.heads, "dim": spec.dim, "topk": spec.topk},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="c4a_decode_b4_1m")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    import torch
+    from compressed_sparse_long_c4a_gb300 import inputs as I
+
+    ws, rank, local = _dist()
+    spec = I.WORKLOADS[args.workload]()
+    case = I.make_case(spec, seed=0)
+
+    if args.impl == "reference":
+        line = run_reference(args, spec, case)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    from compressed_sparse_long_c4a_gb300 import v4a
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    scan_b, gather_b, win_b = algorithmic_bytes(spec)
+    step_bytes = scan_b + gather_b + win_b
+    replicas = max(2, math.ceil(2 * L2_BYTES / max(step_bytes, 1)) + 1)
+    layers = [v4a.DeviceLayer.from_case(case, dev) for _ in range(replicas)]
+    steps = [v4a.Step(L) for L in layers]
+    stream = torch.cuda.Stream(device=dev)
+
+    # warm-up (also checks the device status word)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            steps[i % replicas].run(stream)
+    torch.cuda.synchronize()
+    for L in layers:
+        assert int(L.status.item()) == 0, "device status set during warm-up"
+
+    # CUDA graphs of one step per replica
+    graphs = []
+    for st in steps:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            st.run(torch.cuda.current_stream())
+        graphs.append(g)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % replicas].replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K graph replays ----
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for i in range(args.steps):
+                graphs[i % replicas].replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    if ws > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    tokens_per_step = spec.tokens
+    value = ws * tokens_per_step / (ms * 1e-3)
+
+    # ---- per-stage CUDA-event timing (same replicas, direct calls) ----
+    names = ["compress_insert", "index_scores", "index_select", "sparse_attn", "inv_rope_quant"]
+    acc = {n: 0.0 for n in names}
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        st = steps[i % replicas]
+        L = st.layer
+        with torch.cuda.stream(stream):
+            ev[0].record(stream)
+            v4a.compress_insert(L, stream)
+            ev[1].record(stream)
+            if spec.ix_heads:
+                v4a.index_scores(L, st.idx, st.ws_index, stream)
+            ev[2].record(stream)
+            if spec.ix_heads:
+                v4a.index_select(L, st.idx, st.ws_index, stream)
+            ev[3].record(stream)
+            v4a.sparse_attn(L, st.idx, st.o, st.lse, st.ws_attn, stream)
+            ev[4].record(stream)
+            v4a.inv_rope_quant(L, st.o, st.out, st.out_scale, stream)
+            ev[5].record(stream)
+        torch.cuda.synchronize()
+        for k, n in enumerate(names):
+            acc[n] += ev[k].elapsed_time(ev[k + 1])
+    stage_us = {n: acc[n] / args.steps * 1e3 for n in names}
+    hbm_peak, bf16_peak, peak_kind = _peaks()
+    scan_us = stage_us["index_scores"]
+    dominant = max(stage_us, key=stage_us.get)
+    roof = {"bound": "hbm", "kernel": "index_scores (indexer-key scan)",
+            "achieved": scan_b / (scan_us * 1e-6) / 1e9 if scan_us > 0 else None,
+            "peak": hbm_peak, "unit": "GB/s", "traffic": None,
+            "algorithmic_bytes_per_launch": scan_b, "peak_kind": peak_kind}
+    roof["frac"] = roof["achieved"] / hbm_peak if roof["achieved"] else None
+    traffic_file = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(traffic_file):
+        tr = json.load(open(traffic_file)).get(spec.name, {})
+        roof["traffic"] = tr.get("index_scores")
+
+    # ---- end to end: pinned host inputs -> step -> host output ----
+    in_names = [n for n in ("seq_ids", "positions", "x", "gate", "x_i", "gate_i", "k_swa", "q", "q_i",
+                            "q_i_scale", "w_i") if n in layers[0].t]
+    host_in = {n: getattr(case, n).contiguous().pin_memory() for n in in_names}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    out_host = torch.empty_like(steps[0].out, device="cpu").pin_memory()
+    sc_host = (torch.empty_like(steps[0].out_scale, device="cpu").pin_memory()
+               if steps[0].out_scale is not None else None)
+    d2h = out_host.numel() * out_host.element_size() + (sc_host.numel() * 4 if sc_host is not None else 0)
+    torch.cuda.synchronize()
+    barrier()
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        f0.record(stream)
+        for i in range(args.steps):
+            r = i % replicas
+            for n in in_names:
+                layers[r].t[n].copy_(host_in[n], non_blocking=True)
+            graphs[r].replay()
+            out_host.copy_(steps[r].out, non_blocking=True)
+            if sc_host is not None:
+                sc_host.copy_(steps[r].out_scale, non_blocking=True)
+        f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = f0.elapsed_time(f1) / args.steps
+    if ws > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    # ---- kernel launches per step (torch profiler over two graph-free steps) ----
+    launches = None
+    try:
+        from torch.profiler import profile, ProfilerActivity
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            with torch.cuda.stream(stream):
+                for i in range(2):
+                    steps[i % replicas].run(stream)
+            torch.cuda.synchronize()
+        ours = [e for e in prof.events() if e.device_type.name == "CUDA" and
+                any(k in e.name for k in ("compress_insert", "index_score", "topk_", "attn_", "inv_rope",
+                                          "v4a"))]
+        launches = len(ours) // 2 * args.steps
+    except Exception:
+        launches = None
+
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "us_per_layer": ms * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8/fp4 caches, fp32 accumulate",
+        "data": "synthetic (seeded)",
+        "config": {"workload": spec.name, "batch": spec.batch, "context": spec.cached[0] + 1,
+                   "visible_entries": (spec.cached[0] + 1) // spec.ratio, "heads": spec.heads,
+                   "dim": spec.dim, "topk": spec.topk, "indexer": f"{spec.ix_heads}x{spec.ix_dim}",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "l2": f"rotates over {replicas} layer replicas ({replicas * step_bytes / 2**20:.0f} MiB "
+                         f"touched per rotation > 2x L2)", "cuda_graph": True},
+        "roofline": roof,
+        "step_hbm_frac": step_bytes / (ms * 1e-3) / 1e9 / hbm_peak,
+        "stage_us": stage_us, "dominant_stage": dominant,
+        "algorithmic_bytes_per_step": {"scan": scan_b, "gather": gather_b, "window": win_b},
+        "e2e": {"value": ws * tokens_per_step / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        t0 = time.perf_counter()
+        oracle_token(case, 0, 1.0)
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": 1.0 / dt, "unit": "tokens/s", "cores": cpu_cores(),
+                                "kind": "oracle",
+                                "sample": "one full query of the workload (compress, indexer over all "
+                                          "visible entries, top-k, attention, output) in fp64 numpy"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

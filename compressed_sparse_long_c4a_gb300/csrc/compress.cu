@@ -1,0 +1,340 @@
+// Fused KV compressor + RMSNorm + RoPE + paged-cache insert, and the
+// sliding-window key RoPE + insert, in one launch.
+//
+// Method: "DeepSeek V4 in vLLM: Efficient Long-context Attention",
+// Background (c4a: weighted sum of 8 tokens at stride 4; c128a: 128 tokens at
+// stride 128), Method details fusion (1) (compress -> RMSNorm -> RoPE -> cache
+// insert, separate for the indexer and the main cache) and fusion (3) (window
+// key RoPE + insert), Appendix "exact position ranges and causality" (windows
+// [4i-4, 4i+3] / [128i, 128i+127], RoPE once at the last native position).
+//
+// Grid: (T tokens, 3 roles).  Role 0 = main compressor, 1 = indexer
+// compressor, 2 = window key.  Each CTA owns one token; thread p owns the
+// element pair (2p, 2p+1) of the row, which is also one RoPE pair.  A CTA of
+// a compressor role always writes its token into the ring; if the token ends
+// a window (position P with (P+1) % ratio == 0) it also builds the entry.
+// Window positions that belong to this call are read from the call's inputs,
+// older ones from the ring; ring capacity >= window - 1 + tokens per sequence
+// guarantees no ring slot written by this call is one of those older slots.
+
+#include "v4a_common.cuh"
+#include "v4a_internal.h"
+
+namespace v4a {
+
+struct CompressSide {
+  int active, is_indexer;
+  int ratio, dim, rope_dims, format;
+  float theta, eps;
+  uint8_t* pool;
+  int64_t num_blocks, block_bytes;
+  const int32_t* bt;
+  int max_blocks;
+  const uint16_t* x;
+  const float* gate;
+  const float* bias;
+  const float* gamma;
+  uint16_t* ring_x;
+  float* ring_gate;
+  int ring_cap;
+};
+
+struct WindowSide {
+  int active, dim, rope_dims, format;
+  float theta;
+  const uint16_t* k;
+  uint8_t* ring;
+  float* ring_scale;
+  int ring_cap;
+};
+
+struct BatchDev {
+  int T, B, max_new;
+  const int32_t* seq_ids;
+  const int32_t* positions;
+};
+
+__device__ __forceinline__ bool token_ok(const BatchDev& bt, int t, int b, int P) {
+  if (b < 0 || b >= bt.B || P < 0) return false;
+  if (t > 0 && bt.seq_ids[t - 1] == b && bt.positions[t - 1] != P - 1) return false;
+  if (t >= bt.max_new && bt.seq_ids[t - bt.max_new] == b) return false;
+  return true;
+}
+
+// Encodes the pair (v0, v1) owned by thread p into a row of the given format.
+// All threads of the CTA must call it (it contains block reductions).
+__device__ void store_kv_row(int format, int dim, int p, bool own, float v0, float v1,
+                             uint8_t* row, float* scale_slot, float* red) {
+  if (format == V4A_KV_BF16) {
+    if (own) {
+      const uint32_t packed = uint32_t(f32_to_bf16(v0)) | (uint32_t(f32_to_bf16(v1)) << 16);
+      reinterpret_cast<uint32_t*>(row)[p] = packed;
+    }
+    return;
+  }
+  // fp8 e4m3 with one fp32 scale per row: amax / 448
+  float a = own ? fmaxf(fabsf(v0), fabsf(v1)) : 0.f;
+  const float amax = block_reduce<true>(a, red);
+  const float s = amax > 0.f ? amax / 448.f : 1.f;
+  if (own) {
+    const uint16_t c = uint16_t(f32_to_e4m3(v0 / s)) | (uint16_t(f32_to_e4m3(v1 / s)) << 8);
+    reinterpret_cast<uint16_t*>(row)[p] = c;
+  }
+  if (threadIdx.x == 0 && scale_slot) *scale_slot = s;
+}
+
+__device__ void store_ix_row(int format, int dim, int p, bool own, float v0, float v1,
+                             uint8_t* row, float* scales, float* red) {
+  if (format == V4A_IX_BF16) {
+    if (own) {
+      const uint32_t packed = uint32_t(f32_to_bf16(v0)) | (uint32_t(f32_to_bf16(v1)) << 16);
+      reinterpret_cast<uint32_t*>(row)[p] = packed;
+    }
+    return;
+  }
+  const float a = own ? fmaxf(fabsf(v0), fabsf(v1)) : 0.f;
+  if (format == V4A_IX_FP4_B32) {
+    // 32 elements = 16 pairs = one half-warp
+    float m = a;
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float s = m > 0.f ? m / 6.f : 1.f;
+    if (own) {
+      const uint32_t c0 = f32_to_e2m1(v0 / s), c1 = f32_to_e2m1(v1 / s);
+      row[p] = uint8_t(c0 | (c1 << 4));
+      if ((p & 15) == 0) scales[p >> 4] = s;
+    }
+    return;
+  }
+  // fp8 with one scale per 128 elements = 64 pairs = two warps
+  const float wm = warp_max(a);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) red[warp] = wm;
+  __syncthreads();
+  const float m = fmaxf(red[(warp & ~1)], red[(warp & ~1) + 1]);
+  const float s = m > 0.f ? m / 448.f : 1.f;
+  if (own) {
+    const uint16_t c = uint16_t(f32_to_e4m3(v0 / s)) | (uint16_t(f32_to_e4m3(v1 / s)) << 8);
+    reinterpret_cast<uint16_t*>(row)[p] = c;
+    if ((p & 63) == 0) scales[p >> 6] = s;
+  }
+  __syncthreads();
+}
+
+__device__ void compress_token(const CompressSide& c, const BatchDev& bt, int t, int b, int P,
+                               int32_t* status) {
+  __shared__ float w_s[128];
+  __shared__ const uint16_t* src_s[128];
+  __shared__ float red[32];
+  const int p = threadIdx.x;
+  const int npairs = c.dim >> 1;
+  const bool own = p < npairs;
+
+  // 1. this token's raw (x, gate) into the ring
+  const int slot_r = P % c.ring_cap;
+  const uint32_t* xin = reinterpret_cast<const uint32_t*>(c.x + int64_t(t) * c.dim);
+  uint32_t* rx = reinterpret_cast<uint32_t*>(c.ring_x + (int64_t(b) * c.ring_cap + slot_r) * c.dim);
+  if (own) rx[p] = xin[p];
+  if (p == 0) c.ring_gate[int64_t(b) * c.ring_cap + slot_r] = c.gate[t];
+
+  if ((P + 1) % c.ratio != 0) return;
+  const int i = (P + 1) / c.ratio - 1;
+  const int W = c.ratio == 4 ? 8 : 128;
+  const int p0 = c.ratio == 4 ? 4 * i - 4 : 128 * i;
+
+  // 2. window logits and source rows
+  float logit = -INFINITY;
+  for (int j = p; j < W; j += blockDim.x) {
+    const int pos = p0 + j;
+    const uint16_t* row = nullptr;
+    float g = 0.f;
+    if (pos >= 0) {
+      const int d = P - pos;                 // 0 .. W-1
+      if (t - d >= 0 && bt.seq_ids[t - d] == b) {
+        row = c.x + int64_t(t - d) * c.dim;
+        g = c.gate[t - d];
+      } else {
+        const int64_t rs = int64_t(b) * c.ring_cap + pos % c.ring_cap;
+        row = c.ring_x + rs * c.dim;
+        g = c.ring_gate[rs];
+      }
+      logit = fmaxf(logit, g + c.bias[j]);
+    }
+    w_s[j] = pos >= 0 ? g + c.bias[j] : -INFINITY;
+    src_s[j] = row;
+  }
+  const float mx = block_reduce<true>(logit, red);
+  float e = 0.f;
+  for (int j = p; j < W; j += blockDim.x) {
+    const float v = src_s[j] ? expf(w_s[j] - mx) : 0.f;
+    w_s[j] = v;
+    e += v;
+  }
+  const float sum = block_reduce<false>(e, red);   // also orders the w_s writes
+  const float inv = 1.f / sum;
+
+  // 3. weighted sum of the window rows (pair per thread)
+  float a0 = 0.f, a1 = 0.f;
+  if (own) {
+    for (int j = 0; j < W; ++j) {
+      const uint16_t* row = src_s[j];
+      if (!row) continue;
+      const uint32_t v = reinterpret_cast<const uint32_t*>(row)[p];
+      const float wj = w_s[j] * inv;
+      a0 = fmaf(wj, bf16_to_f32(uint16_t(v & 0xffffu)), a0);
+      a1 = fmaf(wj, bf16_to_f32(uint16_t(v >> 16)), a1);
+    }
+  }
+  // 4. RMSNorm
+  const float ss = block_reduce<false>(own ? a0 * a0 + a1 * a1 : 0.f, red);
+  const float r = 1.f / sqrtf(ss / float(c.dim) + c.eps);
+  float v0 = 0.f, v1 = 0.f;
+  if (own) {
+    v0 = a0 * r * c.gamma[2 * p];
+    v1 = a1 * r * c.gamma[2 * p + 1];
+    // 5. RoPE at the anchor (= this token's position)
+    const int first = c.dim - c.rope_dims;
+    if (2 * p >= first) {
+      float cs, sn;
+      rope_cos_sin(P, (2 * p - first) >> 1, c.rope_dims, c.theta, &cs, &sn);
+      const float x0 = v0, x1 = v1;
+      v0 = x0 * cs - x1 * sn;
+      v1 = x0 * sn + x1 * cs;
+    }
+  }
+  // 6. encode + insert at (block_table[b][i / E], i % E)
+  const int E = entries_per_block(c.ratio);
+  __shared__ int64_t blk_s;
+  if (p == 0) {
+    v4a_cache cc;
+    cc.ratio = c.ratio; cc.block_table = c.bt; cc.max_blocks = c.max_blocks;
+    cc.num_blocks = c.num_blocks;
+    blk_s = block_of(cc, b, i, status);
+  }
+  __syncthreads();
+  const int64_t blk = blk_s;
+  if (blk < 0) return;   // uniform across the CTA
+  uint8_t* base = c.pool + blk * c.block_bytes;
+  const int slot = i % E;
+  if (!c.is_indexer) {
+    const int64_t rb = kv_row_bytes(c.format, c.dim);
+    store_kv_row(c.format, c.dim, p, own, v0, v1, base + slot * rb,
+                 reinterpret_cast<float*>(base + E * rb) + slot, red);
+  } else {
+    const int64_t rb = ix_row_bytes(c.format, c.dim);
+    const int ns = ix_scales_per_row(c.format, c.dim);
+    store_ix_row(c.format, c.dim, p, own, v0, v1, base + slot * rb,
+                 reinterpret_cast<float*>(base + 64 * rb) + int64_t(slot) * ns, red);
+  }
+}
+
+__device__ void window_token(const WindowSide& w, int t, int b, int P) {
+  __shared__ float red[32];
+  const int p = threadIdx.x;
+  const bool own = p < (w.dim >> 1);
+  float v0 = 0.f, v1 = 0.f;
+  if (own) {
+    const uint32_t v = reinterpret_cast<const uint32_t*>(w.k + int64_t(t) * w.dim)[p];
+    v0 = bf16_to_f32(uint16_t(v & 0xffffu));
+    v1 = bf16_to_f32(uint16_t(v >> 16));
+    const int first = w.dim - w.rope_dims;
+    if (2 * p >= first) {
+      float cs, sn;
+      rope_cos_sin(P, (2 * p - first) >> 1, w.rope_dims, w.theta, &cs, &sn);
+      const float x0 = v0, x1 = v1;
+      v0 = x0 * cs - x1 * sn;
+      v1 = x0 * sn + x1 * cs;
+    }
+  }
+  const int64_t slot = int64_t(b) * w.ring_cap + P % w.ring_cap;
+  uint8_t* row = w.ring + slot * kv_row_bytes(w.format, w.dim);
+  store_kv_row(w.format, w.dim, p, own, v0, v1, row,
+               w.format == V4A_KV_FP8_TOKEN ? w.ring_scale + slot : nullptr, red);
+}
+
+__global__ void compress_insert_kernel(BatchDev bt, CompressSide mainc, CompressSide ixc,
+                                       WindowSide win, int32_t* status) {
+  const int t = blockIdx.x;
+  const int role = blockIdx.y;
+  const int b = bt.seq_ids[t];
+  const int P = bt.positions[t];
+  if (!token_ok(bt, t, b, P)) {
+    if (threadIdx.x == 0 && role == 0) report(status, V4A_DEV_BAD_BATCH);
+    return;
+  }
+  if (role == 0 && mainc.active) compress_token(mainc, bt, t, b, P, status);
+  if (role == 1 && ixc.active) compress_token(ixc, bt, t, b, P, status);
+  if (role == 2 && win.active) window_token(win, t, b, P);
+}
+
+static int fill_side(const v4a_compressor* c, bool indexer, CompressSide* s, int max_new) {
+  *s = CompressSide{};
+  if (!c) return V4A_OK;
+  const v4a_cache& k = c->cache;
+  if (!k.pool || !k.block_table || !c->x || !c->gate || !c->bias || !c->gamma || !c->ring_x ||
+      !c->ring_gate)
+    return V4A_ERR_INVALID_ARG;
+  if (k.ratio != 4 && k.ratio != 128) return V4A_ERR_INVALID_ARG;
+  if (indexer && k.ratio != 4) return V4A_ERR_UNSUPPORTED;
+  if (k.dim <= 0 || k.dim % 64 || k.dim > 1024) return V4A_ERR_UNSUPPORTED;
+  if (k.rope_dims < 0 || k.rope_dims > k.dim || k.rope_dims % 2) return V4A_ERR_INVALID_ARG;
+  if (k.num_blocks <= 0 || k.max_blocks <= 0 || c->ring_cap <= 0) return V4A_ERR_INVALID_ARG;
+  const int W = k.ratio == 4 ? 8 : 128;
+  if (c->ring_cap < W - 1 + max_new) return V4A_ERR_RING_TOO_SMALL;
+  if (!indexer) {
+    if (k.format != V4A_KV_BF16 && k.format != V4A_KV_FP8_TOKEN) return V4A_ERR_INVALID_ARG;
+  } else {
+    if (k.format != V4A_IX_BF16 && k.format != V4A_IX_FP8_B128 && k.format != V4A_IX_FP4_B32)
+      return V4A_ERR_INVALID_ARG;
+    if (k.format == V4A_IX_FP8_B128 && k.dim % 128) return V4A_ERR_UNSUPPORTED;
+  }
+  s->active = 1;
+  s->is_indexer = indexer;
+  s->ratio = k.ratio; s->dim = k.dim; s->rope_dims = k.rope_dims; s->format = k.format;
+  s->theta = k.rope_theta; s->eps = c->eps;
+  s->pool = static_cast<uint8_t*>(k.pool);
+  s->num_blocks = k.num_blocks;
+  s->block_bytes = indexer ? ix_block_bytes(k.format, k.dim) : kv_block_bytes(k.format, k.ratio, k.dim);
+  s->bt = k.block_table; s->max_blocks = k.max_blocks;
+  s->x = c->x; s->gate = c->gate; s->bias = c->bias; s->gamma = c->gamma;
+  s->ring_x = c->ring_x; s->ring_gate = c->ring_gate; s->ring_cap = c->ring_cap;
+  return V4A_OK;
+}
+
+int compress_insert(const v4a_compress_args* a, cudaStream_t stream) {
+  if (!a) return V4A_ERR_INVALID_ARG;
+  const v4a_batch& B = a->batch;
+  if (B.num_tokens < 0 || B.num_seqs <= 0 || B.max_new_per_seq <= 0) return V4A_ERR_INVALID_ARG;
+  if (B.num_tokens > 0 && (!B.seq_ids || !B.positions)) return V4A_ERR_INVALID_ARG;
+  CompressSide mc, ic;
+  int rc = fill_side(a->main, false, &mc, B.max_new_per_seq);
+  if (rc) return rc;
+  rc = fill_side(a->indexer, true, &ic, B.max_new_per_seq);
+  if (rc) return rc;
+  WindowSide ws{};
+  if (a->window) {
+    const v4a_window& w = *a->window;
+    if (!w.k || !w.ring || w.ring_cap <= 0) return V4A_ERR_INVALID_ARG;
+    if (w.dim <= 0 || w.dim % 64 || w.dim > 1024) return V4A_ERR_UNSUPPORTED;
+    if (w.rope_dims < 0 || w.rope_dims > w.dim || w.rope_dims % 2) return V4A_ERR_INVALID_ARG;
+    if (w.format != V4A_KV_BF16 && w.format != V4A_KV_FP8_TOKEN) return V4A_ERR_INVALID_ARG;
+    if (w.format == V4A_KV_FP8_TOKEN && !w.ring_scale) return V4A_ERR_INVALID_ARG;
+    if (w.ring_cap < 127 + B.max_new_per_seq) return V4A_ERR_RING_TOO_SMALL;
+    ws.active = 1; ws.dim = w.dim; ws.rope_dims = w.rope_dims; ws.format = w.format;
+    ws.theta = w.rope_theta; ws.k = w.k; ws.ring = static_cast<uint8_t*>(w.ring);
+    ws.ring_scale = w.ring_scale; ws.ring_cap = w.ring_cap;
+  }
+  if (B.num_tokens == 0 || (!mc.active && !ic.active && !ws.active)) return V4A_OK;
+  int maxdim = 64;
+  if (mc.active) maxdim = max(maxdim, mc.dim);
+  if (ic.active) maxdim = max(maxdim, ic.dim);
+  if (ws.active) maxdim = max(maxdim, ws.dim);
+  const int threads = ((maxdim / 2) + 31) / 32 * 32;
+  BatchDev bd{B.num_tokens, B.num_seqs, B.max_new_per_seq, B.seq_ids, B.positions};
+  dim3 grid(B.num_tokens, 3);
+  compress_insert_kernel<<<grid, max(threads, 64), 0, stream>>>(bd, mc, ic, ws, a->status);
+  return cudaGetLastError() == cudaSuccess ? V4A_OK : V4A_ERR_CUDA;
+}
+
+}  // namespace v4a

@@ -1,0 +1,519 @@
+// Indexer scoring and top-k selection.
+//
+// Method: "DeepSeek V4 in vLLM: Efficient Long-context Attention", Background
+// "DeepSeek Sparse Attention" (the query attends only to the top-k compressed
+// entries; a 1M-token sequence still holds ~250k c4a entries) and Appendix
+// "exact values of k".  Score rule: score_i = sum_h w_h * ReLU(q_h . k_i) over
+// the entries the query may see (anchor 4i+3 <= m).  Ties go to the lower
+// index; the selected set is written in ascending index order, -1 padded.
+//
+// Kernels:
+//  * index_score_simt  - CUDA-core scores for bf16 / fp8 / fp4 key caches
+//                         (one CTA per (query, 64-entry physical block)).
+//  * index_score_tc    - tcgen05 scores for fp8 / fp4 caches (index_tc.cu).
+//  * topk_smem         - one CTA per query when the row fits in shared memory:
+//                         radix select of the k-th largest (score, -index)
+//                         composite, then an ordered compaction.
+//  * topk_hist / topk_select - long rows: a 4096-bin histogram of the score
+//                         keys (fused into the tcgen05 scan when it runs),
+//                         then every CTA compacts its slice (bins above the
+//                         threshold bin are taken, the threshold bin goes to a
+//                         candidate list) and the last CTA of a query resolves
+//                         the candidates exactly and sorts the selection.
+//                         The "last CTA" is found with an atomic counter; no
+//                         CTA ever waits on another.
+
+#include <cstdio>
+
+#include "v4a_common.cuh"
+#include "v4a_internal.h"
+#include "index_tc.h"
+
+namespace v4a {
+
+constexpr int kSmemTopkMax = 32768;   // rows up to this length use topk_smem
+constexpr int kHistBins = 4096;       // top 12 bits of the order-preserving key
+constexpr int kMaxK = 16384;
+
+struct IndexWs {
+  float* scores;        // [T][row]
+  uint32_t* hist;       // [T][kHistBins]
+  uint32_t* counters;   // [T][4]: selected, candidates, done, resolved
+  uint32_t* flag;       // 1 word: ~0 when stage 1 already built the histogram
+  uint64_t* cand;       // [T][row]
+  int32_t* sel;         // [T][k]
+  int64_t row;
+  size_t zero_bytes;    // bytes of hist + counters (cleared per call)
+  size_t total;
+};
+
+static int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+
+static IndexWs ws_layout(const v4a_index_args* a, void* base) {
+  IndexWs w{};
+  const int64_t T = a->batch.num_tokens;
+  w.row = round_up(int64_t(a->keys.max_blocks) * 64, 128);
+  char* p = static_cast<char*>(base);
+  size_t off = 0;
+  auto take = [&](size_t bytes) { char* r = p ? p + off : nullptr; off += round_up(bytes, 256); return r; };
+  w.hist = reinterpret_cast<uint32_t*>(take(size_t(T) * kHistBins * 4));
+  w.counters = reinterpret_cast<uint32_t*>(take(size_t(T) * 4 * 4 + 4));
+  w.flag = w.counters ? w.counters + size_t(T) * 4 : nullptr;
+  w.zero_bytes = off;
+  w.scores = reinterpret_cast<float*>(take(size_t(T) * w.row * 4));
+  if (w.row > kSmemTopkMax) {
+    w.cand = reinterpret_cast<uint64_t*>(take(size_t(T) * w.row * 8));
+    w.sel = reinterpret_cast<int32_t*>(take(size_t(T) * a->k * 4));
+  }
+  w.total = off;
+  return w;
+}
+
+// ------------------------------------------------------------------------------
+// CUDA-core scores
+// ------------------------------------------------------------------------------
+
+struct ScoreArgs {
+  int T, H, dim, k_fmt, q_fmt;
+  const int32_t* seq_ids;
+  const int32_t* positions;
+  v4a_cache keys;
+  int64_t block_bytes;
+  const void* q;
+  const float* q_scale;
+  const float* w;
+  float* scores;
+  int64_t row;
+  int32_t* status;
+};
+
+__global__ void __launch_bounds__(256) index_score_simt(ScoreArgs a) {
+  extern __shared__ float smem[];
+  const int t = blockIdx.y;
+  const int j = blockIdx.x;                  // logical 64-entry block
+  const int m = a.positions[t];
+  const int n = (m + 1) / 4;
+  if (j * 64 >= n) return;
+  const int b = a.seq_ids[t];
+  const int H = a.H, D = a.dim, DP = a.dim + 1;
+  float* q_s = smem;                         // [H][D+1]
+  float* w_s = q_s + H * DP;                 // [H]
+  float* k_s = w_s + H;                      // [64][D+1]
+  for (int i = threadIdx.x; i < H * D; i += blockDim.x) {
+    const int h = i / D, d = i % D;
+    float v;
+    if (a.q_fmt == V4A_Q_BF16) {
+      v = bf16_to_f32(static_cast<const uint16_t*>(a.q)[(int64_t(t) * H + h) * D + d]);
+    } else {
+      v = e4m3_to_f32(static_cast<const uint8_t*>(a.q)[(int64_t(t) * H + h) * D + d]) *
+          a.q_scale[int64_t(t) * H + h];
+    }
+    q_s[h * DP + d] = v;
+  }
+  for (int h = threadIdx.x; h < H; h += blockDim.x) w_s[h] = a.w[int64_t(t) * H + h];
+  __shared__ int64_t blk_s;
+  if (threadIdx.x == 0) blk_s = block_of(a.keys, b, j * 64, a.status);
+  __syncthreads();
+  const int64_t blk = blk_s;
+  if (blk < 0) {
+    for (int e = threadIdx.x; e < 64; e += blockDim.x)
+      if (j * 64 + e < n) a.scores[int64_t(t) * a.row + j * 64 + e] = -INFINITY;
+    return;
+  }
+  const uint8_t* base = static_cast<const uint8_t*>(a.keys.pool) + blk * a.block_bytes;
+  for (int i = threadIdx.x; i < 64 * D; i += blockDim.x) {
+    const int e = i / D, d = i % D;
+    float v;
+    if (a.k_fmt == V4A_IX_BF16) {
+      v = bf16_to_f32(reinterpret_cast<const uint16_t*>(base)[i]);
+    } else if (a.k_fmt == V4A_IX_FP8_B128) {
+      const float* sc = reinterpret_cast<const float*>(base + 64 * D);
+      v = e4m3_to_f32(base[i]) * sc[e * (D / 128) + d / 128];
+    } else {
+      const float* sc = reinterpret_cast<const float*>(base + 64 * (D / 2));
+      const uint8_t byte = base[e * (D / 2) + d / 2];
+      v = e2m1_to_f32((d & 1) ? (byte >> 4) : (byte & 15)) * sc[e * (D / 32) + d / 32];
+    }
+    k_s[e * DP + d] = v;
+  }
+  __syncthreads();
+  const int e = threadIdx.x >> 2, part = threadIdx.x & 3;
+  float acc = 0.f;
+  for (int h = part; h < H; h += 4) {
+    float dot = 0.f;
+    const float* qh = q_s + h * DP;
+    const float* ke = k_s + e * DP;
+    for (int d = 0; d < D; ++d) dot = fmaf(qh[d], ke[d], dot);
+    acc = fmaf(w_s[h], fmaxf(dot, 0.f), acc);
+  }
+  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+  if (part == 0 && j * 64 + e < n) a.scores[int64_t(t) * a.row + j * 64 + e] = acc;
+}
+
+// ------------------------------------------------------------------------------
+// Radix select over unique 64-bit composites (key << 32 | ~index)
+// ------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint64_t composite(uint32_t key, int idx) {
+  return (uint64_t(key) << 32) | uint64_t(0xFFFFFFFFu - uint32_t(idx));
+}
+
+// Returns thr such that exactly `need` (>= 1) of the n composites are >= thr.
+// All threads of the CTA call it; hist = 256 words of shared memory.
+template <class Get>
+__device__ uint64_t select_threshold(int n, int need, Get get, uint32_t* hist, uint32_t* sh) {
+  uint64_t prefix = 0, mask = 0;
+  for (int pass = 0; pass < 8; ++pass) {
+    const int shift = 56 - 8 * pass;
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const uint64_t c = get(i);
+      if ((c & mask) == prefix) atomicAdd(&hist[(c >> shift) & 255], 1u);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      // warp 0: find the digit where the running count from the top reaches need
+      uint32_t loc[8], s = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) { loc[q] = hist[255 - (threadIdx.x * 8 + q)]; s += loc[q]; }
+      uint32_t incl = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (threadIdx.x >= o) incl += v;
+      }
+      const uint32_t excl = incl - s;
+      if (excl < uint32_t(need) && uint32_t(need) <= incl) {
+        uint32_t acc = excl;
+        int q = 0;
+        for (; q < 8; ++q) {
+          if (acc + loc[q] >= uint32_t(need)) break;
+          acc += loc[q];
+        }
+        sh[0] = 255 - (threadIdx.x * 8 + q);
+        sh[1] = acc;
+        sh[2] = loc[q];
+      }
+    }
+    __syncthreads();
+    const int d = int(sh[0]);
+    const uint32_t above = sh[1], inbin = sh[2];
+    __syncthreads();
+    need -= int(above);
+    prefix |= uint64_t(d) << shift;
+    mask |= uint64_t(255) << shift;
+    if (inbin == uint32_t(need)) return prefix;
+  }
+  return prefix;
+}
+
+// Block-wide exclusive scan of one value per thread (blockDim <= 1024).
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* scratch, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t s = lane < nw ? scratch[lane] : 0;
+    uint32_t si = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t x = __shfl_up_sync(0xffffffffu, si, o);
+      if (lane >= o) si += x;
+    }
+    if (lane < nw) scratch[lane] = si - s;
+    if (lane == nw - 1) scratch[32] = si;
+  }
+  __syncthreads();
+  const uint32_t r = scratch[warp] + incl - v;
+  if (total) *total = scratch[32];
+  __syncthreads();
+  return r;
+}
+
+__device__ void write_all_visible(int32_t* out, int n, int k) {
+  for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = i < n ? i : -1;
+}
+
+// ------------------------------------------------------------------------------
+// Single-CTA top-k (rows that fit in shared memory)
+// ------------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(1024) topk_smem(const float* scores, int64_t row,
+                                                 const int32_t* positions, int k, int32_t* out) {
+  extern __shared__ uint32_t keys_s[];
+  __shared__ uint32_t hist[256];
+  __shared__ uint32_t sh[4];
+  __shared__ uint32_t scan[40];
+  const int t = blockIdx.x;
+  const int n = (positions[t] + 1) / 4;
+  int32_t* o = out + int64_t(t) * k;
+  if (n <= k) { write_all_visible(o, n, k); return; }
+  const float* s = scores + int64_t(t) * row;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) keys_s[i] = float_key(s[i]);
+  __syncthreads();
+  const uint64_t thr = select_threshold(
+      n, k, [&](int i) { return composite(keys_s[i], i); }, hist, sh);
+  // ordered compaction: thread c owns indices [c*chunk, (c+1)*chunk)
+  const int chunk = (n + blockDim.x - 1) / blockDim.x;
+  const int lo = threadIdx.x * chunk, hi = min(n, lo + chunk);
+  uint32_t cnt = 0;
+  for (int i = lo; i < hi; ++i) cnt += composite(keys_s[i], i) >= thr;
+  uint32_t off = block_excl_scan(cnt, scan, nullptr);
+  for (int i = lo; i < hi; ++i)
+    if (composite(keys_s[i], i) >= thr) o[off++] = i;
+}
+
+// ------------------------------------------------------------------------------
+// Multi-CTA top-k for long rows
+// ------------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(512) topk_hist(const float* scores, int64_t row,
+                                                const int32_t* positions, int k, int slices,
+                                                uint32_t* hist, const uint32_t* flag) {
+  __shared__ uint32_t h_s[kHistBins];
+  const int t = blockIdx.y;
+  const int n = (positions[t] + 1) / 4;
+  if (n <= k) return;
+  if (*flag == 0xFFFFFFFFu) return;   // the tensor-core scan already built the histogram
+  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h_s[i] = 0;
+  __syncthreads();
+  const int per = (n + slices - 1) / slices;
+  const int lo = blockIdx.x * per, hi = min(n, lo + per);
+  const float* s = scores + int64_t(t) * row;
+  for (int i = lo + threadIdx.x; i < hi; i += blockDim.x)
+    atomicAdd(&h_s[float_key(s[i]) >> 20], 1u);
+  __syncthreads();
+  uint32_t* g = hist + int64_t(t) * kHistBins;
+  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x)
+    if (h_s[i]) atomicAdd(&g[i], h_s[i]);
+}
+
+__global__ void __launch_bounds__(1024) topk_select(const float* scores, int64_t row,
+                                                   const int32_t* positions, int k, int slices,
+                                                   const uint32_t* hist, uint32_t* counters,
+                                                   uint64_t* cand, int32_t* sel, int32_t* out) {
+  extern __shared__ int32_t sort_s[];   // [pow2 >= k] (last CTA only)
+  __shared__ uint32_t scan[40];
+  __shared__ uint32_t hist256[256];
+  __shared__ uint32_t sh[4];
+  __shared__ int tbin_s;
+  __shared__ uint32_t above_s;
+  __shared__ int last_s;
+  const int t = blockIdx.y;
+  const int n = (positions[t] + 1) / 4;
+  int32_t* o = out + int64_t(t) * k;
+  if (n <= k) {
+    if (blockIdx.x == 0) write_all_visible(o, n, k);
+    return;
+  }
+  // 1. threshold bin from the histogram (bins scanned from the top, 4 per thread)
+  const uint32_t* h = hist + int64_t(t) * kHistBins;
+  uint32_t loc[4], s4 = 0;
+  for (int q = 0; q < 4; ++q) {
+    const int bin = kHistBins - 1 - (threadIdx.x * 4 + q);
+    loc[q] = bin >= 0 ? h[bin] : 0;
+    s4 += loc[q];
+  }
+  uint32_t total;
+  const uint32_t excl = block_excl_scan(s4, scan, &total);
+  if (excl < uint32_t(k) && uint32_t(k) <= excl + s4) {
+    uint32_t acc = excl;
+    int q = 0;
+    for (; q < 4; ++q) {
+      if (acc + loc[q] >= uint32_t(k)) break;
+      acc += loc[q];
+    }
+    tbin_s = kHistBins - 1 - (threadIdx.x * 4 + q);
+    above_s = acc;
+  }
+  __syncthreads();
+  const uint32_t tbin = uint32_t(tbin_s);
+  // 2. compact this CTA's slice
+  uint32_t* cnt = counters + int64_t(t) * 4;
+  uint64_t* cd = cand + int64_t(t) * row;
+  int32_t* sl = sel + int64_t(t) * k;
+  const int per = (n + slices - 1) / slices;
+  const int lo = blockIdx.x * per, hi = min(n, lo + per);
+  const float* s = scores + int64_t(t) * row;
+  const int lane = threadIdx.x & 31;
+  for (int base = lo; base < hi; base += blockDim.x) {
+    const int i = base + threadIdx.x;
+    uint32_t key = 0, bin = 0;
+    const bool in = i < hi;
+    if (in) { key = float_key(s[i]); bin = key >> 20; }
+    const bool take = in && bin > tbin;
+    const bool maybe = in && bin == tbin;
+    const uint32_t mt = __ballot_sync(0xffffffffu, take);
+    const uint32_t mm = __ballot_sync(0xffffffffu, maybe);
+    uint32_t bt = 0, bm = 0;
+    if (lane == 0) {
+      if (mt) bt = atomicAdd(&cnt[0], __popc(mt));
+      if (mm) bm = atomicAdd(&cnt[1], __popc(mm));
+    }
+    bt = __shfl_sync(0xffffffffu, bt, 0);
+    bm = __shfl_sync(0xffffffffu, bm, 0);
+    const uint32_t below = (1u << lane) - 1u;
+    if (take) sl[bt + __popc(mt & below)] = i;
+    if (maybe) cd[bm + __popc(mm & below)] = composite(key, i);
+  }
+  // 3. the last CTA of this query resolves the threshold bin and sorts
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last_s = atomicAdd(&cnt[2], 1u) == uint32_t(slices - 1);
+  __syncthreads();
+  if (!last_s) return;
+  __threadfence();
+  const uint32_t above = __ldcg(&cnt[0]);
+  const int nc = int(__ldcg(&cnt[1]));
+  const int need = k - int(above);
+  if (need > 0) {
+    const uint64_t thr = select_threshold(
+        nc, need, [&](int i) { return __ldcg(&cd[i]); }, hist256, sh);
+    for (int base = 0; base < nc; base += blockDim.x) {
+      const int i = base + threadIdx.x;
+      const bool take = i < nc && __ldcg(&cd[i]) >= thr;
+      const uint32_t mt = __ballot_sync(0xffffffffu, take);
+      uint32_t bt = 0;
+      if (lane == 0 && mt) bt = atomicAdd(&cnt[3], __popc(mt));
+      bt = __shfl_sync(0xffffffffu, bt, 0);
+      if (take) sl[above + bt + __popc(mt & ((1u << lane) - 1u))] = int32_t(0xFFFFFFFFu - uint32_t(__ldcg(&cd[i]) & 0xFFFFFFFFu));
+    }
+    __threadfence();
+    __syncthreads();
+  }
+  // bitonic sort of the k selected indices (ascending)
+  int P2 = 1;
+  while (P2 < k) P2 <<= 1;
+  for (int i = threadIdx.x; i < P2; i += blockDim.x) sort_s[i] = i < k ? __ldcg(&sl[i]) : 0x7FFFFFFF;
+  __syncthreads();
+  for (int size = 2; size <= P2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < P2 / 2; i += blockDim.x) {
+        const int lo2 = (i / stride) * stride * 2 + (i % stride);
+        const int hi2 = lo2 + stride;
+        const bool up = ((lo2 / size) & 1) == 0;
+        const int a = sort_s[lo2], c = sort_s[hi2];
+        if ((a > c) == up) { sort_s[lo2] = c; sort_s[hi2] = a; }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < k; i += blockDim.x) o[i] = sort_s[i];
+}
+
+// ------------------------------------------------------------------------------
+// Host side
+// ------------------------------------------------------------------------------
+
+// Shapes and formats only (enough to size the workspace).
+static int validate_shape(const v4a_index_args* a) {
+  if (!a) return V4A_ERR_INVALID_ARG;
+  const v4a_batch& B = a->batch;
+  if (B.num_tokens < 0 || B.num_seqs <= 0) return V4A_ERR_INVALID_ARG;
+  if (B.num_tokens > 65535) return V4A_ERR_UNSUPPORTED;
+  const v4a_cache& c = a->keys;
+  if (c.ratio != 4) return V4A_ERR_UNSUPPORTED;
+  if (c.num_blocks <= 0 || c.max_blocks <= 0) return V4A_ERR_INVALID_ARG;
+  if (a->k < 1 || a->k > kMaxK) return V4A_ERR_UNSUPPORTED;
+  if (a->num_heads < 1 || a->num_heads > 128) return V4A_ERR_UNSUPPORTED;
+  if (c.dim < 32 || c.dim > 256 || c.dim % 32) return V4A_ERR_UNSUPPORTED;
+  if (c.format == V4A_IX_BF16) {
+    if (a->q_format != V4A_Q_BF16) return V4A_ERR_UNSUPPORTED;
+  } else if (c.format == V4A_IX_FP8_B128 || c.format == V4A_IX_FP4_B32) {
+    if (a->q_format != V4A_Q_FP8_HEAD) return V4A_ERR_UNSUPPORTED;
+    if (c.format == V4A_IX_FP8_B128 && c.dim % 128) return V4A_ERR_UNSUPPORTED;
+  } else {
+    return V4A_ERR_INVALID_ARG;
+  }
+  return V4A_OK;
+}
+
+static int validate(const v4a_index_args* a) {
+  const int rc = validate_shape(a);
+  if (rc) return rc;
+  if (a->batch.num_tokens == 0) return V4A_OK;
+  if (!a->batch.seq_ids || !a->batch.positions || !a->q || !a->weights || !a->out_idx ||
+      !a->keys.pool || !a->keys.block_table)
+    return V4A_ERR_INVALID_ARG;
+  if (a->q_format == V4A_Q_FP8_HEAD && !a->q_scale) return V4A_ERR_INVALID_ARG;
+  return V4A_OK;
+}
+
+size_t index_workspace_size(const v4a_index_args* a) {
+  if (validate_shape(a)) return 0;
+  return ws_layout(a, nullptr).total;
+}
+
+// Stage 1: clear the histogram/counters and score every visible entry.
+int index_scores(const v4a_index_args* a, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  int rc = validate(a);
+  if (rc) return rc;
+  const int T = a->batch.num_tokens;
+  if (T == 0) return V4A_OK;
+  IndexWs w = ws_layout(a, nullptr);
+  if (!ws || ws_bytes < w.total) return V4A_ERR_WORKSPACE;
+  w = ws_layout(a, ws);
+  const v4a_cache& c = a->keys;
+  if (cudaMemsetAsync(w.hist, 0, w.zero_bytes, stream) != cudaSuccess) return V4A_ERR_CUDA;
+  bool hist_done = false;
+  if (index_score_tc(a, w.scores, w.row, w.row > kSmemTopkMax ? w.hist : nullptr, stream,
+                     &hist_done, &rc)) {
+    if (rc) return rc;
+    if (hist_done && cudaMemsetAsync(w.flag, 0xFF, 4, stream) != cudaSuccess) return V4A_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? V4A_OK : V4A_ERR_CUDA;
+  }
+  ScoreArgs sa;
+  sa.T = T; sa.H = a->num_heads; sa.dim = c.dim; sa.k_fmt = c.format; sa.q_fmt = a->q_format;
+  sa.seq_ids = a->batch.seq_ids; sa.positions = a->batch.positions; sa.keys = c;
+  sa.block_bytes = ix_block_bytes(c.format, c.dim);
+  sa.q = a->q; sa.q_scale = a->q_scale; sa.w = a->weights; sa.scores = w.scores; sa.row = w.row;
+  sa.status = a->status;
+  const size_t smem = size_t(a->num_heads * (c.dim + 1) + a->num_heads + 64 * (c.dim + 1)) * 4;
+  if (smem > 227 * 1024) return V4A_ERR_UNSUPPORTED;
+  cudaFuncSetAttribute(index_score_simt, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  index_score_simt<<<dim3(unsigned(c.max_blocks), unsigned(T)), 256, smem, stream>>>(sa);
+  return cudaGetLastError() == cudaSuccess ? V4A_OK : V4A_ERR_CUDA;
+}
+
+// Stage 2: top-k of the scores left in the workspace by stage 1.
+int index_select(const v4a_index_args* a, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  int rc = validate(a);
+  if (rc) return rc;
+  const int T = a->batch.num_tokens;
+  if (T == 0) return V4A_OK;
+  IndexWs w = ws_layout(a, nullptr);
+  if (!ws || ws_bytes < w.total) return V4A_ERR_WORKSPACE;
+  w = ws_layout(a, ws);
+  if (w.row <= kSmemTopkMax) {
+    const size_t smem = size_t(w.row) * 4;
+    cudaFuncSetAttribute(topk_smem, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    topk_smem<<<T, 1024, smem, stream>>>(w.scores, w.row, a->batch.positions, a->k, a->out_idx);
+  } else {
+    const int slices = int((w.row + 4095) / 4096);
+    topk_hist<<<dim3(slices, T), 512, 0, stream>>>(w.scores, w.row, a->batch.positions, a->k,
+                                                   slices, w.hist, w.flag);
+    int P2 = 1;
+    while (P2 < a->k) P2 <<= 1;
+    const size_t smem = size_t(P2) * 4;
+    cudaFuncSetAttribute(topk_select, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    topk_select<<<dim3(slices, T), 1024, smem, stream>>>(w.scores, w.row, a->batch.positions, a->k,
+                                                         slices, w.hist, w.counters, w.cand, w.sel,
+                                                         a->out_idx);
+  }
+  return cudaGetLastError() == cudaSuccess ? V4A_OK : V4A_ERR_CUDA;
+}
+
+int index_topk(const v4a_index_args* a, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  const int rc = index_scores(a, ws, ws_bytes, stream);
+  return rc ? rc : index_select(a, ws, ws_bytes, stream);
+}
+
+}  // namespace v4a

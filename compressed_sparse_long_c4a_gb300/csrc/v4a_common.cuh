@@ -1,0 +1,138 @@
+// Device helpers shared by the libv4a kernels: bf16/e4m3/e2m1 conversions,
+// rotary angles, slot mapping, status reporting and block reductions.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_fp4.h>
+#include <stdint.h>
+
+#include "v4a.h"
+
+namespace v4a {
+
+constexpr int kBlockPositions = 256;   // one logical block = 256 native positions
+
+__device__ __forceinline__ void report(int32_t* status, int bits) {
+  if (status) atomicOr(status, bits);
+}
+
+// ---- bf16 -------------------------------------------------------------------
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+__device__ __forceinline__ uint16_t f32_to_bf16(float f) {
+  __nv_bfloat16 h = __float2bfloat16_rn(f);
+  return *reinterpret_cast<uint16_t*>(&h);
+}
+
+// ---- fp8 e4m3 ------------------------------------------------------------------
+__device__ __forceinline__ float e4m3_to_f32(uint8_t c) {
+  __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(c), __NV_E4M3);
+  return __half2float(__half(h));
+}
+__device__ __forceinline__ uint8_t f32_to_e4m3(float f) {
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(f, __NV_SATFINITE, __NV_E4M3));
+}
+
+// ---- fp4 e2m1 ------------------------------------------------------------------
+// Magnitudes of the OCP e2m1 codes 0..7 (sign in bit 3).
+__device__ __forceinline__ float e2m1_to_f32(uint32_t nib) {
+  const float mag[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
+  float v = mag[nib & 7u];
+  return (nib & 8u) ? -v : v;
+}
+__device__ __forceinline__ uint32_t f32_to_e2m1(float f) {
+  return static_cast<uint32_t>(__nv_cvt_float_to_fp4(f, __NV_E2M1, cudaRoundNearest)) & 0xFu;
+}
+
+// ---- rotary angles ------------------------------------------------------------
+// angle_j = pos * theta^(-2j/R), formed in fp64 (positions reach 1e6) and
+// reduced before the fp32 rotation is applied.
+__device__ __forceinline__ void rope_cos_sin(int pos, int j, int rope_dims, float theta,
+                                             float* c, float* s) {
+  double inv_freq = pow(static_cast<double>(theta), -2.0 * j / static_cast<double>(rope_dims));
+  double ang = static_cast<double>(pos) * inv_freq;
+  double sd, cd;
+  sincos(ang, &sd, &cd);
+  *c = static_cast<float>(cd);
+  *s = static_cast<float>(sd);
+}
+
+// ---- paged cache geometry ----------------------------------------------------
+__host__ __device__ __forceinline__ int entries_per_block(int ratio) {
+  return kBlockPositions / ratio;
+}
+
+__host__ __device__ __forceinline__ int64_t kv_block_bytes(int fmt, int ratio, int dim) {
+  const int64_t e = entries_per_block(ratio);
+  return fmt == V4A_KV_BF16 ? e * dim * 2 : e * (dim + 4);
+}
+
+__host__ __device__ __forceinline__ int64_t kv_row_bytes(int fmt, int dim) {
+  return fmt == V4A_KV_BF16 ? int64_t(dim) * 2 : int64_t(dim);
+}
+
+__host__ __device__ __forceinline__ int64_t ix_row_bytes(int fmt, int dim) {
+  return fmt == V4A_IX_BF16 ? int64_t(dim) * 2 : (fmt == V4A_IX_FP8_B128 ? dim : dim / 2);
+}
+
+__host__ __device__ __forceinline__ int ix_scales_per_row(int fmt, int dim) {
+  return fmt == V4A_IX_FP8_B128 ? dim / 128 : (fmt == V4A_IX_FP4_B32 ? dim / 32 : 0);
+}
+
+__host__ __device__ __forceinline__ int64_t ix_block_bytes(int fmt, int dim) {
+  return 64 * (ix_row_bytes(fmt, dim) + 4 * ix_scales_per_row(fmt, dim));
+}
+
+// Physical block of logical entry i, or -1 (and a status bit) if unusable.
+__device__ __forceinline__ int64_t block_of(const v4a_cache& c, int seq, int i,
+                                            int32_t* status) {
+  const int e = entries_per_block(c.ratio);
+  const int lb = i / e;
+  if (lb >= c.max_blocks) { report(status, V4A_DEV_BAD_BLOCK); return -1; }
+  const int32_t blk = c.block_table[int64_t(seq) * c.max_blocks + lb];
+  if (blk < 0 || blk >= c.num_blocks) { report(status, V4A_DEV_BAD_BLOCK); return -1; }
+  return blk;
+}
+
+// ---- reductions -----------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Block-wide reduction; `red` must hold >= 32 floats.  All threads get the result.
+template <bool kMax>
+__device__ __forceinline__ float block_reduce(float v, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = (blockDim.x + 31) >> 5;
+  v = kMax ? warp_max(v) : warp_sum(v);
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float r = (lane < nw) ? red[lane] : (kMax ? -INFINITY : 0.f);
+  if (warp == 0) {
+    r = kMax ? warp_max(r) : warp_sum(r);
+    if (lane == 0) red[0] = r;
+  }
+  __syncthreads();
+  r = red[0];
+  __syncthreads();
+  return r;
+}
+
+// Order-preserving map of a float to uint32 (larger float -> larger key).
+__device__ __forceinline__ uint32_t float_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+}  // namespace v4a

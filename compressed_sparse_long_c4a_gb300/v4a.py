@@ -1,0 +1,281 @@
+"""ctypes binding of libv4a (argument marshalling only).
+
+Every function here builds the C argument structs from torch CUDA tensors and
+calls the library; all arithmetic runs in the CUDA kernels.  If libv4a.so is
+missing the first call raises: there is no CPU or eager fallback.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import math
+import os
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libv4a.so")
+
+V4A_OK = 0
+ERRORS = {1: "invalid argument", 2: "unsupported", 3: "ring too small", 4: "workspace", 5: "cuda"}
+DEV_BAD_BLOCK, DEV_BAD_BATCH, DEV_BAD_INDEX = 1, 2, 4
+KV_BF16, KV_FP8_TOKEN = 0, 1
+IX_BF16, IX_FP8_B128, IX_FP4_B32 = 0, 1, 2
+Q_BF16, Q_FP8_HEAD = 0, 1
+OUT_BF16, OUT_FP8_TOKEN = 0, 1
+
+_p = C.c_void_p
+
+
+class Batch(C.Structure):
+    _fields_ = [("num_tokens", C.c_int32), ("seq_ids", _p), ("positions", _p),
+                ("num_seqs", C.c_int32), ("max_new_per_seq", C.c_int32)]
+
+
+class Cache(C.Structure):
+    _fields_ = [("ratio", C.c_int32), ("dim", C.c_int32), ("rope_dims", C.c_int32),
+                ("rope_theta", C.c_float), ("format", C.c_int32), ("pool", _p),
+                ("num_blocks", C.c_int64), ("block_table", _p), ("max_blocks", C.c_int32)]
+
+
+class Compressor(C.Structure):
+    _fields_ = [("cache", Cache), ("x", _p), ("gate", _p), ("bias", _p), ("gamma", _p),
+                ("eps", C.c_float), ("ring_x", _p), ("ring_gate", _p), ("ring_cap", C.c_int32)]
+
+
+class Window(C.Structure):
+    _fields_ = [("k", _p), ("dim", C.c_int32), ("rope_dims", C.c_int32), ("rope_theta", C.c_float),
+                ("format", C.c_int32), ("ring", _p), ("ring_scale", _p), ("ring_cap", C.c_int32)]
+
+
+class CompressArgs(C.Structure):
+    _fields_ = [("batch", Batch), ("main", C.POINTER(Compressor)), ("indexer", C.POINTER(Compressor)),
+                ("window", C.POINTER(Window)), ("status", _p)]
+
+
+class IndexArgs(C.Structure):
+    _fields_ = [("batch", Batch), ("keys", Cache), ("num_heads", C.c_int32), ("q_format", C.c_int32),
+                ("q", _p), ("q_scale", _p), ("weights", _p), ("k", C.c_int32), ("out_idx", _p),
+                ("status", _p)]
+
+
+class AttnArgs(C.Structure):
+    _fields_ = [("batch", Batch), ("kv", Cache), ("idx", _p), ("k", C.c_int32), ("window", _p),
+                ("window_scale", _p), ("window_cap", C.c_int32), ("window_format", C.c_int32),
+                ("window_len", C.c_int32), ("num_heads", C.c_int32), ("q", _p),
+                ("softmax_scale", C.c_float), ("out", _p), ("lse", _p), ("status", _p)]
+
+
+class OutputArgs(C.Structure):
+    _fields_ = [("num_tokens", C.c_int32), ("positions", _p), ("num_heads", C.c_int32),
+                ("dim", C.c_int32), ("rope_dims", C.c_int32), ("rope_theta", C.c_float),
+                ("in_", _p), ("out_format", C.c_int32), ("out", _p), ("out_scale", _p)]
+
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """The loaded libv4a; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libv4a.so not found at {LIB_PATH}: run __graft_entry__.build()")
+        L = C.CDLL(LIB_PATH)
+        L.v4a_compress_insert.argtypes = [C.POINTER(CompressArgs), _p]
+        L.v4a_index_workspace_size.argtypes = [C.POINTER(IndexArgs)]
+        L.v4a_index_workspace_size.restype = C.c_size_t
+        L.v4a_index_topk.argtypes = [C.POINTER(IndexArgs), _p, C.c_size_t, _p]
+        L.v4a_index_scores.argtypes = [C.POINTER(IndexArgs), _p, C.c_size_t, _p]
+        L.v4a_index_select.argtypes = [C.POINTER(IndexArgs), _p, C.c_size_t, _p]
+        L.v4a_attn_workspace_size.argtypes = [C.POINTER(AttnArgs)]
+        L.v4a_attn_workspace_size.restype = C.c_size_t
+        L.v4a_sparse_attn.argtypes = [C.POINTER(AttnArgs), _p, C.c_size_t, _p]
+        L.v4a_inv_rope_quant.argtypes = [C.POINTER(OutputArgs), _p]
+        L.v4a_status_string.restype = C.c_char_p
+        L.v4a_status_string.argtypes = [C.c_int]
+        _lib = L
+    return _lib
+
+
+class V4AError(RuntimeError):
+    def __init__(self, where: str, code: int):
+        super().__init__(f"{where}: {lib().v4a_status_string(code).decode()} (code {code})")
+        self.code = code
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _check(where: str, rc: int):
+    if rc != V4A_OK:
+        raise V4AError(where, rc)
+
+# --------------------------------------------------------------------------
+# Device-resident layer state
+# --------------------------------------------------------------------------
+
+
+@dataclass
+class DeviceLayer:
+    """One layer's caches, rings, block table and the step inputs on the GPU."""
+    spec: object
+    t: dict            # name -> CUDA tensor
+    status: torch.Tensor
+
+    @classmethod
+    def from_case(cls, case, device="cuda") -> "DeviceLayer":
+        t = {}
+        for f in ("seq_ids", "positions", "block_table", "kv_pool", "x", "gate", "bias", "gamma",
+                  "ring_x", "ring_gate", "k_swa", "swa_ring", "swa_scale", "q", "ix_pool", "x_i",
+                  "gate_i", "bias_i", "gamma_i", "ring_x_i", "ring_gate_i", "q_i", "q_i_scale",
+                  "w_i", "o_in"):
+            v = getattr(case, f)
+            if v is not None and v.numel() > 0:
+                t[f] = v.to(device).contiguous()
+        return cls(spec=case.spec, t=t, status=torch.zeros(1, dtype=torch.int32, device=device))
+
+    # ---- argument structs -------------------------------------------------
+    def batch(self) -> Batch:
+        s = self.spec
+        return Batch(s.tokens, _ptr(self.t["seq_ids"]), _ptr(self.t["positions"]), s.batch, s.new)
+
+    def kv_cache(self) -> Cache:
+        s = self.spec
+        return Cache(s.ratio, s.dim, s.rope_dims, s.theta, s.kv_fmt, _ptr(self.t["kv_pool"]),
+                     s.num_blocks, _ptr(self.t["block_table"]), s.max_blocks)
+
+    def ix_cache(self) -> Cache:
+        s = self.spec
+        return Cache(4, s.ix_dim, s.ix_rope_dims, s.theta, s.ix_fmt, _ptr(self.t["ix_pool"]),
+                     s.num_blocks, _ptr(self.t["block_table"]), s.max_blocks)
+
+    def compress_args(self):
+        s, t = self.spec, self.t
+        keep = []
+        main = Compressor(self.kv_cache(), _ptr(t["x"]), _ptr(t["gate"]), _ptr(t["bias"]),
+                          _ptr(t["gamma"]), 1e-6, _ptr(t["ring_x"]), _ptr(t["ring_gate"]), s.ring_cap)
+        keep.append(main)
+        ix = None
+        if s.ix_heads:
+            ix = Compressor(self.ix_cache(), _ptr(t["x_i"]), _ptr(t["gate_i"]), _ptr(t["bias_i"]),
+                            _ptr(t["gamma_i"]), 1e-6, _ptr(t["ring_x_i"]), _ptr(t["ring_gate_i"]),
+                            s.ix_ring_cap)
+            keep.append(ix)
+        win = Window(_ptr(t["k_swa"]), s.dim, s.rope_dims, s.theta, s.swa_fmt, _ptr(t["swa_ring"]),
+                     _ptr(t.get("swa_scale")), s.swa_cap)
+        keep.append(win)
+        a = CompressArgs(self.batch(), C.pointer(main), C.pointer(ix) if ix else None,
+                         C.pointer(win), _ptr(self.status))
+        return a, keep
+
+    def index_args(self, out_idx: torch.Tensor) -> IndexArgs:
+        s, t = self.spec, self.t
+        return IndexArgs(self.batch(), self.ix_cache(), s.ix_heads, s.ix_q_fmt, _ptr(t["q_i"]),
+                         _ptr(t["q_i_scale"]), _ptr(t["w_i"]), s.topk, _ptr(out_idx),
+                         _ptr(self.status))
+
+    def attn_args(self, idx: torch.Tensor | None, out: torch.Tensor, lse: torch.Tensor | None) -> AttnArgs:
+        s, t = self.spec, self.t
+        return AttnArgs(self.batch(), self.kv_cache(), _ptr(idx), s.topk if idx is not None else 0,
+                        _ptr(t["swa_ring"]), _ptr(t.get("swa_scale")), s.swa_cap, s.swa_fmt, s.swa,
+                        s.heads, _ptr(t["q"]), 1.0 / math.sqrt(s.dim), _ptr(out), _ptr(lse),
+                        _ptr(self.status))
+
+    def output_args(self, o: torch.Tensor, out: torch.Tensor, out_scale: torch.Tensor | None) -> OutputArgs:
+        s = self.spec
+        return OutputArgs(s.tokens, _ptr(self.t["positions"]), s.heads, s.dim, s.rope_dims, s.theta,
+                          _ptr(o), s.out_fmt, _ptr(out), _ptr(out_scale))
+
+# --------------------------------------------------------------------------
+# Calls
+# --------------------------------------------------------------------------
+
+
+def compress_insert(layer: DeviceLayer, stream=None):
+    a, keep = layer.compress_args()
+    _check("v4a_compress_insert", lib().v4a_compress_insert(C.byref(a), _stream(stream)))
+
+
+def index_workspace_bytes(layer: DeviceLayer) -> int:
+    out = torch.empty(0, dtype=torch.int32)
+    a = layer.index_args(out)
+    return int(lib().v4a_index_workspace_size(C.byref(a)))
+
+
+def index_topk(layer: DeviceLayer, out_idx: torch.Tensor, workspace: torch.Tensor, stream=None):
+    a = layer.index_args(out_idx)
+    _check("v4a_index_topk", lib().v4a_index_topk(C.byref(a), _ptr(workspace), workspace.numel(),
+                                                  _stream(stream)))
+
+
+def index_scores(layer: DeviceLayer, out_idx: torch.Tensor, workspace: torch.Tensor, stream=None):
+    a = layer.index_args(out_idx)
+    _check("v4a_index_scores", lib().v4a_index_scores(C.byref(a), _ptr(workspace), workspace.numel(),
+                                                      _stream(stream)))
+
+
+def index_select(layer: DeviceLayer, out_idx: torch.Tensor, workspace: torch.Tensor, stream=None):
+    a = layer.index_args(out_idx)
+    _check("v4a_index_select", lib().v4a_index_select(C.byref(a), _ptr(workspace), workspace.numel(),
+                                                      _stream(stream)))
+
+
+def attn_workspace_bytes(layer: DeviceLayer, with_idx: bool) -> int:
+    dummy = torch.empty(0, dtype=torch.int32)
+    a = layer.attn_args(dummy if with_idx else None, dummy, None)
+    if with_idx:
+        a.idx = 1   # any non-null value: only the presence matters for sizing
+    return int(lib().v4a_attn_workspace_size(C.byref(a)))
+
+
+def sparse_attn(layer: DeviceLayer, idx: torch.Tensor | None, out: torch.Tensor,
+                lse: torch.Tensor | None, workspace: torch.Tensor, stream=None):
+    a = layer.attn_args(idx, out, lse)
+    _check("v4a_sparse_attn", lib().v4a_sparse_attn(C.byref(a), _ptr(workspace), workspace.numel(),
+                                                    _stream(stream)))
+
+
+def inv_rope_quant(layer: DeviceLayer, o: torch.Tensor, out: torch.Tensor,
+                   out_scale: torch.Tensor | None, stream=None):
+    a = layer.output_args(o, out, out_scale)
+    _check("v4a_inv_rope_quant", lib().v4a_inv_rope_quant(C.byref(a), _stream(stream)))
+
+
+class Step:
+    """Output buffers + workspaces for running whole layer steps on a DeviceLayer."""
+
+    def __init__(self, layer: DeviceLayer):
+        s = layer.spec
+        dev = layer.status.device
+        self.layer = layer
+        T = s.tokens
+        self.idx = torch.full((T, s.topk), -1, dtype=torch.int32, device=dev) if s.ix_heads else None
+        self.o = torch.empty((T, s.heads, s.dim), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((T, s.heads), dtype=torch.float32, device=dev)
+        if s.out_fmt == OUT_BF16:
+            self.out = torch.empty((T, s.heads, s.dim), dtype=torch.bfloat16, device=dev)
+            self.out_scale = None
+        else:
+            self.out = torch.empty((T, s.heads, s.dim), dtype=torch.uint8, device=dev)
+            self.out_scale = torch.empty((T,), dtype=torch.float32, device=dev)
+        self.ws_index = torch.empty(max(index_workspace_bytes(layer) if s.ix_heads else 0, 256),
+                                    dtype=torch.uint8, device=dev)
+        self.ws_attn = torch.empty(max(attn_workspace_bytes(layer, s.ix_heads > 0), 256),
+                                   dtype=torch.uint8, device=dev)
+
+    def run(self, stream=None):
+        """compress_insert -> index_topk -> sparse_attn -> inv_rope_quant."""
+        L = self.layer
+        compress_insert(L, stream)
+        if L.spec.ix_heads:
+            index_topk(L, self.idx, self.ws_index, stream)
+        sparse_attn(L, self.idx, self.o, self.lse, self.ws_attn, stream)
+        inv_rope_quant(L, self.o, self.out, self.out_scale, stream)

@@ -41,6 +41,12 @@ extern "C" {
 
 #define V4A_ABI_VERSION 1
 
+#if defined(__GNUC__)
+#define V4A_API __attribute__((visibility("default")))
+#else
+#define V4A_API
+#endif
+
 /* ---- host return codes ---------------------------------------------------- */
 #define V4A_OK                 0
 #define V4A_ERR_INVALID_ARG    1  /* null pointer, bad size, bad enum */
@@ -156,7 +162,7 @@ typedef struct {
  * One launch.  Returns V4A_ERR_RING_TOO_SMALL when a ring cannot hold the
  * call's tokens without overwriting positions a window still reads.
  */
-int v4a_compress_insert(const v4a_compress_args* args, void* stream);
+V4A_API int v4a_compress_insert(const v4a_compress_args* args, void* stream);
 
 /*
  * Indexer scoring and top-k (vLLM page, Background "DeepSeek Sparse
@@ -180,9 +186,20 @@ typedef struct {
   int32_t* status;
 } v4a_index_args;
 
-size_t v4a_index_workspace_size(const v4a_index_args* args);
-int v4a_index_topk(const v4a_index_args* args, void* workspace, size_t workspace_bytes,
+/* Bytes of device workspace v4a_index_topk / _scores / _select need (0 on a bad
+ * shape).  The workspace holds the scores of every visible entry of every
+ * query plus selection scratch; it is only read and written by these calls. */
+V4A_API size_t v4a_index_workspace_size(const v4a_index_args* args);
+V4A_API int v4a_index_topk(const v4a_index_args* args, void* workspace, size_t workspace_bytes,
                    void* stream);
+/* v4a_index_topk in two launches-groups on the same stream: _scores writes
+ * every visible entry's score into the workspace, _select reads them and
+ * writes out_idx.  Calling _scores then _select with the same arguments and
+ * workspace is exactly v4a_index_topk. */
+V4A_API int v4a_index_scores(const v4a_index_args* args, void* workspace, size_t workspace_bytes,
+                     void* stream);
+V4A_API int v4a_index_select(const v4a_index_args* args, void* workspace, size_t workspace_bytes,
+                     void* stream);
 
 /*
  * Sparse attention with shared K=V (vLLM page, Background and appendix "why
@@ -211,8 +228,9 @@ typedef struct {
   int32_t* status;
 } v4a_attn_args;
 
-size_t v4a_attn_workspace_size(const v4a_attn_args* args);
-int v4a_sparse_attn(const v4a_attn_args* args, void* workspace, size_t workspace_bytes,
+/* Bytes of device workspace v4a_sparse_attn needs (split partials; 0 on a bad shape). */
+V4A_API size_t v4a_attn_workspace_size(const v4a_attn_args* args);
+V4A_API int v4a_sparse_attn(const v4a_attn_args* args, void* workspace, size_t workspace_bytes,
                     void* stream);
 
 /*
@@ -232,11 +250,11 @@ typedef struct {
   float* out_scale;            /* [T] (fp8 only) */
 } v4a_output_args;
 
-int v4a_inv_rope_quant(const v4a_output_args* args, void* stream);
+V4A_API int v4a_inv_rope_quant(const v4a_output_args* args, void* stream);
 
 /* Human-readable text of a V4A_* return code. */
-const char* v4a_status_string(int code);
-int v4a_abi_version(void);
+V4A_API const char* v4a_status_string(int code);
+V4A_API int v4a_abi_version(void);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,113 @@
+"""Comparison helpers for the GPU parity tests (GPU output vs fp64 oracle)."""
+from __future__ import annotations
+
+import numpy as np
+
+from oracle import formats as F
+from oracle import geometry as G
+
+BF16_TOL = (2e-2, 2e-3)     # attention output, bf16 caches: max-abs, mean-abs
+FP8_TOL = (6e-2, 6e-3)      # attention output, fp8 / fp4 caches
+TOPK_REL = 1e-5             # near-tie band around the k-th score
+
+
+def check_topk(gpu_idx: np.ndarray, ref_idx: np.ndarray, scores: np.ndarray, k: int, where=""):
+    """Sets equal except swaps among scores within TOPK_REL of the k-th score;
+    the GPU row must be ascending, unique, -1 padded and inside the visible range."""
+    n = scores.shape[0]
+    g = gpu_idx.tolist()
+    valid = [v for v in g if v >= 0]
+    assert len(valid) == min(n, k), (where, len(valid), min(n, k))
+    assert g[:len(valid)] == sorted(valid) and len(set(valid)) == len(valid), where
+    assert all(v == -1 for v in g[len(valid):]), where
+    assert all(0 <= v < n for v in valid), where
+    if n <= k:
+        assert sorted(valid) == list(range(n)), where
+        return 0
+    kth = np.sort(scores)[::-1][k - 1]
+    diff = set(valid) ^ set(int(v) for v in ref_idx if v >= 0)
+    for e in diff:
+        assert abs(scores[e] - kth) <= TOPK_REL * max(abs(kth), 1e-30), \
+            (where, e, scores[e], kth)
+    return len(diff)
+
+
+def check_close(gpu: np.ndarray, ref: np.ndarray, tol, where=""):
+    err = np.abs(np.asarray(gpu, np.float64) - ref)
+    mx, mean = float(err.max()), float(err.mean())
+    assert mx <= tol[0] and mean <= tol[1], (where, mx, mean)
+    return mx, mean
+
+
+# The kernels compute in fp32: a sum of up to 128 weighted terms, or a
+# rotation, leaves an absolute error of a few fp32 ulps of the row's largest
+# element.  An element that cancels to near zero cannot be within one bf16
+# ulp of its own tiny value, so each element may also differ by this floor
+# (2^-18 of the row's max, about 1e-3 of a bf16 ulp at that magnitude).
+FP32_FLOOR = 2.0 ** -18
+
+
+def check_bf16_row(gpu_bits: np.ndarray, ref: np.ndarray, where=""):
+    """Stored bf16 within 1 ulp of the fp64 value (plus the fp32 floor)."""
+    got = F.bf16_decode(gpu_bits)
+    ulp = F.bf16_ulp(ref)
+    floor = FP32_FLOOR * float(np.max(np.abs(ref)))
+    bad = np.abs(got - ref) > ulp * 1.0000001 + floor + 1e-30
+    assert not bad.any(), (where, np.nonzero(bad)[0][:5], got[bad][:5], ref[bad][:5])
+
+
+def check_fp8_row(codes: np.ndarray, scale: float, ref: np.ndarray, where=""):
+    """Per-row fp8: scale = amax/448 (relative 1e-6), values within 1 e4m3 ulp * scale."""
+    amax = np.max(np.abs(ref))
+    assert abs(scale - amax / 448) <= 1e-6 * amax / 448 + 1e-30, (where, scale, amax / 448)
+    got = F.e4m3_decode(codes) * scale
+    ulp = F.e4m3_ulp(ref / scale) * scale
+    bad = np.abs(got - ref) > ulp * 1.0000001 + 1e-30
+    assert not bad.any(), (where, np.nonzero(bad)[0][:5])
+
+
+def check_fp8_blocks(codes, scales, ref, block, where=""):
+    for b in range(ref.shape[0] // block):
+        check_fp8_row(codes[b * block:(b + 1) * block], float(scales[b]), ref[b * block:(b + 1) * block],
+                      f"{where}/blk{b}")
+
+
+def check_fp4_blocks(packed, scales, ref, where=""):
+    nib = F.unpack_nibbles(packed)
+    for b in range(ref.shape[0] // 32):
+        seg = ref[32 * b:32 * b + 32]
+        amax = np.max(np.abs(seg))
+        s = float(scales[b])
+        assert abs(s - amax / 6) <= 1e-6 * amax / 6 + 1e-30, (where, b, s, amax / 6)
+        got = F.e2m1_decode(nib[32 * b:32 * b + 32]) * s
+        ulp = F.e2m1_ulp(seg / s) * s
+        bad = np.abs(got - seg) > ulp * 1.0000001 + 1e-30
+        assert not bad.any(), (where, b, np.nonzero(bad)[0][:5])
+
+
+def kv_slot_bytes(pool: np.ndarray, spec, blk: int, slot: int):
+    """(row bytes, scale or None) of one shared-KV entry."""
+    E, D = spec.entries_per_block, spec.dim
+    base = blk * spec.kv_block_bytes
+    if spec.kv_fmt == F.KV_BF16:
+        return pool[base + slot * 2 * D: base + (slot + 1) * 2 * D].copy().view(np.uint16), None
+    row = pool[base + slot * D: base + (slot + 1) * D].copy()
+    sc = pool[base + E * D + 4 * slot: base + E * D + 4 * slot + 4].copy().view(np.float32)[0]
+    return row, float(sc)
+
+
+def ix_slot_bytes(pool: np.ndarray, spec, blk: int, slot: int):
+    d, fmt = spec.ix_dim, spec.ix_fmt
+    base = blk * spec.ix_block_bytes
+    if fmt == F.IX_BF16:
+        return pool[base + slot * 2 * d: base + (slot + 1) * 2 * d].copy().view(np.uint16), None
+    rb = d if fmt == F.IX_FP8_B128 else d // 2
+    ns = d // 128 if fmt == F.IX_FP8_B128 else d // 32
+    row = pool[base + slot * rb: base + (slot + 1) * rb].copy()
+    off = base + 64 * rb + 4 * ns * slot
+    sc = pool[off: off + 4 * ns].copy().view(np.float32).astype(np.float64)
+    return row, sc
+
+
+def entry_slots(spec, block_table: np.ndarray, entries: dict, ratio: int):
+    return {(b, i): G.slot_of(block_table[b], i, ratio) for (b, i) in entries}

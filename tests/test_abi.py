@@ -1,0 +1,118 @@
+"""The C-ABI library loads on a machine without a GPU, exports every entry
+point the header declares, and rejects bad arguments on the host (no GPU
+call is made on these paths)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from compressed_sparse_long_c4a_gb300 import inputs as I
+from compressed_sparse_long_c4a_gb300 import v4a
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(v4a.LIB_PATH):
+        from compressed_sparse_long_c4a_gb300 import build
+        build.build()
+    return v4a.lib()
+
+
+def test_exports_every_declared_symbol(lib):
+    hdr = open(os.path.join(ROOT, "include", "v4a.h")).read()
+    names = re.findall(r"V4A_API\s+[\w\s\*]+?\b(v4a_\w+)\s*\(", hdr)
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), n
+    assert lib.v4a_abi_version() == 1
+    for code in range(6):
+        assert lib.v4a_status_string(code).decode() != "unknown status"
+
+
+class _FakeLayer(v4a.DeviceLayer):
+    """Argument structs with fake (never dereferenced) device pointers."""
+
+    def __init__(self, spec):
+        self.spec = spec
+        self.t = {}
+        self.status = None
+
+    def batch(self):
+        s = self.spec
+        return v4a.Batch(s.tokens, 0x1000, 0x2000, s.batch, s.new)
+
+    def kv_cache(self):
+        s = self.spec
+        return v4a.Cache(s.ratio, s.dim, s.rope_dims, s.theta, s.kv_fmt, 0x3000, s.num_blocks, 0x4000,
+                         s.max_blocks)
+
+    def ix_cache(self):
+        s = self.spec
+        return v4a.Cache(4, s.ix_dim, s.ix_rope_dims, s.theta, s.ix_fmt, 0x5000, s.num_blocks, 0x4000,
+                         s.max_blocks)
+
+
+def _compressor(layer, cap):
+    return v4a.Compressor(layer.kv_cache(), 0x10, 0x20, 0x30, 0x40, 1e-6, 0x50, 0x60, cap)
+
+
+def test_host_validation_of_compress(lib):
+    spec = I.c4a_prefill_4x4k()
+    L = _FakeLayer(spec)
+    assert lib.v4a_compress_insert(None, None) == 1
+    comp = _compressor(L, spec.ring_cap - 1)           # one slot short: window - 2 + new
+    a = v4a.CompressArgs(L.batch(), C.pointer(comp), None, None, None)
+    assert lib.v4a_compress_insert(C.byref(a), None) == 3
+    win = v4a.Window(0x70, spec.dim, 64, 1e4, 0, 0x80, None, 127 + spec.new - 1)
+    a = v4a.CompressArgs(L.batch(), None, None, C.pointer(win), None)
+    assert lib.v4a_compress_insert(C.byref(a), None) == 3
+    bad = _compressor(L, spec.ring_cap)
+    bad.cache.ratio = 5
+    a = v4a.CompressArgs(L.batch(), C.pointer(bad), None, None, None)
+    assert lib.v4a_compress_insert(C.byref(a), None) == 1
+    odd = _compressor(L, spec.ring_cap)
+    odd.cache.dim = 96
+    a = v4a.CompressArgs(L.batch(), C.pointer(odd), None, None, None)
+    assert lib.v4a_compress_insert(C.byref(a), None) == 2
+
+
+def test_host_validation_of_index_and_workspace_sizes(lib):
+    spec = I.c4a_decode_1m()
+    L = _FakeLayer(spec)
+    a = v4a.IndexArgs(L.batch(), L.ix_cache(), spec.ix_heads, spec.ix_q_fmt, 0x10, 0x20, 0x30, spec.topk,
+                      0x40, None)
+    need = lib.v4a_index_workspace_size(C.byref(a))
+    # scores for every visible entry of every query at least
+    assert need >= spec.tokens * spec.max_blocks * 64 * 4
+    assert lib.v4a_index_topk(C.byref(a), None, 0, None) == 4           # no workspace
+    assert lib.v4a_index_topk(C.byref(a), 0x1000, need - 1, None) == 4
+    a.k = 0
+    assert lib.v4a_index_topk(C.byref(a), 0x1000, need, None) == 2
+    a.k = spec.topk
+    a.q_format = v4a.Q_BF16                                              # fp4 keys need an fp8 query
+    assert lib.v4a_index_topk(C.byref(a), 0x1000, need, None) == 2
+    a.q_format = v4a.Q_FP8_HEAD
+    a.keys.ratio = 128
+    assert lib.v4a_index_topk(C.byref(a), 0x1000, need, None) == 2
+
+
+def test_host_validation_of_attention_and_output(lib):
+    spec = I.c4a_decode_1m()
+    L = _FakeLayer(spec)
+    a = v4a.AttnArgs(L.batch(), L.kv_cache(), 0x10, spec.topk, 0x20, 0x30, spec.swa_cap, spec.swa_fmt,
+                     spec.swa, spec.heads, 0x40, 0.04, 0x50, None, None)
+    need = lib.v4a_attn_workspace_size(C.byref(a))
+    assert need > 0
+    assert lib.v4a_sparse_attn(C.byref(a), None, 0, None) == 4
+    a.window_scale = None                                                # fp8 window needs scales
+    assert lib.v4a_sparse_attn(C.byref(a), 0x1000, need, None) == 1
+    a.window_scale = 0x30
+    a.kv.dim = 96
+    assert lib.v4a_sparse_attn(C.byref(a), 0x1000, need, None) == 2
+    o = v4a.OutputArgs(4, 0x10, 128, 512, 64, 1e4, 0x20, 1, 0x30, None)  # fp8 output needs scales
+    assert lib.v4a_inv_rope_quant(C.byref(o), None) == 1
+    o = v4a.OutputArgs(0, None, 128, 512, 64, 1e4, None, 0, None, None)  # empty batch: no work
+    assert lib.v4a_inv_rope_quant(C.byref(o), None) == 0

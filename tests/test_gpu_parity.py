@@ -1,0 +1,270 @@
+"""GPU parity of every stage against the fp64 oracle, through the C ABI.
+
+Each stage is run on the GPU on seeded inputs and compared with the oracle
+run on the same inputs (the oracle never takes a GPU output as input).
+Workloads: reduced variants of the five layer workloads (same formats, a few
+tiles and ragged tails, seconds for the oracle) and the full-size workloads
+(decode: every query; prefill: a stated subsample of queries).
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from compressed_sparse_long_c4a_gb300 import inputs as I
+from oracle import formats as F
+from oracle import geometry as G
+from tests import gpu_util as U
+from tests import oracle_bridge as OB
+
+pytestmark = pytest.mark.gpu
+
+
+def _small_workloads():
+    s2 = I.c4a_decode_b32_32k_64k()
+    s2 = dataclasses.replace(s2, name="c4a_decode_small_fp8ix", batch=6,
+                             cached=(4 * 700 + 3, 256 * 3 + 3, 256 * 4 + 255, 256 * 5, 3001, 2222))
+    s3 = I.c128a_decode_b64_64k_128k()
+    s3 = dataclasses.replace(s3, name="c128a_decode_small", batch=8,
+                             cached=(5, 126, 127, 128 * 7 + 127, 128 * 9 + 127, 3000, 1999, 640))
+    s4 = I.c4a_prefill_4x4k()
+    s4 = dataclasses.replace(s4, name="c4a_prefill_small", batch=2, cached=(1000, 1535), new=300,
+                             topk=64)
+    s5 = I.c4a_decode_1m()
+    s5 = dataclasses.replace(s5, name="c4a_decode_small_fp4ix_fp8kv", batch=2,
+                             cached=(4 * 10000 + 3, 39001))
+    return [I.c4a_decode_1k(), s2, s3, s4, s5]
+
+
+SMALL = {s.name: s for s in _small_workloads()}
+FULL = {n: f() for n, f in I.WORKLOADS.items()}
+# prefill at full size: oracle on a subsample of queries (first/last 64 and every 97th)
+PREFILL_ROWS = sorted(set(list(range(64)) + list(range(16384 - 64, 16384)) + list(range(0, 16384, 97))))
+
+
+class Run:
+    """GPU stage outputs and oracle results for one workload (cached per module)."""
+
+    def __init__(self, spec):
+        self.spec = spec
+        self.case = I.make_case(spec, seed=0)
+        self._oracle = {}
+
+    def layer(self):
+        from compressed_sparse_long_c4a_gb300 import v4a
+        return v4a.DeviceLayer.from_case(self.case)
+
+    def oracle_compress(self):
+        if "compress" not in self._oracle:
+            self._oracle["compress"] = OB.oracle_compress(self.case)
+        return self._oracle["compress"]
+
+    def rows(self):
+        if self.spec.name == "c4a_prefill_4x32k_plus_4k":
+            return PREFILL_ROWS
+        return list(range(self.spec.tokens))
+
+    def oracle_index_on_inputs(self):
+        if "index" not in self._oracle:
+            self._oracle["index"] = OB.oracle_index(self.case, OB.u8(self.case.ix_pool), rows=self.rows())
+        return self._oracle["index"]
+
+
+_RUNS = {}
+
+
+def run_for(name) -> Run:
+    if name not in _RUNS:
+        _RUNS[name] = Run(SMALL.get(name) or FULL[name])
+    return _RUNS[name]
+
+
+ALL = list(SMALL) + list(FULL)
+C4A = [n for n in ALL if (SMALL.get(n) or FULL[n]).ratio == 4]
+
+
+def _marks(n):
+    return pytest.param(n, marks=pytest.mark.slow) if n in FULL else n
+
+
+@pytest.mark.parametrize("name", [_marks(n) for n in ALL])
+def test_compress_insert(name):
+    from compressed_sparse_long_c4a_gb300 import v4a
+    r = run_for(name)
+    s, case = r.spec, r.case
+    L = r.layer()
+    v4a.compress_insert(L)
+    torch.cuda.synchronize()
+    assert int(L.status.item()) == 0
+    main, ix, swa = r.oracle_compress()
+    bt = case.block_table.numpy()
+    kv_in, kv_out = OB.u8(case.kv_pool), L.t["kv_pool"].cpu().numpy()
+    touched = np.zeros(kv_in.shape[0], bool)
+    for (b, i), ref in main.items():
+        blk, slot = G.slot_of(bt[b], i, s.ratio)
+        row, sc = U.kv_slot_bytes(kv_out, s, blk, slot)
+        if s.kv_fmt == F.KV_BF16:
+            U.check_bf16_row(row, ref, f"main {b},{i}")
+            base = blk * s.kv_block_bytes + slot * 2 * s.dim
+            touched[base:base + 2 * s.dim] = True
+        else:
+            U.check_fp8_row(row, sc, ref, f"main {b},{i}")
+            base = blk * s.kv_block_bytes
+            touched[base + slot * s.dim: base + (slot + 1) * s.dim] = True
+            off = base + s.entries_per_block * s.dim + 4 * slot
+            touched[off:off + 4] = True
+    assert np.array_equal(kv_out[~touched], kv_in[~touched]), "bytes outside emitted slots changed"
+    assert len(main) == sum(1 for p in case.positions.tolist() if (p + 1) % s.ratio == 0)
+    if s.ix_heads:
+        ix_in, ix_out = OB.u8(case.ix_pool), L.t["ix_pool"].cpu().numpy()
+        itouched = np.zeros(ix_in.shape[0], bool)
+        for (b, i), ref in ix.items():
+            blk, slot = G.slot_of(bt[b], i, 4)
+            row, sc = U.ix_slot_bytes(ix_out, s, blk, slot)
+            if s.ix_fmt == F.IX_BF16:
+                U.check_bf16_row(row, ref, f"ix {b},{i}")
+            elif s.ix_fmt == F.IX_FP8_B128:
+                U.check_fp8_blocks(row, sc, ref, 128, f"ix {b},{i}")
+            else:
+                U.check_fp4_blocks(row, sc, ref, f"ix {b},{i}")
+            base = blk * s.ix_block_bytes
+            rb = row.nbytes
+            itouched[base + slot * rb: base + (slot + 1) * rb] = True
+            ns = 0 if sc is None else len(sc)
+            itouched[base + 64 * rb + 4 * ns * slot: base + 64 * rb + 4 * ns * (slot + 1)] = True
+        assert np.array_equal(ix_out[~itouched], ix_in[~itouched])
+    # window ring: every new token rotated and encoded at position % cap
+    ring = L.t["swa_ring"].cpu()
+    cap = s.swa_cap
+    for (b, p), ref in list(swa.items())[:: max(1, len(swa) // 256)]:
+        if s.swa_fmt == F.KV_BF16:
+            U.check_bf16_row(OB.u16(ring[b, p % cap]), ref, f"swa {b},{p}")
+        else:
+            sc = float(L.t["swa_scale"][b, p % cap].item())
+            U.check_fp8_row(ring[b, p % cap].numpy(), sc, ref, f"swa {b},{p}")
+    # compressor rings hold the raw new tokens
+    rx = L.t["ring_x"].cpu()
+    for t in range(0, s.tokens, max(1, s.tokens // 64)):
+        b, p = int(case.seq_ids[t]), int(case.positions[t])
+        assert torch.equal(rx[b, p % s.ring_cap], case.x[t])
+        assert float(L.t["ring_gate"][b, p % s.ring_cap]) == float(case.gate[t])
+
+
+@pytest.mark.parametrize("name", [_marks(n) for n in C4A])
+def test_index_topk(name):
+    from compressed_sparse_long_c4a_gb300 import v4a
+    r = run_for(name)
+    s = r.spec
+    L = r.layer()
+    step = v4a.Step(L)
+    v4a.index_topk(L, step.idx, step.ws_index)
+    torch.cuda.synchronize()
+    assert int(L.status.item()) == 0
+    idx, scores = r.oracle_index_on_inputs()
+    gpu = step.idx.cpu().numpy()
+    swaps = 0
+    for t in idx:
+        swaps += U.check_topk(gpu[t], idx[t], scores[t], s.topk, f"{name} t={t}")
+    assert swaps <= max(2, len(idx) // 4)
+
+
+@pytest.mark.parametrize("name", [_marks(n) for n in ALL])
+def test_sparse_attn(name):
+    """Attention on a selection computed by the oracle (c4a) or on every
+    visible entry (c128a), over the generator's caches and window ring."""
+    from compressed_sparse_long_c4a_gb300 import v4a
+    r = run_for(name)
+    s, case = r.spec, r.case
+    L = r.layer()
+    step = v4a.Step(L)
+    rows = r.rows()
+    if s.ix_heads:
+        oidx, _ = r.oracle_index_on_inputs()
+        full = np.full((s.tokens, s.topk), -1, np.int64)
+        for t, v in oidx.items():
+            full[t] = v
+        if len(oidx) < s.tokens:          # prefill subsample: other rows get a valid causal set
+            for t in range(s.tokens):
+                if t not in oidx:
+                    n = G.n_visible(int(case.positions[t]), 4)
+                    full[t, :min(n, s.topk)] = np.arange(min(n, s.topk))
+        idx_t = torch.from_numpy(full.astype(np.int32)).cuda()
+        v4a.sparse_attn(L, idx_t, step.o, step.lse, step.ws_attn)
+        sel = {t: full[t] for t in rows}
+    else:
+        v4a.sparse_attn(L, None, step.o, step.lse, step.ws_attn)
+        sel = None
+    torch.cuda.synchronize()
+    assert int(L.status.item()) == 0
+    ring = OB.u16(case.swa_ring) if s.swa_fmt == F.KV_BF16 else OB.u8(case.swa_ring)
+    rsc = None if s.swa_fmt == F.KV_BF16 else case.swa_scale.double().numpy()
+    ref = OB.oracle_attention(case, OB.u8(case.kv_pool), ring, rsc, sel, rows=rows)
+    o = step.o.float().cpu().numpy()
+    lse = step.lse.cpu().numpy()
+    tol = U.BF16_TOL if s.kv_fmt == F.KV_BF16 else U.FP8_TOL
+    U.check_close(o[rows], np.stack([ref[t][0] for t in rows]), tol, name)
+    assert np.allclose(lse[rows], np.stack([ref[t][1] for t in rows]), atol=1e-3, rtol=1e-4)
+
+
+@pytest.mark.parametrize("name", [_marks(n) for n in ALL])
+def test_inv_rope_quant(name):
+    from compressed_sparse_long_c4a_gb300 import v4a
+    r = run_for(name)
+    s, case = r.spec, r.case
+    L = r.layer()
+    step = v4a.Step(L)
+    v4a.inv_rope_quant(L, L.t["o_in"], step.out, step.out_scale)
+    torch.cuda.synchronize()
+    rows = r.rows()[:256]
+    ref = OB.oracle_output(case, OB.u16(case.o_in))
+    out = step.out.cpu()
+    for t in rows:
+        o_ref = ref[t][0]
+        if s.out_fmt == F.KV_BF16:
+            U.check_bf16_row(OB.u16(out[t]).reshape(-1), o_ref.reshape(-1), f"t={t}")
+        else:
+            U.check_fp8_row(out[t].numpy().reshape(-1), float(step.out_scale[t]), o_ref.reshape(-1),
+                            f"t={t}")
+
+
+@pytest.mark.parametrize("name", [_marks(n) for n in ALL])
+def test_end_to_end(name):
+    """Full GPU step (compress -> index -> attention -> output) against the
+    oracle's own chain on the same inputs."""
+    from compressed_sparse_long_c4a_gb300 import v4a
+    r = run_for(name)
+    s, case = r.spec, r.case
+    L = r.layer()
+    step = v4a.Step(L)
+    step.run()
+    torch.cuda.synchronize()
+    assert int(L.status.item()) == 0
+    rows = r.rows()
+    main, ix, swa = r.oracle_compress()
+    kv, ixp, ring, rsc = OB.oracle_state_after_compress(case, main, ix, swa)
+    idx = None
+    if s.ix_heads:
+        idx, scores = OB.oracle_index(case, ixp, rows=rows)
+        gpu_idx = step.idx.cpu().numpy()
+        for t in rows:
+            U.check_topk(gpu_idx[t], idx[t], scores[t], s.topk, f"{name} t={t}")
+    att = OB.oracle_attention(case, kv, ring, rsc, idx, rows=rows)
+    o_ref = np.stack([att[t][0] for t in rows])
+    tol = U.BF16_TOL if s.kv_fmt == F.KV_BF16 else U.FP8_TOL
+    U.check_close(step.o.float().cpu().numpy()[rows], o_ref, tol, name)
+    out = step.out.cpu()
+    oo = OB.oracle_output(case, F.bf16_encode(np.stack([att.get(t, (np.zeros((s.heads, s.dim)),))[0]
+                                                         for t in range(s.tokens)])))
+    for t in rows[:64]:
+        ref_t = oo[t][0]
+        if s.out_fmt == F.KV_BF16:
+            got = F.bf16_decode(OB.u16(out[t]))
+            bound = tol[0]
+        else:
+            sc = float(step.out_scale[t])
+            got = F.e4m3_decode(out[t].numpy()) * sc
+            bound = F.e4m3_ulp(ref_t / sc) * sc + tol[0]
+        assert np.all(np.abs(got - ref_t) <= bound), (name, t)
