@@ -13,6 +13,10 @@ size_t v4a_index_workspace_size(const v4a_index_args* args) {
   return v4a::index_workspace_size(args);
 }
 
+int v4a_index_scores_layout(const v4a_index_args* args, size_t* offset, int64_t* row_stride) {
+  return v4a::index_scores_layout(args, offset, row_stride);
+}
+
 int v4a_index_topk(const v4a_index_args* args, void* workspace, size_t workspace_bytes,
                    void* stream) {
   return v4a::index_topk(args, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));

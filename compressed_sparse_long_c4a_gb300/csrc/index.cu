@@ -92,7 +92,8 @@ __global__ void __launch_bounds__(256) index_score_simt(ScoreArgs a) {
   const int t = blockIdx.y;
   const int j = blockIdx.x;                  // logical 64-entry block
   const int m = a.positions[t];
-  const int n = (m + 1) / 4;
+  const int n = min((m + 1) / 4, a.keys.max_blocks * 64);
+  if (j == 0 && threadIdx.x == 0 && (m + 1) / 4 > n) report(a.status, V4A_DEV_BAD_BLOCK);
   if (j * 64 >= n) return;
   const int b = a.seq_ids[t];
   const int H = a.H, D = a.dim, DP = a.dim + 1;
@@ -246,14 +247,14 @@ __device__ void write_all_visible(int32_t* out, int n, int k) {
 // Single-CTA top-k (rows that fit in shared memory)
 // ------------------------------------------------------------------------------
 
-__global__ void __launch_bounds__(1024) topk_smem(const float* scores, int64_t row,
+__global__ void __launch_bounds__(1024) topk_smem(const float* scores, int64_t row, int max_entries,
                                                  const int32_t* positions, int k, int32_t* out) {
   extern __shared__ uint32_t keys_s[];
   __shared__ uint32_t hist[256];
   __shared__ uint32_t sh[4];
   __shared__ uint32_t scan[40];
   const int t = blockIdx.x;
-  const int n = (positions[t] + 1) / 4;
+  const int n = min((positions[t] + 1) / 4, max_entries);
   int32_t* o = out + int64_t(t) * k;
   if (n <= k) { write_all_visible(o, n, k); return; }
   const float* s = scores + int64_t(t) * row;
@@ -275,12 +276,12 @@ __global__ void __launch_bounds__(1024) topk_smem(const float* scores, int64_t r
 // Multi-CTA top-k for long rows
 // ------------------------------------------------------------------------------
 
-__global__ void __launch_bounds__(512) topk_hist(const float* scores, int64_t row,
+__global__ void __launch_bounds__(512) topk_hist(const float* scores, int64_t row, int max_entries,
                                                 const int32_t* positions, int k, int slices,
                                                 uint32_t* hist, const uint32_t* flag) {
   __shared__ uint32_t h_s[kHistBins];
   const int t = blockIdx.y;
-  const int n = (positions[t] + 1) / 4;
+  const int n = min((positions[t] + 1) / 4, max_entries);
   if (n <= k) return;
   if (*flag == 0xFFFFFFFFu) return;   // the tensor-core scan already built the histogram
   for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h_s[i] = 0;
@@ -296,7 +297,7 @@ __global__ void __launch_bounds__(512) topk_hist(const float* scores, int64_t ro
     if (h_s[i]) atomicAdd(&g[i], h_s[i]);
 }
 
-__global__ void __launch_bounds__(1024) topk_select(const float* scores, int64_t row,
+__global__ void __launch_bounds__(1024) topk_select(const float* scores, int64_t row, int max_entries,
                                                    const int32_t* positions, int k, int slices,
                                                    const uint32_t* hist, uint32_t* counters,
                                                    uint64_t* cand, int32_t* sel, int32_t* out) {
@@ -308,7 +309,7 @@ __global__ void __launch_bounds__(1024) topk_select(const float* scores, int64_t
   __shared__ uint32_t above_s;
   __shared__ int last_s;
   const int t = blockIdx.y;
-  const int n = (positions[t] + 1) / 4;
+  const int n = min((positions[t] + 1) / 4, max_entries);
   int32_t* o = out + int64_t(t) * k;
   if (n <= k) {
     if (blockIdx.x == 0) write_all_visible(o, n, k);
@@ -447,6 +448,15 @@ static int validate(const v4a_index_args* a) {
   return V4A_OK;
 }
 
+int index_scores_layout(const v4a_index_args* a, size_t* offset, int64_t* row_stride) {
+  if (validate_shape(a)) return V4A_ERR_INVALID_ARG;
+  char* fake = reinterpret_cast<char*>(size_t(1) << 40);
+  const IndexWs w = ws_layout(a, fake);
+  if (offset) *offset = size_t(reinterpret_cast<char*>(w.scores) - fake);
+  if (row_stride) *row_stride = w.row;
+  return V4A_OK;
+}
+
 size_t index_workspace_size(const v4a_index_args* a) {
   if (validate_shape(a)) return 0;
   return ws_layout(a, nullptr).total;
@@ -495,18 +505,19 @@ int index_select(const v4a_index_args* a, void* ws, size_t ws_bytes, cudaStream_
   if (w.row <= kSmemTopkMax) {
     const size_t smem = size_t(w.row) * 4;
     cudaFuncSetAttribute(topk_smem, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    topk_smem<<<T, 1024, smem, stream>>>(w.scores, w.row, a->batch.positions, a->k, a->out_idx);
+    topk_smem<<<T, 1024, smem, stream>>>(w.scores, w.row, a->keys.max_blocks * 64, a->batch.positions,
+                                         a->k, a->out_idx);
   } else {
     const int slices = int((w.row + 4095) / 4096);
-    topk_hist<<<dim3(slices, T), 512, 0, stream>>>(w.scores, w.row, a->batch.positions, a->k,
-                                                   slices, w.hist, w.flag);
+    topk_hist<<<dim3(slices, T), 512, 0, stream>>>(w.scores, w.row, a->keys.max_blocks * 64,
+                                                   a->batch.positions, a->k, slices, w.hist, w.flag);
     int P2 = 1;
     while (P2 < a->k) P2 <<= 1;
     const size_t smem = size_t(P2) * 4;
     cudaFuncSetAttribute(topk_select, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    topk_select<<<dim3(slices, T), 1024, smem, stream>>>(w.scores, w.row, a->batch.positions, a->k,
-                                                         slices, w.hist, w.counters, w.cand, w.sel,
-                                                         a->out_idx);
+    topk_select<<<dim3(slices, T), 1024, smem, stream>>>(w.scores, w.row, a->keys.max_blocks * 64,
+                                                         a->batch.positions, a->k, slices, w.hist,
+                                                         w.counters, w.cand, w.sel, a->out_idx);
   }
   return cudaGetLastError() == cudaSuccess ? V4A_OK : V4A_ERR_CUDA;
 }

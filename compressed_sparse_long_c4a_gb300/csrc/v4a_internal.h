@@ -6,6 +6,7 @@
 namespace v4a {
 int compress_insert(const v4a_compress_args* a, cudaStream_t stream);
 size_t index_workspace_size(const v4a_index_args* a);
+int index_scores_layout(const v4a_index_args* a, size_t* offset, int64_t* row_stride);
 int index_topk(const v4a_index_args* a, void* ws, size_t ws_bytes, cudaStream_t stream);
 int index_scores(const v4a_index_args* a, void* ws, size_t ws_bytes, cudaStream_t stream);
 int index_select(const v4a_index_args* a, void* ws, size_t ws_bytes, cudaStream_t stream);

@@ -88,6 +88,8 @@ def lib() -> C.CDLL:
         L.v4a_index_topk.argtypes = [C.POINTER(IndexArgs), _p, C.c_size_t, _p]
         L.v4a_index_scores.argtypes = [C.POINTER(IndexArgs), _p, C.c_size_t, _p]
         L.v4a_index_select.argtypes = [C.POINTER(IndexArgs), _p, C.c_size_t, _p]
+        L.v4a_index_scores_layout.argtypes = [C.POINTER(IndexArgs), C.POINTER(C.c_size_t),
+                                              C.POINTER(C.c_int64)]
         L.v4a_attn_workspace_size.argtypes = [C.POINTER(AttnArgs)]
         L.v4a_attn_workspace_size.restype = C.c_size_t
         L.v4a_sparse_attn.argtypes = [C.POINTER(AttnArgs), _p, C.c_size_t, _p]
@@ -226,6 +228,15 @@ def index_select(layer: DeviceLayer, out_idx: torch.Tensor, workspace: torch.Ten
     a = layer.index_args(out_idx)
     _check("v4a_index_select", lib().v4a_index_select(C.byref(a), _ptr(workspace), workspace.numel(),
                                                       _stream(stream)))
+
+
+def index_scores_view(layer: DeviceLayer, workspace: torch.Tensor) -> torch.Tensor:
+    """The [T][row] fp32 score matrix that v4a_index_scores left in `workspace`."""
+    a = layer.index_args(torch.empty(0, dtype=torch.int32))
+    off, row = C.c_size_t(), C.c_int64()
+    _check("v4a_index_scores_layout", lib().v4a_index_scores_layout(C.byref(a), C.byref(off), C.byref(row)))
+    T = layer.spec.tokens
+    return workspace[off.value: off.value + 4 * T * row.value].view(torch.float32).view(T, row.value)
 
 
 def attn_workspace_bytes(layer: DeviceLayer, with_idx: bool) -> int:

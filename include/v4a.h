@@ -60,6 +60,8 @@ extern "C" {
 #define V4A_DEV_BAD_BATCH  2  /* seq id out of range, positions not consecutive in a
                                  sequence's run, or a run longer than max_new_per_seq */
 #define V4A_DEV_BAD_INDEX  4  /* a selected entry index is >= the visible count */
+#define V4A_DEV_TIMEOUT    8  /* a bounded wait inside a tensor-core kernel gave up; that call's
+                                 outputs are incomplete (never expected; reported, never hung) */
 
 /* ---- formats ---------------------------------------------------------------- */
 /* Shared-K=V cache and window ring rows. */
@@ -198,6 +200,10 @@ V4A_API int v4a_index_topk(const v4a_index_args* args, void* workspace, size_t w
  * workspace is exactly v4a_index_topk. */
 V4A_API int v4a_index_scores(const v4a_index_args* args, void* workspace, size_t workspace_bytes,
                      void* stream);
+/* Where v4a_index_scores leaves the scores: query t's score of entry i is the
+ * float at byte offset (*offset + 4 * (t * *row_stride + i)) of the workspace,
+ * for i < the query's visible count. */
+V4A_API int v4a_index_scores_layout(const v4a_index_args* args, size_t* offset, int64_t* row_stride);
 V4A_API int v4a_index_select(const v4a_index_args* args, void* workspace, size_t workspace_bytes,
                      void* stream);
 

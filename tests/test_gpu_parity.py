@@ -171,6 +171,30 @@ def test_index_topk(name):
     assert swaps <= max(2, len(idx) // 4)
 
 
+@pytest.mark.parametrize("name", [_marks(n) for n in C4A])
+def test_index_scores_elementwise(name):
+    """Every visible entry's score against the oracle's fp64 score: relative
+    error within 1e-5 of the query's score scale (fp32 accumulation of exact
+    code products, then fp32 scales)."""
+    from compressed_sparse_long_c4a_gb300 import v4a
+    r = run_for(name)
+    L = r.layer()
+    step = v4a.Step(L)
+    v4a.index_scores(L, step.idx, step.ws_index)
+    torch.cuda.synchronize()
+    assert int(L.status.item()) == 0
+    sc = v4a.index_scores_view(L, step.ws_index).cpu().numpy()
+    _, scores = r.oracle_index_on_inputs()
+    worst = 0.0
+    for t, ref in scores.items():
+        got = sc[t, :ref.shape[0]].astype(np.float64)
+        scale = np.max(np.abs(ref))
+        err = np.max(np.abs(got - ref)) / scale
+        worst = max(worst, err)
+        assert err <= 1e-5, (name, t, err)
+    print(name, "max rel err", worst)
+
+
 @pytest.mark.parametrize("name", [_marks(n) for n in ALL])
 def test_sparse_attn(name):
     """Attention on a selection computed by the oracle (c4a) or on every
