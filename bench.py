@@ -75,7 +75,7 @@ class ClockSampler:
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -110,7 +110,7 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "window": "1 s of identical graph replays around the timed region"}
 
 
 def _dist():
@@ -257,7 +257,18 @@ def main():
     # ---- timed region: K graph replays ----
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    def busy(seconds):
+        # keeps the GPU under the same load around the (short) timed region so the
+        # clock samples describe the conditions the timed steps ran in
+        t_end = time.perf_counter() + seconds
+        with torch.cuda.stream(stream):
+            while time.perf_counter() < t_end:
+                for i in range(replicas):
+                    graphs[i].replay()
+                torch.cuda.synchronize()
+
     with ClockSampler(local) as clk:
+        busy(0.6)
         barrier()
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
@@ -267,6 +278,7 @@ def main():
             e1.record(stream)
         torch.cuda.synchronize()
         barrier()
+        busy(0.4)
     ms = e0.elapsed_time(e1) / args.steps
     if ws > 1:
         import torch.distributed as dist
@@ -285,6 +297,9 @@ def main():
         st = steps[i % replicas]
         L = st.layer
         with torch.cuda.stream(stream):
+            # a spin kernel holds the stream while the host queues every stage, so the
+            # events below bracket GPU execution only (no host launch gaps)
+            torch.cuda._sleep(2_000_000)
             ev[0].record(stream)
             v4a.compress_insert(L, stream)
             ev[1].record(stream)
@@ -347,21 +362,8 @@ def main():
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_ms = float(tt.item())
 
-    # ---- kernel launches per step (torch profiler over two graph-free steps) ----
-    launches = None
-    try:
-        from torch.profiler import profile, ProfilerActivity
-        with profile(activities=[ProfilerActivity.CUDA]) as prof:
-            with torch.cuda.stream(stream):
-                for i in range(2):
-                    steps[i % replicas].run(stream)
-            torch.cuda.synchronize()
-        ours = [e for e in prof.events() if e.device_type.name == "CUDA" and
-                any(k in e.name for k in ("compress_insert", "index_score", "topk_", "attn_", "inv_rope",
-                                          "v4a"))]
-        launches = len(ours) // 2 * args.steps
-    except Exception:
-        launches = None
+    # ---- our kernel launches in the timed region (per step, from the path taken) ----
+    launches = steps[0].launches_per_step() * args.steps
 
     clocks = clk.summary()
     line = {

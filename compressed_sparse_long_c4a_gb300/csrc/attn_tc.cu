@@ -1,10 +1,421 @@
-// tcgen05 sparse attention: placeholder until the tensor-core kernel lands.
+// Shared-K=V sparse attention on the tensor cores (tcgen05, kind::f16, bf16
+// operands, fp32 accumulate in TMEM), for decode-sized batches.
+//
+// Method: "DeepSeek V4 in vLLM: Efficient Long-context Attention", Background
+// (keys and values share one vector; attend to the top-k compressed entries
+// plus the 128 uncompressed window tokens) and Appendix ("why inverse RoPE":
+// o_m = sum_n softmax(q_m . k_n) k_n).
+//
+// One CTA per (64-key chunk of a query's key list, query):
+//   Q     [128 rows = heads, zero-padded][D] bf16  -> smem, K-major, 128-B swizzle
+//   K     64 gathered rows [64][D] bf16 (fp8 codes are converted exactly to
+//         bf16; their per-row scale is applied to the logits and to P)
+//   S     = Q K^T           M=128, N=64,  K=D   -> TMEM columns [0, 64)
+//   P     = exp(tau*s_n*S - m) * s_n, bf16 -> smem (one thread per head row)
+//   O     = P K             M=128, N=256 per MMA (K as an MN-major operand),
+//                           K=64              -> TMEM columns [0, D) (the S
+//                           columns are reused once S has been read)
+// The chunk's normalised O (bf16) and (max, sum) go to the workspace; a
+// combine kernel merges the chunks of each query.  A single thread issues
+// every MMA; completion is tracked with tcgen05.commit on mbarriers whose
+// waits are bounded.
+
+#include <mutex>
+
 #include "attn_tc.h"
+#include "tc_common.cuh"
 
 namespace v4a {
-size_t attn_tc_workspace_size(const v4a_attn_args*) { return 0; }
-bool attn_tc(const v4a_attn_args*, void*, size_t, cudaStream_t, int* rc) {
-  *rc = V4A_OK;
-  return false;
+namespace {
+
+constexpr int kKeys = 64;            // keys per CTA (one chunk)
+constexpr int kRows = 128;           // MMA M (heads, zero-padded)
+constexpr int kThreads = 128;
+
+struct AtcArgs {
+  int T, H, D, ratio, fmt, wfmt, wlen, wcap, k, splits;
+  const int32_t* seq_ids;
+  const int32_t* positions;
+  const int32_t* bt;
+  int max_blocks;
+  int64_t num_blocks;
+  const uint8_t* pool;
+  int64_t block_bytes;
+  const int32_t* idx;
+  const uint8_t* window;
+  const float* wscale;
+  const uint16_t* q;
+  float scale;
+  uint16_t* out;
+  float* lse;
+  uint16_t* part_o;   // [T][splits][H][D] bf16, normalised by the chunk's sum
+  float* part_ml;     // [T][splits][H][2] = (max, sum)
+  int32_t* status;
+  uint32_t idesc_s, idesc_pv;
+};
+
+struct ASmem {
+  uint64_t bar_s, bar_o;
+  uint32_t tmem_base;
+  int abort_flag;
+  const uint8_t* src[kKeys];
+  float kscale[kKeys];
+  int kfmt[kKeys];                  // -1: no key in this slot
+};
+
+// MN-major operand (B of P*K): 64-element (128-byte) rows along N, consecutive
+// K rows 128 bytes apart, 8-row groups 1024 bytes apart (SBO), the next
+// 64-element N chunk `lbo` bytes further (LBO), 128-byte swizzle.
+__device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t saddr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
 }
+
+__device__ __forceinline__ uint32_t bf16x2_from_e4m3x2(uint16_t two) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
+  const float2 f = __half22float2(__half2(h));
+  const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);   // exact: e4m3 values are bf16 values
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int D = a.D, nsub = D / 64;
+  uint8_t* Qs = base;                                  // nsub x [128 rows][128 B]
+  uint8_t* Ks = Qs + nsub * kRows * 128;               // nsub x [64 rows][128 B]
+  uint8_t* Ps = Ks + nsub * kKeys * 128;               // [128 rows][128 B]
+  ASmem& s = *reinterpret_cast<ASmem*>(Ps + kRows * 128);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t = blockIdx.y, sp = blockIdx.x;
+  const int b = a.seq_ids[t], m = a.positions[t];
+  const int nvis = (m + 1) / a.ratio;
+  const int nsel = a.idx ? a.k : nvis;
+  const int wstart = max(0, m - a.wlen + 1);
+  const int L = nsel + (m - wstart + 1);
+  const int lo = sp * kKeys;
+  const int64_t pi0 = int64_t(t) * a.splits + sp;
+
+  if (lo >= L) {   // this query's list is shorter than the longest: empty chunk
+    for (int h = tid; h < a.H; h += blockDim.x) {
+      a.part_ml[(pi0 * a.H + h) * 2] = -INFINITY;
+      a.part_ml[(pi0 * a.H + h) * 2 + 1] = 0.f;
+    }
+    return;
+  }
+  if (tid == 0) {
+    tc::mbar_init(&s.bar_s, 1);
+    tc::mbar_init(&s.bar_o, 1);
+    s.abort_flag = 0;
+    tc::mbar_fence_init();
+  }
+  __syncwarp();   // tcgen05.alloc is warp-collective: reconverge warp 0 after the init above
+  if (warp == 0) tc::tmem_alloc(&s.tmem_base, D < 64 ? 64 : D);
+
+  // ---- key slots of this chunk (sources, scales) ----
+  if (tid < kKeys) {
+    const int li = lo + tid;
+    const uint8_t* src = nullptr;
+    int f = -1;
+    float sc = 1.f;
+    if (li < L) {
+      if (li < nsel) {
+        const int e = a.idx ? a.idx[int64_t(t) * a.k + li] : li;
+        if (e >= 0) {
+          const int E = entries_per_block(a.ratio);
+          const int lb = e / E;
+          if (e >= nvis) {
+            report(a.status, V4A_DEV_BAD_INDEX);
+          } else if (lb >= a.max_blocks) {
+            report(a.status, V4A_DEV_BAD_BLOCK);
+          } else {
+            const int32_t blk = a.bt[int64_t(b) * a.max_blocks + lb];
+            if (blk < 0 || blk >= a.num_blocks) {
+              report(a.status, V4A_DEV_BAD_BLOCK);
+            } else {
+              const uint8_t* bb = a.pool + int64_t(blk) * a.block_bytes;
+              const int slot = e % E;
+              f = a.fmt;
+              src = bb + int64_t(slot) * (a.fmt == V4A_KV_BF16 ? 2 * D : D);
+              if (a.fmt == V4A_KV_FP8_TOKEN) sc = reinterpret_cast<const float*>(bb + int64_t(E) * D)[slot];
+            }
+          }
+        }
+      } else {
+        const int p = wstart + (li - nsel);
+        const int64_t slot = int64_t(b) * a.wcap + p % a.wcap;
+        f = a.wfmt;
+        src = a.window + slot * (a.wfmt == V4A_KV_BF16 ? 2 * D : D);
+        if (a.wfmt == V4A_KV_FP8_TOKEN) sc = a.wscale[slot];
+      }
+    }
+    s.src[tid] = src;
+    s.kscale[tid] = sc;
+    s.kfmt[tid] = f;
+  }
+  __syncthreads();
+
+  // ---- stage Q (rows >= H are zero) and K into swizzled smem ----
+  const uint16_t* qt = a.q + int64_t(t) * a.H * D;
+  const int qchunks = kRows * (D / 8);
+  for (int c = tid; c < qchunks; c += blockDim.x) {
+    const int r = c / (D / 8), cc = c % (D / 8);
+    uint8_t* dst = Qs + (cc >> 3) * (kRows * 128) + r * 128 + (((cc & 7) ^ (r & 7)) << 4);
+    if (r < a.H) {
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)),
+                   "l"(qt + int64_t(r) * D + cc * 8)
+                   : "memory");
+    } else {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  const int kchunks = kKeys * (D / 8);
+  for (int c = tid; c < kchunks; c += blockDim.x) {
+    const int r = c / (D / 8), cc = c % (D / 8);
+    uint8_t* dst = Ks + (cc >> 3) * (kKeys * 128) + r * 128 + (((cc & 7) ^ (r & 7)) << 4);
+    const int f = s.kfmt[r];
+    if (f == V4A_KV_BF16) {
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)),
+                   "l"(s.src[r] + cc * 16)
+                   : "memory");
+    } else if (f == V4A_KV_FP8_TOKEN) {
+      const uint2 codes = *reinterpret_cast<const uint2*>(s.src[r] + cc * 8);
+      uint4 v;
+      v.x = bf16x2_from_e4m3x2(uint16_t(codes.x & 0xffffu));
+      v.y = bf16x2_from_e4m3x2(uint16_t(codes.x >> 16));
+      v.z = bf16x2_from_e4m3x2(uint16_t(codes.y & 0xffffu));
+      v.w = bf16x2_from_e4m3x2(uint16_t(codes.y >> 16));
+      *reinterpret_cast<uint4*>(dst) = v;
+    } else {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  tc::fence_proxy_async();
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+  volatile int* abort_flag = &s.abort_flag;
+
+  // ---- S = Q K^T ----
+  if (tid == 0) {
+    const uint32_t q0 = tc::smem_u32(Qs), k0 = tc::smem_u32(Ks);
+    for (int st = 0; st < D / 16; ++st) {
+      const uint64_t ad = tc::desc_sw128(q0 + (st >> 2) * (kRows * 128)) + 2 * (st & 3);
+      const uint64_t bd = tc::desc_sw128(k0 + (st >> 2) * (kKeys * 128)) + 2 * (st & 3);
+      tc::mma_f16(tmem, ad, bd, a.idesc_s, st > 0);
+    }
+    tc::mma_commit(&s.bar_s);
+  }
+  // ---- softmax: thread = head row ----
+  const int row = tid;                           // warp w reads TMEM lanes 32w..32w+31
+  const uint32_t lane_addr = tmem + (uint32_t(warp * 32) << 16);
+  // Collective tcgen05 loads below are always executed by whole warps; `ok`
+  // is made warp-uniform and only gates the arithmetic and the stores.
+  bool ok = __all_sync(0xffffffffu, tc::mbar_wait(&s.bar_s, 0, a.status, abort_flag));
+  tc::tc_fence_after();
+  float mx = -INFINITY, l = 0.f;
+  {
+    float v[64];
+    tc::tmem_ld64(lane_addr, v);
+#pragma unroll
+    for (int n = 0; n < 64; ++n) {
+      const float z = s.kfmt[n] >= 0 ? v[n] * a.scale * s.kscale[n] : -INFINITY;
+      v[n] = z;
+      mx = fmaxf(mx, z);
+    }
+    uint32_t pk[32];
+#pragma unroll
+    for (int n = 0; n < 64; n += 2) {
+      const float p0 = s.kfmt[n] >= 0 ? __expf(v[n] - mx) : 0.f;
+      const float p1 = s.kfmt[n + 1] >= 0 ? __expf(v[n + 1] - mx) : 0.f;
+      l += p0 + p1;
+      const __nv_bfloat162 pb = __floats2bfloat162_rn(p0 * s.kscale[n], p1 * s.kscale[n + 1]);
+      pk[n >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      *reinterpret_cast<uint4*>(Ps + row * 128 + ((c ^ (row & 7)) << 4)) =
+          make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+  }
+  tc::fence_proxy_async();
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  // ---- O = P K (S columns are free again) ----
+  if (tid == 0 && !*abort_flag) {
+    const uint32_t p0 = tc::smem_u32(Ps), k0 = tc::smem_u32(Ks);
+    const int halves = D > 256 ? D / 256 : 1;
+    const int nchunk = D > 256 ? 4 : nsub;        // 64-column N chunks per MMA
+    for (int st = 0; st < kKeys / 16; ++st) {
+      const uint64_t ad = tc::desc_sw128(p0) + 2 * st;
+      for (int hf = 0; hf < halves; ++hf) {
+        const uint64_t bd =
+            desc_sw128_mn(k0 + hf * nchunk * (kKeys * 128) + st * 16 * 128, kKeys * 128);
+        tc::mma_f16(tmem + hf * 256, ad, bd, a.idesc_pv, st > 0);
+      }
+    }
+    tc::mma_commit(&s.bar_o);
+  }
+  ok = __all_sync(0xffffffffu, ok && tc::mbar_wait(&s.bar_o, 0, a.status, abort_flag));
+  tc::tc_fence_after();
+  const bool store = ok && row < a.H;   // H need not be a multiple of 32: loads stay warp-wide
+  {
+    const float inv = 1.f / l;
+    const bool direct = a.splits == 1;
+    uint16_t* dst = direct ? a.out + (int64_t(t) * a.H + row) * D : a.part_o + (pi0 * a.H + row) * D;
+    for (int c = 0; c < nsub; ++c) {
+      float v[64];
+      tc::tmem_ld64(lane_addr + c * 64, v);
+      if (!store) continue;
+#pragma unroll
+      for (int i = 0; i < 64; i += 8) {
+        uint4 o;
+        __nv_bfloat162 b0 = __floats2bfloat162_rn(v[i] * inv, v[i + 1] * inv);
+        __nv_bfloat162 b1 = __floats2bfloat162_rn(v[i + 2] * inv, v[i + 3] * inv);
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(v[i + 4] * inv, v[i + 5] * inv);
+        __nv_bfloat162 b3 = __floats2bfloat162_rn(v[i + 6] * inv, v[i + 7] * inv);
+        o.x = *reinterpret_cast<uint32_t*>(&b0);
+        o.y = *reinterpret_cast<uint32_t*>(&b1);
+        o.z = *reinterpret_cast<uint32_t*>(&b2);
+        o.w = *reinterpret_cast<uint32_t*>(&b3);
+        *reinterpret_cast<uint4*>(dst + c * 64 + i) = o;
+      }
+    }
+    if (!store) {
+    } else if (direct) {
+      if (a.lse) a.lse[int64_t(t) * a.H + row] = mx + logf(l);
+    } else {
+      a.part_ml[(pi0 * a.H + row) * 2] = mx;
+      a.part_ml[(pi0 * a.H + row) * 2 + 1] = l;
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, D < 64 ? 64 : D);
+  }
+}
+
+// out = sum_s w_s * O_s with w_s = l_s e^{m_s} / sum_s' l_s' e^{m_s'}; one CTA per (head, query).
+__global__ void attn_combine_bf16(int H, int D, int splits, const uint16_t* part_o, const float* part_ml,
+                                  uint16_t* out, float* lse) {
+  const int t = blockIdx.y, h = blockIdx.x;
+  __shared__ float wsm[512];
+  __shared__ float tot_s;
+  float mx = -INFINITY;
+  for (int s = 0; s < splits; ++s) mx = fmaxf(mx, part_ml[((int64_t(t) * splits + s) * H + h) * 2]);
+  for (int s = threadIdx.x; s < splits; s += blockDim.x) {
+    const int64_t pi = (int64_t(t) * splits + s) * H + h;
+    const float ms = part_ml[pi * 2];
+    wsm[s] = ms == -INFINITY ? 0.f : part_ml[pi * 2 + 1] * __expf(ms - mx);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float tot = 0.f;
+    for (int s = 0; s < splits; ++s) tot += wsm[s];
+    tot_s = tot;
+    if (lse) lse[int64_t(t) * H + h] = mx + logf(tot);
+  }
+  __syncthreads();
+  const float inv = 1.f / tot_s;
+  for (int d = threadIdx.x * 2; d < D; d += blockDim.x * 2) {
+    float a0 = 0.f, a1 = 0.f;
+    for (int s = 0; s < splits; ++s) {
+      const float w = wsm[s];
+      if (w == 0.f) continue;
+      const uint32_t v = *reinterpret_cast<const uint32_t*>(part_o + ((int64_t(t) * splits + s) * H + h) * D + d);
+      a0 = fmaf(w, bf16_to_f32(uint16_t(v & 0xffffu)), a0);
+      a1 = fmaf(w, bf16_to_f32(uint16_t(v >> 16)), a1);
+    }
+    *reinterpret_cast<uint32_t*>(out + (int64_t(t) * H + h) * D + d) =
+        uint32_t(f32_to_bf16(a0 * inv)) | (uint32_t(f32_to_bf16(a1 * inv)) << 16);
+  }
+}
+
+int splits_of(const v4a_attn_args* a) {
+  const int E = entries_per_block(a->kv.ratio);
+  const int64_t nsel = a->idx ? a->k : int64_t(a->kv.max_blocks) * E;
+  return int((nsel + a->window_len + kKeys - 1) / kKeys);
+}
+
+// The chunked tensor-core path serves decode-sized batches: one CTA per 64
+// keys of each query, so the CTA count is T * splits.  Long prefill batches
+// use the CUDA-core path (one CTA walks a whole split of a query).
+bool handled(const v4a_attn_args* a) {
+  const int D = a->kv.dim;
+  if (D != 128 && D != 256 && D != 512) return false;
+  if (a->num_heads > kRows) return false;
+  const int64_t ctas = int64_t(a->batch.num_tokens) * splits_of(a);
+  if (ctas > 16 * 152) return false;
+  if (splits_of(a) > 512) return false;
+  return true;
+}
+
+}  // namespace
+
+size_t attn_tc_workspace_size(const v4a_attn_args* a) {
+  if (!handled(a)) return 0;
+  const size_t T = a->batch.num_tokens, S = splits_of(a), H = a->num_heads, D = a->kv.dim;
+  return T * S * H * D * 2 + T * S * H * 2 * 4 + 512;
+}
+
+bool attn_tc(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t stream, int* rc) {
+  *rc = V4A_OK;
+  if (!handled(a)) return false;
+  if (ws_bytes < attn_tc_workspace_size(a)) { *rc = V4A_ERR_WORKSPACE; return true; }
+  AtcArgs t{};
+  t.T = a->batch.num_tokens;
+  t.H = a->num_heads;
+  t.D = a->kv.dim;
+  t.ratio = a->kv.ratio;
+  t.fmt = a->kv.format;
+  t.wfmt = a->window_format;
+  t.wlen = a->window_len;
+  t.wcap = a->window_cap;
+  t.k = a->k;
+  t.splits = splits_of(a);
+  t.seq_ids = a->batch.seq_ids;
+  t.positions = a->batch.positions;
+  t.bt = a->kv.block_table;
+  t.max_blocks = a->kv.max_blocks;
+  t.num_blocks = a->kv.num_blocks;
+  t.pool = static_cast<const uint8_t*>(a->kv.pool);
+  t.block_bytes = kv_block_bytes(a->kv.format, a->kv.ratio, a->kv.dim);
+  t.idx = a->idx;
+  t.window = static_cast<const uint8_t*>(a->window);
+  t.wscale = a->window_scale;
+  t.q = a->q;
+  t.scale = a->softmax_scale;
+  t.out = a->out;
+  t.lse = a->lse;
+  const size_t T = t.T, S = t.splits, H = t.H, D = t.D;
+  t.part_o = static_cast<uint16_t*>(ws);
+  t.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + ((T * S * H * D * 2 + 255) & ~size_t(255)));
+  t.status = a->status;
+  t.idesc_s = tc::make_idesc(1, 1, kRows, kKeys);
+  t.idesc_pv = tc::make_idesc(1, 1, kRows, D > 256 ? 256 : D) | (1u << 16);   // B is MN-major
+  // At least 116 KB so that no two CTAs of a TMEM-allocating kernel ever share
+  // an SM: every tcgen05 kernel in this library runs one CTA per SM.
+  size_t smem = 1024 + D * kRows * 2 + D * kKeys * 2 + kRows * 128 + sizeof(ASmem);
+  if (smem < 116 * 1024) smem = 116 * 1024;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute(attn_chunk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  });
+  if (smem > 227 * 1024) return false;
+  attn_chunk_tc<<<dim3(t.splits, t.T), kThreads, smem, stream>>>(t);
+  if (t.splits > 1)
+    attn_combine_bf16<<<dim3(t.H, t.T), 128, 0, stream>>>(t.H, t.D, t.splits, t.part_o, t.part_ml, t.out, t.lse);
+  if (cudaGetLastError() != cudaSuccess) *rc = V4A_ERR_CUDA;
+  return true;
+}
+
 }  // namespace v4a

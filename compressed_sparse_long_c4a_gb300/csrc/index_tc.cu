@@ -155,6 +155,7 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap tmap) {
     tc::mbar_fence_init();
   }
   if (warp == 0 && lane == 0) tc::prefetch_tmap(&tmap);
+  __syncwarp();   // tcgen05.alloc is warp-collective
   if (warp == 1) tc::tmem_alloc(&s.tmem_base, 2 * a.acc_cols);
   for (int i = threadIdx.x; i < 4 * kHist; i += blockDim.x) hist_all[i] = 0;
   tc::tc_fence_before();
@@ -297,7 +298,8 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap tmap) {
         b = a.seq_ids[t];
         n = visible_of(a, t);
         srow = a.scores + int64_t(t) * a.row;
-        if (!tc::mbar_wait(&s.qfull[qi & 1], (qi >> 1) & 1, a.status, abort_flag)) break;
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(&s.qfull[qi & 1], (qi >> 1) & 1, a.status, abort_flag)))
+          break;
         wq = s.wq[qi & 1];
       }
       const int e = j * 128 + row;
@@ -319,7 +321,8 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap tmap) {
           }
         }
       }
-      if (!tc::mbar_wait(&s.tfull[acc], aphase, a.status, abort_flag)) break;
+      // warp-uniform decision: the tcgen05.ld below is warp-collective
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&s.tfull[acc], aphase, a.status, abort_flag))) break;
       tc::tc_fence_after();
       float score;
       const uint32_t acc_addr = lane_addr + acc * a.acc_cols;

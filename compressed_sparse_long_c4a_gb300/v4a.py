@@ -282,6 +282,17 @@ class Step:
         self.ws_attn = torch.empty(max(attn_workspace_bytes(layer, s.ix_heads > 0), 256),
                                    dtype=torch.uint8, device=dev)
 
+    def launches_per_step(self) -> int:
+        """libv4a kernels one run() launches: compress (1); indexer scan (1) +
+        top-k (1 for rows that fit in shared memory, else histogram + select);
+        attention (1, + combine when the key list is split); output (1)."""
+        s = self.layer.spec
+        n = 1
+        if s.ix_heads:
+            n += 1 + (1 if s.max_blocks * 64 <= 32768 else 2)
+        n += 1 + (1 if self.ws_attn.numel() > 256 else 0)
+        return n + 1
+
     def run(self, stream=None):
         """compress_insert -> index_topk -> sparse_attn -> inv_rope_quant."""
         L = self.layer
