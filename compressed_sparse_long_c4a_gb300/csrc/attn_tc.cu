@@ -174,26 +174,44 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a) {
       *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
     }
   }
+  // keys: bf16 rows go straight to smem with cp.async; fp8 rows are loaded
+  // into registers first (all loads in flight together), then converted
+  // exactly to bf16 and stored swizzled.
   const int kchunks = kKeys * (D / 8);
-  for (int c = tid; c < kchunks; c += blockDim.x) {
+  constexpr int kMaxPer = kKeys * (512 / 8) / kThreads;   // 32 for D = 512
+  uint2 raw[kMaxPer];
+#pragma unroll
+  for (int i = 0; i < kMaxPer; ++i) {
+    const int c = tid + i * kThreads;
+    raw[i] = make_uint2(0, 0);
+    if (c >= kchunks) continue;
     const int r = c / (D / 8), cc = c % (D / 8);
-    uint8_t* dst = Ks + (cc >> 3) * (kKeys * 128) + r * 128 + (((cc & 7) ^ (r & 7)) << 4);
     const int f = s.kfmt[r];
     if (f == V4A_KV_BF16) {
+      uint8_t* dst = Ks + (cc >> 3) * (kKeys * 128) + r * 128 + (((cc & 7) ^ (r & 7)) << 4);
       asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)),
                    "l"(s.src[r] + cc * 16)
                    : "memory");
     } else if (f == V4A_KV_FP8_TOKEN) {
-      const uint2 codes = *reinterpret_cast<const uint2*>(s.src[r] + cc * 8);
-      uint4 v;
-      v.x = bf16x2_from_e4m3x2(uint16_t(codes.x & 0xffffu));
-      v.y = bf16x2_from_e4m3x2(uint16_t(codes.x >> 16));
-      v.z = bf16x2_from_e4m3x2(uint16_t(codes.y & 0xffffu));
-      v.w = bf16x2_from_e4m3x2(uint16_t(codes.y >> 16));
-      *reinterpret_cast<uint4*>(dst) = v;
-    } else {
-      *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+      raw[i] = __ldg(reinterpret_cast<const uint2*>(s.src[r] + cc * 8));
     }
+  }
+#pragma unroll
+  for (int i = 0; i < kMaxPer; ++i) {
+    const int c = tid + i * kThreads;
+    if (c >= kchunks) continue;
+    const int r = c / (D / 8), cc = c % (D / 8);
+    const int f = s.kfmt[r];
+    if (f == V4A_KV_BF16) continue;
+    uint8_t* dst = Ks + (cc >> 3) * (kKeys * 128) + r * 128 + (((cc & 7) ^ (r & 7)) << 4);
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (f == V4A_KV_FP8_TOKEN) {
+      v.x = bf16x2_from_e4m3x2(uint16_t(raw[i].x & 0xffffu));
+      v.y = bf16x2_from_e4m3x2(uint16_t(raw[i].x >> 16));
+      v.z = bf16x2_from_e4m3x2(uint16_t(raw[i].y & 0xffffu));
+      v.w = bf16x2_from_e4m3x2(uint16_t(raw[i].y >> 16));
+    }
+    *reinterpret_cast<uint4*>(dst) = v;
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
   tc::fence_proxy_async();
@@ -267,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a) {
   tc::tc_fence_after();
   const bool store = ok && row < a.H;   // H need not be a multiple of 32: loads stay warp-wide
   {
-    const float inv = 1.f / l;
+    const float inv = l > 0.f ? 1.f / l : 0.f;   // a chunk of only padding (-1) entries has l = 0
     const bool direct = a.splits == 1;
     uint16_t* dst = direct ? a.out + (int64_t(t) * a.H + row) * D : a.part_o + (pi0 * a.H + row) * D;
     for (int c = 0; c < nsub; ++c) {
@@ -304,40 +322,58 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a) {
   }
 }
 
-// out = sum_s w_s * O_s with w_s = l_s e^{m_s} / sum_s' l_s' e^{m_s'}; one CTA per (head, query).
+// out = sum_s w_s * O_s with w_s = l_s e^{m_s} / sum_s' l_s' e^{m_s'}.
+// One CTA of D/8 threads per (head, query); each thread owns 8 dims and
+// keeps all of its split loads in flight together.
 __global__ void attn_combine_bf16(int H, int D, int splits, const uint16_t* part_o, const float* part_ml,
                                   uint16_t* out, float* lse) {
   const int t = blockIdx.y, h = blockIdx.x;
   __shared__ float wsm[512];
-  __shared__ float tot_s;
+  __shared__ float inv_s;
+  const float* ml = part_ml + (int64_t(t) * splits * H + h) * 2;
   float mx = -INFINITY;
-  for (int s = 0; s < splits; ++s) mx = fmaxf(mx, part_ml[((int64_t(t) * splits + s) * H + h) * 2]);
+  for (int s = 0; s < splits; ++s) mx = fmaxf(mx, ml[int64_t(s) * H * 2]);
   for (int s = threadIdx.x; s < splits; s += blockDim.x) {
-    const int64_t pi = (int64_t(t) * splits + s) * H + h;
-    const float ms = part_ml[pi * 2];
-    wsm[s] = ms == -INFINITY ? 0.f : part_ml[pi * 2 + 1] * __expf(ms - mx);
+    const float ms = ml[int64_t(s) * H * 2];
+    wsm[s] = ms == -INFINITY ? 0.f : ml[int64_t(s) * H * 2 + 1] * __expf(ms - mx);
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     float tot = 0.f;
     for (int s = 0; s < splits; ++s) tot += wsm[s];
-    tot_s = tot;
+    inv_s = 1.f / tot;
     if (lse) lse[int64_t(t) * H + h] = mx + logf(tot);
   }
   __syncthreads();
-  const float inv = 1.f / tot_s;
-  for (int d = threadIdx.x * 2; d < D; d += blockDim.x * 2) {
-    float a0 = 0.f, a1 = 0.f;
-    for (int s = 0; s < splits; ++s) {
-      const float w = wsm[s];
-      if (w == 0.f) continue;
-      const uint32_t v = *reinterpret_cast<const uint32_t*>(part_o + ((int64_t(t) * splits + s) * H + h) * D + d);
-      a0 = fmaf(w, bf16_to_f32(uint16_t(v & 0xffffu)), a0);
-      a1 = fmaf(w, bf16_to_f32(uint16_t(v >> 16)), a1);
+  const int d = threadIdx.x * 8;
+  if (d >= D) return;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const uint16_t* po = part_o + (int64_t(t) * splits * H + h) * D + d;
+  constexpr int kUnroll = 8;
+  for (int s0 = 0; s0 < splits; s0 += kUnroll) {
+    uint4 v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      v[u] = (s0 + u < splits) ? *reinterpret_cast<const uint4*>(po + int64_t(s0 + u) * H * D)
+                               : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const float w = (s0 + u < splits) ? wsm[s0 + u] : 0.f;
+      if (w == 0.f) continue;   // empty chunk: its partial carries no weight (and may be garbage)
+      const uint32_t q[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = fmaf(w, bf16_to_f32(uint16_t(q[i] & 0xffffu)), acc[2 * i]);
+        acc[2 * i + 1] = fmaf(w, bf16_to_f32(uint16_t(q[i] >> 16)), acc[2 * i + 1]);
+      }
     }
-    *reinterpret_cast<uint32_t*>(out + (int64_t(t) * H + h) * D + d) =
-        uint32_t(f32_to_bf16(a0 * inv)) | (uint32_t(f32_to_bf16(a1 * inv)) << 16);
   }
+  const float inv = inv_s;
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    o[i] = uint32_t(f32_to_bf16(acc[2 * i] * inv)) | (uint32_t(f32_to_bf16(acc[2 * i + 1] * inv)) << 16);
+  *reinterpret_cast<uint4*>(out + (int64_t(t) * H + h) * D + d) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 int splits_of(const v4a_attn_args* a) {
@@ -413,7 +449,8 @@ bool attn_tc(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t str
   if (smem > 227 * 1024) return false;
   attn_chunk_tc<<<dim3(t.splits, t.T), kThreads, smem, stream>>>(t);
   if (t.splits > 1)
-    attn_combine_bf16<<<dim3(t.H, t.T), 128, 0, stream>>>(t.H, t.D, t.splits, t.part_o, t.part_ml, t.out, t.lse);
+    attn_combine_bf16<<<dim3(t.H, t.T), t.D / 8 < 32 ? 32 : t.D / 8, 0, stream>>>(t.H, t.D, t.splits, t.part_o,
+                                                                                t.part_ml, t.out, t.lse);
   if (cudaGetLastError() != cudaSuccess) *rc = V4A_ERR_CUDA;
   return true;
 }

@@ -23,6 +23,7 @@
 namespace v4a {
 
 struct CompressSide {
+  RopeFreq rope;
   int active, is_indexer;
   int ratio, dim, rope_dims, format;
   float theta, eps;
@@ -40,6 +41,7 @@ struct CompressSide {
 };
 
 struct WindowSide {
+  RopeFreq rope;
   int active, dim, rope_dims, format;
   float theta;
   const uint16_t* k;
@@ -197,7 +199,7 @@ __device__ void compress_token(const CompressSide& c, const BatchDev& bt, int t,
     const int first = c.dim - c.rope_dims;
     if (2 * p >= first) {
       float cs, sn;
-      rope_cos_sin(P, (2 * p - first) >> 1, c.rope_dims, c.theta, &cs, &sn);
+      rope_cos_sin(P, c.rope.inv[(2 * p - first) >> 1], &cs, &sn);
       const float x0 = v0, x1 = v1;
       v0 = x0 * cs - x1 * sn;
       v1 = x0 * sn + x1 * cs;
@@ -241,7 +243,7 @@ __device__ void window_token(const WindowSide& w, int t, int b, int P) {
     const int first = w.dim - w.rope_dims;
     if (2 * p >= first) {
       float cs, sn;
-      rope_cos_sin(P, (2 * p - first) >> 1, w.rope_dims, w.theta, &cs, &sn);
+      rope_cos_sin(P, w.rope.inv[(2 * p - first) >> 1], &cs, &sn);
       const float x0 = v0, x1 = v1;
       v0 = x0 * cs - x1 * sn;
       v1 = x0 * sn + x1 * cs;
@@ -289,6 +291,8 @@ static int fill_side(const v4a_compressor* c, bool indexer, CompressSide* s, int
       return V4A_ERR_INVALID_ARG;
     if (k.format == V4A_IX_FP8_B128 && k.dim % 128) return V4A_ERR_UNSUPPORTED;
   }
+  if (k.rope_dims > 128) return V4A_ERR_UNSUPPORTED;
+  s->rope = make_rope_freq(k.rope_dims, k.rope_theta);
   s->active = 1;
   s->is_indexer = indexer;
   s->ratio = k.ratio; s->dim = k.dim; s->rope_dims = k.rope_dims; s->format = k.format;
@@ -321,6 +325,8 @@ int compress_insert(const v4a_compress_args* a, cudaStream_t stream) {
     if (w.format != V4A_KV_BF16 && w.format != V4A_KV_FP8_TOKEN) return V4A_ERR_INVALID_ARG;
     if (w.format == V4A_KV_FP8_TOKEN && !w.ring_scale) return V4A_ERR_INVALID_ARG;
     if (w.ring_cap < 127 + B.max_new_per_seq) return V4A_ERR_RING_TOO_SMALL;
+    if (w.rope_dims > 128) return V4A_ERR_UNSUPPORTED;
+    ws.rope = make_rope_freq(w.rope_dims, w.rope_theta);
     ws.active = 1; ws.dim = w.dim; ws.rope_dims = w.rope_dims; ws.format = w.format;
     ws.theta = w.rope_theta; ws.k = w.k; ws.ring = static_cast<uint8_t*>(w.ring);
     ws.ring_scale = w.ring_scale; ws.ring_cap = w.ring_cap;

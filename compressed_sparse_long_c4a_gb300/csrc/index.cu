@@ -15,7 +15,7 @@
 //                         radix select of the k-th largest (score, -index)
 //                         composite, then an ordered compaction.
 //  * topk_hist / topk_select - long rows: a 4096-bin histogram of the score
-//                         keys (fused into the tcgen05 scan when it runs),
+//                         keys,
 //                         then every CTA compacts its slice (bins above the
 //                         threshold bin are taken, the threshold bin goes to a
 //                         candidate list) and the last CTA of a query resolves
@@ -37,9 +37,9 @@ constexpr int kMaxK = 16384;
 
 struct IndexWs {
   float* scores;        // [T][row]
-  uint32_t* hist;       // [T][kHistBins]
+  uint32_t* hist;       // [T][kHistBins]   top 12 key bits of every score
+  uint32_t* hist2;      // [T][kHistBins]   next 12 bits of the threshold bin's scores
   uint32_t* counters;   // [T][4]: selected, candidates, done, resolved
-  uint32_t* flag;       // 1 word: ~0 when stage 1 already built the histogram
   uint64_t* cand;       // [T][row]
   int32_t* sel;         // [T][k]
   int64_t row;
@@ -57,8 +57,8 @@ static IndexWs ws_layout(const v4a_index_args* a, void* base) {
   size_t off = 0;
   auto take = [&](size_t bytes) { char* r = p ? p + off : nullptr; off += round_up(bytes, 256); return r; };
   w.hist = reinterpret_cast<uint32_t*>(take(size_t(T) * kHistBins * 4));
-  w.counters = reinterpret_cast<uint32_t*>(take(size_t(T) * 4 * 4 + 4));
-  w.flag = w.counters ? w.counters + size_t(T) * 4 : nullptr;
+  w.hist2 = reinterpret_cast<uint32_t*>(take(size_t(T) * kHistBins * 4));
+  w.counters = reinterpret_cast<uint32_t*>(take(size_t(T) * 4 * 4));
   w.zero_bytes = off;
   w.scores = reinterpret_cast<float*>(take(size_t(T) * w.row * 4));
   if (w.row > kSmemTopkMax) {
@@ -278,12 +278,11 @@ __global__ void __launch_bounds__(1024) topk_smem(const float* scores, int64_t r
 
 __global__ void __launch_bounds__(512) topk_hist(const float* scores, int64_t row, int max_entries,
                                                 const int32_t* positions, int k, int slices,
-                                                uint32_t* hist, const uint32_t* flag) {
+                                                uint32_t* hist) {
   __shared__ uint32_t h_s[kHistBins];
   const int t = blockIdx.y;
   const int n = min((positions[t] + 1) / 4, max_entries);
   if (n <= k) return;
-  if (*flag == 0xFFFFFFFFu) return;   // the tensor-core scan already built the histogram
   for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h_s[i] = 0;
   __syncthreads();
   const int per = (n + slices - 1) / slices;
@@ -297,27 +296,14 @@ __global__ void __launch_bounds__(512) topk_hist(const float* scores, int64_t ro
     if (h_s[i]) atomicAdd(&g[i], h_s[i]);
 }
 
-__global__ void __launch_bounds__(1024) topk_select(const float* scores, int64_t row, int max_entries,
-                                                   const int32_t* positions, int k, int slices,
-                                                   const uint32_t* hist, uint32_t* counters,
-                                                   uint64_t* cand, int32_t* sel, int32_t* out) {
-  extern __shared__ int32_t sort_s[];   // [pow2 >= k] (last CTA only)
-  __shared__ uint32_t scan[40];
-  __shared__ uint32_t hist256[256];
-  __shared__ uint32_t sh[4];
-  __shared__ int tbin_s;
-  __shared__ uint32_t above_s;
-  __shared__ int last_s;
-  const int t = blockIdx.y;
-  const int n = min((positions[t] + 1) / 4, max_entries);
-  int32_t* o = out + int64_t(t) * k;
-  if (n <= k) {
-    if (blockIdx.x == 0) write_all_visible(o, n, k);
-    return;
-  }
-  // 1. threshold bin from the histogram (bins scanned from the top, 4 per thread)
-  const uint32_t* h = hist + int64_t(t) * kHistBins;
+// Threshold bin of a 4096-bin histogram: the bin b such that fewer than `need`
+// counts lie strictly above it and at least `need` at or above it.  Block of
+// 1024 threads, 4 bins each (scanned from the top).  Returns b and, through
+// *above, the count strictly above it.
+__device__ int threshold_bin(const uint32_t* h, uint32_t need, uint32_t* scan, int* bin_s,
+                             uint32_t* above_s, uint32_t* above) {
   uint32_t loc[4], s4 = 0;
+#pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int bin = kHistBins - 1 - (threadIdx.x * 4 + q);
     loc[q] = bin >= 0 ? h[bin] : 0;
@@ -325,31 +311,67 @@ __global__ void __launch_bounds__(1024) topk_select(const float* scores, int64_t
   }
   uint32_t total;
   const uint32_t excl = block_excl_scan(s4, scan, &total);
-  if (excl < uint32_t(k) && uint32_t(k) <= excl + s4) {
+  if (excl < need && need <= excl + s4) {
     uint32_t acc = excl;
     int q = 0;
     for (; q < 4; ++q) {
-      if (acc + loc[q] >= uint32_t(k)) break;
+      if (acc + loc[q] >= need) break;
       acc += loc[q];
     }
-    tbin_s = kHistBins - 1 - (threadIdx.x * 4 + q);
-    above_s = acc;
+    *bin_s = kHistBins - 1 - (threadIdx.x * 4 + q);
+    *above_s = acc;
   }
   __syncthreads();
-  const uint32_t tbin = uint32_t(tbin_s);
-  // 2. compact this CTA's slice
+  *above = *above_s;
+  const int b = *bin_s;
+  __syncthreads();
+  return b;
+}
+
+constexpr int kFine = 2048;   // capacity of the last CTA's exact-resolve list
+
+__global__ void __launch_bounds__(1024) topk_select(const float* scores, int64_t row, int max_entries,
+                                                   const int32_t* positions, int k, int slices,
+                                                   const uint32_t* hist, uint32_t* hist2,
+                                                   uint32_t* counters, uint64_t* cand, int32_t* sel,
+                                                   int32_t* out) {
+  extern __shared__ int32_t sort_s[];   // [pow2 >= k] (last CTA only)
+  __shared__ uint32_t scan[40];
+  __shared__ uint32_t h2_s[kHistBins];
+  __shared__ uint64_t fine_s[kFine];
+  __shared__ uint32_t hist256[256];
+  __shared__ uint32_t sh[4];
+  __shared__ int bin_s;
+  __shared__ uint32_t above_s;
+  __shared__ int last_s;
+  __shared__ uint32_t nfine_s;
+  const int t = blockIdx.y;
+  const int n = min((positions[t] + 1) / 4, max_entries);
+  int32_t* o = out + int64_t(t) * k;
+  if (n <= k) {
+    if (blockIdx.x == 0) write_all_visible(o, n, k);
+    return;
+  }
+  // 1. threshold bin of the top 12 key bits
+  uint32_t above1;
+  const uint32_t tbin = uint32_t(threshold_bin(hist + int64_t(t) * kHistBins, uint32_t(k), scan, &bin_s,
+                                               &above_s, &above1));
+  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h2_s[i] = 0;
+  __syncthreads();
+  // 2. compact this CTA's slice: above the bin -> selected, in the bin -> candidates
+  //    (and their next 12 key bits into the second-level histogram)
   uint32_t* cnt = counters + int64_t(t) * 4;
   uint64_t* cd = cand + int64_t(t) * row;
   int32_t* sl = sel + int64_t(t) * k;
   const int per = (n + slices - 1) / slices;
   const int lo = blockIdx.x * per, hi = min(n, lo + per);
-  const float* s = scores + int64_t(t) * row;
+  const float* sc = scores + int64_t(t) * row;
   const int lane = threadIdx.x & 31;
   for (int base = lo; base < hi; base += blockDim.x) {
     const int i = base + threadIdx.x;
     uint32_t key = 0, bin = 0;
     const bool in = i < hi;
-    if (in) { key = float_key(s[i]); bin = key >> 20; }
+    if (in) { key = float_key(sc[i]); bin = key >> 20; }
     const bool take = in && bin > tbin;
     const bool maybe = in && bin == tbin;
     const uint32_t mt = __ballot_sync(0xffffffffu, take);
@@ -363,8 +385,15 @@ __global__ void __launch_bounds__(1024) topk_select(const float* scores, int64_t
     bm = __shfl_sync(0xffffffffu, bm, 0);
     const uint32_t below = (1u << lane) - 1u;
     if (take) sl[bt + __popc(mt & below)] = i;
-    if (maybe) cd[bm + __popc(mm & below)] = composite(key, i);
+    if (maybe) {
+      cd[bm + __popc(mm & below)] = composite(key, i);
+      atomicAdd(&h2_s[(key >> 8) & (kHistBins - 1)], 1u);
+    }
   }
+  __syncthreads();
+  uint32_t* g2 = hist2 + int64_t(t) * kHistBins;
+  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x)
+    if (h2_s[i]) atomicAdd(&g2[i], h2_s[i]);
   // 3. the last CTA of this query resolves the threshold bin and sorts
   __threadfence();
   __syncthreads();
@@ -376,16 +405,55 @@ __global__ void __launch_bounds__(1024) topk_select(const float* scores, int64_t
   const int nc = int(__ldcg(&cnt[1]));
   const int need = k - int(above);
   if (need > 0) {
-    const uint64_t thr = select_threshold(
-        nc, need, [&](int i) { return __ldcg(&cd[i]); }, hist256, sh);
+    for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h2_s[i] = __ldcg(&g2[i]);
+    if (threadIdx.x == 0) nfine_s = 0;
+    __syncthreads();
+    uint32_t above2;
+    const uint32_t tbin2 = uint32_t(threshold_bin(h2_s, uint32_t(need), scan, &bin_s, &above_s, &above2));
+    const bool fits = h2_s[tbin2] <= uint32_t(kFine);
+    // candidates above the sub-bin are taken; the sub-bin's go to the fine list
     for (int base = 0; base < nc; base += blockDim.x) {
       const int i = base + threadIdx.x;
-      const bool take = i < nc && __ldcg(&cd[i]) >= thr;
+      uint64_t c = 0;
+      uint32_t b2 = 0;
+      if (i < nc) { c = __ldcg(&cd[i]); b2 = uint32_t(c >> 40) & (kHistBins - 1); }
+      const bool take = i < nc && b2 > tbin2;
       const uint32_t mt = __ballot_sync(0xffffffffu, take);
       uint32_t bt = 0;
       if (lane == 0 && mt) bt = atomicAdd(&cnt[3], __popc(mt));
       bt = __shfl_sync(0xffffffffu, bt, 0);
-      if (take) sl[above + bt + __popc(mt & ((1u << lane) - 1u))] = int32_t(0xFFFFFFFFu - uint32_t(__ldcg(&cd[i]) & 0xFFFFFFFFu));
+      if (take) sl[above + bt + __popc(mt & ((1u << lane) - 1u))] = int32_t(0xFFFFFFFFu - uint32_t(c));
+      if (fits && i < nc && b2 == tbin2) fine_s[atomicAdd(&nfine_s, 1u)] = c;
+    }
+    __syncthreads();
+    const int need2 = need - int(above2);
+    uint64_t thr;
+    int nsrc;
+    if (fits) {
+      nsrc = int(nfine_s);
+      thr = select_threshold(nsrc, need2, [&](int i) { return fine_s[i]; }, hist256, sh);
+    } else {
+      // degenerate (e.g. all scores equal): exact select over every candidate of the sub-bin
+      nsrc = nc;
+      thr = select_threshold(nc, need2, [&](int i) {
+        const uint64_t c = __ldcg(&cd[i]);
+        return (uint32_t(c >> 40) & (kHistBins - 1)) == tbin2 ? c : uint64_t(0);
+      }, hist256, sh);
+    }
+    if (threadIdx.x == 0) sh[3] = 0;
+    __syncthreads();
+    const uint32_t base_out = above + above2;
+    for (int b0 = 0; b0 < nsrc; b0 += blockDim.x) {
+      const int i = b0 + threadIdx.x;
+      uint64_t c = 0;
+      if (i < nsrc) c = fits ? fine_s[i] : __ldcg(&cd[i]);
+      const bool take = i < nsrc && (uint32_t(c >> 40) & (kHistBins - 1)) == tbin2 &&
+                        (c >> 32) >> 20 == tbin && c >= thr;
+      const uint32_t mt = __ballot_sync(0xffffffffu, take);
+      uint32_t bt = 0;
+      if (lane == 0 && mt) bt = atomicAdd(&sh[3], __popc(mt));
+      bt = __shfl_sync(0xffffffffu, bt, 0);
+      if (take) sl[base_out + bt + __popc(mt & ((1u << lane) - 1u))] = int32_t(0xFFFFFFFFu - uint32_t(c));
     }
     __threadfence();
     __syncthreads();
@@ -473,13 +541,7 @@ int index_scores(const v4a_index_args* a, void* ws, size_t ws_bytes, cudaStream_
   w = ws_layout(a, ws);
   const v4a_cache& c = a->keys;
   if (cudaMemsetAsync(w.hist, 0, w.zero_bytes, stream) != cudaSuccess) return V4A_ERR_CUDA;
-  bool hist_done = false;
-  if (index_score_tc(a, w.scores, w.row, w.row > kSmemTopkMax ? w.hist : nullptr, stream,
-                     &hist_done, &rc)) {
-    if (rc) return rc;
-    if (hist_done && cudaMemsetAsync(w.flag, 0xFF, 4, stream) != cudaSuccess) return V4A_ERR_CUDA;
-    return cudaGetLastError() == cudaSuccess ? V4A_OK : V4A_ERR_CUDA;
-  }
+  if (index_score_tc(a, w.scores, w.row, stream, &rc)) return rc;
   ScoreArgs sa;
   sa.T = T; sa.H = a->num_heads; sa.dim = c.dim; sa.k_fmt = c.format; sa.q_fmt = a->q_format;
   sa.seq_ids = a->batch.seq_ids; sa.positions = a->batch.positions; sa.keys = c;
@@ -510,14 +572,14 @@ int index_select(const v4a_index_args* a, void* ws, size_t ws_bytes, cudaStream_
   } else {
     const int slices = int((w.row + 4095) / 4096);
     topk_hist<<<dim3(slices, T), 512, 0, stream>>>(w.scores, w.row, a->keys.max_blocks * 64,
-                                                   a->batch.positions, a->k, slices, w.hist, w.flag);
+                                                   a->batch.positions, a->k, slices, w.hist);
     int P2 = 1;
     while (P2 < a->k) P2 <<= 1;
     const size_t smem = size_t(P2) * 4;
     cudaFuncSetAttribute(topk_select, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     topk_select<<<dim3(slices, T), 1024, smem, stream>>>(w.scores, w.row, a->keys.max_blocks * 64,
                                                          a->batch.positions, a->k, slices, w.hist,
-                                                         w.counters, w.cand, w.sel, a->out_idx);
+                                                         w.hist2, w.counters, w.cand, w.sel, a->out_idx);
   }
   return cudaGetLastError() == cudaSuccess ? V4A_OK : V4A_ERR_CUDA;
 }

@@ -8,6 +8,8 @@
 #include <cuda_fp4.h>
 #include <stdint.h>
 
+#include <cmath>
+
 #include "v4a.h"
 
 namespace v4a {
@@ -48,16 +50,33 @@ __device__ __forceinline__ uint32_t f32_to_e2m1(float f) {
 }
 
 // ---- rotary angles ------------------------------------------------------------
-// angle_j = pos * theta^(-2j/R), formed in fp64 (positions reach 1e6) and
-// reduced before the fp32 rotation is applied.
-__device__ __forceinline__ void rope_cos_sin(int pos, int j, int rope_dims, float theta,
-                                             float* c, float* s) {
-  double inv_freq = pow(static_cast<double>(theta), -2.0 * j / static_cast<double>(rope_dims));
-  double ang = static_cast<double>(pos) * inv_freq;
-  double sd, cd;
-  sincos(ang, &sd, &cd);
-  *c = static_cast<float>(cd);
-  *s = static_cast<float>(sd);
+// angle_j = pos * theta^(-2j/R).  inv_freq_j = theta^(-2j/R) is computed on the
+// host in fp64; the angle is formed and reduced to [-pi, pi] in fp64 on the
+// device (positions reach 1e6, where an fp32 angle would be off by ~0.06 rad)
+// and only then rotated with fp32 sincosf.
+struct RopeFreq {
+  double inv[64];   // inv_freq_j for j < rope_dims / 2 (rope_dims <= 128)
+};
+
+inline RopeFreq make_rope_freq(int rope_dims, float theta) {
+  RopeFreq f{};
+  for (int j = 0; j < rope_dims / 2 && j < 64; ++j)
+    f.inv[j] = std::pow(static_cast<double>(theta), -2.0 * j / static_cast<double>(rope_dims));
+  return f;
+}
+
+__device__ __forceinline__ void rope_cos_sin(int pos, double inv_freq, float* c, float* s) {
+  const double ang = static_cast<double>(pos) * inv_freq;
+  const double two_pi = 6.283185307179586476925286766559;
+  const double red = fma(-rint(ang * (1.0 / two_pi)), two_pi, ang);
+  sincosf(static_cast<float>(red), s, c);
+}
+
+// cos/sin of the R/2 angles of position `pos` into cs[0..R/2) and cs[R/2..R),
+// computed by threads 0..R/2-1 of the block (the caller synchronises).
+__device__ __forceinline__ void rope_table(int pos, int rope_dims, const RopeFreq& f, float* cs) {
+  for (int j = threadIdx.x; j < rope_dims / 2; j += blockDim.x)
+    rope_cos_sin(pos, f.inv[j], &cs[j], &cs[rope_dims / 2 + j]);
 }
 
 // ---- paged cache geometry ----------------------------------------------------
