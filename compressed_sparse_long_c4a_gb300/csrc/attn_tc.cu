@@ -30,7 +30,7 @@ namespace {
 
 constexpr int kKeys = 64;            // keys per CTA (one chunk)
 constexpr int kRows = 128;           // MMA M (heads, zero-padded)
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;      // warps 0-3 own TMEM lane quarters for the softmax; all 8 drain
 
 struct AtcArgs {
   int T, H, D, ratio, fmt, wfmt, wlen, wcap, k, splits;
@@ -55,12 +55,13 @@ struct AtcArgs {
 };
 
 struct ASmem {
-  uint64_t bar_s, bar_o;
+  uint64_t bar_q, bar_s, bar_o;
   uint32_t tmem_base;
   int abort_flag;
   const uint8_t* src[kKeys];
   float kscale[kKeys];
   int kfmt[kKeys];                  // -1: no key in this slot
+  float row_l[kRows], row_m[kRows];   // softmax sums / maxima handed to the drain warps
 };
 
 // MN-major operand (B of P*K): 64-element (128-byte) rows along N, consecutive
@@ -83,7 +84,8 @@ __device__ __forceinline__ uint32_t bf16x2_from_e4m3x2(uint16_t two) {
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
+                                                             const __grid_constant__ CUtensorMap qmap) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int D = a.D, nsub = D / 64;
@@ -109,10 +111,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a) {
     return;
   }
   if (tid == 0) {
+    tc::mbar_init(&s.bar_q, 1);
     tc::mbar_init(&s.bar_s, 1);
     tc::mbar_init(&s.bar_o, 1);
     s.abort_flag = 0;
     tc::mbar_fence_init();
+    // Q: 128 rows from this query's first head (rows past the last head are
+    // the next query's or zero-filled; their outputs are never stored), one
+    // 64-column swizzled box per K sub-tile
+    tc::mbar_arrive_expect_tx(&s.bar_q, uint32_t(nsub * kRows * 128));
+    for (int sub = 0; sub < nsub; ++sub)
+      tc::tma_load_2d(Qs + sub * (kRows * 128), &qmap, sub * 64, t * a.H, &s.bar_q);
   }
   __syncwarp();   // tcgen05.alloc is warp-collective: reconverge warp 0 after the init above
   if (warp == 0) tc::tmem_alloc(&s.tmem_base, D < 64 ? 64 : D);
@@ -160,25 +169,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a) {
   }
   __syncthreads();
 
-  // ---- stage Q (rows >= H are zero) and K into swizzled smem ----
-  const uint16_t* qt = a.q + int64_t(t) * a.H * D;
-  const int qchunks = kRows * (D / 8);
-  for (int c = tid; c < qchunks; c += blockDim.x) {
-    const int r = c / (D / 8), cc = c % (D / 8);
-    uint8_t* dst = Qs + (cc >> 3) * (kRows * 128) + r * 128 + (((cc & 7) ^ (r & 7)) << 4);
-    if (r < a.H) {
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)),
-                   "l"(qt + int64_t(r) * D + cc * 8)
-                   : "memory");
-    } else {
-      *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-    }
-  }
+  // ---- stage K into swizzled smem ----
   // keys: bf16 rows go straight to smem with cp.async; fp8 rows are loaded
   // into registers first (all loads in flight together), then converted
   // exactly to bf16 and stored swizzled.
   const int kchunks = kKeys * (D / 8);
-  constexpr int kMaxPer = kKeys * (512 / 8) / kThreads;   // 32 for D = 512
+  constexpr int kMaxPer = kKeys * (512 / 8) / kThreads;   // 16 for D = 512
   uint2 raw[kMaxPer];
 #pragma unroll
   for (int i = 0; i < kMaxPer; ++i) {
@@ -214,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a) {
     *reinterpret_cast<uint4*>(dst) = v;
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
+  tc::mbar_wait(&s.bar_q, 0, a.status, &s.abort_flag);
   tc::fence_proxy_async();
   tc::tc_fence_before();
   __syncthreads();
@@ -231,15 +228,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a) {
     }
     tc::mma_commit(&s.bar_s);
   }
-  // ---- softmax: thread = head row ----
-  const int row = tid;                           // warp w reads TMEM lanes 32w..32w+31
-  const uint32_t lane_addr = tmem + (uint32_t(warp * 32) << 16);
+  // ---- softmax: warps 0-3, thread = head row ----
+  const int row = tid & (kRows - 1);             // warp w reads TMEM lanes 32(w%4)..+31
+  const uint32_t lane_addr = tmem + (uint32_t((warp & 3) * 32) << 16);
   // Collective tcgen05 loads below are always executed by whole warps; `ok`
   // is made warp-uniform and only gates the arithmetic and the stores.
   bool ok = __all_sync(0xffffffffu, tc::mbar_wait(&s.bar_s, 0, a.status, abort_flag));
   tc::tc_fence_after();
   float mx = -INFINITY, l = 0.f;
-  {
+  if (warp < 4) {
     float v[64];
     tc::tmem_ld64(lane_addr, v);
 #pragma unroll
@@ -281,14 +278,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a) {
     }
     tc::mma_commit(&s.bar_o);
   }
+  if (warp < 4) { s.row_l[row] = l; s.row_m[row] = mx; }
   ok = __all_sync(0xffffffffu, ok && tc::mbar_wait(&s.bar_o, 0, a.status, abort_flag));
+  __syncthreads();
   tc::tc_fence_after();
+  l = s.row_l[row];
+  mx = s.row_m[row];
   const bool store = ok && row < a.H;   // H need not be a multiple of 32: loads stay warp-wide
   {
     const float inv = l > 0.f ? 1.f / l : 0.f;   // a chunk of only padding (-1) entries has l = 0
     const bool direct = a.splits == 1;
     uint16_t* dst = direct ? a.out + (int64_t(t) * a.H + row) * D : a.part_o + (pi0 * a.H + row) * D;
-    for (int c = 0; c < nsub; ++c) {
+    // warps 0-3 drain the first half of the 64-column groups, warps 4-7 the rest
+    const int half = nsub / 2;
+    const int c0 = warp < 4 ? 0 : half, c1 = warp < 4 ? half : nsub;
+    for (int c = c0; c < c1; ++c) {
       float v[64];
       tc::tmem_ld64(lane_addr + c * 64, v);
       if (!store) continue;
@@ -306,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a) {
         *reinterpret_cast<uint4*>(dst + c * 64 + i) = o;
       }
     }
-    if (!store) {
+    if (!store || warp >= 4) {
     } else if (direct) {
       if (a.lse) a.lse[int64_t(t) * a.H + row] = mx + logf(l);
     } else {
@@ -440,6 +444,20 @@ bool attn_tc(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t str
   t.idesc_pv = tc::make_idesc(1, 1, kRows, D > 256 ? 256 : D) | (1u << 16);   // B is MN-major
   // At least 116 KB so that no two CTAs of a TMEM-allocating kernel ever share
   // an SM: every tcgen05 kernel in this library runs one CTA per SM.
+  // Q as a 2-D tensor [T*H rows][D] bf16, boxes of 64 columns x 128 rows, 128-B swizzle
+  CUtensorMap qmap;
+  {
+    auto encode = tc::encode_fn();
+    if (!encode) return false;
+    const cuuint64_t gdim[2] = {cuuint64_t(D), cuuint64_t(T) * H};
+    const cuuint64_t gstride[1] = {cuuint64_t(D) * 2};
+    const cuuint32_t box[2] = {64, kRows};
+    const cuuint32_t es[2] = {1, 1};
+    if (encode(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(a->q), gdim, gstride, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
   size_t smem = 1024 + D * kRows * 2 + D * kKeys * 2 + kRows * 128 + sizeof(ASmem);
   if (smem < 116 * 1024) smem = 116 * 1024;
   static std::once_flag once;
@@ -447,7 +465,7 @@ bool attn_tc(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t str
     cudaFuncSetAttribute(attn_chunk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   });
   if (smem > 227 * 1024) return false;
-  attn_chunk_tc<<<dim3(t.splits, t.T), kThreads, smem, stream>>>(t);
+  attn_chunk_tc<<<dim3(t.splits, t.T), kThreads, smem, stream>>>(t, qmap);
   if (t.splits > 1)
     attn_combine_bf16<<<dim3(t.H, t.T), t.D / 8 < 32 ? 32 : t.D / 8, 0, stream>>>(t.H, t.D, t.splits, t.part_o,
                                                                                 t.part_ml, t.out, t.lse);

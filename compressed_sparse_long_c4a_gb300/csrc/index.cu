@@ -288,8 +288,24 @@ __global__ void __launch_bounds__(512) topk_hist(const float* scores, int64_t ro
   const int per = (n + slices - 1) / slices;
   const int lo = blockIdx.x * per, hi = min(n, lo + per);
   const float* s = scores + int64_t(t) * row;
-  for (int i = lo + threadIdx.x; i < hi; i += blockDim.x)
-    atomicAdd(&h_s[float_key(s[i]) >> 20], 1u);
+  const int lane = threadIdx.x & 31;
+  constexpr int kU = 4;   // loads in flight per thread
+  for (int base = lo; base < hi; base += kU * blockDim.x) {
+    float v[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = base + u * blockDim.x + threadIdx.x;
+      v[u] = i < hi ? s[i] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = base + u * blockDim.x + threadIdx.x;
+      const uint32_t bin = i < hi ? (float_key(v[u]) >> 20) : 0xFFFFFFFFu;
+      // one shared atomic per distinct bin of the warp (scores cluster in few bins)
+      const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+      if (bin != 0xFFFFFFFFu && lane == __ffs(peers) - 1) atomicAdd(&h_s[bin], __popc(peers));
+    }
+  }
   __syncthreads();
   uint32_t* g = hist + int64_t(t) * kHistBins;
   for (int i = threadIdx.x; i < kHistBins; i += blockDim.x)
@@ -367,11 +383,20 @@ __global__ void __launch_bounds__(1024) topk_select(const float* scores, int64_t
   const int lo = blockIdx.x * per, hi = min(n, lo + per);
   const float* sc = scores + int64_t(t) * row;
   const int lane = threadIdx.x & 31;
-  for (int base = lo; base < hi; base += blockDim.x) {
-    const int i = base + threadIdx.x;
+  constexpr int kU = 4;   // loads in flight per thread
+  for (int base0 = lo; base0 < hi; base0 += kU * blockDim.x) {
+    float vals[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = base0 + u * blockDim.x + threadIdx.x;
+      vals[u] = i < hi ? sc[i] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+    const int i = base0 + u * blockDim.x + threadIdx.x;
     uint32_t key = 0, bin = 0;
     const bool in = i < hi;
-    if (in) { key = float_key(sc[i]); bin = key >> 20; }
+    if (in) { key = float_key(vals[u]); bin = key >> 20; }
     const bool take = in && bin > tbin;
     const bool maybe = in && bin == tbin;
     const uint32_t mt = __ballot_sync(0xffffffffu, take);
@@ -388,6 +413,7 @@ __global__ void __launch_bounds__(1024) topk_select(const float* scores, int64_t
     if (maybe) {
       cd[bm + __popc(mm & below)] = composite(key, i);
       atomicAdd(&h2_s[(key >> 8) & (kHistBins - 1)], 1u);
+    }
     }
   }
   __syncthreads();
@@ -412,11 +438,19 @@ __global__ void __launch_bounds__(1024) topk_select(const float* scores, int64_t
     const uint32_t tbin2 = uint32_t(threshold_bin(h2_s, uint32_t(need), scan, &bin_s, &above_s, &above2));
     const bool fits = h2_s[tbin2] <= uint32_t(kFine);
     // candidates above the sub-bin are taken; the sub-bin's go to the fine list
-    for (int base = 0; base < nc; base += blockDim.x) {
-      const int i = base + threadIdx.x;
+    for (int base0 = 0; base0 < nc; base0 += kU * blockDim.x) {
+      uint64_t cs[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = base0 + u * blockDim.x + threadIdx.x;
+        cs[u] = i < nc ? __ldcg(reinterpret_cast<const unsigned long long*>(&cd[i])) : 0ull;
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+      const int i = base0 + u * blockDim.x + threadIdx.x;
       uint64_t c = 0;
       uint32_t b2 = 0;
-      if (i < nc) { c = __ldcg(&cd[i]); b2 = uint32_t(c >> 40) & (kHistBins - 1); }
+      if (i < nc) { c = cs[u]; b2 = uint32_t(c >> 40) & (kHistBins - 1); }
       const bool take = i < nc && b2 > tbin2;
       const uint32_t mt = __ballot_sync(0xffffffffu, take);
       uint32_t bt = 0;
@@ -424,6 +458,7 @@ __global__ void __launch_bounds__(1024) topk_select(const float* scores, int64_t
       bt = __shfl_sync(0xffffffffu, bt, 0);
       if (take) sl[above + bt + __popc(mt & ((1u << lane) - 1u))] = int32_t(0xFFFFFFFFu - uint32_t(c));
       if (fits && i < nc && b2 == tbin2) fine_s[atomicAdd(&nfine_s, 1u)] = c;
+      }
     }
     __syncthreads();
     const int need2 = need - int(above2);

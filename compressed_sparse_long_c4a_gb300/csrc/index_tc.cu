@@ -10,10 +10,13 @@
 // scale per head), k_i = kcode_i * s_i,b per 32- or 128-element block b.
 //
 // Tile = 128 entries (two 64-entry physical blocks) x 64 heads x 128 dims:
-//  A = key codes, M = 128 rows (TMEM lane = entry), K-major, 128-byte swizzle,
-//      loaded by TMA straight from the paged pool (3-D tensor map: row bytes,
-//      64 rows, block id; fp4 rows land in the padded 16-elements-per-16-bytes
-//      layout the f8f6f4 MMA reads);
+//  each physical block (codes + scale words, 5120 B for fp4, 8448 B for fp8)
+//  arrives with ONE 1-D bulk copy into a raw stage; the MMA warp converts the
+//  codes into the K-major, 128-byte-swizzled A operand (fp4: 16 elements in
+//  the first 8 bytes of each 16-byte container, the layout kind::f8f6f4 reads
+//  for e2m1; fp8: plain swizzled rows).  Large copies matter: the copy engine
+//  spends a roughly fixed time per copy, so many small (row-sized) requests
+//  cannot keep up with HBM.
 //  B = the query's e4m3 codes, N = 64 heads, staged once per query;
 //  K = 128 in four MMAs of K = 32.  fp8 keys: the four MMAs accumulate into
 //      one 64-column fp32 accumulator (one scale per entry, factored out of
@@ -25,21 +28,20 @@
 //
 // Warp roles (320 threads, one CTA per SM, persistent over a contiguous range
 // of (query, tile) work items):
-//   warp 0      TMA producer: kStages-deep ring of key tiles, each with the
-//               two blocks' fp32 scale words (1-D bulk copies); also copies
-//               the query codes and w_h * qs_h into double-buffered smem.
-//   warp 1      TMEM allocator and single-thread MMA issuer; accumulators are
-//               double-buffered in TMEM.
-//   warps 2..9  two epilogue warpgroups, one per accumulator (alternate
+//   warp 0      producer: kStages-deep ring of raw tiles (two bulk copies per
+//               tile, block ids from a shared-memory window of the block
+//               table); also copies the query codes and w_h * qs_h into
+//               double-buffered smem.
+//   warp 1      TMEM allocator and single-thread MMA issuer (double-buffered
+//               TMEM accumulators).
+//   warp 2      converter: raw tile -> swizzled MMA operand (kOps buffers).
+//   warps 3..10 two epilogue warpgroups, one per accumulator (alternate
 //               tiles): one thread per entry (TMEM lane) reads its
-//               accumulators, applies scales, ReLU and head weights with
-//               packed fp32x2 FMAs and writes the score.
-// A stage is refilled only after the MMA (commit) and the owning epilogue
-// warpgroup (scale words read) have released it.
+//               accumulators and its scale words, applies scales, ReLU and
+//               head weights with packed fp32x2 FMAs and writes the score.
+// A raw stage is refilled only after the converter (codes copied) and the
+// owning epilogue warpgroup (scale words read) have released it.
 // Every mbarrier wait is bounded (V4A_DEV_TIMEOUT, then a clean exit).
-
-#include <cuda.h>
-#include <cudaTypedefs.h>
 
 #include <mutex>
 
@@ -51,11 +53,11 @@ namespace {
 
 constexpr int kStages = 8;
 constexpr int kTileBytes = 128 * 128;    // 128 rows x 128 smem bytes (one MMA operand)
-constexpr int kBlockSmem = 64 * 128;     // one 64-entry block in smem
-constexpr int kScaleBytes = 2048;        // scale words of the two blocks of a tile (fp4: 2 x 1 KB)
 constexpr int kQBytes = 64 * 128;        // 64 heads x 128 codes
+constexpr int kOps = 4;                  // converted MMA operand buffers
 constexpr int kEpiWarps = 8;             // two epilogue warpgroups
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kEpi0 = 3;                 // first epilogue warp
+constexpr int kThreads = 32 * kEpi0 + 32 * kEpiWarps;
 
 struct TcArgs {
   int T, fmt, acc_cols;
@@ -68,6 +70,7 @@ struct TcArgs {
   int64_t block_bytes;
   int64_t scale_off;          // byte offset of the scale words inside a block
   uint32_t scale_bytes;       // scale bytes of one block (64 entries)
+  uint32_t raw_stage;         // bytes of one raw stage = 2 * block_bytes
   const uint8_t* q;           // [T][64][128] e4m3
   const float* qs;            // [T][64]
   const float* w;             // [T][64]
@@ -75,15 +78,16 @@ struct TcArgs {
   int64_t row;
   int32_t* status;
   uint32_t idesc;
-  uint32_t tx_per_block;
 };
 
 struct Smem {
-  uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], qfull[2], qempty[2], done;
+  uint64_t full[kStages], empty[kStages], opfull[kOps], opempty[kOps], tfull[2], tempty[2], qfull[2],
+      qempty[2], done;
   uint32_t tmem_base;
   int abort_flag;
   int t0, j0, count;
   uint32_t valid[kStages];  // bit h: block h of the stage's tile was loaded
+  int32_t btc[1024];        // producer's window of the current query's block-table row
   uint32_t part[kThreads];
   float wq[2][64];          // w_h * qs_h of the query in each query buffer
 };
@@ -144,20 +148,24 @@ __device__ void plan(const TcArgs& a, Smem& s) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap tmap) {
+index_scan_tc(const TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* tiles = base;                                   // kStages x 16 KB
-  uint8_t* qbuf = tiles + kStages * kTileBytes;            // 2 x 8 KB
-  uint8_t* scl = qbuf + 2 * kQBytes;                       // kStages x 2 KB
-  Smem& s = *reinterpret_cast<Smem*>(scl + kStages * kScaleBytes);
+  uint8_t* ops = base;                                     // kOps x 16 KB converted MMA operands
+  uint8_t* qbuf = ops + kOps * kTileBytes;                 // 2 x 8 KB
+  uint8_t* raw = qbuf + 2 * kQBytes;                       // kStages x (2 blocks as stored in the pool)
+  Smem& s = *reinterpret_cast<Smem*>(raw + kStages * a.raw_stage);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort_flag = &s.abort_flag;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       tc::mbar_init(&s.full[i], 1);
-      tc::mbar_init(&s.empty[i], 1 + 4);            // MMA commit + the owning warpgroup
+      tc::mbar_init(&s.empty[i], 1 + 4);            // converter + the owning epilogue warpgroup
+    }
+    for (int i = 0; i < kOps; ++i) {
+      tc::mbar_init(&s.opfull[i], 1);               // converter
+      tc::mbar_init(&s.opempty[i], 1);              // MMA commit
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&s.tfull[i], 1);
@@ -169,7 +177,6 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap tmap) {
     s.abort_flag = 0;
     tc::mbar_fence_init();
   }
-  if (warp == 0 && lane == 0) tc::prefetch_tmap(&tmap);
   __syncwarp();   // tcgen05.alloc is warp-collective
   if (warp == 1) tc::tmem_alloc(&s.tmem_base, 2 * a.acc_cols);
   tc::tc_fence_before();
@@ -186,7 +193,7 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap tmap) {
     uint32_t phase = 0;
     uint32_t last_phase[kStages];
     int issued = 0;
-    int b = 0, nblk = 0;
+    int b = 0, nblk = 0, btc_base = 0, btc_end = 0;
     for (int it = 0; it < count; ++it) {
       if (c.t != cur_t) {
         cur_t = c.t;
@@ -194,6 +201,7 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap tmap) {
         const int qb = qi & 1;
         b = a.seq_ids[cur_t];
         nblk = (visible_of(a, cur_t) + 63) / 64;
+        btc_base = btc_end = 0;                       // refill the block-table window below
         if (lane == 0 && (a.positions[cur_t] + 1) / 4 > a.max_blocks * 64) report(a.status, V4A_DEV_BAD_BLOCK);
         if (lane == 0 && qi >= 2) tc::mbar_wait(&s.qempty[qb], ((qi >> 1) - 1) & 1, a.status, abort_flag);
         __syncwarp();
@@ -210,6 +218,16 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap tmap) {
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&s.qfull[qb]);
       }
+      // block-table entries of this tile come from a shared-memory window of the
+      // row, refilled with coalesced loads by the whole warp
+      if (2 * c.j + 1 >= btc_end && 2 * c.j < nblk) {
+        btc_base = 2 * c.j;
+        btc_end = min(nblk, btc_base + 1024);
+        __syncwarp();
+        for (int i = lane; i < btc_end - btc_base; i += 32)
+          s.btc[i] = a.bt[int64_t(b) * a.max_blocks + btc_base + i];
+        __syncwarp();
+      }
       if (lane == 0) {
         if (!tc::mbar_wait(&s.empty[stage], phase ^ 1, a.status, abort_flag)) *abort_flag = 1;
       }
@@ -222,19 +240,18 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap tmap) {
           const int lb = 2 * c.j + h;
           p[h] = -1;
           if (lb >= nblk) continue;
-          p[h] = a.bt[int64_t(b) * a.max_blocks + lb];
+          p[h] = s.btc[lb - btc_base];
           if (p[h] < 0 || p[h] >= a.num_blocks) { p[h] = -1; report(a.status, V4A_DEV_BAD_BLOCK); continue; }
-          bytes += a.tx_per_block + a.scale_bytes;
+          bytes += uint32_t(a.block_bytes);
           valid |= 1u << h;
         }
         s.valid[stage] = valid;
         tc::mbar_arrive_expect_tx(&s.full[stage], bytes);
-        for (int h = 0; h < 2; ++h) {
-          if (p[h] < 0) continue;
-          tc::tma_load_3d(tiles + stage * kTileBytes + h * kBlockSmem, &tmap, 0, 0, int(p[h]), &s.full[stage]);
-          tc::bulk_load(scl + stage * kScaleBytes + h * (kScaleBytes / 2),
-                        a.pool + p[h] * a.block_bytes + a.scale_off, a.scale_bytes, &s.full[stage]);
-        }
+        // one bulk copy per physical block: codes and scale words together
+        for (int h = 0; h < 2; ++h)
+          if (p[h] >= 0)
+            tc::bulk_load(raw + stage * a.raw_stage + h * a.block_bytes, a.pool + p[h] * a.block_bytes,
+                          uint32_t(a.block_bytes), &s.full[stage]);
         last_phase[stage] = phase;
       }
       ++issued;
@@ -255,20 +272,21 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap tmap) {
     if (lane == 0) {
       Cursor c;
       c.init(a, s.t0, s.j0);
-      int cur_t = -1, qi = -1, stage = 0, acc = 0;
-      uint32_t phase = 0, aphase = 0;
-      const uint32_t q0 = tc::smem_u32(qbuf), t0a = tc::smem_u32(tiles);
+      int cur_t = -1, qi = -1, acc = 0;
+      uint32_t aphase = 0;
+      const uint32_t q0 = tc::smem_u32(qbuf), op0 = tc::smem_u32(ops);
       for (int it = 0; it < count; ++it) {
+        const int j = it % kOps;
         if (c.t != cur_t) {
           if (qi >= 0) tc::mma_commit(&s.qempty[qi & 1]);
           cur_t = c.t;
           ++qi;
           if (!tc::mbar_wait(&s.qfull[qi & 1], (qi >> 1) & 1, a.status, abort_flag)) break;
         }
-        if (!tc::mbar_wait(&s.full[stage], phase, a.status, abort_flag)) break;
+        if (!tc::mbar_wait(&s.opfull[j], (it / kOps) & 1, a.status, abort_flag)) break;
         if (!tc::mbar_wait(&s.tempty[acc], aphase ^ 1, a.status, abort_flag)) break;
         tc::tc_fence_after();
-        const uint64_t adesc = tc::desc_sw128(t0a + stage * kTileBytes);
+        const uint64_t adesc = tc::desc_sw128(op0 + j * kTileBytes);
         const uint64_t bdesc = tc::desc_sw128(q0 + (qi & 1) * kQBytes);
         const uint32_t d = tmem + acc * a.acc_cols;
 #pragma unroll
@@ -279,9 +297,8 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap tmap) {
           else
             tc::mma_f8f6f4(d + 64 * kb, adesc + 2 * kb, bdesc + 2 * kb, a.idesc, 0);
         }
-        tc::mma_commit(&s.empty[stage]);
+        tc::mma_commit(&s.opempty[j]);
         tc::mma_commit(&s.tfull[acc]);
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
         if (++acc == 2) { acc = 0; aphase ^= 1; }
         c.next(a);
       }
@@ -291,11 +308,65 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap tmap) {
       while (!tc::mbar_try_wait(&s.done, 0) && clock64() - t0 < 2000000000LL) {}
     }
     __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ converter
+    // Turns each landed raw tile into the K-major, 128-byte-swizzled A operand
+    // (fp4: 16 codes in the first 8 bytes of each 16-byte container; fp8: the
+    // row's 16-byte chunks swizzled).  Every load of a pass is issued before
+    // any store so the shared-memory latency overlaps.
+    const bool fp8 = a.fmt == V4A_IX_FP8_B128;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int it = 0; it < count; ++it) {
+      const int j = it % kOps;
+      bool ok = tc::mbar_wait(&s.full[stage], phase, a.status, abort_flag);
+      ok = ok && tc::mbar_wait(&s.opempty[j], ((it / kOps) & 1) ^ 1, a.status, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc::tc_fence_after();
+      const uint8_t* src = raw + stage * a.raw_stage;
+      uint8_t* dst = ops + j * kTileBytes;
+      if (fp8) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint4 v[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {         // row = 64*half + 4k + lane/8, chunk = lane%8
+            const int r = half * 64 + k * 4 + (lane >> 3);
+            v[k] = *reinterpret_cast<const uint4*>(src + (r >> 6) * a.block_bytes + (r & 63) * 128 + (lane & 7) * 16);
+          }
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int r = half * 64 + k * 4 + (lane >> 3), ch = lane & 7;
+            *reinterpret_cast<uint4*>(dst + r * 128 + ((ch ^ (r & 7)) << 4)) = v[k];
+          }
+        }
+      } else {
+        uint4 v[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {           // row = 8k + lane/4, 16 bytes = containers 2p, 2p+1
+          const int r = k * 8 + (lane >> 2);
+          v[k] = *reinterpret_cast<const uint4*>(src + (r >> 6) * a.block_bytes + (r & 63) * 64 + (lane & 3) * 16);
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int r = k * 8 + (lane >> 2), p2 = (lane & 3) * 2;
+          *reinterpret_cast<uint2*>(dst + r * 128 + ((p2 ^ (r & 7)) << 4)) = make_uint2(v[k].x, v[k].y);
+          *reinterpret_cast<uint2*>(dst + r * 128 + (((p2 + 1) ^ (r & 7)) << 4)) = make_uint2(v[k].z, v[k].w);
+        }
+      }
+      tc::fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive(&s.opfull[j]);
+        tc::mbar_arrive(&s.empty[stage]);                  // codes copied out of the raw stage
+      }
+      if (++stage == kStages) { stage = 0; phase ^= 1; }
+    }
   } else {
     // ------------------------------------------------------------ epilogue
-    // Warpgroup g (warps 2+4g .. 5+4g) owns accumulator g, i.e. every other
+    // Warpgroup g (warps 3+4g .. 6+4g) owns accumulator g, i.e. every other
     // tile; both warpgroups walk every item to follow the query switches.
-    const int g = (warp - 2) >> 2;
+    const int g = (warp - kEpi0) >> 2;
     const int quarter = warp & 3;                // TMEM lanes 32*quarter .. +31
     const int row = quarter * 32 + lane;         // entry within the tile
     const uint32_t lane_addr = tmem + (uint32_t(quarter * 32) << 16) + g * a.acc_cols;
@@ -326,7 +397,7 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap tmap) {
         ok = __all_sync(0xffffffffu, ok && tc::mbar_wait(&s.tfull[g], aphase, a.status, abort_flag));
         if (!ok) break;
         const bool blk_ok = (s.valid[stage] >> (row >> 6)) & 1u;
-        const uint8_t* sp = scl + stage * kScaleBytes + (row >> 6) * (kScaleBytes / 2);
+        const uint8_t* sp = raw + stage * a.raw_stage + (row >> 6) * a.block_bytes + a.scale_off;
         float sc0, sc1 = 0.f, sc2 = 0.f, sc3 = 0.f;
         if (a.fmt == V4A_IX_FP8_B128) {
           sc0 = reinterpret_cast<const float*>(sp)[row & 63];
@@ -389,32 +460,6 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap tmap) {
 
 // ---- host side -------------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-int sm_count() {
-  static int n = 0;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  });
-  return n;
-}
-
 }  // namespace
 
 bool index_score_tc(const v4a_index_args* a, float* scores, int64_t row, cudaStream_t stream, int* rc) {
@@ -422,9 +467,7 @@ bool index_score_tc(const v4a_index_args* a, float* scores, int64_t row, cudaStr
   const v4a_cache& c = a->keys;
   if (c.format != V4A_IX_FP8_B128 && c.format != V4A_IX_FP4_B32) return false;
   if (a->q_format != V4A_Q_FP8_HEAD || a->num_heads != 64 || c.dim != 128) return false;
-  if ((reinterpret_cast<uintptr_t>(c.pool) & 31) || (reinterpret_cast<uintptr_t>(a->q) & 15)) return false;
-  auto encode = encode_fn();
-  if (!encode) return false;
+  if ((reinterpret_cast<uintptr_t>(c.pool) & 15) || (reinterpret_cast<uintptr_t>(a->q) & 15)) return false;
   const bool fp4 = c.format == V4A_IX_FP4_B32;
   TcArgs t{};
   t.T = a->batch.num_tokens;
@@ -446,26 +489,14 @@ bool index_score_tc(const v4a_index_args* a, float* scores, int64_t row, cudaStr
   t.row = row;
   t.status = a->status;
   t.idesc = tc::make_idesc(fp4 ? 5u : 0u, 0u, 128, 64);
-  // transaction bytes of one block's TMA copy: the global bytes read (for the
-  // padded 4-bit type that is half of what lands in shared memory)
-  t.tx_per_block = uint32_t(64 * ix_row_bytes(c.format, c.dim));
-
-  CUtensorMap map;
-  const cuuint64_t gdim[3] = {128, 64, cuuint64_t(c.num_blocks)};
-  const cuuint64_t gstride[2] = {cuuint64_t(ix_row_bytes(c.format, c.dim)), cuuint64_t(t.block_bytes)};
-  const cuuint32_t box[3] = {128, 64, 1};
-  const cuuint32_t estride[3] = {1, 1, 1};
-  CUresult r = encode(&map, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
-                      const_cast<void*>(c.pool), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return false;
-  const size_t smem = 1024 + size_t(kStages) * (kTileBytes + kScaleBytes) + 2 * kQBytes + sizeof(Smem);
+  t.raw_stage = uint32_t(2 * t.block_bytes);
+  const size_t smem = 1024 + size_t(kOps) * kTileBytes + 2 * kQBytes + size_t(kStages) * t.raw_stage + sizeof(Smem);
+  if (smem > 227 * 1024) return false;
   static std::once_flag attr_once;
-  std::call_once(attr_once, [smem] {
-    cudaFuncSetAttribute(index_scan_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  std::call_once(attr_once, [] {
+    cudaFuncSetAttribute(index_scan_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   });
-  index_scan_tc<<<sm_count(), kThreads, smem, stream>>>(t, map);
+  index_scan_tc<<<tc::sm_count(), kThreads, smem, stream>>>(t);
   if (cudaGetLastError() != cudaSuccess) { *rc = V4A_ERR_CUDA; return true; }
   return true;
 }
