@@ -88,6 +88,7 @@ def lib() -> C.CDLL:
         L.v4a_index_topk.argtypes = [C.POINTER(IndexArgs), _p, C.c_size_t, _p]
         L.v4a_index_scores.argtypes = [C.POINTER(IndexArgs), _p, C.c_size_t, _p]
         L.v4a_index_select.argtypes = [C.POINTER(IndexArgs), _p, C.c_size_t, _p]
+        L.v4a_index_topk_static.argtypes = [C.POINTER(IndexArgs), _p]
         L.v4a_index_scores_layout.argtypes = [C.POINTER(IndexArgs), C.POINTER(C.c_size_t),
                                               C.POINTER(C.c_int64)]
         L.v4a_attn_workspace_size.argtypes = [C.POINTER(AttnArgs)]
@@ -216,6 +217,17 @@ def index_topk(layer: DeviceLayer, out_idx: torch.Tensor, workspace: torch.Tenso
     a = layer.index_args(out_idx)
     _check("v4a_index_topk", lib().v4a_index_topk(C.byref(a), _ptr(workspace), workspace.numel(),
                                                   _stream(stream)))
+
+
+# Scratch limit of v4a_index_topk_static (V4A_INDEX_STATIC_SCRATCH_BYTES in v4a.h).
+INDEX_STATIC_SCRATCH_BYTES = 16 << 20
+
+
+def index_topk_static(layer: DeviceLayer, out_idx: torch.Tensor, stream=None):
+    """v4a_index_topk with the library's fixed device scratch: no workspace is
+    passed, nothing is allocated (for callers that may not allocate)."""
+    a = layer.index_args(out_idx)
+    _check("v4a_index_topk_static", lib().v4a_index_topk_static(C.byref(a), _stream(stream)))
 
 
 def index_scores(layer: DeviceLayer, out_idx: torch.Tensor, workspace: torch.Tensor, stream=None):

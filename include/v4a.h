@@ -207,6 +207,31 @@ V4A_API int v4a_index_scores_layout(const v4a_index_args* args, size_t* offset, 
 V4A_API int v4a_index_select(const v4a_index_args* args, void* workspace, size_t workspace_bytes,
                      void* stream);
 
+/* v4a_index_topk without a workspace argument.  The method itself has no
+ * counterpart: this variant exists for callers that may not allocate device
+ * memory on the step path (a serving loop that gave all free HBM to the paged
+ * KV pool at start-up; a binding with no device allocator of its own).
+ *
+ * Scratch is one fixed array of V4A_INDEX_STATIC_SCRATCH_BYTES inside this
+ * library's device image (device memory it holds once its device code is
+ * loaded on a device); the call allocates and frees nothing.  Returns
+ * V4A_ERR_WORKSPACE, launching nothing, when the arguments need more than that
+ * (v4a_index_workspace_size(args) > V4A_INDEX_STATIC_SCRATCH_BYTES; 16 MiB
+ * holds, at k = 2048, 4 queries over 262,144 visible entries each or 16 over
+ * 65,536);
+ * otherwise it returns exactly what v4a_index_topk would with a workspace of
+ * that size, and writes the same out_idx.
+ *
+ * The first call on each device looks up the array's address there with that
+ * device current (cudaGetSymbolAddress; V4A_ERR_CUDA if that fails), which may
+ * load this library's device code: make it before any stream capture starts.
+ * All calls on a device share the array, so calls that may be in flight at the
+ * same time (other streams or host threads, unordered) race and must be
+ * ordered by the caller.  The part of the scratch that must start at zero
+ * (histograms and counters) is cleared by every call on its own stream. */
+#define V4A_INDEX_STATIC_SCRATCH_BYTES (16u << 20)
+V4A_API int v4a_index_topk_static(const v4a_index_args* args, void* stream);
+
 /*
  * Sparse attention with shared K=V (vLLM page, Background and appendix "why
  * inverse RoPE").  For query t at position m and head h, over the keys
