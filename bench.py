@@ -199,6 +199,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="c4a_decode_b4_1m")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--replicas", type=int, default=0,
+                    help="layer replicas to rotate over (default: enough to defeat L2); a smaller "
+                         "count only serves profiler captures, never a reported number")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
@@ -230,6 +233,8 @@ def main():
     scan_b, gather_b, win_b = algorithmic_bytes(spec)
     step_bytes = scan_b + gather_b + win_b
     replicas = max(2, math.ceil(2 * L2_BYTES / max(step_bytes, 1)) + 1)
+    if args.replicas > 0:
+        replicas = args.replicas
     layers = [v4a.DeviceLayer.from_case(case, dev) for _ in range(replicas)]
     steps = [v4a.Step(L) for L in layers]
     stream = torch.cuda.Stream(device=dev)

@@ -14,12 +14,14 @@
 //  * topk_smem         - one CTA per query when the row fits in shared memory:
 //                         radix select of the k-th largest (score, -index)
 //                         composite, then an ordered compaction.
-//  * topk_hist / topk_select - long rows: a 4096-bin histogram of the score
-//                         keys,
-//                         then every CTA compacts its slice (bins above the
-//                         threshold bin are taken, the threshold bin goes to a
-//                         candidate list) and the last CTA of a query resolves
-//                         the candidates exactly and sorts the selection.
+//  * topk_hist / topk_select - long rows, one CTA per 4096-score slice: a
+//                         4096-bin histogram of the score keys' top 12 bits
+//                         gives the threshold bin; every slice then compacts,
+//                         in index order, its entries above that bin ("takes")
+//                         and those in it ("candidates", plus a histogram of
+//                         their next 12 bits).  The last slice CTA of a query
+//                         resolves the exact threshold among the candidates
+//                         and merges the two ordered lists into the output.
 //                         The "last CTA" is found with an atomic counter; no
 //                         CTA ever waits on another.
 
@@ -34,14 +36,16 @@ namespace v4a {
 constexpr int kSmemTopkMax = 32768;   // rows up to this length use topk_smem
 constexpr int kHistBins = 4096;       // top 12 bits of the order-preserving key
 constexpr int kMaxK = 16384;
+constexpr int kSlice = 4096;          // scores per CTA of the long-row top-k
+constexpr int kMaxSlices = 1024;      // rows up to 4M entries
 
 struct IndexWs {
   float* scores;        // [T][row]
   uint32_t* hist;       // [T][kHistBins]   top 12 key bits of every score
   uint32_t* hist2;      // [T][kHistBins]   next 12 bits of the threshold bin's scores
   uint32_t* counters;   // [T][4]: selected, candidates, done, resolved
-  uint64_t* cand;       // [T][row]
-  int32_t* sel;         // [T][k]
+  uint64_t* cand;       // [T][row]: slice s keeps its takes at [lo, ..) and its candidates at [.., hi)
+  uint32_t* info;       // [T][slices]: takes | candidates << 16 of each slice
   int64_t row;
   size_t zero_bytes;    // bytes of hist + counters (cleared per call)
   size_t total;
@@ -63,7 +67,7 @@ static IndexWs ws_layout(const v4a_index_args* a, void* base) {
   w.scores = reinterpret_cast<float*>(take(size_t(T) * w.row * 4));
   if (w.row > kSmemTopkMax) {
     w.cand = reinterpret_cast<uint64_t*>(take(size_t(T) * w.row * 8));
-    w.sel = reinterpret_cast<int32_t*>(take(size_t(T) * a->k * 4));
+    w.info = reinterpret_cast<uint32_t*>(take(size_t(T) * ((w.row + kSlice - 1) / kSlice) * 4));
   }
   w.total = off;
   return w;
@@ -162,10 +166,17 @@ __device__ __forceinline__ uint64_t composite(uint32_t key, int idx) {
 
 // Returns thr such that exactly `need` (>= 1) of the n composites are >= thr.
 // All threads of the CTA call it; hist = 256 words of shared memory.
+// Passes before `first_pass` are skipped: the caller guarantees that all n
+// composites agree on their top 8 * first_pass bits.
 template <class Get>
-__device__ uint64_t select_threshold(int n, int need, Get get, uint32_t* hist, uint32_t* sh) {
+__device__ uint64_t select_threshold(int n, int need, Get get, uint32_t* hist, uint32_t* sh,
+                                     int first_pass = 0) {
   uint64_t prefix = 0, mask = 0;
-  for (int pass = 0; pass < 8; ++pass) {
+  if (first_pass > 0) {
+    mask = ~uint64_t(0) << (64 - 8 * first_pass);
+    prefix = get(0) & mask;
+  }
+  for (int pass = first_pass; pass < 8; ++pass) {
     const int shift = 56 - 8 * pass;
     for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
     __syncthreads();
@@ -344,173 +355,175 @@ __device__ int threshold_bin(const uint32_t* h, uint32_t need, uint32_t* scan, i
   return b;
 }
 
-constexpr int kFine = 2048;   // capacity of the last CTA's exact-resolve list
+constexpr int kFine = 2048;   // capacity of the resolving CTA's exact-select list
 
-__global__ void __launch_bounds__(1024) topk_select(const float* scores, int64_t row, int max_entries,
+// Position of j among the slices' ranges: the largest s with pre[s] <= j.
+__device__ __forceinline__ int slice_of(const uint32_t* pre, int nsl, uint32_t j) {
+  int lo = 0, hi = nsl - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pre[mid] <= j) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Number of elements of the ascending list l[0..n) below x.
+__device__ __forceinline__ int count_below(const int32_t* l, int n, int32_t x) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (l[mid] < x) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(1024, 2) topk_select(const float* scores, int64_t row, int max_entries,
                                                    const int32_t* positions, int k, int slices,
                                                    const uint32_t* hist, uint32_t* hist2,
-                                                   uint32_t* counters, uint64_t* cand, int32_t* sel,
+                                                   uint32_t* counters, uint64_t* cand, uint32_t* info,
                                                    int32_t* out) {
-  extern __shared__ int32_t sort_s[];   // [pow2 >= k] (last CTA only)
+  extern __shared__ int32_t lists_s[];   // resolving CTA: [k] takes, then [k] selected candidates
   __shared__ uint32_t scan[40];
   __shared__ uint32_t h2_s[kHistBins];
   __shared__ uint64_t fine_s[kFine];
+  __shared__ uint32_t pre_s[2][kMaxSlices + 1];
   __shared__ uint32_t hist256[256];
   __shared__ uint32_t sh[4];
   __shared__ int bin_s;
   __shared__ uint32_t above_s;
   __shared__ int last_s;
   __shared__ uint32_t nfine_s;
-  const int t = blockIdx.y;
+  const int t = blockIdx.y, sl = blockIdx.x;
   const int n = min((positions[t] + 1) / 4, max_entries);
   int32_t* o = out + int64_t(t) * k;
   if (n <= k) {
-    if (blockIdx.x == 0) write_all_visible(o, n, k);
+    if (sl == 0) write_all_visible(o, n, k);
     return;
   }
+  const int nsl = (n + kSlice - 1) / kSlice;
+  if (sl >= nsl) return;
   // 1. threshold bin of the top 12 key bits
   uint32_t above1;
   const uint32_t tbin = uint32_t(threshold_bin(hist + int64_t(t) * kHistBins, uint32_t(k), scan, &bin_s,
                                                &above_s, &above1));
   for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h2_s[i] = 0;
-  __syncthreads();
-  // 2. compact this CTA's slice: above the bin -> selected, in the bin -> candidates
-  //    (and their next 12 key bits into the second-level histogram)
-  uint32_t* cnt = counters + int64_t(t) * 4;
-  uint64_t* cd = cand + int64_t(t) * row;
-  int32_t* sl = sel + int64_t(t) * k;
-  const int per = (n + slices - 1) / slices;
-  const int lo = blockIdx.x * per, hi = min(n, lo + per);
+  // 2. ordered compaction of this slice: thread c owns entries lo + 4c .. lo + 4c + 3
+  const int lo = sl * kSlice, hi = min(n, lo + kSlice);
   const float* sc = scores + int64_t(t) * row;
-  const int lane = threadIdx.x & 31;
-  constexpr int kU = 4;   // loads in flight per thread
-  for (int base0 = lo; base0 < hi; base0 += kU * blockDim.x) {
-    float vals[kU];
+  const int i0 = lo + 4 * int(threadIdx.x);
+  float v[4];
+  if (i0 + 3 < hi) {
+    const float4 f = *reinterpret_cast<const float4*>(sc + i0);
+    v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+  } else {
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int i = base0 + u * blockDim.x + threadIdx.x;
-      vals[u] = i < hi ? sc[i] : 0.f;
-    }
+    for (int u = 0; u < 4; ++u) v[u] = i0 + u < hi ? sc[i0 + u] : 0.f;
+  }
+  uint32_t key[4], ntk = 0, ncd = 0;
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
-    const int i = base0 + u * blockDim.x + threadIdx.x;
-    uint32_t key = 0, bin = 0;
-    const bool in = i < hi;
-    if (in) { key = float_key(vals[u]); bin = key >> 20; }
-    const bool take = in && bin > tbin;
-    const bool maybe = in && bin == tbin;
-    const uint32_t mt = __ballot_sync(0xffffffffu, take);
-    const uint32_t mm = __ballot_sync(0xffffffffu, maybe);
-    uint32_t bt = 0, bm = 0;
-    if (lane == 0) {
-      if (mt) bt = atomicAdd(&cnt[0], __popc(mt));
-      if (mm) bm = atomicAdd(&cnt[1], __popc(mm));
-    }
-    bt = __shfl_sync(0xffffffffu, bt, 0);
-    bm = __shfl_sync(0xffffffffu, bm, 0);
-    const uint32_t below = (1u << lane) - 1u;
-    if (take) sl[bt + __popc(mt & below)] = i;
-    if (maybe) {
-      cd[bm + __popc(mm & below)] = composite(key, i);
-      atomicAdd(&h2_s[(key >> 8) & (kHistBins - 1)], 1u);
-    }
+  for (int u = 0; u < 4; ++u) {
+    key[u] = float_key(v[u]);
+    const bool in = i0 + u < hi;
+    ntk += in && (key[u] >> 20) > tbin;
+    ncd += in && (key[u] >> 20) == tbin;
+  }
+  uint32_t tot;
+  const uint32_t off = block_excl_scan(ntk | (ncd << 16), scan, &tot);   // both halves <= 4096
+  const uint32_t NCD = tot >> 16;
+  uint32_t otk = off & 0xFFFFu, ocd = off >> 16;
+  uint64_t* cd = cand + int64_t(t) * row;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int i = i0 + u;
+    if (i >= hi) continue;
+    const uint32_t b = key[u] >> 20;
+    if (b > tbin) {
+      cd[lo + otk++] = uint64_t(i);
+    } else if (b == tbin) {
+      cd[hi - NCD + ocd++] = composite(key[u], i);
+      atomicAdd(&h2_s[(key[u] >> 8) & (kHistBins - 1)], 1u);
     }
   }
   __syncthreads();
   uint32_t* g2 = hist2 + int64_t(t) * kHistBins;
   for (int i = threadIdx.x; i < kHistBins; i += blockDim.x)
     if (h2_s[i]) atomicAdd(&g2[i], h2_s[i]);
-  // 3. the last CTA of this query resolves the threshold bin and sorts
+  if (threadIdx.x == 0) info[int64_t(t) * slices + sl] = tot;
+  // 3. the last slice CTA of this query resolves the threshold and merges
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) last_s = atomicAdd(&cnt[2], 1u) == uint32_t(slices - 1);
+  if (threadIdx.x == 0) last_s = atomicAdd(&counters[int64_t(t) * 4 + 2], 1u) == uint32_t(nsl - 1);
   __syncthreads();
   if (!last_s) return;
   __threadfence();
-  const uint32_t above = __ldcg(&cnt[0]);
-  const int nc = int(__ldcg(&cnt[1]));
-  const int need = k - int(above);
-  if (need > 0) {
-    for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h2_s[i] = __ldcg(&g2[i]);
-    if (threadIdx.x == 0) nfine_s = 0;
-    __syncthreads();
-    uint32_t above2;
-    const uint32_t tbin2 = uint32_t(threshold_bin(h2_s, uint32_t(need), scan, &bin_s, &above_s, &above2));
-    const bool fits = h2_s[tbin2] <= uint32_t(kFine);
-    // candidates above the sub-bin are taken; the sub-bin's go to the fine list
-    for (int base0 = 0; base0 < nc; base0 += kU * blockDim.x) {
-      uint64_t cs[kU];
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int i = base0 + u * blockDim.x + threadIdx.x;
-        cs[u] = i < nc ? __ldcg(reinterpret_cast<const unsigned long long*>(&cd[i])) : 0ull;
-      }
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-      const int i = base0 + u * blockDim.x + threadIdx.x;
-      uint64_t c = 0;
-      uint32_t b2 = 0;
-      if (i < nc) { c = cs[u]; b2 = uint32_t(c >> 40) & (kHistBins - 1); }
-      const bool take = i < nc && b2 > tbin2;
-      const uint32_t mt = __ballot_sync(0xffffffffu, take);
-      uint32_t bt = 0;
-      if (lane == 0 && mt) bt = atomicAdd(&cnt[3], __popc(mt));
-      bt = __shfl_sync(0xffffffffu, bt, 0);
-      if (take) sl[above + bt + __popc(mt & ((1u << lane) - 1u))] = int32_t(0xFFFFFFFFu - uint32_t(c));
-      if (fits && i < nc && b2 == tbin2) fine_s[atomicAdd(&nfine_s, 1u)] = c;
-      }
-    }
-    __syncthreads();
-    const int need2 = need - int(above2);
-    uint64_t thr;
-    int nsrc;
-    if (fits) {
-      nsrc = int(nfine_s);
-      thr = select_threshold(nsrc, need2, [&](int i) { return fine_s[i]; }, hist256, sh);
-    } else {
-      // degenerate (e.g. all scores equal): exact select over every candidate of the sub-bin
-      nsrc = nc;
-      thr = select_threshold(nc, need2, [&](int i) {
-        const uint64_t c = __ldcg(&cd[i]);
-        return (uint32_t(c >> 40) & (kHistBins - 1)) == tbin2 ? c : uint64_t(0);
-      }, hist256, sh);
-    }
-    if (threadIdx.x == 0) sh[3] = 0;
-    __syncthreads();
-    const uint32_t base_out = above + above2;
-    for (int b0 = 0; b0 < nsrc; b0 += blockDim.x) {
-      const int i = b0 + threadIdx.x;
-      uint64_t c = 0;
-      if (i < nsrc) c = fits ? fine_s[i] : __ldcg(&cd[i]);
-      const bool take = i < nsrc && (uint32_t(c >> 40) & (kHistBins - 1)) == tbin2 &&
-                        (c >> 32) >> 20 == tbin && c >= thr;
-      const uint32_t mt = __ballot_sync(0xffffffffu, take);
-      uint32_t bt = 0;
-      if (lane == 0 && mt) bt = atomicAdd(&sh[3], __popc(mt));
-      bt = __shfl_sync(0xffffffffu, bt, 0);
-      if (take) sl[base_out + bt + __popc(mt & ((1u << lane) - 1u))] = int32_t(0xFFFFFFFFu - uint32_t(c));
-    }
-    __threadfence();
-    __syncthreads();
+  {
+    const uint32_t x = int(threadIdx.x) < nsl ? __ldcg(&info[int64_t(t) * slices + threadIdx.x]) : 0u;
+    uint32_t tk_tot, cd_tot;
+    const uint32_t ptk = block_excl_scan(x & 0xFFFFu, scan, &tk_tot);
+    const uint32_t pcd = block_excl_scan(x >> 16, scan, &cd_tot);
+    if (int(threadIdx.x) < nsl) { pre_s[0][threadIdx.x] = ptk; pre_s[1][threadIdx.x] = pcd; }
+    if (threadIdx.x == 0) { pre_s[0][nsl] = tk_tot; pre_s[1][nsl] = cd_tot; nfine_s = 0; }
   }
-  // bitonic sort of the k selected indices (ascending)
-  int P2 = 1;
-  while (P2 < k) P2 <<= 1;
-  for (int i = threadIdx.x; i < P2; i += blockDim.x) sort_s[i] = i < k ? __ldcg(&sl[i]) : 0x7FFFFFFF;
+  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h2_s[i] = __ldcg(&g2[i]);
   __syncthreads();
-  for (int size = 2; size <= P2; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < P2 / 2; i += blockDim.x) {
-        const int lo2 = (i / stride) * stride * 2 + (i % stride);
-        const int hi2 = lo2 + stride;
-        const bool up = ((lo2 / size) & 1) == 0;
-        const int a = sort_s[lo2], c = sort_s[hi2];
-        if ((a > c) == up) { sort_s[lo2] = c; sort_s[hi2] = a; }
-      }
-      __syncthreads();
+  const int above = int(pre_s[0][nsl]);      // entries above the threshold bin (< k)
+  const int nc = int(pre_s[1][nsl]);         // entries in it (>= k - above)
+  const int need = k - above;
+  auto cand_at = [&](int j) -> uint64_t {    // j-th candidate in index order
+    const int s2 = slice_of(pre_s[1], nsl, uint32_t(j));
+    const int hi2 = min(n, (s2 + 1) * kSlice);
+    const int ncd2 = int(pre_s[1][s2 + 1] - pre_s[1][s2]);
+    return __ldcg(reinterpret_cast<const unsigned long long*>(&cd[hi2 - ncd2 + (j - int(pre_s[1][s2]))]));
+  };
+  uint32_t above2;
+  const uint32_t tbin2 = uint32_t(threshold_bin(h2_s, uint32_t(need), scan, &bin_s, &above_s, &above2));
+  const int need2 = need - int(above2);
+  const bool fits = h2_s[tbin2] <= uint32_t(kFine);
+  uint64_t thr;
+  if (fits) {
+    // the sub-bin's candidates share their top 24 key bits: select on the rest
+    for (int j = threadIdx.x; j < nc; j += blockDim.x) {
+      const uint64_t c = cand_at(j);
+      if ((uint32_t(c >> 40) & (kHistBins - 1)) == tbin2) fine_s[atomicAdd(&nfine_s, 1u)] = c;
     }
+    __syncthreads();
+    thr = select_threshold(int(nfine_s), need2, [&](int i) { return fine_s[i]; }, hist256, sh, 3);
+  } else {
+    // degenerate (e.g. all scores equal): exact select over every candidate of the sub-bin
+    thr = select_threshold(nc, need2, [&](int j) {
+      const uint64_t c = cand_at(j);
+      return (uint32_t(c >> 40) & (kHistBins - 1)) == tbin2 ? c : uint64_t(0);
+    }, hist256, sh);
   }
-  for (int i = threadIdx.x; i < k; i += blockDim.x) o[i] = sort_s[i];
+  // selected candidates (composite >= thr), in index order
+  int32_t* take_l = lists_s;
+  int32_t* csel_l = lists_s + k;
+  uint32_t carry = 0;
+  for (int b0 = 0; b0 < nc; b0 += blockDim.x) {
+    const int j = b0 + int(threadIdx.x);
+    const uint64_t c = j < nc ? cand_at(j) : 0ull;
+    const bool f = j < nc && c >= thr;
+    uint32_t cnt;
+    const uint32_t pos = block_excl_scan(f ? 1u : 0u, scan, &cnt);
+    if (f) csel_l[carry + pos] = int32_t(0xFFFFFFFFu - uint32_t(c));
+    carry += cnt;
+  }
+  // takes, in index order
+  for (int j = threadIdx.x; j < above; j += blockDim.x) {
+    const int s2 = slice_of(pre_s[0], nsl, uint32_t(j));
+    take_l[j] = int32_t(__ldcg(reinterpret_cast<const unsigned long long*>(
+        &cd[int64_t(s2) * kSlice + (j - int(pre_s[0][s2]))])));
+  }
+  __syncthreads();
+  // merge the two ascending lists (disjoint indices) into the output
+  for (int j = threadIdx.x; j < above; j += blockDim.x) {
+    const int32_t x = take_l[j];
+    o[j + count_below(csel_l, need, x)] = x;
+  }
+  for (int j = threadIdx.x; j < need; j += blockDim.x) {
+    const int32_t y = csel_l[j];
+    o[j + count_below(take_l, above, y)] = y;
+  }
 }
 
 // ------------------------------------------------------------------------------
@@ -526,6 +539,7 @@ static int validate_shape(const v4a_index_args* a) {
   const v4a_cache& c = a->keys;
   if (c.ratio != 4) return V4A_ERR_UNSUPPORTED;
   if (c.num_blocks <= 0 || c.max_blocks <= 0) return V4A_ERR_INVALID_ARG;
+  if (int64_t(c.max_blocks) * 64 > int64_t(kMaxSlices) * kSlice) return V4A_ERR_UNSUPPORTED;
   if (a->k < 1 || a->k > kMaxK) return V4A_ERR_UNSUPPORTED;
   if (a->num_heads < 1 || a->num_heads > 128) return V4A_ERR_UNSUPPORTED;
   if (c.dim < 32 || c.dim > 256 || c.dim % 32) return V4A_ERR_UNSUPPORTED;
@@ -605,16 +619,14 @@ int index_select(const v4a_index_args* a, void* ws, size_t ws_bytes, cudaStream_
     topk_smem<<<T, 1024, smem, stream>>>(w.scores, w.row, a->keys.max_blocks * 64, a->batch.positions,
                                          a->k, a->out_idx);
   } else {
-    const int slices = int((w.row + 4095) / 4096);
+    const int slices = int((w.row + kSlice - 1) / kSlice);
     topk_hist<<<dim3(slices, T), 512, 0, stream>>>(w.scores, w.row, a->keys.max_blocks * 64,
                                                    a->batch.positions, a->k, slices, w.hist);
-    int P2 = 1;
-    while (P2 < a->k) P2 <<= 1;
-    const size_t smem = size_t(P2) * 4;
+    const size_t smem = size_t(2) * a->k * 4;
     cudaFuncSetAttribute(topk_select, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     topk_select<<<dim3(slices, T), 1024, smem, stream>>>(w.scores, w.row, a->keys.max_blocks * 64,
                                                          a->batch.positions, a->k, slices, w.hist,
-                                                         w.hist2, w.counters, w.cand, w.sel, a->out_idx);
+                                                         w.hist2, w.counters, w.cand, w.info, a->out_idx);
   }
   return cudaGetLastError() == cudaSuccess ? V4A_OK : V4A_ERR_CUDA;
 }

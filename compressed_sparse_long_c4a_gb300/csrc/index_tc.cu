@@ -124,14 +124,22 @@ __device__ void plan(const TcArgs& a, Smem& s) {
   const int c0 = threadIdx.x * per, c1 = min(a.T, c0 + per);
   uint32_t mine = 0;
   for (int t = c0; t < c1; ++t) mine += tiles_of(a, t);
-  s.part[threadIdx.x] = mine;
+  // exclusive scan of `mine` over the block: warp shuffles, then warp totals
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  uint32_t incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  if (lane == 31) s.part[wid] = incl;
   if (threadIdx.x == 0) { s.count = 0; s.t0 = a.T; s.j0 = 0; }
   __syncthreads();
-  uint32_t before = 0, all = 0;
-  for (int i = 0; i < int(blockDim.x); ++i) {
-    const uint32_t v = s.part[i];
-    if (i < int(threadIdx.x)) before += v;
-    all += v;
+  uint32_t before = incl - mine, all = 0;
+  for (int w = 0; w < nw; ++w) {
+    const uint32_t x = s.part[w];
+    if (w < wid) before += x;
+    all += x;
   }
   const uint32_t lo = uint32_t((uint64_t(all) * blockIdx.x) / gridDim.x);
   const uint32_t hi = uint32_t((uint64_t(all) * (blockIdx.x + 1)) / gridDim.x);
@@ -267,6 +275,7 @@ index_scan_tc(const TcArgs a) {
         while (!tc::mbar_try_wait(&s.full[stage], last_phase[stage]) && clock64() - t0 < 2000000000LL) {}
       }
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -449,6 +458,7 @@ index_scan_tc(const TcArgs a) {
       if (++stage == kStages) { stage = 0; phase ^= 1; }
       c.next(a);
     }
+    __syncwarp();
   }
   tc::tc_fence_before();
   __syncthreads();

@@ -67,10 +67,11 @@ def test_fewer_entries_than_k_and_first_entry():
     U.check_close(step.o.float().cpu().numpy(), np.stack([att[t][0] for t in range(2)]), U.BF16_TOL)
 
 
-@pytest.mark.parametrize("cached", [(12000, 16000), (40003, 39000)])
+@pytest.mark.parametrize("cached", [(12000, 16000), (40003, 39000), (150003, 140000)])
 def test_all_tied_scores_take_lowest_indices(cached):
     """w = 0 makes every score 0: the top-k must be the k lowest entry indices
-    (single-CTA path for short rows, multi-CTA path beyond 32K entries)."""
+    (single-CTA path while a block-table row spans <= 32K entries, multi-CTA
+    path beyond: 150,003 positions give rows of 37,504 entries)."""
     v4a = _v4a()
     spec = dataclasses.replace(I.c4a_decode_1m(), name="ties", batch=2, cached=cached)
     case = I.make_case(spec, seed=2)
