@@ -14,16 +14,20 @@
 //  * topk_smem         - one CTA per query when the row fits in shared memory:
 //                         radix select of the k-th largest (score, -index)
 //                         composite, then an ordered compaction.
-//  * topk_hist / topk_select - long rows, one CTA per 4096-score slice: a
+//  * topk_hist / topk_select - long rows, one CTA per 8192-score slice: a
 //                         4096-bin histogram of the score keys' top 12 bits
-//                         gives the threshold bin; every slice then compacts,
+//                         (built by the tensor-core scan itself when that
+//                         path scored the row, else by topk_hist) gives the
+//                         threshold bin; every slice then compacts,
 //                         in index order, its entries above that bin ("takes")
 //                         and those in it ("candidates", plus a histogram of
 //                         their next 12 bits).  The last slice CTA of a query
 //                         resolves the exact threshold among the candidates
 //                         and merges the two ordered lists into the output.
 //                         The "last CTA" is found with an atomic counter; no
-//                         CTA ever waits on another.
+//                         CTA ever waits on another.  It holds up to 8
+//                         candidates per thread in registers, so the
+//                         candidates are read from L2 once.
 
 #include <cstdio>
 
@@ -36,8 +40,8 @@ namespace v4a {
 constexpr int kSmemTopkMax = 32768;   // rows up to this length use topk_smem
 constexpr int kHistBins = 4096;       // top 12 bits of the order-preserving key
 constexpr int kMaxK = 16384;
-constexpr int kSlice = 4096;          // scores per CTA of the long-row top-k
-constexpr int kMaxSlices = 1024;      // rows up to 4M entries
+constexpr int kSlice = 8192;          // scores per CTA of the long-row top-k (8 per thread)
+constexpr int kMaxSlices = 1024;      // rows up to 8M entries
 
 struct IndexWs {
   float* scores;        // [T][row]
@@ -356,6 +360,7 @@ __device__ int threshold_bin(const uint32_t* h, uint32_t need, uint32_t* scan, i
 }
 
 constexpr int kFine = 2048;   // capacity of the resolving CTA's exact-select list
+constexpr int kRegCands = 8;  // threshold-bin candidates per thread held in registers while resolving
 
 // Position of j among the slices' ranges: the largest s with pre[s] <= j.
 __device__ __forceinline__ int slice_of(const uint32_t* pre, int nsl, uint32_t j) {
@@ -377,7 +382,7 @@ __device__ __forceinline__ int count_below(const int32_t* l, int n, int32_t x) {
   return lo;
 }
 
-__global__ void __launch_bounds__(1024, 2) topk_select(const float* scores, int64_t row, int max_entries,
+__global__ void __launch_bounds__(1024, 1) topk_select(const float* scores, int64_t row, int max_entries,
                                                    const int32_t* positions, int k, int slices,
                                                    const uint32_t* hist, uint32_t* hist2,
                                                    uint32_t* counters, uint64_t* cand, uint32_t* info,
@@ -402,38 +407,46 @@ __global__ void __launch_bounds__(1024, 2) topk_select(const float* scores, int6
   }
   const int nsl = (n + kSlice - 1) / kSlice;
   if (sl >= nsl) return;
-  // 1. threshold bin of the top 12 key bits
+  // 1. this slice's scores (thread c owns entries lo + 8c .. lo + 8c + 7), loaded
+  //    first so that their latency overlaps the threshold search below
+  constexpr int kPer = kSlice / 1024;
+  const int lo = sl * kSlice, hi = min(n, lo + kSlice);
+  const float* sc = scores + int64_t(t) * row;
+  const int i0 = lo + kPer * int(threadIdx.x);
+  float v[kPer];
+  if (i0 + kPer - 1 < hi) {
+#pragma unroll
+    for (int u = 0; u < kPer; u += 4) {
+      const float4 f = __ldcg(reinterpret_cast<const float4*>(sc + i0 + u));
+      v[u] = f.x; v[u + 1] = f.y; v[u + 2] = f.z; v[u + 3] = f.w;
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) v[u] = i0 + u < hi ? __ldcg(sc + i0 + u) : 0.f;
+  }
+  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h2_s[i] = 0;
+  // 2. threshold bin of the top 12 key bits
   uint32_t above1;
   const uint32_t tbin = uint32_t(threshold_bin(hist + int64_t(t) * kHistBins, uint32_t(k), scan, &bin_s,
                                                &above_s, &above1));
-  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h2_s[i] = 0;
-  // 2. ordered compaction of this slice: thread c owns entries lo + 4c .. lo + 4c + 3
-  const int lo = sl * kSlice, hi = min(n, lo + kSlice);
-  const float* sc = scores + int64_t(t) * row;
-  const int i0 = lo + 4 * int(threadIdx.x);
-  float v[4];
-  if (i0 + 3 < hi) {
-    const float4 f = *reinterpret_cast<const float4*>(sc + i0);
-    v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
-  } else {
+  // 3. ordered compaction of this slice into its range of the candidate array:
+  //    entries above the threshold bin ("takes", as indices) from the front,
+  //    entries in it (as composites) at the back
+  uint32_t key[kPer], ntk = 0, ncd = 0;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) v[u] = i0 + u < hi ? sc[i0 + u] : 0.f;
-  }
-  uint32_t key[4], ntk = 0, ncd = 0;
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
+  for (int u = 0; u < kPer; ++u) {
     key[u] = float_key(v[u]);
     const bool in = i0 + u < hi;
     ntk += in && (key[u] >> 20) > tbin;
     ncd += in && (key[u] >> 20) == tbin;
   }
   uint32_t tot;
-  const uint32_t off = block_excl_scan(ntk | (ncd << 16), scan, &tot);   // both halves <= 4096
+  const uint32_t off = block_excl_scan(ntk | (ncd << 16), scan, &tot);   // both halves <= kSlice < 2^16
   const uint32_t NCD = tot >> 16;
   uint32_t otk = off & 0xFFFFu, ocd = off >> 16;
   uint64_t* cd = cand + int64_t(t) * row;
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
+  for (int u = 0; u < kPer; ++u) {
     const int i = i0 + u;
     if (i >= hi) continue;
     const uint32_t b = key[u] >> 20;
@@ -449,7 +462,7 @@ __global__ void __launch_bounds__(1024, 2) topk_select(const float* scores, int6
   for (int i = threadIdx.x; i < kHistBins; i += blockDim.x)
     if (h2_s[i]) atomicAdd(&g2[i], h2_s[i]);
   if (threadIdx.x == 0) info[int64_t(t) * slices + sl] = tot;
-  // 3. the last slice CTA of this query resolves the threshold and merges
+  // 4. the last slice CTA of this query resolves the threshold and merges
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) last_s = atomicAdd(&counters[int64_t(t) * 4 + 2], 1u) == uint32_t(nsl - 1);
@@ -457,62 +470,87 @@ __global__ void __launch_bounds__(1024, 2) topk_select(const float* scores, int6
   if (!last_s) return;
   __threadfence();
   {
+    // slice counts and the second-level histogram, both loads in flight together
     const uint32_t x = int(threadIdx.x) < nsl ? __ldcg(&info[int64_t(t) * slices + threadIdx.x]) : 0u;
+    for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h2_s[i] = __ldcg(&g2[i]);
     uint32_t tk_tot, cd_tot;
     const uint32_t ptk = block_excl_scan(x & 0xFFFFu, scan, &tk_tot);
     const uint32_t pcd = block_excl_scan(x >> 16, scan, &cd_tot);
     if (int(threadIdx.x) < nsl) { pre_s[0][threadIdx.x] = ptk; pre_s[1][threadIdx.x] = pcd; }
     if (threadIdx.x == 0) { pre_s[0][nsl] = tk_tot; pre_s[1][nsl] = cd_tot; nfine_s = 0; }
   }
-  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h2_s[i] = __ldcg(&g2[i]);
   __syncthreads();
   const int above = int(pre_s[0][nsl]);      // entries above the threshold bin (< k)
   const int nc = int(pre_s[1][nsl]);         // entries in it (>= k - above)
   const int need = k - above;
+  int32_t* take_l = lists_s;
+  int32_t* csel_l = lists_s + k;
   auto cand_at = [&](int j) -> uint64_t {    // j-th candidate in index order
     const int s2 = slice_of(pre_s[1], nsl, uint32_t(j));
     const int hi2 = min(n, (s2 + 1) * kSlice);
     const int ncd2 = int(pre_s[1][s2 + 1] - pre_s[1][s2]);
     return __ldcg(reinterpret_cast<const unsigned long long*>(&cd[hi2 - ncd2 + (j - int(pre_s[1][s2]))]));
   };
-  uint32_t above2;
-  const uint32_t tbin2 = uint32_t(threshold_bin(h2_s, uint32_t(need), scan, &bin_s, &above_s, &above2));
-  const int need2 = need - int(above2);
-  const bool fits = h2_s[tbin2] <= uint32_t(kFine);
-  uint64_t thr;
-  if (fits) {
-    // the sub-bin's candidates share their top 24 key bits: select on the rest
-    for (int j = threadIdx.x; j < nc; j += blockDim.x) {
-      const uint64_t c = cand_at(j);
-      if ((uint32_t(c >> 40) & (kHistBins - 1)) == tbin2) fine_s[atomicAdd(&nfine_s, 1u)] = c;
-    }
-    __syncthreads();
-    thr = select_threshold(int(nfine_s), need2, [&](int i) { return fine_s[i]; }, hist256, sh, 3);
-  } else {
-    // degenerate (e.g. all scores equal): exact select over every candidate of the sub-bin
-    thr = select_threshold(nc, need2, [&](int j) {
-      const uint64_t c = cand_at(j);
-      return (uint32_t(c >> 40) & (kHistBins - 1)) == tbin2 ? c : uint64_t(0);
-    }, hist256, sh);
-  }
-  // selected candidates (composite >= thr), in index order
-  int32_t* take_l = lists_s;
-  int32_t* csel_l = lists_s + k;
-  uint32_t carry = 0;
-  for (int b0 = 0; b0 < nc; b0 += blockDim.x) {
-    const int j = b0 + int(threadIdx.x);
-    const uint64_t c = j < nc ? cand_at(j) : 0ull;
-    const bool f = j < nc && c >= thr;
-    uint32_t cnt;
-    const uint32_t pos = block_excl_scan(f ? 1u : 0u, scan, &cnt);
-    if (f) csel_l[carry + pos] = int32_t(0xFFFFFFFFu - uint32_t(c));
-    carry += cnt;
-  }
-  // takes, in index order
+  // takes, in index order (independent of the exact threshold)
   for (int j = threadIdx.x; j < above; j += blockDim.x) {
     const int s2 = slice_of(pre_s[0], nsl, uint32_t(j));
     take_l[j] = int32_t(__ldcg(reinterpret_cast<const unsigned long long*>(
         &cd[int64_t(s2) * kSlice + (j - int(pre_s[0][s2]))])));
+  }
+  if (nc <= int(blockDim.x) * kRegCands) {
+    // common case: every candidate is read once into registers; thread c owns
+    // the run [c*R, c*R + R) of the candidates, so its selected ones are
+    // consecutive in index order
+    const int R = (nc + int(blockDim.x) - 1) / int(blockDim.x);
+    const int j0 = int(threadIdx.x) * R;
+    uint64_t c[kRegCands];
+#pragma unroll
+    for (int u = 0; u < kRegCands; ++u) c[u] = (u < R && j0 + u < nc) ? cand_at(j0 + u) : 0ull;
+    uint32_t above2;
+    const uint32_t tbin2 = uint32_t(threshold_bin(h2_s, uint32_t(need), scan, &bin_s, &above_s, &above2));
+    const int need2 = need - int(above2);
+    uint64_t thr;
+    if (h2_s[tbin2] <= uint32_t(kFine)) {
+#pragma unroll
+      for (int u = 0; u < kRegCands; ++u)
+        if (u < R && j0 + u < nc && ((uint32_t(c[u] >> 40) & (kHistBins - 1)) == tbin2))
+          fine_s[atomicAdd(&nfine_s, 1u)] = c[u];
+      __syncthreads();
+      // the sub-bin's candidates share their top 24 key bits: select on the rest
+      thr = select_threshold(int(nfine_s), need2, [&](int i) { return fine_s[i]; }, hist256, sh, 3);
+    } else {
+      // degenerate (e.g. all scores equal): exact select over every candidate of the sub-bin
+      thr = select_threshold(nc, need2, [&](int j) {
+        const uint64_t cc = cand_at(j);
+        return (uint32_t(cc >> 40) & (kHistBins - 1)) == tbin2 ? cc : uint64_t(0);
+      }, hist256, sh);
+    }
+    uint32_t cnt = 0;
+#pragma unroll
+    for (int u = 0; u < kRegCands; ++u) cnt += (u < R && j0 + u < nc && c[u] >= thr) ? 1u : 0u;
+    uint32_t pos = block_excl_scan(cnt, scan, nullptr);
+#pragma unroll
+    for (int u = 0; u < kRegCands; ++u)
+      if (u < R && j0 + u < nc && c[u] >= thr) csel_l[pos++] = int32_t(0xFFFFFFFFu - uint32_t(c[u]));
+  } else {
+    // more candidates than registers hold: stream them from L2 in each pass
+    uint32_t above2;
+    const uint32_t tbin2 = uint32_t(threshold_bin(h2_s, uint32_t(need), scan, &bin_s, &above_s, &above2));
+    const int need2 = need - int(above2);
+    const uint64_t thr = select_threshold(nc, need2, [&](int j) {
+      const uint64_t cc = cand_at(j);
+      return (uint32_t(cc >> 40) & (kHistBins - 1)) == tbin2 ? cc : uint64_t(0);
+    }, hist256, sh);
+    uint32_t carry = 0;
+    for (int b0 = 0; b0 < nc; b0 += blockDim.x) {
+      const int j = b0 + int(threadIdx.x);
+      const uint64_t cc = j < nc ? cand_at(j) : 0ull;
+      const bool f = j < nc && cc >= thr;
+      uint32_t cnt;
+      const uint32_t pos = block_excl_scan(f ? 1u : 0u, scan, &cnt);
+      if (f) csel_l[carry + pos] = int32_t(0xFFFFFFFFu - uint32_t(cc));
+      carry += cnt;
+    }
   }
   __syncthreads();
   // merge the two ascending lists (disjoint indices) into the output
@@ -590,7 +628,7 @@ int index_scores(const v4a_index_args* a, void* ws, size_t ws_bytes, cudaStream_
   w = ws_layout(a, ws);
   const v4a_cache& c = a->keys;
   if (cudaMemsetAsync(w.hist, 0, w.zero_bytes, stream) != cudaSuccess) return V4A_ERR_CUDA;
-  if (index_score_tc(a, w.scores, w.row, stream, &rc)) return rc;
+  if (index_score_tc(a, w.scores, w.row, w.row > kSmemTopkMax ? w.hist : nullptr, stream, &rc)) return rc;
   ScoreArgs sa;
   sa.T = T; sa.H = a->num_heads; sa.dim = c.dim; sa.k_fmt = c.format; sa.q_fmt = a->q_format;
   sa.seq_ids = a->batch.seq_ids; sa.positions = a->batch.positions; sa.keys = c;
@@ -620,8 +658,10 @@ int index_select(const v4a_index_args* a, void* ws, size_t ws_bytes, cudaStream_
                                          a->k, a->out_idx);
   } else {
     const int slices = int((w.row + kSlice - 1) / kSlice);
-    topk_hist<<<dim3(slices, T), 512, 0, stream>>>(w.scores, w.row, a->keys.max_blocks * 64,
-                                                   a->batch.positions, a->k, slices, w.hist);
+    // the tensor-core scan already left the first-level histogram
+    if (!index_score_tc_supported(a))
+      topk_hist<<<dim3(slices, T), 512, 0, stream>>>(w.scores, w.row, a->keys.max_blocks * 64,
+                                                     a->batch.positions, a->k, slices, w.hist);
     const size_t smem = size_t(2) * a->k * 4;
     cudaFuncSetAttribute(topk_select, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     topk_select<<<dim3(slices, T), 1024, smem, stream>>>(w.scores, w.row, a->keys.max_blocks * 64,
