@@ -7,18 +7,25 @@
 // o_m = sum_n softmax(q_m . k_n) k_n).
 //
 // One CTA per (64-key chunk of a query's key list, query):
-//   Q     [128 rows = heads, zero-padded][D] bf16  -> smem, K-major, 128-B swizzle
+//   Q     [128 rows = heads, zero-padded][D] bf16  -> smem by TMA, K-major,
+//         128-B swizzle
 //   K     64 gathered rows [64][D] bf16 (fp8 codes are converted exactly to
-//         bf16; their per-row scale is applied to the logits and to P)
+//         bf16 on the way in; their per-row scale is applied to the logits
+//         and to P)
 //   S     = Q K^T           M=128, N=64,  K=D   -> TMEM columns [0, 64)
-//   P     = exp(tau*s_n*S - m) * s_n, bf16 -> smem (one thread per head row)
+//   P     = 2^(S*f_n - max) * s_n, bf16 -> smem (one thread per head row;
+//         f_n = tau * log2(e) * s_n folds the softmax scale and the key's
+//         dequantisation scale into one factor per key)
 //   O     = P K             M=128, N=256 per MMA (K as an MN-major operand),
 //                           K=64              -> TMEM columns [0, D) (the S
 //                           columns are reused once S has been read)
-// The chunk's normalised O (bf16) and (max, sum) go to the workspace; a
-// combine kernel merges the chunks of each query.  A single thread issues
-// every MMA; completion is tracked with tcgen05.commit on mbarriers whose
-// waits are bounded.
+// The chunk's normalised O is written as bf16 rows into shared memory (the Q
+// buffer, free once S is done) in the 128-byte swizzled layout of 64-column
+// boxes, and leaves with TMA tensor stores: whole lines, no partial-sector
+// writes.  With several chunks per query the rows go to the workspace with
+// the chunk's (max, sum) and a combine kernel merges them; with one chunk
+// they are the output.  A single thread issues every MMA; completion is
+// tracked with tcgen05.commit on mbarriers whose waits are bounded.
 
 #include <mutex>
 
@@ -30,7 +37,8 @@ namespace {
 
 constexpr int kKeys = 64;            // keys per CTA (one chunk)
 constexpr int kRows = 128;           // MMA M (heads, zero-padded)
-constexpr int kThreads = 256;      // warps 0-3 own TMEM lane quarters for the softmax; all 8 drain
+constexpr int kThreads = 256;        // warps 0-3 own TMEM lane quarters for the softmax; all 8 drain
+constexpr float kLog2e = 1.4426950408889634f;
 
 struct AtcArgs {
   int T, H, D, ratio, fmt, wfmt, wlen, wcap, k, splits;
@@ -49,17 +57,19 @@ struct AtcArgs {
   uint16_t* out;
   float* lse;
   uint16_t* part_o;   // [T][splits][H][D] bf16, normalised by the chunk's sum
-  float* part_ml;     // [T][splits][H][2] = (max, sum)
+  float* part_ml;     // [T][splits][H][2] = (max, sum); max in log2 units
   int32_t* status;
   uint32_t idesc_s, idesc_pv;
+  int tma_out;        // rows leave through the output tensor map (H % 8 == 0)
 };
 
-struct ASmem {
-  uint64_t bar_q, bar_s, bar_o;
+struct ASmem {   // every field read with vector loads carries its alignment explicitly
+  uint64_t bar_q, bar_s, bar_o[2];
   uint32_t tmem_base;
   int abort_flag;
   const uint8_t* src[kKeys];
-  float kscale[kKeys];
+  alignas(16) float kf[kKeys];      // tau * log2(e) * key scale, or 0 for an empty slot (read as float4)
+  alignas(16) float ks[kKeys];      // key scale (applied to P), 0 for an empty slot (read as float4)
   int kfmt[kKeys];                  // -1: no key in this slot
   float row_l[kRows], row_m[kRows];   // softmax sums / maxima handed to the drain warps
 };
@@ -84,16 +94,20 @@ __device__ __forceinline__ uint32_t bf16x2_from_e4m3x2(uint16_t two) {
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
+// Byte offset of 16-byte chunk `ch` (0..7) of row r inside a 128-byte swizzled box.
+__device__ __forceinline__ uint32_t sw_off(int r, int ch) { return uint32_t(r * 128 + ((ch ^ (r & 7)) << 4)); }
+
 __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
-                                                             const __grid_constant__ CUtensorMap qmap) {
+                                                             const __grid_constant__ CUtensorMap qmap,
+                                                             const __grid_constant__ CUtensorMap omap) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int D = a.D, nsub = D / 64;
-  uint8_t* Qs = base;                                  // nsub x [128 rows][128 B]
+  uint8_t* Qs = base;                                  // nsub x [128 rows][128 B]; later the O rows
   uint8_t* Ks = Qs + nsub * kRows * 128;               // nsub x [64 rows][128 B]
   uint8_t* Ps = Ks + nsub * kKeys * 128;               // [128 rows][128 B]
   ASmem& s = *reinterpret_cast<ASmem*>(Ps + kRows * 128);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int t = blockIdx.y, sp = blockIdx.x;
   const int b = a.seq_ids[t], m = a.positions[t];
   const int nvis = (m + 1) / a.ratio;
@@ -113,9 +127,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
   if (tid == 0) {
     tc::mbar_init(&s.bar_q, 1);
     tc::mbar_init(&s.bar_s, 1);
-    tc::mbar_init(&s.bar_o, 1);
+    tc::mbar_init(&s.bar_o[0], 1);
+    tc::mbar_init(&s.bar_o[1], 1);
     s.abort_flag = 0;
     tc::mbar_fence_init();
+    if (a.tma_out) tc::prefetch_tmap(&omap);
     // Q: 128 rows from this query's first head (rows past the last head are
     // the next query's or zero-filled; their outputs are never stored), one
     // 64-column swizzled box per K sub-tile
@@ -164,50 +180,59 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
       }
     }
     s.src[tid] = src;
-    s.kscale[tid] = sc;
+    s.kf[tid] = f >= 0 ? sc * a.scale * kLog2e : 0.f;
+    s.ks[tid] = f >= 0 ? sc : 0.f;
     s.kfmt[tid] = f;
   }
   __syncthreads();
 
   // ---- stage K into swizzled smem ----
-  // keys: bf16 rows go straight to smem with cp.async; fp8 rows are loaded
-  // into registers first (all loads in flight together), then converted
-  // exactly to bf16 and stored swizzled.
-  const int kchunks = kKeys * (D / 8);
-  constexpr int kMaxPer = kKeys * (512 / 8) / kThreads;   // 16 for D = 512
-  uint2 raw[kMaxPer];
+  // bf16 rows: 16-byte cp.async straight into place.  fp8 rows: 16-byte loads
+  // (16 codes) into registers, all in flight together, then each converted
+  // exactly to 16 bf16 values = two 16-byte chunks.
+  {
+    const int bchunks = kKeys * (D / 8);              // 16-byte bf16 chunks of the tile
+    const int fchunks = kKeys * (D / 16);             // 16-byte fp8 chunks of the tile
+    constexpr int kMaxPer = kKeys * (512 / 16) / kThreads;   // 8 for D = 512
+    uint4 raw[kMaxPer];
 #pragma unroll
-  for (int i = 0; i < kMaxPer; ++i) {
-    const int c = tid + i * kThreads;
-    raw[i] = make_uint2(0, 0);
-    if (c >= kchunks) continue;
-    const int r = c / (D / 8), cc = c % (D / 8);
-    const int f = s.kfmt[r];
-    if (f == V4A_KV_BF16) {
-      uint8_t* dst = Ks + (cc >> 3) * (kKeys * 128) + r * 128 + (((cc & 7) ^ (r & 7)) << 4);
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)),
-                   "l"(s.src[r] + cc * 16)
+    for (int i = 0; i < kMaxPer; ++i) {
+      const int c = tid + i * kThreads;
+      raw[i] = make_uint4(0, 0, 0, 0);
+      if (c >= fchunks) continue;
+      const int r = c / (D / 16), cc = c % (D / 16);
+      if (s.kfmt[r] == V4A_KV_FP8_TOKEN) raw[i] = __ldg(reinterpret_cast<const uint4*>(s.src[r] + cc * 16));
+    }
+    for (int c = tid; c < bchunks; c += kThreads) {
+      const int r = c / (D / 8), cc = c % (D / 8);
+      if (s.kfmt[r] != V4A_KV_BF16) continue;
+      uint8_t* dst = Ks + (cc >> 3) * (kKeys * 128) + sw_off(r, cc & 7);
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(s.src[r] + cc * 16)
                    : "memory");
-    } else if (f == V4A_KV_FP8_TOKEN) {
-      raw[i] = __ldg(reinterpret_cast<const uint2*>(s.src[r] + cc * 8));
     }
-  }
 #pragma unroll
-  for (int i = 0; i < kMaxPer; ++i) {
-    const int c = tid + i * kThreads;
-    if (c >= kchunks) continue;
-    const int r = c / (D / 8), cc = c % (D / 8);
-    const int f = s.kfmt[r];
-    if (f == V4A_KV_BF16) continue;
-    uint8_t* dst = Ks + (cc >> 3) * (kKeys * 128) + r * 128 + (((cc & 7) ^ (r & 7)) << 4);
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (f == V4A_KV_FP8_TOKEN) {
-      v.x = bf16x2_from_e4m3x2(uint16_t(raw[i].x & 0xffffu));
-      v.y = bf16x2_from_e4m3x2(uint16_t(raw[i].x >> 16));
-      v.z = bf16x2_from_e4m3x2(uint16_t(raw[i].y & 0xffffu));
-      v.w = bf16x2_from_e4m3x2(uint16_t(raw[i].y >> 16));
+    for (int i = 0; i < kMaxPer; ++i) {
+      const int c = tid + i * kThreads;
+      if (c >= fchunks) continue;
+      const int r = c / (D / 16), cc = c % (D / 16);   // fp8 chunk cc -> bf16 chunks 2cc, 2cc+1
+      const int f = s.kfmt[r];
+      if (f == V4A_KV_BF16) continue;
+      uint4 v0 = make_uint4(0, 0, 0, 0), v1 = make_uint4(0, 0, 0, 0);
+      if (f == V4A_KV_FP8_TOKEN) {
+        v0.x = bf16x2_from_e4m3x2(uint16_t(raw[i].x & 0xffffu));
+        v0.y = bf16x2_from_e4m3x2(uint16_t(raw[i].x >> 16));
+        v0.z = bf16x2_from_e4m3x2(uint16_t(raw[i].y & 0xffffu));
+        v0.w = bf16x2_from_e4m3x2(uint16_t(raw[i].y >> 16));
+        v1.x = bf16x2_from_e4m3x2(uint16_t(raw[i].z & 0xffffu));
+        v1.y = bf16x2_from_e4m3x2(uint16_t(raw[i].z >> 16));
+        v1.z = bf16x2_from_e4m3x2(uint16_t(raw[i].w & 0xffffu));
+        v1.w = bf16x2_from_e4m3x2(uint16_t(raw[i].w >> 16));
+      }
+      const int c0 = 2 * cc;
+      uint8_t* sub = Ks + (c0 >> 3) * (kKeys * 128);
+      *reinterpret_cast<uint4*>(sub + sw_off(r, c0 & 7)) = v0;
+      *reinterpret_cast<uint4*>(sub + sw_off(r, (c0 + 1) & 7)) = v1;
     }
-    *reinterpret_cast<uint4*>(dst) = v;
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
   tc::mbar_wait(&s.bar_q, 0, a.status, &s.abort_flag);
@@ -239,80 +264,110 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
   if (warp < 4) {
     float v[64];
     tc::tmem_ld64(lane_addr, v);
+    const float4* kf4 = reinterpret_cast<const float4*>(s.kf);
 #pragma unroll
-    for (int n = 0; n < 64; ++n) {
-      const float z = s.kfmt[n] >= 0 ? v[n] * a.scale * s.kscale[n] : -INFINITY;
-      v[n] = z;
-      mx = fmaxf(mx, z);
+    for (int n = 0; n < 64; n += 4) {
+      const float4 f = kf4[n >> 2];
+      // z in log2 units; an empty slot has factor 0 and is masked below
+      v[n] *= f.x; v[n + 1] *= f.y; v[n + 2] *= f.z; v[n + 3] *= f.w;
+      if (f.x != 0.f) mx = fmaxf(mx, v[n]);
+      if (f.y != 0.f) mx = fmaxf(mx, v[n + 1]);
+      if (f.z != 0.f) mx = fmaxf(mx, v[n + 2]);
+      if (f.w != 0.f) mx = fmaxf(mx, v[n + 3]);
     }
+    const float4* ks4 = reinterpret_cast<const float4*>(s.ks);
     uint32_t pk[32];
 #pragma unroll
-    for (int n = 0; n < 64; n += 2) {
-      const float p0 = s.kfmt[n] >= 0 ? __expf(v[n] - mx) : 0.f;
-      const float p1 = s.kfmt[n + 1] >= 0 ? __expf(v[n + 1] - mx) : 0.f;
-      l += p0 + p1;
-      const __nv_bfloat162 pb = __floats2bfloat162_rn(p0 * s.kscale[n], p1 * s.kscale[n + 1]);
-      pk[n >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
+    for (int n = 0; n < 64; n += 4) {
+      const float4 k = ks4[n >> 2];
+      const float p0 = k.x != 0.f ? exp2f(v[n] - mx) : 0.f;
+      const float p1 = k.y != 0.f ? exp2f(v[n + 1] - mx) : 0.f;
+      const float p2 = k.z != 0.f ? exp2f(v[n + 2] - mx) : 0.f;
+      const float p3 = k.w != 0.f ? exp2f(v[n + 3] - mx) : 0.f;
+      l += (p0 + p1) + (p2 + p3);
+      const __nv_bfloat162 b01 = __floats2bfloat162_rn(p0 * k.x, p1 * k.y);
+      const __nv_bfloat162 b23 = __floats2bfloat162_rn(p2 * k.z, p3 * k.w);
+      pk[n >> 1] = *reinterpret_cast<const uint32_t*>(&b01);
+      pk[(n >> 1) + 1] = *reinterpret_cast<const uint32_t*>(&b23);
     }
 #pragma unroll
     for (int c = 0; c < 8; ++c)
-      *reinterpret_cast<uint4*>(Ps + row * 128 + ((c ^ (row & 7)) << 4)) =
-          make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      *reinterpret_cast<uint4*>(Ps + sw_off(row, c)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
   }
   tc::fence_proxy_async();
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   // ---- O = P K (S columns are free again) ----
+  // Two N = 256 halves, each with its own commit, so the first half drains
+  // while the tensor core computes the second.
+  const int halves = D > 256 ? D / 256 : 1;
   if (tid == 0 && !*abort_flag) {
     const uint32_t p0 = tc::smem_u32(Ps), k0 = tc::smem_u32(Ks);
-    const int halves = D > 256 ? D / 256 : 1;
     const int nchunk = D > 256 ? 4 : nsub;        // 64-column N chunks per MMA
-    for (int st = 0; st < kKeys / 16; ++st) {
-      const uint64_t ad = tc::desc_sw128(p0) + 2 * st;
-      for (int hf = 0; hf < halves; ++hf) {
-        const uint64_t bd =
-            desc_sw128_mn(k0 + hf * nchunk * (kKeys * 128) + st * 16 * 128, kKeys * 128);
+    for (int hf = 0; hf < halves; ++hf) {
+      for (int st = 0; st < kKeys / 16; ++st) {
+        const uint64_t ad = tc::desc_sw128(p0) + 2 * st;
+        const uint64_t bd = desc_sw128_mn(k0 + hf * nchunk * (kKeys * 128) + st * 16 * 128, kKeys * 128);
         tc::mma_f16(tmem + hf * 256, ad, bd, a.idesc_pv, st > 0);
       }
+      tc::mma_commit(&s.bar_o[hf]);
     }
-    tc::mma_commit(&s.bar_o);
   }
   if (warp < 4) { s.row_l[row] = l; s.row_m[row] = mx; }
-  ok = __all_sync(0xffffffffu, ok && tc::mbar_wait(&s.bar_o, 0, a.status, abort_flag));
   __syncthreads();
-  tc::tc_fence_after();
   l = s.row_l[row];
   mx = s.row_m[row];
   const bool store = ok && row < a.H;   // H need not be a multiple of 32: loads stay warp-wide
-  {
-    const float inv = l > 0.f ? 1.f / l : 0.f;   // a chunk of only padding (-1) entries has l = 0
-    const bool direct = a.splits == 1;
-    uint16_t* dst = direct ? a.out + (int64_t(t) * a.H + row) * D : a.part_o + (pi0 * a.H + row) * D;
-    // warps 0-3 drain the first half of the 64-column groups, warps 4-7 the rest
-    const int half = nsub / 2;
-    const int c0 = warp < 4 ? 0 : half, c1 = warp < 4 ? half : nsub;
+  const float inv = l > 0.f ? 1.f / l : 0.f;   // a chunk of only padding (-1) entries has l = 0
+  const bool direct = a.splits == 1;
+  // half hf's 64-column groups: warps 0-3 drain the first half of them, warps 4-7 the rest
+  const int per_half = nsub / halves;
+  for (int hf = 0; hf < halves; ++hf) {
+    ok = __all_sync(0xffffffffu, ok && tc::mbar_wait(&s.bar_o[hf], 0, a.status, abort_flag));
+    tc::tc_fence_after();
+    const int g0 = hf * per_half, gh = per_half / 2;
+    const int c0 = warp < 4 ? g0 : g0 + gh, c1 = warp < 4 ? g0 + gh : g0 + per_half;
     for (int c = c0; c < c1; ++c) {
       float v[64];
       tc::tmem_ld64(lane_addr + c * 64, v);
-      if (!store) continue;
+      if (!(store && ok)) continue;
+      uint4 o[8];
 #pragma unroll
       for (int i = 0; i < 64; i += 8) {
-        uint4 o;
         __nv_bfloat162 b0 = __floats2bfloat162_rn(v[i] * inv, v[i + 1] * inv);
         __nv_bfloat162 b1 = __floats2bfloat162_rn(v[i + 2] * inv, v[i + 3] * inv);
         __nv_bfloat162 b2 = __floats2bfloat162_rn(v[i + 4] * inv, v[i + 5] * inv);
         __nv_bfloat162 b3 = __floats2bfloat162_rn(v[i + 6] * inv, v[i + 7] * inv);
-        o.x = *reinterpret_cast<uint32_t*>(&b0);
-        o.y = *reinterpret_cast<uint32_t*>(&b1);
-        o.z = *reinterpret_cast<uint32_t*>(&b2);
-        o.w = *reinterpret_cast<uint32_t*>(&b3);
-        *reinterpret_cast<uint4*>(dst + c * 64 + i) = o;
+        o[i >> 3] = make_uint4(*reinterpret_cast<uint32_t*>(&b0), *reinterpret_cast<uint32_t*>(&b1),
+                               *reinterpret_cast<uint32_t*>(&b2), *reinterpret_cast<uint32_t*>(&b3));
+      }
+      if (a.tma_out) {
+        // rows -> bf16 in the (free) Q buffer as a swizzled 64-column box
+        uint8_t* box = Qs + c * (kRows * 128);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) *reinterpret_cast<uint4*>(box + sw_off(row, i)) = o[i];
+      } else {
+        uint16_t* dst = direct ? a.out + (int64_t(t) * a.H + row) * D : a.part_o + (pi0 * a.H + row) * D;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) *reinterpret_cast<uint4*>(dst + c * 64 + i * 8) = o[i];
       }
     }
-    if (!store || warp >= 4) {
-    } else if (direct) {
-      if (a.lse) a.lse[int64_t(t) * a.H + row] = mx + logf(l);
+    if (a.tma_out) {
+      // this half's boxes leave with TMA tensor stores while the next half drains
+      tc::fence_proxy_async();
+      __syncthreads();
+      if (tid == 0 && ok) {
+        const int y = direct ? t * a.H : int(pi0) * a.H;
+        for (int c = g0; c < g0 + per_half; ++c) tc::tma_store_2d(&omap, Qs + c * (kRows * 128), c * 64, y);
+        tc::bulk_commit();
+      }
+    }
+  }
+  if (a.tma_out && tid == 0) tc::bulk_wait_read();   // shared memory stays valid until the stores have read it
+  if (store && warp < 4) {
+    if (direct) {
+      if (a.lse) a.lse[int64_t(t) * a.H + row] = (mx + log2f(l)) * (1.f / kLog2e);
     } else {
       a.part_ml[(pi0 * a.H + row) * 2] = mx;
       a.part_ml[(pi0 * a.H + row) * 2 + 1] = l;
@@ -326,58 +381,72 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
   }
 }
 
-// out = sum_s w_s * O_s with w_s = l_s e^{m_s} / sum_s' l_s' e^{m_s'}.
-// One CTA of D/8 threads per (head, query); each thread owns 8 dims and
-// keeps all of its split loads in flight together.
-__global__ void attn_combine_bf16(int H, int D, int splits, const uint16_t* part_o, const float* part_ml,
-                                  uint16_t* out, float* lse) {
-  const int t = blockIdx.y, h = blockIdx.x;
-  __shared__ float wsm[512];
-  __shared__ float inv_s;
-  const float* ml = part_ml + (int64_t(t) * splits * H + h) * 2;
-  float mx = -INFINITY;
-  for (int s = 0; s < splits; ++s) mx = fmaxf(mx, ml[int64_t(s) * H * 2]);
-  for (int s = threadIdx.x; s < splits; s += blockDim.x) {
-    const float ms = ml[int64_t(s) * H * 2];
-    wsm[s] = ms == -INFINITY ? 0.f : ml[int64_t(s) * H * 2 + 1] * __expf(ms - mx);
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
+// out = sum_s w_s * O_s with w_s = l_s 2^{m_s} / sum_s' l_s' 2^{m_s'} (m in log2 units).
+// One CTA of 256 threads per (query, group of 4 heads): thread = (head, 8-dim
+// chunk, split group); each thread keeps the loads of its splits in flight
+// together, and the split groups are summed through shared memory.
+constexpr int kCombHeads = 4;
+
+__global__ void __launch_bounds__(256) attn_combine_bf16(int H, int D, int splits, const uint16_t* part_o,
+                                                         const float* part_ml, uint16_t* out, float* lse) {
+  __shared__ float wsm[kCombHeads][512];
+  __shared__ float inv_s[kCombHeads];
+  const int t = blockIdx.y, h0 = blockIdx.x * kCombHeads;
+  // 1. weights of every split of the CTA's heads
+  for (int i = threadIdx.x; i < kCombHeads * 32; i += blockDim.x) {
+    const int hh = i >> 5, lane = i & 31, h = h0 + hh;
+    if (h >= H) continue;
+    const float* ml = part_ml + (int64_t(t) * splits * H + h) * 2;
+    float mx = -INFINITY;
+    for (int s = lane; s < splits; s += 32) mx = fmaxf(mx, ml[int64_t(s) * H * 2]);
+    mx = warp_max(mx);
     float tot = 0.f;
-    for (int s = 0; s < splits; ++s) tot += wsm[s];
-    inv_s = 1.f / tot;
-    if (lse) lse[int64_t(t) * H + h] = mx + logf(tot);
-  }
-  __syncthreads();
-  const int d = threadIdx.x * 8;
-  if (d >= D) return;
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  const uint16_t* po = part_o + (int64_t(t) * splits * H + h) * D + d;
-  constexpr int kUnroll = 8;
-  for (int s0 = 0; s0 < splits; s0 += kUnroll) {
-    uint4 v[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-      v[u] = (s0 + u < splits) ? *reinterpret_cast<const uint4*>(po + int64_t(s0 + u) * H * D)
-                               : make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const float w = (s0 + u < splits) ? wsm[s0 + u] : 0.f;
-      if (w == 0.f) continue;   // empty chunk: its partial carries no weight (and may be garbage)
-      const uint32_t q[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        acc[2 * i] = fmaf(w, bf16_to_f32(uint16_t(q[i] & 0xffffu)), acc[2 * i]);
-        acc[2 * i + 1] = fmaf(w, bf16_to_f32(uint16_t(q[i] >> 16)), acc[2 * i + 1]);
-      }
+    for (int s = lane; s < splits; s += 32) {
+      const float ms = ml[int64_t(s) * H * 2];
+      const float w = ms == -INFINITY ? 0.f : ml[int64_t(s) * H * 2 + 1] * exp2f(ms - mx);
+      wsm[hh][s] = w;
+      tot += w;
+    }
+    tot = warp_sum(tot);
+    if (lane == 0) {
+      inv_s[hh] = tot > 0.f ? 1.f / tot : 0.f;
+      if (lse) lse[int64_t(t) * H + h] = (mx + log2f(tot)) * 0.6931471805599453f;
     }
   }
-  const float inv = inv_s;
-  uint32_t o[4];
+  __syncthreads();
+  // 2. weighted sum: thread = (head, 8-dim chunk); D/8 chunks per head
+  const int per_head = D / 8;
+  for (int i = threadIdx.x; i < kCombHeads * per_head; i += blockDim.x) {
+    const int hh = i / per_head, d = (i % per_head) * 8, h = h0 + hh;
+    if (h >= H) continue;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const uint16_t* po = part_o + (int64_t(t) * splits * H + h) * D + d;
+    constexpr int kUnroll = 16;
+    for (int s0 = 0; s0 < splits; s0 += kUnroll) {
+      uint4 v[kUnroll];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-    o[i] = uint32_t(f32_to_bf16(acc[2 * i] * inv)) | (uint32_t(f32_to_bf16(acc[2 * i + 1] * inv)) << 16);
-  *reinterpret_cast<uint4*>(out + (int64_t(t) * H + h) * D + d) = make_uint4(o[0], o[1], o[2], o[3]);
+      for (int u = 0; u < kUnroll; ++u)
+        v[u] = (s0 + u < splits && wsm[hh][s0 + u] != 0.f)
+                   ? __ldcg(reinterpret_cast<const uint4*>(po + int64_t(s0 + u) * H * D))
+                   : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const float w = (s0 + u < splits) ? wsm[hh][s0 + u] : 0.f;
+        const uint32_t q[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc[2 * j] = fmaf(w, bf16_to_f32(uint16_t(q[j] & 0xffffu)), acc[2 * j]);
+          acc[2 * j + 1] = fmaf(w, bf16_to_f32(uint16_t(q[j] >> 16)), acc[2 * j + 1]);
+        }
+      }
+    }
+    const float inv = inv_s[hh];
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      o[j] = uint32_t(f32_to_bf16(acc[2 * j] * inv)) | (uint32_t(f32_to_bf16(acc[2 * j + 1] * inv)) << 16);
+    *reinterpret_cast<uint4*>(out + (int64_t(t) * H + h) * D + d) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
 }
 
 int splits_of(const v4a_attn_args* a) {
@@ -397,6 +466,19 @@ bool handled(const v4a_attn_args* a) {
   if (ctas > 16 * 152) return false;
   if (splits_of(a) > 512) return false;
   return true;
+}
+
+// 2-D bf16 tensor map [rows][D] with boxes of 64 columns x box_rows rows, 128-B swizzle.
+bool encode_rows(CUtensorMap* map, const void* base, int64_t rows, int D, int box_rows) {
+  auto encode = tc::encode_fn();
+  if (!encode) return false;
+  const cuuint64_t gdim[2] = {cuuint64_t(D), cuuint64_t(rows)};
+  const cuuint64_t gstride[1] = {cuuint64_t(D) * 2};
+  const cuuint32_t box[2] = {64, cuuint32_t(box_rows)};
+  const cuuint32_t es[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -442,33 +524,30 @@ bool attn_tc(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t str
   t.status = a->status;
   t.idesc_s = tc::make_idesc(1, 1, kRows, kKeys);
   t.idesc_pv = tc::make_idesc(1, 1, kRows, D > 256 ? 256 : D) | (1u << 16);   // B is MN-major
+  // Q as a 2-D tensor [T*H rows][D] bf16, boxes of 64 columns x 128 rows, 128-B swizzle
+  CUtensorMap qmap, omap;
+  if (!encode_rows(&qmap, a->q, int64_t(T) * H, int(D), kRows)) return false;
+  // output rows leave through a tensor map when whole boxes of H rows fit the swizzle atom
+  t.tma_out = (H % 8 == 0) && (reinterpret_cast<uintptr_t>(S == 1 ? static_cast<void*>(a->out) : ws) & 15) == 0;
+  if (t.tma_out) {
+    const void* dst = S == 1 ? static_cast<const void*>(a->out) : static_cast<const void*>(t.part_o);
+    const int64_t rows = S == 1 ? int64_t(T) * H : int64_t(T) * S * H;
+    if (!encode_rows(&omap, dst, rows, int(D), int(H))) t.tma_out = 0;
+  }
+  if (!t.tma_out) omap = qmap;   // unused
+  size_t smem = 1024 + D * kRows * 2 + D * kKeys * 2 + kRows * 128 + sizeof(ASmem);
   // At least 116 KB so that no two CTAs of a TMEM-allocating kernel ever share
   // an SM: every tcgen05 kernel in this library runs one CTA per SM.
-  // Q as a 2-D tensor [T*H rows][D] bf16, boxes of 64 columns x 128 rows, 128-B swizzle
-  CUtensorMap qmap;
-  {
-    auto encode = tc::encode_fn();
-    if (!encode) return false;
-    const cuuint64_t gdim[2] = {cuuint64_t(D), cuuint64_t(T) * H};
-    const cuuint64_t gstride[1] = {cuuint64_t(D) * 2};
-    const cuuint32_t box[2] = {64, kRows};
-    const cuuint32_t es[2] = {1, 1};
-    if (encode(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(a->q), gdim, gstride, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return false;
-  }
-  size_t smem = 1024 + D * kRows * 2 + D * kKeys * 2 + kRows * 128 + sizeof(ASmem);
   if (smem < 116 * 1024) smem = 116 * 1024;
   static std::once_flag once;
   std::call_once(once, [] {
     cudaFuncSetAttribute(attn_chunk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   });
   if (smem > 227 * 1024) return false;
-  attn_chunk_tc<<<dim3(t.splits, t.T), kThreads, smem, stream>>>(t, qmap);
+  attn_chunk_tc<<<dim3(t.splits, t.T), kThreads, smem, stream>>>(t, qmap, omap);
   if (t.splits > 1)
-    attn_combine_bf16<<<dim3(t.H, t.T), t.D / 8 < 32 ? 32 : t.D / 8, 0, stream>>>(t.H, t.D, t.splits, t.part_o,
-                                                                                t.part_ml, t.out, t.lse);
+    attn_combine_bf16<<<dim3((t.H + kCombHeads - 1) / kCombHeads, t.T), 256, 0, stream>>>(
+        t.H, t.D, t.splits, t.part_o, t.part_ml, t.out, t.lse);
   if (cudaGetLastError() != cudaSuccess) *rc = V4A_ERR_CUDA;
   return true;
 }

@@ -30,6 +30,7 @@
 //                         candidates are read from L2 once.
 
 #include <cstdio>
+#include <mutex>
 
 #include "v4a_common.cuh"
 #include "v4a_internal.h"
@@ -47,9 +48,11 @@ struct IndexWs {
   float* scores;        // [T][row]
   uint32_t* hist;       // [T][kHistBins]   top 12 key bits of every score
   uint32_t* hist2;      // [T][kHistBins]   next 12 bits of the threshold bin's scores
-  uint32_t* counters;   // [T][4]: selected, candidates, done, resolved
+  uint32_t* hist3;      // [T][256]         last 8 bits of the threshold sub-bin's scores
+  uint32_t* counters;   // [T][4]: arrivals at the cooperative select's barriers / "done" of the fallback
   uint64_t* cand;       // [T][row]: slice s keeps its takes at [lo, ..) and its candidates at [.., hi)
   uint32_t* info;       // [T][slices]: takes | candidates << 16 of each slice
+  uint2* gteq;          // [T][slices]: entries above / equal to the exact threshold key, per slice
   int64_t row;
   size_t zero_bytes;    // bytes of hist + counters (cleared per call)
   size_t total;
@@ -66,12 +69,14 @@ static IndexWs ws_layout(const v4a_index_args* a, void* base) {
   auto take = [&](size_t bytes) { char* r = p ? p + off : nullptr; off += round_up(bytes, 256); return r; };
   w.hist = reinterpret_cast<uint32_t*>(take(size_t(T) * kHistBins * 4));
   w.hist2 = reinterpret_cast<uint32_t*>(take(size_t(T) * kHistBins * 4));
+  w.hist3 = reinterpret_cast<uint32_t*>(take(size_t(T) * 256 * 4));
   w.counters = reinterpret_cast<uint32_t*>(take(size_t(T) * 4 * 4));
   w.zero_bytes = off;
   w.scores = reinterpret_cast<float*>(take(size_t(T) * w.row * 4));
   if (w.row > kSmemTopkMax) {
     w.cand = reinterpret_cast<uint64_t*>(take(size_t(T) * w.row * 8));
     w.info = reinterpret_cast<uint32_t*>(take(size_t(T) * ((w.row + kSlice - 1) / kSlice) * 4));
+    w.gteq = reinterpret_cast<uint2*>(take(size_t(T) * ((w.row + kSlice - 1) / kSlice) * 8));
   }
   w.total = off;
   return w;
@@ -556,17 +561,240 @@ __global__ void __launch_bounds__(1024, 1) topk_select(const float* scores, int6
   // merge the two ascending lists (disjoint indices) into the output
   for (int j = threadIdx.x; j < above; j += blockDim.x) {
     const int32_t x = take_l[j];
-    o[j + count_below(csel_l, need, x)] = x;
+    const int d = j + count_below(csel_l, need, x);
+    if (d < k) o[d] = x;
   }
   for (int j = threadIdx.x; j < need; j += blockDim.x) {
     const int32_t y = csel_l[j];
-    o[j + count_below(take_l, above, y)] = y;
+    const int d = j + count_below(take_l, above, y);
+    if (d < k) o[d] = y;
+  }
+}
+
+// ------------------------------------------------------------------------------
+// Cooperative long-row top-k (all CTAs of the grid co-resident)
+// ------------------------------------------------------------------------------
+//
+// One CTA per 8192-score slice of a query, every slice kept in registers.
+// The exact k-th largest key K* is found with three histogram levels of the
+// order-preserving key (top 12 bits: built by the tensor-core scan; next 12
+// bits; last 8 bits), each level a global histogram filled by the query's
+// CTAs and read by all of them after a barrier of the query's CTAs.  Then
+// every CTA publishes how many of its entries lie above K* and at K*; after a
+// last barrier each CTA knows, from the prefix over the slices before it, its
+// share of the ties at K* (lowest indices first) and its output offset, and
+// writes its selected indices in ascending order.  No candidate lists, no
+// single resolving CTA.
+
+// Waits until `target` CTAs have arrived at *counter (bounded; false if it gave up).
+__device__ __forceinline__ bool slice_barrier(uint32_t* counter, uint32_t target, int32_t* status, int* give_up) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(counter, 1u);
+    const long long t0 = clock64();
+    uint32_t v = 0;
+    while (true) {
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+      if (v >= target) break;
+      if (clock64() - t0 > 2000000000LL) {
+        report(status, V4A_DEV_TIMEOUT);
+        *give_up = 1;
+        break;
+      }
+      __nanosleep(64);
+    }
+    __threadfence();
+  }
+  __syncthreads();
+  return *give_up == 0;
+}
+
+// Threshold of a 256-bin histogram (warp 0 scans; result broadcast through shared memory).
+__device__ int threshold_bin256(const uint32_t* h, uint32_t need, int* bin_s, uint32_t* above_s,
+                                uint32_t* above) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    uint32_t loc[8], s8 = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) { loc[q] = __ldcg(&h[255 - (lane * 8 + q)]); s8 += loc[q]; }
+    uint32_t incl = s8;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += x;
+    }
+    const uint32_t excl = incl - s8;
+    if (excl < need && need <= incl) {
+      uint32_t acc = excl;
+      int q = 0;
+      for (; q < 8; ++q) {
+        if (acc + loc[q] >= need) break;
+        acc += loc[q];
+      }
+      *bin_s = 255 - (lane * 8 + q);
+      *above_s = acc;
+    }
+  }
+  __syncthreads();
+  *above = *above_s;
+  const int b = *bin_s;
+  __syncthreads();
+  return b;
+}
+
+__global__ void __launch_bounds__(1024, 1) topk_coop(const float* scores, int64_t row, int max_entries,
+                                                 const int32_t* positions, int k, int slices,
+                                                 const uint32_t* hist1, uint32_t* hist2, uint32_t* hist3,
+                                                 uint32_t* counters, uint2* gteq, int32_t* out, int32_t* status) {
+  __shared__ uint32_t scan[40];
+  __shared__ uint32_t h_s[kHistBins];
+  __shared__ int bin_s, give_up;
+  __shared__ uint32_t above_s;
+  constexpr int kPer = kSlice / 1024;
+  const int t = blockIdx.y, sl = blockIdx.x;
+  const int n = min((positions[t] + 1) / 4, max_entries);
+  int32_t* o = out + int64_t(t) * k;
+  if (n <= k) {                        // every CTA of this query leaves together
+    if (sl == 0) write_all_visible(o, n, k);
+    return;
+  }
+  const int nsl = (n + kSlice - 1) / kSlice;
+  if (sl >= nsl) return;               // not one of this query's slices
+  if (threadIdx.x == 0) give_up = 0;
+  const int lo = sl * kSlice, hi = min(n, lo + kSlice);
+  const float* sc = scores + int64_t(t) * row;
+  const int i0 = lo + kPer * int(threadIdx.x);
+  uint32_t key[kPer];
+  {
+    float v[kPer];
+    if (i0 + kPer - 1 < hi) {
+#pragma unroll
+      for (int u = 0; u < kPer; u += 4) {
+        const float4 f = __ldcg(reinterpret_cast<const float4*>(sc + i0 + u));
+        v[u] = f.x; v[u + 1] = f.y; v[u + 2] = f.z; v[u + 3] = f.w;
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) v[u] = i0 + u < hi ? __ldcg(sc + i0 + u) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) key[u] = i0 + u < hi ? float_key(v[u]) : 0u;   // key 0: below every score
+  }
+  uint32_t* cnt = counters + int64_t(t) * 4;
+  // level 1: top 12 bits (histogram from the scan)
+  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h_s[i] = 0;
+  uint32_t above1;
+  const uint32_t b1 = uint32_t(threshold_bin(hist1 + int64_t(t) * kHistBins, uint32_t(k), scan, &bin_s, &above_s,
+                                             &above1));
+  // level 2: next 12 bits of the entries in bin b1
+#pragma unroll
+  for (int u = 0; u < kPer; ++u)
+    if (i0 + u < hi && (key[u] >> 20) == b1) atomicAdd(&h_s[(key[u] >> 8) & (kHistBins - 1)], 1u);
+  __syncthreads();
+  uint32_t* g2 = hist2 + int64_t(t) * kHistBins;
+  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) {
+    if (h_s[i]) atomicAdd(&g2[i], h_s[i]);
+    h_s[i] = 0;
+  }
+  if (!slice_barrier(&cnt[0], uint32_t(nsl), status, &give_up)) return;
+  const uint32_t need1 = uint32_t(k) - above1;
+  uint32_t above2;
+  const uint32_t b2 = uint32_t(threshold_bin(g2, need1, scan, &bin_s, &above_s, &above2));
+  // level 3: last 8 bits of the entries in sub-bin (b1, b2)
+  const uint32_t top24 = (b1 << 12) | b2;
+#pragma unroll
+  for (int u = 0; u < kPer; ++u)
+    if (i0 + u < hi && (key[u] >> 8) == top24) atomicAdd(&h_s[key[u] & 255u], 1u);
+  __syncthreads();
+  uint32_t* g3 = hist3 + int64_t(t) * 256;
+  for (int i = threadIdx.x; i < 256; i += blockDim.x)
+    if (h_s[i]) atomicAdd(&g3[i], h_s[i]);
+  if (!slice_barrier(&cnt[1], uint32_t(nsl), status, &give_up)) return;
+  const uint32_t need2 = need1 - above2;
+  uint32_t above3;
+  const uint32_t b3 = uint32_t(threshold_bin256(g3, need2, &bin_s, &above_s, &above3));
+  const uint32_t K = (top24 << 8) | b3;                       // exact key of the k-th largest
+  const uint32_t need = need2 - above3;                       // entries equal to K to take (>= 1)
+  // this slice's entries above K and equal to K
+  uint32_t gt = 0, eq = 0;
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const bool in = i0 + u < hi;
+    gt += in && key[u] > K;
+    eq += in && key[u] == K;
+  }
+  uint32_t tot;
+  const uint32_t eq_before = block_excl_scan(eq, scan, &tot);   // ties of this slice before this thread
+  const uint32_t eq_slice = tot;
+  const uint32_t gt_slice = block_excl_scan(gt, scan, &tot), gt_total = tot;
+  (void)gt_slice;
+  if (threadIdx.x == 0) gteq[int64_t(t) * slices + sl] = make_uint2(gt_total, eq_slice);
+  if (!slice_barrier(&cnt[2], uint32_t(nsl), status, &give_up)) return;
+  // ties taken by the slices before this one, and this slice's output offset
+  __shared__ uint32_t pre_eq_s, pre_sel_s;
+  {
+    uint32_t e = 0, sel = 0, ge = 0;
+    if (int(threadIdx.x) < sl) {
+      const uint2 x = __ldcg(&gteq[int64_t(t) * slices + threadIdx.x]);
+      ge = x.x;
+      e = x.y;
+    }
+    const uint32_t pe = block_excl_scan(e, scan, &tot);         // ties in slices before slice threadIdx.x
+    if (int(threadIdx.x) < sl) {
+      const uint32_t take = pe >= need ? 0u : min(e, need - pe);
+      sel = ge + take;
+    }
+    uint32_t sel_tot;
+    block_excl_scan(sel, scan, &sel_tot);
+    if (threadIdx.x == 0) { pre_eq_s = tot; pre_sel_s = sel_tot; }
+    __syncthreads();
+  }
+  const uint32_t pre_eq = pre_eq_s, pre_sel = pre_sel_s;
+  // ordered compaction: entry selected if key > K, or key == K and it is among
+  // the first `need` ties of the row in index order
+  uint32_t mine = 0;
+  {
+    uint32_t r = pre_eq + eq_before;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const bool in = i0 + u < hi;
+      if (in && key[u] > K) ++mine;
+      else if (in && key[u] == K) { if (r < need) ++mine; ++r; }
+    }
+  }
+  uint32_t pos = pre_sel + block_excl_scan(mine, scan, &tot);
+  {
+    uint32_t r = pre_eq + eq_before;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const bool in = i0 + u < hi;
+      bool take = false;
+      if (in && key[u] > K) take = true;
+      else if (in && key[u] == K) { take = r < need; ++r; }
+      if (take && pos < uint32_t(k)) o[pos++] = i0 + u;   // the bound holds unless the histograms were incomplete
+    }
   }
 }
 
 // ------------------------------------------------------------------------------
 // Host side
 // ------------------------------------------------------------------------------
+
+// CTAs of topk_coop that can be resident at once on this device (its grid
+// must not exceed this: its CTAs wait for one another).
+static int64_t coop_capacity() {
+  static int64_t cap = -1;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    int dev = 0, sms = 0, per = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, topk_coop, 1024, 0) != cudaSuccess) per = 0;
+    cap = int64_t(sms) * per;
+  });
+  return cap;
+}
 
 // Shapes and formats only (enough to size the workspace).
 static int validate_shape(const v4a_index_args* a) {
@@ -662,11 +890,30 @@ int index_select(const v4a_index_args* a, void* ws, size_t ws_bytes, cudaStream_
     if (!index_score_tc_supported(a))
       topk_hist<<<dim3(slices, T), 512, 0, stream>>>(w.scores, w.row, a->keys.max_blocks * 64,
                                                      a->batch.positions, a->k, slices, w.hist);
-    const size_t smem = size_t(2) * a->k * 4;
-    cudaFuncSetAttribute(topk_select, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    topk_select<<<dim3(slices, T), 1024, smem, stream>>>(w.scores, w.row, a->keys.max_blocks * 64,
-                                                         a->batch.positions, a->k, slices, w.hist,
-                                                         w.hist2, w.counters, w.cand, w.info, a->out_idx);
+    // all of a query's slices resolve together in one cooperative grid when
+    // the whole grid fits on the GPU at once; otherwise one CTA per query
+    // resolves after the others have compacted their slices
+    if (int64_t(slices) * T <= coop_capacity()) {
+      cudaLaunchConfig_t lc = {};
+      lc.gridDim = dim3(unsigned(slices), unsigned(T));
+      lc.blockDim = dim3(1024);
+      lc.stream = stream;
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeCooperative;
+      at[0].val.cooperative = 1;
+      lc.attrs = at;
+      lc.numAttrs = 1;
+      if (cudaLaunchKernelEx(&lc, topk_coop, static_cast<const float*>(w.scores), w.row, a->keys.max_blocks * 64,
+                             a->batch.positions, a->k, slices, static_cast<const uint32_t*>(w.hist), w.hist2,
+                             w.hist3, w.counters, w.gteq, a->out_idx, a->status) != cudaSuccess)
+        return V4A_ERR_CUDA;
+    } else {
+      const size_t smem = size_t(2) * a->k * 4;
+      cudaFuncSetAttribute(topk_select, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+      topk_select<<<dim3(slices, T), 1024, smem, stream>>>(w.scores, w.row, a->keys.max_blocks * 64,
+                                                           a->batch.positions, a->k, slices, w.hist,
+                                                           w.hist2, w.counters, w.cand, w.info, a->out_idx);
+    }
   }
   return cudaGetLastError() == cudaSuccess ? V4A_OK : V4A_ERR_CUDA;
 }

@@ -10,14 +10,17 @@
 // scale per head), k_i = kcode_i * s_i,b per 32- or 128-element block b.
 //
 // Tile = 128 entries (two 64-entry physical blocks) x 64 heads x 128 dims.
-//  The codes of each physical block arrive with one TMA tile copy through a
-//  3-D tensor map over the pool ({128 elements, 64 rows, block}); the copy
-//  itself writes the K-major, 128-byte-swizzled MMA operand: fp8 rows as they
-//  are, fp4 rows expanded by the copy engine to 16 codes per 16-byte
-//  container (the shared-memory form kind::f8f6f4 reads for e2m1).  The
-//  block's scale words follow with one 1-D bulk copy.  No thread touches the
-//  codes.
-//  B = the query's e4m3 codes, N = 64 heads, staged once per query;
+//  Each physical block (codes + scale words, 5120 B for fp4, 8448 B for fp8)
+//  arrives with ONE 1-D bulk copy into a raw stage.  The copy engine spends a
+//  roughly fixed time on every copy (about 0.1 us on GB300, measured), so one
+//  copy per block, issued from several warps, is what keeps HBM busy;
+//  splitting a block into a tensor copy of its codes plus a copy of its scale
+//  words halves the throughput.  The codes are then written into the K-major,
+//  128-byte-swizzled A operand (fp4: 16 codes in the first 8 bytes of each
+//  16-byte container, the layout kind::f8f6f4 reads for e2m1; fp8: the row's
+//  16-byte chunks swizzled).
+//  B = the query's e4m3 codes, N = 64 heads, staged once per query by a TMA
+//  tensor copy (which writes the swizzled operand itself);
 //  K = 128 in four MMAs of K = 32.  fp8 keys: the four MMAs accumulate into
 //      one 64-column fp32 accumulator (one scale per entry, factored out of
 //      the ReLU since scales are positive).  fp4 keys: each MMA writes its own
@@ -26,23 +29,26 @@
 // Products of e4m3 x e4m3 / e2m1 codes and their sums are exact or nearly so
 // in the fp32 accumulator; the fp32 scales are applied in the epilogue.
 //
-// Warp roles (320 threads, one CTA per SM, persistent over a contiguous range
+// Warp roles (384 threads, one CTA per SM, persistent over a contiguous range
 // of (query, tile) work items):
-//   warp 0      producer: kStages-deep ring of tiles (block ids from a
-//               shared-memory window of the block table); also stages the
-//               query codes and w_h * qs_h, double-buffered.
-//   warp 1      TMEM allocator and single-thread MMA issuer (double-buffered
+//   warp 0      TMEM allocator and single-thread MMA issuer (double-buffered
 //               TMEM accumulators).
-//   warps 2..9  two epilogue warpgroups, one per accumulator (alternate
-//               tiles): one thread per entry (TMEM lane) reads its scale
-//               words as soon as the tile lands, then its accumulators, and
-//               applies scales, ReLU and head weights with packed fp32x2 FMAs.
-//               With a histogram requested it also counts the top 12 bits of
-//               the score's order-preserving key in shared memory (flushed
-//               to the query's global histogram at every query switch), the
-//               first level of the long-row top-k.
-// A stage is refilled once its MMAs have completed (commit) and the owning
-// epilogue warpgroup has read its scale words.
+//   warps 1..3  producer-converters, tiles round-robin: each owns a private
+//               ring of raw stages and keeps that many of its tiles in flight
+//               (lanes 0 and 1 issue the two block copies of a tile in one
+//               instruction); once a tile has landed it writes the operand,
+//               hands the tile's block ids to the epilogue and reuses the
+//               stage for its next tile at once.  Warp 1 also stages each
+//               query (TMA copy of its codes, w_h * qs_h), double-buffered.
+//   warps 4..11 two epilogue warpgroups, one per accumulator (alternate
+//               tiles): one thread per entry (TMEM lane) fetches its scale
+//               words from global memory (L2, the block was just fetched)
+//               while the MMA runs, then reads its accumulators and applies
+//               scales, ReLU and head weights with packed fp32x2 FMAs.  With a
+//               histogram requested it also counts the top 12 bits of the
+//               score's order-preserving key in shared memory (flushed to the
+//               query's global histogram at every query switch), the first
+//               level of the long-row top-k.
 // Every mbarrier wait is bounded (V4A_DEV_TIMEOUT, then a clean exit).
 
 #include <mutex>
@@ -53,19 +59,20 @@
 namespace v4a {
 namespace {
 
-constexpr int kStages = 10;
-constexpr int kBoxBytes = 64 * 128;          // one physical block's codes as an MMA operand (64 rows)
-constexpr int kOpBytes = 2 * kBoxBytes;      // 128 rows x 128 smem bytes
-constexpr int kScaleBytes = 2 * 1024;        // scale words of two blocks (fp4: 64 x 16 B each)
-constexpr int kStageBytes = kOpBytes + kScaleBytes;
+constexpr int kMaxStages = 18;
+constexpr int kOpBytes = 128 * 128;          // one MMA A operand: 128 rows x 128 smem bytes
+constexpr int kOps = 3;                      // converted operand buffers
+constexpr int kRing = 8;                     // per-tile block ids handed to the epilogue
 constexpr int kQBytes = 64 * 128;            // 64 heads x 128 codes
 constexpr int kHistBins = 4096;
+constexpr int kPC = 3;                       // producer-converter warps (tiles round-robin)
+constexpr int kEpi0 = 1 + kPC;               // first epilogue warp
 constexpr int kEpiWarps = 8;                 // two epilogue warpgroups
-constexpr int kEpi0 = 2;                     // first epilogue warp
-constexpr int kThreads = 32 * kEpi0 + 32 * kEpiWarps;
+constexpr int kThreads = 32 * (kEpi0 + kEpiWarps);
+constexpr int kWin = 256;                    // block-table window of each producer-converter
 
 struct TcArgs {
-  int T, fmt, acc_cols;
+  int T, fmt, acc_cols, stages;
   const int32_t* seq_ids;
   const int32_t* positions;
   const int32_t* bt;
@@ -74,9 +81,7 @@ struct TcArgs {
   const uint8_t* pool;
   int64_t block_bytes;
   int64_t scale_off;          // byte offset of the scale words inside a block
-  uint32_t scale_bytes;       // scale bytes of one block (64 entries)
-  uint32_t box_tx;            // transaction bytes of one code box: the packed bytes read (fp4: 4096)
-  const uint8_t* q;           // [T][64][128] e4m3
+  uint32_t raw_stage;         // bytes of one raw stage = 2 * block_bytes
   const float* qs;            // [T][64]
   const float* w;             // [T][64]
   float* scores;
@@ -87,15 +92,19 @@ struct TcArgs {
 };
 
 struct Smem {
-  uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], qfull[2], qempty[2], done, hsync, hclear;
+  uint64_t full[kMaxStages], opfull[kOps], opempty[kOps], rfull[kRing], tfull[2], tempty[2], qfull[2], qempty[2],
+      done, hsync, hclear;
   uint32_t tmem_base;
   int abort_flag;
   int t0, j0, count;
-  uint32_t valid[kStages];  // bit h: block h of the stage's tile was loaded
-  int32_t btc[1024];        // producer's window of the current query's block-table row
+  int32_t sblk[kMaxStages][2];      // physical blocks of each raw stage's tile (-1: not loaded)
+  int32_t rblk[kRing][2];           // the same, per tile, for the epilogue (scale words)
+  int32_t btc[kPC][kWin];           // each producer-converter's window of the current block-table row
   uint32_t part[kThreads];
-  float wq[2][64];          // w_h * qs_h of the query in each query buffer
+  float wq[2][64];                  // w_h * qs_h of the query in each query buffer
 };
+
+constexpr size_t kFixedSmem = 1024 + size_t(kOps) * kOpBytes + 2 * kQBytes + kHistBins * 4 + sizeof(Smem);
 
 // Visible entries of query t, never beyond what its block-table row can address.
 __device__ __forceinline__ int visible_of(const TcArgs& a, int t) {
@@ -187,22 +196,39 @@ __device__ __forceinline__ bool flush_hist(uint64_t* hsync, uint64_t* hclear, ui
   return ok;
 }
 
+// Layout constants of one key format (64 heads x 128 dims; 64 entries per block).
+template <bool FP8>
+struct Fmt {
+  static constexpr int kRowBytes = FP8 ? 128 : 64;                 // codes of one entry
+  static constexpr int kScaleOff = 64 * kRowBytes;                 // scale words after the 64 rows
+  static constexpr int kScaleBytes = FP8 ? 4 : 16;                 // scale bytes of one entry
+  static constexpr int kBlockBytes = kScaleOff + 64 * kScaleBytes; // 8448 / 5120
+  static constexpr int kRawStage = 2 * kBlockBytes;
+  static constexpr int kAccCols = FP8 ? 64 : 256;                  // fp32 columns of one accumulator
+};
+
+template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
-index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap) {
+index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap qmap) {
+  using F = Fmt<FP8>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* stages = base;                                   // kStages x (operand, scale words)
-  uint8_t* qbuf = stages + kStages * kStageBytes;           // 2 x 8 KB
+  uint8_t* ops = base;                                      // kOps x 16 KB converted MMA operands
+  uint8_t* qbuf = ops + kOps * kOpBytes;                    // 2 x 8 KB
   uint32_t* hist_s = reinterpret_cast<uint32_t*>(qbuf + 2 * kQBytes);
-  Smem& s = *reinterpret_cast<Smem*>(hist_s + kHistBins);
+  uint8_t* raw = reinterpret_cast<uint8_t*>(hist_s + kHistBins);   // stages x (2 blocks as stored in the pool)
+  Smem& s = *reinterpret_cast<Smem*>(raw + size_t(a.stages) * F::kRawStage);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int L = a.stages / kPC;                             // raw stages of each producer-converter
   volatile int* abort_flag = &s.abort_flag;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      tc::mbar_init(&s.full[i], 1);
-      tc::mbar_init(&s.empty[i], 1 + 4);            // MMA commit + the owning epilogue warpgroup
+    for (int i = 0; i < a.stages; ++i) tc::mbar_init(&s.full[i], 1);
+    for (int i = 0; i < kOps; ++i) {
+      tc::mbar_init(&s.opfull[i], 1);               // producer-converter
+      tc::mbar_init(&s.opempty[i], 1);              // MMA commit
     }
+    for (int i = 0; i < kRing; ++i) tc::mbar_init(&s.rfull[i], 1);   // producer-converter
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&s.tfull[i], 1);
       tc::mbar_init(&s.tempty[i], 4);
@@ -218,133 +244,204 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap) {
   if (a.hist)
     for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) hist_s[i] = 0;
   __syncwarp();   // tcgen05.alloc is warp-collective
-  if (warp == 1) tc::tmem_alloc(&s.tmem_base, 2 * a.acc_cols);
+  if (warp == 0) tc::tmem_alloc(&s.tmem_base, 2 * F::kAccCols);
   tc::tc_fence_before();
   plan(a, s);              // contains __syncthreads
   tc::tc_fence_after();
   const uint32_t tmem = s.tmem_base;
   const int count = s.count;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) tc::prefetch_tmap(&kmap);
-    Cursor c;
-    c.init(a, s.t0, s.j0);
-    int cur_t = -1, qi = -1, stage = 0;
-    uint32_t phase = 0;
-    int issued = 0;
-    int b = 0, nblk = 0, btc_base = 0, btc_end = 0;
-    for (int it = 0; it < count; ++it) {
-      if (c.t != cur_t) {
-        cur_t = c.t;
-        ++qi;
-        const int qb = qi & 1;
-        b = a.seq_ids[cur_t];
-        nblk = (visible_of(a, cur_t) + 63) / 64;
-        btc_base = btc_end = 0;                       // refill the block-table window below
-        if (lane == 0 && (a.positions[cur_t] + 1) / 4 > a.max_blocks * 64) report(a.status, V4A_DEV_BAD_BLOCK);
-        if (lane == 0 && qi >= 2) tc::mbar_wait(&s.qempty[qb], ((qi >> 1) - 1) & 1, a.status, abort_flag);
+  if (warp >= 1 && warp <= kPC) {
+    // ------------------------------------------------------------ producer-converters
+    // Warp pc owns the tiles it = pc, pc + 3, ... and raw stages [pc*L, pc*L + L).
+    // It keeps L of its tiles in flight: after converting own tile m it reuses
+    // that stage for own tile m + L at once (nobody else reads a raw stage).
+    const int pc = warp - 1;
+    int32_t* btc = s.btc[pc];
+    if (pc == 0 && lane == 0) tc::prefetch_tmap(&qmap);
+    // issue side
+    Cursor ci;
+    ci.init(a, s.t0, s.j0);
+    int i_it = 0, i_t = -1, i_b = 0, i_nblk = 0, btc_base = 0, btc_end = 0;
+    for (int k = 0; k < pc && i_it < count; ++k, ++i_it) ci.next(a);   // first own tile
+    auto issue_next = [&](int m) -> bool {     // own tile number m -> its stage; advances ci by kPC items
+      if (i_it >= count) return false;
+      if (ci.t != i_t) {
+        i_t = ci.t;
+        i_b = a.seq_ids[i_t];
+        i_nblk = (visible_of(a, i_t) + 63) / 64;
+        btc_base = btc_end = 0;
+        if (pc == 0 && lane == 0 && (a.positions[i_t] + 1) / 4 > a.max_blocks * 64)
+          report(a.status, V4A_DEV_BAD_BLOCK);
+      }
+      // block-table entries come from a shared-memory window of the row,
+      // refilled by the whole warp with all of its loads in flight together
+      if (2 * ci.j + 1 >= btc_end && 2 * ci.j < i_nblk) {
+        btc_base = 2 * ci.j;
+        btc_end = min(i_nblk, btc_base + kWin);
+        const int n = btc_end - btc_base;
+        const int32_t* row = a.bt + int64_t(i_b) * a.max_blocks + btc_base;
         __syncwarp();
-        if (*abort_flag) break;
-        const uint4* src = reinterpret_cast<const uint4*>(a.q + int64_t(cur_t) * kQBytes);
-        uint8_t* dst = qbuf + qb * kQBytes;
-        for (int cc = lane; cc < kQBytes / 16; cc += 32) {
-          const int r = cc >> 3, ch = cc & 7;
-          *reinterpret_cast<uint4*>(dst + r * 128 + ((ch ^ (r & 7)) << 4)) = src[cc];
+        for (int i0 = 0; i0 < n; i0 += 32 * 8) {
+          int32_t v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * 32 + lane;
+            v[u] = i < n ? row[i] : 0;
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * 32 + lane;
+            if (i < n) btc[i] = v[u];
+          }
         }
-        for (int h = lane; h < 64; h += 32)
-          s.wq[qb][h] = a.w[int64_t(cur_t) * 64 + h] * a.qs[int64_t(cur_t) * 64 + h];
+        __syncwarp();
+      }
+      const int stage = pc * L + (m % L);
+      // lane h < 2 issues block h's copy; both copies leave in one instruction
+      int32_t p = -1;
+      if (lane < 2) {
+        const int lb = 2 * ci.j + lane;
+        if (lb < i_nblk) {
+          p = btc[lb - btc_base];
+          if (p < 0 || p >= a.num_blocks) { p = -1; report(a.status, V4A_DEV_BAD_BLOCK); }
+        }
+        s.sblk[stage][lane] = p;
+      }
+      const uint32_t valid = __ballot_sync(0xffffffffu, p >= 0) & 3u;
+      if (lane == 0) tc::mbar_arrive_expect_tx(&s.full[stage], uint32_t(__popc(valid)) * uint32_t(F::kBlockBytes));
+      __syncwarp();
+      if (p >= 0)
+        tc::bulk_load(raw + stage * F::kRawStage + lane * F::kBlockBytes, a.pool + int64_t(p) * F::kBlockBytes,
+                      uint32_t(F::kBlockBytes), &s.full[stage]);
+      for (int k = 0; k < kPC && i_it < count; ++k, ++i_it) ci.next(a);
+      return true;
+    };
+    int issued = 0;                            // own tiles issued so far (all copies of tile m < issued)
+    while (issued < L && issue_next(issued)) ++issued;
+    // convert side (walks every item: warp 0 of this role also stages each query)
+    Cursor cc;
+    cc.init(a, s.t0, s.j0);
+    int c_t = -1, qi = -1;
+    bool q_in_flight = false, ok = true;
+    for (int it = 0, m = 0; it < count && ok; ++it) {
+      if (cc.t != c_t) {
+        c_t = cc.t;
+        ++qi;
+        if (pc == 0) {
+          const int qb = qi & 1;
+          bool qok = true;
+          if (lane == 0 && qi >= 2) qok = tc::mbar_wait(&s.qempty[qb], ((qi >> 1) - 1) & 1, a.status, abort_flag);
+          if (!__shfl_sync(0xffffffffu, qok, 0)) break;
+          for (int h = lane; h < 64; h += 32)
+            s.wq[qb][h] = a.w[int64_t(c_t) * 64 + h] * a.qs[int64_t(c_t) * 64 + h];
+          __syncwarp();
+          if (lane == 0) {
+            tc::mbar_arrive_expect_tx(&s.qfull[qb], uint32_t(kQBytes));
+            tc::tma_load_2d(qbuf + qb * kQBytes, &qmap, 0, c_t * 64, &s.qfull[qb]);
+          }
+          q_in_flight = true;
+        }
+      }
+      if ((it % kPC) == pc) {
+        const int stage = pc * L + (m % L);
+        const int j = it % kOps;
+        bool w = tc::mbar_wait(&s.full[stage], uint32_t((m / L) & 1), a.status, abort_flag);
+        w = w && tc::mbar_wait(&s.opempty[j], ((it / kOps) & 1) ^ 1, a.status, abort_flag);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        const uint8_t* src = raw + stage * F::kRawStage;
+        uint8_t* dst = ops + j * kOpBytes;
+        if (FP8) {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint4 v[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {         // row = 64*half + 4k + lane/8, chunk = lane%8
+              const int r = half * 64 + k * 4 + (lane >> 3);
+              v[k] = *reinterpret_cast<const uint4*>(src + (r >> 6) * F::kBlockBytes + (r & 63) * 128 + (lane & 7) * 16);
+            }
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const int r = half * 64 + k * 4 + (lane >> 3), ch = lane & 7;
+              *reinterpret_cast<uint4*>(dst + r * 128 + ((ch ^ (r & 7)) << 4)) = v[k];
+            }
+          }
+        } else {
+          uint4 v[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {           // row = 8k + lane/4, 16 bytes = containers 2p, 2p+1
+            const int r = k * 8 + (lane >> 2);
+            v[k] = *reinterpret_cast<const uint4*>(src + (r >> 6) * F::kBlockBytes + (r & 63) * 64 + (lane & 3) * 16);
+          }
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int r = k * 8 + (lane >> 2), p2 = (lane & 3) * 2;
+            *reinterpret_cast<uint2*>(dst + r * 128 + ((p2 ^ (r & 7)) << 4)) = make_uint2(v[k].x, v[k].y);
+            *reinterpret_cast<uint2*>(dst + r * 128 + (((p2 + 1) ^ (r & 7)) << 4)) = make_uint2(v[k].z, v[k].w);
+          }
+        }
+        if (lane < 2) s.rblk[it % kRing][lane] = s.sblk[stage][lane];
+        // the operand writes (and the reads of the raw stage) are ordered before
+        // the tensor core's reads and before the next copy into this stage
         tc::fence_proxy_async();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&s.qfull[qb]);
-      }
-      // block-table entries of this tile come from a shared-memory window of the
-      // row, refilled with coalesced loads by the whole warp
-      if (2 * c.j + 1 >= btc_end && 2 * c.j < nblk) {
-        btc_base = 2 * c.j;
-        btc_end = min(nblk, btc_base + 1024);
-        __syncwarp();
-        for (int i = lane; i < btc_end - btc_base; i += 32)
-          s.btc[i] = a.bt[int64_t(b) * a.max_blocks + btc_base + i];
-        __syncwarp();
-      }
-      if (lane == 0) {
-        if (!tc::mbar_wait(&s.empty[stage], phase ^ 1, a.status, abort_flag)) *abort_flag = 1;
-      }
-      __syncwarp();
-      if (*abort_flag) break;
-      if (lane == 0) {
-        int32_t p[2];
-        uint32_t bytes = 0, valid = 0;
-        for (int h = 0; h < 2; ++h) {
-          const int lb = 2 * c.j + h;
-          p[h] = -1;
-          if (lb >= nblk) continue;
-          p[h] = s.btc[lb - btc_base];
-          if (p[h] < 0 || p[h] >= a.num_blocks) { p[h] = -1; report(a.status, V4A_DEV_BAD_BLOCK); continue; }
-          bytes += a.box_tx + a.scale_bytes;
-          valid |= 1u << h;
+        if (lane == 0) {
+          tc::mbar_arrive(&s.opfull[j]);
+          tc::mbar_arrive(&s.rfull[it % kRing]);
         }
-        s.valid[stage] = valid;
-        uint8_t* st = stages + stage * kStageBytes;
-        tc::mbar_arrive_expect_tx(&s.full[stage], bytes);
-        for (int h = 0; h < 2; ++h)
-          if (p[h] >= 0) {
-            tc::tma_load_3d(st + h * kBoxBytes, &kmap, 0, 0, p[h], &s.full[stage]);
-            tc::bulk_load(st + kOpBytes + h * a.scale_bytes, a.pool + int64_t(p[h]) * a.block_bytes + a.scale_off,
-                          a.scale_bytes, &s.full[stage]);
-          }
+        if (issued == m + L && issue_next(m + L)) ++issued;   // the stage just read takes own tile m + L
+        ++m;
       }
-      ++issued;
-      if (++stage == kStages) { stage = 0; phase ^= 1; }
-      c.next(a);
+      cc.next(a);
     }
-    // drain: every issued copy has landed before the CTA can exit (a stage's
-    // full barrier completes once per use, so the last phase of each of the
-    // last min(issued, kStages) stages is waited for)
+    // drain: the last fill of each of this warp's stages has landed before the
+    // CTA can exit; so has the last copy into each query buffer
     if (lane == 0) {
-      const int nd = issued < kStages ? issued : kStages;
-      for (int d = 0; d < nd; ++d) {
-        stage = (stage + kStages - 1) % kStages;
-        const int use = (issued - 1 - d) / kStages;    // how many times this stage was filled before
+      for (int m = max(0, issued - L); m < issued; ++m) {
+        const int stage = pc * L + (m % L);
         const long long t0 = clock64();
-        while (!tc::mbar_try_wait(&s.full[stage], uint32_t(use & 1)) && clock64() - t0 < 2000000000LL) {}
+        while (!tc::mbar_try_wait(&s.full[stage], uint32_t((m / L) & 1)) && clock64() - t0 < 2000000000LL) {}
       }
+      if (q_in_flight)
+        for (int q = qi; q >= 0 && q > qi - 2; --q) {
+          const long long t0 = clock64();
+          while (!tc::mbar_try_wait(&s.qfull[q & 1], uint32_t((q >> 1) & 1)) && clock64() - t0 < 2000000000LL) {}
+        }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == 0) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       Cursor c;
       c.init(a, s.t0, s.j0);
-      int cur_t = -1, qi = -1, acc = 0, stage = 0;
-      uint32_t phase = 0, aphase = 0;
-      const uint32_t q0 = tc::smem_u32(qbuf), op0 = tc::smem_u32(stages);
+      int cur_t = -1, qi = -1, acc = 0;
+      uint32_t aphase = 0;
+      const uint32_t q0 = tc::smem_u32(qbuf), op0 = tc::smem_u32(ops);
       for (int it = 0; it < count; ++it) {
+        const int j = it % kOps;
         if (c.t != cur_t) {
           if (qi >= 0) tc::mma_commit(&s.qempty[qi & 1]);
           cur_t = c.t;
           ++qi;
           if (!tc::mbar_wait(&s.qfull[qi & 1], (qi >> 1) & 1, a.status, abort_flag)) break;
         }
-        if (!tc::mbar_wait(&s.full[stage], phase, a.status, abort_flag)) break;
+        if (!tc::mbar_wait(&s.opfull[j], (it / kOps) & 1, a.status, abort_flag)) break;
         if (!tc::mbar_wait(&s.tempty[acc], aphase ^ 1, a.status, abort_flag)) break;
         tc::tc_fence_after();
-        const uint64_t adesc = tc::desc_sw128(op0 + stage * kStageBytes);
+        const uint64_t adesc = tc::desc_sw128(op0 + j * kOpBytes);
         const uint64_t bdesc = tc::desc_sw128(q0 + (qi & 1) * kQBytes);
-        const uint32_t d = tmem + acc * a.acc_cols;
+        const uint32_t d = tmem + acc * F::kAccCols;
 #pragma unroll
         for (int kb = 0; kb < 4; ++kb) {
           // advance 32 bytes of K inside the swizzled 128-byte rows
-          if (a.fmt == V4A_IX_FP8_B128)
+          if (FP8)
             tc::mma_f8f6f4(d, adesc + 2 * kb, bdesc + 2 * kb, a.idesc, kb > 0);
           else
             tc::mma_f8f6f4(d + 64 * kb, adesc + 2 * kb, bdesc + 2 * kb, a.idesc, 0);
         }
-        tc::mma_commit(&s.empty[stage]);
+        tc::mma_commit(&s.opempty[j]);
         tc::mma_commit(&s.tfull[acc]);
         if (++acc == 2) { acc = 0; aphase ^= 1; }
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
         c.next(a);
       }
       // all issued MMAs complete before TMEM is released
@@ -355,18 +452,17 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap) {
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    // Warpgroup g (warps 2+4g .. 5+4g) owns accumulator g, i.e. every other
+    // Warpgroup g (warps 4+4g .. 7+4g) owns accumulator g, i.e. every other
     // tile; both warpgroups walk every item to follow the query switches.
     const int g = (warp - kEpi0) >> 2;
     const int quarter = warp & 3;                // TMEM lanes 32*quarter .. +31
     const int row = quarter * 32 + lane;         // entry within the tile
     const int et = threadIdx.x - 32 * kEpi0;     // 0 .. 255
-    const uint32_t lane_addr = tmem + (uint32_t(quarter * 32) << 16) + g * a.acc_cols;
-    const bool fp8 = a.fmt == V4A_IX_FP8_B128;
+    const uint32_t lane_addr = tmem + (uint32_t(quarter * 32) << 16) + g * F::kAccCols;
     Cursor c;
     c.init(a, s.t0, s.j0);
-    int cur_t = -1, qi = -1, n = 0, stage = 0;
-    uint32_t phase = 0, aphase = 0, hph = 0;
+    int cur_t = -1, qi = -1, n = 0;
+    uint32_t aphase = 0, hph = 0;
     float* srow = nullptr;
     const float* wq = nullptr;
     bool aborted = false;
@@ -393,30 +489,35 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap) {
       }
       if ((it & 1) == g) {
         const int e = c.j * 128 + row;
-        // scale words and validity land with the stage's copies: read them and
-        // release the stage's scale part before the accumulator is ready
-        if (!__all_sync(0xffffffffu, tc::mbar_wait(&s.full[stage], phase, a.status, abort_flag))) {
+        // the tile's block ids come through a ring slot of their own (an
+        // operand buffer's barrier may already be two phases ahead); its
+        // scale words are read from global memory (L2: the block was just
+        // fetched) while the MMA runs.  Slot it % kRing is rewritten only for
+        // tile it + kRing, which needs MMA it + kRing - kOps, which needs this
+        // warpgroup's tile it finished: no slot is overwritten or two phases
+        // ahead before it has been read here.
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(&s.rfull[it % kRing], (it / kRing) & 1, a.status, abort_flag))) {
           aborted = true;
           break;
         }
-        const bool blk_ok = (s.valid[stage] >> (row >> 6)) & 1u;
-        const uint8_t* sp = stages + stage * kStageBytes + kOpBytes + (row >> 6) * a.scale_bytes;
-        float sc0, sc1 = 0.f, sc2 = 0.f, sc3 = 0.f;
-        if (fp8) {
-          sc0 = reinterpret_cast<const float*>(sp)[row & 63];
-        } else {
-          const float4 v4 = reinterpret_cast<const float4*>(sp)[row & 63];
-          sc0 = v4.x; sc1 = v4.y; sc2 = v4.z; sc3 = v4.w;
+        const int32_t blk = s.rblk[it % kRing][row >> 6];
+        float sc0 = 0.f, sc1 = 0.f, sc2 = 0.f, sc3 = 0.f;
+        if (blk >= 0) {
+          const uint8_t* sp = a.pool + int64_t(blk) * F::kBlockBytes + F::kScaleOff;
+          if (FP8) {
+            sc0 = __ldg(reinterpret_cast<const float*>(sp) + (row & 63));
+          } else {
+            const float4 v4 = __ldg(reinterpret_cast<const float4*>(sp) + (row & 63));
+            sc0 = v4.x; sc1 = v4.y; sc2 = v4.z; sc3 = v4.w;
+          }
         }
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&s.empty[stage]);
         if (!__all_sync(0xffffffffu, tc::mbar_wait(&s.tfull[g], aphase, a.status, abort_flag))) {
           aborted = true;
           break;
         }
         tc::tc_fence_after();
         float score;
-        if (fp8) {
+        if (FP8) {
           float v[64];
           tc::tmem_ld64(lane_addr, v);
           float2 sum = make_float2(0.f, 0.f);
@@ -427,13 +528,19 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap) {
           }
           score = (sum.x + sum.y) * sc0;
         } else {
+          // 16 heads per round (their 4 block accumulators = 64 columns); the
+          // next round's TMEM loads are in flight while this round is summed
           float2 sum = make_float2(0.f, 0.f);
           const float2 s0 = make_float2(sc0, sc0), s1 = make_float2(sc1, sc1);
           const float2 s2 = make_float2(sc2, sc2), s3 = make_float2(sc3, sc3);
+          float va[64], vb[64];
+          tc::tmem_ld4x16_nowait(lane_addr, 64, va);
+          tc::tmem_wait_ld(va);
 #pragma unroll
           for (int hg = 0; hg < 4; ++hg) {
-            float v[64];
-            tc::tmem_ld4x16(lane_addr + hg * 16, 64, v);
+            float* v = (hg & 1) ? vb : va;
+            float* nx = (hg & 1) ? va : vb;
+            if (hg < 3) tc::tmem_ld4x16_nowait(lane_addr + (hg + 1) * 16, 64, nx);
 #pragma unroll
             for (int i = 0; i < 16; i += 2) {
               float2 d = __fmul2_rn(make_float2(v[i], v[i + 1]), s0);
@@ -444,6 +551,7 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap) {
               d.y = fmaxf(d.y, 0.f);
               sum = __ffma2_rn(d, make_float2(wq[hg * 16 + i], wq[hg * 16 + i + 1]), sum);
             }
+            if (hg < 3) tc::tmem_wait_ld(nx);
           }
           score = sum.x + sum.y;
         }
@@ -451,13 +559,12 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap) {
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&s.tempty[g]);
         if (e < n) {
-          const float sv = blk_ok ? score : -INFINITY;
+          const float sv = blk >= 0 ? score : -INFINITY;
           srow[e] = sv;
           if (a.hist) atomicAdd(&hist_s[float_key(sv) >> 20], 1u);
         }
         aphase ^= 1;
       }
-      if (++stage == kStages) { stage = 0; phase ^= 1; }
       c.next(a);
     }
     // the last query's counts (a warp that gave up skips this; the others'
@@ -468,13 +575,23 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap) {
   }
   tc::tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 0) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, 2 * a.acc_cols);
+    tc::tmem_dealloc(tmem, 2 * F::kAccCols);
   }
 }
 
 // ---- host side -------------------------------------------------------------------
+
+// Raw stages that fit next to the fixed part of shared memory, a multiple of
+// the producer-converter count (each owns the same number of stages).
+int stages_for(int64_t block_bytes) {
+  // block_bytes: 5120 (fp4) or 8448 (fp8)
+  const int64_t room = int64_t(227 * 1024) - int64_t(kFixedSmem);
+  int n = int(room / (2 * block_bytes));
+  if (n > kMaxStages) n = kMaxStages;
+  return n / kPC * kPC;
+}
 
 }  // namespace
 
@@ -482,11 +599,9 @@ bool index_score_tc_supported(const v4a_index_args* a) {
   const v4a_cache& c = a->keys;
   if (c.format != V4A_IX_FP8_B128 && c.format != V4A_IX_FP4_B32) return false;
   if (a->q_format != V4A_Q_FP8_HEAD || a->num_heads != 64 || c.dim != 128) return false;
-  // the fp4 tensor map wants a 32-byte aligned pool (block sizes are multiples of 32)
-  if ((reinterpret_cast<uintptr_t>(c.pool) & 31) || (reinterpret_cast<uintptr_t>(a->q) & 15)) return false;
-  if (c.num_blocks > INT32_MAX) return false;
-  const size_t smem = 1024 + size_t(kStages) * kStageBytes + 2 * kQBytes + kHistBins * 4 + sizeof(Smem);
-  return smem <= 227 * 1024;
+  if ((reinterpret_cast<uintptr_t>(c.pool) & 15) || (reinterpret_cast<uintptr_t>(a->q) & 15)) return false;
+  if (a->batch.num_tokens > (1 << 24)) return false;   // query rows of the tensor map stay in int range
+  return stages_for(ix_block_bytes(c.format, c.dim)) >= 2 * kPC;
 }
 
 bool index_score_tc(const v4a_index_args* a, float* scores, int64_t row, uint32_t* hist, cudaStream_t stream,
@@ -507,9 +622,8 @@ bool index_score_tc(const v4a_index_args* a, float* scores, int64_t row, uint32_
   t.pool = static_cast<const uint8_t*>(c.pool);
   t.block_bytes = ix_block_bytes(c.format, c.dim);
   t.scale_off = 64 * ix_row_bytes(c.format, c.dim);
-  t.scale_bytes = uint32_t(64 * 4 * ix_scales_per_row(c.format, c.dim));
-  t.box_tx = uint32_t(64 * ix_row_bytes(c.format, c.dim));
-  t.q = static_cast<const uint8_t*>(a->q);
+  t.raw_stage = uint32_t(2 * t.block_bytes);
+  t.stages = stages_for(t.block_bytes);
   t.qs = a->q_scale;
   t.w = a->weights;
   t.scores = scores;
@@ -517,31 +631,33 @@ bool index_score_tc(const v4a_index_args* a, float* scores, int64_t row, uint32_
   t.hist = hist;
   t.status = a->status;
   t.idesc = tc::make_idesc(fp4 ? 5u : 0u, 0u, 128, 64);
-  // The pool's codes as a 3-D tensor {128 elements, 64 rows, num_blocks}; one
-  // box is one block's 64 rows, written as 128-byte swizzled K-major rows
-  // (fp4: the 16U4_ALIGN16B type pads each 16 codes to 16 bytes on the way in).
-  CUtensorMap kmap;
+  // the query codes as a 2-D tensor [T*64 rows][128 B]: one box = one query's
+  // 64 heads, written as the 128-byte swizzled K-major B operand
+  CUtensorMap qmap;
   {
     auto encode = tc::encode_fn();
     if (!encode) { *rc = V4A_ERR_CUDA; return true; }
-    const cuuint64_t gdim[3] = {128, 64, cuuint64_t(c.num_blocks)};
-    const cuuint64_t gstride[2] = {cuuint64_t(ix_row_bytes(c.format, c.dim)), cuuint64_t(t.block_bytes)};
-    const cuuint32_t box[3] = {128, 64, 1};
-    const cuuint32_t es[3] = {1, 1, 1};
-    const CUtensorMapDataType dt = fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-    if (encode(&kmap, dt, 3, const_cast<void*>(c.pool), gdim, gstride, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    const cuuint64_t gdim[2] = {128, cuuint64_t(t.T) * 64};
+    const cuuint64_t gstride[1] = {128};
+    const cuuint32_t box[2] = {128, 64};
+    const cuuint32_t es[2] = {1, 1};
+    if (encode(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(a->q), gdim, gstride, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
       *rc = V4A_ERR_CUDA;
       return true;
     }
   }
-  const size_t smem = 1024 + size_t(kStages) * kStageBytes + 2 * kQBytes + kHistBins * 4 + sizeof(Smem);
+  const size_t smem = kFixedSmem + size_t(t.stages) * t.raw_stage;
   static std::once_flag attr_once;
   std::call_once(attr_once, [] {
-    cudaFuncSetAttribute(index_scan_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaFuncSetAttribute(index_scan_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaFuncSetAttribute(index_scan_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   });
-  index_scan_tc<<<tc::sm_count(), kThreads, smem, stream>>>(t, kmap);
+  if (fp4)
+    index_scan_tc<false><<<tc::sm_count(), kThreads, smem, stream>>>(t, qmap);
+  else
+    index_scan_tc<true><<<tc::sm_count(), kThreads, smem, stream>>>(t, qmap);
   if (cudaGetLastError() != cudaSuccess) { *rc = V4A_ERR_CUDA; return true; }
   return true;
 }
