@@ -10,15 +10,15 @@
 // scale per head), k_i = kcode_i * s_i,b per 32- or 128-element block b.
 //
 // Tile = 128 entries (two 64-entry physical blocks) x 64 heads x 128 dims.
-//  Each physical block (codes + scale words, 5120 B for fp4, 8448 B for fp8)
-//  arrives with ONE 1-D bulk copy into a raw stage.  The copy engine spends a
+//  The codes of each physical block arrive with ONE TMA tensor copy through a
+//  3-D map over the pool ({128 elements, 64 rows, block}) that writes the
+//  K-major, 128-byte-swizzled A operand itself (fp4: the 16U4_ALIGN16B type
+//  expands each 16 codes to a 16-byte container, the layout kind::f8f6f4
+//  reads for e2m1; fp8: plain swizzled rows).  The copy engine spends a
 //  roughly fixed time on every copy (about 0.1 us on GB300, measured), so one
-//  copy per block, issued from several warps, is what keeps HBM busy;
-//  splitting a block into a tensor copy of its codes plus a copy of its scale
-//  words halves the throughput.  The codes are then written into the K-major,
-//  128-byte-swizzled A operand (fp4: 16 codes in the first 8 bytes of each
-//  16-byte container, the layout kind::f8f6f4 reads for e2m1; fp8: the row's
-//  16-byte chunks swizzled).
+//  copy per block, issued by two producer warps, is what keeps HBM busy; the
+//  scale words (1 KB or 256 B per block) are not copied at all: each epilogue
+//  thread loads its entry's words from global memory one tile ahead.
 //  B = the query's e4m3 codes, N = 64 heads, staged once per query by a TMA
 //  tensor copy (which writes the swizzled operand itself);
 //  K = 128 in four MMAs of K = 32.  fp8 keys: the four MMAs accumulate into
@@ -32,23 +32,20 @@
 // Warp roles (384 threads, one CTA per SM, persistent over a contiguous range
 // of (query, tile) work items):
 //   warp 0      TMEM allocator and single-thread MMA issuer (double-buffered
-//               TMEM accumulators).
-//   warps 1..3  producer-converters, tiles round-robin: each owns a private
-//               ring of raw stages and keeps that many of its tiles in flight
-//               (lanes 0 and 1 issue the two block copies of a tile in one
-//               instruction); once a tile has landed it writes the operand,
-//               hands the tile's block ids to the epilogue and reuses the
-//               stage for its next tile at once.  Warp 1 also stages each
-//               query (TMA copy of its codes, w_h * qs_h), double-buffered.
+//               TMEM accumulators); a stage is released by the MMA's commit.
+//   warps 1, 2  producers, alternating tiles: lanes 0 and 1 issue the two
+//               block copies of a tile in one instruction (block ids from a
+//               shared-memory window of the block table) and hand the ids to
+//               the epilogue through a ring.
+//   warp 3      query stager: TMA copy of each query's codes, w_h * qs_h,
+//               double-buffered.
 //   warps 4..11 two epilogue warpgroups, one per accumulator (alternate
-//               tiles): one thread per entry (TMEM lane) fetches its scale
-//               words from global memory (L2, the block was just fetched)
-//               while the MMA runs, then reads its accumulators and applies
-//               scales, ReLU and head weights with packed fp32x2 FMAs.  With a
-//               histogram requested it also counts the top 12 bits of the
-//               score's order-preserving key in shared memory (flushed to the
-//               query's global histogram at every query switch), the first
-//               level of the long-row top-k.
+//               tiles): one thread per entry (TMEM lane) reads its
+//               accumulators and applies scales, ReLU and head weights with
+//               packed fp32x2 FMAs.  With a histogram requested it also counts
+//               the top 12 bits of the score's order-preserving key in shared
+//               memory (flushed to the query's global histogram at every query
+//               switch), the first level of the long-row top-k.
 // Every mbarrier wait is bounded (V4A_DEV_TIMEOUT, then a clean exit).
 
 #include <mutex>
@@ -59,17 +56,18 @@
 namespace v4a {
 namespace {
 
-constexpr int kMaxStages = 18;
-constexpr int kOpBytes = 128 * 128;          // one MMA A operand: 128 rows x 128 smem bytes
-constexpr int kOps = 3;                      // converted operand buffers
-constexpr int kRing = 8;                     // per-tile block ids handed to the epilogue
+constexpr int kMaxStages = 16;
+constexpr int kBoxBytes = 64 * 128;          // one block's codes as 64 operand rows
+constexpr int kStageBytes = 2 * kBoxBytes;   // one MMA A operand: 128 rows x 128 smem bytes
+constexpr int kRing = 32;                    // per-tile block ids handed to the epilogue
 constexpr int kQBytes = 64 * 128;            // 64 heads x 128 codes
 constexpr int kHistBins = 4096;
-constexpr int kPC = 3;                       // producer-converter warps (tiles round-robin)
-constexpr int kEpi0 = 1 + kPC;               // first epilogue warp
+constexpr int kProd = 2;                     // producer warps (alternate tiles)
+constexpr int kQw = 1 + kProd;               // query-stager warp
+constexpr int kEpi0 = kQw + 1;               // first epilogue warp
 constexpr int kEpiWarps = 8;                 // two epilogue warpgroups
 constexpr int kThreads = 32 * (kEpi0 + kEpiWarps);
-constexpr int kWin = 256;                    // block-table window of each producer-converter
+constexpr int kWin = 512;                    // block-table window of each producer
 
 struct TcArgs {
   int T, fmt, acc_cols, stages;
@@ -81,7 +79,7 @@ struct TcArgs {
   const uint8_t* pool;
   int64_t block_bytes;
   int64_t scale_off;          // byte offset of the scale words inside a block
-  uint32_t raw_stage;         // bytes of one raw stage = 2 * block_bytes
+  uint32_t box_tx;            // transaction bytes of one code box (the packed bytes read: 4096 / 8192)
   const float* qs;            // [T][64]
   const float* w;             // [T][64]
   float* scores;
@@ -92,19 +90,18 @@ struct TcArgs {
 };
 
 struct Smem {
-  uint64_t full[kMaxStages], opfull[kOps], opempty[kOps], rfull[kRing], tfull[2], tempty[2], qfull[2], qempty[2],
-      done, hsync, hclear;
+  uint64_t full[kMaxStages], empty[kMaxStages], rfull[kRing], tfull[2], tempty[2], qfull[2], qempty[2], done,
+      hsync, hclear;
   uint32_t tmem_base;
   int abort_flag;
   int t0, j0, count;
-  int32_t sblk[kMaxStages][2];      // physical blocks of each raw stage's tile (-1: not loaded)
-  int32_t rblk[kRing][2];           // the same, per tile, for the epilogue (scale words)
-  int32_t btc[kPC][kWin];           // each producer-converter's window of the current block-table row
+  int32_t rblk[kRing][2];           // physical blocks of each tile (-1: not loaded), for the scale words
+  int32_t btc[kProd][kWin];         // each producer's window of the current query's block-table row
   uint32_t part[kThreads];
   float wq[2][64];                  // w_h * qs_h of the query in each query buffer
 };
 
-constexpr size_t kFixedSmem = 1024 + size_t(kOps) * kOpBytes + 2 * kQBytes + kHistBins * 4 + sizeof(Smem);
+constexpr size_t kFixedSmem = 1024 + 2 * kQBytes + kHistBins * 4 + sizeof(Smem);
 
 // Visible entries of query t, never beyond what its block-table row can address.
 __device__ __forceinline__ int visible_of(const TcArgs& a, int t) {
@@ -203,32 +200,29 @@ struct Fmt {
   static constexpr int kScaleOff = 64 * kRowBytes;                 // scale words after the 64 rows
   static constexpr int kScaleBytes = FP8 ? 4 : 16;                 // scale bytes of one entry
   static constexpr int kBlockBytes = kScaleOff + 64 * kScaleBytes; // 8448 / 5120
-  static constexpr int kRawStage = 2 * kBlockBytes;
   static constexpr int kAccCols = FP8 ? 64 : 256;                  // fp32 columns of one accumulator
 };
 
 template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
-index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap qmap) {
+index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap) {
   using F = Fmt<FP8>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* ops = base;                                      // kOps x 16 KB converted MMA operands
-  uint8_t* qbuf = ops + kOps * kOpBytes;                    // 2 x 8 KB
+  uint8_t* stages = base;                                   // stages x 16 KB: the MMA A operands
+  uint8_t* qbuf = stages + size_t(a.stages) * kStageBytes;  // 2 x 8 KB
   uint32_t* hist_s = reinterpret_cast<uint32_t*>(qbuf + 2 * kQBytes);
-  uint8_t* raw = reinterpret_cast<uint8_t*>(hist_s + kHistBins);   // stages x (2 blocks as stored in the pool)
-  Smem& s = *reinterpret_cast<Smem*>(raw + size_t(a.stages) * F::kRawStage);
+  Smem& s = *reinterpret_cast<Smem*>(hist_s + kHistBins);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int L = a.stages / kPC;                             // raw stages of each producer-converter
+  const int S = a.stages;
   volatile int* abort_flag = &s.abort_flag;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < a.stages; ++i) tc::mbar_init(&s.full[i], 1);
-    for (int i = 0; i < kOps; ++i) {
-      tc::mbar_init(&s.opfull[i], 1);               // producer-converter
-      tc::mbar_init(&s.opempty[i], 1);              // MMA commit
+    for (int i = 0; i < S; ++i) {
+      tc::mbar_init(&s.full[i], 1);
+      tc::mbar_init(&s.empty[i], 1);                // MMA commit
     }
-    for (int i = 0; i < kRing; ++i) tc::mbar_init(&s.rfull[i], 1);   // producer-converter
+    for (int i = 0; i < kRing; ++i) tc::mbar_init(&s.rfull[i], 1);   // producer
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&s.tfull[i], 1);
       tc::mbar_init(&s.tempty[i], 4);
@@ -251,184 +245,147 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap qmap) {
   const uint32_t tmem = s.tmem_base;
   const int count = s.count;
 
-  if (warp >= 1 && warp <= kPC) {
-    // ------------------------------------------------------------ producer-converters
-    // Warp pc owns the tiles it = pc, pc + 3, ... and raw stages [pc*L, pc*L + L).
-    // It keeps L of its tiles in flight: after converting own tile m it reuses
-    // that stage for own tile m + L at once (nobody else reads a raw stage).
-    const int pc = warp - 1;
-    int32_t* btc = s.btc[pc];
-    if (pc == 0 && lane == 0) tc::prefetch_tmap(&qmap);
-    // issue side
-    Cursor ci;
-    ci.init(a, s.t0, s.j0);
-    int i_it = 0, i_t = -1, i_b = 0, i_nblk = 0, btc_base = 0, btc_end = 0;
-    for (int k = 0; k < pc && i_it < count; ++k, ++i_it) ci.next(a);   // first own tile
-    auto issue_next = [&](int m) -> bool {     // own tile number m -> its stage; advances ci by kPC items
-      if (i_it >= count) return false;
-      if (ci.t != i_t) {
-        i_t = ci.t;
-        i_b = a.seq_ids[i_t];
-        i_nblk = (visible_of(a, i_t) + 63) / 64;
-        btc_base = btc_end = 0;
-        if (pc == 0 && lane == 0 && (a.positions[i_t] + 1) / 4 > a.max_blocks * 64)
+  if (warp >= 1 && warp <= kProd) {
+    // ------------------------------------------------------------ producers
+    const int pr = warp - 1;
+    int32_t* btc = s.btc[pr];
+    if (lane == 0) tc::prefetch_tmap(&kmap);
+    Cursor c;
+    c.init(a, s.t0, s.j0);
+    int cur_t = -1, stage = 0;
+    uint32_t phase = 0;
+    int last_par[kMaxStages];              // parity of this producer's last fill of each stage, -1 if none
+#pragma unroll
+    for (int i = 0; i < kMaxStages; ++i) last_par[i] = -1;
+    int b = 0, nblk = 0, btc_base = 0, btc_end = 0;
+    for (int it = 0; it < count; ++it) {
+      if (c.t != cur_t) {
+        cur_t = c.t;
+        b = a.seq_ids[cur_t];
+        nblk = (visible_of(a, cur_t) + 63) / 64;
+        btc_base = btc_end = 0;                       // refill the block-table window below
+        if (pr == 0 && lane == 0 && (a.positions[cur_t] + 1) / 4 > a.max_blocks * 64)
           report(a.status, V4A_DEV_BAD_BLOCK);
       }
-      // block-table entries come from a shared-memory window of the row,
-      // refilled by the whole warp with all of its loads in flight together
-      if (2 * ci.j + 1 >= btc_end && 2 * ci.j < i_nblk) {
-        btc_base = 2 * ci.j;
-        btc_end = min(i_nblk, btc_base + kWin);
-        const int n = btc_end - btc_base;
-        const int32_t* row = a.bt + int64_t(i_b) * a.max_blocks + btc_base;
-        __syncwarp();
-        for (int i0 = 0; i0 < n; i0 += 32 * 8) {
-          int32_t v[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int i = i0 + u * 32 + lane;
-            v[u] = i < n ? row[i] : 0;
-          }
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int i = i0 + u * 32 + lane;
-            if (i < n) btc[i] = v[u];
-          }
-        }
-        __syncwarp();
-      }
-      const int stage = pc * L + (m % L);
-      // lane h < 2 issues block h's copy; both copies leave in one instruction
-      int32_t p = -1;
-      if (lane < 2) {
-        const int lb = 2 * ci.j + lane;
-        if (lb < i_nblk) {
-          p = btc[lb - btc_base];
-          if (p < 0 || p >= a.num_blocks) { p = -1; report(a.status, V4A_DEV_BAD_BLOCK); }
-        }
-        s.sblk[stage][lane] = p;
-      }
-      const uint32_t valid = __ballot_sync(0xffffffffu, p >= 0) & 3u;
-      if (lane == 0) tc::mbar_arrive_expect_tx(&s.full[stage], uint32_t(__popc(valid)) * uint32_t(F::kBlockBytes));
-      __syncwarp();
-      if (p >= 0)
-        tc::bulk_load(raw + stage * F::kRawStage + lane * F::kBlockBytes, a.pool + int64_t(p) * F::kBlockBytes,
-                      uint32_t(F::kBlockBytes), &s.full[stage]);
-      for (int k = 0; k < kPC && i_it < count; ++k, ++i_it) ci.next(a);
-      return true;
-    };
-    int issued = 0;                            // own tiles issued so far (all copies of tile m < issued)
-    while (issued < L && issue_next(issued)) ++issued;
-    // convert side (walks every item: warp 0 of this role also stages each query)
-    Cursor cc;
-    cc.init(a, s.t0, s.j0);
-    int c_t = -1, qi = -1;
-    bool q_in_flight = false, ok = true;
-    for (int it = 0, m = 0; it < count && ok; ++it) {
-      if (cc.t != c_t) {
-        c_t = cc.t;
-        ++qi;
-        if (pc == 0) {
-          const int qb = qi & 1;
-          bool qok = true;
-          if (lane == 0 && qi >= 2) qok = tc::mbar_wait(&s.qempty[qb], ((qi >> 1) - 1) & 1, a.status, abort_flag);
-          if (!__shfl_sync(0xffffffffu, qok, 0)) break;
-          for (int h = lane; h < 64; h += 32)
-            s.wq[qb][h] = a.w[int64_t(c_t) * 64 + h] * a.qs[int64_t(c_t) * 64 + h];
+      if ((it % kProd) == pr) {
+        // block-table entries come from a shared-memory window of the row,
+        // refilled by the whole warp with all of its loads in flight together
+        if (2 * c.j + 1 >= btc_end && 2 * c.j < nblk) {
+          btc_base = 2 * c.j;
+          btc_end = min(nblk, btc_base + kWin);
+          const int n = btc_end - btc_base;
+          const int32_t* row = a.bt + int64_t(b) * a.max_blocks + btc_base;
           __syncwarp();
-          if (lane == 0) {
-            tc::mbar_arrive_expect_tx(&s.qfull[qb], uint32_t(kQBytes));
-            tc::tma_load_2d(qbuf + qb * kQBytes, &qmap, 0, c_t * 64, &s.qfull[qb]);
+          for (int i0 = 0; i0 < n; i0 += 32 * 8) {
+            int32_t v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int i = i0 + u * 32 + lane;
+              v[u] = i < n ? row[i] : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int i = i0 + u * 32 + lane;
+              if (i < n) btc[i] = v[u];
+            }
           }
-          q_in_flight = true;
+          __syncwarp();
+        }
+        bool ok = true;
+        if (lane == 0) ok = tc::mbar_wait(&s.empty[stage], phase ^ 1, a.status, abort_flag);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        // lane h < 2 issues block h's copy; both copies leave in one instruction
+        int32_t p = -1;
+        if (lane < 2) {
+          const int lb = 2 * c.j + lane;
+          if (lb < nblk) {
+            p = btc[lb - btc_base];
+            if (p < 0 || p >= a.num_blocks) { p = -1; report(a.status, V4A_DEV_BAD_BLOCK); }
+          }
+          s.rblk[it % kRing][lane] = p;
+        }
+        const uint32_t valid = __ballot_sync(0xffffffffu, p >= 0) & 3u;
+        if (lane == 0) {
+          tc::mbar_arrive_expect_tx(&s.full[stage], uint32_t(__popc(valid)) * a.box_tx);
+          last_par[stage] = int(phase);
+        }
+        __syncwarp();
+        if (p >= 0) tc::tma_load_3d(stages + stage * kStageBytes + lane * kBoxBytes, &kmap, 0, 0, p, &s.full[stage]);
+        if (lane == 0) tc::mbar_arrive(&s.rfull[it % kRing]);   // block ids for the epilogue
+        // the blocks' scale words are pulled into L2 now, so the epilogue's loads
+        // of them, a few tiles later, do not wait on HBM
+        {
+          constexpr int kLines = (64 * F::kScaleBytes) / 128;   // 128-byte lines of one block's scale words
+          const int h = lane / kLines, ln = lane % kLines;
+          const int32_t ph = __shfl_sync(0xffffffffu, p, h < 2 ? h : 0);
+          if (h < 2 && ph >= 0)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(a.pool + int64_t(ph) * F::kBlockBytes + F::kScaleOff + ln * 128));
         }
       }
-      if ((it % kPC) == pc) {
-        const int stage = pc * L + (m % L);
-        const int j = it % kOps;
-        bool w = tc::mbar_wait(&s.full[stage], uint32_t((m / L) & 1), a.status, abort_flag);
-        w = w && tc::mbar_wait(&s.opempty[j], ((it / kOps) & 1) ^ 1, a.status, abort_flag);
-        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-        const uint8_t* src = raw + stage * F::kRawStage;
-        uint8_t* dst = ops + j * kOpBytes;
-        if (FP8) {
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint4 v[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {         // row = 64*half + 4k + lane/8, chunk = lane%8
-              const int r = half * 64 + k * 4 + (lane >> 3);
-              v[k] = *reinterpret_cast<const uint4*>(src + (r >> 6) * F::kBlockBytes + (r & 63) * 128 + (lane & 7) * 16);
-            }
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              const int r = half * 64 + k * 4 + (lane >> 3), ch = lane & 7;
-              *reinterpret_cast<uint4*>(dst + r * 128 + ((ch ^ (r & 7)) << 4)) = v[k];
-            }
-          }
-        } else {
-          uint4 v[16];
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {           // row = 8k + lane/4, 16 bytes = containers 2p, 2p+1
-            const int r = k * 8 + (lane >> 2);
-            v[k] = *reinterpret_cast<const uint4*>(src + (r >> 6) * F::kBlockBytes + (r & 63) * 64 + (lane & 3) * 16);
-          }
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const int r = k * 8 + (lane >> 2), p2 = (lane & 3) * 2;
-            *reinterpret_cast<uint2*>(dst + r * 128 + ((p2 ^ (r & 7)) << 4)) = make_uint2(v[k].x, v[k].y);
-            *reinterpret_cast<uint2*>(dst + r * 128 + (((p2 + 1) ^ (r & 7)) << 4)) = make_uint2(v[k].z, v[k].w);
-          }
-        }
-        if (lane < 2) s.rblk[it % kRing][lane] = s.sblk[stage][lane];
-        // the operand writes (and the reads of the raw stage) are ordered before
-        // the tensor core's reads and before the next copy into this stage
-        tc::fence_proxy_async();
+      if (++stage == S) { stage = 0; phase ^= 1; }
+      c.next(a);
+    }
+    // drain: every copy this producer issued has landed before the CTA can
+    // exit (each stage belongs to one producer, so its last fill is the
+    // barrier's latest phase)
+    if (lane == 0) {
+      for (int i = 0; i < S; ++i) {
+        if (last_par[i] < 0) continue;
+        const long long t0 = clock64();
+        while (!tc::mbar_try_wait(&s.full[i], uint32_t(last_par[i])) && clock64() - t0 < 2000000000LL) {}
+      }
+    }
+    __syncwarp();
+  } else if (warp == kQw) {
+    // ------------------------------------------------------------ query stager
+    if (lane == 0) tc::prefetch_tmap(&qmap);
+    Cursor c;
+    c.init(a, s.t0, s.j0);
+    int cur_t = -1, qi = -1;
+    for (int it = 0; it < count; ++it) {
+      if (c.t != cur_t) {
+        cur_t = c.t;
+        ++qi;
+        const int qb = qi & 1;
+        bool ok = true;
+        if (lane == 0 && qi >= 2) ok = tc::mbar_wait(&s.qempty[qb], ((qi >> 1) - 1) & 1, a.status, abort_flag);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) { --qi; break; }
+        for (int h = lane; h < 64; h += 32)
+          s.wq[qb][h] = a.w[int64_t(cur_t) * 64 + h] * a.qs[int64_t(cur_t) * 64 + h];
         __syncwarp();
         if (lane == 0) {
-          tc::mbar_arrive(&s.opfull[j]);
-          tc::mbar_arrive(&s.rfull[it % kRing]);
+          tc::mbar_arrive_expect_tx(&s.qfull[qb], uint32_t(kQBytes));
+          tc::tma_load_2d(qbuf + qb * kQBytes, &qmap, 0, cur_t * 64, &s.qfull[qb]);
         }
-        if (issued == m + L && issue_next(m + L)) ++issued;   // the stage just read takes own tile m + L
-        ++m;
       }
-      cc.next(a);
+      c.next(a);
     }
-    // drain: the last fill of each of this warp's stages has landed before the
-    // CTA can exit; so has the last copy into each query buffer
-    if (lane == 0) {
-      for (int m = max(0, issued - L); m < issued; ++m) {
-        const int stage = pc * L + (m % L);
+    // the last copy into each query buffer has landed before the CTA can exit
+    if (lane == 0)
+      for (int q = qi; q >= 0 && q > qi - 2; --q) {
         const long long t0 = clock64();
-        while (!tc::mbar_try_wait(&s.full[stage], uint32_t((m / L) & 1)) && clock64() - t0 < 2000000000LL) {}
+        while (!tc::mbar_try_wait(&s.qfull[q & 1], uint32_t((q >> 1) & 1)) && clock64() - t0 < 2000000000LL) {}
       }
-      if (q_in_flight)
-        for (int q = qi; q >= 0 && q > qi - 2; --q) {
-          const long long t0 = clock64();
-          while (!tc::mbar_try_wait(&s.qfull[q & 1], uint32_t((q >> 1) & 1)) && clock64() - t0 < 2000000000LL) {}
-        }
-    }
     __syncwarp();
   } else if (warp == 0) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       Cursor c;
       c.init(a, s.t0, s.j0);
-      int cur_t = -1, qi = -1, acc = 0;
-      uint32_t aphase = 0;
-      const uint32_t q0 = tc::smem_u32(qbuf), op0 = tc::smem_u32(ops);
+      int cur_t = -1, qi = -1, acc = 0, stage = 0;
+      uint32_t phase = 0, aphase = 0;
+      const uint32_t q0 = tc::smem_u32(qbuf), st0 = tc::smem_u32(stages);
       for (int it = 0; it < count; ++it) {
-        const int j = it % kOps;
         if (c.t != cur_t) {
           if (qi >= 0) tc::mma_commit(&s.qempty[qi & 1]);
           cur_t = c.t;
           ++qi;
           if (!tc::mbar_wait(&s.qfull[qi & 1], (qi >> 1) & 1, a.status, abort_flag)) break;
         }
-        if (!tc::mbar_wait(&s.opfull[j], (it / kOps) & 1, a.status, abort_flag)) break;
+        if (!tc::mbar_wait(&s.full[stage], phase, a.status, abort_flag)) break;
         if (!tc::mbar_wait(&s.tempty[acc], aphase ^ 1, a.status, abort_flag)) break;
         tc::tc_fence_after();
-        const uint64_t adesc = tc::desc_sw128(op0 + j * kOpBytes);
+        const uint64_t adesc = tc::desc_sw128(st0 + stage * kStageBytes);
         const uint64_t bdesc = tc::desc_sw128(q0 + (qi & 1) * kQBytes);
         const uint32_t d = tmem + acc * F::kAccCols;
 #pragma unroll
@@ -439,9 +396,10 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap qmap) {
           else
             tc::mma_f8f6f4(d + 64 * kb, adesc + 2 * kb, bdesc + 2 * kb, a.idesc, 0);
         }
-        tc::mma_commit(&s.opempty[j]);
+        tc::mma_commit(&s.empty[stage]);
         tc::mma_commit(&s.tfull[acc]);
         if (++acc == 2) { acc = 0; aphase ^= 1; }
+        if (++stage == S) { stage = 0; phase ^= 1; }
         c.next(a);
       }
       // all issued MMAs complete before TMEM is released
@@ -466,7 +424,28 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap qmap) {
     float* srow = nullptr;
     const float* wq = nullptr;
     bool aborted = false;
-    for (int it = 0; it < count; ++it) {
+    // the scale words of this warpgroup's next tile are loaded one tile ahead
+    // (block ids from the ring slot the producer filled when it issued the tile)
+    auto load_scales = [&](int itn, float4& sc, int32_t& blk) -> bool {
+      sc = make_float4(0.f, 0.f, 0.f, 0.f);
+      blk = -1;
+      if (itn >= count) return true;
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&s.rfull[itn % kRing], (itn / kRing) & 1, a.status, abort_flag)))
+        return false;
+      blk = s.rblk[itn % kRing][row >> 6];
+      if (blk >= 0) {
+        const uint8_t* sp = a.pool + int64_t(blk) * F::kBlockBytes + F::kScaleOff;
+        if (FP8)
+          sc.x = __ldg(reinterpret_cast<const float*>(sp) + (row & 63));
+        else
+          sc = __ldg(reinterpret_cast<const float4*>(sp) + (row & 63));
+      }
+      return true;
+    };
+    float4 nsc;
+    int32_t nblk_id;
+    if (!load_scales(g, nsc, nblk_id)) aborted = true;
+    for (int it = 0; it < count && !aborted; ++it) {
       if (c.t != cur_t) {
         if (cur_t >= 0) {
           __syncwarp();
@@ -489,28 +468,9 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap qmap) {
       }
       if ((it & 1) == g) {
         const int e = c.j * 128 + row;
-        // the tile's block ids come through a ring slot of their own (an
-        // operand buffer's barrier may already be two phases ahead); its
-        // scale words are read from global memory (L2: the block was just
-        // fetched) while the MMA runs.  Slot it % kRing is rewritten only for
-        // tile it + kRing, which needs MMA it + kRing - kOps, which needs this
-        // warpgroup's tile it finished: no slot is overwritten or two phases
-        // ahead before it has been read here.
-        if (!__all_sync(0xffffffffu, tc::mbar_wait(&s.rfull[it % kRing], (it / kRing) & 1, a.status, abort_flag))) {
-          aborted = true;
-          break;
-        }
-        const int32_t blk = s.rblk[it % kRing][row >> 6];
-        float sc0 = 0.f, sc1 = 0.f, sc2 = 0.f, sc3 = 0.f;
-        if (blk >= 0) {
-          const uint8_t* sp = a.pool + int64_t(blk) * F::kBlockBytes + F::kScaleOff;
-          if (FP8) {
-            sc0 = __ldg(reinterpret_cast<const float*>(sp) + (row & 63));
-          } else {
-            const float4 v4 = __ldg(reinterpret_cast<const float4*>(sp) + (row & 63));
-            sc0 = v4.x; sc1 = v4.y; sc2 = v4.z; sc3 = v4.w;
-          }
-        }
+        const float4 scv = nsc;
+        const int32_t blk = nblk_id;
+        if (!load_scales(it + 2, nsc, nblk_id)) { aborted = true; break; }
         if (!__all_sync(0xffffffffu, tc::mbar_wait(&s.tfull[g], aphase, a.status, abort_flag))) {
           aborted = true;
           break;
@@ -520,19 +480,22 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap qmap) {
         if (FP8) {
           float v[64];
           tc::tmem_ld64(lane_addr, v);
-          float2 sum = make_float2(0.f, 0.f);
+          float2 sum = make_float2(0.f, 0.f), sum2 = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int h = 0; h < 64; h += 2) {
+          for (int h = 0; h < 64; h += 4) {
             const float2 r = make_float2(fmaxf(v[h], 0.f), fmaxf(v[h + 1], 0.f));
+            const float2 r2 = make_float2(fmaxf(v[h + 2], 0.f), fmaxf(v[h + 3], 0.f));
             sum = __ffma2_rn(r, make_float2(wq[h], wq[h + 1]), sum);
+            sum2 = __ffma2_rn(r2, make_float2(wq[h + 2], wq[h + 3]), sum2);
           }
-          score = (sum.x + sum.y) * sc0;
+          score = ((sum.x + sum2.x) + (sum.y + sum2.y)) * scv.x;
         } else {
           // 16 heads per round (their 4 block accumulators = 64 columns); the
-          // next round's TMEM loads are in flight while this round is summed
-          float2 sum = make_float2(0.f, 0.f);
-          const float2 s0 = make_float2(sc0, sc0), s1 = make_float2(sc1, sc1);
-          const float2 s2 = make_float2(sc2, sc2), s3 = make_float2(sc3, sc3);
+          // next round's TMEM loads are in flight while this round is summed.
+          // Two independent partial sums keep the FMA chains short.
+          float2 sum = make_float2(0.f, 0.f), sum2 = make_float2(0.f, 0.f);
+          const float2 s0 = make_float2(scv.x, scv.x), s1 = make_float2(scv.y, scv.y);
+          const float2 s2 = make_float2(scv.z, scv.z), s3 = make_float2(scv.w, scv.w);
           float va[64], vb[64];
           tc::tmem_ld4x16_nowait(lane_addr, 64, va);
           tc::tmem_wait_ld(va);
@@ -549,11 +512,14 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap qmap) {
               d = __ffma2_rn(make_float2(v[48 + i], v[49 + i]), s3, d);
               d.x = fmaxf(d.x, 0.f);
               d.y = fmaxf(d.y, 0.f);
-              sum = __ffma2_rn(d, make_float2(wq[hg * 16 + i], wq[hg * 16 + i + 1]), sum);
+              if ((i & 2) == 0)
+                sum = __ffma2_rn(d, make_float2(wq[hg * 16 + i], wq[hg * 16 + i + 1]), sum);
+              else
+                sum2 = __ffma2_rn(d, make_float2(wq[hg * 16 + i], wq[hg * 16 + i + 1]), sum2);
             }
             if (hg < 3) tc::tmem_wait_ld(nx);
           }
-          score = sum.x + sum.y;
+          score = (sum.x + sum2.x) + (sum.y + sum2.y);
         }
         tc::tc_fence_before();
         __syncwarp();
@@ -583,14 +549,13 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap qmap) {
 
 // ---- host side -------------------------------------------------------------------
 
-// Raw stages that fit next to the fixed part of shared memory, a multiple of
-// the producer-converter count (each owns the same number of stages).
-int stages_for(int64_t block_bytes) {
-  // block_bytes: 5120 (fp4) or 8448 (fp8)
+// Operand stages that fit next to the fixed part of shared memory, an even
+// number so that each stage always belongs to the same producer.
+int stages_count() {
   const int64_t room = int64_t(227 * 1024) - int64_t(kFixedSmem);
-  int n = int(room / (2 * block_bytes));
+  int n = int(room / kStageBytes);
   if (n > kMaxStages) n = kMaxStages;
-  return n / kPC * kPC;
+  return n & ~1;
 }
 
 }  // namespace
@@ -599,9 +564,11 @@ bool index_score_tc_supported(const v4a_index_args* a) {
   const v4a_cache& c = a->keys;
   if (c.format != V4A_IX_FP8_B128 && c.format != V4A_IX_FP4_B32) return false;
   if (a->q_format != V4A_Q_FP8_HEAD || a->num_heads != 64 || c.dim != 128) return false;
-  if ((reinterpret_cast<uintptr_t>(c.pool) & 15) || (reinterpret_cast<uintptr_t>(a->q) & 15)) return false;
+  // the fp4 tensor map wants a 32-byte aligned pool (block sizes are multiples of 32)
+  if ((reinterpret_cast<uintptr_t>(c.pool) & 31) || (reinterpret_cast<uintptr_t>(a->q) & 15)) return false;
+  if (c.num_blocks > INT32_MAX) return false;
   if (a->batch.num_tokens > (1 << 24)) return false;   // query rows of the tensor map stay in int range
-  return stages_for(ix_block_bytes(c.format, c.dim)) >= 2 * kPC;
+  return stages_count() >= 4;
 }
 
 bool index_score_tc(const v4a_index_args* a, float* scores, int64_t row, uint32_t* hist, cudaStream_t stream,
@@ -622,8 +589,8 @@ bool index_score_tc(const v4a_index_args* a, float* scores, int64_t row, uint32_
   t.pool = static_cast<const uint8_t*>(c.pool);
   t.block_bytes = ix_block_bytes(c.format, c.dim);
   t.scale_off = 64 * ix_row_bytes(c.format, c.dim);
-  t.raw_stage = uint32_t(2 * t.block_bytes);
-  t.stages = stages_for(t.block_bytes);
+  t.box_tx = uint32_t(64 * ix_row_bytes(c.format, c.dim));
+  t.stages = stages_count();
   t.qs = a->q_scale;
   t.w = a->weights;
   t.scores = scores;
@@ -631,12 +598,29 @@ bool index_score_tc(const v4a_index_args* a, float* scores, int64_t row, uint32_
   t.hist = hist;
   t.status = a->status;
   t.idesc = tc::make_idesc(fp4 ? 5u : 0u, 0u, 128, 64);
+  auto encode = tc::encode_fn();
+  if (!encode) { *rc = V4A_ERR_CUDA; return true; }
+  // The pool's codes as a 3-D tensor {128 elements, 64 rows, num_blocks}; one
+  // box is one block's 64 rows, written as 128-byte swizzled K-major rows
+  // (fp4: the 16U4_ALIGN16B type pads each 16 codes to 16 bytes on the way in).
+  CUtensorMap kmap;
+  {
+    const cuuint64_t gdim[3] = {128, 64, cuuint64_t(c.num_blocks)};
+    const cuuint64_t gstride[2] = {cuuint64_t(ix_row_bytes(c.format, c.dim)), cuuint64_t(t.block_bytes)};
+    const cuuint32_t box[3] = {128, 64, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    const CUtensorMapDataType dt = fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    if (encode(&kmap, dt, 3, const_cast<void*>(c.pool), gdim, gstride, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+      *rc = V4A_ERR_CUDA;
+      return true;
+    }
+  }
   // the query codes as a 2-D tensor [T*64 rows][128 B]: one box = one query's
   // 64 heads, written as the 128-byte swizzled K-major B operand
   CUtensorMap qmap;
   {
-    auto encode = tc::encode_fn();
-    if (!encode) { *rc = V4A_ERR_CUDA; return true; }
     const cuuint64_t gdim[2] = {128, cuuint64_t(t.T) * 64};
     const cuuint64_t gstride[1] = {128};
     const cuuint32_t box[2] = {128, 64};
@@ -648,16 +632,16 @@ bool index_score_tc(const v4a_index_args* a, float* scores, int64_t row, uint32_
       return true;
     }
   }
-  const size_t smem = kFixedSmem + size_t(t.stages) * t.raw_stage;
+  const size_t smem = kFixedSmem + size_t(t.stages) * kStageBytes;
   static std::once_flag attr_once;
   std::call_once(attr_once, [] {
     cudaFuncSetAttribute(index_scan_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     cudaFuncSetAttribute(index_scan_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   });
   if (fp4)
-    index_scan_tc<false><<<tc::sm_count(), kThreads, smem, stream>>>(t, qmap);
+    index_scan_tc<false><<<tc::sm_count(), kThreads, smem, stream>>>(t, kmap, qmap);
   else
-    index_scan_tc<true><<<tc::sm_count(), kThreads, smem, stream>>>(t, qmap);
+    index_scan_tc<true><<<tc::sm_count(), kThreads, smem, stream>>>(t, kmap, qmap);
   if (cudaGetLastError() != cudaSuccess) { *rc = V4A_ERR_CUDA; return true; }
   return true;
 }
