@@ -382,70 +382,84 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
 }
 
 // out = sum_s w_s * O_s with w_s = l_s 2^{m_s} / sum_s' l_s' 2^{m_s'} (m in log2 units).
-// One CTA of 256 threads per (query, group of 4 heads): thread = (head, 8-dim
-// chunk, split group); each thread keeps the loads of its splits in flight
-// together, and the split groups are summed through shared memory.
-constexpr int kCombHeads = 4;
+// One CTA per (head, query), 256 threads = 4 split groups x 64 threads; a
+// thread owns one 8-dim chunk of the row (D <= 512) and the splits
+// s = group (mod 4).  Its partial-row loads are issued first, before the
+// split weights are known, so the whole CTA waits on one L2 round trip; the
+// four groups are summed through shared memory.  Many small CTAs spread the
+// partial rows over every SM (one SM alone streams them slowly).
+constexpr int kCombGroups = 4;
+constexpr int kCombMax = 16;     // splits per group held in registers (splits <= 64)
 
-__global__ void __launch_bounds__(256) attn_combine_bf16(int H, int D, int splits, const uint16_t* part_o,
-                                                         const float* part_ml, uint16_t* out, float* lse) {
-  __shared__ float wsm[kCombHeads][512];
-  __shared__ float inv_s[kCombHeads];
-  const int t = blockIdx.y, h0 = blockIdx.x * kCombHeads;
-  // 1. weights of every split of the CTA's heads
-  for (int i = threadIdx.x; i < kCombHeads * 32; i += blockDim.x) {
-    const int hh = i >> 5, lane = i & 31, h = h0 + hh;
-    if (h >= H) continue;
+__global__ void __launch_bounds__(256, 2) attn_combine_bf16(int H, int D, int splits, const uint16_t* part_o,
+                                                            const float* part_ml, uint16_t* out, float* lse) {
+  __shared__ float wsm[kCombGroups * kCombMax];
+  __shared__ float inv_s;
+  __shared__ float4 part_s[kCombGroups - 1][64][2];
+  const int t = blockIdx.y, h = blockIdx.x;
+  const int grp = threadIdx.x >> 6, c = threadIdx.x & 63;
+  const bool active = c < D / 8;
+  // 1. this thread's partial chunks, all loads in flight together
+  const uint16_t* po = part_o + (int64_t(t) * splits * H + h) * D + c * 8;
+  uint4 v[kCombMax];
+#pragma unroll
+  for (int u = 0; u < kCombMax; ++u) {
+    const int sp = grp + u * kCombGroups;
+    v[u] = (active && sp < splits) ? __ldcg(reinterpret_cast<const uint4*>(po + int64_t(sp) * H * D))
+                                   : make_uint4(0, 0, 0, 0);
+  }
+  // 2. weights of every split (warp 0), while those loads are in flight
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
     const float* ml = part_ml + (int64_t(t) * splits * H + h) * 2;
-    float mx = -INFINITY;
-    for (int s = lane; s < splits; s += 32) mx = fmaxf(mx, ml[int64_t(s) * H * 2]);
-    mx = warp_max(mx);
-    float tot = 0.f;
-    for (int s = lane; s < splits; s += 32) {
-      const float ms = ml[int64_t(s) * H * 2];
-      const float w = ms == -INFINITY ? 0.f : ml[int64_t(s) * H * 2 + 1] * exp2f(ms - mx);
-      wsm[hh][s] = w;
-      tot += w;
-    }
-    tot = warp_sum(tot);
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    if (lane < splits) { m0 = ml[int64_t(lane) * H * 2]; l0 = ml[int64_t(lane) * H * 2 + 1]; }
+    if (lane + 32 < splits) { m1 = ml[int64_t(lane + 32) * H * 2]; l1 = ml[int64_t(lane + 32) * H * 2 + 1]; }
+    const float mx = warp_max(fmaxf(m0, m1));
+    const float w0 = m0 == -INFINITY ? 0.f : l0 * exp2f(m0 - mx);
+    const float w1 = m1 == -INFINITY ? 0.f : l1 * exp2f(m1 - mx);
+    if (lane < splits) wsm[lane] = w0;
+    if (lane + 32 < splits) wsm[lane + 32] = w1;
+    const float tot = warp_sum(w0 + w1);
     if (lane == 0) {
-      inv_s[hh] = tot > 0.f ? 1.f / tot : 0.f;
+      inv_s = tot > 0.f ? 1.f / tot : 0.f;
       if (lse) lse[int64_t(t) * H + h] = (mx + log2f(tot)) * 0.6931471805599453f;
     }
   }
   __syncthreads();
-  // 2. weighted sum: thread = (head, 8-dim chunk); D/8 chunks per head
-  const int per_head = D / 8;
-  for (int i = threadIdx.x; i < kCombHeads * per_head; i += blockDim.x) {
-    const int hh = i / per_head, d = (i % per_head) * 8, h = h0 + hh;
-    if (h >= H) continue;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    const uint16_t* po = part_o + (int64_t(t) * splits * H + h) * D + d;
-    constexpr int kUnroll = 16;
-    for (int s0 = 0; s0 < splits; s0 += kUnroll) {
-      uint4 v[kUnroll];
+  // 3. weighted sum of this thread's splits (an empty chunk has weight 0 and
+  //    its partial row is never read into the sum)
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u)
-        v[u] = (s0 + u < splits && wsm[hh][s0 + u] != 0.f)
-                   ? __ldcg(reinterpret_cast<const uint4*>(po + int64_t(s0 + u) * H * D))
-                   : make_uint4(0, 0, 0, 0);
+  for (int u = 0; u < kCombMax; ++u) {
+    const int sp = grp + u * kCombGroups;
+    const float w = sp < splits ? wsm[sp] : 0.f;
+    if (w == 0.f) continue;
+    const uint32_t q[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const float w = (s0 + u < splits) ? wsm[hh][s0 + u] : 0.f;
-        const uint32_t q[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          acc[2 * j] = fmaf(w, bf16_to_f32(uint16_t(q[j] & 0xffffu)), acc[2 * j]);
-          acc[2 * j + 1] = fmaf(w, bf16_to_f32(uint16_t(q[j] >> 16)), acc[2 * j + 1]);
-        }
-      }
+    for (int j = 0; j < 4; ++j) {
+      acc[2 * j] = fmaf(w, bf16_to_f32(uint16_t(q[j] & 0xffffu)), acc[2 * j]);
+      acc[2 * j + 1] = fmaf(w, bf16_to_f32(uint16_t(q[j] >> 16)), acc[2 * j + 1]);
     }
-    const float inv = inv_s[hh];
+  }
+  if (grp > 0) {
+    part_s[grp - 1][c][0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    part_s[grp - 1][c][1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+  __syncthreads();
+  if (grp == 0 && active) {
+#pragma unroll
+    for (int g2 = 0; g2 < kCombGroups - 1; ++g2) {
+      const float4 x = part_s[g2][c][0], y = part_s[g2][c][1];
+      acc[0] += x.x; acc[1] += x.y; acc[2] += x.z; acc[3] += x.w;
+      acc[4] += y.x; acc[5] += y.y; acc[6] += y.z; acc[7] += y.w;
+    }
+    const float inv = inv_s;
     uint32_t o[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j)
       o[j] = uint32_t(f32_to_bf16(acc[2 * j] * inv)) | (uint32_t(f32_to_bf16(acc[2 * j + 1] * inv)) << 16);
-    *reinterpret_cast<uint4*>(out + (int64_t(t) * H + h) * D + d) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4*>(out + (int64_t(t) * H + h) * D + c * 8) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -464,7 +478,7 @@ bool handled(const v4a_attn_args* a) {
   if (a->num_heads > kRows) return false;
   const int64_t ctas = int64_t(a->batch.num_tokens) * splits_of(a);
   if (ctas > 16 * 152) return false;
-  if (splits_of(a) > 512) return false;
+  if (splits_of(a) > kCombGroups * kCombMax) return false;   // the combine holds at most 64 splits
   return true;
 }
 
@@ -546,7 +560,7 @@ bool attn_tc(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t str
   if (smem > 227 * 1024) return false;
   attn_chunk_tc<<<dim3(t.splits, t.T), kThreads, smem, stream>>>(t, qmap, omap);
   if (t.splits > 1)
-    attn_combine_bf16<<<dim3((t.H + kCombHeads - 1) / kCombHeads, t.T), 256, 0, stream>>>(
+    attn_combine_bf16<<<dim3(t.H, t.T), 256, 0, stream>>>(
         t.H, t.D, t.splits, t.part_o, t.part_ml, t.out, t.lse);
   if (cudaGetLastError() != cudaSuccess) *rc = V4A_ERR_CUDA;
   return true;

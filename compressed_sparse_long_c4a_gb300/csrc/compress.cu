@@ -124,78 +124,108 @@ __device__ void store_ix_row(int format, int dim, int p, bool own, float v0, flo
   __syncthreads();
 }
 
-__device__ void compress_token(const CompressSide& c, const BatchDev& bt, int t, int b, int P,
+// Latency matters more than bandwidth here (a handful of tokens per call), so
+// every load that depends only on (token, sequence, position) is issued in
+// one round before anything waits: this token's row, its block-table entry,
+// gamma, and for each window position the gate of both possible sources (the
+// call's inputs or the ring) with the sequence id that decides between them.
+__device__ void compress_token(const CompressSide& c, const BatchDev& bt, int t, int b, int P, bool tok_ok,
                                int32_t* status) {
   __shared__ float w_s[128];
   __shared__ const uint16_t* src_s[128];
   __shared__ float red[32];
+  __shared__ int64_t blk_s;
   const int p = threadIdx.x;
   const int npairs = c.dim >> 1;
   const bool own = p < npairs;
-
-  // 1. this token's raw (x, gate) into the ring
-  const int slot_r = P % c.ring_cap;
-  const uint32_t* xin = reinterpret_cast<const uint32_t*>(c.x + int64_t(t) * c.dim);
-  uint32_t* rx = reinterpret_cast<uint32_t*>(c.ring_x + (int64_t(b) * c.ring_cap + slot_r) * c.dim);
-  if (own) rx[p] = xin[p];
-  if (p == 0) c.ring_gate[int64_t(b) * c.ring_cap + slot_r] = c.gate[t];
-
-  if ((P + 1) % c.ratio != 0) return;
+  const bool emit = (P + 1) % c.ratio == 0;
   const int i = (P + 1) / c.ratio - 1;
   const int W = c.ratio == 4 ? 8 : 128;
   const int p0 = c.ratio == 4 ? 4 * i - 4 : 128 * i;
 
-  // 2. window logits and source rows
+  // ---- round 1: independent loads ----
+  const uint32_t* xin = reinterpret_cast<const uint32_t*>(c.x + int64_t(t) * c.dim);
+  const uint32_t xv = own ? xin[p] : 0u;
+  const float gt = p == 0 ? c.gate[t] : 0.f;
+  float gm0 = 0.f, gm1 = 0.f;
+  if (emit && own) { gm0 = c.gamma[2 * p]; gm1 = c.gamma[2 * p + 1]; }
+  if (emit && p == blockDim.x - 1) {
+    v4a_cache cc;
+    cc.ratio = c.ratio; cc.block_table = c.bt; cc.max_blocks = c.max_blocks;
+    cc.num_blocks = c.num_blocks;
+    blk_s = block_of(cc, b, i, status);
+  }
   float logit = -INFINITY;
-  for (int j = p; j < W; j += blockDim.x) {
-    const int pos = p0 + j;
+  if (emit && p < W) {
+    const int j = p, pos = p0 + j;
     const uint16_t* row = nullptr;
-    float g = 0.f;
     if (pos >= 0) {
       const int d = P - pos;                 // 0 .. W-1
-      if (t - d >= 0 && bt.seq_ids[t - d] == b) {
-        row = c.x + int64_t(t - d) * c.dim;
-        g = c.gate[t - d];
-      } else {
-        const int64_t rs = int64_t(b) * c.ring_cap + pos % c.ring_cap;
-        row = c.ring_x + rs * c.dim;
-        g = c.ring_gate[rs];
-      }
-      logit = fmaxf(logit, g + c.bias[j]);
+      const int64_t rs = int64_t(b) * c.ring_cap + pos % c.ring_cap;
+      const bool in_call_ok = t - d >= 0;
+      const int sid = in_call_ok ? bt.seq_ids[t - d] : -1;
+      const float g_call = in_call_ok ? c.gate[t - d] : 0.f;
+      const float g_ring = c.ring_gate[rs];
+      const float bias = c.bias[j];
+      const bool in_call = in_call_ok && sid == b;
+      row = in_call ? c.x + int64_t(t - d) * c.dim : c.ring_x + rs * c.dim;
+      logit = (in_call ? g_call : g_ring) + bias;
     }
-    w_s[j] = pos >= 0 ? g + c.bias[j] : -INFINITY;
     src_s[j] = row;
   }
-  const float mx = block_reduce<true>(logit, red);
-  float e = 0.f;
-  for (int j = p; j < W; j += blockDim.x) {
-    const float v = src_s[j] ? expf(w_s[j] - mx) : 0.f;
-    w_s[j] = v;
-    e += v;
-  }
-  const float sum = block_reduce<false>(e, red);   // also orders the w_s writes
-  const float inv = 1.f / sum;
+  if (!tok_ok) return;                       // uniform: the whole CTA leaves before writing
 
-  // 3. weighted sum of the window rows (pair per thread)
+  // this token's raw (x, gate) into the ring (no window position read below is
+  // this slot: ring capacity >= window - 1 + tokens per sequence)
+  const int slot_r = P % c.ring_cap;
+  uint32_t* rx = reinterpret_cast<uint32_t*>(c.ring_x + (int64_t(b) * c.ring_cap + slot_r) * c.dim);
+  if (own) rx[p] = xv;
+  if (p == 0) c.ring_gate[int64_t(b) * c.ring_cap + slot_r] = gt;
+  if (!emit) return;
+
+  // ---- window weights: softmax over the valid positions ----
+  if (W <= 32) {
+    if (p < 32) {                             // one warp
+      const float mx = warp_max(logit);
+      const float e = (p < W && logit > -INFINITY) ? expf(logit - mx) : 0.f;
+      const float sum = warp_sum(e);
+      if (p < W) w_s[p] = e / sum;
+    }
+    __syncthreads();
+  } else {
+    const float mx = block_reduce<true>(logit, red);
+    const float e = (p < W && logit > -INFINITY) ? expf(logit - mx) : 0.f;
+    const float sum = block_reduce<false>(e, red);
+    if (p < W) w_s[p] = e / sum;
+    __syncthreads();
+  }
+
+  // ---- round 2: weighted sum of the window rows (pair per thread) ----
   float a0 = 0.f, a1 = 0.f;
   if (own) {
-    for (int j = 0; j < W; ++j) {
-      const uint16_t* row = src_s[j];
-      if (!row) continue;
-      const uint32_t v = reinterpret_cast<const uint32_t*>(row)[p];
-      const float wj = w_s[j] * inv;
-      a0 = fmaf(wj, bf16_to_f32(uint16_t(v & 0xffffu)), a0);
-      a1 = fmaf(wj, bf16_to_f32(uint16_t(v >> 16)), a1);
+    for (int j0 = 0; j0 < W; j0 += 8) {
+      uint32_t v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint16_t* row = src_s[j0 + u];
+        v[u] = row ? reinterpret_cast<const uint32_t*>(row)[p] : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float wj = w_s[j0 + u];
+        a0 = fmaf(wj, bf16_to_f32(uint16_t(v[u] & 0xffffu)), a0);
+        a1 = fmaf(wj, bf16_to_f32(uint16_t(v[u] >> 16)), a1);
+      }
     }
   }
-  // 4. RMSNorm
+  // ---- RMSNorm ----
   const float ss = block_reduce<false>(own ? a0 * a0 + a1 * a1 : 0.f, red);
   const float r = 1.f / sqrtf(ss / float(c.dim) + c.eps);
   float v0 = 0.f, v1 = 0.f;
   if (own) {
-    v0 = a0 * r * c.gamma[2 * p];
-    v1 = a1 * r * c.gamma[2 * p + 1];
-    // 5. RoPE at the anchor (= this token's position)
+    v0 = a0 * r * gm0;
+    v1 = a1 * r * gm1;
+    // RoPE at the anchor (= this token's position)
     const int first = c.dim - c.rope_dims;
     if (2 * p >= first) {
       float cs, sn;
@@ -205,17 +235,9 @@ __device__ void compress_token(const CompressSide& c, const BatchDev& bt, int t,
       v1 = x0 * sn + x1 * cs;
     }
   }
-  // 6. encode + insert at (block_table[b][i / E], i % E)
+  // ---- encode + insert at (block_table[b][i / E], i % E) ----
   const int E = entries_per_block(c.ratio);
-  __shared__ int64_t blk_s;
-  if (p == 0) {
-    v4a_cache cc;
-    cc.ratio = c.ratio; cc.block_table = c.bt; cc.max_blocks = c.max_blocks;
-    cc.num_blocks = c.num_blocks;
-    blk_s = block_of(cc, b, i, status);
-  }
-  __syncthreads();
-  const int64_t blk = blk_s;
+  const int64_t blk = blk_s;                 // written before the reductions' barriers
   if (blk < 0) return;   // uniform across the CTA
   uint8_t* base = c.pool + blk * c.block_bytes;
   const int slot = i % E;
@@ -261,13 +283,18 @@ __global__ void compress_insert_kernel(BatchDev bt, CompressSide mainc, Compress
   const int role = blockIdx.y;
   const int b = bt.seq_ids[t];
   const int P = bt.positions[t];
-  if (!token_ok(bt, t, b, P)) {
+  // a sequence id out of range or a negative position stops the CTA before any
+  // address is formed from them; the run checks (consecutive positions, run
+  // length) load while the compressor issues its own loads
+  if (b < 0 || b >= bt.B || P < 0) {
     if (threadIdx.x == 0 && role == 0) report(status, V4A_DEV_BAD_BATCH);
     return;
   }
-  if (role == 0 && mainc.active) compress_token(mainc, bt, t, b, P, status);
-  if (role == 1 && ixc.active) compress_token(ixc, bt, t, b, P, status);
-  if (role == 2 && win.active) window_token(win, t, b, P);
+  const bool ok = token_ok(bt, t, b, P);
+  if (!ok && threadIdx.x == 0 && role == 0) report(status, V4A_DEV_BAD_BATCH);
+  if (role == 0 && mainc.active) compress_token(mainc, bt, t, b, P, ok, status);
+  if (role == 1 && ixc.active) compress_token(ixc, bt, t, b, P, ok, status);
+  if (role == 2 && win.active && ok) window_token(win, t, b, P);
 }
 
 static int fill_side(const v4a_compressor* c, bool indexer, CompressSide* s, int max_new) {
@@ -336,7 +363,9 @@ int compress_insert(const v4a_compress_args* a, cudaStream_t stream) {
   if (mc.active) maxdim = max(maxdim, mc.dim);
   if (ic.active) maxdim = max(maxdim, ic.dim);
   if (ws.active) maxdim = max(maxdim, ws.dim);
-  const int threads = ((maxdim / 2) + 31) / 32 * 32;
+  int threads = ((maxdim / 2) + 31) / 32 * 32;
+  // one thread per window position as well (128 for c128a compressors)
+  if ((mc.active && mc.ratio == 128) || (ic.active && ic.ratio == 128)) threads = max(threads, 128);
   BatchDev bd{B.num_tokens, B.num_seqs, B.max_new_per_seq, B.seq_ids, B.positions};
   dim3 grid(B.num_tokens, 3);
   compress_insert_kernel<<<grid, max(threads, 64), 0, stream>>>(bd, mc, ic, ws, a->status);
