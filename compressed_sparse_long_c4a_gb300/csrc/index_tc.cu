@@ -17,8 +17,10 @@
 //  reads for e2m1; fp8: plain swizzled rows).  The copy engine spends a
 //  roughly fixed time on every copy (about 0.1 us on GB300, measured), so one
 //  copy per block, issued by two producer warps, is what keeps HBM busy; the
-//  scale words (1 KB or 256 B per block) are not copied at all: each epilogue
-//  thread loads its entry's words from global memory one tile ahead.
+//  scale words (1 KB or 256 B per block) travel on the load/store path
+//  instead: every lane of the issuing producer warp puts 16-byte cp.async
+//  copies of them into the tile's slot of a shared-memory ring, whose
+//  barrier completes when they have landed.
 //  B = the query's e4m3 codes, N = 64 heads, staged once per query by a TMA
 //  tensor copy (which writes the swizzled operand itself);
 //  K = 128 in four MMAs of K = 32.  fp8 keys: the four MMAs accumulate into
@@ -42,10 +44,13 @@
 //   warps 4..11 two epilogue warpgroups, one per accumulator (alternate
 //               tiles): one thread per entry (TMEM lane) reads its
 //               accumulators and applies scales, ReLU and head weights with
-//               packed fp32x2 FMAs.  With a histogram requested it also counts
-//               the top 12 bits of the score's order-preserving key in shared
-//               memory (flushed to the query's global histogram at every query
-//               switch), the first level of the long-row top-k.
+//               packed fp32x2 FMAs, releasing the accumulator as soon as its
+//               last TMEM load has landed.  With a histogram requested it also
+//               counts the top 12 bits of the score's order-preserving key in
+//               shared memory (flushed to the query's global histogram at
+//               every query switch), the first level of the long-row top-k.
+//               Lane 0 of each warp does the warp's barrier waits: a wait by
+//               all 32 lanes of a warp costs several times more.
 // Every mbarrier wait is bounded (V4A_DEV_TIMEOUT, then a clean exit).
 
 #include <mutex>
@@ -68,6 +73,8 @@ constexpr int kEpi0 = kQw + 1;               // first epilogue warp
 constexpr int kEpiWarps = 8;                 // two epilogue warpgroups
 constexpr int kThreads = 32 * (kEpi0 + kEpiWarps);
 constexpr int kWin = 512;                    // block-table window of each producer
+constexpr int kScRing = 12;                  // tiles of scale words staged in shared memory
+constexpr int kScSlot = 128 * 16;            // one tile's scale words (fp4: 16 B per entry; fp8: 4 B)
 
 struct TcArgs {
   int T, fmt, acc_cols, stages;
@@ -90,7 +97,7 @@ struct TcArgs {
 };
 
 struct Smem {
-  uint64_t full[kMaxStages], empty[kMaxStages], rfull[kRing], tfull[2], tempty[2], qfull[2], qempty[2], done,
+  uint64_t full[kMaxStages], empty[kMaxStages], rfull[kRing], tfull[2], tempty[2], qfull[2], qempty[2], sfull[kScRing], done,
       hsync, hclear;
   uint32_t tmem_base;
   int abort_flag;
@@ -101,7 +108,7 @@ struct Smem {
   float wq[2][64];                  // w_h * qs_h of the query in each query buffer
 };
 
-constexpr size_t kFixedSmem = 1024 + 2 * kQBytes + kHistBins * 4 + sizeof(Smem);
+constexpr size_t kFixedSmem = 1024 + 2 * kQBytes + kScRing * kScSlot + kHistBins * 4 + sizeof(Smem);
 
 // Visible entries of query t, never beyond what its block-table row can address.
 __device__ __forceinline__ int visible_of(const TcArgs& a, int t) {
@@ -166,6 +173,16 @@ __device__ void plan(const TcArgs& a, Smem& s) {
   __syncthreads();
 }
 
+// Lane 0 waits for the phase (bounded) and the warp proceeds together; the
+// warp barrier orders the other lanes' reads after lane 0's observation.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int32_t* status, volatile int* abort_flag) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = tc::mbar_wait(bar, parity, status, abort_flag);
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok;
+}
+
 // Adds the shared-memory histogram of query t to its global row and clears it.
 // Called by all eight epilogue warps at the same item; they meet on two
 // mbarriers (bounded waits, so a warp that gave up elsewhere cannot hang the
@@ -211,7 +228,8 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const __
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = base;                                   // stages x 16 KB: the MMA A operands
   uint8_t* qbuf = stages + size_t(a.stages) * kStageBytes;  // 2 x 8 KB
-  uint32_t* hist_s = reinterpret_cast<uint32_t*>(qbuf + 2 * kQBytes);
+  uint8_t* scale_s = qbuf + 2 * kQBytes;                    // kScRing x 2 KB: scale words of each tile
+  uint32_t* hist_s = reinterpret_cast<uint32_t*>(scale_s + kScRing * kScSlot);
   Smem& s = *reinterpret_cast<Smem*>(hist_s + kHistBins);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = a.stages;
@@ -225,10 +243,11 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const __
     for (int i = 0; i < kRing; ++i) tc::mbar_init(&s.rfull[i], 1);   // producer
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&s.tfull[i], 1);
-      tc::mbar_init(&s.tempty[i], 4);
+      tc::mbar_init(&s.tempty[i], 4);   // the owning warpgroup's warps
       tc::mbar_init(&s.qfull[i], 1);
       tc::mbar_init(&s.qempty[i], 1 + kEpiWarps);   // MMA commit + every epilogue warp
     }
+    for (int i = 0; i < kScRing; ++i) tc::mbar_init(&s.sfull[i], 32);   // every lane of the issuing producer
     tc::mbar_init(&s.done, 1);
     tc::mbar_init(&s.hsync, kEpiWarps);
     tc::mbar_init(&s.hclear, kEpiWarps);
@@ -312,14 +331,22 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const __
         __syncwarp();
         if (p >= 0) tc::tma_load_3d(stages + stage * kStageBytes + lane * kBoxBytes, &kmap, 0, 0, p, &s.full[stage]);
         if (lane == 0) tc::mbar_arrive(&s.rfull[it % kRing]);   // block ids for the epilogue
-        // the blocks' scale words are pulled into L2 now, so the epilogue's loads
-        // of them, a few tiles later, do not wait on HBM
+        // the blocks' scale words go to the tile's slot of the scale ring by
+        // 16-byte asynchronous copies from every lane; the slot's barrier
+        // completes when all of them have landed
         {
-          constexpr int kLines = (64 * F::kScaleBytes) / 128;   // 128-byte lines of one block's scale words
-          const int h = lane / kLines, ln = lane % kLines;
-          const int32_t ph = __shfl_sync(0xffffffffu, p, h < 2 ? h : 0);
-          if (h < 2 && ph >= 0)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(a.pool + int64_t(ph) * F::kBlockBytes + F::kScaleOff + ln * 128));
+          uint8_t* slot = scale_s + (it % kScRing) * kScSlot;
+          const int32_t p0 = __shfl_sync(0xffffffffu, p, 0), p1 = __shfl_sync(0xffffffffu, p, 1);
+          constexpr int kChunks = (2 * 64 * F::kScaleBytes) / 16;   // 16-byte chunks of the tile's words
+#pragma unroll
+          for (int u = 0; u < kChunks / 32; ++u) {
+            const int ch = lane + 32 * u;
+            const int h = ch / (kChunks / 2), r = ch % (kChunks / 2);
+            const int32_t ph = h ? p1 : p0;
+            if (ph >= 0)
+              tc::cp_async16(slot + ch * 16, a.pool + int64_t(ph) * F::kBlockBytes + F::kScaleOff + r * 16);
+          }
+          tc::cp_async_arrive_noinc(&s.sfull[it % kScRing]);
         }
       }
       if (++stage == S) { stage = 0; phase ^= 1; }
@@ -328,6 +355,7 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const __
     // drain: every copy this producer issued has landed before the CTA can
     // exit (each stage belongs to one producer, so its last fill is the
     // barrier's latest phase)
+    tc::cp_async_wait_all();
     if (lane == 0) {
       for (int i = 0; i < S; ++i) {
         if (last_par[i] < 0) continue;
@@ -424,27 +452,6 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const __
     float* srow = nullptr;
     const float* wq = nullptr;
     bool aborted = false;
-    // the scale words of this warpgroup's next tile are loaded one tile ahead
-    // (block ids from the ring slot the producer filled when it issued the tile)
-    auto load_scales = [&](int itn, float4& sc, int32_t& blk) -> bool {
-      sc = make_float4(0.f, 0.f, 0.f, 0.f);
-      blk = -1;
-      if (itn >= count) return true;
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(&s.rfull[itn % kRing], (itn / kRing) & 1, a.status, abort_flag)))
-        return false;
-      blk = s.rblk[itn % kRing][row >> 6];
-      if (blk >= 0) {
-        const uint8_t* sp = a.pool + int64_t(blk) * F::kBlockBytes + F::kScaleOff;
-        if (FP8)
-          sc.x = __ldg(reinterpret_cast<const float*>(sp) + (row & 63));
-        else
-          sc = __ldg(reinterpret_cast<const float4*>(sp) + (row & 63));
-      }
-      return true;
-    };
-    float4 nsc;
-    int32_t nblk_id;
-    if (!load_scales(g, nsc, nblk_id)) aborted = true;
     for (int it = 0; it < count && !aborted; ++it) {
       if (c.t != cur_t) {
         if (cur_t >= 0) {
@@ -460,7 +467,7 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const __
         ++qi;
         n = visible_of(a, cur_t);
         srow = a.scores + int64_t(cur_t) * a.row;
-        if (!__all_sync(0xffffffffu, tc::mbar_wait(&s.qfull[qi & 1], (qi >> 1) & 1, a.status, abort_flag))) {
+        if (!warp_wait(&s.qfull[qi & 1], (qi >> 1) & 1, a.status, abort_flag)) {
           aborted = true;
           break;
         }
@@ -468,10 +475,22 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const __
       }
       if ((it & 1) == g) {
         const int e = c.j * 128 + row;
-        const float4 scv = nsc;
-        const int32_t blk = nblk_id;
-        if (!load_scales(it + 2, nsc, nblk_id)) { aborted = true; break; }
-        if (!__all_sync(0xffffffffu, tc::mbar_wait(&s.tfull[g], aphase, a.status, abort_flag))) {
+        // the tile's block ids and this entry's scale words, read before the
+        // accumulator is released: the producer rewrites their ring slots
+        // only after that release (through the operand stages)
+        if (!warp_wait(&s.rfull[it % kRing], (it / kRing) & 1, a.status, abort_flag) ||
+            !warp_wait(&s.sfull[it % kScRing], (it / kScRing) & 1, a.status, abort_flag)) {
+          aborted = true;
+          break;
+        }
+        const int32_t blk = s.rblk[it % kRing][row >> 6];
+        const uint8_t* slot = scale_s + (it % kScRing) * kScSlot;
+        float4 scv;
+        if (FP8)
+          scv = make_float4(reinterpret_cast<const float*>(slot)[row], 0.f, 0.f, 0.f);
+        else
+          scv = reinterpret_cast<const float4*>(slot)[row];
+        if (!warp_wait(&s.tfull[g], aphase, a.status, abort_flag)) {
           aborted = true;
           break;
         }
@@ -480,6 +499,9 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const __
         if (FP8) {
           float v[64];
           tc::tmem_ld64(lane_addr, v);
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&s.tempty[g]);
           float2 sum = make_float2(0.f, 0.f), sum2 = make_float2(0.f, 0.f);
 #pragma unroll
           for (int h = 0; h < 64; h += 4) {
@@ -491,7 +513,8 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const __
           score = ((sum.x + sum2.x) + (sum.y + sum2.y)) * scv.x;
         } else {
           // 16 heads per round (their 4 block accumulators = 64 columns); the
-          // next round's TMEM loads are in flight while this round is summed.
+          // next round's TMEM loads are in flight while this round is summed,
+          // and the accumulator is released as soon as the last round landed.
           // Two independent partial sums keep the FMA chains short.
           float2 sum = make_float2(0.f, 0.f), sum2 = make_float2(0.f, 0.f);
           const float2 s0 = make_float2(scv.x, scv.x), s1 = make_float2(scv.y, scv.y);
@@ -518,12 +541,14 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const __
                 sum2 = __ffma2_rn(d, make_float2(wq[hg * 16 + i], wq[hg * 16 + i + 1]), sum2);
             }
             if (hg < 3) tc::tmem_wait_ld(nx);
+            if (hg == 2) {
+              tc::tc_fence_before();
+              __syncwarp();
+              if (lane == 0) tc::mbar_arrive(&s.tempty[g]);
+            }
           }
           score = (sum.x + sum2.x) + (sum.y + sum2.y);
         }
-        tc::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&s.tempty[g]);
         if (e < n) {
           const float sv = blk >= 0 ? score : -INFINITY;
           srow[e] = sv;
@@ -555,6 +580,7 @@ int stages_count() {
   const int64_t room = int64_t(227 * 1024) - int64_t(kFixedSmem);
   int n = int(room / kStageBytes);
   if (n > kMaxStages) n = kMaxStages;
+  if (n > kScRing - 2) n = kScRing - 2;   // the scale ring outruns the stages by two tiles
   return n & ~1;
 }
 
