@@ -18,9 +18,8 @@
 //  roughly fixed time on every copy (about 0.1 us on GB300, measured), so one
 //  copy per block, issued by two producer warps, is what keeps HBM busy; the
 //  scale words (1 KB or 256 B per block) travel on the load/store path
-//  instead: every lane of the issuing producer warp puts 16-byte cp.async
-//  copies of them into the tile's slot of a shared-memory ring, whose
-//  barrier completes when they have landed.
+//  instead: each epilogue thread copies its own entry's words into shared
+//  memory with cp.async a few tiles ahead of their use.
 //  B = the query's e4m3 codes, N = 64 heads, staged once per query by a TMA
 //  tensor copy (which writes the swizzled operand itself);
 //  K = 128 in four MMAs of K = 32.  fp8 keys: the four MMAs accumulate into
@@ -73,7 +72,8 @@ constexpr int kEpi0 = kQw + 1;               // first epilogue warp
 constexpr int kEpiWarps = 8;                 // two epilogue warpgroups
 constexpr int kThreads = 32 * (kEpi0 + kEpiWarps);
 constexpr int kWin = 512;                    // block-table window of each producer
-constexpr int kScRing = 12;                  // tiles of scale words staged in shared memory
+constexpr int kScLead = 3;                   // own tiles an epilogue thread copies its scale words ahead
+constexpr int kScSlots = kScLead + 1;        // scale-word slots of each epilogue warpgroup
 constexpr int kScSlot = 128 * 16;            // one tile's scale words (fp4: 16 B per entry; fp8: 4 B)
 
 struct TcArgs {
@@ -97,7 +97,7 @@ struct TcArgs {
 };
 
 struct Smem {
-  uint64_t full[kMaxStages], empty[kMaxStages], rfull[kRing], tfull[2], tempty[2], qfull[2], qempty[2], sfull[kScRing], done,
+  uint64_t full[kMaxStages], empty[kMaxStages], rfull[kRing], tfull[2], tempty[2], qfull[2], qempty[2], done,
       hsync, hclear;
   uint32_t tmem_base;
   int abort_flag;
@@ -108,7 +108,7 @@ struct Smem {
   float wq[2][64];                  // w_h * qs_h of the query in each query buffer
 };
 
-constexpr size_t kFixedSmem = 1024 + 2 * kQBytes + kScRing * kScSlot + kHistBins * 4 + sizeof(Smem);
+constexpr size_t kFixedSmem = 1024 + 2 * kQBytes + 2 * kScSlots * kScSlot + kHistBins * 4 + sizeof(Smem);
 
 // Visible entries of query t, never beyond what its block-table row can address.
 __device__ __forceinline__ int visible_of(const TcArgs& a, int t) {
@@ -228,8 +228,8 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const __
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = base;                                   // stages x 16 KB: the MMA A operands
   uint8_t* qbuf = stages + size_t(a.stages) * kStageBytes;  // 2 x 8 KB
-  uint8_t* scale_s = qbuf + 2 * kQBytes;                    // kScRing x 2 KB: scale words of each tile
-  uint32_t* hist_s = reinterpret_cast<uint32_t*>(scale_s + kScRing * kScSlot);
+  uint8_t* scale_s = qbuf + 2 * kQBytes;                    // 2 x kScSlots x 2 KB: epilogue scale words
+  uint32_t* hist_s = reinterpret_cast<uint32_t*>(scale_s + 2 * kScSlots * kScSlot);
   Smem& s = *reinterpret_cast<Smem*>(hist_s + kHistBins);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = a.stages;
@@ -247,7 +247,6 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const __
       tc::mbar_init(&s.qfull[i], 1);
       tc::mbar_init(&s.qempty[i], 1 + kEpiWarps);   // MMA commit + every epilogue warp
     }
-    for (int i = 0; i < kScRing; ++i) tc::mbar_init(&s.sfull[i], 32);   // every lane of the issuing producer
     tc::mbar_init(&s.done, 1);
     tc::mbar_init(&s.hsync, kEpiWarps);
     tc::mbar_init(&s.hclear, kEpiWarps);
@@ -331,23 +330,6 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const __
         __syncwarp();
         if (p >= 0) tc::tma_load_3d(stages + stage * kStageBytes + lane * kBoxBytes, &kmap, 0, 0, p, &s.full[stage]);
         if (lane == 0) tc::mbar_arrive(&s.rfull[it % kRing]);   // block ids for the epilogue
-        // the blocks' scale words go to the tile's slot of the scale ring by
-        // 16-byte asynchronous copies from every lane; the slot's barrier
-        // completes when all of them have landed
-        {
-          uint8_t* slot = scale_s + (it % kScRing) * kScSlot;
-          const int32_t p0 = __shfl_sync(0xffffffffu, p, 0), p1 = __shfl_sync(0xffffffffu, p, 1);
-          constexpr int kChunks = (2 * 64 * F::kScaleBytes) / 16;   // 16-byte chunks of the tile's words
-#pragma unroll
-          for (int u = 0; u < kChunks / 32; ++u) {
-            const int ch = lane + 32 * u;
-            const int h = ch / (kChunks / 2), r = ch % (kChunks / 2);
-            const int32_t ph = h ? p1 : p0;
-            if (ph >= 0)
-              tc::cp_async16(slot + ch * 16, a.pool + int64_t(ph) * F::kBlockBytes + F::kScaleOff + r * 16);
-          }
-          tc::cp_async_arrive_noinc(&s.sfull[it % kScRing]);
-        }
       }
       if (++stage == S) { stage = 0; phase ^= 1; }
       c.next(a);
@@ -355,7 +337,6 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const __
     // drain: every copy this producer issued has landed before the CTA can
     // exit (each stage belongs to one producer, so its last fill is the
     // barrier's latest phase)
-    tc::cp_async_wait_all();
     if (lane == 0) {
       for (int i = 0; i < S; ++i) {
         if (last_par[i] < 0) continue;
@@ -452,6 +433,31 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const __
     float* srow = nullptr;
     const float* wq = nullptr;
     bool aborted = false;
+    // Scale words: each thread copies its own entry's words for the tile
+    // kScLead own tiles ahead into its warpgroup's ring with cp.async; one
+    // commit group per own tile, so waiting until kScLead groups remain
+    // pending means this tile's words have landed (no barrier needed: every
+    // thread reads only what it copied itself).
+    uint8_t* my_ring = scale_s + g * kScSlots * kScSlot;
+    auto issue_scales = [&](int o) -> bool {   // own tile o = item 2o + g
+      const int itn = 2 * o + g;
+      if (itn < count) {
+        if (!warp_wait(&s.rfull[itn % kRing], (itn / kRing) & 1, a.status, abort_flag)) return false;
+        const int32_t b = s.rblk[itn % kRing][row >> 6];
+        if (b >= 0) {
+          uint8_t* dst = my_ring + (o % kScSlots) * kScSlot + row * F::kScaleBytes;
+          const uint8_t* src = a.pool + int64_t(b) * F::kBlockBytes + F::kScaleOff + (row & 63) * F::kScaleBytes;
+          if (FP8)
+            tc::cp_async4(dst, src);
+          else
+            tc::cp_async16(dst, src);
+        }
+      }
+      tc::cp_async_commit();
+      return true;
+    };
+    for (int o = 0; o < kScLead && !aborted; ++o)
+      if (!issue_scales(o)) aborted = true;
     for (int it = 0; it < count && !aborted; ++it) {
       if (c.t != cur_t) {
         if (cur_t >= 0) {
@@ -475,16 +481,13 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const __
       }
       if ((it & 1) == g) {
         const int e = c.j * 128 + row;
-        // the tile's block ids and this entry's scale words, read before the
-        // accumulator is released: the producer rewrites their ring slots
-        // only after that release (through the operand stages)
-        if (!warp_wait(&s.rfull[it % kRing], (it / kRing) & 1, a.status, abort_flag) ||
-            !warp_wait(&s.sfull[it % kScRing], (it / kScRing) & 1, a.status, abort_flag)) {
-          aborted = true;
-          break;
-        }
+        const int o = it >> 1;
+        if (!issue_scales(o + kScLead)) { aborted = true; break; }
+        tc::cp_async_wait_group<kScLead>();
+        // the block id was seen when this tile's copy was issued; the ring
+        // slot is rewritten only kRing items later
         const int32_t blk = s.rblk[it % kRing][row >> 6];
-        const uint8_t* slot = scale_s + (it % kScRing) * kScSlot;
+        const uint8_t* slot = my_ring + (o % kScSlots) * kScSlot;
         float4 scv;
         if (FP8)
           scv = make_float4(reinterpret_cast<const float*>(slot)[row], 0.f, 0.f, 0.f);
@@ -562,6 +565,7 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const __
     // bounded waits then see the abort flag)
     if (a.hist && cur_t >= 0 && !aborted)
       flush_hist(&s.hsync, &s.hclear, hph, hist_s, a.hist + int64_t(cur_t) * kHistBins, et, a.status, abort_flag);
+    tc::cp_async_wait_all();   // no copy into shared memory outlives the CTA
     __syncwarp();
   }
   tc::tc_fence_before();
@@ -580,7 +584,6 @@ int stages_count() {
   const int64_t room = int64_t(227 * 1024) - int64_t(kFixedSmem);
   int n = int(room / kStageBytes);
   if (n > kMaxStages) n = kMaxStages;
-  if (n > kScRing - 2) n = kScRing - 2;   // the scale ring outruns the stages by two tiles
   return n & ~1;
 }
 
@@ -594,7 +597,9 @@ bool index_score_tc_supported(const v4a_index_args* a) {
   if ((reinterpret_cast<uintptr_t>(c.pool) & 31) || (reinterpret_cast<uintptr_t>(a->q) & 15)) return false;
   if (c.num_blocks > INT32_MAX) return false;
   if (a->batch.num_tokens > (1 << 24)) return false;   // query rows of the tensor map stay in int range
-  return stages_count() >= 4;
+  // an epilogue thread waits for the producer to issue the tile 2 * kScLead
+  // items ahead, which needs the stages to hold more than that many tiles
+  return stages_count() >= 2 * kScLead + 2;
 }
 
 bool index_score_tc(const v4a_index_args* a, float* scores, int64_t row, uint32_t* hist, cudaStream_t stream,
