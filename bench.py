@@ -153,6 +153,24 @@ def oracle_token(case, t, frac=1.0):
     OB.oracle_output(sub, F.bf16_encode(o))
 
 
+def max_over_ranks(x: float, device="cpu") -> float:
+    """The largest x over the ranks of the default process group (x itself
+    without one): every rank's timed region counts, the slowest decides."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world_size: int, units_per_rank_step: int, ms_per_step: float) -> float:
+    """Units per second over all ranks: every rank runs its own replica of the
+    step (the path shards by sequence), all within the max-over-ranks time."""
+    return world_size * units_per_rank_step / (ms_per_step * 1e-3)
+
+
 def cpu_cores():
     for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
         if os.environ.get(v):
@@ -284,14 +302,9 @@ def main():
         torch.cuda.synchronize()
         barrier()
         busy(0.4)
-    ms = e0.elapsed_time(e1) / args.steps
-    if ws > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
     tokens_per_step = spec.tokens
-    value = ws * tokens_per_step / (ms * 1e-3)
+    value = whole_job_rate(ws, tokens_per_step, ms)
 
     # ---- per-stage CUDA-event timing (same replicas, direct calls) ----
     names = ["compress_insert", "index_scores", "index_select", "sparse_attn", "inv_rope_quant"]
@@ -360,12 +373,7 @@ def main():
                 sc_host.copy_(steps[r].out_scale, non_blocking=True)
         f1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = f0.elapsed_time(f1) / args.steps
-    if ws > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1) / args.steps, dev)
 
     # ---- our kernel launches in the timed region (per step, from the path taken) ----
     launches = steps[0].launches_per_step() * args.steps
@@ -386,7 +394,7 @@ def main():
         "step_hbm_frac": step_bytes / (ms * 1e-3) / 1e9 / hbm_peak,
         "stage_us": stage_us, "dominant_stage": dominant,
         "algorithmic_bytes_per_step": {"scan": scan_b, "gather": gather_b, "window": win_b},
-        "e2e": {"value": ws * tokens_per_step / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": whole_job_rate(ws, tokens_per_step, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches,
         "clocks": clocks,

@@ -28,6 +28,14 @@
 //                         CTA ever waits on another.  It holds up to 8
 //                         candidates per thread in registers, so the
 //                         candidates are read from L2 once.
+//  * topk_coop          - long rows when every slice CTA of the batch fits on
+//                         the GPU at once (cooperative launch): the exact
+//                         k-th largest key comes from three histogram levels
+//                         (12 + 12 + 8 bits) shared by the query's slices
+//                         through bounded global barriers, then each slice
+//                         writes its share in ascending index order.  This
+//                         is the path of the 1M-context decode; topk_select
+//                         covers batches too large for one wave.
 
 #include <cstdio>
 #include <mutex>
