@@ -116,8 +116,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
   const int L = nsel + (m - wstart + 1);
   const int lo = sp * kKeys;
   const int64_t pi0 = int64_t(t) * a.splits + sp;
+  pdl_trigger();
 
   if (lo >= L) {   // this query's list is shorter than the longest: empty chunk
+    pdl_wait();
     for (int h = tid; h < a.H; h += blockDim.x) {
       a.part_ml[(pi0 * a.H + h) * 2] = -INFINITY;
       a.part_ml[(pi0 * a.H + h) * 2 + 1] = 0.f;
@@ -141,6 +143,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
   }
   __syncwarp();   // tcgen05.alloc is warp-collective: reconverge warp 0 after the init above
   if (warp == 0) tc::tmem_alloc(&s.tmem_base, D < 64 ? 64 : D);
+  // everything above overlaps the previous kernel; the selected indices, the
+  // caches and the window ring are read only after it has completed
+  pdl_wait();
 
   // ---- key slots of this chunk (sources, scales) ----
   if (tid < kKeys) {
@@ -393,6 +398,8 @@ constexpr int kCombMax = 16;     // splits per group held in registers (splits <
 
 __global__ void __launch_bounds__(256, 2) attn_combine_bf16(int H, int D, int splits, const uint16_t* part_o,
                                                             const float* part_ml, uint16_t* out, float* lse) {
+  pdl_trigger();
+  pdl_wait();   // the partials are the previous kernel's output
   __shared__ float wsm[kCombGroups * kCombMax];
   __shared__ float inv_s;
   __shared__ float4 part_s[kCombGroups - 1][64][2];
@@ -558,11 +565,12 @@ bool attn_tc(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t str
     cudaFuncSetAttribute(attn_chunk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   });
   if (smem > 227 * 1024) return false;
-  attn_chunk_tc<<<dim3(t.splits, t.T), kThreads, smem, stream>>>(t, qmap, omap);
-  if (t.splits > 1)
-    attn_combine_bf16<<<dim3(t.H, t.T), 256, 0, stream>>>(
-        t.H, t.D, t.splits, t.part_o, t.part_ml, t.out, t.lse);
-  if (cudaGetLastError() != cudaSuccess) *rc = V4A_ERR_CUDA;
+  // both may start while the kernel before them runs (they wait in-kernel)
+  cudaError_t e = launch_pdl(attn_chunk_tc, dim3(t.splits, t.T), dim3(kThreads), smem, stream, t, qmap, omap);
+  if (e == cudaSuccess && t.splits > 1)
+    e = launch_pdl(attn_combine_bf16, dim3(t.H, t.T), dim3(256), 0, stream, t.H, t.D, t.splits,
+                   static_cast<const uint16_t*>(t.part_o), static_cast<const float*>(t.part_ml), t.out, t.lse);
+  if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) *rc = V4A_ERR_CUDA;
   return true;
 }
 

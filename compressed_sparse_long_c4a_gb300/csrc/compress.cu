@@ -279,6 +279,7 @@ __device__ void window_token(const WindowSide& w, int t, int b, int P) {
 
 __global__ void compress_insert_kernel(BatchDev bt, CompressSide mainc, CompressSide ixc,
                                        WindowSide win, int32_t* status) {
+  pdl_trigger();   // the next kernel may be scheduled now (it waits for this one in-kernel)
   const int t = blockIdx.x;
   const int role = blockIdx.y;
   const int b = bt.seq_ids[t];

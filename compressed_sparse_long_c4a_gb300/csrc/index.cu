@@ -38,6 +38,7 @@
 //                         covers batches too large for one wave.
 
 #include <cstdio>
+#include <algorithm>
 #include <mutex>
 
 #include "v4a_common.cuh"
@@ -655,6 +656,7 @@ __global__ void __launch_bounds__(1024, 1) topk_coop(const float* scores, int64_
                                                  const int32_t* positions, int k, int slices,
                                                  const uint32_t* hist1, uint32_t* hist2, uint32_t* hist3,
                                                  uint32_t* counters, uint2* gteq, int32_t* out, int32_t* status) {
+  pdl_trigger();   // the attention kernel may be scheduled on SMs this grid leaves free
   __shared__ uint32_t scan[40];
   __shared__ uint32_t h_s[kHistBins];
   __shared__ int bin_s, give_up;
@@ -853,6 +855,15 @@ size_t index_workspace_size(const v4a_index_args* a) {
   return ws_layout(a, nullptr).total;
 }
 
+// Zeroes the histogram/counter part of the workspace.  Launched so that it may
+// start early; it waits for the kernel before it (which may still be reading
+// the previous call's histograms) before it writes.
+__global__ void __launch_bounds__(256) clear_words(uint32_t* p, size_t n) {
+  pdl_trigger();
+  pdl_wait();
+  for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += size_t(gridDim.x) * blockDim.x) p[i] = 0u;
+}
+
 // Stage 1: clear the histogram/counters and score every visible entry.
 int index_scores(const v4a_index_args* a, void* ws, size_t ws_bytes, cudaStream_t stream) {
   int rc = validate(a);
@@ -863,7 +874,11 @@ int index_scores(const v4a_index_args* a, void* ws, size_t ws_bytes, cudaStream_
   if (!ws || ws_bytes < w.total) return V4A_ERR_WORKSPACE;
   w = ws_layout(a, ws);
   const v4a_cache& c = a->keys;
-  if (cudaMemsetAsync(w.hist, 0, w.zero_bytes, stream) != cudaSuccess) return V4A_ERR_CUDA;
+  {
+    const size_t words = w.zero_bytes / 4;
+    const unsigned blocks = unsigned(std::min<size_t>((words + 255) / 256, 1024));
+    if (launch_pdl(clear_words, dim3(blocks), dim3(256), 0, stream, w.hist, words) != cudaSuccess) return V4A_ERR_CUDA;
+  }
   if (index_score_tc(a, w.scores, w.row, w.row > kSmemTopkMax ? w.hist : nullptr, stream, &rc)) return rc;
   ScoreArgs sa;
   sa.T = T; sa.H = a->num_heads; sa.dim = c.dim; sa.k_fmt = c.format; sa.q_fmt = a->q_format;

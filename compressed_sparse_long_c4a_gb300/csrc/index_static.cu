@@ -17,7 +17,7 @@
 // them) race on it and may return each other's selections: order them on one
 // stream or with events.  The histogram and counter part of the scratch must
 // start at zero; each call clears it on its own stream before the scan
-// (cudaMemsetAsync), so nothing depends on the array's initial contents.
+// (a clearing kernel), so nothing depends on the array's initial contents.
 
 #include <mutex>
 

@@ -234,6 +234,7 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const __
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = a.stages;
   volatile int* abort_flag = &s.abort_flag;
+  pdl_trigger();
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
@@ -259,6 +260,10 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const __
   if (warp == 0) tc::tmem_alloc(&s.tmem_base, 2 * F::kAccCols);
   tc::tc_fence_before();
   plan(a, s);              // contains __syncthreads
+  // the set-up above (inputs only) overlaps the previous kernels; the pool,
+  // which they write, and the histogram, which they clear, are touched only
+  // after they have completed
+  pdl_wait();
   tc::tc_fence_after();
   const uint32_t tmem = s.tmem_base;
   const int count = s.count;
@@ -669,11 +674,11 @@ bool index_score_tc(const v4a_index_args* a, float* scores, int64_t row, uint32_
     cudaFuncSetAttribute(index_scan_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     cudaFuncSetAttribute(index_scan_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   });
-  if (fp4)
-    index_scan_tc<false><<<tc::sm_count(), kThreads, smem, stream>>>(t, kmap, qmap);
-  else
-    index_scan_tc<true><<<tc::sm_count(), kThreads, smem, stream>>>(t, kmap, qmap);
-  if (cudaGetLastError() != cudaSuccess) { *rc = V4A_ERR_CUDA; return true; }
+  const cudaError_t e = fp4 ? launch_pdl(index_scan_tc<false>, dim3(tc::sm_count()), dim3(kThreads), smem, stream, t,
+                                          kmap, qmap)
+                           : launch_pdl(index_scan_tc<true>, dim3(tc::sm_count()), dim3(kThreads), smem, stream, t,
+                                        kmap, qmap);
+  if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) { *rc = V4A_ERR_CUDA; return true; }
   return true;
 }
 

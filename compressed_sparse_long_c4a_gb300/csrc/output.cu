@@ -77,6 +77,8 @@ inv_rope_quant_kernel(const OutDev a) {
     tc::mbar_fence_init();
   }
   __syncthreads();   // the barrier is initialised before any thread waits on it
+  pdl_trigger();
+  pdl_wait();        // the attention output is the previous kernel's
   // the slice fits the buffer and the copy starts on 16 bytes (checked on the host as well)
   const bool copy_ok = nchunks > 0 && nchunks * 16 <= kMaxSlice && (reinterpret_cast<uintptr_t>(in) & 15) == 0;
   if (threadIdx.x == 0 && copy_ok) {
@@ -158,7 +160,8 @@ int inv_rope_quant(const v4a_output_args* a, cudaStream_t stream) {
   d.rope = make_rope_freq(a->rope_dims, a->rope_theta);
   d.T = a->num_tokens; d.H = a->num_heads; d.D = a->dim; d.R = a->rope_dims; d.fmt = a->out_format;
   d.positions = a->positions; d.in = a->in; d.out = a->out; d.out_scale = a->out_scale;
-  inv_rope_quant_kernel<<<a->num_tokens * kSlices, kThreads, 0, stream>>>(d);
+  if (launch_pdl(inv_rope_quant_kernel, dim3(a->num_tokens * kSlices), dim3(kThreads), 0, stream, d) != cudaSuccess)
+    return V4A_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? V4A_OK : V4A_ERR_CUDA;
 }
 

@@ -20,6 +20,31 @@ __device__ __forceinline__ void report(int32_t* status, int bits) {
   if (status) atomicOr(status, bits);
 }
 
+// ---- programmatic dependent launch -----------------------------------------------
+// A kernel launched with launch_pdl may start while the kernel before it on the
+// stream is still running.  Every CTA of such a kernel calls pdl_wait() before
+// it reads anything an earlier kernel writes (or writes anything an earlier
+// kernel reads); pdl_wait returns once the earlier kernel has completed and its
+// writes are visible.  pdl_trigger() lets the next such kernel be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = smem;
+  lc.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---- bf16 -------------------------------------------------------------------
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
