@@ -307,7 +307,9 @@ def main():
     value = whole_job_rate(ws, tokens_per_step, ms)
 
     # ---- per-stage CUDA-event timing (same replicas, direct calls) ----
-    names = ["compress_insert", "index_scores", "index_select", "sparse_attn", "inv_rope_quant"]
+    fused = steps[0].fused_out
+    names = ["compress_insert", "index_scores", "index_select",
+             *(["sparse_attn_out"] if fused else ["sparse_attn", "inv_rope_quant"])]
     acc = {n: 0.0 for n in names}
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
     torch.cuda.synchronize()
@@ -327,10 +329,14 @@ def main():
             if spec.ix_heads:
                 v4a.index_select(L, st.idx, st.ws_index, stream)
             ev[3].record(stream)
-            v4a.sparse_attn(L, st.idx, st.o, st.lse, st.ws_attn, stream)
-            ev[4].record(stream)
-            v4a.inv_rope_quant(L, st.o, st.out, st.out_scale, stream)
-            ev[5].record(stream)
+            if fused:
+                v4a.sparse_attn_out(L, st.idx, st.out, st.out_scale, st.ws_attn, stream)
+                ev[4].record(stream)
+            else:
+                v4a.sparse_attn(L, st.idx, st.o, st.lse, st.ws_attn, stream)
+                ev[4].record(stream)
+                v4a.inv_rope_quant(L, st.o, st.out, st.out_scale, stream)
+                ev[5].record(stream)
         torch.cuda.synchronize()
         for k, n in enumerate(names):
             acc[n] += ev[k].elapsed_time(ev[k + 1])

@@ -43,6 +43,11 @@ int v4a_inv_rope_quant(const v4a_output_args* args, void* stream) {
   return v4a::inv_rope_quant(args, static_cast<cudaStream_t>(stream));
 }
 
+int v4a_sparse_attn_out(const v4a_attn_args* attn, const v4a_output_args* out, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  return v4a::sparse_attn_out(attn, out, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
 const char* v4a_status_string(int code) {
   switch (code) {
     case V4A_OK: return "ok";

@@ -209,11 +209,11 @@ static int validate_shape(const v4a_attn_args* a) {
   return V4A_OK;
 }
 
-static int validate(const v4a_attn_args* a) {
+static int validate(const v4a_attn_args* a, bool need_out = true) {
   const int rc = validate_shape(a);
   if (rc) return rc;
   if (a->batch.num_tokens == 0) return V4A_OK;
-  if (!a->batch.seq_ids || !a->batch.positions || !a->q || !a->out || !a->window ||
+  if (!a->batch.seq_ids || !a->batch.positions || !a->q || (need_out && !a->out) || !a->window ||
       !a->kv.pool || !a->kv.block_table)
     return V4A_ERR_INVALID_ARG;
   if (a->window_format == V4A_KV_FP8_TOKEN && !a->window_scale) return V4A_ERR_INVALID_ARG;
@@ -241,6 +241,9 @@ size_t attn_workspace_size(const v4a_attn_args* a) {
   const size_t T = a->batch.num_tokens, S = splits_for(a), H = a->num_heads, D = a->kv.dim;
   return S == 1 ? 256 : T * S * H * (D + 2) * 4 + 256;
 }
+
+// For the fused attention + output call, which does not write a->out.
+int validate_attn(const v4a_attn_args* a) { return validate(a, false); }
 
 int sparse_attn(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t stream) {
   int rc = validate(a);

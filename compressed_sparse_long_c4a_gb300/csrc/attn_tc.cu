@@ -61,6 +61,7 @@ struct AtcArgs {
   int32_t* status;
   uint32_t idesc_s, idesc_pv;
   int tma_out;        // rows leave through the output tensor map (H % 8 == 0)
+  int direct;         // one chunk per query and no merge kernel after: rows are the output
 };
 
 struct ASmem {   // every field read with vector loads carries its alignment explicitly
@@ -325,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
   mx = s.row_m[row];
   const bool store = ok && row < a.H;   // H need not be a multiple of 32: loads stay warp-wide
   const float inv = l > 0.f ? 1.f / l : 0.f;   // a chunk of only padding (-1) entries has l = 0
-  const bool direct = a.splits == 1;
+  const bool direct = a.direct != 0;
   // half hf's 64-column groups: warps 0-3 drain the first half of them, warps 4-7 the rest
   const int per_half = nsub / halves;
   for (int hf = 0; hf < halves; ++hf) {
@@ -510,7 +511,8 @@ size_t attn_tc_workspace_size(const v4a_attn_args* a) {
   return T * S * H * D * 2 + T * S * H * 2 * 4 + 512;
 }
 
-bool attn_tc(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t stream, int* rc) {
+bool attn_tc(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t stream, int* rc,
+             AttnPartials* keep) {
   *rc = V4A_OK;
   if (!handled(a)) return false;
   if (ws_bytes < attn_tc_workspace_size(a)) { *rc = V4A_ERR_WORKSPACE; return true; }
@@ -542,6 +544,8 @@ bool attn_tc(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t str
   const size_t T = t.T, S = t.splits, H = t.H, D = t.D;
   t.part_o = static_cast<uint16_t*>(ws);
   t.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + ((T * S * H * D * 2 + 255) & ~size_t(255)));
+  t.direct = (S == 1 && !keep) ? 1 : 0;
+  if (keep) *keep = AttnPartials{t.part_o, t.part_ml, int(S)};
   t.status = a->status;
   t.idesc_s = tc::make_idesc(1, 1, kRows, kKeys);
   t.idesc_pv = tc::make_idesc(1, 1, kRows, D > 256 ? 256 : D) | (1u << 16);   // B is MN-major
@@ -549,10 +553,10 @@ bool attn_tc(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t str
   CUtensorMap qmap, omap;
   if (!encode_rows(&qmap, a->q, int64_t(T) * H, int(D), kRows)) return false;
   // output rows leave through a tensor map when whole boxes of H rows fit the swizzle atom
-  t.tma_out = (H % 8 == 0) && (reinterpret_cast<uintptr_t>(S == 1 ? static_cast<void*>(a->out) : ws) & 15) == 0;
+  t.tma_out = (H % 8 == 0) && (reinterpret_cast<uintptr_t>(t.direct ? static_cast<void*>(a->out) : ws) & 15) == 0;
   if (t.tma_out) {
-    const void* dst = S == 1 ? static_cast<const void*>(a->out) : static_cast<const void*>(t.part_o);
-    const int64_t rows = S == 1 ? int64_t(T) * H : int64_t(T) * S * H;
+    const void* dst = t.direct ? static_cast<const void*>(a->out) : static_cast<const void*>(t.part_o);
+    const int64_t rows = t.direct ? int64_t(T) * H : int64_t(T) * S * H;
     if (!encode_rows(&omap, dst, rows, int(D), int(H))) t.tma_out = 0;
   }
   if (!t.tma_out) omap = qmap;   // unused
@@ -567,7 +571,7 @@ bool attn_tc(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t str
   if (smem > 227 * 1024) return false;
   // both may start while the kernel before them runs (they wait in-kernel)
   cudaError_t e = launch_pdl(attn_chunk_tc, dim3(t.splits, t.T), dim3(kThreads), smem, stream, t, qmap, omap);
-  if (e == cudaSuccess && t.splits > 1)
+  if (e == cudaSuccess && !t.direct && !keep)
     e = launch_pdl(attn_combine_bf16, dim3(t.H, t.T), dim3(256), 0, stream, t.H, t.D, t.splits,
                    static_cast<const uint16_t*>(t.part_o), static_cast<const float*>(t.part_ml), t.out, t.lse);
   if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) *rc = V4A_ERR_CUDA;

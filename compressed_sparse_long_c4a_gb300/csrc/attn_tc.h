@@ -5,5 +5,20 @@
 
 namespace v4a {
 size_t attn_tc_workspace_size(const v4a_attn_args* a);   // 0 when not handled
-bool attn_tc(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t stream, int* rc);
+
+// The per-chunk results the attention kernel leaves in the workspace:
+// o [T][splits][H][D] bf16 rows normalised by their chunk's softmax sum, and
+// ml [T][splits][H][2] = (max in log2 units, sum); an empty chunk has max -inf.
+struct AttnPartials {
+  const uint16_t* o;
+  const float* ml;
+  int splits;
+};
+
+// Launches the tensor-core attention when it handles the shapes (returns false
+// otherwise, launching nothing); *rc is the call's result code.  With `keep`
+// the chunk results stay in the workspace (described in *keep) and no merge
+// kernel runs: the caller merges them.
+bool attn_tc(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t stream, int* rc,
+             AttnPartials* keep = nullptr);
 }  // namespace v4a

@@ -17,6 +17,7 @@
 
 #include <mutex>
 
+#include "attn_tc.h"
 #include "tc_common.cuh"
 #include "v4a_internal.h"
 
@@ -141,7 +142,245 @@ inv_rope_quant_kernel(const OutDev a) {
   if (rank == 0 && threadIdx.x == 0) a.out_scale[t] = s;
 }
 
+// ---- attention merge fused with the output stage ------------------------------
+//
+// For the tensor-core attention's chunk results (normalised bf16 rows plus
+// (max, sum) per chunk): one cluster of `csize` CTAs per token, CTA r owning
+// heads [r*H/csize, (r+1)*H/csize).  Each thread merges one (head, 8-dim chunk)
+// over all chunks of the query with the weights and the summation order of the
+// stand-alone merge (four interleaved groups of chunks, then group 0 + 1 + 2 +
+// 3), rounds to bf16 as the stored attention output would be, and leaves the
+// row in shared memory; the rest is the output stage above (rotation by
+// -angle, token amax through distributed shared memory, encode), so the bytes
+// equal those of the two-call path.  The bf16 attention output never goes to
+// HBM and one kernel boundary disappears.
+constexpr int kMergeThreads = 512;
+constexpr int kMergeGroups = 4;
+constexpr int kMergeBatch = 12;          // chunk rows in flight per thread (a multiple of kMergeGroups)
+static_assert(kMergeBatch % 4 == 0, "chunk groups must be fixed per batch slot");
+constexpr int kMergeMaxSplits = 64;
+constexpr int kMergeMaxRows = 16;        // heads per CTA
+
+struct MergeDev {
+  RopeFreq rope;
+  int T, H, D, R, fmt, splits;
+  const int32_t* positions;
+  const uint16_t* part_o;
+  const float* part_ml;
+  void* out;
+  float* out_scale;
+};
+
+__global__ void __launch_bounds__(kMergeThreads) merge_out_kernel(const MergeDev a) {
+  __shared__ __align__(128) uint4 rows_s[kMaxSlice / 16];
+  __shared__ float wsm[kMergeMaxRows][kMergeMaxSplits];
+  __shared__ float inv_s[kMergeMaxRows];
+  __shared__ float cs[128];
+  __shared__ float red[32];
+  __shared__ float slice_amax;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int csize = int(cluster.num_blocks());
+  const int rank = int(cluster.block_rank());
+  const int t = blockIdx.x / csize;
+  const int hp = a.H / csize, h0 = rank * hp;
+  const int per_head = a.D / 8;
+  const int nchunks = hp * per_head;                   // 16-byte chunks of this CTA's rows
+  const int first = a.D - a.R;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
+  rope_table(a.positions[t], a.R, a.rope, cs);        // positions are a step input
+  pdl_wait();                                          // the chunk results are the previous kernel's
+  // 1. chunk weights of every head of this CTA (as in the stand-alone merge)
+  for (int hh = warp; hh < hp; hh += kMergeThreads / 32) {
+    const float* ml = a.part_ml + (int64_t(t) * a.splits * a.H + h0 + hh) * 2;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    if (lane < a.splits) { m0 = ml[int64_t(lane) * a.H * 2]; l0 = ml[int64_t(lane) * a.H * 2 + 1]; }
+    if (lane + 32 < a.splits) { m1 = ml[int64_t(lane + 32) * a.H * 2]; l1 = ml[int64_t(lane + 32) * a.H * 2 + 1]; }
+    const float mx = warp_max(fmaxf(m0, m1));
+    const float w0 = m0 == -INFINITY ? 0.f : l0 * exp2f(m0 - mx);
+    const float w1 = m1 == -INFINITY ? 0.f : l1 * exp2f(m1 - mx);
+    if (lane < a.splits) wsm[hh][lane] = w0;
+    if (lane + 32 < a.splits) wsm[hh][lane + 32] = w1;
+    const float tot = warp_sum(w0 + w1);
+    if (lane == 0) inv_s[hh] = tot > 0.f ? 1.f / tot : 0.f;
+  }
+  __syncthreads();
+  // 2. merged rows, rounded to bf16, into shared memory
+  for (int c = threadIdx.x; c < nchunks; c += kMergeThreads) {
+    const int hh = c / per_head, cc = c % per_head;
+    const uint16_t* po = a.part_o + (int64_t(t) * a.splits * a.H + h0 + hh) * a.D + cc * 8;
+    if (a.splits == 1) {   // one chunk: its normalised row is the attention output as stored
+      rows_s[c] = __ldcg(reinterpret_cast<const uint4*>(po));
+      continue;
+    }
+    float acc[kMergeGroups][8];
+#pragma unroll
+    for (int g = 0; g < kMergeGroups; ++g)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[g][i] = 0.f;
+    for (int sp0 = 0; sp0 < a.splits; sp0 += kMergeBatch) {
+      uint4 v[kMergeBatch];
+#pragma unroll
+      for (int u = 0; u < kMergeBatch; ++u) {
+        const int sp = sp0 + u;
+        v[u] = sp < a.splits ? __ldcg(reinterpret_cast<const uint4*>(po + int64_t(sp) * a.H * a.D))
+                             : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < kMergeBatch; ++u) {
+        const int sp = sp0 + u;
+        const float w = sp < a.splits ? wsm[hh][sp] : 0.f;
+        if (w == 0.f) continue;
+        // chunk sp belongs to group sp % 4 = u % 4 (sp0 is a multiple of
+        // kMergeBatch, itself a multiple of the group count)
+        const uint32_t q[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        float* ag = acc[u % kMergeGroups];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          ag[2 * j] = fmaf(w, bf16_to_f32(uint16_t(q[j] & 0xffffu)), ag[2 * j]);
+          ag[2 * j + 1] = fmaf(w, bf16_to_f32(uint16_t(q[j] >> 16)), ag[2 * j + 1]);
+        }
+      }
+    }
+    const float inv = inv_s[hh];
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float e0 = acc[0][2 * j], e1 = acc[0][2 * j + 1];
+#pragma unroll
+      for (int g = 1; g < kMergeGroups; ++g) { e0 += acc[g][2 * j]; e1 += acc[g][2 * j + 1]; }
+      o[j] = uint32_t(f32_to_bf16(e0 * inv)) | (uint32_t(f32_to_bf16(e1 * inv)) << 16);
+    }
+    rows_s[c] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  __syncthreads();
+  // 3. the output stage on those rows
+  const int c0 = rank * nchunks;                       // first chunk of the slice within the token
+  if (a.fmt == V4A_OUT_BF16) {
+    uint4* out = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + int64_t(t) * a.H * a.D) + c0;
+    for (int c = threadIdx.x; c < nchunks; c += kMergeThreads) {
+      float x[8];
+      rotated_chunk(rows_s[c], ((c0 + c) % per_head) * 8, first, a.R, cs, x);
+      uint32_t u[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) u[i] = uint32_t(f32_to_bf16(x[2 * i])) | (uint32_t(f32_to_bf16(x[2 * i + 1])) << 16);
+      out[c] = make_uint4(u[0], u[1], u[2], u[3]);
+    }
+    return;
+  }
+  float amax = 0.f;
+  for (int c = threadIdx.x; c < nchunks; c += kMergeThreads) {
+    float x[8];
+    rotated_chunk(rows_s[c], ((c0 + c) % per_head) * 8, first, a.R, cs, x);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  }
+  amax = block_reduce<true>(amax, red);
+  if (threadIdx.x == 0) slice_amax = amax;
+  cluster.sync();
+  if (threadIdx.x == 0) {
+    float mx = 0.f;
+    for (int r = 0; r < csize; ++r) mx = fmaxf(mx, *cluster.map_shared_rank(&slice_amax, r));
+    red[0] = mx;
+  }
+  cluster.sync();   // no CTA leaves while others may still read its slice_amax
+  const float tok = red[0];
+  const float sc = tok > 0.f ? tok / 448.f : 1.f;
+  uint2* out = reinterpret_cast<uint2*>(static_cast<uint8_t*>(a.out) + int64_t(t) * a.H * a.D) + c0;
+  for (int c = threadIdx.x; c < nchunks; c += kMergeThreads) {
+    float x[8];
+    rotated_chunk(rows_s[c], ((c0 + c) % per_head) * 8, first, a.R, cs, x);
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) lo |= uint32_t(f32_to_e4m3(x[i] / sc)) << (8 * i);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) hi |= uint32_t(f32_to_e4m3(x[4 + i] / sc)) << (8 * i);
+    out[c] = make_uint2(lo, hi);
+  }
+  if (rank == 0 && threadIdx.x == 0) a.out_scale[t] = sc;
+}
+
+// Largest cluster (16, else 8) the merge kernel can run with on this device.
+int merge_cluster_size() {
+  static int cached = 0;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute(merge_out_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    for (int cs : {16, 8}) {
+      cudaLaunchConfig_t lc = {};
+      lc.gridDim = dim3(cs);
+      lc.blockDim = dim3(kMergeThreads);
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = cs;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      lc.attrs = at;
+      lc.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, merge_out_kernel, &lc) == cudaSuccess && n > 0) {
+        cached = cs;
+        break;
+      }
+      cudaGetLastError();
+    }
+  });
+  return cached;
+}
+
 }  // namespace
+
+// Output-stage argument checks shared by both entry points.
+static int check_output_args(const v4a_output_args* a, bool need_in) {
+  if (!a) return V4A_ERR_INVALID_ARG;
+  if (a->num_tokens < 0 || a->num_heads < 1 || a->dim < 8 || a->dim % 8) return V4A_ERR_INVALID_ARG;
+  if (a->rope_dims < 0 || a->rope_dims > a->dim || a->rope_dims % 2) return V4A_ERR_INVALID_ARG;
+  if (a->rope_dims > 128) return V4A_ERR_UNSUPPORTED;
+  if (a->out_format != V4A_OUT_BF16 && a->out_format != V4A_OUT_FP8_TOKEN) return V4A_ERR_INVALID_ARG;
+  if (a->num_tokens == 0) return V4A_OK;
+  if (!a->positions || !a->out || (need_in && !a->in)) return V4A_ERR_INVALID_ARG;
+  if (a->out_format == V4A_OUT_FP8_TOKEN && !a->out_scale) return V4A_ERR_INVALID_ARG;
+  return V4A_OK;
+}
+
+int sparse_attn_out(const v4a_attn_args* at, const v4a_output_args* a, void* ws, size_t ws_bytes,
+                    cudaStream_t stream) {
+  if (!at) return V4A_ERR_INVALID_ARG;
+  int rc = check_output_args(a, false);
+  if (rc) return rc;
+  if (a->num_tokens != at->batch.num_tokens || a->num_heads != at->num_heads || a->dim != at->kv.dim)
+    return V4A_ERR_INVALID_ARG;
+  const int csize = merge_cluster_size();
+  if (csize == 0 || a->num_heads % csize || a->num_heads / csize > kMergeMaxRows) return V4A_ERR_UNSUPPORTED;
+  if (int64_t(a->num_heads / csize) * a->dim * 2 > kMaxSlice) return V4A_ERR_UNSUPPORTED;
+  rc = validate_attn(at);
+  if (rc) return rc;
+  if (a->num_tokens == 0) return V4A_OK;
+  AttnPartials p{};
+  if (!attn_tc(at, ws, ws_bytes, stream, &rc, &p)) return V4A_ERR_UNSUPPORTED;
+  if (rc) return rc;
+  if (p.splits > kMergeMaxSplits) return V4A_ERR_UNSUPPORTED;
+  MergeDev d;
+  d.rope = make_rope_freq(a->rope_dims, a->rope_theta);
+  d.T = a->num_tokens; d.H = a->num_heads; d.D = a->dim; d.R = a->rope_dims; d.fmt = a->out_format;
+  d.splits = p.splits; d.positions = a->positions; d.part_o = p.o; d.part_ml = p.ml;
+  d.out = a->out; d.out_scale = a->out_scale;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(unsigned(a->num_tokens * csize));
+  lc.blockDim = dim3(kMergeThreads);
+  lc.stream = stream;
+  cudaLaunchAttribute la[2];
+  la[0].id = cudaLaunchAttributeClusterDimension;
+  la[0].val.clusterDim.x = unsigned(csize);
+  la[0].val.clusterDim.y = 1;
+  la[0].val.clusterDim.z = 1;
+  la[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  la[1].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = la;
+  lc.numAttrs = 2;
+  if (cudaLaunchKernelEx(&lc, merge_out_kernel, d) != cudaSuccess) return V4A_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? V4A_OK : V4A_ERR_CUDA;
+}
 
 int inv_rope_quant(const v4a_output_args* a, cudaStream_t stream) {
   if (!a) return V4A_ERR_INVALID_ARG;

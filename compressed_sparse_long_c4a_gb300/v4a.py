@@ -95,6 +95,7 @@ def lib() -> C.CDLL:
         L.v4a_attn_workspace_size.restype = C.c_size_t
         L.v4a_sparse_attn.argtypes = [C.POINTER(AttnArgs), _p, C.c_size_t, _p]
         L.v4a_inv_rope_quant.argtypes = [C.POINTER(OutputArgs), _p]
+        L.v4a_sparse_attn_out.argtypes = [C.POINTER(AttnArgs), C.POINTER(OutputArgs), _p, C.c_size_t, _p]
         L.v4a_status_string.restype = C.c_char_p
         L.v4a_status_string.argtypes = [C.c_int]
         _lib = L
@@ -272,13 +273,34 @@ def inv_rope_quant(layer: DeviceLayer, o: torch.Tensor, out: torch.Tensor,
     _check("v4a_inv_rope_quant", lib().v4a_inv_rope_quant(C.byref(a), _stream(stream)))
 
 
-class Step:
-    """Output buffers + workspaces for running whole layer steps on a DeviceLayer."""
+V4A_ERR_UNSUPPORTED = 2
 
-    def __init__(self, layer: DeviceLayer):
+
+def sparse_attn_out(layer: DeviceLayer, idx: torch.Tensor | None, out: torch.Tensor,
+                    out_scale: torch.Tensor | None, workspace: torch.Tensor, stream=None) -> bool:
+    """Attention + inverse RoPE + output encode in one call (the bf16 attention
+    output is not stored).  False, with nothing launched, when the shapes are
+    outside the fused path; any other failure raises."""
+    a = layer.attn_args(idx, None, None)
+    o = layer.output_args(None, out, out_scale)
+    rc = lib().v4a_sparse_attn_out(C.byref(a), C.byref(o), _ptr(workspace), workspace.numel(), _stream(stream))
+    if rc == V4A_ERR_UNSUPPORTED:
+        return False
+    _check("v4a_sparse_attn_out", rc)
+    return True
+
+
+class Step:
+    """Output buffers + workspaces for running whole layer steps on a DeviceLayer.
+
+    fused_out: attention and output stage as one call (v4a_sparse_attn_out)
+    where the library takes the shapes; self.o is then not written."""
+
+    def __init__(self, layer: DeviceLayer, fused_out: bool = True):
         s = layer.spec
         dev = layer.status.device
         self.layer = layer
+        self.fused_out = fused_out
         T = s.tokens
         self.idx = torch.full((T, s.topk), -1, dtype=torch.int32, device=dev) if s.ix_heads else None
         self.o = torch.empty((T, s.heads, s.dim), dtype=torch.bfloat16, device=dev)
@@ -305,6 +327,8 @@ class Step:
         if s.ix_heads:
             tc_scan = s.ix_fmt in (IX_FP8_B128, IX_FP4_B32) and s.ix_heads == 64 and s.ix_dim == 128
             n += 2 + (1 if s.max_blocks * 64 <= 32768 or tc_scan else 2)
+        if self.fused_out:
+            return n + 2                      # attention + merge/output kernel
         n += 1 + (1 if self.ws_attn.numel() > 256 else 0)
         return n + 1
 
@@ -314,5 +338,9 @@ class Step:
         compress_insert(L, stream)
         if L.spec.ix_heads:
             index_topk(L, self.idx, self.ws_index, stream)
+        if self.fused_out:
+            if sparse_attn_out(L, self.idx, self.out, self.out_scale, self.ws_attn, stream):
+                return
+            self.fused_out = False            # shapes outside the fused path: the two calls
         sparse_attn(L, self.idx, self.o, self.lse, self.ws_attn, stream)
         inv_rope_quant(L, self.o, self.out, self.out_scale, stream)

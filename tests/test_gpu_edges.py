@@ -48,7 +48,7 @@ def test_fewer_entries_than_k_and_first_entry():
     spec = dataclasses.replace(I.c4a_decode_1k(), name="short", batch=2, cached=(3, 41))
     case = I.make_case(spec, seed=1)
     L = v4a.DeviceLayer.from_case(case)
-    step = v4a.Step(L)
+    step = v4a.Step(L, fused_out=False)   # the bf16 attention output is checked
     step.run()
     torch.cuda.synchronize()
     assert int(L.status.item()) == 0
@@ -92,7 +92,7 @@ def test_unallocated_block_sets_status_without_fault():
     case = I.make_case(spec, seed=3)
     case.block_table[1, 3] = -1           # a block the indexer and attention both need
     L = v4a.DeviceLayer.from_case(case)
-    step = v4a.Step(L)
+    step = v4a.Step(L, fused_out=False)
     step.run()
     torch.cuda.synchronize()
     st = int(L.status.item())
@@ -100,6 +100,14 @@ def test_unallocated_block_sets_status_without_fault():
     assert not st & 8                    # no timeout
     o = step.o.float().cpu().numpy()
     assert np.isfinite(o).all()
+    # the fused attention + output call on the same holes: same status, finite output
+    L2 = v4a.DeviceLayer.from_case(case)
+    fused = v4a.Step(L2, fused_out=True)
+    fused.run()
+    torch.cuda.synchronize()
+    st2 = int(L2.status.item())
+    assert st2 & v4a.DEV_BAD_BLOCK and not st2 & 8
+    assert torch.equal(fused.out.cpu(), step.out.cpu())
 
 
 def _sub_batch(L, case, rows):

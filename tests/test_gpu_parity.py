@@ -262,7 +262,7 @@ def test_end_to_end(name):
     r = run_for(name)
     s, case = r.spec, r.case
     L = r.layer()
-    step = v4a.Step(L)
+    step = v4a.Step(L, fused_out=False)   # two calls: the bf16 attention output is checked too
     step.run()
     torch.cuda.synchronize()
     assert int(L.status.item()) == 0
@@ -292,3 +292,30 @@ def test_end_to_end(name):
             got = F.e4m3_decode(out[t].numpy()) * sc
             bound = F.e4m3_ulp(ref_t / sc) * sc + tol[0]
         assert np.all(np.abs(got - ref_t) <= bound), (name, t)
+
+
+# Workloads whose attention the fused attention + output call must take.
+FUSED_EXPECTED = {"c4a_decode_b4_1m", "c4a_decode_b32_32k_64k", "c128a_decode_b64_64k_128k",
+                  "c4a_decode_small_fp8ix", "c4a_decode_small_fp4ix_fp8kv"}
+
+
+@pytest.mark.parametrize("name", [_marks(n) for n in ALL])
+def test_fused_output_equals_two_calls(name):
+    """v4a_sparse_attn_out writes the same bytes as v4a_sparse_attn followed by
+    v4a_inv_rope_quant (same inputs, separate layer copies); the two-call path
+    is checked against the oracle by test_end_to_end."""
+    from compressed_sparse_long_c4a_gb300 import v4a
+    r = run_for(name)
+    La, Lb = r.layer(), r.layer()
+    fused, plain = v4a.Step(La, fused_out=True), v4a.Step(Lb, fused_out=False)
+    fused.run()
+    plain.run()
+    torch.cuda.synchronize()
+    assert int(La.status.item()) == 0 and int(Lb.status.item()) == 0
+    if name in FUSED_EXPECTED:
+        assert fused.fused_out, "the fused call declined a shape it should take"
+    if not fused.fused_out:
+        pytest.skip("shapes outside the fused path: the step used the two calls")
+    assert torch.equal(fused.out.cpu(), plain.out.cpu())
+    if plain.out_scale is not None:
+        assert torch.equal(fused.out_scale.cpu(), plain.out_scale.cpu())
