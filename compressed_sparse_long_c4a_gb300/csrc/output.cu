@@ -154,10 +154,10 @@ inv_rope_quant_kernel(const OutDev a) {
 // -angle, token amax through distributed shared memory, encode), so the bytes
 // equal those of the two-call path.  The bf16 attention output never goes to
 // HBM and one kernel boundary disappears.
-constexpr int kMergeThreads = 512;
-constexpr int kMergeGroups = 4;
-constexpr int kMergeBatch = 12;          // chunk rows in flight per thread (a multiple of kMergeGroups)
-static_assert(kMergeBatch % 4 == 0, "chunk groups must be fixed per batch slot");
+constexpr int kMergeThreads = 1024;
+constexpr int kMergeGroups = 4;          // chunk groups: chunk sp belongs to group sp % 4
+constexpr int kMergeItems = kMergeThreads / kMergeGroups;   // (head, 8-dim chunk) items per round
+constexpr int kMergeBatch = 9;           // chunk rows in flight per thread (34 chunks: one batch)
 constexpr int kMergeMaxSplits = 64;
 constexpr int kMergeMaxRows = 16;        // heads per CTA
 
@@ -173,6 +173,7 @@ struct MergeDev {
 
 __global__ void __launch_bounds__(kMergeThreads) merge_out_kernel(const MergeDev a) {
   __shared__ __align__(128) uint4 rows_s[kMaxSlice / 16];
+  __shared__ float4 part_s[kMergeGroups - 1][kMergeItems][2];
   __shared__ float wsm[kMergeMaxRows][kMergeMaxSplits];
   __shared__ float inv_s[kMergeMaxRows];
   __shared__ float cs[128];
@@ -205,53 +206,63 @@ __global__ void __launch_bounds__(kMergeThreads) merge_out_kernel(const MergeDev
     if (lane == 0) inv_s[hh] = tot > 0.f ? 1.f / tot : 0.f;
   }
   __syncthreads();
-  // 2. merged rows, rounded to bf16, into shared memory
-  for (int c = threadIdx.x; c < nchunks; c += kMergeThreads) {
-    const int hh = c / per_head, cc = c % per_head;
+  // 2. merged rows, rounded to bf16, into shared memory.  Thread (g, i) sums
+  //    the chunks of group g for item i of the round in increasing order (one
+  //    warp = 32 consecutive items of one group: whole 512-byte runs per load);
+  //    group 0 then adds groups 1, 2, 3 in that order.
+  const int g = threadIdx.x / kMergeItems, il = threadIdx.x % kMergeItems;
+  for (int base = 0; base < nchunks; base += kMergeItems) {
+    const int c = base + il;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const bool live = c < nchunks;
+    const int hh = live ? c / per_head : 0, cc = live ? c % per_head : 0;
     const uint16_t* po = a.part_o + (int64_t(t) * a.splits * a.H + h0 + hh) * a.D + cc * 8;
-    if (a.splits == 1) {   // one chunk: its normalised row is the attention output as stored
-      rows_s[c] = __ldcg(reinterpret_cast<const uint4*>(po));
+    if (a.splits == 1) {
+      // one chunk: its normalised row is the attention output as stored
+      if (live && g == 0) rows_s[c] = __ldcg(reinterpret_cast<const uint4*>(po));
       continue;
     }
-    float acc[kMergeGroups][8];
-#pragma unroll
-    for (int g = 0; g < kMergeGroups; ++g)
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[g][i] = 0.f;
-    for (int sp0 = 0; sp0 < a.splits; sp0 += kMergeBatch) {
+    for (int u0 = 0; live && g + kMergeGroups * u0 < a.splits; u0 += kMergeBatch) {
       uint4 v[kMergeBatch];
 #pragma unroll
       for (int u = 0; u < kMergeBatch; ++u) {
-        const int sp = sp0 + u;
+        const int sp = g + kMergeGroups * (u0 + u);
         v[u] = sp < a.splits ? __ldcg(reinterpret_cast<const uint4*>(po + int64_t(sp) * a.H * a.D))
                              : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int u = 0; u < kMergeBatch; ++u) {
-        const int sp = sp0 + u;
+        const int sp = g + kMergeGroups * (u0 + u);
         const float w = sp < a.splits ? wsm[hh][sp] : 0.f;
         if (w == 0.f) continue;
-        // chunk sp belongs to group sp % 4 = u % 4 (sp0 is a multiple of
-        // kMergeBatch, itself a multiple of the group count)
         const uint32_t q[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-        float* ag = acc[u % kMergeGroups];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          ag[2 * j] = fmaf(w, bf16_to_f32(uint16_t(q[j] & 0xffffu)), ag[2 * j]);
-          ag[2 * j + 1] = fmaf(w, bf16_to_f32(uint16_t(q[j] >> 16)), ag[2 * j + 1]);
+          acc[2 * j] = fmaf(w, bf16_to_f32(uint16_t(q[j] & 0xffffu)), acc[2 * j]);
+          acc[2 * j + 1] = fmaf(w, bf16_to_f32(uint16_t(q[j] >> 16)), acc[2 * j + 1]);
         }
       }
     }
-    const float inv = inv_s[hh];
-    uint32_t o[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float e0 = acc[0][2 * j], e1 = acc[0][2 * j + 1];
-#pragma unroll
-      for (int g = 1; g < kMergeGroups; ++g) { e0 += acc[g][2 * j]; e1 += acc[g][2 * j + 1]; }
-      o[j] = uint32_t(f32_to_bf16(e0 * inv)) | (uint32_t(f32_to_bf16(e1 * inv)) << 16);
+    if (g > 0) {
+      part_s[g - 1][il][0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      part_s[g - 1][il][1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
-    rows_s[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    __syncthreads();
+    if (g == 0 && live) {
+#pragma unroll
+      for (int g2 = 0; g2 < kMergeGroups - 1; ++g2) {
+        const float4 x = part_s[g2][il][0], y = part_s[g2][il][1];
+        acc[0] += x.x; acc[1] += x.y; acc[2] += x.z; acc[3] += x.w;
+        acc[4] += y.x; acc[5] += y.y; acc[6] += y.z; acc[7] += y.w;
+      }
+      const float inv = inv_s[hh];
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        o[j] = uint32_t(f32_to_bf16(acc[2 * j] * inv)) | (uint32_t(f32_to_bf16(acc[2 * j + 1] * inv)) << 16);
+      rows_s[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    __syncthreads();   // part_s is rewritten by the next round
   }
   __syncthreads();
   // 3. the output stage on those rows
