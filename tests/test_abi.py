@@ -116,3 +116,27 @@ def test_host_validation_of_attention_and_output(lib):
     assert lib.v4a_inv_rope_quant(C.byref(o), None) == 1
     o = v4a.OutputArgs(0, None, 128, 512, 64, 1e4, None, 0, None, None)  # empty batch: no work
     assert lib.v4a_inv_rope_quant(C.byref(o), None) == 0
+
+
+def test_host_validation_of_fused_attention_output(lib):
+    """v4a_sparse_attn_out rejects bad or mismatched arguments before any
+    device call (the checks come before the cluster-size query)."""
+    spec = I.c4a_decode_1m()
+    L = _FakeLayer(spec)
+    a = v4a.AttnArgs(L.batch(), L.kv_cache(), 0x10, spec.topk, 0x20, 0x30, spec.swa_cap, spec.swa_fmt,
+                     spec.swa, spec.heads, 0x40, 0.04, None, None, None)
+    o = v4a.OutputArgs(spec.tokens, 0x2000, spec.heads, spec.dim, spec.rope_dims, spec.theta, None,
+                       spec.out_fmt, 0x60, 0x70)
+    assert lib.v4a_sparse_attn_out(None, C.byref(o), 0x1000, 1 << 30, None) == 1
+    assert lib.v4a_sparse_attn_out(C.byref(a), None, 0x1000, 1 << 30, None) == 1
+    o.num_tokens = spec.tokens + 1                                        # not the attention's tokens
+    assert lib.v4a_sparse_attn_out(C.byref(a), C.byref(o), 0x1000, 1 << 30, None) == 1
+    o.num_tokens = spec.tokens
+    o.num_heads = spec.heads // 2                                         # not the attention's heads
+    assert lib.v4a_sparse_attn_out(C.byref(a), C.byref(o), 0x1000, 1 << 30, None) == 1
+    o.num_heads = spec.heads
+    o.out_format = 7
+    assert lib.v4a_sparse_attn_out(C.byref(a), C.byref(o), 0x1000, 1 << 30, None) == 1
+    o.out_format = spec.out_fmt
+    o.out_scale = None                                                    # fp8 output needs its scales
+    assert lib.v4a_sparse_attn_out(C.byref(a), C.byref(o), 0x1000, 1 << 30, None) == 1
