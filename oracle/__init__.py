@@ -19,10 +19,13 @@ Pinning status (what each part is checked against, in ``tests/``):
                 enumeration of slot mapping.
   compressor  - closed forms (equal logits -> mean, dominant logit -> copy,
                 RMS = 1), RoPE group identities, chunk == step.
-  indexer     - brute-force sort on tiny inputs, all-tie rule.
-  attention   - dense special case against torch fp64 softmax + matmul,
-                SWA coverage, translation invariance after inverse RoPE.
+  indexer     - brute-force sort on tiny inputs, all-tie rule, a hand-worked
+                two-head score (ReLU, head weights).
+  attention   - hand-worked two- and three-key examples (weights, values =
+                keys, log-sum-exp), dense special case against torch fp64
+                softmax + matmul, SWA coverage, translation invariance after
+                inverse RoPE, a hand-worked inverse rotation.
   kvbytes     - the page's 9.62 GiB / 83.9 GiB / 8.7x figures.
-  Absolute attention values on general inputs: parity unpinned beyond the
-  above (the page prints no worked numerical example).
+  The page prints no worked numerical example; the hand examples above are
+  computed from the definitions, not by this package.
 """

@@ -95,3 +95,53 @@ def test_attention_softmax_is_a_distribution_over_union():
         a, _ = A.shared_kv_attention(q, ks, 0.3)
         b, _ = A.shared_kv_attention(q, ks[list(perm)], 0.3)
         assert np.allclose(a, b, atol=1e-14)
+
+
+# ---- hand-worked examples (values computed by hand, not by the oracle) -------
+
+def test_index_score_hand_example():
+    """Two heads: q_1.k = 3, q_2.k = -2 (ReLU drops it), w = (0.5, 2):
+    score = 0.5 * 3 + 2 * 0 = 1.5.  A second key with q_1.k = -1, q_2.k = 4
+    scores 2 * 4 = 8 and ranks first."""
+    q = np.array([[1.0, 1.0, 0.0], [0.0, -1.0, 1.0]])
+    w = np.array([0.5, 2.0])
+    keys = np.array([[1.0, 2.0, 0.0],      # q1.k = 3, q2.k = -2
+                     [0.0, -1.0, 3.0]])    # q1.k = -1, q2.k = 4
+    s = I.index_scores(q, w, keys)
+    assert s.tolist() == [1.5, 8.0]
+    assert I.topk_set(s, 1).tolist() == [1]
+
+
+def test_attention_two_keys_hand_example():
+    """tau = ln(3)/2, q = (1, 0), k1 = (2, 0), k2 = (0, 5): logits ln 3 and 0,
+    weights 3/4 and 1/4, output 3/4 k1 + 1/4 k2 = (1.5, 1.25), lse = ln 4."""
+    tau = math.log(3.0) / 2.0
+    q = np.array([[1.0, 0.0]])
+    keys = np.array([[2.0, 0.0], [0.0, 5.0]])
+    o, lse = A.shared_kv_attention(q, keys, tau)
+    assert np.allclose(o, [[1.5, 1.25]], rtol=0, atol=1e-15)
+    assert math.isclose(lse[0], math.log(4.0), rel_tol=1e-15)
+
+
+def test_attention_three_keys_two_heads_hand_example():
+    """tau = ln 2.  Head 1 (q = (2, 0)): logits 2 ln 2, ln 2, 0 -> weights
+    4/7, 2/7, 1/7; head 2 (q = (0, 1)): keys' second coordinates 0, 0, 1 ->
+    logits 0, 0, ln 2 -> weights 1/4, 1/4, 1/2.  Keys are the values."""
+    tau = math.log(2.0)
+    q = np.array([[2.0, 0.0], [0.0, 1.0]])
+    keys = np.array([[1.0, 0.0], [0.5, 0.0], [0.0, 1.0]])
+    o, lse = A.shared_kv_attention(q, keys, tau)
+    exp1 = (4 * keys[0] + 2 * keys[1] + 1 * keys[2]) / 7     # (5/7, 1/7)
+    exp2 = (1 * keys[0] + 1 * keys[1] + 2 * keys[2]) / 4     # (3/8, 1/2)
+    assert np.allclose(o[0], [5 / 7, 1 / 7], atol=1e-15) and np.allclose(o[0], exp1, atol=1e-15)
+    assert np.allclose(o[1], [3 / 8, 1 / 2], atol=1e-15) and np.allclose(o[1], exp2, atol=1e-15)
+    assert np.allclose(lse, [math.log(7.0), math.log(4.0)], atol=1e-15)
+
+
+def test_inverse_rope_of_a_hand_output():
+    """Rope dims 2 (one pair), theta irrelevant for pair 0 (frequency 1): at
+    position m = 1 the angle is 1 rad, so R_1^{-1} (cos 1, sin 1) = (1, 0) and
+    the non-rope dims are untouched."""
+    o = np.array([[7.0, math.cos(1.0), math.sin(1.0)]])
+    r = A.inverse_rope(o, 1, 2, 10000.0)
+    assert np.allclose(r, [[7.0, 1.0, 0.0]], atol=1e-15)
