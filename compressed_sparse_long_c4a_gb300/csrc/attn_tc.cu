@@ -484,10 +484,17 @@ bool handled(const v4a_attn_args* a) {
   const int D = a->kv.dim;
   if (D != 128 && D != 256 && D != 512) return false;
   if (a->num_heads > kRows) return false;
-  const int64_t ctas = int64_t(a->batch.num_tokens) * splits_of(a);
-  if (ctas > 16 * 152) return false;
   if (splits_of(a) > kCombGroups * kCombMax) return false;   // the combine holds at most 64 splits
   return true;
+}
+
+// Queries per launch: long batches (chunked prefill) run as several launches
+// of at most kMaxBatchCtas CTAs, each reusing the same chunk-result workspace.
+constexpr int64_t kMaxBatchCtas = 64 * 152;
+int64_t batch_queries(const v4a_attn_args* a) {
+  const int64_t T = a->batch.num_tokens, S = splits_of(a);
+  const int64_t q = kMaxBatchCtas / S;
+  return q < 1 ? 1 : (q < T ? q : T);
 }
 
 // 2-D bf16 tensor map [rows][D] with boxes of 64 columns x box_rows rows, 128-B swizzle.
@@ -507,17 +514,30 @@ bool encode_rows(CUtensorMap* map, const void* base, int64_t rows, int D, int bo
 
 size_t attn_tc_workspace_size(const v4a_attn_args* a) {
   if (!handled(a)) return 0;
-  const size_t T = a->batch.num_tokens, S = splits_of(a), H = a->num_heads, D = a->kv.dim;
+  const size_t T = size_t(batch_queries(a)), S = splits_of(a), H = a->num_heads, D = a->kv.dim;
   return T * S * H * D * 2 + T * S * H * 2 * 4 + 512;
 }
 
+int attn_tc_batch_queries(const v4a_attn_args* a) { return handled(a) ? int(batch_queries(a)) : 0; }
+
 bool attn_tc(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t stream, int* rc,
-             AttnPartials* keep) {
+             AttnPartials* keep, int t0, int tn) {
   *rc = V4A_OK;
   if (!handled(a)) return false;
   if (ws_bytes < attn_tc_workspace_size(a)) { *rc = V4A_ERR_WORKSPACE; return true; }
+  const int Tall = a->batch.num_tokens, Tb = int(batch_queries(a));
+  if (tn < 0) {
+    // the whole batch: with the merge inside, launch batch after batch here;
+    // a caller that merges itself (keep) walks the batches and passes each one
+    if (keep && Tall > Tb) { *rc = V4A_ERR_INVALID_ARG; return true; }
+    for (int b0 = 0; b0 < Tall && *rc == V4A_OK; b0 += Tb)
+      attn_tc(a, ws, ws_bytes, stream, rc, keep, b0, Tall - b0 < Tb ? Tall - b0 : Tb);
+    return true;
+  }
+  if (t0 < 0 || tn < 1 || tn > Tb || t0 + tn > Tall) { *rc = V4A_ERR_INVALID_ARG; return true; }
+  const int64_t qrow = int64_t(t0) * a->num_heads;     // first query row of this launch
   AtcArgs t{};
-  t.T = a->batch.num_tokens;
+  t.T = tn;
   t.H = a->num_heads;
   t.D = a->kv.dim;
   t.ratio = a->kv.ratio;
@@ -527,20 +547,20 @@ bool attn_tc(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t str
   t.wcap = a->window_cap;
   t.k = a->k;
   t.splits = splits_of(a);
-  t.seq_ids = a->batch.seq_ids;
-  t.positions = a->batch.positions;
+  t.seq_ids = a->batch.seq_ids + t0;
+  t.positions = a->batch.positions + t0;
   t.bt = a->kv.block_table;
   t.max_blocks = a->kv.max_blocks;
   t.num_blocks = a->kv.num_blocks;
   t.pool = static_cast<const uint8_t*>(a->kv.pool);
   t.block_bytes = kv_block_bytes(a->kv.format, a->kv.ratio, a->kv.dim);
-  t.idx = a->idx;
+  t.idx = a->idx ? a->idx + int64_t(t0) * a->k : nullptr;
   t.window = static_cast<const uint8_t*>(a->window);
   t.wscale = a->window_scale;
-  t.q = a->q;
+  t.q = a->q + qrow * a->kv.dim;
   t.scale = a->softmax_scale;
-  t.out = a->out;
-  t.lse = a->lse;
+  t.out = a->out ? a->out + qrow * a->kv.dim : nullptr;
+  t.lse = a->lse ? a->lse + qrow : nullptr;
   const size_t T = t.T, S = t.splits, H = t.H, D = t.D;
   t.part_o = static_cast<uint16_t*>(ws);
   t.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + ((T * S * H * D * 2 + 255) & ~size_t(255)));
@@ -551,11 +571,11 @@ bool attn_tc(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t str
   t.idesc_pv = tc::make_idesc(1, 1, kRows, D > 256 ? 256 : D) | (1u << 16);   // B is MN-major
   // Q as a 2-D tensor [T*H rows][D] bf16, boxes of 64 columns x 128 rows, 128-B swizzle
   CUtensorMap qmap, omap;
-  if (!encode_rows(&qmap, a->q, int64_t(T) * H, int(D), kRows)) return false;
+  if (!encode_rows(&qmap, t.q, int64_t(T) * H, int(D), kRows)) { *rc = V4A_ERR_CUDA; return true; }
   // output rows leave through a tensor map when whole boxes of H rows fit the swizzle atom
-  t.tma_out = (H % 8 == 0) && (reinterpret_cast<uintptr_t>(t.direct ? static_cast<void*>(a->out) : ws) & 15) == 0;
+  t.tma_out = (H % 8 == 0) && (reinterpret_cast<uintptr_t>(t.direct ? static_cast<void*>(t.out) : ws) & 15) == 0;
   if (t.tma_out) {
-    const void* dst = t.direct ? static_cast<const void*>(a->out) : static_cast<const void*>(t.part_o);
+    const void* dst = t.direct ? static_cast<const void*>(t.out) : static_cast<const void*>(t.part_o);
     const int64_t rows = t.direct ? int64_t(T) * H : int64_t(T) * S * H;
     if (!encode_rows(&omap, dst, rows, int(D), int(H))) t.tma_out = 0;
   }
@@ -568,7 +588,7 @@ bool attn_tc(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t str
   std::call_once(once, [] {
     cudaFuncSetAttribute(attn_chunk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   });
-  if (smem > 227 * 1024) return false;
+  if (smem > 227 * 1024) { *rc = V4A_ERR_UNSUPPORTED; return true; }
   // both may start while the kernel before them runs (they wait in-kernel)
   cudaError_t e = launch_pdl(attn_chunk_tc, dim3(t.splits, t.T), dim3(kThreads), smem, stream, t, qmap, omap);
   if (e == cudaSuccess && !t.direct && !keep)

@@ -19,6 +19,13 @@ struct AttnPartials {
 // otherwise, launching nothing); *rc is the call's result code.  With `keep`
 // the chunk results stay in the workspace (described in *keep) and no merge
 // kernel runs: the caller merges them.
+//
+// Long batches run as several launches of attn_tc_batch_queries(a) queries
+// each, sharing the workspace.  With tn < 0 the call covers every query (with
+// `keep`, only when they fit one launch); otherwise it covers queries
+// [t0, t0 + tn), tn <= attn_tc_batch_queries(a), and a caller that merges the
+// chunk results itself walks the launches one by one.
 bool attn_tc(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t stream, int* rc,
-             AttnPartials* keep = nullptr);
+             AttnPartials* keep = nullptr, int t0 = 0, int tn = -1);
+int attn_tc_batch_queries(const v4a_attn_args* a);   // 0 when not handled
 }  // namespace v4a

@@ -367,29 +367,39 @@ int sparse_attn_out(const v4a_attn_args* at, const v4a_output_args* a, void* ws,
   rc = validate_attn(at);
   if (rc) return rc;
   if (a->num_tokens == 0) return V4A_OK;
-  AttnPartials p{};
-  if (!attn_tc(at, ws, ws_bytes, stream, &rc, &p)) return V4A_ERR_UNSUPPORTED;
-  if (rc) return rc;
-  if (p.splits > kMergeMaxSplits) return V4A_ERR_UNSUPPORTED;
-  MergeDev d;
-  d.rope = make_rope_freq(a->rope_dims, a->rope_theta);
-  d.T = a->num_tokens; d.H = a->num_heads; d.D = a->dim; d.R = a->rope_dims; d.fmt = a->out_format;
-  d.splits = p.splits; d.positions = a->positions; d.part_o = p.o; d.part_ml = p.ml;
-  d.out = a->out; d.out_scale = a->out_scale;
-  cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(unsigned(a->num_tokens * csize));
-  lc.blockDim = dim3(kMergeThreads);
-  lc.stream = stream;
-  cudaLaunchAttribute la[2];
-  la[0].id = cudaLaunchAttributeClusterDimension;
-  la[0].val.clusterDim.x = unsigned(csize);
-  la[0].val.clusterDim.y = 1;
-  la[0].val.clusterDim.z = 1;
-  la[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  la[1].val.programmaticStreamSerializationAllowed = 1;
-  lc.attrs = la;
-  lc.numAttrs = 2;
-  if (cudaLaunchKernelEx(&lc, merge_out_kernel, d) != cudaSuccess) return V4A_ERR_CUDA;
+  // one attention launch and one merge launch per group of queries (long
+  // chunked-prefill batches take several, sharing the workspace)
+  const int Tb = attn_tc_batch_queries(at);
+  if (Tb == 0) return V4A_ERR_UNSUPPORTED;
+  RopeFreq rope = make_rope_freq(a->rope_dims, a->rope_theta);
+  const size_t out_elem = a->out_format == V4A_OUT_BF16 ? 2 : 1;
+  for (int t0 = 0; t0 < a->num_tokens; t0 += Tb) {
+    const int tn = a->num_tokens - t0 < Tb ? a->num_tokens - t0 : Tb;
+    AttnPartials p{};
+    if (!attn_tc(at, ws, ws_bytes, stream, &rc, &p, t0, tn)) return V4A_ERR_UNSUPPORTED;
+    if (rc) return rc;
+    if (p.splits > kMergeMaxSplits) return V4A_ERR_UNSUPPORTED;
+    MergeDev d;
+    d.rope = rope;
+    d.T = tn; d.H = a->num_heads; d.D = a->dim; d.R = a->rope_dims; d.fmt = a->out_format;
+    d.splits = p.splits; d.positions = a->positions + t0; d.part_o = p.o; d.part_ml = p.ml;
+    d.out = static_cast<uint8_t*>(a->out) + size_t(t0) * a->num_heads * a->dim * out_elem;
+    d.out_scale = a->out_scale ? a->out_scale + t0 : nullptr;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(unsigned(tn * csize));
+    lc.blockDim = dim3(kMergeThreads);
+    lc.stream = stream;
+    cudaLaunchAttribute la[2];
+    la[0].id = cudaLaunchAttributeClusterDimension;
+    la[0].val.clusterDim.x = unsigned(csize);
+    la[0].val.clusterDim.y = 1;
+    la[0].val.clusterDim.z = 1;
+    la[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    la[1].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = la;
+    lc.numAttrs = 2;
+    if (cudaLaunchKernelEx(&lc, merge_out_kernel, d) != cudaSuccess) return V4A_ERR_CUDA;
+  }
   return cudaGetLastError() == cudaSuccess ? V4A_OK : V4A_ERR_CUDA;
 }
 

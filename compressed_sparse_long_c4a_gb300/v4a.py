@@ -327,9 +327,16 @@ class Step:
         if s.ix_heads:
             tc_scan = s.ix_fmt in (IX_FP8_B128, IX_FP4_B32) and s.ix_heads == 64 and s.ix_dim == 128
             n += 2 + (1 if s.max_blocks * 64 <= 32768 or tc_scan else 2)
+        # the tensor-core attention runs long batches (chunked prefill) as
+        # several launches of at most 64 waves of 152 CTAs, one CTA per
+        # 64-key chunk of a query's list
+        nsel = s.topk if s.ix_heads else s.max_blocks * (256 // s.ratio)
+        chunks = -(-(nsel + s.swa) // 64)
+        per = max(1, min(s.tokens, (64 * 152) // chunks))
+        batches = -(-s.tokens // per)
         if self.fused_out:
-            return n + 2                      # attention + merge/output kernel
-        n += 1 + (1 if self.ws_attn.numel() > 256 else 0)
+            return n + 2 * batches            # attention + merge/output kernel per batch
+        n += batches * (1 + (1 if chunks > 1 else 0))
         return n + 1
 
     def run(self, stream=None):
