@@ -259,7 +259,10 @@ typedef struct {
   int32_t* status;
 } v4a_attn_args;
 
-/* Bytes of device workspace v4a_sparse_attn needs (split partials; 0 on a bad shape). */
+/* Bytes of device workspace v4a_sparse_attn needs: the per-chunk results of
+ * the queries of one launch (long batches such as chunked prefill run as
+ * several launches that reuse it, in stream order); 0 on a bad shape.
+ * Caller-owned; its contents need no initialisation. */
 V4A_API size_t v4a_attn_workspace_size(const v4a_attn_args* args);
 V4A_API int v4a_sparse_attn(const v4a_attn_args* args, void* workspace, size_t workspace_bytes,
                     void* stream);
