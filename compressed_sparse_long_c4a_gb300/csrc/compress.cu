@@ -143,7 +143,7 @@ __device__ void compress_token(const CompressSide& c, const BatchDev& bt, int t,
   const int W = c.ratio == 4 ? 8 : 128;
   const int p0 = c.ratio == 4 ? 4 * i - 4 : 128 * i;
 
-  // ---- round 1: independent loads ----
+  // ---- phase 1: independent loads ----
   const uint32_t* xin = reinterpret_cast<const uint32_t*>(c.x + int64_t(t) * c.dim);
   const uint32_t xv = own ? xin[p] : 0u;
   const float gt = p == 0 ? c.gate[t] : 0.f;
@@ -200,7 +200,7 @@ __device__ void compress_token(const CompressSide& c, const BatchDev& bt, int t,
     __syncthreads();
   }
 
-  // ---- round 2: weighted sum of the window rows (pair per thread) ----
+  // ---- phase 2: weighted sum of the window rows (pair per thread) ----
   float a0 = 0.f, a1 = 0.f;
   if (own) {
     for (int j0 = 0; j0 < W; j0 += 8) {
