@@ -201,17 +201,21 @@ __device__ void compress_token(const CompressSide& c, const BatchDev& bt, int t,
   }
 
   // ---- phase 2: weighted sum of the window rows (pair per thread) ----
+  // 32 rows' loads in flight per batch (a 128-token window takes 4 round
+  // trips, not 16); the sum runs over the rows in window order either way
+  constexpr int kRowsInFlight = 32;
   float a0 = 0.f, a1 = 0.f;
   if (own) {
-    for (int j0 = 0; j0 < W; j0 += 8) {
-      uint32_t v[8];
+    for (int j0 = 0; j0 < W; j0 += kRowsInFlight) {
+      uint32_t v[kRowsInFlight];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const uint16_t* row = src_s[j0 + u];
+      for (int u = 0; u < kRowsInFlight; ++u) {
+        const uint16_t* row = j0 + u < W ? src_s[j0 + u] : nullptr;
         v[u] = row ? reinterpret_cast<const uint32_t*>(row)[p] : 0u;
       }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < kRowsInFlight; ++u) {
+        if (j0 + u >= W) break;
         const float wj = w_s[j0 + u];
         a0 = fmaf(wj, bf16_to_f32(uint16_t(v[u] & 0xffffu)), a0);
         a1 = fmaf(wj, bf16_to_f32(uint16_t(v[u] >> 16)), a1);
