@@ -60,6 +60,24 @@ def algorithmic_bytes(spec):
     return scan, gather, win
 
 
+def default_replicas(spec) -> int:
+    """Layer replicas the timed steps rotate over: enough distinct caches that
+    the bytes a step touches never come from L2."""
+    scan_b, gather_b, win_b = algorithmic_bytes(spec)
+    return max(2, math.ceil(2 * L2_BYTES / max(scan_b + gather_b + win_b, 1)) + 1)
+
+
+def workload_config(spec, replicas: int, world_size: int) -> dict:
+    """The `config` object of the JSON line (the same for both arms)."""
+    step_bytes = sum(algorithmic_bytes(spec))
+    return {"workload": spec.name, "batch": spec.batch, "context": spec.cached[0] + 1,
+            "visible_entries": (spec.cached[0] + 1) // spec.ratio, "heads": spec.heads,
+            "dim": spec.dim, "topk": spec.topk, "indexer": f"{spec.ix_heads}x{spec.ix_dim}",
+            "parallelism": f"replicas x{world_size}" if world_size > 1 else "single GPU",
+            "l2": f"rotates over {replicas} layer replicas ({replicas * step_bytes / 2**20:.0f} MiB "
+                  f"touched per rotation > 2x L2)", "cuda_graph": True}
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle samples during the timed region."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -202,8 +220,7 @@ def run_reference(args, spec, case):
             "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
             "impl": "reference",
-            "config": {"workload": spec.name, "batch": spec.batch, "context": spec.cached[0] + 1,
-                       "heads": spec.heads, "dim": spec.dim, "topk": spec.topk},
+            "config": workload_config(spec, args.replicas or default_replicas(spec), ws),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -250,9 +267,7 @@ def main():
 
     scan_b, gather_b, win_b = algorithmic_bytes(spec)
     step_bytes = scan_b + gather_b + win_b
-    replicas = max(2, math.ceil(2 * L2_BYTES / max(step_bytes, 1)) + 1)
-    if args.replicas > 0:
-        replicas = args.replicas
+    replicas = args.replicas if args.replicas > 0 else default_replicas(spec)
     layers = [v4a.DeviceLayer.from_case(case, dev) for _ in range(replicas)]
     steps = [v4a.Step(L) for L in layers]
     stream = torch.cuda.Stream(device=dev)
@@ -390,12 +405,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms, "us_per_layer": ms * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp8/fp4 caches, fp32 accumulate",
         "data": "synthetic (seeded)",
-        "config": {"workload": spec.name, "batch": spec.batch, "context": spec.cached[0] + 1,
-                   "visible_entries": (spec.cached[0] + 1) // spec.ratio, "heads": spec.heads,
-                   "dim": spec.dim, "topk": spec.topk, "indexer": f"{spec.ix_heads}x{spec.ix_dim}",
-                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                   "l2": f"rotates over {replicas} layer replicas ({replicas * step_bytes / 2**20:.0f} MiB "
-                         f"touched per rotation > 2x L2)", "cuda_graph": True},
+        "config": workload_config(spec, replicas, ws),
         "roofline": roof,
         "step_hbm_frac": step_bytes / (ms * 1e-3) / 1e9 / hbm_peak,
         "stage_us": stage_us, "dominant_stage": dominant,
