@@ -140,3 +140,26 @@ def test_host_validation_of_fused_attention_output(lib):
     o.out_format = spec.out_fmt
     o.out_scale = None                                                    # fp8 output needs its scales
     assert lib.v4a_sparse_attn_out(C.byref(a), C.byref(o), 0x1000, 1 << 30, None) == 1
+
+
+def test_attention_workspace_covers_one_launch_of_a_long_batch(lib):
+    """Chunked prefill (16,384 queries, 10 key chunks each) runs as several
+    launches that reuse one launch's worth of chunk results: the workspace is
+    sized for at most 64 waves of 152 CTAs, not for the whole batch."""
+    spec = I.c4a_prefill_4x4k()
+    L = _FakeLayer(spec)
+    a = v4a.AttnArgs(L.batch(), L.kv_cache(), 0x10, spec.topk, 0x20, 0x30, spec.swa_cap, spec.swa_fmt,
+                     spec.swa, spec.heads, 0x40, 0.04, 0x50, None, None)
+    need = lib.v4a_attn_workspace_size(C.byref(a))
+    chunks = -(-(spec.topk + spec.swa) // 64)
+    per_launch = (64 * 152) // chunks
+    row = chunks * spec.heads * (spec.dim * 2 + 8)          # bf16 row + (max, sum) per chunk and head
+    assert spec.tokens > per_launch                          # the batch needs several launches
+    assert per_launch * row <= need < 2 * per_launch * row
+    # a decode batch fits one launch: its workspace covers every query
+    d = I.c4a_decode_1m()
+    Ld = _FakeLayer(d)
+    ad = v4a.AttnArgs(Ld.batch(), Ld.kv_cache(), 0x10, d.topk, 0x20, 0x30, d.swa_cap, d.swa_fmt,
+                      d.swa, d.heads, 0x40, 0.04, 0x50, None, None)
+    dchunks = -(-(d.topk + d.swa) // 64)
+    assert lib.v4a_attn_workspace_size(C.byref(ad)) >= d.tokens * dchunks * d.heads * (d.dim * 2 + 8)
