@@ -14,7 +14,9 @@ silent.
 
 Pinning status (what each part is checked against, in ``tests/``):
   formats     - exhaustive codec checks against torch.float8_e4m3fn and the
-                OCP e2m1 value table; bf16 against torch.bfloat16.
+                OCP e2m1 value table; bf16 against torch.bfloat16; the MX
+                power-of-two block scale by hand-worked blocks and its
+                error bound.
   geometry    - closed forms for counts/windows/causality, brute-force
                 enumeration of slot mapping.
   compressor  - closed forms (equal logits -> mean, dominant logit -> copy,
@@ -25,6 +27,10 @@ Pinning status (what each part is checked against, in ``tests/``):
                 keys, log-sum-exp), dense special case against torch fp64
                 softmax + matmul, SWA coverage, translation invariance after
                 inverse RoPE, a hand-worked inverse rotation.
+  layer       - window keys rotated at their own positions (hand cos/sin
+                values) and translation invariance of the whole chain
+                (compress, window keys, attention, inverse RoPE) under a
+                shift of every position by a multiple of 256.
   kvbytes     - the page's 9.62 GiB / 83.9 GiB / 8.7x figures.
   The page prints no worked numerical example; the hand examples above are
   computed from the definitions, not by this package.

@@ -19,6 +19,13 @@ Sources and readings
   e2m1 (values 0, .5, 1, 1.5, 2, 3, 4, 6), round-to-nearest-even, saturating to
   +-6, one fp32 scale per 32 elements = amax/6 (1 when amax == 0); element 2j
   in the low nibble and 2j+1 in the high nibble of byte j.
+* fp4 indexer cache with power-of-two block scales (the same bytes; reading
+  of the summary article's remark that the indexer "computes in true FP4": a
+  native fp4 tensor-core product scales each 32-element block by a power of
+  two, the OCP Microscaling (MX) v1.0 convention for e2m1 with an E8M0 shared
+  scale).  The scale is chosen by the MX conversion rule,
+  X = 2^(floor(log2 amax) - 2), written into the fp32 scale word; codes are
+  e2m1 of v / X (nearest-even, saturating to +-6).
 * Block layout (vLLM page, "A single logical block size": every compressed
   layer's logical block is 256 native positions, so a c4a block holds 64
   entries and a c128a block 2).  Reading taken for the bytes inside one
@@ -188,6 +195,36 @@ def fp4_blocks_encode(v: np.ndarray, block: int = 32):
     return pack_nibbles(nib), scales
 
 
+def mx_shared_scale(block: np.ndarray, emax_elem: int = 2) -> float:
+    """Shared power-of-two scale of one block under the OCP Microscaling (MX)
+    rule: X = 2^(floor(log2(amax)) - emax_elem), emax_elem = 2 for e2m1 (its
+    largest power of two is 4).  amax = 0 gives 1 (the convention of the other
+    scaled formats here).  The exponent is clamped to the normal fp32 range
+    [-126, 127] because the scale is stored as an fp32 word."""
+    amax = float(np.max(np.abs(block))) if block.size else 0.0
+    if amax == 0.0:
+        return 1.0
+    _, e = np.frexp(amax)            # amax = f * 2^e, f in [0.5, 1)  ->  floor(log2 amax) = e - 1
+    x = int(e) - 1 - emax_elem
+    return float(np.ldexp(1.0, min(max(x, -126), 127)))
+
+
+def fp4_mx_blocks_encode(v: np.ndarray, block: int = 32):
+    """Per-32-element fp4 quantisation with OCP MX shared scales -> (packed
+    bytes, scales).  v / X lies in [4, 8) for the block's largest element, so
+    e2m1's saturation to +-6 clips what lies above 6 (as the MX conversion
+    prescribes); every scale is an exact power of two."""
+    n = v.shape[-1] // block
+    nib = np.empty(v.shape[-1], np.uint8)
+    scales = np.empty(n, np.float64)
+    for b in range(n):
+        seg = v[b * block:(b + 1) * block]
+        s = mx_shared_scale(seg)
+        nib[b * block:(b + 1) * block] = e2m1_encode(seg / s)
+        scales[b] = s
+    return pack_nibbles(nib), scales
+
+
 def pack_nibbles(nib: np.ndarray) -> np.ndarray:
     nib = np.asarray(nib, np.uint8)
     return (nib[..., 0::2] | (nib[..., 1::2] << 4)).astype(np.uint8)
@@ -205,7 +242,10 @@ def unpack_nibbles(packed: np.ndarray) -> np.ndarray:
 # --------------------------------------------------------------------------
 
 KV_BF16, KV_FP8_TOKEN = 0, 1
-IX_BF16, IX_FP8_B128, IX_FP4_B32 = 0, 1, 2
+# IX_FP4_MX32: the IX_FP4_B32 byte layout with every scale a power of two
+# chosen by the OCP MX rule (mx_shared_scale).
+IX_BF16, IX_FP8_B128, IX_FP4_B32, IX_FP4_MX32 = 0, 1, 2, 3
+FP4_FORMATS = (IX_FP4_B32, IX_FP4_MX32)
 
 
 def kv_block_bytes(fmt: int, entries: int, dim: int) -> int:
@@ -223,7 +263,7 @@ def ix_block_bytes(fmt: int, dim: int, entries: int = 64) -> int:
         return entries * dim * 2
     if fmt == IX_FP8_B128:
         return entries * dim + entries * (dim // 128) * 4
-    if fmt == IX_FP4_B32:
+    if fmt in FP4_FORMATS:
         return entries * dim // 2 + entries * (dim // 32) * 4
     raise ValueError(fmt)
 
@@ -255,7 +295,7 @@ def ix_block_decode(raw: np.ndarray, fmt: int, dim: int, entries: int = 64) -> n
         sc = raw[..., entries * dim:entries * dim + 4 * entries * nb].copy().view(np.float32)
         sc = sc.astype(np.float64).reshape(lead + (entries, nb))
         return e4m3_decode(codes) * np.repeat(sc, 128, axis=-1)
-    if fmt == IX_FP4_B32:
+    if fmt in FP4_FORMATS:
         nb = dim // 32
         packed = raw[..., :entries * dim // 2].reshape(lead + (entries, dim // 2))
         sc = raw[..., entries * dim // 2:entries * dim // 2 + 4 * entries * nb].copy().view(np.float32)

@@ -101,6 +101,8 @@ def encode_ix_row(v: np.ndarray, fmt: int):
         return F.bf16_encode(v).view(np.uint8), None
     if fmt == F.IX_FP8_B128:
         return F.fp8_blocks_encode(v, 128)
+    if fmt == F.IX_FP4_MX32:
+        return F.fp4_mx_blocks_encode(v, 32)
     return F.fp4_blocks_encode(v, 32)
 
 

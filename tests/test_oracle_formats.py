@@ -154,3 +154,54 @@ def test_kv_fp8_and_ix_fp4_block_decode_apply_scales():
     raw[64 * 64:] = s4.reshape(-1).view(np.uint8)
     dec = F.ix_block_decode(raw, F.IX_FP4_B32, dI)
     assert dec[3, 41] == 3.0 and np.count_nonzero(dec) == 1
+
+
+def test_mx_shared_scale_rule_hand_worked():
+    # OCP MX rule: X = 2^(floor(log2 amax) - 2) for e2m1 (emax_elem = 2)
+    assert F.mx_shared_scale(np.array([5.0, -0.7, 0.3])) == 1.0          # floor(log2 5) = 2
+    assert F.mx_shared_scale(np.array([-4.0, 1.0])) == 1.0              # exact power of two: 2 - 2 = 0
+    assert F.mx_shared_scale(np.array([3.99, 0.0])) == 0.5              # floor(log2 3.99) = 1
+    assert F.mx_shared_scale(np.array([0.2, -0.1])) == 2.0 ** -5        # floor(log2 0.2) = -3
+    assert F.mx_shared_scale(np.array([1000.0])) == 2.0 ** 7            # floor(log2 1000) = 9
+    assert F.mx_shared_scale(np.zeros(32)) == 1.0
+    assert F.mx_shared_scale(np.array([1e-45])) == 2.0 ** -126          # clamped to a normal fp32 word
+
+
+def test_fp4_mx_block_hand_worked_codes():
+    v = np.zeros(32)
+    v[:6] = [5.0, -0.7, 0.3, 7.5, 6.0, -2.6]
+    packed, sc = F.fp4_mx_blocks_encode(v)
+    assert sc.tolist() == [1.0]                                            # amax 7.5 -> floor(log2) = 2
+    nib = F.unpack_nibbles(packed)
+    # 5.0 is the midpoint of 4 and 6 -> even code (4); -0.7 -> -0.5; 0.3 -> 0.5;
+    # 7.5 saturates to 6; 6 stays; -2.6 -> -3 (nearest)
+    assert F.e2m1_decode(nib[:6]).tolist() == [4.0, -0.5, 0.5, 6.0, 6.0, -3.0]
+    assert nib[:6].tolist() == [0x6, 0x9, 0x1, 0x7, 0x7, 0xD]
+    assert not np.any(nib[6:])
+
+
+def test_fp4_mx_scales_are_powers_of_two_and_error_bounded():
+    rng = np.random.default_rng(11)
+    for _ in range(300):
+        v = rng.standard_normal(128) * 10.0 ** rng.uniform(-4, 4)
+        packed, sc = F.fp4_mx_blocks_encode(v)
+        m, e = np.frexp(sc)
+        assert np.all(m == 0.5), "every MX scale is an exact power of two"
+        dec = F.e2m1_decode(F.unpack_nibbles(packed)) * np.repeat(sc, 32)
+        for b in range(4):
+            seg, d = v[32 * b:32 * b + 32], dec[32 * b:32 * b + 32]
+            amax = np.abs(seg).max()
+            assert 4.0 <= amax / sc[b] < 8.0
+            # inside the e2m1 range the error is at most half a step of the grid
+            # at that magnitude; above 6 * X the value clips to 6 * X
+            inside = np.abs(seg) <= 6.0 * sc[b]
+            assert np.all(np.abs(seg - d)[inside] <= F.e2m1_ulp(seg[inside] / sc[b]) * sc[b] / 2 + 1e-300)
+            assert np.all(np.abs(d[~inside]) == 6.0 * sc[b])
+
+
+def test_fp4_mx_layout_equals_fp4_layout():
+    assert F.ix_block_bytes(F.IX_FP4_MX32, 128) == F.ix_block_bytes(F.IX_FP4_B32, 128) == 64 * 80
+    rng = np.random.default_rng(2)
+    raw = rng.integers(0, 256, F.ix_block_bytes(F.IX_FP4_B32, 128), dtype=np.uint8)
+    raw[64 * 64:] = np.ldexp(1.0, rng.integers(-5, 5, 64 * 4)).astype(np.float32).view(np.uint8)
+    assert np.array_equal(F.ix_block_decode(raw, F.IX_FP4_MX32, 128), F.ix_block_decode(raw, F.IX_FP4_B32, 128))

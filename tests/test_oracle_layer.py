@@ -103,3 +103,74 @@ def test_generator_structure():
     bt = case.block_table
     used = bt[bt >= 0]
     assert used.unique().numel() == used.numel()
+
+
+# --------------------------------------------------------------------------
+# Window keys: rotated at their own positions
+# --------------------------------------------------------------------------
+
+def test_window_key_rotated_at_its_own_position_hand_values():
+    """One key per position, a unit vector on a rope pair: the stored key is
+    that pair rotated by exactly (position x the pair's frequency).  With
+    rope_dims = 4 the pairs are (4, 5) at frequency 1 and (6, 7) at frequency
+    10000^(-1/2) = 0.01.  cos/sin values from a table."""
+    k = np.zeros((2, 8))
+    k[0, 4] = k[1, 4] = 1.0
+    out = L.window_keys(np.array([0, 0]), np.array([2, 3]), F.bf16_encode(k), 4, 10000.0)
+    cos2, sin2 = -0.4161468365471424, 0.9092974268256817
+    cos3, sin3 = -0.9899924966004454, 0.1411200080598672
+    cos003, sin003 = 0.9995500337489875, 0.02999550020249566
+    # two tokens of one call: each rotated at its own position, not the call's first or last
+    assert np.allclose(out[(0, 2)], [0, 0, 0, 0, cos2, sin2, 0, 0], atol=1e-15)
+    assert np.allclose(out[(0, 3)], [0, 0, 0, 0, cos3, sin3, 0, 0], atol=1e-15)
+    k2 = np.zeros((2, 8))
+    k2[0, 4] = 1.0
+    k2[1, 6] = 1.0
+    out2 = L.window_keys(np.array([0, 1]), np.array([3, 3]), F.bf16_encode(k2), 4, 10000.0)
+    assert np.allclose(out2[(0, 3)], [0, 0, 0, 0, cos3, sin3, 0, 0], atol=1e-15)
+    assert np.allclose(out2[(1, 3)], [0, 0, 0, 0, 0, 0, cos003, sin003], atol=1e-15)
+
+
+def _window_chain(delta: int):
+    """The oracle's chain for the last query of one call of 160 tokens at
+    positions 256 + delta ..: the call's compressed entries (compress) and
+    window keys (window_keys) as keys, fp64 attention, inverse RoPE.  Every
+    random draw is independent of delta."""
+    from oracle import attention as A
+    from oracle import compressor as Cm
+    rng = np.random.default_rng(21)
+    D, R, th, H, n_new, P0 = 64, 32, 10000.0, 2, 160, 256
+    cap = 8 - 1 + n_new
+    x = F.bf16_encode(rng.standard_normal((n_new, D)))
+    g = rng.standard_normal(n_new)
+    bias, gamma = rng.normal(0, 0.5, 8), 1 + rng.normal(0, 0.1, D)
+    older, older_g = F.bf16_encode(rng.standard_normal((4, D))), rng.standard_normal(4)
+    kw = F.bf16_encode(rng.standard_normal((n_new, D)))
+    qt = rng.standard_normal((H, D))
+    ring_x, ring_g = np.zeros((1, cap, D), np.uint16), np.zeros((1, cap))
+    for j in range(4):                                   # positions 252 + delta .. 255 + delta
+        p = P0 + delta - 4 + j
+        ring_x[0, p % cap], ring_g[0, p % cap] = older[j], older_g[j]
+    comp = L.Compressor(4, D, R, th, bias, gamma, ring_x, ring_g)
+    pos = np.arange(P0 + delta, P0 + delta + n_new)
+    seq = np.zeros(n_new, int)
+    entries = L.compress(seq, pos, x, g, comp)
+    win = L.window_keys(seq, pos, kw, R, th)
+    m = int(pos[-1])
+    keys = [v for (_, i), v in sorted(entries.items()) if G.anchor(i, 4) <= m]
+    keys += [win[(0, p)] for p in G.swa_positions(m, 128)]
+    assert len(keys) == n_new // 4 + 128
+    o, _ = A.shared_kv_attention(Cm.rope(qt, m, R, th), np.stack(keys), 1 / math.sqrt(D))
+    return A.inverse_rope(o, m, R, th)
+
+
+def test_window_keys_translation_invariance_through_the_layer_chain(monkeypatch):
+    """Shifting every position of the call (query, compressed anchors, window
+    keys) by a multiple of 256 leaves R_m^{-1} o_m unchanged to fp64 round-off
+    ("DeepSeek V4 in vLLM", appendix "why inverse RoPE": the output depends on
+    relative positions only).  Negative control: window keys left unrotated."""
+    base = _window_chain(0)
+    for delta in (256, 768, 1 << 20):
+        assert np.allclose(_window_chain(delta), base, atol=1e-10)
+    monkeypatch.setattr(L, "rope", lambda v, pos, rope_dims, theta, inverse=False: v)
+    assert not np.allclose(_window_chain(768), _window_chain(0), atol=1e-3)
