@@ -95,12 +95,21 @@ __device__ void store_ix_row(int format, int dim, int p, bool own, float v0, flo
     return;
   }
   const float a = own ? fmaxf(fabsf(v0), fabsf(v1)) : 0.f;
-  if (format == V4A_IX_FP4_B32) {
+  if (ix_is_fp4(format)) {
     // 32 elements = 16 pairs = one half-warp
     float m = a;
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    const float s = m > 0.f ? m / 6.f : 1.f;
+    float s;
+    if (format == V4A_IX_FP4_B32) {
+      s = m > 0.f ? m / 6.f : 1.f;
+    } else {
+      // OCP MX shared scale: 2^(floor(log2 amax) - 2), 2 = the largest power
+      // of two of e2m1; exponent clamped to the normal fp32 range
+      const int e = int((__float_as_uint(m) >> 23) & 0xFFu) - 127;   // floor(log2 m) for normal m
+      const int x = min(max(e - 2, -126), 127);
+      s = m > 0.f ? __uint_as_float(uint32_t(x + 127) << 23) : 1.f;
+    }
     if (own) {
       const uint32_t c0 = f32_to_e2m1(v0 / s), c1 = f32_to_e2m1(v1 / s);
       row[p] = uint8_t(c0 | (c1 << 4));
@@ -319,7 +328,7 @@ static int fill_side(const v4a_compressor* c, bool indexer, CompressSide* s, int
   if (!indexer) {
     if (k.format != V4A_KV_BF16 && k.format != V4A_KV_FP8_TOKEN) return V4A_ERR_INVALID_ARG;
   } else {
-    if (k.format != V4A_IX_BF16 && k.format != V4A_IX_FP8_B128 && k.format != V4A_IX_FP4_B32)
+    if (k.format != V4A_IX_BF16 && k.format != V4A_IX_FP8_B128 && !ix_is_fp4(k.format))
       return V4A_ERR_INVALID_ARG;
     if (k.format == V4A_IX_FP8_B128 && k.dim % 128) return V4A_ERR_UNSUPPORTED;
   }

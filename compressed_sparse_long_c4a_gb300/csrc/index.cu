@@ -821,7 +821,7 @@ static int validate_shape(const v4a_index_args* a) {
   if (c.dim < 32 || c.dim > 256 || c.dim % 32) return V4A_ERR_UNSUPPORTED;
   if (c.format == V4A_IX_BF16) {
     if (a->q_format != V4A_Q_BF16) return V4A_ERR_UNSUPPORTED;
-  } else if (c.format == V4A_IX_FP8_B128 || c.format == V4A_IX_FP4_B32) {
+  } else if (c.format == V4A_IX_FP8_B128 || ix_is_fp4(c.format)) {
     if (a->q_format != V4A_Q_FP8_HEAD) return V4A_ERR_UNSUPPORTED;
     if (c.format == V4A_IX_FP8_B128 && c.dim % 128) return V4A_ERR_UNSUPPORTED;
   } else {
@@ -879,7 +879,9 @@ int index_scores(const v4a_index_args* a, void* ws, size_t ws_bytes, cudaStream_
     const unsigned blocks = unsigned(std::min<size_t>((words + 255) / 256, 1024));
     if (launch_pdl(clear_words, dim3(blocks), dim3(256), 0, stream, w.hist, words) != cudaSuccess) return V4A_ERR_CUDA;
   }
-  if (index_score_tc(a, w.scores, w.row, w.row > kSmemTopkMax ? w.hist : nullptr, stream, &rc)) return rc;
+  uint32_t* hist = w.row > kSmemTopkMax ? w.hist : nullptr;
+  if (index_score_mx(a, w.scores, w.row, hist, stream, &rc)) return rc;
+  if (index_score_tc(a, w.scores, w.row, hist, stream, &rc)) return rc;
   ScoreArgs sa;
   sa.T = T; sa.H = a->num_heads; sa.dim = c.dim; sa.k_fmt = c.format; sa.q_fmt = a->q_format;
   sa.seq_ids = a->batch.seq_ids; sa.positions = a->batch.positions; sa.keys = c;
@@ -909,8 +911,8 @@ int index_select(const v4a_index_args* a, void* ws, size_t ws_bytes, cudaStream_
                                          a->k, a->out_idx);
   } else {
     const int slices = int((w.row + kSlice - 1) / kSlice);
-    // the tensor-core scan already left the first-level histogram
-    if (!index_score_tc_supported(a))
+    // the tensor-core scans already left the first-level histogram
+    if (!index_score_mx_supported(a) && !index_score_tc_supported(a))
       topk_hist<<<dim3(slices, T), 512, 0, stream>>>(w.scores, w.row, a->keys.max_blocks * 64,
                                                      a->batch.positions, a->k, slices, w.hist);
     // all of a query's slices resolve together in one cooperative grid when

@@ -55,6 +55,7 @@
 #include <mutex>
 
 #include "index_tc.h"
+#include "scan_common.cuh"
 #include "tc_common.cuh"
 
 namespace v4a {
@@ -65,7 +66,7 @@ constexpr int kBoxBytes = 64 * 128;          // one block's codes as 64 operand 
 constexpr int kStageBytes = 2 * kBoxBytes;   // one MMA A operand: 128 rows x 128 smem bytes
 constexpr int kRing = 32;                    // per-tile block ids handed to the epilogue
 constexpr int kQBytes = 64 * 128;            // 64 heads x 128 codes
-constexpr int kHistBins = 4096;
+constexpr int kHistBins = scan::kHistBins;
 constexpr int kProd = 2;                     // producer warps (alternate tiles)
 constexpr int kQw = 1 + kProd;               // query-stager warp
 constexpr int kEpi0 = kQw + 1;               // first epilogue warp
@@ -110,105 +111,9 @@ struct Smem {
 
 constexpr size_t kFixedSmem = 1024 + 2 * kQBytes + 2 * kScSlots * kScSlot + kHistBins * 4 + sizeof(Smem);
 
-// Visible entries of query t, never beyond what its block-table row can address.
-__device__ __forceinline__ int visible_of(const TcArgs& a, int t) {
-  return min((a.positions[t] + 1) / 4, a.max_blocks * 64);
-}
-
-__device__ __forceinline__ int tiles_of(const TcArgs& a, int t) {
-  return (visible_of(a, t) + 127) / 128;
-}
-
-// Walks the flattened (query, tile) list; the tile count of the current query
-// is cached so the hot loop touches global memory only at query switches.
-struct Cursor {
-  int t, j, nt;
-  __device__ void init(const TcArgs& a, int t0, int j0) {
-    t = t0; j = j0; nt = t0 < a.T ? tiles_of(a, t0) : 0;
-  }
-  __device__ void next(const TcArgs& a) {
-    if (++j >= nt) {
-      j = 0;
-      do { ++t; nt = t < a.T ? tiles_of(a, t) : 0; } while (t < a.T && nt == 0);
-    }
-  }
-};
-
-// Contiguous share of the flattened (query, tile) list for this CTA.  Each
-// thread sums the tiles of a contiguous chunk of queries; the chunk holding
-// the CTA's first item is then walked by its owner.
-__device__ void plan(const TcArgs& a, Smem& s) {
-  const int per = (a.T + blockDim.x - 1) / blockDim.x;
-  const int c0 = threadIdx.x * per, c1 = min(a.T, c0 + per);
-  uint32_t mine = 0;
-  for (int t = c0; t < c1; ++t) mine += tiles_of(a, t);
-  // exclusive scan of `mine` over the block: warp shuffles, then warp totals
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
-  uint32_t incl = mine;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += x;
-  }
-  if (lane == 31) s.part[wid] = incl;
-  if (threadIdx.x == 0) { s.count = 0; s.t0 = a.T; s.j0 = 0; }
-  __syncthreads();
-  uint32_t before = incl - mine, all = 0;
-  for (int w = 0; w < nw; ++w) {
-    const uint32_t x = s.part[w];
-    if (w < wid) before += x;
-    all += x;
-  }
-  const uint32_t lo = uint32_t((uint64_t(all) * blockIdx.x) / gridDim.x);
-  const uint32_t hi = uint32_t((uint64_t(all) * (blockIdx.x + 1)) / gridDim.x);
-  if (hi > lo && lo >= before && lo < before + mine) {
-    uint32_t acc = before;
-    for (int t = c0; t < c1; ++t) {
-      const uint32_t n = tiles_of(a, t);
-      if (lo < acc + n) { s.t0 = t; s.j0 = int(lo - acc); break; }
-      acc += n;
-    }
-    s.count = int(hi - lo);
-  }
-  __syncthreads();
-}
-
-// Lane 0 waits for the phase (bounded) and the warp proceeds together; the
-// warp barrier orders the other lanes' reads after lane 0's observation.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int32_t* status, volatile int* abort_flag) {
-  bool ok = true;
-  if ((threadIdx.x & 31) == 0) ok = tc::mbar_wait(bar, parity, status, abort_flag);
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  __syncwarp();
-  return ok;
-}
-
-// Adds the shared-memory histogram of query t to its global row and clears it.
-// Called by all eight epilogue warps at the same item; they meet on two
-// mbarriers (bounded waits, so a warp that gave up elsewhere cannot hang the
-// others): every add of the old query is done before any bin is read, and
-// every bin is cleared before any add of the next query.
-__device__ __forceinline__ bool flush_hist(uint64_t* hsync, uint64_t* hclear, uint32_t& hph, uint32_t* h_s,
-                                           uint32_t* g, int et, int32_t* status, volatile int* abort_flag) {
-  const int lane = threadIdx.x & 31;
-  __syncwarp();
-  if (lane == 0) tc::mbar_arrive(hsync);
-  bool ok = __all_sync(0xffffffffu, tc::mbar_wait(hsync, hph, status, abort_flag));
-  if (ok) {
-    for (int i = et; i < kHistBins; i += 32 * kEpiWarps) {
-      const uint32_t v = h_s[i];
-      if (v) {
-        atomicAdd(&g[i], v);
-        h_s[i] = 0;
-      }
-    }
-  }
-  __syncwarp();
-  if (lane == 0) tc::mbar_arrive(hclear);
-  ok = __all_sync(0xffffffffu, ok && tc::mbar_wait(hclear, hph, status, abort_flag));
-  hph ^= 1;
-  return ok;
-}
+using scan::Cursor;
+using scan::visible_of;
+using scan::warp_wait;
 
 // Layout constants of one key format (64 heads x 128 dims; 64 entries per block).
 template <bool FP8>
@@ -259,7 +164,7 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const __
   __syncwarp();   // tcgen05.alloc is warp-collective
   if (warp == 0) tc::tmem_alloc(&s.tmem_base, 2 * F::kAccCols);
   tc::tc_fence_before();
-  plan(a, s);              // contains __syncthreads
+  scan::plan(a, s.part, &s.t0, &s.j0, &s.count);   // contains __syncthreads
   // the set-up above (inputs only) overlaps the previous kernels; the pool,
   // which they write, and the histogram, which they clear, are touched only
   // after they have completed
@@ -468,7 +373,7 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const __
         if (cur_t >= 0) {
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&s.qempty[qi & 1]);   // done with the old head weights
-          if (a.hist && !flush_hist(&s.hsync, &s.hclear, hph, hist_s, a.hist + int64_t(cur_t) * kHistBins, et,
+          if (a.hist && !scan::flush_hist<kEpiWarps>(&s.hsync, &s.hclear, hph, hist_s, a.hist + int64_t(cur_t) * kHistBins, et,
                                     a.status, abort_flag)) {
             aborted = true;
             break;
@@ -569,7 +474,7 @@ index_scan_tc(const TcArgs a, const __grid_constant__ CUtensorMap kmap, const __
     // the last query's counts (a warp that gave up skips this; the others'
     // bounded waits then see the abort flag)
     if (a.hist && cur_t >= 0 && !aborted)
-      flush_hist(&s.hsync, &s.hclear, hph, hist_s, a.hist + int64_t(cur_t) * kHistBins, et, a.status, abort_flag);
+      scan::flush_hist<kEpiWarps>(&s.hsync, &s.hclear, hph, hist_s, a.hist + int64_t(cur_t) * kHistBins, et, a.status, abort_flag);
     tc::cp_async_wait_all();   // no copy into shared memory outlives the CTA
     __syncwarp();
   }
@@ -596,7 +501,8 @@ int stages_count() {
 
 bool index_score_tc_supported(const v4a_index_args* a) {
   const v4a_cache& c = a->keys;
-  if (c.format != V4A_IX_FP8_B128 && c.format != V4A_IX_FP4_B32) return false;
+  // power-of-two (MX) scales are a special case of the fp32 scales
+  if (c.format != V4A_IX_FP8_B128 && !ix_is_fp4(c.format)) return false;
   if (a->q_format != V4A_Q_FP8_HEAD || a->num_heads != 64 || c.dim != 128) return false;
   // the fp4 tensor map wants a 32-byte aligned pool (block sizes are multiples of 32)
   if ((reinterpret_cast<uintptr_t>(c.pool) & 31) || (reinterpret_cast<uintptr_t>(a->q) & 15)) return false;
@@ -612,7 +518,7 @@ bool index_score_tc(const v4a_index_args* a, float* scores, int64_t row, uint32_
   *rc = V4A_OK;
   if (!index_score_tc_supported(a)) return false;
   const v4a_cache& c = a->keys;
-  const bool fp4 = c.format == V4A_IX_FP4_B32;
+  const bool fp4 = ix_is_fp4(c.format);
   TcArgs t{};
   t.T = a->batch.num_tokens;
   t.fmt = c.format;

@@ -14,4 +14,10 @@ bool index_score_tc(const v4a_index_args* a, float* scores, int64_t row, uint32_
                     int* rc);
 // True when index_score_tc would launch for these arguments.
 bool index_score_tc_supported(const v4a_index_args* a);
+// The same for fp4 keys with power-of-two (MX) block scales, on the
+// block-scaled MMA (index_mx.cu); V4A_IX_FP4_MX32 keys with an fp8 query, 64
+// heads x 128 dims.
+bool index_score_mx(const v4a_index_args* a, float* scores, int64_t row, uint32_t* hist, cudaStream_t stream,
+                    int* rc);
+bool index_score_mx_supported(const v4a_index_args* a);
 }  // namespace v4a

@@ -118,12 +118,16 @@ __host__ __device__ __forceinline__ int64_t kv_row_bytes(int fmt, int dim) {
   return fmt == V4A_KV_BF16 ? int64_t(dim) * 2 : int64_t(dim);
 }
 
+__host__ __device__ __forceinline__ bool ix_is_fp4(int fmt) {
+  return fmt == V4A_IX_FP4_B32 || fmt == V4A_IX_FP4_MX32;
+}
+
 __host__ __device__ __forceinline__ int64_t ix_row_bytes(int fmt, int dim) {
   return fmt == V4A_IX_BF16 ? int64_t(dim) * 2 : (fmt == V4A_IX_FP8_B128 ? dim : dim / 2);
 }
 
 __host__ __device__ __forceinline__ int ix_scales_per_row(int fmt, int dim) {
-  return fmt == V4A_IX_FP8_B128 ? dim / 128 : (fmt == V4A_IX_FP4_B32 ? dim / 32 : 0);
+  return fmt == V4A_IX_FP8_B128 ? dim / 128 : (ix_is_fp4(fmt) ? dim / 32 : 0);
 }
 
 __host__ __device__ __forceinline__ int64_t ix_block_bytes(int fmt, int dim) {

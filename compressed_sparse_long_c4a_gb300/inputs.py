@@ -19,7 +19,8 @@ the queries.  Distributions follow the five workloads of the layer:
   +-448, with fp32 scales ~ U(0.5,1.5)/100, so decoded values are ~N(0,1);
 * fp4 codes are drawn from a fixed categorical law over the 8 e2m1
   magnitudes (small codes most likely) with a random sign, with fp32 scales
-  ~ U(0.5,1.5)/2;
+  ~ U(0.5,1.5)/2, or, for the power-of-two (MX) scale format, scales 2^e with
+  e uniform on {-3, -2, -1};
 * block tables are a seeded random permutation of the physical pool.
 
 Sub-seeds: every tensor gets its own generator seeded with (seed, tensor id).
@@ -34,7 +35,7 @@ import torch
 
 BLOCK_POSITIONS = 256
 KV_BF16, KV_FP8_TOKEN = 0, 1
-IX_BF16, IX_FP8_B128, IX_FP4_B32 = 0, 1, 2
+IX_BF16, IX_FP8_B128, IX_FP4_B32, IX_FP4_MX32 = 0, 1, 2, 3
 Q_BF16, Q_FP8_HEAD = 0, 1
 OUT_BF16, OUT_FP8_TOKEN = 0, 1
 
@@ -157,6 +158,11 @@ def _scales(n, seed, tid, base) -> torch.Tensor:
     return _rand((n,), seed, tid, 0.5, 1.5) / base
 
 
+def _pow2_scales(n, seed, tid) -> torch.Tensor:
+    e = torch.randint(-3, 0, (n,), generator=_gen(seed, tid))
+    return torch.pow(2.0, e.to(torch.float32))
+
+
 @dataclass
 class Case:
     """All tensors of one layer step (CPU), in the library's layouts."""
@@ -239,8 +245,11 @@ def make_case(spec: LayerSpec, seed: int = 0) -> Case:
             ix = torch.cat([codes, sc], dim=1)
         else:
             packed = _fp4_bytes((nb, 64 * dI // 2), seed, 20)
-            sc = _scales(nb * 64 * (dI // 32), seed, 21, 2.0).view(torch.uint8).reshape(nb, -1)
-            ix = torch.cat([packed, sc], dim=1)
+            if s.ix_fmt == IX_FP4_MX32:
+                sc = _pow2_scales(nb * 64 * (dI // 32), seed, 21)
+            else:
+                sc = _scales(nb * 64 * (dI // 32), seed, 21, 2.0)
+            ix = torch.cat([packed, sc.view(torch.uint8).reshape(nb, -1)], dim=1)
         case.ix_pool = ix.reshape(-1).contiguous()
         case.x_i = _bf16(_randn((T, dI), seed, 22))
         case.gate_i = _randn((T,), seed, 23)
@@ -314,12 +323,20 @@ def c4a_decode_1m() -> LayerSpec:
                      topk=2048, out_fmt=OUT_FP8_TOKEN, spare_blocks=1)
 
 
+def c4a_decode_1m_mx() -> LayerSpec:
+    """c4a_decode_b4_1m with the fp4 indexer's per-32 fp32 scales restricted to
+    powers of two (the OCP MX rule; same bytes per entry), which the tensor
+    cores apply inside a block-scaled MMA."""
+    return dataclasses.replace(c4a_decode_1m(), name="c4a_decode_b4_1m_mx", ix_fmt=IX_FP4_MX32)
+
+
 WORKLOADS = {
     "c4a_decode_b1_1k": c4a_decode_1k,
     "c4a_decode_b32_32k_64k": c4a_decode_b32_32k_64k,
     "c128a_decode_b64_64k_128k": c128a_decode_b64_64k_128k,
     "c4a_prefill_4x32k_plus_4k": c4a_prefill_4x4k,
     "c4a_decode_b4_1m": c4a_decode_1m,
+    "c4a_decode_b4_1m_mx": c4a_decode_1m_mx,
 }
 
 

@@ -20,7 +20,7 @@ V4A_OK = 0
 ERRORS = {1: "invalid argument", 2: "unsupported", 3: "ring too small", 4: "workspace", 5: "cuda"}
 DEV_BAD_BLOCK, DEV_BAD_BATCH, DEV_BAD_INDEX = 1, 2, 4
 KV_BF16, KV_FP8_TOKEN = 0, 1
-IX_BF16, IX_FP8_B128, IX_FP4_B32 = 0, 1, 2
+IX_BF16, IX_FP8_B128, IX_FP4_B32, IX_FP4_MX32 = 0, 1, 2, 3
 Q_BF16, Q_FP8_HEAD = 0, 1
 OUT_BF16, OUT_FP8_TOKEN = 0, 1
 
@@ -325,7 +325,7 @@ class Step:
         s = self.layer.spec
         n = 1
         if s.ix_heads:
-            tc_scan = s.ix_fmt in (IX_FP8_B128, IX_FP4_B32) and s.ix_heads == 64 and s.ix_dim == 128
+            tc_scan = s.ix_fmt in (IX_FP8_B128, IX_FP4_B32, IX_FP4_MX32) and s.ix_heads == 64 and s.ix_dim == 128
             n += 2 + (1 if s.max_blocks * 64 <= 32768 or tc_scan else 2)
         # the tensor-core attention runs long batches (chunked prefill) as
         # several launches of at most 64 waves of 152 CTAs, one CTA per

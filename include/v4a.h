@@ -71,6 +71,11 @@ extern "C" {
 #define V4A_IX_BF16       0  /* row = dim bf16 */
 #define V4A_IX_FP8_B128   1  /* row = dim e4m3; one fp32 scale per 128 elements (132 B at dim 128) */
 #define V4A_IX_FP4_B32    2  /* row = dim/2 bytes e2m1; one fp32 scale per 32 elements */
+#define V4A_IX_FP4_MX32   3  /* the V4A_IX_FP4_B32 bytes with every scale a power of two, chosen by the
+                                OCP Microscaling (MX) rule 2^(floor(log2 amax) - 2); the tensor cores
+                                then apply the scales inside the MMA.  A scale word that is not a
+                                power of two is read as its power-of-two part by the tensor-core
+                                scan (its mantissa bits are ignored). */
 /* Indexer query. */
 #define V4A_Q_BF16        0  /* [T][H_I][dim] bf16 */
 #define V4A_Q_FP8_HEAD    1  /* [T][H_I][dim] e4m3 + [T][H_I] fp32 scale */
@@ -101,7 +106,7 @@ typedef struct {
  * then the fp32 scale words ([E][scales per row]) if the format has any.
  * Block bytes:  KV_BF16 E*dim*2;  KV_FP8_TOKEN E*(dim+4);
  *               IX_BF16 64*dim*2;  IX_FP8_B128 64*(dim + 4*dim/128);
- *               IX_FP4_B32 64*(dim/2 + 4*dim/32).
+ *               IX_FP4_B32, IX_FP4_MX32 64*(dim/2 + 4*dim/32).
  */
 typedef struct {
   int32_t ratio;               /* 4 (c4a) or 128 (c128a); indexer caches use 4 */

@@ -85,6 +85,27 @@ def check_fp4_blocks(packed, scales, ref, where=""):
         assert not bad.any(), (where, b, np.nonzero(bad)[0][:5])
 
 
+def check_fp4_mx_blocks(packed, scales, ref, where=""):
+    """MX fp4: every scale a power of two equal to the oracle's shared scale
+    (or the neighbouring one when the fp32 amax rounds across a power of two),
+    codes within 1 e2m1 ulp, values above 6 * scale clipped to 6 * scale."""
+    nib = F.unpack_nibbles(packed)
+    for b in range(ref.shape[0] // 32):
+        seg = ref[32 * b:32 * b + 32]
+        s = float(scales[b])
+        m, _ = np.frexp(s)
+        assert m == 0.5, (where, b, s)
+        want = F.mx_shared_scale(seg)
+        amax = float(np.max(np.abs(seg)))
+        near_pow2 = abs(np.frexp(amax)[0] - 0.5) < 1e-6 or abs(np.frexp(amax)[0] - 1.0) < 1e-6
+        assert s == want or (near_pow2 and s in (want / 2, want * 2)), (where, b, s, want)
+        got = F.e2m1_decode(nib[32 * b:32 * b + 32]) * s
+        clipped = np.clip(seg, -6 * s, 6 * s)
+        ulp = F.e2m1_ulp(clipped / s) * s
+        bad = np.abs(got - clipped) > ulp * 1.0000001 + 1e-30
+        assert not bad.any(), (where, b, np.nonzero(bad)[0][:5])
+
+
 def kv_slot_bytes(pool: np.ndarray, spec, blk: int, slot: int):
     """(row bytes, scale or None) of one shared-KV entry."""
     E, D = spec.entries_per_block, spec.dim

@@ -36,7 +36,9 @@ def _small_workloads():
     s5 = I.c4a_decode_1m()
     s5 = dataclasses.replace(s5, name="c4a_decode_small_fp4ix_fp8kv", batch=2,
                              cached=(4 * 10000 + 3, 39001))
-    return [I.c4a_decode_1k(), s2, s3, s4, s5]
+    s5mx = dataclasses.replace(I.c4a_decode_1m_mx(), name="c4a_decode_small_mx4ix_fp8kv", batch=3,
+                               cached=(4 * 10000 + 3, 39001, 256 * 90 + 255))
+    return [I.c4a_decode_1k(), s2, s3, s4, s5, s5mx]
 
 
 SMALL = {s.name: s for s in _small_workloads()}
@@ -128,6 +130,8 @@ def test_compress_insert(name):
                 U.check_bf16_row(row, ref, f"ix {b},{i}")
             elif s.ix_fmt == F.IX_FP8_B128:
                 U.check_fp8_blocks(row, sc, ref, 128, f"ix {b},{i}")
+            elif s.ix_fmt == F.IX_FP4_MX32:
+                U.check_fp4_mx_blocks(row, sc, ref, f"ix {b},{i}")
             else:
                 U.check_fp4_blocks(row, sc, ref, f"ix {b},{i}")
             base = blk * s.ix_block_bytes
@@ -295,8 +299,9 @@ def test_end_to_end(name):
 
 
 # Workloads whose attention the fused attention + output call must take.
-FUSED_EXPECTED = {"c4a_decode_b4_1m", "c4a_decode_b32_32k_64k", "c128a_decode_b64_64k_128k",
-                  "c4a_decode_small_fp8ix", "c4a_decode_small_fp4ix_fp8kv"}
+FUSED_EXPECTED = {"c4a_decode_b4_1m", "c4a_decode_b4_1m_mx", "c4a_decode_b32_32k_64k",
+                  "c128a_decode_b64_64k_128k", "c4a_decode_small_fp8ix", "c4a_decode_small_fp4ix_fp8kv",
+                  "c4a_decode_small_mx4ix_fp8kv"}
 
 
 @pytest.mark.parametrize("name", [_marks(n) for n in ALL])
