@@ -14,29 +14,16 @@
 //  * topk_smem         - one CTA per query when the row fits in shared memory:
 //                         radix select of the k-th largest (score, -index)
 //                         composite, then an ordered compaction.
-//  * topk_hist / topk_select - long rows, one CTA per 8192-score slice: a
-//                         4096-bin histogram of the score keys' top 12 bits
-//                         (built by the tensor-core scan itself when that
-//                         path scored the row, else by topk_hist) gives the
-//                         threshold bin; every slice then compacts,
-//                         in index order, its entries above that bin ("takes")
-//                         and those in it ("candidates", plus a histogram of
-//                         their next 12 bits).  The last slice CTA of a query
-//                         resolves the exact threshold among the candidates
-//                         and merges the two ordered lists into the output.
-//                         The "last CTA" is found with an atomic counter; no
-//                         CTA ever waits on another.  It holds up to 8
-//                         candidates per thread in registers, so the
-//                         candidates are read from L2 once.
-//  * topk_coop          - long rows when every slice CTA of the batch fits on
-//                         the GPU at once (cooperative launch): the exact
-//                         k-th largest key comes from three histogram levels
-//                         (12 + 12 + 8 bits) shared by the query's slices
-//                         through bounded global barriers, then each slice
-//                         writes its share in ascending index order.  This
-//                         is the path of the 1M-context decode; topk_select
-//                         covers batches too large for one wave.
+//  * topk_hist         - the 4096-bin histogram of the score keys' top 12 bits
+//                         for long rows scored on the CUDA cores (the
+//                         tensor-core scans build it themselves).
+//  * topk_cluster      - long rows (up to 2^20 entries): one thread-block
+//                         cluster per query finds the exact k-th largest key
+//                         from three histogram levels combined through
+//                         distributed shared memory, then every CTA writes
+//                         its selected indices in ascending order.
 
+#include <cooperative_groups.h>
 #include <cstdio>
 #include <algorithm>
 #include <mutex>
@@ -45,25 +32,24 @@
 #include "v4a_internal.h"
 #include "index_tc.h"
 
+namespace cg = cooperative_groups;
+
 namespace v4a {
 
 constexpr int kSmemTopkMax = 32768;   // rows up to this length use topk_smem
 constexpr int kHistBins = 4096;       // top 12 bits of the order-preserving key
 constexpr int kMaxK = 16384;
 constexpr int kSlice = 8192;          // scores per CTA of the long-row top-k (8 per thread)
-constexpr int kMaxSlices = 1024;      // rows up to 8M entries
+constexpr int kBitmapMax = 1 << 20;   // longest supported row (entries; 4M native positions)
 
 struct IndexWs {
   float* scores;        // [T][row]
   uint32_t* hist;       // [T][kHistBins]   top 12 key bits of every score
-  uint32_t* hist2;      // [T][kHistBins]   next 12 bits of the threshold bin's scores
-  uint32_t* hist3;      // [T][256]         last 8 bits of the threshold sub-bin's scores
-  uint32_t* counters;   // [T][4]: arrivals at the cooperative select's barriers / "done" of the fallback
-  uint64_t* cand;       // [T][row]: slice s keeps its takes at [lo, ..) and its candidates at [.., hi)
-  uint32_t* info;       // [T][slices]: takes | candidates << 16 of each slice
-  uint2* gteq;          // [T][slices]: entries above / equal to the exact threshold key, per slice
+  uint32_t* hist2;      // [T][kHistBins]   next 12 bits of the threshold bin's scores (long rows)
+  uint32_t* hist3;      // [T][256]         last 8 bits of the threshold sub-bin's scores (long rows)
+  uint2* gteq;          // [T][16]          each cluster CTA's entries above / equal to the exact cut
   int64_t row;
-  size_t zero_bytes;    // bytes of hist + counters (cleared per call)
+  size_t zero_bytes;    // bytes of hist, hist2 and hist3 (cleared per call)
   size_t total;
 };
 
@@ -79,14 +65,9 @@ static IndexWs ws_layout(const v4a_index_args* a, void* base) {
   w.hist = reinterpret_cast<uint32_t*>(take(size_t(T) * kHistBins * 4));
   w.hist2 = reinterpret_cast<uint32_t*>(take(size_t(T) * kHistBins * 4));
   w.hist3 = reinterpret_cast<uint32_t*>(take(size_t(T) * 256 * 4));
-  w.counters = reinterpret_cast<uint32_t*>(take(size_t(T) * 4 * 4));
   w.zero_bytes = off;
+  w.gteq = reinterpret_cast<uint2*>(take(size_t(T) * 16 * 8));
   w.scores = reinterpret_cast<float*>(take(size_t(T) * w.row * 4));
-  if (w.row > kSmemTopkMax) {
-    w.cand = reinterpret_cast<uint64_t*>(take(size_t(T) * w.row * 8));
-    w.info = reinterpret_cast<uint32_t*>(take(size_t(T) * ((w.row + kSlice - 1) / kSlice) * 4));
-    w.gteq = reinterpret_cast<uint2*>(take(size_t(T) * ((w.row + kSlice - 1) / kSlice) * 8));
-  }
   w.total = off;
   return w;
 }
@@ -341,17 +322,37 @@ __global__ void __launch_bounds__(512) topk_hist(const float* scores, int64_t ro
     if (h_s[i]) atomicAdd(&g[i], h_s[i]);
 }
 
-// Threshold bin of a 4096-bin histogram: the bin b such that fewer than `need`
-// counts lie strictly above it and at least `need` at or above it.  Block of
-// 1024 threads, 4 bins each (scanned from the top).  Returns b and, through
-// *above, the count strictly above it.
-__device__ int threshold_bin(const uint32_t* h, uint32_t need, uint32_t* scan, int* bin_s,
-                             uint32_t* above_s, uint32_t* above) {
+// ------------------------------------------------------------------------------
+// Cluster long-row top-k
+// ------------------------------------------------------------------------------
+//
+// One thread-block cluster per query (16 CTAs, else 8), 1024 threads per CTA,
+// PER consecutive scores of the row per thread, held in registers.  The exact
+// k-th largest key K* comes from three histogram levels of the
+// order-preserving key: the top 12 bits (built by the scan), the next 12 bits
+// and the last 8 bits of the entries in the threshold bins.  Each CTA counts
+// a level in shared memory and adds its nonzero counts to the query's global
+// histogram; after a cluster barrier (a hardware barrier of co-scheduled
+// CTAs whose release / acquire also orders global memory: no CTA waits on a
+// grid) every CTA reads the level whole.  Then every CTA learns, from the
+// counts of the CTAs before it (one lane each), its share of the ties at K*
+// (lowest indices first) and its output offset, and writes its selected
+// indices in ascending order.  Three cluster barriers in all: measured on
+// GB300, a cluster barrier costs ~1 us and a distributed-shared-memory read
+// ~0.25 us, so the levels are combined in L2 rather than through remote
+// shared memory.
+
+// Threshold bin of a 4096-bin histogram given as a function bin -> count: the
+// bin b with fewer than `need` counts strictly above it and at least `need`
+// at or above it; *above receives the count strictly above.  All 1024
+// threads call it (4 bins each, scanned from the top).
+template <class Get>
+__device__ int threshold_bin_of(Get count, uint32_t need, uint32_t* scan, int* bin_s, uint32_t* above_s,
+                                uint32_t* above) {
   uint32_t loc[4], s4 = 0;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const int bin = kHistBins - 1 - (threadIdx.x * 4 + q);
-    loc[q] = bin >= 0 ? h[bin] : 0;
+    loc[q] = count(kHistBins - 1 - (int(threadIdx.x) * 4 + q));
     s4 += loc[q];
   }
   uint32_t total;
@@ -363,7 +364,7 @@ __device__ int threshold_bin(const uint32_t* h, uint32_t need, uint32_t* scan, i
       if (acc + loc[q] >= need) break;
       acc += loc[q];
     }
-    *bin_s = kHistBins - 1 - (threadIdx.x * 4 + q);
+    *bin_s = kHistBins - 1 - (int(threadIdx.x) * 4 + q);
     *above_s = acc;
   }
   __syncthreads();
@@ -373,415 +374,158 @@ __device__ int threshold_bin(const uint32_t* h, uint32_t need, uint32_t* scan, i
   return b;
 }
 
-constexpr int kFine = 2048;   // capacity of the resolving CTA's exact-select list
-constexpr int kRegCands = 8;  // threshold-bin candidates per thread held in registers while resolving
-
-// Position of j among the slices' ranges: the largest s with pre[s] <= j.
-__device__ __forceinline__ int slice_of(const uint32_t* pre, int nsl, uint32_t j) {
-  int lo = 0, hi = nsl - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (pre[mid] <= j) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
-// Number of elements of the ascending list l[0..n) below x.
-__device__ __forceinline__ int count_below(const int32_t* l, int n, int32_t x) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (l[mid] < x) lo = mid + 1; else hi = mid;
-  }
-  return lo;
-}
-
-__global__ void __launch_bounds__(1024, 1) topk_select(const float* scores, int64_t row, int max_entries,
-                                                   const int32_t* positions, int k, int slices,
-                                                   const uint32_t* hist, uint32_t* hist2,
-                                                   uint32_t* counters, uint64_t* cand, uint32_t* info,
-                                                   int32_t* out) {
-  extern __shared__ int32_t lists_s[];   // resolving CTA: [k] takes, then [k] selected candidates
+template <int PER>
+__global__ void __launch_bounds__(1024, 1) topk_cluster(const float* scores, int64_t row, int max_entries,
+                                                    const int32_t* positions, int k, const uint32_t* hist1,
+                                                    uint32_t* hist2, uint32_t* hist3, uint2* gteq, int32_t* out) {
+  pdl_trigger();
   __shared__ uint32_t scan[40];
-  __shared__ uint32_t h2_s[kHistBins];
-  __shared__ uint64_t fine_s[kFine];
-  __shared__ uint32_t pre_s[2][kMaxSlices + 1];
-  __shared__ uint32_t hist256[256];
-  __shared__ uint32_t sh[4];
+  __shared__ uint32_t h_s[kHistBins];  // this CTA's counts of the level being built
+  __shared__ uint32_t pre_s[2];        // ties in and entries selected by the CTAs before this one
   __shared__ int bin_s;
   __shared__ uint32_t above_s;
-  __shared__ int last_s;
-  __shared__ uint32_t nfine_s;
-  const int t = blockIdx.y, sl = blockIdx.x;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int r = int(cluster.block_rank());
+  const int t = blockIdx.y;
+  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h_s[i] = 0;
+  pdl_wait();   // the scores and the first-level histogram are the previous kernel's output
   const int n = min((positions[t] + 1) / 4, max_entries);
   int32_t* o = out + int64_t(t) * k;
-  if (n <= k) {
-    if (sl == 0) write_all_visible(o, n, k);
+  if (n <= k) {   // every CTA of the cluster takes this branch together
+    if (r == 0) write_all_visible(o, n, k);
     return;
   }
-  const int nsl = (n + kSlice - 1) / kSlice;
-  if (sl >= nsl) return;
-  // 1. this slice's scores (thread c owns entries lo + 8c .. lo + 8c + 7), loaded
-  //    first so that their latency overlaps the threshold search below
-  constexpr int kPer = kSlice / 1024;
-  const int lo = sl * kSlice, hi = min(n, lo + kSlice);
+  // this thread's PER consecutive entries
+  const int i0 = (r * int(blockDim.x) + int(threadIdx.x)) * PER;
   const float* sc = scores + int64_t(t) * row;
-  const int i0 = lo + kPer * int(threadIdx.x);
-  float v[kPer];
-  if (i0 + kPer - 1 < hi) {
+  uint32_t key[PER];
+  if (i0 + PER <= n) {
 #pragma unroll
-    for (int u = 0; u < kPer; u += 4) {
+    for (int u = 0; u < PER; u += 4) {
       const float4 f = __ldcg(reinterpret_cast<const float4*>(sc + i0 + u));
-      v[u] = f.x; v[u + 1] = f.y; v[u + 2] = f.z; v[u + 3] = f.w;
+      key[u] = float_key(f.x); key[u + 1] = float_key(f.y); key[u + 2] = float_key(f.z); key[u + 3] = float_key(f.w);
     }
   } else {
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) v[u] = i0 + u < hi ? __ldcg(sc + i0 + u) : 0.f;
+    for (int u = 0; u < PER; ++u) key[u] = i0 + u < n ? float_key(__ldcg(sc + i0 + u)) : 0u;
   }
-  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h2_s[i] = 0;
-  // 2. threshold bin of the top 12 key bits
+  // level 1: the top 12 bits (histogram from the scan)
   uint32_t above1;
-  const uint32_t tbin = uint32_t(threshold_bin(hist + int64_t(t) * kHistBins, uint32_t(k), scan, &bin_s,
-                                               &above_s, &above1));
-  // 3. ordered compaction of this slice into its range of the candidate array:
-  //    entries above the threshold bin ("takes", as indices) from the front,
-  //    entries in it (as composites) at the back
-  uint32_t key[kPer], ntk = 0, ncd = 0;
+  const uint32_t* g1 = hist1 + int64_t(t) * kHistBins;
+  const uint32_t b1 = uint32_t(threshold_bin_of([&](int b) { return __ldcg(&g1[b]); }, uint32_t(k), scan, &bin_s,
+                                                &above_s, &above1));
+  const uint32_t need1 = uint32_t(k) - above1;
+  // level 2: the next 12 bits of the entries in bin b1; each CTA's nonzero
+  // counts go to the query's global histogram, complete after the cluster
+  // barrier (its release / acquire covers global memory)
 #pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    key[u] = float_key(v[u]);
-    const bool in = i0 + u < hi;
-    ntk += in && (key[u] >> 20) > tbin;
-    ncd += in && (key[u] >> 20) == tbin;
-  }
-  uint32_t tot;
-  const uint32_t off = block_excl_scan(ntk | (ncd << 16), scan, &tot);   // both halves <= kSlice < 2^16
-  const uint32_t NCD = tot >> 16;
-  uint32_t otk = off & 0xFFFFu, ocd = off >> 16;
-  uint64_t* cd = cand + int64_t(t) * row;
-#pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const int i = i0 + u;
-    if (i >= hi) continue;
-    const uint32_t b = key[u] >> 20;
-    if (b > tbin) {
-      cd[lo + otk++] = uint64_t(i);
-    } else if (b == tbin) {
-      cd[hi - NCD + ocd++] = composite(key[u], i);
-      atomicAdd(&h2_s[(key[u] >> 8) & (kHistBins - 1)], 1u);
-    }
-  }
+  for (int u = 0; u < PER; ++u)
+    if (i0 + u < n && (key[u] >> 20) == b1) atomicAdd(&h_s[(key[u] >> 8) & (kHistBins - 1)], 1u);
   __syncthreads();
   uint32_t* g2 = hist2 + int64_t(t) * kHistBins;
-  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x)
-    if (h2_s[i]) atomicAdd(&g2[i], h2_s[i]);
-  if (threadIdx.x == 0) info[int64_t(t) * slices + sl] = tot;
-  // 4. the last slice CTA of this query resolves the threshold and merges
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) last_s = atomicAdd(&counters[int64_t(t) * 4 + 2], 1u) == uint32_t(nsl - 1);
-  __syncthreads();
-  if (!last_s) return;
-  __threadfence();
-  {
-    // slice counts and the second-level histogram, both loads in flight together
-    const uint32_t x = int(threadIdx.x) < nsl ? __ldcg(&info[int64_t(t) * slices + threadIdx.x]) : 0u;
-    for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h2_s[i] = __ldcg(&g2[i]);
-    uint32_t tk_tot, cd_tot;
-    const uint32_t ptk = block_excl_scan(x & 0xFFFFu, scan, &tk_tot);
-    const uint32_t pcd = block_excl_scan(x >> 16, scan, &cd_tot);
-    if (int(threadIdx.x) < nsl) { pre_s[0][threadIdx.x] = ptk; pre_s[1][threadIdx.x] = pcd; }
-    if (threadIdx.x == 0) { pre_s[0][nsl] = tk_tot; pre_s[1][nsl] = cd_tot; nfine_s = 0; }
-  }
-  __syncthreads();
-  const int above = int(pre_s[0][nsl]);      // entries above the threshold bin (< k)
-  const int nc = int(pre_s[1][nsl]);         // entries in it (>= k - above)
-  const int need = k - above;
-  int32_t* take_l = lists_s;
-  int32_t* csel_l = lists_s + k;
-  auto cand_at = [&](int j) -> uint64_t {    // j-th candidate in index order
-    const int s2 = slice_of(pre_s[1], nsl, uint32_t(j));
-    const int hi2 = min(n, (s2 + 1) * kSlice);
-    const int ncd2 = int(pre_s[1][s2 + 1] - pre_s[1][s2]);
-    return __ldcg(reinterpret_cast<const unsigned long long*>(&cd[hi2 - ncd2 + (j - int(pre_s[1][s2]))]));
-  };
-  // takes, in index order (independent of the exact threshold)
-  for (int j = threadIdx.x; j < above; j += blockDim.x) {
-    const int s2 = slice_of(pre_s[0], nsl, uint32_t(j));
-    take_l[j] = int32_t(__ldcg(reinterpret_cast<const unsigned long long*>(
-        &cd[int64_t(s2) * kSlice + (j - int(pre_s[0][s2]))])));
-  }
-  if (nc <= int(blockDim.x) * kRegCands) {
-    // common case: every candidate is read once into registers; thread c owns
-    // the run [c*R, c*R + R) of the candidates, so its selected ones are
-    // consecutive in index order
-    const int R = (nc + int(blockDim.x) - 1) / int(blockDim.x);
-    const int j0 = int(threadIdx.x) * R;
-    uint64_t c[kRegCands];
-#pragma unroll
-    for (int u = 0; u < kRegCands; ++u) c[u] = (u < R && j0 + u < nc) ? cand_at(j0 + u) : 0ull;
-    uint32_t above2;
-    const uint32_t tbin2 = uint32_t(threshold_bin(h2_s, uint32_t(need), scan, &bin_s, &above_s, &above2));
-    const int need2 = need - int(above2);
-    uint64_t thr;
-    if (h2_s[tbin2] <= uint32_t(kFine)) {
-#pragma unroll
-      for (int u = 0; u < kRegCands; ++u)
-        if (u < R && j0 + u < nc && ((uint32_t(c[u] >> 40) & (kHistBins - 1)) == tbin2))
-          fine_s[atomicAdd(&nfine_s, 1u)] = c[u];
-      __syncthreads();
-      // the sub-bin's candidates share their top 24 key bits: select on the rest
-      thr = select_threshold(int(nfine_s), need2, [&](int i) { return fine_s[i]; }, hist256, sh, 3);
-    } else {
-      // degenerate (e.g. all scores equal): exact select over every candidate of the sub-bin
-      thr = select_threshold(nc, need2, [&](int j) {
-        const uint64_t cc = cand_at(j);
-        return (uint32_t(cc >> 40) & (kHistBins - 1)) == tbin2 ? cc : uint64_t(0);
-      }, hist256, sh);
-    }
-    uint32_t cnt = 0;
-#pragma unroll
-    for (int u = 0; u < kRegCands; ++u) cnt += (u < R && j0 + u < nc && c[u] >= thr) ? 1u : 0u;
-    uint32_t pos = block_excl_scan(cnt, scan, nullptr);
-#pragma unroll
-    for (int u = 0; u < kRegCands; ++u)
-      if (u < R && j0 + u < nc && c[u] >= thr) csel_l[pos++] = int32_t(0xFFFFFFFFu - uint32_t(c[u]));
-  } else {
-    // more candidates than registers hold: stream them from L2 in each pass
-    uint32_t above2;
-    const uint32_t tbin2 = uint32_t(threshold_bin(h2_s, uint32_t(need), scan, &bin_s, &above_s, &above2));
-    const int need2 = need - int(above2);
-    const uint64_t thr = select_threshold(nc, need2, [&](int j) {
-      const uint64_t cc = cand_at(j);
-      return (uint32_t(cc >> 40) & (kHistBins - 1)) == tbin2 ? cc : uint64_t(0);
-    }, hist256, sh);
-    uint32_t carry = 0;
-    for (int b0 = 0; b0 < nc; b0 += blockDim.x) {
-      const int j = b0 + int(threadIdx.x);
-      const uint64_t cc = j < nc ? cand_at(j) : 0ull;
-      const bool f = j < nc && cc >= thr;
-      uint32_t cnt;
-      const uint32_t pos = block_excl_scan(f ? 1u : 0u, scan, &cnt);
-      if (f) csel_l[carry + pos] = int32_t(0xFFFFFFFFu - uint32_t(cc));
-      carry += cnt;
+  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) {
+    const uint32_t c = h_s[i];
+    if (c) {
+      atomicAdd(&g2[i], c);
+      h_s[i] = 0;
     }
   }
+  cluster.sync();
+  uint32_t above2;
+  const uint32_t b2 = uint32_t(threshold_bin_of([&](int b) { return __ldcg(&g2[b]); }, need1, scan, &bin_s,
+                                                &above_s, &above2));
+  const uint32_t need2 = need1 - above2;
+  // level 3: the last 8 bits of the entries in sub-bin (b1, b2)
+  const uint32_t top24 = (b1 << 12) | b2;
+#pragma unroll
+  for (int u = 0; u < PER; ++u)
+    if (i0 + u < n && (key[u] >> 8) == top24) atomicAdd(&h_s[key[u] & 255u], 1u);
   __syncthreads();
-  // merge the two ascending lists (disjoint indices) into the output
-  for (int j = threadIdx.x; j < above; j += blockDim.x) {
-    const int32_t x = take_l[j];
-    const int d = j + count_below(csel_l, need, x);
-    if (d < k) o[d] = x;
-  }
-  for (int j = threadIdx.x; j < need; j += blockDim.x) {
-    const int32_t y = csel_l[j];
-    const int d = j + count_below(take_l, above, y);
-    if (d < k) o[d] = y;
-  }
-}
-
-// ------------------------------------------------------------------------------
-// Cooperative long-row top-k (all CTAs of the grid co-resident)
-// ------------------------------------------------------------------------------
-//
-// One CTA per 8192-score slice of a query, every slice kept in registers.
-// The exact k-th largest key K* is found with three histogram levels of the
-// order-preserving key (top 12 bits: built by the tensor-core scan; next 12
-// bits; last 8 bits), each level a global histogram filled by the query's
-// CTAs and read by all of them after a barrier of the query's CTAs.  Then
-// every CTA publishes how many of its entries lie above K* and at K*; after a
-// last barrier each CTA knows, from the prefix over the slices before it, its
-// share of the ties at K* (lowest indices first) and its output offset, and
-// writes its selected indices in ascending order.  No candidate lists, no
-// single resolving CTA.
-
-// Waits until `target` CTAs have arrived at *counter (bounded; false if it gave up).
-__device__ __forceinline__ bool slice_barrier(uint32_t* counter, uint32_t target, int32_t* status, int* give_up) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(counter, 1u);
-    const long long t0 = clock64();
-    uint32_t v = 0;
-    while (true) {
-      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
-      if (v >= target) break;
-      if (clock64() - t0 > 2000000000LL) {
-        report(status, V4A_DEV_TIMEOUT);
-        *give_up = 1;
-        break;
-      }
-      __nanosleep(64);
-    }
-    __threadfence();
-  }
-  __syncthreads();
-  return *give_up == 0;
-}
-
-// Threshold of a 256-bin histogram (warp 0 scans; result broadcast through shared memory).
-__device__ int threshold_bin256(const uint32_t* h, uint32_t need, int* bin_s, uint32_t* above_s,
-                                uint32_t* above) {
+  uint32_t* g3 = hist3 + int64_t(t) * 256;
+  if (threadIdx.x < 256 && h_s[threadIdx.x]) atomicAdd(&g3[threadIdx.x], h_s[threadIdx.x]);
+  cluster.sync();
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     uint32_t loc[8], s8 = 0;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) { loc[q] = __ldcg(&h[255 - (lane * 8 + q)]); s8 += loc[q]; }
+    for (int q = 0; q < 8; ++q) { loc[q] = __ldcg(&g3[255 - (lane * 8 + q)]); s8 += loc[q]; }
     uint32_t incl = s8;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += x;
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t x = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += x;
     }
     const uint32_t excl = incl - s8;
-    if (excl < need && need <= incl) {
+    if (excl < need2 && need2 <= incl) {
       uint32_t acc = excl;
       int q = 0;
       for (; q < 8; ++q) {
-        if (acc + loc[q] >= need) break;
+        if (acc + loc[q] >= need2) break;
         acc += loc[q];
       }
-      *bin_s = 255 - (lane * 8 + q);
-      *above_s = acc;
+      bin_s = 255 - (lane * 8 + q);
+      above_s = acc;
     }
   }
   __syncthreads();
-  *above = *above_s;
-  const int b = *bin_s;
-  __syncthreads();
-  return b;
-}
-
-__global__ void __launch_bounds__(1024, 1) topk_coop(const float* scores, int64_t row, int max_entries,
-                                                 const int32_t* positions, int k, int slices,
-                                                 const uint32_t* hist1, uint32_t* hist2, uint32_t* hist3,
-                                                 uint32_t* counters, uint2* gteq, int32_t* out, int32_t* status) {
-  pdl_trigger();   // the attention kernel may be scheduled on SMs this grid leaves free
-  __shared__ uint32_t scan[40];
-  __shared__ uint32_t h_s[kHistBins];
-  __shared__ int bin_s, give_up;
-  __shared__ uint32_t above_s;
-  constexpr int kPer = kSlice / 1024;
-  const int t = blockIdx.y, sl = blockIdx.x;
-  const int n = min((positions[t] + 1) / 4, max_entries);
-  int32_t* o = out + int64_t(t) * k;
-  if (n <= k) {                        // every CTA of this query leaves together
-    if (sl == 0) write_all_visible(o, n, k);
-    return;
-  }
-  const int nsl = (n + kSlice - 1) / kSlice;
-  if (sl >= nsl) return;               // not one of this query's slices
-  if (threadIdx.x == 0) give_up = 0;
-  const int lo = sl * kSlice, hi = min(n, lo + kSlice);
-  const float* sc = scores + int64_t(t) * row;
-  const int i0 = lo + kPer * int(threadIdx.x);
-  uint32_t key[kPer];
-  {
-    float v[kPer];
-    if (i0 + kPer - 1 < hi) {
-#pragma unroll
-      for (int u = 0; u < kPer; u += 4) {
-        const float4 f = __ldcg(reinterpret_cast<const float4*>(sc + i0 + u));
-        v[u] = f.x; v[u + 1] = f.y; v[u + 2] = f.z; v[u + 3] = f.w;
-      }
-    } else {
-#pragma unroll
-      for (int u = 0; u < kPer; ++u) v[u] = i0 + u < hi ? __ldcg(sc + i0 + u) : 0.f;
-    }
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) key[u] = i0 + u < hi ? float_key(v[u]) : 0u;   // key 0: below every score
-  }
-  uint32_t* cnt = counters + int64_t(t) * 4;
-  // level 1: top 12 bits (histogram from the scan)
-  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h_s[i] = 0;
-  uint32_t above1;
-  const uint32_t b1 = uint32_t(threshold_bin(hist1 + int64_t(t) * kHistBins, uint32_t(k), scan, &bin_s, &above_s,
-                                             &above1));
-  // level 2: next 12 bits of the entries in bin b1
-#pragma unroll
-  for (int u = 0; u < kPer; ++u)
-    if (i0 + u < hi && (key[u] >> 20) == b1) atomicAdd(&h_s[(key[u] >> 8) & (kHistBins - 1)], 1u);
-  __syncthreads();
-  uint32_t* g2 = hist2 + int64_t(t) * kHistBins;
-  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) {
-    if (h_s[i]) atomicAdd(&g2[i], h_s[i]);
-    h_s[i] = 0;
-  }
-  if (!slice_barrier(&cnt[0], uint32_t(nsl), status, &give_up)) return;
-  const uint32_t need1 = uint32_t(k) - above1;
-  uint32_t above2;
-  const uint32_t b2 = uint32_t(threshold_bin(g2, need1, scan, &bin_s, &above_s, &above2));
-  // level 3: last 8 bits of the entries in sub-bin (b1, b2)
-  const uint32_t top24 = (b1 << 12) | b2;
-#pragma unroll
-  for (int u = 0; u < kPer; ++u)
-    if (i0 + u < hi && (key[u] >> 8) == top24) atomicAdd(&h_s[key[u] & 255u], 1u);
-  __syncthreads();
-  uint32_t* g3 = hist3 + int64_t(t) * 256;
-  for (int i = threadIdx.x; i < 256; i += blockDim.x)
-    if (h_s[i]) atomicAdd(&g3[i], h_s[i]);
-  if (!slice_barrier(&cnt[1], uint32_t(nsl), status, &give_up)) return;
-  const uint32_t need2 = need1 - above2;
-  uint32_t above3;
-  const uint32_t b3 = uint32_t(threshold_bin256(g3, need2, &bin_s, &above_s, &above3));
-  const uint32_t K = (top24 << 8) | b3;                       // exact key of the k-th largest
-  const uint32_t need = need2 - above3;                       // entries equal to K to take (>= 1)
-  // this slice's entries above K and equal to K
+  const uint32_t K = (top24 << 8) | uint32_t(bin_s);   // exact key of the k-th largest
+  const uint32_t need = need2 - above_s;               // entries equal to K to take (>= 1)
+  // this thread's entries above K and equal to K
   uint32_t gt = 0, eq = 0;
 #pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const bool in = i0 + u < hi;
+  for (int u = 0; u < PER; ++u) {
+    const bool in = i0 + u < n;
     gt += in && key[u] > K;
     eq += in && key[u] == K;
   }
   uint32_t tot;
-  const uint32_t eq_before = block_excl_scan(eq, scan, &tot);   // ties of this slice before this thread
-  const uint32_t eq_slice = tot;
-  const uint32_t gt_slice = block_excl_scan(gt, scan, &tot), gt_total = tot;
-  (void)gt_slice;
-  if (threadIdx.x == 0) gteq[int64_t(t) * slices + sl] = make_uint2(gt_total, eq_slice);
-  if (!slice_barrier(&cnt[2], uint32_t(nsl), status, &give_up)) return;
-  // ties taken by the slices before this one, and this slice's output offset
-  __shared__ uint32_t pre_eq_s, pre_sel_s;
-  {
-    uint32_t e = 0, sel = 0, ge = 0;
-    if (int(threadIdx.x) < sl) {
-      const uint2 x = __ldcg(&gteq[int64_t(t) * slices + threadIdx.x]);
-      ge = x.x;
-      e = x.y;
+  const uint32_t eq_before = block_excl_scan(eq, scan, &tot);   // ties of this CTA before this thread
+  const uint32_t eq_cta = tot;
+  block_excl_scan(gt, scan, &tot);
+  uint2* ge = gteq + int64_t(t) * 16;
+  if (threadIdx.x == 0) ge[r] = make_uint2(tot, eq_cta);
+  cluster.sync();
+  if (threadIdx.x < 32) {
+    // the CTAs before this one, one lane each: ties are taken in index order,
+    // CTA rr takes min(eq_rr, need - ties before it)
+    const int lane = threadIdx.x;
+    const uint2 x = lane < r ? __ldcg(&ge[lane]) : make_uint2(0u, 0u);
+    uint32_t ie = x.y;                              // inclusive prefix of the ties
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, ie, off);
+      if (lane >= off) ie += v;
     }
-    const uint32_t pe = block_excl_scan(e, scan, &tot);         // ties in slices before slice threadIdx.x
-    if (int(threadIdx.x) < sl) {
-      const uint32_t take = pe >= need ? 0u : min(e, need - pe);
-      sel = ge + take;
-    }
-    uint32_t sel_tot;
-    block_excl_scan(sel, scan, &sel_tot);
-    if (threadIdx.x == 0) { pre_eq_s = tot; pre_sel_s = sel_tot; }
-    __syncthreads();
+    const uint32_t e_before = ie - x.y;
+    const uint32_t take = e_before >= need ? 0u : min(x.y, need - e_before);
+    uint32_t sel = x.x + take;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sel += __shfl_xor_sync(0xffffffffu, sel, off);
+    const uint32_t all_e = __shfl_sync(0xffffffffu, ie, 31);
+    if (lane == 0) { pre_s[0] = all_e; pre_s[1] = sel; }
   }
-  const uint32_t pre_eq = pre_eq_s, pre_sel = pre_sel_s;
-  // ordered compaction: entry selected if key > K, or key == K and it is among
-  // the first `need` ties of the row in index order
+  __syncthreads();
+  const uint32_t pre_eq = pre_s[0];
+  // selected: key > K, or key == K and among the first `need` ties of the row
   uint32_t mine = 0;
   {
-    uint32_t r = pre_eq + eq_before;
+    uint32_t rk = pre_eq + eq_before;
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const bool in = i0 + u < hi;
+    for (int u = 0; u < PER; ++u) {
+      const bool in = i0 + u < n;
       if (in && key[u] > K) ++mine;
-      else if (in && key[u] == K) { if (r < need) ++mine; ++r; }
+      else if (in && key[u] == K) { if (rk < need) ++mine; ++rk; }
     }
   }
-  uint32_t pos = pre_sel + block_excl_scan(mine, scan, &tot);
+  uint32_t pos = pre_s[1] + block_excl_scan(mine, scan, &tot);
   {
-    uint32_t r = pre_eq + eq_before;
+    uint32_t rk = pre_eq + eq_before;
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const bool in = i0 + u < hi;
+    for (int u = 0; u < PER; ++u) {
+      const bool in = i0 + u < n;
       bool take = false;
       if (in && key[u] > K) take = true;
-      else if (in && key[u] == K) { take = r < need; ++r; }
+      else if (in && key[u] == K) { take = rk < need; ++rk; }
       if (take && pos < uint32_t(k)) o[pos++] = i0 + u;   // the bound holds unless the histograms were incomplete
     }
   }
@@ -791,19 +535,33 @@ __global__ void __launch_bounds__(1024, 1) topk_coop(const float* scores, int64_
 // Host side
 // ------------------------------------------------------------------------------
 
-// CTAs of topk_coop that can be resident at once on this device (its grid
-// must not exceed this: its CTAs wait for one another).
-static int64_t coop_capacity() {
-  static int64_t cap = -1;
+// Largest cluster (16, else 8) topk_cluster runs with on this device (0 if none).
+static int topk_cluster_size() {
+  static int cached = 0;
   static std::once_flag once;
   std::call_once(once, [] {
-    int dev = 0, sms = 0, per = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, topk_coop, 1024, 0) != cudaSuccess) per = 0;
-    cap = int64_t(sms) * per;
+    for (auto f : {topk_cluster<16>, topk_cluster<32>, topk_cluster<64>})
+      cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    for (int cs : {16, 8}) {
+      cudaLaunchConfig_t lc = {};
+      lc.gridDim = dim3(unsigned(cs));
+      lc.blockDim = dim3(1024);
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = unsigned(cs);
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      lc.attrs = at;
+      lc.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, topk_cluster<64>, &lc) == cudaSuccess && n > 0) {
+        cached = cs;
+        break;
+      }
+      cudaGetLastError();
+    }
   });
-  return cap;
+  return cached;
 }
 
 // Shapes and formats only (enough to size the workspace).
@@ -815,7 +573,7 @@ static int validate_shape(const v4a_index_args* a) {
   const v4a_cache& c = a->keys;
   if (c.ratio != 4) return V4A_ERR_UNSUPPORTED;
   if (c.num_blocks <= 0 || c.max_blocks <= 0) return V4A_ERR_INVALID_ARG;
-  if (int64_t(c.max_blocks) * 64 > int64_t(kMaxSlices) * kSlice) return V4A_ERR_UNSUPPORTED;
+  if (int64_t(c.max_blocks) * 64 > kBitmapMax) return V4A_ERR_UNSUPPORTED;
   if (a->k < 1 || a->k > kMaxK) return V4A_ERR_UNSUPPORTED;
   if (a->num_heads < 1 || a->num_heads > 128) return V4A_ERR_UNSUPPORTED;
   if (c.dim < 32 || c.dim > 256 || c.dim % 32) return V4A_ERR_UNSUPPORTED;
@@ -915,30 +673,38 @@ int index_select(const v4a_index_args* a, void* ws, size_t ws_bytes, cudaStream_
     if (!index_score_mx_supported(a) && !index_score_tc_supported(a))
       topk_hist<<<dim3(slices, T), 512, 0, stream>>>(w.scores, w.row, a->keys.max_blocks * 64,
                                                      a->batch.positions, a->k, slices, w.hist);
-    // all of a query's slices resolve together in one cooperative grid when
-    // the whole grid fits on the GPU at once; otherwise one CTA per query
-    // resolves after the others have compacted their slices
-    if (int64_t(slices) * T <= coop_capacity()) {
-      cudaLaunchConfig_t lc = {};
-      lc.gridDim = dim3(unsigned(slices), unsigned(T));
-      lc.blockDim = dim3(1024);
-      lc.stream = stream;
-      cudaLaunchAttribute at[1];
-      at[0].id = cudaLaunchAttributeCooperative;
-      at[0].val.cooperative = 1;
-      lc.attrs = at;
-      lc.numAttrs = 1;
-      if (cudaLaunchKernelEx(&lc, topk_coop, static_cast<const float*>(w.scores), w.row, a->keys.max_blocks * 64,
-                             a->batch.positions, a->k, slices, static_cast<const uint32_t*>(w.hist), w.hist2,
-                             w.hist3, w.counters, w.gteq, a->out_idx, a->status) != cudaSuccess)
-        return V4A_ERR_CUDA;
-    } else {
-      const size_t smem = size_t(2) * a->k * 4;
-      cudaFuncSetAttribute(topk_select, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-      topk_select<<<dim3(slices, T), 1024, smem, stream>>>(w.scores, w.row, a->keys.max_blocks * 64,
-                                                           a->batch.positions, a->k, slices, w.hist,
-                                                           w.hist2, w.counters, w.cand, w.info, a->out_idx);
-    }
+    // one cluster per query; each thread holds PER consecutive scores
+    const int cs = topk_cluster_size();
+    if (cs == 0) return V4A_ERR_UNSUPPORTED;
+    const int64_t per_needed = (w.row + int64_t(cs) * 1024 - 1) / (int64_t(cs) * 1024);
+    if (per_needed > 64) return V4A_ERR_UNSUPPORTED;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(unsigned(cs), unsigned(T));
+    lc.blockDim = dim3(1024);
+    lc.stream = stream;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = unsigned(cs);
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = at;
+    lc.numAttrs = 2;
+    const float* sc = w.scores;
+    const uint32_t* h1 = w.hist;
+    const int me = a->keys.max_blocks * 64;
+    cudaError_t e;
+    if (per_needed <= 16)
+      e = cudaLaunchKernelEx(&lc, topk_cluster<16>, sc, w.row, me, a->batch.positions, a->k, h1, w.hist2, w.hist3,
+                             w.gteq, a->out_idx);
+    else if (per_needed <= 32)
+      e = cudaLaunchKernelEx(&lc, topk_cluster<32>, sc, w.row, me, a->batch.positions, a->k, h1, w.hist2, w.hist3,
+                             w.gteq, a->out_idx);
+    else
+      e = cudaLaunchKernelEx(&lc, topk_cluster<64>, sc, w.row, me, a->batch.positions, a->k, h1, w.hist2, w.hist3,
+                             w.gteq, a->out_idx);
+    if (e != cudaSuccess) return V4A_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? V4A_OK : V4A_ERR_CUDA;
 }

@@ -318,14 +318,15 @@ class Step:
 
     def launches_per_step(self) -> int:
         """libv4a kernels one run() launches: compress (1); indexer workspace
-        clear (1) + scan (1) + top-k (1 for rows that fit in shared memory; for
-        longer rows 1 when the tensor-core scan built the histogram, else
-        histogram + select); attention (1, + combine when the key list is
-        split); output (1)."""
+        clear (1) + scan (1) + top-k (1, plus the histogram kernel for long
+        rows scored on the CUDA cores); attention (1, + combine when the key
+        list is split); output (1)."""
         s = self.layer.spec
         n = 1
         if s.ix_heads:
             tc_scan = s.ix_fmt in (IX_FP8_B128, IX_FP4_B32, IX_FP4_MX32) and s.ix_heads == 64 and s.ix_dim == 128
+            # clear + scan, then the top-k: one kernel (plus the histogram
+            # kernel for long rows scored on the CUDA cores)
             n += 2 + (1 if s.max_blocks * 64 <= 32768 or tc_scan else 2)
         # the tensor-core attention runs long batches (chunked prefill) as
         # several launches of at most 64 waves of 152 CTAs, one CTA per

@@ -188,7 +188,8 @@ typedef struct {
   const void* q;               /* [T][H_I][keys.dim] */
   const float* q_scale;        /* [T][H_I] (fp8 query only) */
   const float* weights;        /* [T][H_I] */
-  int32_t k;                   /* 1 <= k <= 16384 */
+  int32_t k;                   /* 1 <= k <= 16384; V4A_ERR_UNSUPPORTED when a block-table row
+                                  addresses more than 2^20 entries (keys.max_blocks * 64) */
   int32_t* out_idx;            /* [T][k] */
   int32_t* status;
 } v4a_index_args;
@@ -221,9 +222,9 @@ V4A_API int v4a_index_select(const v4a_index_args* args, void* workspace, size_t
  * library's device image (device memory it holds once its device code is
  * loaded on a device); the call allocates and frees nothing.  Returns
  * V4A_ERR_WORKSPACE, launching nothing, when the arguments need more than that
- * (v4a_index_workspace_size(args) > V4A_INDEX_STATIC_SCRATCH_BYTES; 16 MiB
- * holds, at k = 2048, 4 queries over 262,144 visible entries each or 16 over
- * 65,536);
+ * (v4a_index_workspace_size(args) > V4A_INDEX_STATIC_SCRATCH_BYTES; the
+ * scratch is 4 bytes per entry a query's block-table row can address plus
+ * 16 KB per query, so 16 MiB holds 15 queries over 262,144 entries each);
  * otherwise it returns exactly what v4a_index_topk would with a workspace of
  * that size, and writes the same out_idx.
  *

@@ -67,13 +67,14 @@ def test_fewer_entries_than_k_and_first_entry():
     U.check_close(step.o.float().cpu().numpy(), np.stack([att[t][0] for t in range(2)]), U.BF16_TOL)
 
 
+@pytest.mark.parametrize("fmt", [I.IX_FP4_B32, I.IX_FP4_MX32])
 @pytest.mark.parametrize("cached", [(12000, 16000), (40003, 39000), (150003, 140000)])
-def test_all_tied_scores_take_lowest_indices(cached):
+def test_all_tied_scores_take_lowest_indices(cached, fmt):
     """w = 0 makes every score 0: the top-k must be the k lowest entry indices
     (single-CTA path while a block-table row spans <= 32K entries, multi-CTA
     path beyond: 150,003 positions give rows of 37,504 entries)."""
     v4a = _v4a()
-    spec = dataclasses.replace(I.c4a_decode_1m(), name="ties", batch=2, cached=cached)
+    spec = dataclasses.replace(I.c4a_decode_1m(), name="ties", batch=2, cached=cached, ix_fmt=fmt)
     case = I.make_case(spec, seed=2)
     case.w_i = torch.zeros_like(case.w_i)
     L = v4a.DeviceLayer.from_case(case)

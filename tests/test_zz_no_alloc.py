@@ -37,8 +37,8 @@ def _shape_only_args(spec) -> v4a.IndexArgs:
 
 
 def _oversize_spec():
-    # 30 prefill queries over ~50K entries: ~19 MB of scratch (> 16 MiB)
-    return dataclasses.replace(I.c4a_decode_1m(), name="static_oversize", batch=1, cached=(200001,), new=30)
+    # 90 prefill queries over ~50K entries: ~20 MB of scratch (> 16 MiB)
+    return dataclasses.replace(I.c4a_decode_1m(), name="static_oversize", batch=1, cached=(200001,), new=90)
 
 
 def test_oversize_rejected_on_host():
