@@ -60,6 +60,8 @@ struct AtcArgs {
   float* part_ml;     // [T][splits][H][2] = (max, sum); max in log2 units
   int32_t* status;
   uint32_t idesc_s, idesc_pv;
+  int sparts;         // S partial accumulators (K split over that many MMA issuers)
+  int nq;             // N groups of O = P K (one MMA issuer each)
   int tma_out;        // rows leave through the output tensor map (H % 8 == 0)
   int direct;         // one chunk per query and no merge kernel after: rows are the output
 };
@@ -129,9 +131,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
   }
   if (tid == 0) {
     tc::mbar_init(&s.bar_q, 1);
-    tc::mbar_init(&s.bar_s, 1);
-    tc::mbar_init(&s.bar_o[0], 1);
-    tc::mbar_init(&s.bar_o[1], 1);
+    tc::mbar_init(&s.bar_s, uint32_t(a.sparts));           // every S issuer's commit
+    const int halves = D > 256 ? D / 256 : 1;
+    tc::mbar_init(&s.bar_o[0], uint32_t(a.nq / halves));   // the O issuers of each half
+    tc::mbar_init(&s.bar_o[1], uint32_t(a.nq / halves));
     s.abort_flag = 0;
     tc::mbar_fence_init();
     if (a.tma_out) tc::prefetch_tmap(&omap);
@@ -250,12 +253,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
   volatile int* abort_flag = &s.abort_flag;
 
   // ---- S = Q K^T ----
-  if (tid == 0) {
+  // A thread issuing tcgen05.mma waits ~0.1 us per instruction (measured on
+  // GB300; several issuing warps multiply the rate), so the D/16 K steps are
+  // split over `sparts` issuers (lane 0 of warps 0..sparts-1), each into its
+  // own 64-column partial accumulator; the softmax sums the partials.
+  if ((tid & 31) == 0 && warp < a.sparts) {
     const uint32_t q0 = tc::smem_u32(Qs), k0 = tc::smem_u32(Ks);
-    for (int st = 0; st < D / 16; ++st) {
+    const int nst = D / 16, per = nst / a.sparts;
+    for (int st = warp * per; st < (warp + 1) * per; ++st) {
       const uint64_t ad = tc::desc_sw128(q0 + (st >> 2) * (kRows * 128)) + 2 * (st & 3);
       const uint64_t bd = tc::desc_sw128(k0 + (st >> 2) * (kKeys * 128)) + 2 * (st & 3);
-      tc::mma_f16(tmem, ad, bd, a.idesc_s, st > 0);
+      tc::mma_f16(tmem + 64 * warp, ad, bd, a.idesc_s, st > warp * per);
     }
     tc::mma_commit(&s.bar_s);
   }
@@ -270,6 +278,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
   if (warp < 4) {
     float v[64];
     tc::tmem_ld64(lane_addr, v);
+    for (int pi = 1; pi < a.sparts; ++pi) {
+      float w[64];
+      tc::tmem_ld64(lane_addr + 64 * pi, w);
+#pragma unroll
+      for (int n = 0; n < 64; ++n) v[n] += w[n];
+    }
     const float4* kf4 = reinterpret_cast<const float4*>(s.kf);
 #pragma unroll
     for (int n = 0; n < 64; n += 4) {
@@ -305,20 +319,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
   __syncthreads();
   tc::tc_fence_after();
   // ---- O = P K (S columns are free again) ----
-  // Two N = 256 halves, each with its own commit, so the first half drains
-  // while the tensor core computes the second.
+  // D split into `nq` N groups, one MMA issuer each (lane 0 of warps
+  // 0..nq-1); the groups of each N = 256 half commit to that half's barrier,
+  // so the first half drains while the tensor core computes the second.
   const int halves = D > 256 ? D / 256 : 1;
-  if (tid == 0 && !*abort_flag) {
+  if ((tid & 31) == 0 && warp < a.nq && !*abort_flag) {
     const uint32_t p0 = tc::smem_u32(Ps), k0 = tc::smem_u32(Ks);
-    const int nchunk = D > 256 ? 4 : nsub;        // 64-column N chunks per MMA
-    for (int hf = 0; hf < halves; ++hf) {
-      for (int st = 0; st < kKeys / 16; ++st) {
-        const uint64_t ad = tc::desc_sw128(p0) + 2 * st;
-        const uint64_t bd = desc_sw128_mn(k0 + hf * nchunk * (kKeys * 128) + st * 16 * 128, kKeys * 128);
-        tc::mma_f16(tmem + hf * 256, ad, bd, a.idesc_pv, st > 0);
-      }
-      tc::mma_commit(&s.bar_o[hf]);
+    const int N = D / a.nq, g = warp;              // this issuer's columns [g * N, g * N + N)
+    for (int st = 0; st < kKeys / 16; ++st) {
+      const uint64_t ad = tc::desc_sw128(p0) + 2 * st;
+      const uint64_t bd = desc_sw128_mn(k0 + g * (N / 64) * (kKeys * 128) + st * 16 * 128, kKeys * 128);
+      tc::mma_f16(tmem + g * N, ad, bd, a.idesc_pv, st > 0);
     }
+    tc::mma_commit(&s.bar_o[(g * N) / (D / halves)]);
   }
   if (warp < 4) { s.row_l[row] = l; s.row_m[row] = mx; }
   __syncthreads();
@@ -568,7 +581,10 @@ bool attn_tc(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t str
   if (keep) *keep = AttnPartials{t.part_o, t.part_ml, int(S)};
   t.status = a->status;
   t.idesc_s = tc::make_idesc(1, 1, kRows, kKeys);
-  t.idesc_pv = tc::make_idesc(1, 1, kRows, D > 256 ? 256 : D) | (1u << 16);   // B is MN-major
+  // S partials: 64 columns each within the D columns allocated; O groups of >= 64 columns
+  t.sparts = D >= 256 ? 4 : 2;
+  t.nq = D >= 256 ? 4 : 2;
+  t.idesc_pv = tc::make_idesc(1, 1, kRows, uint32_t(D / t.nq)) | (1u << 16);   // B is MN-major
   // Q as a 2-D tensor [T*H rows][D] bf16, boxes of 64 columns x 128 rows, 128-B swizzle
   CUtensorMap qmap, omap;
   if (!encode_rows(&qmap, t.q, int64_t(T) * H, int(D), kRows)) { *rc = V4A_ERR_CUDA; return true; }

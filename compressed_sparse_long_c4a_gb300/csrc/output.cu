@@ -91,7 +91,8 @@ inv_rope_quant_kernel(const OutDev a) {
   // this token's output unwritten rather than hanging the GPU)
   const long long t0 = clock64();
   bool landed = false;
-  while (copy_ok && !(landed = tc::mbar_try_wait_sleep(&bar, 0, 20000u)) && clock64() - t0 < 2000000000LL) {}
+  // (non-blocking polls: a thread suspended in try_wait resumed up to ~0.5 us late on GB300)
+  while (copy_ok && !(landed = tc::mbar_test(&bar, 0)) && clock64() - t0 < 2000000000LL) {}
   __syncthreads();
 
   if (a.fmt == V4A_OUT_BF16) {
@@ -119,10 +120,11 @@ inv_rope_quant_kernel(const OutDev a) {
   amax = block_reduce<true>(amax, red);
   if (threadIdx.x == 0) slice_amax = amax;
   cluster.sync();
-  if (threadIdx.x == 0) {
-    float mx = 0.f;
-    for (int r = 0; r < kSlices; ++r) mx = fmaxf(mx, *cluster.map_shared_rank(&slice_amax, r));
-    red[0] = mx;
+  if (threadIdx.x < 32) {
+    // one lane per CTA of the cluster, all remote reads in flight together
+    float mx = threadIdx.x < unsigned(kSlices) ? *cluster.map_shared_rank(&slice_amax, int(threadIdx.x)) : 0.f;
+    mx = warp_max(mx);
+    if (threadIdx.x == 0) red[0] = mx;
   }
   cluster.sync();   // no CTA leaves while others may still read its slice_amax
   const float tok = red[0];
@@ -289,10 +291,12 @@ __global__ void __launch_bounds__(kMergeThreads) merge_out_kernel(const MergeDev
   amax = block_reduce<true>(amax, red);
   if (threadIdx.x == 0) slice_amax = amax;
   cluster.sync();
-  if (threadIdx.x == 0) {
-    float mx = 0.f;
-    for (int r = 0; r < csize; ++r) mx = fmaxf(mx, *cluster.map_shared_rank(&slice_amax, r));
-    red[0] = mx;
+  if (threadIdx.x < 32) {
+    // one lane per CTA of the cluster: remote shared-memory reads take ~0.25 us
+    // each on GB300, so they are issued together rather than one after another
+    float mx = threadIdx.x < unsigned(csize) ? *cluster.map_shared_rank(&slice_amax, int(threadIdx.x)) : 0.f;
+    mx = warp_max(mx);
+    if (threadIdx.x == 0) red[0] = mx;
   }
   cluster.sync();   // no CTA leaves while others may still read its slice_amax
   const float tok = red[0];
