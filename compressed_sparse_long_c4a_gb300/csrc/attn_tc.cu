@@ -12,7 +12,8 @@
 //   K     64 gathered rows [64][D] bf16 (fp8 codes are converted exactly to
 //         bf16 on the way in; their per-row scale is applied to the logits
 //         and to P)
-//   S     = Q K^T           M=128, N=64,  K=D   -> TMEM columns [0, 64)
+//   S     = Q K^T           M=128, N=64,  K=D   -> summed from 2-4 partial
+//         accumulators of 64 TMEM columns, each over a quarter (half) of K
 //   P     = 2^(S*f_n - max) * s_n, bf16 -> smem (one thread per head row;
 //         f_n = tau * log2(e) * s_n folds the softmax scale and the key's
 //         dequantisation scale into one factor per key)
@@ -24,7 +25,8 @@
 // boxes, and leaves with TMA tensor stores: whole lines, no partial-sector
 // writes.  With several chunks per query the rows go to the workspace with
 // the chunk's (max, sum) and a combine kernel merges them; with one chunk
-// they are the output.  A single thread issues every MMA; completion is
+// they are the output.  The MMAs are issued by one lane of each of several
+// warps (an issuing thread stalls ~0.1 us per instruction); completion is
 // tracked with tcgen05.commit on mbarriers whose waits are bounded.
 
 #include <mutex>
@@ -61,6 +63,7 @@ struct AtcArgs {
   int32_t* status;
   uint32_t idesc_s, idesc_pv;
   int sparts;         // S partial accumulators (K split over that many MMA issuers)
+  int rshift, eshift; // log2 of the compression ratio and of the entries per block
   int nq;             // N groups of O = P K (one MMA issuer each)
   int tma_out;        // rows leave through the output tensor map (H % 8 == 0)
   int direct;         // one chunk per query and no merge kernel after: rows are the output
@@ -74,7 +77,8 @@ struct ASmem {   // every field read with vector loads carries its alignment exp
   alignas(16) float kf[kKeys];      // tau * log2(e) * key scale, or 0 for an empty slot (read as float4)
   alignas(16) float ks[kKeys];      // key scale (applied to P), 0 for an empty slot (read as float4)
   int kfmt[kKeys];                  // -1: no key in this slot
-  float row_l[kRows], row_m[kRows];   // softmax sums / maxima handed to the drain warps
+  const float* sptr[kKeys];         // the key's dequantisation scale, or null (scale 1)
+  float red_m[2][kRows], red_l[2][kRows];   // per-half row maxima / sums of the softmax
 };
 
 // MN-major operand (B of P*K): 64-element (128-byte) rows along N, consecutive
@@ -90,22 +94,51 @@ __device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t saddr, uint32_t lbo) 
   return d;
 }
 
-__device__ __forceinline__ uint32_t bf16x2_from_e4m3x2(uint16_t two) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
-  const float2 f = __half22float2(__half2(h));
-  const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);   // exact: e4m3 values are bf16 values
-  return *reinterpret_cast<const uint32_t*>(&b);
+// 32 lanes x 16 consecutive fp32 columns into v[0..15], not waited for: the
+// registers are valid only after tc::tmem_wait_ld on the array holding them.
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, float* v) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Exact e4m3 -> bf16 of the four codes in w (lowest byte first), in integer
+// and bf16 arithmetic only (the conversion instructions are the slow part of
+// staging a key tile otherwise).  A code's sign goes to bit 15 and its 7
+// magnitude bits to bits 4..10, giving the bf16 whose exponent field is the
+// code's 4-bit exponent field: the code's value times 2^-120, a subnormal bf16
+// for a subnormal code.  One bf16x2 multiply by 2^120 (bf16 arithmetic keeps
+// subnormal inputs) restores it.  The NaN codes 0x7F / 0xFF, which the encoder
+// never writes, come out as +-480.
+__device__ __forceinline__ uint2 bf16x4_from_e4m3x4(uint32_t w) {
+  const uint32_t a = __byte_perm(w, 0u, 0x1404);   // code 1 << 24 | code 0 << 8
+  const uint32_t b = __byte_perm(w, 0u, 0x3424);   // code 3 << 24 | code 2 << 8
+  const uint32_t ma = ((a >> 4) & 0x07F007F0u) | (a & 0x80008000u);
+  const uint32_t mb = ((b >> 4) & 0x07F007F0u) | (b & 0x80008000u);
+  uint2 r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r.x) : "r"(ma), "r"(0x7B807B80u));   // 0x7B80 = bf16 2^120
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r.y) : "r"(mb), "r"(0x7B807B80u));
+  return r;
 }
 
 // Byte offset of 16-byte chunk `ch` (0..7) of row r inside a 128-byte swizzled box.
 __device__ __forceinline__ uint32_t sw_off(int r, int ch) { return uint32_t(r * 128 + ((ch ^ (r & 7)) << 4)); }
 
+// kD: the head dimension as a compile-time constant, so that the index
+// arithmetic of the staging and drain loops is shifts and masks (these
+// phases run on a few warps per SM and are bound by instruction latency).
+template <int kD>
 __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
                                                              const __grid_constant__ CUtensorMap qmap,
                                                              const __grid_constant__ CUtensorMap omap) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int D = a.D, nsub = D / 64;
+  constexpr int D = kD, nsub = kD / 64;
   uint8_t* Qs = base;                                  // nsub x [128 rows][128 B]; later the O rows
   uint8_t* Ks = Qs + nsub * kRows * 128;               // nsub x [64 rows][128 B]
   uint8_t* Ps = Ks + nsub * kKeys * 128;               // [128 rows][128 B]
@@ -113,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
   const int tid = threadIdx.x, warp = tid >> 5;
   const int t = blockIdx.y, sp = blockIdx.x;
   const int b = a.seq_ids[t], m = a.positions[t];
-  const int nvis = (m + 1) / a.ratio;
+  const int nvis = (m + 1) >> a.rshift;
   const int nsel = a.idx ? a.k : nvis;
   const int wstart = max(0, m - a.wlen + 1);
   const int L = nsel + (m - wstart + 1);
@@ -151,18 +184,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
   // caches and the window ring are read only after it has completed
   pdl_wait();
 
-  // ---- key slots of this chunk (sources, scales) ----
+  // ---- key slots of this chunk (sources; the scales are loaded with the rows) ----
   if (tid < kKeys) {
     const int li = lo + tid;
     const uint8_t* src = nullptr;
+    const float* sp = nullptr;
     int f = -1;
-    float sc = 1.f;
     if (li < L) {
       if (li < nsel) {
         const int e = a.idx ? a.idx[int64_t(t) * a.k + li] : li;
         if (e >= 0) {
-          const int E = entries_per_block(a.ratio);
-          const int lb = e / E;
+          const int E = 1 << a.eshift;
+          const int lb = e >> a.eshift;
           if (e >= nvis) {
             report(a.status, V4A_DEV_BAD_INDEX);
           } else if (lb >= a.max_blocks) {
@@ -173,10 +206,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
               report(a.status, V4A_DEV_BAD_BLOCK);
             } else {
               const uint8_t* bb = a.pool + int64_t(blk) * a.block_bytes;
-              const int slot = e % E;
+              const int slot = e & (E - 1);
               f = a.fmt;
               src = bb + int64_t(slot) * (a.fmt == V4A_KV_BF16 ? 2 * D : D);
-              if (a.fmt == V4A_KV_FP8_TOKEN) sc = reinterpret_cast<const float*>(bb + int64_t(E) * D)[slot];
+              if (a.fmt == V4A_KV_FP8_TOKEN) sp = reinterpret_cast<const float*>(bb + int64_t(E) * D) + slot;
             }
           }
         }
@@ -185,12 +218,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
         const int64_t slot = int64_t(b) * a.wcap + p % a.wcap;
         f = a.wfmt;
         src = a.window + slot * (a.wfmt == V4A_KV_BF16 ? 2 * D : D);
-        if (a.wfmt == V4A_KV_FP8_TOKEN) sc = a.wscale[slot];
+        if (a.wfmt == V4A_KV_FP8_TOKEN) sp = a.wscale + slot;
       }
     }
     s.src[tid] = src;
-    s.kf[tid] = f >= 0 ? sc * a.scale * kLog2e : 0.f;
-    s.ks[tid] = f >= 0 ? sc : 0.f;
+    s.sptr[tid] = sp;
     s.kfmt[tid] = f;
   }
   __syncthreads();
@@ -200,47 +232,49 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
   // (16 codes) into registers, all in flight together, then each converted
   // exactly to 16 bf16 values = two 16-byte chunks.
   {
-    const int bchunks = kKeys * (D / 8);              // 16-byte bf16 chunks of the tile
-    const int fchunks = kKeys * (D / 16);             // 16-byte fp8 chunks of the tile
-    constexpr int kMaxPer = kKeys * (512 / 16) / kThreads;   // 8 for D = 512
-    uint4 raw[kMaxPer];
+    constexpr int kBchunks = kKeys * (D / 8);         // 16-byte bf16 chunks of the tile
+    constexpr int kPer = kKeys * (D / 16) / kThreads;  // 16-byte fp8 chunks per thread
+    uint4 raw[kPer];
 #pragma unroll
-    for (int i = 0; i < kMaxPer; ++i) {
+    for (int i = 0; i < kPer; ++i) {
       const int c = tid + i * kThreads;
-      raw[i] = make_uint4(0, 0, 0, 0);
-      if (c >= fchunks) continue;
       const int r = c / (D / 16), cc = c % (D / 16);
+      raw[i] = make_uint4(0, 0, 0, 0);
       if (s.kfmt[r] == V4A_KV_FP8_TOKEN) raw[i] = __ldg(reinterpret_cast<const uint4*>(s.src[r] + cc * 16));
     }
-    for (int c = tid; c < bchunks; c += kThreads) {
-      const int r = c / (D / 8), cc = c % (D / 8);
-      if (s.kfmt[r] != V4A_KV_BF16) continue;
-      uint8_t* dst = Ks + (cc >> 3) * (kKeys * 128) + sw_off(r, cc & 7);
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(s.src[r] + cc * 16)
-                   : "memory");
+    float sc = 1.f;   // thread tid < kKeys: key tid's scale, in flight with the rows
+    if (tid < kKeys && s.sptr[tid]) sc = __ldg(s.sptr[tid]);
+    if (a.fmt == V4A_KV_BF16 || a.wfmt == V4A_KV_BF16) {
+      for (int c = tid; c < kBchunks; c += kThreads) {
+        const int r = c / (D / 8), cc = c % (D / 8);
+        if (s.kfmt[r] != V4A_KV_BF16) continue;
+        uint8_t* dst = Ks + (cc >> 3) * (kKeys * 128) + sw_off(r, cc & 7);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(s.src[r] + cc * 16)
+                     : "memory");
+      }
     }
 #pragma unroll
-    for (int i = 0; i < kMaxPer; ++i) {
+    for (int i = 0; i < kPer; ++i) {
       const int c = tid + i * kThreads;
-      if (c >= fchunks) continue;
       const int r = c / (D / 16), cc = c % (D / 16);   // fp8 chunk cc -> bf16 chunks 2cc, 2cc+1
       const int f = s.kfmt[r];
       if (f == V4A_KV_BF16) continue;
       uint4 v0 = make_uint4(0, 0, 0, 0), v1 = make_uint4(0, 0, 0, 0);
       if (f == V4A_KV_FP8_TOKEN) {
-        v0.x = bf16x2_from_e4m3x2(uint16_t(raw[i].x & 0xffffu));
-        v0.y = bf16x2_from_e4m3x2(uint16_t(raw[i].x >> 16));
-        v0.z = bf16x2_from_e4m3x2(uint16_t(raw[i].y & 0xffffu));
-        v0.w = bf16x2_from_e4m3x2(uint16_t(raw[i].y >> 16));
-        v1.x = bf16x2_from_e4m3x2(uint16_t(raw[i].z & 0xffffu));
-        v1.y = bf16x2_from_e4m3x2(uint16_t(raw[i].z >> 16));
-        v1.z = bf16x2_from_e4m3x2(uint16_t(raw[i].w & 0xffffu));
-        v1.w = bf16x2_from_e4m3x2(uint16_t(raw[i].w >> 16));
+        const uint2 b0 = bf16x4_from_e4m3x4(raw[i].x), b1 = bf16x4_from_e4m3x4(raw[i].y);
+        const uint2 b2 = bf16x4_from_e4m3x4(raw[i].z), b3 = bf16x4_from_e4m3x4(raw[i].w);
+        v0 = make_uint4(b0.x, b0.y, b1.x, b1.y);
+        v1 = make_uint4(b2.x, b2.y, b3.x, b3.y);
       }
       const int c0 = 2 * cc;
       uint8_t* sub = Ks + (c0 >> 3) * (kKeys * 128);
       *reinterpret_cast<uint4*>(sub + sw_off(r, c0 & 7)) = v0;
       *reinterpret_cast<uint4*>(sub + sw_off(r, (c0 + 1) & 7)) = v1;
+    }
+    if (tid < kKeys) {   // read after the barrier before the MMAs
+      const bool live = s.kfmt[tid] >= 0;
+      s.kf[tid] = live ? sc * a.scale * kLog2e : 0.f;
+      s.ks[tid] = live ? sc : 0.f;
     }
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
@@ -253,13 +287,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
   volatile int* abort_flag = &s.abort_flag;
 
   // ---- S = Q K^T ----
-  // A thread issuing tcgen05.mma waits ~0.1 us per instruction (measured on
-  // GB300; several issuing warps multiply the rate), so the D/16 K steps are
-  // split over `sparts` issuers (lane 0 of warps 0..sparts-1), each into its
-  // own 64-column partial accumulator; the softmax sums the partials.
+  // One thread issuing tcgen05.mma stalls ~0.1 us per instruction; several
+  // issuing warps overlap up to the SM's rate of ~30 ns per instruction
+  // (either measured on GB300, at N = 32 or 64).  The D/16 K steps are split
+  // over `sparts` issuers (lane 0 of warps 0..sparts-1), each into its own
+  // 64-column partial accumulator; the softmax sums the partials.
   if ((tid & 31) == 0 && warp < a.sparts) {
     const uint32_t q0 = tc::smem_u32(Qs), k0 = tc::smem_u32(Ks);
-    const int nst = D / 16, per = nst / a.sparts;
+    constexpr int nst = D / 16;
+    const int per = nst / a.sparts;
     for (int st = warp * per; st < (warp + 1) * per; ++st) {
       const uint64_t ad = tc::desc_sw128(q0 + (st >> 2) * (kRows * 128)) + 2 * (st & 3);
       const uint64_t bd = tc::desc_sw128(k0 + (st >> 2) * (kKeys * 128)) + 2 * (st & 3);
@@ -267,52 +303,74 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
     }
     tc::mma_commit(&s.bar_s);
   }
-  // ---- softmax: warps 0-3, thread = head row ----
-  const int row = tid & (kRows - 1);             // warp w reads TMEM lanes 32(w%4)..+31
+  // ---- softmax: all 8 warps; thread (row, hf) takes keys [32 hf, 32 hf + 32) of head row `row` ----
+  // (warps w and w + 4 read the same TMEM lane quarter; the two halves of a
+  // row meet through shared memory for the max and the sum)
+  const int row = tid & (kRows - 1), hf = warp >> 2;
   const uint32_t lane_addr = tmem + (uint32_t((warp & 3) * 32) << 16);
   // Collective tcgen05 loads below are always executed by whole warps; `ok`
   // is made warp-uniform and only gates the arithmetic and the stores.
   bool ok = __all_sync(0xffffffffu, tc::mbar_wait(&s.bar_s, 0, a.status, abort_flag));
   tc::tc_fence_after();
-  float mx = -INFINITY, l = 0.f;
-  if (warp < 4) {
-    float v[64];
-    tc::tmem_ld64(lane_addr, v);
-    for (int pi = 1; pi < a.sparts; ++pi) {
-      float w[64];
-      tc::tmem_ld64(lane_addr + 64 * pi, w);
+  float mx, l;
+  {
+    float v[32];
+    {
+      float w0[64], w1[64];   // w0: partials 0 and 1, w1: partials 2 and 3 (32 columns each)
+      tmem_ld16_nowait(lane_addr + 32 * hf, w0);
+      tmem_ld16_nowait(lane_addr + 32 * hf + 16, w0 + 16);
+      tmem_ld16_nowait(lane_addr + 64 + 32 * hf, w0 + 32);
+      tmem_ld16_nowait(lane_addr + 64 + 32 * hf + 16, w0 + 48);
+      if (a.sparts == 4) {
+        tmem_ld16_nowait(lane_addr + 128 + 32 * hf, w1);
+        tmem_ld16_nowait(lane_addr + 128 + 32 * hf + 16, w1 + 16);
+        tmem_ld16_nowait(lane_addr + 192 + 32 * hf, w1 + 32);
+        tmem_ld16_nowait(lane_addr + 192 + 32 * hf + 16, w1 + 48);
+        tc::tmem_wait_ld(w0);
+        tc::tmem_wait_ld(w1);
 #pragma unroll
-      for (int n = 0; n < 64; ++n) v[n] += w[n];
+        for (int n = 0; n < 32; ++n) v[n] = (w0[n] + w0[32 + n]) + (w1[n] + w1[32 + n]);
+      } else {
+        tc::tmem_wait_ld(w0);
+#pragma unroll
+        for (int n = 0; n < 32; ++n) v[n] = w0[n] + w0[32 + n];
+      }
     }
-    const float4* kf4 = reinterpret_cast<const float4*>(s.kf);
+    const float4* kf4 = reinterpret_cast<const float4*>(s.kf) + 8 * hf;
+    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-    for (int n = 0; n < 64; n += 4) {
+    for (int n = 0; n < 32; n += 4) {
       const float4 f = kf4[n >> 2];
-      // z in log2 units; an empty slot has factor 0 and is masked below
+      // z in log2 units; an empty slot has factor 0 and is masked
       v[n] *= f.x; v[n + 1] *= f.y; v[n + 2] *= f.z; v[n + 3] *= f.w;
-      if (f.x != 0.f) mx = fmaxf(mx, v[n]);
-      if (f.y != 0.f) mx = fmaxf(mx, v[n + 1]);
-      if (f.z != 0.f) mx = fmaxf(mx, v[n + 2]);
-      if (f.w != 0.f) mx = fmaxf(mx, v[n + 3]);
+      if (f.x != 0.f) m4[0] = fmaxf(m4[0], v[n]);
+      if (f.y != 0.f) m4[1] = fmaxf(m4[1], v[n + 1]);
+      if (f.z != 0.f) m4[2] = fmaxf(m4[2], v[n + 2]);
+      if (f.w != 0.f) m4[3] = fmaxf(m4[3], v[n + 3]);
     }
-    const float4* ks4 = reinterpret_cast<const float4*>(s.ks);
-    uint32_t pk[32];
+    s.red_m[hf][row] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+    __syncthreads();
+    mx = fmaxf(s.red_m[0][row], s.red_m[1][row]);
+    const float4* ks4 = reinterpret_cast<const float4*>(s.ks) + 8 * hf;
+    uint32_t pk[16];
+    float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int n = 0; n < 64; n += 4) {
+    for (int n = 0; n < 32; n += 4) {
       const float4 k = ks4[n >> 2];
       const float p0 = k.x != 0.f ? exp2f(v[n] - mx) : 0.f;
       const float p1 = k.y != 0.f ? exp2f(v[n + 1] - mx) : 0.f;
       const float p2 = k.z != 0.f ? exp2f(v[n + 2] - mx) : 0.f;
       const float p3 = k.w != 0.f ? exp2f(v[n + 3] - mx) : 0.f;
-      l += (p0 + p1) + (p2 + p3);
+      l4[0] += p0; l4[1] += p1; l4[2] += p2; l4[3] += p3;
       const __nv_bfloat162 b01 = __floats2bfloat162_rn(p0 * k.x, p1 * k.y);
       const __nv_bfloat162 b23 = __floats2bfloat162_rn(p2 * k.z, p3 * k.w);
       pk[n >> 1] = *reinterpret_cast<const uint32_t*>(&b01);
       pk[(n >> 1) + 1] = *reinterpret_cast<const uint32_t*>(&b23);
     }
 #pragma unroll
-    for (int c = 0; c < 8; ++c)
-      *reinterpret_cast<uint4*>(Ps + sw_off(row, c)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+    for (int c = 0; c < 4; ++c)
+      *reinterpret_cast<uint4*>(Ps + sw_off(row, 4 * hf + c)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+    s.red_l[hf][row] = (l4[0] + l4[1]) + (l4[2] + l4[3]);
   }
   tc::fence_proxy_async();
   tc::tc_fence_before();
@@ -333,19 +391,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
     }
     tc::mma_commit(&s.bar_o[(g * N) / (D / halves)]);
   }
-  if (warp < 4) { s.row_l[row] = l; s.row_m[row] = mx; }
-  __syncthreads();
-  l = s.row_l[row];
-  mx = s.row_m[row];
+  l = s.red_l[0][row] + s.red_l[1][row];   // written before the barrier above
   const bool store = ok && row < a.H;   // H need not be a multiple of 32: loads stay warp-wide
   const float inv = l > 0.f ? 1.f / l : 0.f;   // a chunk of only padding (-1) entries has l = 0
   const bool direct = a.direct != 0;
-  // half hf's 64-column groups: warps 0-3 drain the first half of them, warps 4-7 the rest
+  // each half's 64-column groups: warps 0-3 drain the first half of them, warps 4-7 the rest
   const int per_half = nsub / halves;
-  for (int hf = 0; hf < halves; ++hf) {
-    ok = __all_sync(0xffffffffu, ok && tc::mbar_wait(&s.bar_o[hf], 0, a.status, abort_flag));
+  for (int half = 0; half < halves; ++half) {
+    ok = __all_sync(0xffffffffu, ok && tc::mbar_wait(&s.bar_o[half], 0, a.status, abort_flag));
     tc::tc_fence_after();
-    const int g0 = hf * per_half, gh = per_half / 2;
+    const int g0 = half * per_half, gh = per_half / 2;
     const int c0 = warp < 4 ? g0 : g0 + gh, c1 = warp < 4 ? g0 + gh : g0 + per_half;
     for (int c = c0; c < c1; ++c) {
       float v[64];
@@ -490,9 +545,9 @@ int splits_of(const v4a_attn_args* a) {
   return int((nsel + a->window_len + kKeys - 1) / kKeys);
 }
 
-// The chunked tensor-core path serves decode-sized batches: one CTA per 64
-// keys of each query, so the CTA count is T * splits.  Long prefill batches
-// use the CUDA-core path (one CTA walks a whole split of a query).
+// One CTA per 64 keys of each query, so the CTA count is T * splits; long
+// batches (chunked prefill) run as several launches of at most kMaxBatchCtas
+// CTAs that share the chunk-result workspace (batch_queries below).
 bool handled(const v4a_attn_args* a) {
   const int D = a->kv.dim;
   if (D != 128 && D != 256 && D != 512) return false;
@@ -554,6 +609,8 @@ bool attn_tc(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t str
   t.H = a->num_heads;
   t.D = a->kv.dim;
   t.ratio = a->kv.ratio;
+  t.rshift = a->kv.ratio == 4 ? 2 : 7;                 // ratio is 4 or 128 (validated by the caller)
+  t.eshift = a->kv.ratio == 4 ? 6 : 1;                 // entries per 256-position block: 64 or 2
   t.fmt = a->kv.format;
   t.wfmt = a->window_format;
   t.wlen = a->window_len;
@@ -602,11 +659,14 @@ bool attn_tc(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t str
   if (smem < 116 * 1024) smem = 116 * 1024;
   static std::once_flag once;
   std::call_once(once, [] {
-    cudaFuncSetAttribute(attn_chunk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaFuncSetAttribute(attn_chunk_tc<512>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaFuncSetAttribute(attn_chunk_tc<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaFuncSetAttribute(attn_chunk_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   });
   if (smem > 227 * 1024) { *rc = V4A_ERR_UNSUPPORTED; return true; }
   // both may start while the kernel before them runs (they wait in-kernel)
-  cudaError_t e = launch_pdl(attn_chunk_tc, dim3(t.splits, t.T), dim3(kThreads), smem, stream, t, qmap, omap);
+  auto kern = D == 512 ? attn_chunk_tc<512> : D == 256 ? attn_chunk_tc<256> : attn_chunk_tc<128>;
+  cudaError_t e = launch_pdl(kern, dim3(t.splits, t.T), dim3(kThreads), smem, stream, t, qmap, omap);
   if (e == cudaSuccess && !t.direct && !keep)
     e = launch_pdl(attn_combine_bf16, dim3(t.H, t.T), dim3(256), 0, stream, t.H, t.D, t.splits,
                    static_cast<const uint16_t*>(t.part_o), static_cast<const float*>(t.part_ml), t.out, t.lse);

@@ -9,9 +9,11 @@ size_t attn_tc_workspace_size(const v4a_attn_args* a);   // 0 when not handled
 // The per-chunk results the attention kernel leaves in the workspace:
 // o [T][splits][H][D] bf16 rows normalised by their chunk's softmax sum, and
 // ml [T][splits][H][2] = (max in log2 units, sum); an empty chunk has max -inf.
+// They are workspace: the fused output stage overwrites chunk 0's entries
+// with the merged rows and their amax.
 struct AttnPartials {
-  const uint16_t* o;
-  const float* ml;
+  uint16_t* o;
+  float* ml;
   int splits;
 };
 

@@ -147,200 +147,210 @@ inv_rope_quant_kernel(const OutDev a) {
 // ---- attention merge fused with the output stage ------------------------------
 //
 // For the tensor-core attention's chunk results (normalised bf16 rows plus
-// (max, sum) per chunk): one cluster of `csize` CTAs per token, CTA r owning
-// heads [r*H/csize, (r+1)*H/csize).  Each thread merges one (head, 8-dim chunk)
-// over all chunks of the query with the weights and the summation order of the
-// stand-alone merge (four interleaved groups of chunks, then group 0 + 1 + 2 +
-// 3), rounds to bf16 as the stored attention output would be, and leaves the
-// row in shared memory; the rest is the output stage above (rotation by
-// -angle, token amax through distributed shared memory, encode), so the bytes
-// equal those of the two-call path.  The bf16 attention output never goes to
-// HBM and one kernel boundary disappears.
-constexpr int kMergeThreads = 1024;
+// (max, sum) per chunk), two kernels that need no thread-block cluster, so
+// that both spread over every SM:
+//  merge_amax: one CTA per (head, token) merges the head's chunk rows with the
+//    weights and the summation order of the stand-alone merge (four
+//    interleaved groups of chunks, then group 0 + 1 + 2 + 3), rounds to bf16
+//    as the stored attention output would be, and leaves the row in the
+//    workspace in place of the head's chunk-0 row, with the amax of the row
+//    rotated by -angle in place of chunk 0's (max, sum);
+//  encode_rows: kEncSlices CTAs per token take the token amax over its heads,
+//    rotate their share of the merged rows and encode it.
+// The bf16 attention output never leaves the workspace, and the bytes equal
+// those of the two-call path.
 constexpr int kMergeGroups = 4;          // chunk groups: chunk sp belongs to group sp % 4
-constexpr int kMergeItems = kMergeThreads / kMergeGroups;   // (head, 8-dim chunk) items per round
-constexpr int kMergeBatch = 9;           // chunk rows in flight per thread (34 chunks: one batch)
-constexpr int kMergeMaxSplits = 64;
-constexpr int kMergeMaxRows = 16;        // heads per CTA
+constexpr int kMergeMaxSplits = 64;      // kPer <= 16 chunks per group held in registers
+constexpr int kEncSlices = 16;           // encode CTAs per token
+constexpr int kEncPer = 4;               // 16-byte chunks per encode thread held in registers
 
 struct MergeDev {
   RopeFreq rope;
-  int T, H, D, R, fmt, splits;
+  int H, D, R, fmt, splits;
   const int32_t* positions;
-  const uint16_t* part_o;
-  const float* part_ml;
-  void* out;
-  float* out_scale;
+  uint16_t* part_o;   // [T][splits][H][D]; chunk 0's rows receive the merged rows
+  float* part_ml;     // [T][splits][H][2]; chunk 0's pairs receive (row amax, 0)
 };
 
-__global__ void __launch_bounds__(kMergeThreads) merge_out_kernel(const MergeDev a) {
-  __shared__ __align__(128) uint4 rows_s[kMaxSlice / 16];
-  __shared__ float4 part_s[kMergeGroups - 1][kMergeItems][2];
-  __shared__ float wsm[kMergeMaxRows][kMergeMaxSplits];
-  __shared__ float inv_s[kMergeMaxRows];
+// kPer: chunks per group held in registers (splits <= 4 * kPer), as small as
+// the split count allows so that four CTAs fit an SM and every (head, token)
+// of a decode batch has its loads in flight in one wave.
+template <int kPer>
+__global__ void __launch_bounds__(256, kPer <= 9 ? 4 : 2) merge_amax_kernel(const MergeDev a) {
+  __shared__ float wsm[kMergeMaxSplits];
+  __shared__ float inv_s;
+  __shared__ float4 part_s[kMergeGroups - 1][64][2];
   __shared__ float cs[128];
-  __shared__ float red[32];
-  __shared__ float slice_amax;
-  cg::cluster_group cluster = cg::this_cluster();
-  const int csize = int(cluster.num_blocks());
-  const int rank = int(cluster.block_rank());
-  const int t = blockIdx.x / csize;
-  const int hp = a.H / csize, h0 = rank * hp;
-  const int per_head = a.D / 8;
-  const int nchunks = hp * per_head;                   // 16-byte chunks of this CTA's rows
-  const int first = a.D - a.R;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ float red[2];
+  const int t = blockIdx.y, h = blockIdx.x;
+  const int grp = threadIdx.x >> 6, c = threadIdx.x & 63;
+  const bool active = c < a.D / 8;
+  const bool fp8 = a.fmt == V4A_OUT_FP8_TOKEN;
   pdl_trigger();
-  rope_table(a.positions[t], a.R, a.rope, cs);        // positions are a step input
-  pdl_wait();                                          // the chunk results are the previous kernel's
-  // 1. chunk weights of every head of this CTA (as in the stand-alone merge)
-  for (int hh = warp; hh < hp; hh += kMergeThreads / 32) {
-    const float* ml = a.part_ml + (int64_t(t) * a.splits * a.H + h0 + hh) * 2;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    if (lane < a.splits) { m0 = ml[int64_t(lane) * a.H * 2]; l0 = ml[int64_t(lane) * a.H * 2 + 1]; }
-    if (lane + 32 < a.splits) { m1 = ml[int64_t(lane + 32) * a.H * 2]; l1 = ml[int64_t(lane + 32) * a.H * 2 + 1]; }
-    const float mx = warp_max(fmaxf(m0, m1));
-    const float w0 = m0 == -INFINITY ? 0.f : l0 * exp2f(m0 - mx);
-    const float w1 = m1 == -INFINITY ? 0.f : l1 * exp2f(m1 - mx);
-    if (lane < a.splits) wsm[hh][lane] = w0;
-    if (lane + 32 < a.splits) wsm[hh][lane + 32] = w1;
-    const float tot = warp_sum(w0 + w1);
-    if (lane == 0) inv_s[hh] = tot > 0.f ? 1.f / tot : 0.f;
-  }
-  __syncthreads();
-  // 2. merged rows, rounded to bf16, into shared memory.  Thread (g, i) sums
-  //    the chunks of group g for item i of the round in increasing order (one
-  //    warp = 32 consecutive items of one group: whole 512-byte runs per load);
-  //    group 0 then adds groups 1, 2, 3 in that order.
-  const int g = threadIdx.x / kMergeItems, il = threadIdx.x % kMergeItems;
-  for (int base = 0; base < nchunks; base += kMergeItems) {
-    const int c = base + il;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    const bool live = c < nchunks;
-    const int hh = live ? c / per_head : 0, cc = live ? c % per_head : 0;
-    const uint16_t* po = a.part_o + (int64_t(t) * a.splits * a.H + h0 + hh) * a.D + cc * 8;
-    if (a.splits == 1) {
-      // one chunk: its normalised row is the attention output as stored
-      if (live && g == 0) rows_s[c] = __ldcg(reinterpret_cast<const uint4*>(po));
-      continue;
+  if (fp8) rope_table(a.positions[t], a.R, a.rope, cs);   // positions are a step input
+  pdl_wait();                                              // the chunk results are the previous kernel's
+  uint16_t* po = a.part_o + (int64_t(t) * a.splits * a.H + h) * a.D + c * 8;
+  float* ml = a.part_ml + (int64_t(t) * a.splits * a.H + h) * 2;
+  uint4 row = make_uint4(0, 0, 0, 0);   // group 0: the merged 8 values of item c
+  if (a.splits == 1) {
+    // one chunk: its normalised row is the attention output as stored
+    if (grp == 0 && active) row = __ldcg(reinterpret_cast<const uint4*>(po));
+  } else {
+    // 1. this thread's chunk rows, all loads in flight together
+    uint4 v[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int sp = grp + u * kMergeGroups;
+      v[u] = (active && sp < a.splits) ? __ldcg(reinterpret_cast<const uint4*>(po + int64_t(sp) * a.H * a.D))
+                                       : make_uint4(0, 0, 0, 0);
     }
-    for (int u0 = 0; live && g + kMergeGroups * u0 < a.splits; u0 += kMergeBatch) {
-      uint4 v[kMergeBatch];
-#pragma unroll
-      for (int u = 0; u < kMergeBatch; ++u) {
-        const int sp = g + kMergeGroups * (u0 + u);
-        v[u] = sp < a.splits ? __ldcg(reinterpret_cast<const uint4*>(po + int64_t(sp) * a.H * a.D))
-                             : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int u = 0; u < kMergeBatch; ++u) {
-        const int sp = g + kMergeGroups * (u0 + u);
-        const float w = sp < a.splits ? wsm[hh][sp] : 0.f;
-        if (w == 0.f) continue;
-        const uint32_t q[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          acc[2 * j] = fmaf(w, bf16_to_f32(uint16_t(q[j] & 0xffffu)), acc[2 * j]);
-          acc[2 * j + 1] = fmaf(w, bf16_to_f32(uint16_t(q[j] >> 16)), acc[2 * j + 1]);
-        }
-      }
-    }
-    if (g > 0) {
-      part_s[g - 1][il][0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      part_s[g - 1][il][1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    // 2. weights of every chunk (warp 0), while those loads are in flight
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+      if (lane < a.splits) { m0 = ml[int64_t(lane) * a.H * 2]; l0 = ml[int64_t(lane) * a.H * 2 + 1]; }
+      if (lane + 32 < a.splits) { m1 = ml[int64_t(lane + 32) * a.H * 2]; l1 = ml[int64_t(lane + 32) * a.H * 2 + 1]; }
+      const float mx = warp_max(fmaxf(m0, m1));
+      const float w0 = m0 == -INFINITY ? 0.f : l0 * exp2f(m0 - mx);
+      const float w1 = m1 == -INFINITY ? 0.f : l1 * exp2f(m1 - mx);
+      if (lane < a.splits) wsm[lane] = w0;
+      if (lane + 32 < a.splits) wsm[lane + 32] = w1;
+      const float tot = warp_sum(w0 + w1);
+      if (lane == 0) inv_s = tot > 0.f ? 1.f / tot : 0.f;
     }
     __syncthreads();
-    if (g == 0 && live) {
+    // 3. weighted sum of this thread's chunks (an empty chunk has weight 0)
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int sp = grp + u * kMergeGroups;
+      const float w = sp < a.splits ? wsm[sp] : 0.f;
+      if (w == 0.f) continue;
+      const uint32_t q[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        acc[2 * j] = fmaf(w, bf16_to_f32(uint16_t(q[j] & 0xffffu)), acc[2 * j]);
+        acc[2 * j + 1] = fmaf(w, bf16_to_f32(uint16_t(q[j] >> 16)), acc[2 * j + 1]);
+      }
+    }
+    if (grp > 0) {
+      part_s[grp - 1][c][0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      part_s[grp - 1][c][1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+    __syncthreads();
+    if (grp == 0 && active) {
 #pragma unroll
       for (int g2 = 0; g2 < kMergeGroups - 1; ++g2) {
-        const float4 x = part_s[g2][il][0], y = part_s[g2][il][1];
+        const float4 x = part_s[g2][c][0], y = part_s[g2][c][1];
         acc[0] += x.x; acc[1] += x.y; acc[2] += x.z; acc[3] += x.w;
         acc[4] += y.x; acc[5] += y.y; acc[6] += y.z; acc[7] += y.w;
       }
-      const float inv = inv_s[hh];
+      const float inv = inv_s;
       uint32_t o[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         o[j] = uint32_t(f32_to_bf16(acc[2 * j] * inv)) | (uint32_t(f32_to_bf16(acc[2 * j + 1] * inv)) << 16);
-      rows_s[c] = make_uint4(o[0], o[1], o[2], o[3]);
+      row = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    __syncthreads();   // part_s is rewritten by the next round
   }
-  __syncthreads();
-  // 3. the output stage on those rows
-  const int c0 = rank * nchunks;                       // first chunk of the slice within the token
-  if (a.fmt == V4A_OUT_BF16) {
-    uint4* out = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + int64_t(t) * a.H * a.D) + c0;
-    for (int c = threadIdx.x; c < nchunks; c += kMergeThreads) {
+  // 4. group 0: the merged row in place of chunk 0's, and its rotated amax
+  float amax = 0.f;
+  if (grp == 0 && active) {
+    *reinterpret_cast<uint4*>(po) = row;   // this thread read chunk 0's item c above (or never will)
+    if (fp8) {
       float x[8];
-      rotated_chunk(rows_s[c], ((c0 + c) % per_head) * 8, first, a.R, cs, x);
+      rotated_chunk(row, c * 8, a.D - a.R, a.R, cs, x);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    }
+  }
+  if (threadIdx.x < 64) {
+    amax = warp_max(amax);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  }
+  __syncthreads();   // also orders warp 0's reads of chunk 0's (max, sum) before the write below
+  if (threadIdx.x == 0) {
+    ml[0] = fmaxf(red[0], red[1]);
+    ml[1] = 0.f;
+  }
+}
+
+struct EncDev {
+  RopeFreq rope;
+  int H, D, R, fmt, splits;
+  const int32_t* positions;
+  const uint16_t* part_o;   // merged rows: chunk 0's rows of each token
+  const float* part_ml;     // row amax: chunk 0's pairs
+  void* out;
+  float* out_scale;
+};
+
+__global__ void __launch_bounds__(256) encode_rows_kernel(const EncDev a) {
+  __shared__ float cs[128];
+  __shared__ float tok_s;
+  const int t = blockIdx.x / kEncSlices, r = blockIdx.x % kEncSlices;
+  const int per_head = a.D / 8;
+  const int nch = a.H * per_head;                       // 16-byte bf16 chunks of the token
+  const int per = (nch + kEncSlices - 1) / kEncSlices;
+  const int cb = r * per, ce = min(nch, cb + per);
+  const int first = a.D - a.R;
+  pdl_trigger();
+  rope_table(a.positions[t], a.R, a.rope, cs);
+  pdl_wait();                                           // the merged rows are the previous kernel's
+  const uint4* rows = reinterpret_cast<const uint4*>(a.part_o + int64_t(t) * a.splits * a.H * a.D);
+  // this thread's first kEncPer chunks, in flight while the token amax is formed
+  uint4 w[kEncPer];
+#pragma unroll
+  for (int i = 0; i < kEncPer; ++i) {
+    const int c = cb + threadIdx.x + i * int(blockDim.x);
+    w[i] = c < ce ? __ldcg(rows + c) : make_uint4(0, 0, 0, 0);
+  }
+  if (a.fmt == V4A_OUT_BF16) {
+    __syncthreads();   // cs
+    uint4* out = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + int64_t(t) * a.H * a.D);
+    auto put = [&](int c, uint4 v) {
+      float x[8];
+      rotated_chunk(v, (c % per_head) * 8, first, a.R, cs, x);
       uint32_t u[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) u[i] = uint32_t(f32_to_bf16(x[2 * i])) | (uint32_t(f32_to_bf16(x[2 * i + 1])) << 16);
       out[c] = make_uint4(u[0], u[1], u[2], u[3]);
+    };
+#pragma unroll
+    for (int i = 0; i < kEncPer; ++i) {
+      const int c = cb + threadIdx.x + i * int(blockDim.x);
+      if (c < ce) put(c, w[i]);
     }
+    for (int c = cb + threadIdx.x + kEncPer * int(blockDim.x); c < ce; c += blockDim.x) put(c, __ldcg(rows + c));
     return;
   }
-  float amax = 0.f;
-  for (int c = threadIdx.x; c < nchunks; c += kMergeThreads) {
-    float x[8];
-    rotated_chunk(rows_s[c], ((c0 + c) % per_head) * 8, first, a.R, cs, x);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  if (threadIdx.x < 32) {   // token amax = max over the heads' row amax
+    const float* ml = a.part_ml + int64_t(t) * a.splits * a.H * 2;
+    float m = 0.f;
+    for (int h = threadIdx.x; h < a.H; h += 32) m = fmaxf(m, __ldcg(ml + int64_t(h) * 2));
+    m = warp_max(m);
+    if (threadIdx.x == 0) tok_s = m > 0.f ? m / 448.f : 1.f;
   }
-  amax = block_reduce<true>(amax, red);
-  if (threadIdx.x == 0) slice_amax = amax;
-  cluster.sync();
-  if (threadIdx.x < 32) {
-    // one lane per CTA of the cluster: remote shared-memory reads take ~0.25 us
-    // each on GB300, so they are issued together rather than one after another
-    float mx = threadIdx.x < unsigned(csize) ? *cluster.map_shared_rank(&slice_amax, int(threadIdx.x)) : 0.f;
-    mx = warp_max(mx);
-    if (threadIdx.x == 0) red[0] = mx;
-  }
-  cluster.sync();   // no CTA leaves while others may still read its slice_amax
-  const float tok = red[0];
-  const float sc = tok > 0.f ? tok / 448.f : 1.f;
-  uint2* out = reinterpret_cast<uint2*>(static_cast<uint8_t*>(a.out) + int64_t(t) * a.H * a.D) + c0;
-  for (int c = threadIdx.x; c < nchunks; c += kMergeThreads) {
+  __syncthreads();
+  const float sc = tok_s;
+  uint2* out = reinterpret_cast<uint2*>(static_cast<uint8_t*>(a.out) + int64_t(t) * a.H * a.D);
+  auto put = [&](int c, uint4 v) {
     float x[8];
-    rotated_chunk(rows_s[c], ((c0 + c) % per_head) * 8, first, a.R, cs, x);
+    rotated_chunk(v, (c % per_head) * 8, first, a.R, cs, x);
     uint32_t lo = 0, hi = 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) lo |= uint32_t(f32_to_e4m3(x[i] / sc)) << (8 * i);
 #pragma unroll
     for (int i = 0; i < 4; ++i) hi |= uint32_t(f32_to_e4m3(x[4 + i] / sc)) << (8 * i);
     out[c] = make_uint2(lo, hi);
+  };
+#pragma unroll
+  for (int i = 0; i < kEncPer; ++i) {
+    const int c = cb + threadIdx.x + i * int(blockDim.x);
+    if (c < ce) put(c, w[i]);
   }
-  if (rank == 0 && threadIdx.x == 0) a.out_scale[t] = sc;
-}
-
-// Largest cluster (16, else 8) the merge kernel can run with on this device.
-int merge_cluster_size() {
-  static int cached = 0;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    cudaFuncSetAttribute(merge_out_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    for (int cs : {16, 8}) {
-      cudaLaunchConfig_t lc = {};
-      lc.gridDim = dim3(cs);
-      lc.blockDim = dim3(kMergeThreads);
-      cudaLaunchAttribute at[1];
-      at[0].id = cudaLaunchAttributeClusterDimension;
-      at[0].val.clusterDim.x = cs;
-      at[0].val.clusterDim.y = 1;
-      at[0].val.clusterDim.z = 1;
-      lc.attrs = at;
-      lc.numAttrs = 1;
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, merge_out_kernel, &lc) == cudaSuccess && n > 0) {
-        cached = cs;
-        break;
-      }
-      cudaGetLastError();
-    }
-  });
-  return cached;
+  for (int c = cb + threadIdx.x + kEncPer * int(blockDim.x); c < ce; c += blockDim.x) put(c, __ldcg(rows + c));
+  if (r == 0 && threadIdx.x == 0) a.out_scale[t] = sc;
 }
 
 }  // namespace
@@ -365,13 +375,11 @@ int sparse_attn_out(const v4a_attn_args* at, const v4a_output_args* a, void* ws,
   if (rc) return rc;
   if (a->num_tokens != at->batch.num_tokens || a->num_heads != at->num_heads || a->dim != at->kv.dim)
     return V4A_ERR_INVALID_ARG;
-  const int csize = merge_cluster_size();
-  if (csize == 0 || a->num_heads % csize || a->num_heads / csize > kMergeMaxRows) return V4A_ERR_UNSUPPORTED;
-  if (int64_t(a->num_heads / csize) * a->dim * 2 > kMaxSlice) return V4A_ERR_UNSUPPORTED;
+  if (a->dim > 512) return V4A_ERR_UNSUPPORTED;   // one thread per 8 dims of a row, 64 per group
   rc = validate_attn(at);
   if (rc) return rc;
   if (a->num_tokens == 0) return V4A_OK;
-  // one attention launch and one merge launch per group of queries (long
+  // one attention, merge and encode launch per group of queries (long
   // chunked-prefill batches take several, sharing the workspace)
   const int Tb = attn_tc_batch_queries(at);
   if (Tb == 0) return V4A_ERR_UNSUPPORTED;
@@ -383,26 +391,21 @@ int sparse_attn_out(const v4a_attn_args* at, const v4a_output_args* a, void* ws,
     if (!attn_tc(at, ws, ws_bytes, stream, &rc, &p, t0, tn)) return V4A_ERR_UNSUPPORTED;
     if (rc) return rc;
     if (p.splits > kMergeMaxSplits) return V4A_ERR_UNSUPPORTED;
-    MergeDev d;
-    d.rope = rope;
-    d.T = tn; d.H = a->num_heads; d.D = a->dim; d.R = a->rope_dims; d.fmt = a->out_format;
-    d.splits = p.splits; d.positions = a->positions + t0; d.part_o = p.o; d.part_ml = p.ml;
-    d.out = static_cast<uint8_t*>(a->out) + size_t(t0) * a->num_heads * a->dim * out_elem;
-    d.out_scale = a->out_scale ? a->out_scale + t0 : nullptr;
-    cudaLaunchConfig_t lc = {};
-    lc.gridDim = dim3(unsigned(tn * csize));
-    lc.blockDim = dim3(kMergeThreads);
-    lc.stream = stream;
-    cudaLaunchAttribute la[2];
-    la[0].id = cudaLaunchAttributeClusterDimension;
-    la[0].val.clusterDim.x = unsigned(csize);
-    la[0].val.clusterDim.y = 1;
-    la[0].val.clusterDim.z = 1;
-    la[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    la[1].val.programmaticStreamSerializationAllowed = 1;
-    lc.attrs = la;
-    lc.numAttrs = 2;
-    if (cudaLaunchKernelEx(&lc, merge_out_kernel, d) != cudaSuccess) return V4A_ERR_CUDA;
+    MergeDev m;
+    m.rope = rope;
+    m.H = a->num_heads; m.D = a->dim; m.R = a->rope_dims; m.fmt = a->out_format; m.splits = p.splits;
+    m.positions = a->positions + t0; m.part_o = p.o; m.part_ml = p.ml;
+    auto merge = p.splits <= 16 ? merge_amax_kernel<4> : p.splits <= 36 ? merge_amax_kernel<9> : merge_amax_kernel<16>;
+    if (launch_pdl(merge, dim3(unsigned(a->num_heads), unsigned(tn)), dim3(256), 0, stream, m) != cudaSuccess)
+      return V4A_ERR_CUDA;
+    EncDev e;
+    e.rope = rope;
+    e.H = a->num_heads; e.D = a->dim; e.R = a->rope_dims; e.fmt = a->out_format; e.splits = p.splits;
+    e.positions = a->positions + t0; e.part_o = p.o; e.part_ml = p.ml;
+    e.out = static_cast<uint8_t*>(a->out) + size_t(t0) * a->num_heads * a->dim * out_elem;
+    e.out_scale = a->out_scale ? a->out_scale + t0 : nullptr;
+    if (launch_pdl(encode_rows_kernel, dim3(unsigned(tn * kEncSlices)), dim3(256), 0, stream, e) != cudaSuccess)
+      return V4A_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? V4A_OK : V4A_ERR_CUDA;
 }

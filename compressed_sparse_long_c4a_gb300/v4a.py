@@ -336,7 +336,7 @@ class Step:
         per = max(1, min(s.tokens, (64 * 152) // chunks))
         batches = -(-s.tokens // per)
         if self.fused_out:
-            return n + 2 * batches            # attention + merge/output kernel per batch
+            return n + 3 * batches            # attention, merge and encode kernels per batch
         n += batches * (1 + (1 if chunks > 1 else 0))
         return n + 1
 

@@ -297,8 +297,10 @@ V4A_API int v4a_inv_rope_quant(const v4a_output_args* args, void* stream);
  * attention output never goes to memory.  Same passages as the two calls,
  * with the pages' fusion (2) ("DeepSeek V4 in vLLM: Efficient Long-context
  * Attention", Method details) extended to the merge of the attention's key
- * chunks: the chunk results are merged, inverse-rotated and encoded by one
- * kernel.  The bytes of `out` and `out_scale` equal those of the two calls.
+ * chunks: the chunk results are merged (with each row's amax after the
+ * inverse rotation) by one kernel and inverse-rotated and encoded by the
+ * next, the merged rows staying in the workspace.  The bytes of `out` and
+ * `out_scale` equal those of the two calls.
  *
  *   attn: as for v4a_sparse_attn; attn->out and attn->lse are not written and
  *         may be NULL.
@@ -308,8 +310,7 @@ V4A_API int v4a_inv_rope_quant(const v4a_output_args* args, void* stream);
  *   workspace: at least v4a_attn_workspace_size(attn) bytes (caller-owned).
  * Errors: as for the two calls; V4A_ERR_UNSUPPORTED (nothing launched) when
  * the shapes are outside the fused path (the tensor-core attention must take
- * them, and the heads must split evenly over one thread-block cluster per
- * token), in which case the two calls serve.
+ * them), in which case the two calls serve.
  */
 V4A_API int v4a_sparse_attn_out(const v4a_attn_args* attn, const v4a_output_args* out, void* workspace,
                                 size_t workspace_bytes, void* stream);
