@@ -337,24 +337,19 @@ __global__ void __launch_bounds__(512) topk_hist(const float* scores, int64_t ro
 // grid) every CTA reads the level whole.  Then every CTA learns, from the
 // counts of the CTAs before it (one lane each), its share of the ties at K*
 // (lowest indices first) and its output offset, and writes its selected
-// indices in ascending order.  Three cluster barriers in all: measured on
+// indices in ascending order.  The level-1 counts are loaded together with the
+// scores, and the above / equal counts share one block scan.  Three cluster barriers in all: measured on
 // GB300, a cluster barrier costs ~1 us and a distributed-shared-memory read
 // ~0.25 us, so the levels are combined in L2 rather than through remote
 // shared memory.
 
-// Threshold bin of a 4096-bin histogram given as a function bin -> count: the
-// bin b with fewer than `need` counts strictly above it and at least `need`
-// at or above it; *above receives the count strictly above.  All 1024
-// threads call it (4 bins each, scanned from the top).
-template <class Get>
-__device__ int threshold_bin_of(Get count, uint32_t need, uint32_t* scan, int* bin_s, uint32_t* above_s,
-                                uint32_t* above) {
-  uint32_t loc[4], s4 = 0;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    loc[q] = count(kHistBins - 1 - (int(threadIdx.x) * 4 + q));
-    s4 += loc[q];
-  }
+// Threshold bin of a 4096-bin histogram whose counts this thread holds for
+// bins kHistBins-1-(4*tid+q), q < 4: the bin b with fewer than `need` counts
+// strictly above it and at least `need` at or above it; *above receives the
+// count strictly above.  All 1024 threads call it.
+__device__ int threshold_bin4(const uint32_t (&loc)[4], uint32_t need, uint32_t* scan, int* bin_s,
+                              uint32_t* above_s, uint32_t* above) {
+  const uint32_t s4 = (loc[0] + loc[1]) + (loc[2] + loc[3]);
   uint32_t total;
   const uint32_t excl = block_excl_scan(s4, scan, &total);
   if (excl < need && need <= excl + s4) {
@@ -374,12 +369,43 @@ __device__ int threshold_bin_of(Get count, uint32_t need, uint32_t* scan, int* b
   return b;
 }
 
+// Exclusive block-wide prefix sum of two 32-bit counts packed in one 64-bit
+// word (no carry crosses between them while both sums stay below 2^32).
+__device__ __forceinline__ uint64_t block_excl_scan64(uint64_t v, uint64_t* scratch, uint64_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  uint64_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint64_t x = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const uint64_t s = lane < nw ? scratch[lane] : 0;
+    uint64_t si = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint64_t x = __shfl_up_sync(0xffffffffu, si, o);
+      if (lane >= o) si += x;
+    }
+    if (lane < nw) scratch[lane] = si - s;
+    if (lane == nw - 1) scratch[32] = si;
+  }
+  __syncthreads();
+  const uint64_t r = scratch[warp] + incl - v;
+  *total = scratch[32];
+  __syncthreads();
+  return r;
+}
+
 template <int PER>
 __global__ void __launch_bounds__(1024, 1) topk_cluster(const float* scores, int64_t row, int max_entries,
                                                     const int32_t* positions, int k, const uint32_t* hist1,
                                                     uint32_t* hist2, uint32_t* hist3, uint2* gteq, int32_t* out) {
   pdl_trigger();
   __shared__ uint32_t scan[40];
+  __shared__ uint64_t scan64[40];
   __shared__ uint32_t h_s[kHistBins];  // this CTA's counts of the level being built
   __shared__ uint32_t pre_s[2];        // ties in and entries selected by the CTAs before this one
   __shared__ int bin_s;
@@ -395,7 +421,12 @@ __global__ void __launch_bounds__(1024, 1) topk_cluster(const float* scores, int
     if (r == 0) write_all_visible(o, n, k);
     return;
   }
-  // this thread's PER consecutive entries
+  // the level-1 counts of this thread's four bins and its PER consecutive
+  // entries, in flight together
+  const uint32_t* g1 = hist1 + int64_t(t) * kHistBins;
+  uint32_t loc[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) loc[q] = __ldcg(&g1[kHistBins - 1 - (int(threadIdx.x) * 4 + q)]);
   const int i0 = (r * int(blockDim.x) + int(threadIdx.x)) * PER;
   const float* sc = scores + int64_t(t) * row;
   uint32_t key[PER];
@@ -411,9 +442,7 @@ __global__ void __launch_bounds__(1024, 1) topk_cluster(const float* scores, int
   }
   // level 1: the top 12 bits (histogram from the scan)
   uint32_t above1;
-  const uint32_t* g1 = hist1 + int64_t(t) * kHistBins;
-  const uint32_t b1 = uint32_t(threshold_bin_of([&](int b) { return __ldcg(&g1[b]); }, uint32_t(k), scan, &bin_s,
-                                                &above_s, &above1));
+  const uint32_t b1 = uint32_t(threshold_bin4(loc, uint32_t(k), scan, &bin_s, &above_s, &above1));
   const uint32_t need1 = uint32_t(k) - above1;
   // level 2: the next 12 bits of the entries in bin b1; each CTA's nonzero
   // counts go to the query's global histogram, complete after the cluster
@@ -432,8 +461,9 @@ __global__ void __launch_bounds__(1024, 1) topk_cluster(const float* scores, int
   }
   cluster.sync();
   uint32_t above2;
-  const uint32_t b2 = uint32_t(threshold_bin_of([&](int b) { return __ldcg(&g2[b]); }, need1, scan, &bin_s,
-                                                &above_s, &above2));
+#pragma unroll
+  for (int q = 0; q < 4; ++q) loc[q] = __ldcg(&g2[kHistBins - 1 - (int(threadIdx.x) * 4 + q)]);
+  const uint32_t b2 = uint32_t(threshold_bin4(loc, need1, scan, &bin_s, &above_s, &above2));
   const uint32_t need2 = need1 - above2;
   // level 3: the last 8 bits of the entries in sub-bin (b1, b2)
   const uint32_t top24 = (b1 << 12) | b2;
@@ -478,12 +508,11 @@ __global__ void __launch_bounds__(1024, 1) topk_cluster(const float* scores, int
     gt += in && key[u] > K;
     eq += in && key[u] == K;
   }
-  uint32_t tot;
-  const uint32_t eq_before = block_excl_scan(eq, scan, &tot);   // ties of this CTA before this thread
-  const uint32_t eq_cta = tot;
-  block_excl_scan(gt, scan, &tot);
+  uint64_t tot64;
+  const uint64_t pre64 = block_excl_scan64((uint64_t(gt) << 32) | eq, scan64, &tot64);
+  const uint32_t eq_before = uint32_t(pre64);         // ties of this CTA before this thread
   uint2* ge = gteq + int64_t(t) * 16;
-  if (threadIdx.x == 0) ge[r] = make_uint2(tot, eq_cta);
+  if (threadIdx.x == 0) ge[r] = make_uint2(uint32_t(tot64 >> 32), uint32_t(tot64));
   cluster.sync();
   if (threadIdx.x < 32) {
     // the CTAs before this one, one lane each: ties are taken in index order,
@@ -517,6 +546,7 @@ __global__ void __launch_bounds__(1024, 1) topk_cluster(const float* scores, int
       else if (in && key[u] == K) { if (rk < need) ++mine; ++rk; }
     }
   }
+  uint32_t tot;
   uint32_t pos = pre_s[1] + block_excl_scan(mine, scan, &tot);
   {
     uint32_t rk = pre_eq + eq_before;
