@@ -7,11 +7,19 @@ path: compress+insert (main, indexer, window) -> indexer scores -> top-k ->
 sparse attention (+ combine) -> inverse RoPE + fp8 quant.
 
 Prints one JSON line.  `value` = decode tokens/s with inputs resident in HBM,
-timed with CUDA events over K CUDA-graph replays that rotate over enough layer
+timed with CUDA events over windows of K CUDA-graph replays (the median of
+--windows windows; every window is in `windows`) that rotate over enough layer
 replicas (distinct caches) that the bytes a step touches never come from L2;
 `e2e` = the same metric with the step's inputs copied from pinned host memory
 and its output copied back inside the timed region.  `roofline` reports the
 dominant kernel (the indexer scan) against the measured HBM copy bandwidth.
+
+`variants` holds the same measurement for the indexer format with
+power-of-two block scales (the block-scaled tensor-core scan) and, for the
+default workload, for the same layer at 128k context.
+
+--gpus N outside a launcher starts N ranks through torch.distributed.run (one
+replica of the step per GPU: the path shards by sequence, no collective).
 
 --impl reference times the fp64 CPU oracle on the same workload (a bounded
 sample per step, stated in the line) on the host cores.
@@ -226,47 +234,31 @@ def run_reference(args, spec, case):
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="c4a_decode_b4_1m")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--replicas", type=int, default=0,
-                    help="layer replicas to rotate over (default: enough to defeat L2); a smaller "
-                         "count only serves profiler captures, never a reported number")
-    args = ap.parse_args()
-    assert args.warmup >= 3, "at least 3 warm-up steps"
+def _relaunch_if_needed(args) -> None:
+    """--gpus N (N > 1) outside a launcher starts N ranks itself through
+    torch.distributed.run and exits with their status; a world size that does
+    not match N is an error."""
+    ws_env = os.environ.get("WORLD_SIZE")
+    if ws_env is None and args.gpus > 1:
+        import socket
+        with socket.socket() as sk:
+            sk.bind(("127.0.0.1", 0))
+            port = sk.getsockname()[1]
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+               "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *sys.argv[1:]]
+        sys.exit(subprocess.call(cmd))
+    if ws_env is not None and int(ws_env) != args.gpus:
+        sys.exit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={ws_env}")
 
+
+def measure_workload(spec, args, dev, barrier, windows: int):
+    """Graph-replayed steps of `spec` on this rank: `windows` timed windows of
+    args.steps steps each (CUDA events on the launching stream), per-stage
+    times, and the objects the end-to-end leg reuses."""
     import torch
     from compressed_sparse_long_c4a_gb300 import inputs as I
-
-    ws, rank, local = _dist()
-    spec = I.WORKLOADS[args.workload]()
-    case = I.make_case(spec, seed=0)
-
-    if args.impl == "reference":
-        line = run_reference(args, spec, case)
-        if line is not None:
-            print(json.dumps(line), flush=True)
-        return
-
     from compressed_sparse_long_c4a_gb300 import v4a
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-
-    def barrier():
-        if ws > 1:
-            import torch.distributed as dist
-            dist.barrier()
-
-    scan_b, gather_b, win_b = algorithmic_bytes(spec)
-    step_bytes = scan_b + gather_b + win_b
+    case = I.make_case(spec, seed=0)
     replicas = args.replicas if args.replicas > 0 else default_replicas(spec)
     layers = [v4a.DeviceLayer.from_case(case, dev) for _ in range(replicas)]
     steps = [v4a.Step(L) for L in layers]
@@ -292,11 +284,8 @@ def main():
             graphs[i % replicas].replay()
     torch.cuda.synchronize()
 
-    # ---- timed region: K graph replays ----
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
     def busy(seconds):
-        # keeps the GPU under the same load around the (short) timed region so the
+        # keeps the GPU under the same load around the timed windows so the
         # clock samples describe the conditions the timed steps ran in
         t_end = time.perf_counter() + seconds
         with torch.cuda.stream(stream):
@@ -305,28 +294,29 @@ def main():
                     graphs[i].replay()
                 torch.cuda.synchronize()
 
-    with ClockSampler(local) as clk:
+    # ---- timed region: `windows` windows of K graph replays each ----
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(windows)]
+    with ClockSampler(dev.index or 0) as clk:
         busy(0.6)
         barrier()
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
-            e0.record(stream)
-            for i in range(args.steps):
-                graphs[i % replicas].replay()
-            e1.record(stream)
+            for w in range(windows):
+                ev[w][0].record(stream)
+                for i in range(args.steps):
+                    graphs[i % replicas].replay()
+                ev[w][1].record(stream)
         torch.cuda.synchronize()
         barrier()
         busy(0.4)
-    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
-    tokens_per_step = spec.tokens
-    value = whole_job_rate(ws, tokens_per_step, ms)
+    win_ms = [max_over_ranks(a.elapsed_time(b) / args.steps, dev) for a, b in ev]
 
     # ---- per-stage CUDA-event timing (same replicas, direct calls) ----
     fused = steps[0].fused_out
     names = ["compress_insert", "index_scores", "index_select",
              *(["sparse_attn_out"] if fused else ["sparse_attn", "inv_rope_quant"])]
     acc = {n: 0.0 for n in names}
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+    sev = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
     torch.cuda.synchronize()
     for i in range(args.steps):
         st = steps[i % replicas]
@@ -335,27 +325,94 @@ def main():
             # a spin kernel holds the stream while the host queues every stage, so the
             # events below bracket GPU execution only (no host launch gaps)
             torch.cuda._sleep(2_000_000)
-            ev[0].record(stream)
+            sev[0].record(stream)
             v4a.compress_insert(L, stream)
-            ev[1].record(stream)
+            sev[1].record(stream)
             if spec.ix_heads:
                 v4a.index_scores(L, st.idx, st.ws_index, stream)
-            ev[2].record(stream)
+            sev[2].record(stream)
             if spec.ix_heads:
                 v4a.index_select(L, st.idx, st.ws_index, stream)
-            ev[3].record(stream)
+            sev[3].record(stream)
             if fused:
                 v4a.sparse_attn_out(L, st.idx, st.out, st.out_scale, st.ws_attn, stream)
-                ev[4].record(stream)
+                sev[4].record(stream)
             else:
                 v4a.sparse_attn(L, st.idx, st.o, st.lse, st.ws_attn, stream)
-                ev[4].record(stream)
+                sev[4].record(stream)
                 v4a.inv_rope_quant(L, st.o, st.out, st.out_scale, stream)
-                ev[5].record(stream)
+                sev[5].record(stream)
         torch.cuda.synchronize()
         for k, n in enumerate(names):
-            acc[n] += ev[k].elapsed_time(ev[k + 1])
+            acc[n] += sev[k].elapsed_time(sev[k + 1])
     stage_us = {n: acc[n] / args.steps * 1e3 for n in names}
+    return {"case": case, "layers": layers, "steps": steps, "graphs": graphs, "stream": stream,
+            "replicas": replicas, "win_ms": win_ms, "stage_us": stage_us, "clocks": clk.summary()}
+
+
+def window_stats(win_ms):
+    s = sorted(win_ms)
+    med = statistics.median(s)
+    return {"count": len(s), "ms_per_step": [round(x, 5) for x in win_ms], "median": med, "min": s[0],
+            "max": s[-1], "spread_pct": (s[-1] - s[0]) / med * 100.0}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="c4a_decode_b4_1m")
+    ap.add_argument("--windows", type=int, default=10,
+                    help="timed windows of --steps steps each; value is the median window")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the extra measurement of the power-of-two-scale indexer variant")
+    ap.add_argument("--replicas", type=int, default=0,
+                    help="layer replicas to rotate over (default: enough to defeat L2); a smaller "
+                         "count only serves profiler captures, never a reported number")
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    _relaunch_if_needed(args)
+
+    import torch
+    from compressed_sparse_long_c4a_gb300 import inputs as I
+
+    ws, rank, local = _dist()
+    spec = I.WORKLOADS[args.workload]()
+
+    if args.impl == "reference":
+        line = run_reference(args, spec, I.make_case(spec, seed=0))
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    if torch.cuda.device_count() < max(1, ws):
+        sys.exit(f"bench.py: {ws} rank(s) but {torch.cuda.device_count()} visible GPU(s)")
+    from compressed_sparse_long_c4a_gb300 import v4a
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    scan_b, gather_b, win_b = algorithmic_bytes(spec)
+    step_bytes = scan_b + gather_b + win_b
+    m = measure_workload(spec, args, dev, barrier, max(1, args.windows))
+    wst = window_stats(m["win_ms"])
+    ms = wst["median"]
+    stage_us = m["stage_us"]
+    layers, steps, graphs, stream, replicas, case = (m["layers"], m["steps"], m["graphs"], m["stream"],
+                                                     m["replicas"], m["case"])
+    tokens_per_step = spec.tokens
+    value = whole_job_rate(ws, tokens_per_step, ms)
+
     hbm_peak, bf16_peak, peak_kind = _peaks()
     scan_us = stage_us["index_scores"]
     dominant = max(stage_us, key=stage_us.get)
@@ -397,15 +454,15 @@ def main():
     e2e_ms = max_over_ranks(f0.elapsed_time(f1) / args.steps, dev)
 
     # ---- our kernel launches in the timed region (per step, from the path taken) ----
-    launches = steps[0].launches_per_step() * args.steps
+    launches = steps[0].launches_per_step() * args.steps * len(m["win_ms"])
 
-    clocks = clk.summary()
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "us_per_layer": ms * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp8/fp4 caches, fp32 accumulate",
         "data": "synthetic (seeded)",
         "config": workload_config(spec, replicas, ws),
+        "windows": wst,
         "roofline": roof,
         "step_hbm_frac": step_bytes / (ms * 1e-3) / 1e9 / hbm_peak,
         "stage_us": stage_us, "dominant_stage": dominant,
@@ -413,8 +470,33 @@ def main():
         "e2e": {"value": whole_job_rate(ws, tokens_per_step, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches,
-        "clocks": clocks,
+        "gpu_launches_note": f"{steps[0].launches_per_step()} per step x {args.steps} steps x "
+                             f"{len(m['win_ms'])} windows",
+        "clocks": m["clocks"],
     }
+    del m, layers, steps, graphs
+    # the same layer with the indexer's per-32 scales restricted to powers of
+    # two (the block-scaled tensor-core scan): a second configuration of the
+    # same workload, reported beside the headline, not instead of it
+    # and the same layer at 128k context (the low end of the decode target's range)
+    variants = [f"{spec.name}_mx"] + (["c4a_decode_b4_128k"] if spec.name == "c4a_decode_b4_1m" else [])
+    for variant in variants:
+        if args.no_variants or variant not in I.WORKLOADS:
+            continue
+        vspec = I.WORKLOADS[variant]()
+        vscan_b, vgather_b, vwin_b = algorithmic_bytes(vspec)
+        vm = measure_workload(vspec, args, dev, barrier, max(1, args.windows))
+        vst = window_stats(vm["win_ms"])
+        vscan = vm["stage_us"]["index_scores"]
+        line.setdefault("variants", {})[variant] = {
+            "config": workload_config(vspec, vm["replicas"], ws),
+            "ms_per_step": vst["median"], "us_per_layer": vst["median"] * 1e3,
+            "value": whole_job_rate(ws, vspec.tokens, vst["median"]), "windows": vst,
+            "stage_us": vm["stage_us"],
+            "scan_frac": (vscan_b / (vscan * 1e-6) / 1e9 / hbm_peak) if vscan > 0 else None,
+            "step_hbm_frac": (vscan_b + vgather_b + vwin_b) / (vst["median"] * 1e-3) / 1e9 / hbm_peak,
+            "clocks": vm["clocks"]}
+        del vm
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         t0 = time.perf_counter()
         oracle_token(case, 0, 1.0)

@@ -201,7 +201,10 @@ static int validate_shape(const v4a_attn_args* a) {
   if (c.num_blocks <= 0 || c.max_blocks <= 0) return V4A_ERR_INVALID_ARG;
   if (c.format != V4A_KV_BF16 && c.format != V4A_KV_FP8_TOKEN) return V4A_ERR_INVALID_ARG;
   if (a->window_format != V4A_KV_BF16 && a->window_format != V4A_KV_FP8_TOKEN) return V4A_ERR_INVALID_ARG;
-  if (a->window_len < 1 || a->window_cap < a->window_len) return V4A_ERR_INVALID_ARG;
+  if (a->window_len < 1 || a->window_cap < 1) return V4A_ERR_INVALID_ARG;
+  // every query's window [m - window_len + 1, m] must be in the ring at once
+  // (the batch's newest positions were written by the compress call before)
+  if (int64_t(a->window_cap) < int64_t(a->window_len) - 1 + B.max_new_per_seq) return V4A_ERR_RING_TOO_SMALL;
   if (a->idx && (a->k < 1 || a->k > 65536)) return V4A_ERR_INVALID_ARG;
   const int D = c.dim;
   if (D != 64 && D != 128 && D != 256 && D != 512) return V4A_ERR_UNSUPPORTED;

@@ -365,7 +365,10 @@ int compress_insert(const v4a_compress_args* a, cudaStream_t stream) {
     if (w.rope_dims < 0 || w.rope_dims > w.dim || w.rope_dims % 2) return V4A_ERR_INVALID_ARG;
     if (w.format != V4A_KV_BF16 && w.format != V4A_KV_FP8_TOKEN) return V4A_ERR_INVALID_ARG;
     if (w.format == V4A_KV_FP8_TOKEN && !w.ring_scale) return V4A_ERR_INVALID_ARG;
-    if (w.ring_cap < 127 + B.max_new_per_seq) return V4A_ERR_RING_TOO_SMALL;
+    if (w.window_len < 1) return V4A_ERR_INVALID_ARG;
+    // a query's window [P - window_len + 1, P] must still be in the ring after
+    // the call has written its max_new_per_seq positions
+    if (int64_t(w.ring_cap) < int64_t(w.window_len) - 1 + B.max_new_per_seq) return V4A_ERR_RING_TOO_SMALL;
     if (w.rope_dims > 128) return V4A_ERR_UNSUPPORTED;
     ws.rope = make_rope_freq(w.rope_dims, w.rope_theta);
     ws.active = 1; ws.dim = w.dim; ws.rope_dims = w.rope_dims; ws.format = w.format;

@@ -9,8 +9,10 @@
 // the scratch below is the workspace.
 //
 // Nothing here allocates: the array is part of this library's device image.
-// Its address is looked up once per device (with that device current) by
-// cudaGetSymbolAddress on the first call made there; later calls reuse it.
+// Its address is looked up on every call, on the current device, with
+// cudaGetSymbolAddress (a cached address would go stale when a caller resets
+// the device and the module is loaded again; the lookup costs ~1 us of host
+// time and no device work).
 //
 // Every call on a device shares the one array.  Calls whose lifetimes overlap
 // on the device (two streams, or two host threads, without an ordering between
@@ -19,33 +21,19 @@
 // start at zero; each call clears it on its own stream before the scan
 // (a clearing kernel), so nothing depends on the array's initial contents.
 
-#include <mutex>
-
 #include "v4a_internal.h"
 
 namespace v4a {
 namespace {
 
 constexpr size_t kScratchBytes = size_t(V4A_INDEX_STATIC_SCRATCH_BYTES);
-constexpr int kMaxDevices = 64;
-
 __device__ __align__(256) unsigned char g_index_scratch[kScratchBytes];
 
-std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of g_index_scratch on the current device (looked up once).
+// Device address of g_index_scratch on the current device.
 int scratch_of_current_device(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return V4A_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return V4A_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_index_scratch) != cudaSuccess || !p) return V4A_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_index_scratch) != cudaSuccess || !p) return V4A_ERR_CUDA;
+  *out = p;
   return V4A_OK;
 }
 

@@ -330,6 +330,13 @@ def c4a_decode_1m_mx() -> LayerSpec:
     return dataclasses.replace(c4a_decode_1m(), name="c4a_decode_b4_1m_mx", ix_fmt=IX_FP4_MX32)
 
 
+def c4a_decode_128k() -> LayerSpec:
+    """c4a_decode_b4_1m at 128k context: m = 131,071 emits entry 32,767 (the
+    last slot of a block), so each query sees 32,768 entries (the low end of
+    the 128k-1M range the decode target names)."""
+    return dataclasses.replace(c4a_decode_1m(), name="c4a_decode_b4_128k", cached=(131_071,) * 4)
+
+
 WORKLOADS = {
     "c4a_decode_b1_1k": c4a_decode_1k,
     "c4a_decode_b32_32k_64k": c4a_decode_b32_32k_64k,
@@ -337,6 +344,7 @@ WORKLOADS = {
     "c4a_prefill_4x32k_plus_4k": c4a_prefill_4x4k,
     "c4a_decode_b4_1m": c4a_decode_1m,
     "c4a_decode_b4_1m_mx": c4a_decode_1m_mx,
+    "c4a_decode_b4_128k": c4a_decode_128k,
 }
 
 

@@ -45,7 +45,8 @@ class Compressor(C.Structure):
 
 class Window(C.Structure):
     _fields_ = [("k", _p), ("dim", C.c_int32), ("rope_dims", C.c_int32), ("rope_theta", C.c_float),
-                ("format", C.c_int32), ("ring", _p), ("ring_scale", _p), ("ring_cap", C.c_int32)]
+                ("format", C.c_int32), ("ring", _p), ("ring_scale", _p), ("ring_cap", C.c_int32),
+                ("window_len", C.c_int32)]
 
 
 class CompressArgs(C.Structure):
@@ -174,7 +175,7 @@ class DeviceLayer:
                             s.ix_ring_cap)
             keep.append(ix)
         win = Window(_ptr(t["k_swa"]), s.dim, s.rope_dims, s.theta, s.swa_fmt, _ptr(t["swa_ring"]),
-                     _ptr(t.get("swa_scale")), s.swa_cap)
+                     _ptr(t.get("swa_scale")), s.swa_cap, s.swa)
         keep.append(win)
         a = CompressArgs(self.batch(), C.pointer(main), C.pointer(ix) if ix else None,
                          C.pointer(win), _ptr(self.status))

@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define V4A_ABI_VERSION 1
+#define V4A_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define V4A_API __attribute__((visibility("default")))
@@ -151,7 +151,8 @@ typedef struct {
   int32_t format;              /* V4A_KV_BF16 or V4A_KV_FP8_TOKEN */
   void* ring;                  /* [num_seqs][ring_cap][dim] bf16 or e4m3 */
   float* ring_scale;           /* [num_seqs][ring_cap] (fp8 only) */
-  int32_t ring_cap;            /* >= 127 + max_new_per_seq */
+  int32_t ring_cap;            /* >= window_len - 1 + max_new_per_seq, else V4A_ERR_RING_TOO_SMALL */
+  int32_t window_len;          /* the sliding window the ring serves (128); >= 1 */
 } v4a_window;
 
 typedef struct {
@@ -228,8 +229,9 @@ V4A_API int v4a_index_select(const v4a_index_args* args, void* workspace, size_t
  * otherwise it returns exactly what v4a_index_topk would with a workspace of
  * that size, and writes the same out_idx.
  *
- * The first call on each device looks up the array's address there with that
- * device current (cudaGetSymbolAddress; V4A_ERR_CUDA if that fails), which may
+ * Every call looks up the array's address on the current device
+ * (cudaGetSymbolAddress; V4A_ERR_CUDA if that fails; nothing is cached, so a
+ * device reset between calls is harmless).  The first call on a device may
  * load this library's device code: make it before any stream capture starts.
  * All calls on a device share the array, so calls that may be in flight at the
  * same time (other streams or host threads, unordered) race and must be
@@ -254,7 +256,7 @@ typedef struct {
   int32_t k;
   const void* window;          /* [num_seqs][window_cap][kv.dim] */
   const float* window_scale;   /* [num_seqs][window_cap] (fp8 window only) */
-  int32_t window_cap;
+  int32_t window_cap;          /* >= window_len - 1 + max_new_per_seq, else V4A_ERR_RING_TOO_SMALL */
   int32_t window_format;       /* V4A_KV_* */
   int32_t window_len;          /* 128 */
   int32_t num_heads;           /* H */

@@ -1,6 +1,9 @@
 """Comparison helpers for the GPU parity tests (GPU output vs fp64 oracle)."""
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 
 from oracle import formats as F
@@ -9,6 +12,18 @@ from oracle import geometry as G
 BF16_TOL = (2e-2, 2e-3)     # attention output, bf16 caches: max-abs, mean-abs
 FP8_TOL = (6e-2, 6e-3)      # attention output, fp8 / fp4 caches
 TOPK_REL = 1e-5             # near-tie band around the k-th score
+
+# With V4A_PARITY_RECORD set to a file path, every comparison below appends
+# what it observed (errors, swap counts) as one JSON line there; the committed
+# parity record under profiles/ is a summary of such a file from a GPU run.
+_RECORD = os.environ.get("V4A_PARITY_RECORD")
+
+
+def record(kind: str, where: str, **stats):
+    if not _RECORD:
+        return
+    with open(_RECORD, "a") as f:
+        f.write(json.dumps({"kind": kind, "where": str(where), **stats}) + "\n")
 
 
 def check_topk(gpu_idx: np.ndarray, ref_idx: np.ndarray, scores: np.ndarray, k: int, where=""):
@@ -26,15 +41,19 @@ def check_topk(gpu_idx: np.ndarray, ref_idx: np.ndarray, scores: np.ndarray, k: 
         return 0
     kth = np.sort(scores)[::-1][k - 1]
     diff = set(valid) ^ set(int(v) for v in ref_idx if v >= 0)
+    worst = 0.0
     for e in diff:
-        assert abs(scores[e] - kth) <= TOPK_REL * max(abs(kth), 1e-30), \
-            (where, e, scores[e], kth)
+        rel = abs(scores[e] - kth) / max(abs(kth), 1e-30)
+        worst = max(worst, rel)
+        assert rel <= TOPK_REL, (where, e, scores[e], kth)
+    record("topk", where, swaps=len(diff) // 2, worst_swap_rel_to_kth=worst, k=k, entries=n)
     return len(diff)
 
 
 def check_close(gpu: np.ndarray, ref: np.ndarray, tol, where=""):
     err = np.abs(np.asarray(gpu, np.float64) - ref)
     mx, mean = float(err.max()), float(err.mean())
+    record("close", where, max_abs=mx, mean_abs=mean, tol_max=tol[0], tol_mean=tol[1])
     assert mx <= tol[0] and mean <= tol[1], (where, mx, mean)
     return mx, mean
 

@@ -27,7 +27,7 @@ def test_exports_every_declared_symbol(lib):
     assert len(names) >= 8
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.v4a_abi_version() == 1
+    assert lib.v4a_abi_version() == 2
     for code in range(6):
         assert lib.v4a_status_string(code).decode() != "unknown status"
 
@@ -66,9 +66,20 @@ def test_host_validation_of_compress(lib):
     comp = _compressor(L, spec.ring_cap - 1)           # one slot short: window - 2 + new
     a = v4a.CompressArgs(L.batch(), C.pointer(comp), None, None, None)
     assert lib.v4a_compress_insert(C.byref(a), None) == 3
-    win = v4a.Window(0x70, spec.dim, 64, 1e4, 0, 0x80, None, 127 + spec.new - 1)
+    win = v4a.Window(0x70, spec.dim, 64, 1e4, 0, 0x80, None, 127 + spec.new - 1, 128)
     a = v4a.CompressArgs(L.batch(), None, None, C.pointer(win), None)
-    assert lib.v4a_compress_insert(C.byref(a), None) == 3
+    assert lib.v4a_compress_insert(C.byref(a), None) == 3             # one slot short of window - 1 + new
+    # the bound follows the window length: an empty batch validates and
+    # launches nothing, so these calls reach no device
+    b0 = L.batch()
+    b0.num_tokens = 0
+    a0 = v4a.CompressArgs(b0, None, None, C.pointer(win), None)
+    win.ring_cap, win.window_len = 64 + spec.new - 1, 64
+    assert lib.v4a_compress_insert(C.byref(a0), None) == 0
+    win.ring_cap = 64 + spec.new - 2
+    assert lib.v4a_compress_insert(C.byref(a0), None) == 3
+    win.window_len = 0
+    assert lib.v4a_compress_insert(C.byref(a0), None) == 1
     bad = _compressor(L, spec.ring_cap)
     bad.cache.ratio = 5
     a = v4a.CompressArgs(L.batch(), C.pointer(bad), None, None, None)
@@ -110,6 +121,9 @@ def test_host_validation_of_attention_and_output(lib):
     a.window_scale = None                                                # fp8 window needs scales
     assert lib.v4a_sparse_attn(C.byref(a), 0x1000, need, None) == 1
     a.window_scale = 0x30
+    a.window_cap = spec.swa - 2 + spec.new                               # one slot short of window - 1 + new
+    assert lib.v4a_sparse_attn(C.byref(a), 0x1000, need, None) == 3
+    a.window_cap = spec.swa_cap
     a.kv.dim = 96
     assert lib.v4a_sparse_attn(C.byref(a), 0x1000, need, None) == 2
     o = v4a.OutputArgs(4, 0x10, 128, 512, 64, 1e4, 0x20, 1, 0x30, None)  # fp8 output needs scales
