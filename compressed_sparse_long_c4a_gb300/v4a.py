@@ -162,23 +162,27 @@ class DeviceLayer:
         return Cache(4, s.ix_dim, s.ix_rope_dims, s.theta, s.ix_fmt, _ptr(self.t["ix_pool"]),
                      s.num_blocks, _ptr(self.t["block_table"]), s.max_blocks)
 
-    def compress_args(self):
+    def compress_args(self, parts=("main", "indexer", "window")):
+        """Arguments of v4a_compress_insert for the named parts (the others
+        NULL: the call skips them)."""
         s, t = self.spec, self.t
         keep = []
-        main = Compressor(self.kv_cache(), _ptr(t["x"]), _ptr(t["gate"]), _ptr(t["bias"]),
-                          _ptr(t["gamma"]), 1e-6, _ptr(t["ring_x"]), _ptr(t["ring_gate"]), s.ring_cap)
-        keep.append(main)
-        ix = None
-        if s.ix_heads:
+        main = ix = win = None
+        if "main" in parts:
+            main = Compressor(self.kv_cache(), _ptr(t["x"]), _ptr(t["gate"]), _ptr(t["bias"]),
+                              _ptr(t["gamma"]), 1e-6, _ptr(t["ring_x"]), _ptr(t["ring_gate"]), s.ring_cap)
+            keep.append(main)
+        if s.ix_heads and "indexer" in parts:
             ix = Compressor(self.ix_cache(), _ptr(t["x_i"]), _ptr(t["gate_i"]), _ptr(t["bias_i"]),
                             _ptr(t["gamma_i"]), 1e-6, _ptr(t["ring_x_i"]), _ptr(t["ring_gate_i"]),
                             s.ix_ring_cap)
             keep.append(ix)
-        win = Window(_ptr(t["k_swa"]), s.dim, s.rope_dims, s.theta, s.swa_fmt, _ptr(t["swa_ring"]),
-                     _ptr(t.get("swa_scale")), s.swa_cap, s.swa)
-        keep.append(win)
-        a = CompressArgs(self.batch(), C.pointer(main), C.pointer(ix) if ix else None,
-                         C.pointer(win), _ptr(self.status))
+        if "window" in parts:
+            win = Window(_ptr(t["k_swa"]), s.dim, s.rope_dims, s.theta, s.swa_fmt, _ptr(t["swa_ring"]),
+                         _ptr(t.get("swa_scale")), s.swa_cap, s.swa)
+            keep.append(win)
+        a = CompressArgs(self.batch(), C.pointer(main) if main else None, C.pointer(ix) if ix else None,
+                         C.pointer(win) if win else None, _ptr(self.status))
         return a, keep
 
     def index_args(self, out_idx: torch.Tensor) -> IndexArgs:
@@ -204,8 +208,8 @@ class DeviceLayer:
 # --------------------------------------------------------------------------
 
 
-def compress_insert(layer: DeviceLayer, stream=None):
-    a, keep = layer.compress_args()
+def compress_insert(layer: DeviceLayer, stream=None, parts=("main", "indexer", "window")):
+    a, keep = layer.compress_args(parts)
     _check("v4a_compress_insert", lib().v4a_compress_insert(C.byref(a), _stream(stream)))
 
 
@@ -295,13 +299,26 @@ class Step:
     """Output buffers + workspaces for running whole layer steps on a DeviceLayer.
 
     fused_out: attention and output stage as one call (v4a_sparse_attn_out)
-    where the library takes the shapes; self.o is then not written."""
+    where the library takes the shapes; self.o is then not written.
 
-    def __init__(self, layer: DeviceLayer, fused_out: bool = True):
+    overlap: how the compressor calls are placed (layers with an indexer):
+      "serial"  one compress call (all parts), then the indexer, attention;
+      "start"   the indexer pipeline (indexer compressor -> scan -> top-k) on
+                the calling stream and the main compressor + window insert on
+                a side stream from the start of the step, joined before the
+                attention (the pages' separate indexer stream);
+      "select"  as "start", with the side-stream call placed after the scan,
+                where it runs beside the top-k (which leaves most SMs idle)
+                instead of beside the scan (which holds every SM)."""
+
+    def __init__(self, layer: DeviceLayer, fused_out: bool = True, overlap: str = "serial"):
         s = layer.spec
         dev = layer.status.device
         self.layer = layer
         self.fused_out = fused_out
+        assert overlap in ("serial", "start", "select")
+        self.overlap = overlap if s.ix_heads else "serial"
+        self.side = torch.cuda.Stream(device=dev) if self.overlap != "serial" else None
         T = s.tokens
         self.idx = torch.full((T, s.topk), -1, dtype=torch.int32, device=dev) if s.ix_heads else None
         self.o = torch.empty((T, s.heads, s.dim), dtype=torch.bfloat16, device=dev)
@@ -323,7 +340,7 @@ class Step:
         rows scored on the CUDA cores); attention (1, + combine when the key
         list is split); output (1)."""
         s = self.layer.spec
-        n = 1
+        n = 1 if self.overlap == "serial" else 2   # compress (split in two with overlap)
         if s.ix_heads:
             tc_scan = s.ix_fmt in (IX_FP8_B128, IX_FP4_B32, IX_FP4_MX32) and s.ix_heads == 64 and s.ix_dim == 128
             # clear + scan, then the top-k: one kernel (plus the histogram
@@ -342,11 +359,30 @@ class Step:
         return n + 1
 
     def run(self, stream=None):
-        """compress_insert -> index_topk -> sparse_attn -> inv_rope_quant."""
+        """compress_insert -> index_topk -> sparse_attn -> inv_rope_quant
+        (with `overlap`, the compressor's parts split over two streams)."""
         L = self.layer
-        compress_insert(L, stream)
-        if L.spec.ix_heads:
-            index_topk(L, self.idx, self.ws_index, stream)
+        if self.overlap == "serial":
+            compress_insert(L, stream)
+            if L.spec.ix_heads:
+                index_topk(L, self.idx, self.ws_index, stream)
+        else:
+            cur = stream if stream is not None else torch.cuda.current_stream()
+            fork = torch.cuda.Event()
+            joined = torch.cuda.Event()
+            fork.record(cur)
+            compress_insert(L, cur, parts=("indexer",))
+            if self.overlap == "select":
+                index_scores(L, self.idx, self.ws_index, cur)
+                fork.record(cur)
+            self.side.wait_event(fork)
+            compress_insert(L, self.side, parts=("main", "window"))
+            joined.record(self.side)
+            if self.overlap == "select":
+                index_select(L, self.idx, self.ws_index, cur)
+            else:
+                index_topk(L, self.idx, self.ws_index, cur)
+            cur.wait_event(joined)
         if self.fused_out:
             if sparse_attn_out(L, self.idx, self.out, self.out_scale, self.ws_attn, stream):
                 return
