@@ -10,18 +10,23 @@
 // Kernels:
 //  * index_score_simt  - CUDA-core scores for bf16 / fp8 / fp4 key caches
 //                         (one CTA per (query, 64-entry physical block)).
-//  * index_score_tc    - tcgen05 scores for fp8 / fp4 caches (index_tc.cu).
+//  * index_score_tc / index_score_mx - tcgen05 scores for fp8 / fp4 caches
+//                         (index_tc.cu, index_mx.cu); both also leave the
+//                         4096-bin histogram of the score keys' top 12 bits.
 //  * topk_smem         - one CTA per query when the row fits in shared memory:
-//                         radix select of the k-th largest (score, -index)
-//                         composite, then an ordered compaction.
-//  * topk_hist         - the 4096-bin histogram of the score keys' top 12 bits
-//                         for long rows scored on the CUDA cores (the
-//                         tensor-core scans build it themselves).
+//                         level 1 from that histogram when there is one (only
+//                         the threshold bin's entries go through the radix
+//                         passes), else a radix select over the whole row of
+//                         the k-th largest (score, -index) composite; then an
+//                         ordered compaction.
+//  * topk_hist         - the same histogram for long rows scored on the CUDA
+//                         cores.
 //  * topk_cluster      - long rows (up to 2^20 entries): one thread-block
 //                         cluster per query finds the exact k-th largest key
-//                         from three histogram levels combined through
-//                         distributed shared memory, then every CTA writes
-//                         its selected indices in ascending order.
+//                         from three histogram levels (the cluster barrier's
+//                         release / acquire orders the levels' global
+//                         counts), then every CTA writes its selected indices
+//                         in ascending order.
 
 #include <cooperative_groups.h>
 #include <cstdio>
@@ -179,9 +184,19 @@ __device__ uint64_t select_threshold(int n, int need, Get get, uint32_t* hist, u
     const int shift = 56 - 8 * pass;
     for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-      const uint64_t c = get(i);
-      if ((c & mask) == prefix) atomicAdd(&hist[(c >> shift) & 255], 1u);
+    // one shared-memory atomic per distinct digit of a warp: the keys crowd
+    // into few digits in the first passes, and same-address atomics serialise
+    // (a 32K-entry row took ~50 us with one atomic per entry on GB300)
+    for (int base = 0; base < n; base += blockDim.x) {   // the same trip count in every lane
+      const int i = base + int(threadIdx.x);
+      uint32_t digit = 0xFFFFFFFFu;
+      if (i < n) {
+        const uint64_t c = get(i);
+        if ((c & mask) == prefix) digit = uint32_t((c >> shift) & 255);
+      }
+      const uint32_t peers = __match_any_sync(0xffffffffu, digit);
+      if (digit != 0xFFFFFFFFu && (threadIdx.x & 31) == uint32_t(__ffs(peers) - 1))
+        atomicAdd(&hist[digit], uint32_t(__popc(peers)));
     }
     __syncthreads();
     if (threadIdx.x < 32) {
@@ -249,6 +264,32 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* scratc
   return r;
 }
 
+// Threshold bin of a 4096-bin histogram whose counts this thread holds for
+// bins kHistBins-1-(4*tid+q), q < 4: the bin b with fewer than `need` counts
+// strictly above it and at least `need` at or above it; *above receives the
+// count strictly above.  All 1024 threads call it.
+__device__ int threshold_bin4(const uint32_t (&loc)[4], uint32_t need, uint32_t* scan, int* bin_s,
+                              uint32_t* above_s, uint32_t* above) {
+  const uint32_t s4 = (loc[0] + loc[1]) + (loc[2] + loc[3]);
+  uint32_t total;
+  const uint32_t excl = block_excl_scan(s4, scan, &total);
+  if (excl < need && need <= excl + s4) {
+    uint32_t acc = excl;
+    int q = 0;
+    for (; q < 4; ++q) {
+      if (acc + loc[q] >= need) break;
+      acc += loc[q];
+    }
+    *bin_s = kHistBins - 1 - (int(threadIdx.x) * 4 + q);
+    *above_s = acc;
+  }
+  __syncthreads();
+  *above = *above_s;
+  const int b = *bin_s;
+  __syncthreads();
+  return b;
+}
+
 __device__ void write_all_visible(int32_t* out, int n, int k) {
   for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = i < n ? i : -1;
 }
@@ -257,29 +298,110 @@ __device__ void write_all_visible(int32_t* out, int n, int k) {
 // Single-CTA top-k (rows that fit in shared memory)
 // ------------------------------------------------------------------------------
 
+// hist1: the scan's histogram of the top 12 key bits of every score (or null).
+// With it, level 1 comes from the histogram and only the entries of the
+// threshold bin (the candidates, usually ~1% of the row) go through the
+// 8-bit radix passes; every pass over the whole row costs a histogram whose
+// counts crowd into a few bins.
+constexpr int kCandMax = 8192;          // candidates held in shared memory (else: every entry)
+
 __global__ void __launch_bounds__(1024) topk_smem(const float* scores, int64_t row, int max_entries,
-                                                 const int32_t* positions, int k, int32_t* out) {
-  extern __shared__ uint32_t keys_s[];
+                                                 const int32_t* positions, int k, const uint32_t* hist1,
+                                                 int32_t* out) {
+  extern __shared__ __align__(16) uint32_t keys_s[];   // [row] keys, then [kCandMax] candidate indices
   __shared__ uint32_t hist[256];
   __shared__ uint32_t sh[4];
   __shared__ uint32_t scan[40];
+  __shared__ int bin_s;
+  __shared__ uint32_t above_s, ncand_s;
   const int t = blockIdx.x;
   const int n = min((positions[t] + 1) / 4, max_entries);
   int32_t* o = out + int64_t(t) * k;
   if (n <= k) { write_all_visible(o, n, k); return; }
   const float* s = scores + int64_t(t) * row;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) keys_s[i] = float_key(s[i]);
+  // the row into shared memory, kU 16-byte loads in flight per thread (one
+  // load at a time left a 32K-entry row waiting ~30 us on memory latency)
+  {
+    constexpr int kU = 8;
+    const float4* s4 = reinterpret_cast<const float4*>(s);   // rows start on 512 bytes
+    const int n4 = n >> 2;
+    for (int base = 0; base < n4; base += kU * int(blockDim.x)) {
+      float4 v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int j = base + u * int(blockDim.x) + int(threadIdx.x);
+        v[u] = j < n4 ? __ldcg(s4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int j = base + u * int(blockDim.x) + int(threadIdx.x);
+        if (j < n4)
+          reinterpret_cast<uint4*>(keys_s)[j] =
+              make_uint4(float_key(v[u].x), float_key(v[u].y), float_key(v[u].z), float_key(v[u].w));
+      }
+    }
+    for (int i = 4 * n4 + int(threadIdx.x); i < n; i += blockDim.x) keys_s[i] = float_key(s[i]);
+  }
   __syncthreads();
-  const uint64_t thr = select_threshold(
-      n, k, [&](int i) { return composite(keys_s[i], i); }, hist, sh);
-  // ordered compaction: thread c owns indices [c*chunk, (c+1)*chunk)
-  const int chunk = (n + blockDim.x - 1) / blockDim.x;
-  const int lo = threadIdx.x * chunk, hi = min(n, lo + chunk);
+  uint64_t thr;
+  bool done = false;
+  if (hist1) {
+    // level 1 from the scan's histogram: bin b1 holds the k-th largest key
+    const uint32_t* g1 = hist1 + int64_t(t) * kHistBins;
+    uint32_t loc[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) loc[q] = __ldcg(&g1[kHistBins - 1 - (int(threadIdx.x) * 4 + q)]);
+    uint32_t above1;
+    const uint32_t b1 = uint32_t(threshold_bin4(loc, uint32_t(k), scan, &bin_s, &above_s, &above1));
+    const uint32_t in_b1 = __ldcg(&g1[b1]);
+    if (in_b1 <= uint32_t(kCandMax)) {   // uniform: every thread read the same counts
+      // the candidates (key in bin b1) into a list, in any order
+      uint32_t* cand_s = keys_s + ((row + 3) & ~int64_t(3));
+      if (threadIdx.x == 0) ncand_s = 0;
+      __syncthreads();
+      const int lane = threadIdx.x & 31;
+      for (int base = 0; base < n; base += blockDim.x) {
+        const int i = base + int(threadIdx.x);
+        const bool c = i < n && (keys_s[i] >> 20) == b1;
+        const uint32_t bal = __ballot_sync(0xffffffffu, c);
+        uint32_t slot = 0;
+        if (lane == 0 && bal) slot = atomicAdd(&ncand_s, uint32_t(__popc(bal)));
+        slot = __shfl_sync(0xffffffffu, slot, 0);
+        if (c) cand_s[slot + __popc(bal & ((1u << lane) - 1u))] = uint32_t(i);
+      }
+      __syncthreads();
+      const int nc = int(ncand_s);
+      // the candidates agree on their top 12 key bits, so the radix passes
+      // start at the second byte of the composite
+      thr = select_threshold(
+          nc, int(uint32_t(k) - above1),
+          [&](int j) { const uint32_t i = cand_s[j]; return composite(keys_s[i], int(i)); }, hist, sh, 1);
+      done = true;
+    }
+  }
+  if (!done)
+    thr = select_threshold(n, k, [&](int i) { return composite(keys_s[i], i); }, hist, sh);
+  // ordered compaction: warp w owns indices [w*per_w, (w+1)*per_w), read 32
+  // consecutive keys at a time (no bank conflicts) and written in order with
+  // ballots
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int per_w = ((n + nw - 1) / nw + 31) & ~31;
+  const int wlo = min(n, warp * per_w), whi = min(n, wlo + per_w);
   uint32_t cnt = 0;
-  for (int i = lo; i < hi; ++i) cnt += composite(keys_s[i], i) >= thr;
-  uint32_t off = block_excl_scan(cnt, scan, nullptr);
-  for (int i = lo; i < hi; ++i)
-    if (composite(keys_s[i], i) >= thr) o[off++] = i;
+  for (int b = wlo; b < whi; b += 32) {
+    const int i = b + lane;
+    cnt += __popc(__ballot_sync(0xffffffffu, i < whi && composite(keys_s[i], i) >= thr));
+  }
+  uint32_t off = block_excl_scan(lane == 0 ? cnt : 0u, scan, nullptr);
+  off = __shfl_sync(0xffffffffu, off, 0);
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int b = wlo; b < whi; b += 32) {
+    const int i = b + lane;
+    const bool sel = i < whi && composite(keys_s[i], i) >= thr;
+    const uint32_t bal = __ballot_sync(0xffffffffu, sel);
+    if (sel) o[off + __popc(bal & lt)] = i;
+    off += __popc(bal);
+  }
 }
 
 // ------------------------------------------------------------------------------
@@ -342,32 +464,6 @@ __global__ void __launch_bounds__(512) topk_hist(const float* scores, int64_t ro
 // GB300, a cluster barrier costs ~1 us and a distributed-shared-memory read
 // ~0.25 us, so the levels are combined in L2 rather than through remote
 // shared memory.
-
-// Threshold bin of a 4096-bin histogram whose counts this thread holds for
-// bins kHistBins-1-(4*tid+q), q < 4: the bin b with fewer than `need` counts
-// strictly above it and at least `need` at or above it; *above receives the
-// count strictly above.  All 1024 threads call it.
-__device__ int threshold_bin4(const uint32_t (&loc)[4], uint32_t need, uint32_t* scan, int* bin_s,
-                              uint32_t* above_s, uint32_t* above) {
-  const uint32_t s4 = (loc[0] + loc[1]) + (loc[2] + loc[3]);
-  uint32_t total;
-  const uint32_t excl = block_excl_scan(s4, scan, &total);
-  if (excl < need && need <= excl + s4) {
-    uint32_t acc = excl;
-    int q = 0;
-    for (; q < 4; ++q) {
-      if (acc + loc[q] >= need) break;
-      acc += loc[q];
-    }
-    *bin_s = kHistBins - 1 - (int(threadIdx.x) * 4 + q);
-    *above_s = acc;
-  }
-  __syncthreads();
-  *above = *above_s;
-  const int b = *bin_s;
-  __syncthreads();
-  return b;
-}
 
 // Exclusive block-wide prefix sum of two 32-bit counts packed in one 64-bit
 // word (no carry crosses between them while both sums stay below 2^32).
@@ -667,9 +763,9 @@ int index_scores(const v4a_index_args* a, void* ws, size_t ws_bytes, cudaStream_
     const unsigned blocks = unsigned(std::min<size_t>((words + 255) / 256, 1024));
     if (launch_pdl(clear_words, dim3(blocks), dim3(256), 0, stream, w.hist, words) != cudaSuccess) return V4A_ERR_CUDA;
   }
-  uint32_t* hist = w.row > kSmemTopkMax ? w.hist : nullptr;
-  if (index_score_mx(a, w.scores, w.row, hist, stream, &rc)) return rc;
-  if (index_score_tc(a, w.scores, w.row, hist, stream, &rc)) return rc;
+  // the tensor-core scans always leave the level-1 histogram (both top-k paths use it)
+  if (index_score_mx(a, w.scores, w.row, w.hist, stream, &rc)) return rc;
+  if (index_score_tc(a, w.scores, w.row, w.hist, stream, &rc)) return rc;
   ScoreArgs sa;
   sa.T = T; sa.H = a->num_heads; sa.dim = c.dim; sa.k_fmt = c.format; sa.q_fmt = a->q_format;
   sa.seq_ids = a->batch.seq_ids; sa.positions = a->batch.positions; sa.keys = c;
@@ -693,10 +789,11 @@ int index_select(const v4a_index_args* a, void* ws, size_t ws_bytes, cudaStream_
   if (!ws || ws_bytes < w.total) return V4A_ERR_WORKSPACE;
   w = ws_layout(a, ws);
   if (w.row <= kSmemTopkMax) {
-    const size_t smem = size_t(w.row) * 4;
+    const uint32_t* h1 = (index_score_mx_supported(a) || index_score_tc_supported(a)) ? w.hist : nullptr;
+    const size_t smem = (size_t(w.row) + (h1 ? size_t(kCandMax) : 0)) * 4;
     cudaFuncSetAttribute(topk_smem, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     topk_smem<<<T, 1024, smem, stream>>>(w.scores, w.row, a->keys.max_blocks * 64, a->batch.positions,
-                                         a->k, a->out_idx);
+                                         a->k, h1, a->out_idx);
   } else {
     const int slices = int((w.row + kSlice - 1) / kSlice);
     // the tensor-core scans already left the first-level histogram

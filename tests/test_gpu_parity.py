@@ -283,15 +283,17 @@ def test_end_to_end(name):
         for t in rows:
             U.check_topk(gpu_idx[t], idx[t], scores[t], s.topk, f"{name} t={t}")
         gsel = {t: gpu_idx[t].astype(np.int64) for t in rows}
-    att = OB.oracle_attention(case, kv, ring, rsc, idx, rows=rows)
+    # Attention and output against the oracle's attention over the entries the
+    # GPU selected: the set equals the oracle's up to swaps among near-ties of
+    # the k-th score (checked above), and one such swap moves a row's output by
+    # more than the attention tolerance (observed: one swap at 2e-8 of the k-th
+    # score in 1,536 prefill rows), so the rest of the chain is compared on the
+    # GPU's own set.
+    att = OB.oracle_attention(case, kv, ring, rsc, idx if gsel is None else gsel, rows=rows)
     o_ref = np.stack([att[t][0] for t in rows])
     tol = U.BF16_TOL if s.kv_fmt == F.KV_BF16 else U.FP8_TOL
     U.check_close(step.o.float().cpu().numpy()[rows], o_ref, tol, name)
-    # the softmax normaliser: against the oracle's attention over the entries
-    # the GPU selected (a near-tie swap may change it; the set itself is
-    # checked above), so the comparison is as tight as the attention test's
-    att_g = att if gsel is None else OB.oracle_attention(case, kv, ring, rsc, gsel, rows=rows)
-    lse_ref = np.stack([att_g[t][1] for t in rows])
+    lse_ref = np.stack([att[t][1] for t in rows])
     lse = step.lse.cpu().numpy()[rows]
     U.record("lse", name, max_abs=float(np.max(np.abs(lse - lse_ref))))
     assert np.allclose(lse, lse_ref, atol=1e-3, rtol=1e-4), (name, float(np.max(np.abs(lse - lse_ref))))
