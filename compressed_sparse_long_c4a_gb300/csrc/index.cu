@@ -36,6 +36,7 @@
 #include "v4a_common.cuh"
 #include "v4a_internal.h"
 #include "index_tc.h"
+#include "tc_common.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -788,8 +789,15 @@ int index_select(const v4a_index_args* a, void* ws, size_t ws_bytes, cudaStream_
   IndexWs w = ws_layout(a, nullptr);
   if (!ws || ws_bytes < w.total) return V4A_ERR_WORKSPACE;
   w = ws_layout(a, ws);
-  if (w.row <= kSmemTopkMax) {
-    const uint32_t* h1 = (index_score_mx_supported(a) || index_score_tc_supported(a)) ? w.hist : nullptr;
+  const bool tc_hist = index_score_mx_supported(a) || index_score_tc_supported(a);
+  // Rows past kSmemTopkMax take the cluster path.  So do rows of more than
+  // 8192 entries with a level-1 histogram when every query's cluster fits one
+  // wave: its phases cost about the same at 32K entries as at 1M, below one
+  // CTA's passes over a 32K-entry row.
+  const int csz = topk_cluster_size();
+  const bool cluster_wave = tc_hist && csz > 0 && w.row > 8192 && int64_t(T) * csz <= tc::sm_count() / 2;
+  if (w.row <= kSmemTopkMax && !cluster_wave) {
+    const uint32_t* h1 = tc_hist ? w.hist : nullptr;
     const size_t smem = (size_t(w.row) + (h1 ? size_t(kCandMax) : 0)) * 4;
     cudaFuncSetAttribute(topk_smem, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     topk_smem<<<T, 1024, smem, stream>>>(w.scores, w.row, a->keys.max_blocks * 64, a->batch.positions,

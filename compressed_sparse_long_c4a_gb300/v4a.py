@@ -335,10 +335,11 @@ class Step:
                                    dtype=torch.uint8, device=dev)
 
     def launches_per_step(self) -> int:
-        """libv4a kernels one run() launches: compress (1); indexer workspace
-        clear (1) + scan (1) + top-k (1, plus the histogram kernel for long
-        rows scored on the CUDA cores); attention (1, + combine when the key
-        list is split); output (1)."""
+        """libv4a kernels one run() launches: compress (1, 2 when split over
+        two streams); indexer workspace clear (1) + scan (1) + top-k (1, plus
+        the histogram kernel for long rows scored on the CUDA cores); then per
+        batch of queries either attention + merge + encode (fused output) or
+        attention (+ combine when the key list is split) and the output stage."""
         s = self.layer.spec
         n = 1 if self.overlap == "serial" else 2   # compress (split in two with overlap)
         if s.ix_heads:
