@@ -16,7 +16,8 @@ dominant kernel (the indexer scan) against the measured HBM copy bandwidth.
 
 `variants` holds the same measurement for the indexer format with
 power-of-two block scales (the block-scaled tensor-core scan) and, for the
-default workload, for the same layer at 128k context.
+default workload, for the same layer at 128k context; `model_stack` times the
+model's whole attention stack (30 c4a + 31 c128a layers) as one graph.
 
 --gpus N outside a launcher starts N ranks through torch.distributed.run (one
 replica of the step per GPU: the path shards by sequence, no collective).
@@ -350,6 +351,47 @@ def measure_workload(spec, args, dev, barrier, windows: int):
             "replicas": replicas, "win_ms": win_ms, "stage_us": stage_us, "clocks": clk.summary()}
 
 
+def measure_stack(args, dev, c4a_case, barrier, windows: int, reps: int = 3):
+    """The model's whole attention stack (30 c4a + 31 c128a layers at the
+    same batch and context) as one CUDA graph: windows of `reps` replays."""
+    import torch
+    from compressed_sparse_long_c4a_gb300 import stack as S
+    ws, _, _ = _dist()
+    kinds = S.deepseek_v4_mix()
+    st = S.AttentionStack(kinds, S.decode_1m_cases(0, c4a_case), dev)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        st.run(stream)
+    torch.cuda.synchronize()
+    assert st.status() == 0, "device status set in the stack's first step"
+    g = st.capture(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g.replay()
+    torch.cuda.synchronize()
+    barrier()
+    win = []
+    for _ in range(windows):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        win.append(max_over_ranks(e0.elapsed_time(e1) / reps, dev))
+    stats = window_stats(win)
+    ms = stats["median"]
+    n_c4a, n_c128a = kinds.count("c4a"), kinds.count("c128a")
+    out = {"layers": f"{n_c4a} c4a + {n_c128a} c128a, alternating from c128a; decode, batch "
+                     f"{st.tokens} at 1M context; one CUDA graph per step",
+           "ms_per_step": ms, "value": whole_job_rate(ws, st.tokens, ms),
+           "unit": "tokens/s through all attention layers", "us_per_layer_mean": ms * 1e3 / len(kinds),
+           "windows": stats, "gpu_launches_per_step": st.launches_per_step()}
+    del g, st
+    return out
+
+
 def window_stats(win_ms):
     s = sorted(win_ms)
     med = statistics.median(s)
@@ -497,6 +539,12 @@ def main():
             "step_hbm_frac": (vscan_b + vgather_b + vwin_b) / (vst["median"] * 1e-3) / 1e9 / hbm_peak,
             "clocks": vm["clocks"]}
         del vm
+    # the whole attention stack of the model (30 c4a + 31 c128a layers) per token
+    if not args.no_variants and spec.name == "c4a_decode_b4_1m":
+        try:
+            line["model_stack"] = measure_stack(args, dev, case, barrier, max(1, args.windows))
+        except Exception as e:   # reported in the line; the headline above stands
+            line["model_stack"] = {"error": f"{type(e).__name__}: {e}"}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         t0 = time.perf_counter()
         oracle_token(case, 0, 1.0)

@@ -205,7 +205,7 @@ static int validate_shape(const v4a_attn_args* a) {
   // every query's window [m - window_len + 1, m] must be in the ring at once
   // (the batch's newest positions were written by the compress call before)
   if (int64_t(a->window_cap) < int64_t(a->window_len) - 1 + B.max_new_per_seq) return V4A_ERR_RING_TOO_SMALL;
-  if (a->idx && (a->k < 1 || a->k > 65536)) return V4A_ERR_INVALID_ARG;
+  if (a->idx && (a->k < 0 || a->k > 65536)) return V4A_ERR_INVALID_ARG;   // k = 0: window only
   const int D = c.dim;
   if (D != 64 && D != 128 && D != 256 && D != 512) return V4A_ERR_UNSUPPORTED;
   if (a->num_heads < 1 || a->num_heads > 256) return V4A_ERR_UNSUPPORTED;

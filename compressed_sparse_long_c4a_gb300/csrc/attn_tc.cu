@@ -66,6 +66,7 @@ struct AtcArgs {
   int rshift, eshift; // log2 of the compression ratio and of the entries per block
   int nq;             // N groups of O = P K (one MMA issuer each)
   int tma_out;        // rows leave through the output tensor map (H % 8 == 0)
+  int kv_align8;      // cache rows start on 8 bytes only: read them as two 8-byte halves
   int direct;         // one chunk per query and no merge kernel after: rows are the output
 };
 
@@ -240,7 +241,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
       const int c = tid + i * kThreads;
       const int r = c / (D / 16), cc = c % (D / 16);
       raw[i] = make_uint4(0, 0, 0, 0);
-      if (s.kfmt[r] == V4A_KV_FP8_TOKEN) raw[i] = __ldg(reinterpret_cast<const uint4*>(s.src[r] + cc * 16));
+      if (s.kfmt[r] == V4A_KV_FP8_TOKEN) {
+        const uint8_t* src = s.src[r] + cc * 16;
+        if (a.kv_align8) {
+          const uint2 lo = __ldg(reinterpret_cast<const uint2*>(src)), hi = __ldg(reinterpret_cast<const uint2*>(src + 8));
+          raw[i] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+        } else {
+          raw[i] = __ldg(reinterpret_cast<const uint4*>(src));
+        }
+      }
     }
     float sc = 1.f;   // thread tid < kKeys: key tid's scale, in flight with the rows
     if (tid < kKeys && s.sptr[tid]) sc = __ldg(s.sptr[tid]);
@@ -463,20 +472,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
 // four groups are summed through shared memory.  Many small CTAs spread the
 // partial rows over every SM (one SM alone streams them slowly).
 constexpr int kCombGroups = 4;
-constexpr int kCombMax = 16;     // splits per group held in registers (splits <= 64)
+constexpr int kCombMax = 16;     // splits per group held in registers per round (one round up to 64)
+constexpr int kMaxSplits = 1024; // chunks per query (c128a at 1M: 130)
 
 __global__ void __launch_bounds__(256, 2) attn_combine_bf16(int H, int D, int splits, const uint16_t* part_o,
                                                             const float* part_ml, uint16_t* out, float* lse) {
   pdl_trigger();
   pdl_wait();   // the partials are the previous kernel's output
-  __shared__ float wsm[kCombGroups * kCombMax];
+  __shared__ float wsm[kMaxSplits];
   __shared__ float inv_s;
   __shared__ float4 part_s[kCombGroups - 1][64][2];
   const int t = blockIdx.y, h = blockIdx.x;
   const int grp = threadIdx.x >> 6, c = threadIdx.x & 63;
   const bool active = c < D / 8;
-  // 1. this thread's partial chunks, all loads in flight together
   const uint16_t* po = part_o + (int64_t(t) * splits * H + h) * D + c * 8;
+  // 1. this thread's first round of partial chunks, in flight together
   uint4 v[kCombMax];
 #pragma unroll
   for (int u = 0; u < kCombMax; ++u) {
@@ -484,38 +494,50 @@ __global__ void __launch_bounds__(256, 2) attn_combine_bf16(int H, int D, int sp
     v[u] = (active && sp < splits) ? __ldcg(reinterpret_cast<const uint4*>(po + int64_t(sp) * H * D))
                                    : make_uint4(0, 0, 0, 0);
   }
-  // 2. weights of every split (warp 0), while those loads are in flight
+  // 2. weights of every split (warp 0), while those loads are in flight;
+  //    lane l takes splits l, l + 32, ... in order
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     const float* ml = part_ml + (int64_t(t) * splits * H + h) * 2;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    if (lane < splits) { m0 = ml[int64_t(lane) * H * 2]; l0 = ml[int64_t(lane) * H * 2 + 1]; }
-    if (lane + 32 < splits) { m1 = ml[int64_t(lane + 32) * H * 2]; l1 = ml[int64_t(lane + 32) * H * 2 + 1]; }
-    const float mx = warp_max(fmaxf(m0, m1));
-    const float w0 = m0 == -INFINITY ? 0.f : l0 * exp2f(m0 - mx);
-    const float w1 = m1 == -INFINITY ? 0.f : l1 * exp2f(m1 - mx);
-    if (lane < splits) wsm[lane] = w0;
-    if (lane + 32 < splits) wsm[lane + 32] = w1;
-    const float tot = warp_sum(w0 + w1);
+    float mx = -INFINITY;
+    for (int sp = lane; sp < splits; sp += 32) mx = fmaxf(mx, ml[int64_t(sp) * H * 2]);
+    mx = warp_max(mx);
+    float tl = 0.f;
+    for (int sp = lane; sp < splits; sp += 32) {
+      const float m = ml[int64_t(sp) * H * 2], l = ml[int64_t(sp) * H * 2 + 1];
+      const float w = m == -INFINITY ? 0.f : l * exp2f(m - mx);
+      wsm[sp] = w;
+      tl += w;
+    }
+    const float tot = warp_sum(tl);
     if (lane == 0) {
       inv_s = tot > 0.f ? 1.f / tot : 0.f;
       if (lse) lse[int64_t(t) * H + h] = (mx + log2f(tot)) * 0.6931471805599453f;
     }
   }
   __syncthreads();
-  // 3. weighted sum of this thread's splits (an empty chunk has weight 0 and
-  //    its partial row is never read into the sum)
+  // 3. weighted sum of this thread's splits in increasing order, round by
+  //    round (an empty chunk has weight 0 and its row is never read into the sum)
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int u0 = 0;; u0 += kCombMax) {
 #pragma unroll
-  for (int u = 0; u < kCombMax; ++u) {
-    const int sp = grp + u * kCombGroups;
-    const float w = sp < splits ? wsm[sp] : 0.f;
-    if (w == 0.f) continue;
-    const uint32_t q[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+    for (int u = 0; u < kCombMax; ++u) {
+      const int sp = grp + (u0 + u) * kCombGroups;
+      const float w = sp < splits ? wsm[sp] : 0.f;
+      if (w == 0.f) continue;
+      const uint32_t q[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      acc[2 * j] = fmaf(w, bf16_to_f32(uint16_t(q[j] & 0xffffu)), acc[2 * j]);
-      acc[2 * j + 1] = fmaf(w, bf16_to_f32(uint16_t(q[j] >> 16)), acc[2 * j + 1]);
+      for (int j = 0; j < 4; ++j) {
+        acc[2 * j] = fmaf(w, bf16_to_f32(uint16_t(q[j] & 0xffffu)), acc[2 * j]);
+        acc[2 * j + 1] = fmaf(w, bf16_to_f32(uint16_t(q[j] >> 16)), acc[2 * j + 1]);
+      }
+    }
+    if ((u0 + kCombMax) * kCombGroups >= splits) break;
+#pragma unroll
+    for (int u = 0; u < kCombMax; ++u) {   // the next round's rows
+      const int sp = grp + (u0 + kCombMax + u) * kCombGroups;
+      v[u] = (active && sp < splits) ? __ldcg(reinterpret_cast<const uint4*>(po + int64_t(sp) * H * D))
+                                     : make_uint4(0, 0, 0, 0);
     }
   }
   if (grp > 0) {
@@ -552,7 +574,16 @@ bool handled(const v4a_attn_args* a) {
   const int D = a->kv.dim;
   if (D != 128 && D != 256 && D != 512) return false;
   if (a->num_heads > kRows) return false;
-  if (splits_of(a) > kCombGroups * kCombMax) return false;   // the combine holds at most 64 splits
+  if (splits_of(a) > kMaxSplits) return false;
+  // key rows are read with 16-byte loads, or two 8-byte loads when the block
+  // size is a multiple of 8 only (an fp8 c128a block holds 2 x (512 + 4) B),
+  // so the pool and the window ring must start on 16 bytes.  A window-only
+  // call reads no cache entry.
+  const bool reads_cache = !a->idx || a->k > 0;
+  if (reads_cache && ((kv_block_bytes(a->kv.format, a->kv.ratio, D) & 7) ||
+                      (reinterpret_cast<uintptr_t>(a->kv.pool) & 15)))
+    return false;
+  if (reinterpret_cast<uintptr_t>(a->window) & 15) return false;
   return true;
 }
 
@@ -624,6 +655,7 @@ bool attn_tc(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t str
   t.num_blocks = a->kv.num_blocks;
   t.pool = static_cast<const uint8_t*>(a->kv.pool);
   t.block_bytes = kv_block_bytes(a->kv.format, a->kv.ratio, a->kv.dim);
+  t.kv_align8 = (t.block_bytes & 15) != 0 ? 1 : 0;
   t.idx = a->idx ? a->idx + int64_t(t0) * a->k : nullptr;
   t.window = static_cast<const uint8_t*>(a->window);
   t.wscale = a->window_scale;

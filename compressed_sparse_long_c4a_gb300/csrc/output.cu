@@ -160,7 +160,7 @@ inv_rope_quant_kernel(const OutDev a) {
 // The bf16 attention output never leaves the workspace, and the bytes equal
 // those of the two-call path.
 constexpr int kMergeGroups = 4;          // chunk groups: chunk sp belongs to group sp % 4
-constexpr int kMergeMaxSplits = 64;      // kPer <= 16 chunks per group held in registers
+constexpr int kMergeMaxSplits = 1024;    // chunks per query (rounds of kPer per group)
 constexpr int kEncSlices = 16;           // encode CTAs per token
 constexpr int kEncPer = 4;               // 16-byte chunks per encode thread held in registers
 
@@ -172,9 +172,10 @@ struct MergeDev {
   float* part_ml;     // [T][splits][H][2]; chunk 0's pairs receive (row amax, 0)
 };
 
-// kPer: chunks per group held in registers (splits <= 4 * kPer), as small as
-// the split count allows so that four CTAs fit an SM and every (head, token)
-// of a decode batch has its loads in flight in one wave.
+// kPer: chunks per group held in registers per round (one round when
+// splits <= 4 * kPer), as small as the split count allows so that four CTAs
+// fit an SM and every (head, token) of a decode batch has its loads in
+// flight in one wave.
 template <int kPer>
 __global__ void __launch_bounds__(256, kPer <= 9 ? 4 : 2) merge_amax_kernel(const MergeDev a) {
   __shared__ float wsm[kMergeMaxSplits];
@@ -196,7 +197,7 @@ __global__ void __launch_bounds__(256, kPer <= 9 ? 4 : 2) merge_amax_kernel(cons
     // one chunk: its normalised row is the attention output as stored
     if (grp == 0 && active) row = __ldcg(reinterpret_cast<const uint4*>(po));
   } else {
-    // 1. this thread's chunk rows, all loads in flight together
+    // 1. this thread's first round of chunk rows, in flight together
     uint4 v[kPer];
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
@@ -204,33 +205,46 @@ __global__ void __launch_bounds__(256, kPer <= 9 ? 4 : 2) merge_amax_kernel(cons
       v[u] = (active && sp < a.splits) ? __ldcg(reinterpret_cast<const uint4*>(po + int64_t(sp) * a.H * a.D))
                                        : make_uint4(0, 0, 0, 0);
     }
-    // 2. weights of every chunk (warp 0), while those loads are in flight
+    // 2. weights of every chunk (warp 0), while those loads are in flight;
+    //    lane l takes chunks l, l + 32, ... in order
     if (threadIdx.x < 32) {
       const int lane = threadIdx.x;
-      float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-      if (lane < a.splits) { m0 = ml[int64_t(lane) * a.H * 2]; l0 = ml[int64_t(lane) * a.H * 2 + 1]; }
-      if (lane + 32 < a.splits) { m1 = ml[int64_t(lane + 32) * a.H * 2]; l1 = ml[int64_t(lane + 32) * a.H * 2 + 1]; }
-      const float mx = warp_max(fmaxf(m0, m1));
-      const float w0 = m0 == -INFINITY ? 0.f : l0 * exp2f(m0 - mx);
-      const float w1 = m1 == -INFINITY ? 0.f : l1 * exp2f(m1 - mx);
-      if (lane < a.splits) wsm[lane] = w0;
-      if (lane + 32 < a.splits) wsm[lane + 32] = w1;
-      const float tot = warp_sum(w0 + w1);
+      float mx = -INFINITY;
+      for (int sp = lane; sp < a.splits; sp += 32) mx = fmaxf(mx, ml[int64_t(sp) * a.H * 2]);
+      mx = warp_max(mx);
+      float tl = 0.f;
+      for (int sp = lane; sp < a.splits; sp += 32) {
+        const float m = ml[int64_t(sp) * a.H * 2], l = ml[int64_t(sp) * a.H * 2 + 1];
+        const float w = m == -INFINITY ? 0.f : l * exp2f(m - mx);
+        wsm[sp] = w;
+        tl += w;
+      }
+      const float tot = warp_sum(tl);
       if (lane == 0) inv_s = tot > 0.f ? 1.f / tot : 0.f;
     }
     __syncthreads();
-    // 3. weighted sum of this thread's chunks (an empty chunk has weight 0)
+    // 3. weighted sum of this thread's chunks in increasing order, round by
+    //    round (an empty chunk has weight 0)
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int u0 = 0;; u0 += kPer) {
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const int sp = grp + u * kMergeGroups;
-      const float w = sp < a.splits ? wsm[sp] : 0.f;
-      if (w == 0.f) continue;
-      const uint32_t q[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      for (int u = 0; u < kPer; ++u) {
+        const int sp = grp + (u0 + u) * kMergeGroups;
+        const float w = sp < a.splits ? wsm[sp] : 0.f;
+        if (w == 0.f) continue;
+        const uint32_t q[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        acc[2 * j] = fmaf(w, bf16_to_f32(uint16_t(q[j] & 0xffffu)), acc[2 * j]);
-        acc[2 * j + 1] = fmaf(w, bf16_to_f32(uint16_t(q[j] >> 16)), acc[2 * j + 1]);
+        for (int j = 0; j < 4; ++j) {
+          acc[2 * j] = fmaf(w, bf16_to_f32(uint16_t(q[j] & 0xffffu)), acc[2 * j]);
+          acc[2 * j + 1] = fmaf(w, bf16_to_f32(uint16_t(q[j] >> 16)), acc[2 * j + 1]);
+        }
+      }
+      if ((u0 + kPer) * kMergeGroups >= a.splits) break;
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {   // the next round's rows
+        const int sp = grp + (u0 + kPer + u) * kMergeGroups;
+        v[u] = (active && sp < a.splits) ? __ldcg(reinterpret_cast<const uint4*>(po + int64_t(sp) * a.H * a.D))
+                                         : make_uint4(0, 0, 0, 0);
       }
     }
     if (grp > 0) {

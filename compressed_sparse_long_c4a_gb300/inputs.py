@@ -62,6 +62,7 @@ class LayerSpec:
     swa: int = 128
     out_fmt: int = OUT_BF16
     spare_blocks: int = 3      # unused physical blocks in the pool
+    window_only: bool = False  # pure sliding-window layer: attention over the window alone
 
     @property
     def entries_per_block(self) -> int:
@@ -337,6 +338,24 @@ def c4a_decode_128k() -> LayerSpec:
     return dataclasses.replace(c4a_decode_1m(), name="c4a_decode_b4_128k", cached=(131_071,) * 4)
 
 
+def swa_decode_1m() -> LayerSpec:
+    """A pure sliding-window layer of the same model at 1M context, batch 4:
+    attention over the last 128 tokens only (no compressed entries), fp8
+    window, fp8 output.  The compressed-cache geometry is c128a's (its cache
+    is allocated but never read)."""
+    return LayerSpec(name="swa_decode_b4_1m", ratio=128, batch=4, heads=128, dim=512,
+                     cached=(1_048_575,) * 4, kv_fmt=KV_FP8_TOKEN, swa_fmt=KV_FP8_TOKEN,
+                     out_fmt=OUT_FP8_TOKEN, spare_blocks=1, window_only=True)
+
+
+def c128a_decode_1m() -> LayerSpec:
+    """A c128a layer of the same model at 1M context, batch 4: attention over
+    all 8,192 compressed entries plus the window, fp8 caches and output."""
+    return LayerSpec(name="c128a_decode_b4_1m", ratio=128, batch=4, heads=128, dim=512,
+                     cached=(1_048_575,) * 4, kv_fmt=KV_FP8_TOKEN, swa_fmt=KV_FP8_TOKEN,
+                     out_fmt=OUT_FP8_TOKEN, spare_blocks=1)
+
+
 WORKLOADS = {
     "c4a_decode_b1_1k": c4a_decode_1k,
     "c4a_decode_b32_32k_64k": c4a_decode_b32_32k_64k,
@@ -345,6 +364,7 @@ WORKLOADS = {
     "c4a_decode_b4_1m": c4a_decode_1m,
     "c4a_decode_b4_1m_mx": c4a_decode_1m_mx,
     "c4a_decode_b4_128k": c4a_decode_128k,
+    "c128a_decode_b4_1m": c128a_decode_1m,
 }
 
 

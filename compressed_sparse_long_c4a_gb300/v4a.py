@@ -145,6 +145,9 @@ class DeviceLayer:
             v = getattr(case, f)
             if v is not None and v.numel() > 0:
                 t[f] = v.to(device).contiguous()
+        if case.spec.window_only:
+            # any non-NULL idx with k = 0 selects the window alone (never read)
+            t["window_only_idx"] = torch.zeros(1, dtype=torch.int32, device=device)
         return cls(spec=case.spec, t=t, status=torch.zeros(1, dtype=torch.int32, device=device))
 
     # ---- argument structs -------------------------------------------------
@@ -193,7 +196,11 @@ class DeviceLayer:
 
     def attn_args(self, idx: torch.Tensor | None, out: torch.Tensor, lse: torch.Tensor | None) -> AttnArgs:
         s, t = self.spec, self.t
-        return AttnArgs(self.batch(), self.kv_cache(), _ptr(idx), s.topk if idx is not None else 0,
+        if s.window_only:
+            idx, k = t["window_only_idx"], 0
+        else:
+            k = s.topk if idx is not None else 0
+        return AttnArgs(self.batch(), self.kv_cache(), _ptr(idx), k,
                         _ptr(t["swa_ring"]), _ptr(t.get("swa_scale")), s.swa_cap, s.swa_fmt, s.swa,
                         s.heads, _ptr(t["q"]), 1.0 / math.sqrt(s.dim), _ptr(out), _ptr(lse),
                         _ptr(self.status))
@@ -350,7 +357,7 @@ class Step:
         # the tensor-core attention runs long batches (chunked prefill) as
         # several launches of at most 64 waves of 152 CTAs, one CTA per
         # 64-key chunk of a query's list
-        nsel = s.topk if s.ix_heads else s.max_blocks * (256 // s.ratio)
+        nsel = 0 if s.window_only else (s.topk if s.ix_heads else s.max_blocks * (256 // s.ratio))
         chunks = -(-(nsel + s.swa) // 64)
         per = max(1, min(s.tokens, (64 * 152) // chunks))
         batches = -(-s.tokens // per)
@@ -363,7 +370,9 @@ class Step:
         """compress_insert -> index_topk -> sparse_attn -> inv_rope_quant
         (with `overlap`, the compressor's parts split over two streams)."""
         L = self.layer
-        if self.overlap == "serial":
+        if L.spec.window_only:
+            compress_insert(L, stream, parts=("window",))   # a pure sliding-window layer has no compressor
+        elif self.overlap == "serial":
             compress_insert(L, stream)
             if L.spec.ix_heads:
                 index_topk(L, self.idx, self.ws_index, stream)

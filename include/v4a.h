@@ -246,14 +246,17 @@ V4A_API int v4a_index_topk_static(const v4a_index_args* args, void* stream);
  *   S = {selected compressed entries} U {window tokens max(0,m-W+1) .. m}:
  *   z_n = softmax_scale * q_h . k_n,  o_h = sum_n softmax(z)_n k_n.
  * idx == NULL selects every visible entry i < (m+1)/ratio (c128a layers).
- * Entries of idx that are -1 are skipped.  out is bf16; lse (optional) is the
+ * Entries of idx that are -1 are skipped.  idx != NULL with k == 0 selects no
+ * compressed entry: the window alone (the pages' pure sliding-window layers;
+ * idx is then not read, and the kv cache fields must still pass the shape
+ * checks but no entry of it is read).  out is bf16; lse (optional) is the
  * natural-log sum of exp(z) per (t, h).
  */
 typedef struct {
   v4a_batch batch;
   v4a_cache kv;                /* main compressed cache */
   const int32_t* idx;          /* [T][k] or NULL */
-  int32_t k;
+  int32_t k;                   /* 1..65536 with idx; 0 with a non-NULL idx: window only */
   const void* window;          /* [num_seqs][window_cap][kv.dim] */
   const float* window_scale;   /* [num_seqs][window_cap] (fp8 window only) */
   int32_t window_cap;          /* >= window_len - 1 + max_new_per_seq, else V4A_ERR_RING_TOO_SMALL */

@@ -313,7 +313,8 @@ def test_end_to_end(name):
 
 
 # Workloads whose attention the fused attention + output call must take.
-FUSED_EXPECTED = {"c4a_decode_b4_1m", "c4a_decode_b4_1m_mx", "c4a_decode_b4_128k", "c4a_decode_b32_32k_64k",
+FUSED_EXPECTED = {"c4a_decode_b4_1m", "c4a_decode_b4_1m_mx", "c4a_decode_b4_128k", "c128a_decode_b4_1m",
+                  "c4a_decode_b32_32k_64k",
                   "c128a_decode_b64_64k_128k", "c4a_decode_small_fp8ix", "c4a_decode_small_fp4ix_fp8kv",
                   "c4a_decode_small_mx4ix_fp8kv"}
 
