@@ -16,7 +16,10 @@ Pinning status (what each part is checked against, in ``tests/``):
   formats     - exhaustive codec checks against torch.float8_e4m3fn and the
                 OCP e2m1 value table; bf16 against torch.bfloat16; the MX
                 power-of-two block scale by hand-worked blocks and its
-                error bound.
+                error bound; the DeepSeek-V4 584-byte row by the article's
+                byte list and page formula, hand-worked scale bytes, a
+                brute-force search for the scale rule, and its bytes
+                against torch's e4m3 / bf16 casts.
   geometry    - closed forms for counts/windows/causality, brute-force
                 enumeration of slot mapping.
   compressor  - closed forms (equal logits -> mean, dominant logit -> copy,

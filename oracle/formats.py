@@ -26,6 +26,17 @@ Sources and readings
   scale).  The scale is chosen by the MX conversion rule,
   X = 2^(floor(log2 amax) - 2), written into the fp32 scale word; codes are
   e2m1 of v / X (nearest-even, saturating to +-6).
+* DeepSeek-V4 fp8 row of the SGLang KV-pool article (section "DeepSeek-V4",
+  the per-token byte list): 448 fp8 "nope" elements, then the 64 rope
+  elements in bf16 (128 B), then one scale byte per 64 nope elements (7 B),
+  then 1 pad byte: 584 B per token; a page of P tokens is padded to
+  ceil(P * 584 / 576) * 576 bytes.  Readings taken: the nope part is the
+  first D - 64 elements of a D = 512 row and the rope part its last 64 (the
+  rotary dims of every other layout here); a scale byte is an unsigned
+  power-of-two exponent (UE8M0, value 2^(byte - 127)), chosen as the smallest
+  power of two s with amax / s <= 448 (so no code saturates; 1 for amax = 0);
+  codes are e4m3 of v / s (nearest-even); the pad byte is 0; the page's
+  rows are consecutive from its first byte.
 * Block layout (vLLM page, "A single logical block size": every compressed
   layer's logical block is 256 native positions, so a c4a block holds 64
   entries and a c128a block 2).  Reading taken for the bytes inside one
@@ -241,7 +252,8 @@ def unpack_nibbles(packed: np.ndarray) -> np.ndarray:
 # Paged-block byte layouts
 # --------------------------------------------------------------------------
 
-KV_BF16, KV_FP8_TOKEN = 0, 1
+KV_BF16, KV_FP8_TOKEN, KV_FP8_DSV4 = 0, 1, 2
+DSV4_NOPE, DSV4_ROPE, DSV4_QBLOCK, DSV4_ROW, DSV4_PAGE_UNIT = 448, 64, 64, 584, 576
 # IX_FP4_MX32: the IX_FP4_B32 byte layout with every scale a power of two
 # chosen by the OCP MX rule (mx_shared_scale).
 IX_BF16, IX_FP8_B128, IX_FP4_B32, IX_FP4_MX32 = 0, 1, 2, 3
@@ -254,7 +266,47 @@ def kv_block_bytes(fmt: int, entries: int, dim: int) -> int:
         return entries * dim * 2
     if fmt == KV_FP8_TOKEN:
         return entries * dim + entries * 4
+    if fmt == KV_FP8_DSV4:
+        assert dim == DSV4_NOPE + DSV4_ROPE
+        return -(-entries * DSV4_ROW // DSV4_PAGE_UNIT) * DSV4_PAGE_UNIT
     raise ValueError(fmt)
+
+
+def ue8m0_e4m3_scale_byte(block: np.ndarray) -> int:
+    """Scale byte b of one nope block: s = 2^(b - 127) is the smallest power
+    of two with amax / s <= 448.  With amax = f * 2^e (f in [0.5, 1)) and
+    448 = 0.875 * 2^9: amax / 2^k <= 448 iff f * 2^(e - 9 - k) <= 0.875, so
+    k = e - 9, plus 1 when f > 0.875."""
+    amax = float(np.max(np.abs(block))) if block.size else 0.0
+    if amax == 0.0:
+        return 127
+    f, e = np.frexp(amax)
+    k = int(e) - 9 + (1 if f > 0.875 else 0)
+    return min(max(k + 127, 1), 254)
+
+
+def dsv4_row_encode(v: np.ndarray) -> np.ndarray:
+    """One D = 512 row -> its 584 bytes."""
+    v = np.asarray(v, np.float64)
+    out = np.zeros(DSV4_ROW, np.uint8)
+    for j in range(DSV4_NOPE // DSV4_QBLOCK):
+        seg = v[j * DSV4_QBLOCK:(j + 1) * DSV4_QBLOCK]
+        b = ue8m0_e4m3_scale_byte(seg)
+        out[j * DSV4_QBLOCK:(j + 1) * DSV4_QBLOCK] = e4m3_encode(np.ldexp(seg, 127 - b))
+        out[DSV4_NOPE + 2 * DSV4_ROPE + j] = b
+    out[DSV4_NOPE:DSV4_NOPE + 2 * DSV4_ROPE] = bf16_encode(v[DSV4_NOPE:]).view(np.uint8)
+    return out
+
+
+def dsv4_row_decode(raw: np.ndarray) -> np.ndarray:
+    """584 bytes [..., 584] -> float64 [..., 512]."""
+    raw = np.ascontiguousarray(raw, np.uint8)
+    lead = raw.shape[:-1]
+    codes = raw[..., :DSV4_NOPE].reshape(lead + (DSV4_NOPE // DSV4_QBLOCK, DSV4_QBLOCK))
+    b = raw[..., DSV4_NOPE + 2 * DSV4_ROPE:DSV4_NOPE + 2 * DSV4_ROPE + DSV4_NOPE // DSV4_QBLOCK]
+    nope = np.ldexp(e4m3_decode(codes), b.astype(np.int64)[..., None] - 127).reshape(lead + (DSV4_NOPE,))
+    rope = bf16_decode(raw[..., DSV4_NOPE:DSV4_NOPE + 2 * DSV4_ROPE].copy().view(np.uint16))
+    return np.concatenate([nope, rope], axis=-1)
 
 
 def ix_block_bytes(fmt: int, dim: int, entries: int = 64) -> int:
@@ -279,6 +331,9 @@ def kv_block_decode(raw: np.ndarray, fmt: int, entries: int, dim: int) -> np.nda
         codes = raw[..., :entries * dim].reshape(lead + (entries, dim))
         scales = raw[..., entries * dim:entries * dim + 4 * entries].copy().view(np.float32)
         return e4m3_decode(codes) * scales.astype(np.float64)[..., None]
+    if fmt == KV_FP8_DSV4:
+        rows = raw[..., :entries * DSV4_ROW].reshape(lead + (entries, DSV4_ROW))
+        return dsv4_row_decode(rows)
     raise ValueError(fmt)
 
 

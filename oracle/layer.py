@@ -89,9 +89,12 @@ def window_keys(seq_ids, positions, k_bits, rope_dims, theta) -> dict:
 # --------------------------------------------------------------------------
 
 def encode_kv_row(v: np.ndarray, fmt: int):
-    """-> (data bytes, scale or None) of one shared-KV / window row."""
+    """-> (data bytes, scale or None) of one shared-KV / window row (the
+    DeepSeek-V4 row carries its scales inside its 584 bytes)."""
     if fmt == F.KV_BF16:
         return F.bf16_encode(v).view(np.uint8), None
+    if fmt == F.KV_FP8_DSV4:
+        return F.dsv4_row_encode(v), None
     codes, s = F.fp8_token_encode(v)
     return codes, s
 

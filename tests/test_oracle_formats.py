@@ -1,4 +1,6 @@
 """Pins of the oracle's number formats against library casts and the OCP tables."""
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -205,3 +207,49 @@ def test_fp4_mx_layout_equals_fp4_layout():
     raw = rng.integers(0, 256, F.ix_block_bytes(F.IX_FP4_B32, 128), dtype=np.uint8)
     raw[64 * 64:] = np.ldexp(1.0, rng.integers(-5, 5, 64 * 4)).astype(np.float32).view(np.uint8)
     assert np.array_equal(F.ix_block_decode(raw, F.IX_FP4_MX32, 128), F.ix_block_decode(raw, F.IX_FP4_B32, 128))
+
+
+# ---- DeepSeek-V4 fp8 row (SGLang KV-pool article, section "DeepSeek-V4") ----
+
+def test_dsv4_row_and_page_arithmetic_from_the_pages():
+    # the article's per-token byte list: 448 fp8 + 64 x bf16 + 448 / 64 scales + 1 pad
+    assert 448 + 64 * 2 + 448 // 64 + 1 == 584 == F.DSV4_ROW
+    # pages padded to 576-byte units: ceil(page_size * 584 / 576) * 576
+    assert F.kv_block_bytes(F.KV_FP8_DSV4, 64, 512) == math.ceil(64 * 584 / 576) * 576 == 37440
+    assert F.kv_block_bytes(F.KV_FP8_DSV4, 2, 512) == 1728
+
+
+def test_dsv4_scale_byte_hand_values_and_brute_force():
+    # hand-worked: 448 = 0.875 * 2^9 fits scale 1; 449 needs 2; 1.0 fits 2^-8 (1 / 2^-8 = 256 <= 448 < 512)
+    assert F.ue8m0_e4m3_scale_byte(np.array([448.0])) == 127
+    assert F.ue8m0_e4m3_scale_byte(np.array([-449.0, 3.0])) == 128
+    assert F.ue8m0_e4m3_scale_byte(np.array([1.0, -0.25])) == 119
+    assert F.ue8m0_e4m3_scale_byte(np.array([896.5])) == 129
+    assert F.ue8m0_e4m3_scale_byte(np.zeros(64)) == 127
+    rng = np.random.default_rng(5)
+    for amax in np.exp(rng.uniform(-20, 20, 300)):
+        k = -140
+        while amax / 2.0 ** k > 448.0:      # smallest power of two that keeps amax within e4m3
+            k += 1
+        assert F.ue8m0_e4m3_scale_byte(np.array([amax])) == k + 127
+
+
+def test_dsv4_row_bytes_match_library_casts():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(6)
+    v = rng.normal(0, 1, 512) * np.exp(rng.uniform(-3, 3, 512))
+    row = F.dsv4_row_encode(v)
+    assert row.shape == (584,) and row[583] == 0
+    for j in range(7):
+        seg = v[64 * j:64 * (j + 1)]
+        b = int(row[576 + j])
+        want = torch.from_numpy(np.ldexp(seg, 127 - b)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(row[64 * j:64 * (j + 1)], want)
+        assert np.max(np.abs(seg)) <= 448.0 * 2.0 ** (b - 127) < 2 * np.max(np.abs(seg))
+    rope = torch.from_numpy(v[448:]).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint8)
+    assert np.array_equal(row[448:576], rope)
+    # decode: codes times their block's power of two; rope as stored
+    dec = F.dsv4_row_decode(row)
+    codes = torch.from_numpy(row[:448].copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(dec[:448], codes * np.repeat(2.0 ** (row[576:583].astype(np.int64) - 127), 64))
+    assert np.array_equal(dec[448:], torch.from_numpy(v[448:]).to(torch.bfloat16).to(torch.float64).numpy())
