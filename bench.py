@@ -55,7 +55,7 @@ def _peaks():
 def algorithmic_bytes(spec):
     """Indexer-key scan + gathered top-k entries + window tokens, per step."""
     import compressed_sparse_long_c4a_gb300.inputs as I
-    row = spec.dim * 2 if spec.kv_fmt == I.KV_BF16 else spec.dim + 4
+    row = spec.dim * 2 if spec.kv_fmt == I.KV_BF16 else 584 if spec.kv_fmt == I.KV_FP8_DSV4 else spec.dim + 4
     wrow = spec.dim * 2 if spec.swa_fmt == I.KV_BF16 else spec.dim + 4
     ix_row = spec.ix_block_bytes // 64 if spec.ix_heads else 0
     scan = gather = win = 0

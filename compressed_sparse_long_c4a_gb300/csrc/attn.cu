@@ -199,7 +199,8 @@ static int validate_shape(const v4a_attn_args* a) {
   const v4a_cache& c = a->kv;
   if (c.ratio != 4 && c.ratio != 128) return V4A_ERR_INVALID_ARG;
   if (c.num_blocks <= 0 || c.max_blocks <= 0) return V4A_ERR_INVALID_ARG;
-  if (c.format != V4A_KV_BF16 && c.format != V4A_KV_FP8_TOKEN) return V4A_ERR_INVALID_ARG;
+  if (c.format != V4A_KV_BF16 && c.format != V4A_KV_FP8_TOKEN && c.format != V4A_KV_FP8_DSV4)
+    return V4A_ERR_INVALID_ARG;
   if (a->window_format != V4A_KV_BF16 && a->window_format != V4A_KV_FP8_TOKEN) return V4A_ERR_INVALID_ARG;
   if (a->window_len < 1 || a->window_cap < 1) return V4A_ERR_INVALID_ARG;
   // every query's window [m - window_len + 1, m] must be in the ring at once
@@ -256,6 +257,8 @@ int sparse_attn(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t 
   const size_t need = attn_workspace_size(a);
   if (!ws || ws_bytes < need) return V4A_ERR_WORKSPACE;
   if (attn_tc(a, ws, ws_bytes, stream, &rc)) return rc;
+  // the CUDA-core kernels read the per-row-scale formats only
+  if (a->kv.format == V4A_KV_FP8_DSV4) return V4A_ERR_UNSUPPORTED;
   const int S = splits_for(a);
   AttnDev d;
   d.T = T; d.H = a->num_heads; d.D = a->kv.dim; d.ratio = a->kv.ratio; d.fmt = a->kv.format;

@@ -108,6 +108,18 @@ __device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, float* v) {
       : "memory");
 }
 
+// 16 bytes from an address that is 8-byte aligned only, as two 8-byte loads.
+__device__ __forceinline__ uint4 ld16_8x2(const uint8_t* p) {
+  const uint2 lo = __ldg(reinterpret_cast<const uint2*>(p)), hi = __ldg(reinterpret_cast<const uint2*>(p + 8));
+  return make_uint4(lo.x, lo.y, hi.x, hi.y);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t x, uint32_t m) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(m));
+  return r;
+}
+
 // Exact e4m3 -> bf16 of the four codes in w (lowest byte first), in integer
 // and bf16 arithmetic only (the conversion instructions are the slow part of
 // staging a key tile otherwise).  A code's sign goes to bit 15 and its 7
@@ -209,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
               const uint8_t* bb = a.pool + int64_t(blk) * a.block_bytes;
               const int slot = e & (E - 1);
               f = a.fmt;
-              src = bb + int64_t(slot) * (a.fmt == V4A_KV_BF16 ? 2 * D : D);
+              src = bb + int64_t(slot) * kv_row_bytes(a.fmt, D);
               if (a.fmt == V4A_KV_FP8_TOKEN) sp = reinterpret_cast<const float*>(bb + int64_t(E) * D) + slot;
             }
           }
@@ -235,19 +247,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
   {
     constexpr int kBchunks = kKeys * (D / 8);         // 16-byte bf16 chunks of the tile
     constexpr int kPer = kKeys * (D / 16) / kThreads;  // 16-byte fp8 chunks per thread
-    uint4 raw[kPer];
+    // DeepSeek-V4 rows (D = 512): fp8 chunk slots below kNopeChunks hold 16
+    // non-rope codes (scale byte cc / 4); each slot above holds 32 bytes of
+    // the bf16 rope part (two bf16 chunks)
+    constexpr int kNopeChunks = kDsv4Nope / 16;
+    uint4 raw[kPer], raw2[kPer];
+    uint32_t sbyte[kPer];
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
       const int c = tid + i * kThreads;
       const int r = c / (D / 16), cc = c % (D / 16);
       raw[i] = make_uint4(0, 0, 0, 0);
+      raw2[i] = make_uint4(0, 0, 0, 0);
+      sbyte[i] = 127;
       if (s.kfmt[r] == V4A_KV_FP8_TOKEN) {
         const uint8_t* src = s.src[r] + cc * 16;
-        if (a.kv_align8) {
-          const uint2 lo = __ldg(reinterpret_cast<const uint2*>(src)), hi = __ldg(reinterpret_cast<const uint2*>(src + 8));
-          raw[i] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+        raw[i] = a.kv_align8 ? ld16_8x2(src) : __ldg(reinterpret_cast<const uint4*>(src));
+      } else if (s.kfmt[r] == V4A_KV_FP8_DSV4) {   // rows start on 8 bytes (584-byte stride)
+        const uint8_t* row = s.src[r];
+        if (cc < kNopeChunks) {
+          raw[i] = ld16_8x2(row + cc * 16);
+          sbyte[i] = __ldg(row + kDsv4Nope + 2 * kDsv4Rope + (cc >> 2));
         } else {
-          raw[i] = __ldg(reinterpret_cast<const uint4*>(src));
+          const uint8_t* rp = row + kDsv4Nope + 32 * (cc - kNopeChunks);
+          raw[i] = ld16_8x2(rp);
+          raw2[i] = ld16_8x2(rp + 16);
         }
       }
     }
@@ -269,11 +293,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
       const int f = s.kfmt[r];
       if (f == V4A_KV_BF16) continue;
       uint4 v0 = make_uint4(0, 0, 0, 0), v1 = make_uint4(0, 0, 0, 0);
-      if (f == V4A_KV_FP8_TOKEN) {
+      if (f == V4A_KV_FP8_TOKEN || (f == V4A_KV_FP8_DSV4 && cc < kNopeChunks)) {
         const uint2 b0 = bf16x4_from_e4m3x4(raw[i].x), b1 = bf16x4_from_e4m3x4(raw[i].y);
         const uint2 b2 = bf16x4_from_e4m3x4(raw[i].z), b3 = bf16x4_from_e4m3x4(raw[i].w);
         v0 = make_uint4(b0.x, b0.y, b1.x, b1.y);
         v1 = make_uint4(b2.x, b2.y, b3.x, b3.y);
+        if (f == V4A_KV_FP8_DSV4) {
+          // times the block's power of two, a bf16 with exponent field = the
+          // scale byte (exact while the product stays a normal bf16)
+          const uint32_t m = (sbyte[i] << 7) | (sbyte[i] << 23);
+          v0 = make_uint4(bf16x2_mul(v0.x, m), bf16x2_mul(v0.y, m), bf16x2_mul(v0.z, m), bf16x2_mul(v0.w, m));
+          v1 = make_uint4(bf16x2_mul(v1.x, m), bf16x2_mul(v1.y, m), bf16x2_mul(v1.z, m), bf16x2_mul(v1.w, m));
+        }
+      } else if (f == V4A_KV_FP8_DSV4) {   // rope: bf16 as stored
+        v0 = raw[i];
+        v1 = raw2[i];
       }
       const int c0 = 2 * cc;
       uint8_t* sub = Ks + (c0 >> 3) * (kKeys * 128);
@@ -580,6 +614,7 @@ bool handled(const v4a_attn_args* a) {
   // so the pool and the window ring must start on 16 bytes.  A window-only
   // call reads no cache entry.
   const bool reads_cache = !a->idx || a->k > 0;
+  if (a->kv.format == V4A_KV_FP8_DSV4 && D != kDsv4Nope + kDsv4Rope) return false;
   if (reads_cache && ((kv_block_bytes(a->kv.format, a->kv.ratio, D) & 7) ||
                       (reinterpret_cast<uintptr_t>(a->kv.pool) & 15)))
     return false;
@@ -655,7 +690,7 @@ bool attn_tc(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t str
   t.num_blocks = a->kv.num_blocks;
   t.pool = static_cast<const uint8_t*>(a->kv.pool);
   t.block_bytes = kv_block_bytes(a->kv.format, a->kv.ratio, a->kv.dim);
-  t.kv_align8 = (t.block_bytes & 15) != 0 ? 1 : 0;
+  t.kv_align8 = (t.block_bytes & 15) != 0 ? 1 : 0;   // (DeepSeek-V4 rows are always read as 8-byte halves)
   t.idx = a->idx ? a->idx + int64_t(t0) * a->k : nullptr;
   t.window = static_cast<const uint8_t*>(a->window);
   t.wscale = a->window_scale;

@@ -67,6 +67,33 @@ __device__ __forceinline__ bool token_ok(const BatchDev& bt, int t, int b, int P
 // All threads of the CTA must call it (it contains block reductions).
 __device__ void store_kv_row(int format, int dim, int p, bool own, float v0, float v1,
                              uint8_t* row, float* scale_slot, float* red) {
+  if (format == V4A_KV_FP8_DSV4) {
+    // the DeepSeek-V4 584-byte row (dim 512, rope dims 64): pairs below 224
+    // are the non-rope elements, 32 pairs (one warp) per 64-element scale
+    // block; the rest are the rope elements, stored in bf16
+    const int nope_pairs = kDsv4Nope / 2;
+    const bool nope = own && p < nope_pairs;
+    const float amax = warp_max(nope ? fmaxf(fabsf(v0), fabsf(v1)) : 0.f);
+    if (nope) {
+      // the smallest power of two s = 2^k with amax / s <= 448: amax = f 2^e,
+      // f in [0.5, 1), 448 = 0.875 2^9, so k = e - 9, plus 1 when f > 0.875
+      int k = 0;
+      if (amax > 0.f) {
+        int e;
+        const float f = frexpf(amax, &e);
+        k = e - 9 + (f > 0.875f ? 1 : 0);
+      }
+      const int b = min(max(k + 127, 1), 254);
+      const uint16_t c = uint16_t(f32_to_e4m3(ldexpf(v0, 127 - b))) | (uint16_t(f32_to_e4m3(ldexpf(v1, 127 - b))) << 8);
+      reinterpret_cast<uint16_t*>(row)[p] = c;
+      if ((p & 31) == 0) row[kDsv4Nope + 2 * kDsv4Rope + (p >> 5)] = uint8_t(b);
+    } else if (own) {
+      const uint32_t packed = uint32_t(f32_to_bf16(v0)) | (uint32_t(f32_to_bf16(v1)) << 16);
+      reinterpret_cast<uint32_t*>(row + kDsv4Nope)[p - nope_pairs] = packed;
+    }
+    if (p == 0) row[kDsv4Row - 1] = 0;
+    return;
+  }
   if (format == V4A_KV_BF16) {
     if (own) {
       const uint32_t packed = uint32_t(f32_to_bf16(v0)) | (uint32_t(f32_to_bf16(v1)) << 16);
@@ -326,7 +353,10 @@ static int fill_side(const v4a_compressor* c, bool indexer, CompressSide* s, int
   const int W = k.ratio == 4 ? 8 : 128;
   if (c->ring_cap < W - 1 + max_new) return V4A_ERR_RING_TOO_SMALL;
   if (!indexer) {
-    if (k.format != V4A_KV_BF16 && k.format != V4A_KV_FP8_TOKEN) return V4A_ERR_INVALID_ARG;
+    if (k.format != V4A_KV_BF16 && k.format != V4A_KV_FP8_TOKEN && k.format != V4A_KV_FP8_DSV4)
+      return V4A_ERR_INVALID_ARG;
+    if (k.format == V4A_KV_FP8_DSV4 && (k.dim != kDsv4Nope + kDsv4Rope || k.rope_dims != kDsv4Rope))
+      return V4A_ERR_UNSUPPORTED;
   } else {
     if (k.format != V4A_IX_BF16 && k.format != V4A_IX_FP8_B128 && !ix_is_fp4(k.format))
       return V4A_ERR_INVALID_ARG;

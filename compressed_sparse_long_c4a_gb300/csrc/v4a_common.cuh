@@ -109,12 +109,16 @@ __host__ __device__ __forceinline__ int entries_per_block(int ratio) {
   return kBlockPositions / ratio;
 }
 
+constexpr int kDsv4Row = 584, kDsv4Nope = 448, kDsv4Rope = 64, kDsv4Unit = 576;
+
 __host__ __device__ __forceinline__ int64_t kv_block_bytes(int fmt, int ratio, int dim) {
   const int64_t e = entries_per_block(ratio);
+  if (fmt == V4A_KV_FP8_DSV4) return (e * kDsv4Row + kDsv4Unit - 1) / kDsv4Unit * kDsv4Unit;
   return fmt == V4A_KV_BF16 ? e * dim * 2 : e * (dim + 4);
 }
 
 __host__ __device__ __forceinline__ int64_t kv_row_bytes(int fmt, int dim) {
+  if (fmt == V4A_KV_FP8_DSV4) return kDsv4Row;
   return fmt == V4A_KV_BF16 ? int64_t(dim) * 2 : int64_t(dim);
 }
 

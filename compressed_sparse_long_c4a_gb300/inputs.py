@@ -17,6 +17,8 @@ the queries.  Distributions follow the five workloads of the layer:
 * indexer head weights ~ U(0,1);
 * fp8 codes are the e4m3 cast (a library cast) of N(0,1)*100, clamped to
   +-448, with fp32 scales ~ U(0.5,1.5)/100, so decoded values are ~N(0,1);
+* DeepSeek-V4 584-byte rows: e4m3 codes as above, scale bytes uniform on
+  {119, 120, 121} (2^-8 .. 2^-6), rope values ~ N(0,1) in bf16;
 * fp4 codes are drawn from a fixed categorical law over the 8 e2m1
   magnitudes (small codes most likely) with a random sign, with fp32 scales
   ~ U(0.5,1.5)/2, or, for the power-of-two (MX) scale format, scales 2^e with
@@ -34,7 +36,7 @@ from dataclasses import dataclass, field
 import torch
 
 BLOCK_POSITIONS = 256
-KV_BF16, KV_FP8_TOKEN = 0, 1
+KV_BF16, KV_FP8_TOKEN, KV_FP8_DSV4 = 0, 1, 2
 IX_BF16, IX_FP8_B128, IX_FP4_B32, IX_FP4_MX32 = 0, 1, 2, 3
 Q_BF16, Q_FP8_HEAD = 0, 1
 OUT_BF16, OUT_FP8_TOKEN = 0, 1
@@ -95,6 +97,8 @@ class LayerSpec:
     @property
     def kv_block_bytes(self) -> int:
         e = self.entries_per_block
+        if self.kv_fmt == KV_FP8_DSV4:      # 584-byte rows, pages padded to 576-byte units
+            return -(-e * 584 // 576) * 576
         return e * self.dim * 2 if self.kv_fmt == KV_BF16 else e * self.dim + 4 * e
 
     @property
@@ -212,6 +216,15 @@ def make_case(spec: LayerSpec, seed: int = 0) -> Case:
     e = s.entries_per_block
     if s.kv_fmt == KV_BF16:
         kv = _bf16(_randn((nb, e * D), seed, 2)).view(torch.uint8).reshape(nb, -1)
+    elif s.kv_fmt == KV_FP8_DSV4:
+        # 584-byte rows: 448 e4m3 codes, 64 bf16 rope values, 7 scale bytes
+        # (2^-8 .. 2^-6: with the codes' ~N(0,1)*100 the decoded values are
+        # ~N(0,1) within a factor of two), 1 zero pad byte; zero page padding
+        codes = _fp8_codes((nb, e, 448), seed, 2)
+        rope = _bf16(_randn((nb, e, 64), seed, 3)).view(torch.uint8).reshape(nb, e, 128)
+        sb = torch.randint(119, 122, (nb, e, 7), generator=_gen(seed, 15), dtype=torch.int64).to(torch.uint8)
+        rows = torch.cat([codes, rope, sb, torch.zeros((nb, e, 1), dtype=torch.uint8)], dim=2).reshape(nb, -1)
+        kv = torch.cat([rows, torch.zeros((nb, s.kv_block_bytes - e * 584), dtype=torch.uint8)], dim=1)
     else:
         codes = _fp8_codes((nb, e * D), seed, 2)
         sc = _scales(nb * e, seed, 3, 100.0).view(torch.uint8).reshape(nb, -1)
@@ -324,6 +337,13 @@ def c4a_decode_1m() -> LayerSpec:
                      topk=2048, out_fmt=OUT_FP8_TOKEN, spare_blocks=1)
 
 
+def c4a_decode_1m_dsv4() -> LayerSpec:
+    """c4a_decode_b4_1m with the attention cache in the DeepSeek-V4 584-byte
+    fp8 layout of the SGLang KV-pool article (448 fp8 nope with a scale byte
+    per 64, 64 bf16 rope, pages padded to 576-byte units)."""
+    return dataclasses.replace(c4a_decode_1m(), name="c4a_decode_b4_1m_dsv4", kv_fmt=KV_FP8_DSV4)
+
+
 def c4a_decode_1m_mx() -> LayerSpec:
     """c4a_decode_b4_1m with the fp4 indexer's per-32 fp32 scales restricted to
     powers of two (the OCP MX rule; same bytes per entry), which the tensor
@@ -365,6 +385,7 @@ WORKLOADS = {
     "c4a_decode_b4_1m_mx": c4a_decode_1m_mx,
     "c4a_decode_b4_128k": c4a_decode_128k,
     "c128a_decode_b4_1m": c128a_decode_1m,
+    "c4a_decode_b4_1m_dsv4": c4a_decode_1m_dsv4,
 }
 
 

@@ -67,6 +67,12 @@ extern "C" {
 /* Shared-K=V cache and window ring rows. */
 #define V4A_KV_BF16       0  /* row = dim bf16 */
 #define V4A_KV_FP8_TOKEN  1  /* row = dim e4m3 codes; one fp32 scale per row (amax/448) */
+#define V4A_KV_FP8_DSV4   2  /* compressed cache only, dim 512 with 64 rope dims: the DeepSeek-V4
+                                row of the SGLang KV-pool article ("DeepSeek-V4"), 584 B =
+                                448 e4m3 codes of the non-rope dims, the 64 rope dims in bf16,
+                                7 UE8M0 scale bytes (one per 64 codes: the smallest power of
+                                two s with amax/s <= 448; value = code * 2^(byte-127)), 1 zero
+                                pad byte; the scales live inside the row */
 /* Indexer key cache rows. */
 #define V4A_IX_BF16       0  /* row = dim bf16 */
 #define V4A_IX_FP8_B128   1  /* row = dim e4m3; one fp32 scale per 128 elements (132 B at dim 128) */
@@ -105,6 +111,8 @@ typedef struct {
  * E = 256/ratio.  Inside a block all data rows come first ([E][row bytes]),
  * then the fp32 scale words ([E][scales per row]) if the format has any.
  * Block bytes:  KV_BF16 E*dim*2;  KV_FP8_TOKEN E*(dim+4);
+ *               KV_FP8_DSV4 ceil(E*584/576)*576 (rows from the block's first
+ *               byte, the page padded to 576-byte units as in the article);
  *               IX_BF16 64*dim*2;  IX_FP8_B128 64*(dim + 4*dim/128);
  *               IX_FP4_B32, IX_FP4_MX32 64*(dim/2 + 4*dim/32).
  */

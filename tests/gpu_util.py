@@ -125,12 +125,36 @@ def check_fp4_mx_blocks(packed, scales, ref, where=""):
         assert not bad.any(), (where, b, np.nonzero(bad)[0][:5])
 
 
+def check_dsv4_row(row: np.ndarray, ref: np.ndarray, where=""):
+    """DeepSeek-V4 584-byte row: every nope block's scale byte equal to the
+    oracle's rule on the fp64 values (or a neighbour when the block's amax
+    lies within fp32 rounding of a scale boundary), codes within 1 e4m3 ulp of
+    value / scale, rope elements within 1 bf16 ulp, pad byte 0."""
+    assert row.shape == (F.DSV4_ROW,) and row[-1] == 0, where
+    for j in range(F.DSV4_NOPE // F.DSV4_QBLOCK):
+        seg = ref[64 * j:64 * (j + 1)]
+        b = int(row[F.DSV4_NOPE + 2 * F.DSV4_ROPE + j])
+        want = F.ue8m0_e4m3_scale_byte(seg)
+        amax = float(np.max(np.abs(seg)))
+        edge = amax > 0 and any(abs(amax / (448.0 * 2.0 ** (w - 127)) - 1.0) < 1e-6 for w in (want, want - 1))
+        assert b == want or (edge and abs(b - want) == 1), (where, j, b, want)
+        s = 2.0 ** (b - 127)
+        got = F.e4m3_decode(row[64 * j:64 * (j + 1)]) * s
+        ulp = F.e4m3_ulp(np.clip(seg / s, -448, 448)) * s
+        bad = np.abs(got - np.clip(seg, -448 * s, 448 * s)) > ulp * 1.0000001 + 1e-30
+        assert not bad.any(), (where, j, np.nonzero(bad)[0][:5])
+    check_bf16_row(row[F.DSV4_NOPE:F.DSV4_NOPE + 2 * F.DSV4_ROPE].copy().view(np.uint16), ref[F.DSV4_NOPE:],
+                   f"{where}/rope")
+
+
 def kv_slot_bytes(pool: np.ndarray, spec, blk: int, slot: int):
     """(row bytes, scale or None) of one shared-KV entry."""
     E, D = spec.entries_per_block, spec.dim
     base = blk * spec.kv_block_bytes
     if spec.kv_fmt == F.KV_BF16:
         return pool[base + slot * 2 * D: base + (slot + 1) * 2 * D].copy().view(np.uint16), None
+    if spec.kv_fmt == F.KV_FP8_DSV4:
+        return pool[base + slot * F.DSV4_ROW: base + (slot + 1) * F.DSV4_ROW].copy(), None
     row = pool[base + slot * D: base + (slot + 1) * D].copy()
     sc = pool[base + E * D + 4 * slot: base + E * D + 4 * slot + 4].copy().view(np.float32)[0]
     return row, float(sc)

@@ -38,7 +38,9 @@ def _small_workloads():
                              cached=(4 * 10000 + 3, 39001))
     s5mx = dataclasses.replace(I.c4a_decode_1m_mx(), name="c4a_decode_small_mx4ix_fp8kv", batch=3,
                                cached=(4 * 10000 + 3, 39001, 256 * 90 + 255))
-    return [I.c4a_decode_1k(), s2, s3, s4, s5, s5mx]
+    s5d = dataclasses.replace(I.c4a_decode_1m(), name="c4a_decode_small_fp4ix_dsv4kv", batch=3,
+                              kv_fmt=I.KV_FP8_DSV4, cached=(4 * 10000 + 3, 39001, 256 * 90 + 255))
+    return [I.c4a_decode_1k(), s2, s3, s4, s5, s5mx, s5d]
 
 
 SMALL = {s.name: s for s in _small_workloads()}
@@ -113,6 +115,10 @@ def test_compress_insert(name):
             U.check_bf16_row(row, ref, f"main {b},{i}")
             base = blk * s.kv_block_bytes + slot * 2 * s.dim
             touched[base:base + 2 * s.dim] = True
+        elif s.kv_fmt == F.KV_FP8_DSV4:
+            U.check_dsv4_row(row, ref, f"main {b},{i}")
+            base = blk * s.kv_block_bytes + slot * F.DSV4_ROW
+            touched[base:base + F.DSV4_ROW] = True
         else:
             U.check_fp8_row(row, sc, ref, f"main {b},{i}")
             base = blk * s.kv_block_bytes
@@ -316,7 +322,7 @@ def test_end_to_end(name):
 FUSED_EXPECTED = {"c4a_decode_b4_1m", "c4a_decode_b4_1m_mx", "c4a_decode_b4_128k", "c128a_decode_b4_1m",
                   "c4a_decode_b32_32k_64k",
                   "c128a_decode_b64_64k_128k", "c4a_decode_small_fp8ix", "c4a_decode_small_fp4ix_fp8kv",
-                  "c4a_decode_small_mx4ix_fp8kv"}
+                  "c4a_decode_small_mx4ix_fp8kv", "c4a_decode_small_fp4ix_dsv4kv", "c4a_decode_b4_1m_dsv4"}
 
 
 @pytest.mark.parametrize("name", [_marks(n) for n in ALL])
