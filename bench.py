@@ -353,12 +353,18 @@ def measure_workload(spec, args, dev, barrier, windows: int):
 
 def measure_stack(args, dev, c4a_case, barrier, windows: int, reps: int = 3):
     """The model's whole attention stack (30 c4a + 31 c128a layers at the
-    same batch and context) as one CUDA graph: windows of `reps` replays."""
+    same batch and context) as one CUDA graph: windows of `reps` replays.
+    Every layer's caches and rings are pages of the page allocator's three
+    bucket pools."""
     import torch
     from compressed_sparse_long_c4a_gb300 import stack as S
     ws, _, _ = _dist()
     kinds = S.deepseek_v4_mix()
-    st = S.AttentionStack(kinds, S.decode_1m_cases(0, c4a_case), dev)
+    st = S.AttentionStack(kinds, S.decode_1m_cases(0, c4a_case), dev, paged=True)
+    buckets = []
+    for i, bk in enumerate(st.alloc.buckets()):
+        names = sorted(n for n, k in st.slot.items() if st.alloc.info(k).bucket == i)
+        buckets.append({"page_bytes": bk.page_bytes, "pages": bk.num_pages, "kinds": names})
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         st.run(stream)
@@ -387,7 +393,8 @@ def measure_stack(args, dev, c4a_case, barrier, windows: int, reps: int = 3):
                      f"{st.tokens} at 1M context; one CUDA graph per step",
            "ms_per_step": ms, "value": whole_job_rate(ws, st.tokens, ms),
            "unit": "tokens/s through all attention layers", "us_per_layer_mean": ms * 1e3 / len(kinds),
-           "windows": stats, "gpu_launches_per_step": st.launches_per_step()}
+           "windows": stats, "gpu_launches_per_step": st.launches_per_step(),
+           "page_buckets": buckets}
     del g, st
     return out
 

@@ -1,6 +1,7 @@
 """Builds libv4a.so in-tree with nvcc for sm_103a (GB300).
 
-Each .cu file is compiled to an object in parallel, then linked into
+Each .cu file (kernels) and .cpp file (host code) is compiled to an object
+in parallel, then linked into
 ``compressed_sparse_long_c4a_gb300/libv4a.so``.  Objects go to
 ``compressed_sparse_long_c4a_gb300/_build/`` (git-ignored).  Rebuilds only
 what changed (source or header newer than the object).
@@ -35,12 +36,12 @@ def _nvcc() -> str:
 
 def _deps_mtime() -> float:
     hs = glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) + \
-        [os.path.join(INCLUDE, "v4a.h")]
+        glob.glob(os.path.join(INCLUDE, "*.h"))
     return max(os.path.getmtime(h) for h in hs)
 
 
 def _compile(src: str, extra: list[str]) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+    obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
     if os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(src), _deps_mtime()):
         return obj
     cmd = [_nvcc(), *ARCH, *FLAGS, *extra, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
@@ -52,7 +53,7 @@ def _compile(src: str, extra: list[str]) -> str:
 
 def build(verbose: bool = False, extra: list[str] | None = None) -> str:
     os.makedirs(BUILD, exist_ok=True)
-    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(lambda s: _compile(s, extra or []), srcs))
     if not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):

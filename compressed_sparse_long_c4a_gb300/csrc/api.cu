@@ -54,6 +54,7 @@ const char* v4a_status_string(int code) {
     case V4A_ERR_INVALID_ARG: return "invalid argument";
     case V4A_ERR_UNSUPPORTED: return "unsupported shape or format";
     case V4A_ERR_RING_TOO_SMALL: return "ring capacity below window - 1 + tokens per sequence";
+    case V4A_ERR_OUT_OF_PAGES: return "a page-size bucket has too few free pages";
     case V4A_ERR_WORKSPACE: return "workspace missing or too small";
     case V4A_ERR_CUDA: return "CUDA launch failed";
     default: return "unknown status";

@@ -26,14 +26,13 @@ namespace v4a {
 constexpr int kChunk = 128;
 
 struct AttnDev {
-  int T, H, D, ratio, fmt, wfmt, wlen, wcap, k, splits;
+  int T, H, D, ratio, fmt, wfmt, wlen, k, splits;
   const int32_t* seq_ids;
   const int32_t* positions;
   v4a_cache kv;
   int64_t block_bytes;
   const int32_t* idx;
-  const uint8_t* window;
-  const float* wscale;
+  RingDev wring;
   const uint16_t* q;
   float scale;
   float* part_o;     // [T][splits][H][D]
@@ -104,10 +103,14 @@ __global__ void __launch_bounds__(512) attn_split_simt(AttnDev a) {
         }
       } else {
         const int p = wstart + (li - nsel);
-        const int64_t slot = int64_t(b) * a.wcap + p % a.wcap;
-        f = a.wfmt;
-        src = a.window + slot * (a.wfmt == V4A_KV_BF16 ? 2 * D : D);
-        if (a.wfmt == V4A_KV_FP8_TOKEN) s = a.wscale[slot];
+        uint8_t* wrow;
+        float* wsc;
+        ring_slot(a.wring, b, p % a.wring.cap, &wrow, &wsc, (lane == 0 && blockIdx.z == 0) ? a.status : nullptr);
+        if (wrow) {
+          f = a.wfmt;
+          src = wrow;
+          if (wsc) s = *wsc;
+        }
       }
       if (src) {
         const int nb = f == V4A_KV_BF16 ? 2 * D : D;
@@ -217,11 +220,11 @@ static int validate(const v4a_attn_args* a, bool need_out = true) {
   const int rc = validate_shape(a);
   if (rc) return rc;
   if (a->batch.num_tokens == 0) return V4A_OK;
-  if (!a->batch.seq_ids || !a->batch.positions || !a->q || (need_out && !a->out) || !a->window ||
-      !a->kv.pool || !a->kv.block_table)
+  if (!a->batch.seq_ids || !a->batch.positions || !a->q || (need_out && !a->out) || !a->kv.pool ||
+      !a->kv.block_table)
     return V4A_ERR_INVALID_ARG;
-  if (a->window_format == V4A_KV_FP8_TOKEN && !a->window_scale) return V4A_ERR_INVALID_ARG;
-  return V4A_OK;
+  RingDev wr;
+  return attn_window_ring(a, &wr);
 }
 
 // Splits of the key list per query: enough CTAs to cover the GPU twice,
@@ -262,11 +265,12 @@ int sparse_attn(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t 
   const int S = splits_for(a);
   AttnDev d;
   d.T = T; d.H = a->num_heads; d.D = a->kv.dim; d.ratio = a->kv.ratio; d.fmt = a->kv.format;
-  d.wfmt = a->window_format; d.wlen = a->window_len; d.wcap = a->window_cap; d.k = a->k;
+  d.wfmt = a->window_format; d.wlen = a->window_len; d.k = a->k;
+  attn_window_ring(a, &d.wring);     // validated above
   d.splits = S;
   d.seq_ids = a->batch.seq_ids; d.positions = a->batch.positions; d.kv = a->kv;
   d.block_bytes = kv_block_bytes(a->kv.format, a->kv.ratio, a->kv.dim);
-  d.idx = a->idx; d.window = static_cast<const uint8_t*>(a->window); d.wscale = a->window_scale;
+  d.idx = a->idx;
   d.q = a->q; d.scale = a->softmax_scale;
   d.part_o = static_cast<float*>(ws);
   d.part_ml = d.part_o + size_t(T) * S * a->num_heads * a->kv.dim;

@@ -43,7 +43,7 @@ constexpr int kThreads = 256;        // warps 0-3 own TMEM lane quarters for the
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct AtcArgs {
-  int T, H, D, ratio, fmt, wfmt, wlen, wcap, k, splits;
+  int T, H, D, ratio, fmt, wfmt, wlen, k, splits;
   const int32_t* seq_ids;
   const int32_t* positions;
   const int32_t* bt;
@@ -52,8 +52,7 @@ struct AtcArgs {
   const uint8_t* pool;
   int64_t block_bytes;
   const int32_t* idx;
-  const uint8_t* window;
-  const float* wscale;
+  RingDev wring;      // the window ring (dense or paged)
   const uint16_t* q;
   float scale;
   uint16_t* out;
@@ -145,7 +144,10 @@ __device__ __forceinline__ uint32_t sw_off(int r, int ch) { return uint32_t(r * 
 // kD: the head dimension as a compile-time constant, so that the index
 // arithmetic of the staging and drain loops is shifts and masks (these
 // phases run on a few warps per SM and are bound by instruction latency).
-template <int kD>
+// kDsv4: the cache holds DeepSeek-V4 584-byte rows (kD = 512); a separate
+// instance, so that the other formats' staging keeps all its loads in
+// flight without the extra registers that layout needs.
+template <int kD, bool kDsv4 = false>
 __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
                                                              const __grid_constant__ CUtensorMap qmap,
                                                              const __grid_constant__ CUtensorMap omap) {
@@ -228,10 +230,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
         }
       } else {
         const int p = wstart + (li - nsel);
-        const int64_t slot = int64_t(b) * a.wcap + p % a.wcap;
-        f = a.wfmt;
-        src = a.window + slot * (a.wfmt == V4A_KV_BF16 ? 2 * D : D);
-        if (a.wfmt == V4A_KV_FP8_TOKEN) sp = a.wscale + slot;
+        uint8_t* wrow;
+        float* wsc;
+        ring_slot(a.wring, b, p % a.wring.cap, &wrow, &wsc, a.status);
+        if (wrow) {
+          f = a.wfmt;
+          src = wrow;
+          sp = wsc;
+        }
       }
     }
     s.src[tid] = src;
@@ -251,27 +257,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
     // non-rope codes (scale byte cc / 4); each slot above holds 32 bytes of
     // the bf16 rope part (two bf16 chunks)
     constexpr int kNopeChunks = kDsv4Nope / 16;
-    uint4 raw[kPer], raw2[kPer];
-    uint32_t sbyte[kPer];
+    uint4 raw[kPer];
+    uint4 raw2[kDsv4 ? kPer : 1];
+    uint32_t sbyte[kDsv4 ? kPer : 1];
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
       const int c = tid + i * kThreads;
       const int r = c / (D / 16), cc = c % (D / 16);
       raw[i] = make_uint4(0, 0, 0, 0);
-      raw2[i] = make_uint4(0, 0, 0, 0);
-      sbyte[i] = 127;
       if (s.kfmt[r] == V4A_KV_FP8_TOKEN) {
         const uint8_t* src = s.src[r] + cc * 16;
         raw[i] = a.kv_align8 ? ld16_8x2(src) : __ldg(reinterpret_cast<const uint4*>(src));
-      } else if (s.kfmt[r] == V4A_KV_FP8_DSV4) {   // rows start on 8 bytes (584-byte stride)
-        const uint8_t* row = s.src[r];
-        if (cc < kNopeChunks) {
-          raw[i] = ld16_8x2(row + cc * 16);
-          sbyte[i] = __ldg(row + kDsv4Nope + 2 * kDsv4Rope + (cc >> 2));
-        } else {
-          const uint8_t* rp = row + kDsv4Nope + 32 * (cc - kNopeChunks);
-          raw[i] = ld16_8x2(rp);
-          raw2[i] = ld16_8x2(rp + 16);
+      }
+      if constexpr (kDsv4) {
+        raw2[i] = make_uint4(0, 0, 0, 0);
+        sbyte[i] = 127;
+        if (s.kfmt[r] == V4A_KV_FP8_DSV4) {   // rows start on 8 bytes (584-byte stride)
+          const uint8_t* row = s.src[r];
+          if (cc < kNopeChunks) {
+            raw[i] = ld16_8x2(row + cc * 16);
+            sbyte[i] = __ldg(row + kDsv4Nope + 2 * kDsv4Rope + (cc >> 2));
+          } else {
+            const uint8_t* rp = row + kDsv4Nope + 32 * (cc - kNopeChunks);
+            raw[i] = ld16_8x2(rp);
+            raw2[i] = ld16_8x2(rp + 16);
+          }
         }
       }
     }
@@ -293,21 +303,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
       const int f = s.kfmt[r];
       if (f == V4A_KV_BF16) continue;
       uint4 v0 = make_uint4(0, 0, 0, 0), v1 = make_uint4(0, 0, 0, 0);
-      if (f == V4A_KV_FP8_TOKEN || (f == V4A_KV_FP8_DSV4 && cc < kNopeChunks)) {
+      bool codes = f == V4A_KV_FP8_TOKEN;
+      if constexpr (kDsv4) codes = codes || (f == V4A_KV_FP8_DSV4 && cc < kNopeChunks);
+      if (codes) {
         const uint2 b0 = bf16x4_from_e4m3x4(raw[i].x), b1 = bf16x4_from_e4m3x4(raw[i].y);
         const uint2 b2 = bf16x4_from_e4m3x4(raw[i].z), b3 = bf16x4_from_e4m3x4(raw[i].w);
         v0 = make_uint4(b0.x, b0.y, b1.x, b1.y);
         v1 = make_uint4(b2.x, b2.y, b3.x, b3.y);
-        if (f == V4A_KV_FP8_DSV4) {
-          // times the block's power of two, a bf16 with exponent field = the
-          // scale byte (exact while the product stays a normal bf16)
-          const uint32_t m = (sbyte[i] << 7) | (sbyte[i] << 23);
-          v0 = make_uint4(bf16x2_mul(v0.x, m), bf16x2_mul(v0.y, m), bf16x2_mul(v0.z, m), bf16x2_mul(v0.w, m));
-          v1 = make_uint4(bf16x2_mul(v1.x, m), bf16x2_mul(v1.y, m), bf16x2_mul(v1.z, m), bf16x2_mul(v1.w, m));
+        if constexpr (kDsv4) {
+          if (f == V4A_KV_FP8_DSV4) {
+            // times the block's power of two, a bf16 with exponent field = the
+            // scale byte (exact while the product stays a normal bf16)
+            const uint32_t m = (sbyte[i] << 7) | (sbyte[i] << 23);
+            v0 = make_uint4(bf16x2_mul(v0.x, m), bf16x2_mul(v0.y, m), bf16x2_mul(v0.z, m), bf16x2_mul(v0.w, m));
+            v1 = make_uint4(bf16x2_mul(v1.x, m), bf16x2_mul(v1.y, m), bf16x2_mul(v1.z, m), bf16x2_mul(v1.w, m));
+          }
         }
-      } else if (f == V4A_KV_FP8_DSV4) {   // rope: bf16 as stored
-        v0 = raw[i];
-        v1 = raw2[i];
+      } else {
+        if constexpr (kDsv4) {
+          if (f == V4A_KV_FP8_DSV4) {   // rope: bf16 as stored
+            v0 = raw[i];
+            v1 = raw2[i];
+          }
+        }
       }
       const int c0 = 2 * cc;
       uint8_t* sub = Ks + (c0 >> 3) * (kKeys * 128);
@@ -618,7 +636,8 @@ bool handled(const v4a_attn_args* a) {
   if (reads_cache && ((kv_block_bytes(a->kv.format, a->kv.ratio, D) & 7) ||
                       (reinterpret_cast<uintptr_t>(a->kv.pool) & 15)))
     return false;
-  if (reinterpret_cast<uintptr_t>(a->window) & 15) return false;
+  // a paged window ring is 16-byte aligned by its descriptor's rules
+  if (!a->window_pages && (reinterpret_cast<uintptr_t>(a->window) & 15)) return false;
   return true;
 }
 
@@ -680,7 +699,6 @@ bool attn_tc(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t str
   t.fmt = a->kv.format;
   t.wfmt = a->window_format;
   t.wlen = a->window_len;
-  t.wcap = a->window_cap;
   t.k = a->k;
   t.splits = splits_of(a);
   t.seq_ids = a->batch.seq_ids + t0;
@@ -692,8 +710,7 @@ bool attn_tc(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t str
   t.block_bytes = kv_block_bytes(a->kv.format, a->kv.ratio, a->kv.dim);
   t.kv_align8 = (t.block_bytes & 15) != 0 ? 1 : 0;   // (DeepSeek-V4 rows are always read as 8-byte halves)
   t.idx = a->idx ? a->idx + int64_t(t0) * a->k : nullptr;
-  t.window = static_cast<const uint8_t*>(a->window);
-  t.wscale = a->window_scale;
+  if (attn_window_ring(a, &t.wring)) { *rc = V4A_ERR_INVALID_ARG; return true; }
   t.q = a->q + qrow * a->kv.dim;
   t.scale = a->softmax_scale;
   t.out = a->out ? a->out + qrow * a->kv.dim : nullptr;
@@ -727,12 +744,16 @@ bool attn_tc(const v4a_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t str
   static std::once_flag once;
   std::call_once(once, [] {
     cudaFuncSetAttribute(attn_chunk_tc<512>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaFuncSetAttribute(attn_chunk_tc<512, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     cudaFuncSetAttribute(attn_chunk_tc<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     cudaFuncSetAttribute(attn_chunk_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   });
   if (smem > 227 * 1024) { *rc = V4A_ERR_UNSUPPORTED; return true; }
   // both may start while the kernel before them runs (they wait in-kernel)
-  auto kern = D == 512 ? attn_chunk_tc<512> : D == 256 ? attn_chunk_tc<256> : attn_chunk_tc<128>;
+  auto kern = t.fmt == V4A_KV_FP8_DSV4 ? attn_chunk_tc<512, true>
+             : D == 512                 ? attn_chunk_tc<512>
+             : D == 256                 ? attn_chunk_tc<256>
+                                        : attn_chunk_tc<128>;
   cudaError_t e = launch_pdl(kern, dim3(t.splits, t.T), dim3(kThreads), smem, stream, t, qmap, omap);
   if (e == cudaSuccess && !t.direct && !keep)
     e = launch_pdl(attn_combine_bf16, dim3(t.H, t.T), dim3(256), 0, stream, t.H, t.D, t.splits,

@@ -35,9 +35,7 @@ struct CompressSide {
   const float* gate;
   const float* bias;
   const float* gamma;
-  uint16_t* ring_x;
-  float* ring_gate;
-  int ring_cap;
+  RingDev ring;      // rows: bf16 x [dim]; side: gate
 };
 
 struct WindowSide {
@@ -45,9 +43,7 @@ struct WindowSide {
   int active, dim, rope_dims, format;
   float theta;
   const uint16_t* k;
-  uint8_t* ring;
-  float* ring_scale;
-  int ring_cap;
+  RingDev ring;      // rows: the encoded key; side: the fp8 scale
 };
 
 struct BatchDev {
@@ -197,15 +193,18 @@ __device__ void compress_token(const CompressSide& c, const BatchDev& bt, int t,
     const uint16_t* row = nullptr;
     if (pos >= 0) {
       const int d = P - pos;                 // 0 .. W-1
-      const int64_t rs = int64_t(b) * c.ring_cap + pos % c.ring_cap;
+      uint8_t* rrow;
+      float* rgate;
+      ring_slot(c.ring, b, pos % c.ring.cap, &rrow, &rgate, status);
       const bool in_call_ok = t - d >= 0;
       const int sid = in_call_ok ? bt.seq_ids[t - d] : -1;
       const float g_call = in_call_ok ? c.gate[t - d] : 0.f;
-      const float g_ring = c.ring_gate[rs];
+      const float g_ring = rgate ? *rgate : 0.f;
       const float bias = c.bias[j];
       const bool in_call = in_call_ok && sid == b;
-      row = in_call ? c.x + int64_t(t - d) * c.dim : c.ring_x + rs * c.dim;
-      logit = (in_call ? g_call : g_ring) + bias;
+      // a ring slot whose page is missing drops out of the window (reported)
+      row = in_call ? c.x + int64_t(t - d) * c.dim : reinterpret_cast<const uint16_t*>(rrow);
+      if (row) logit = (in_call ? g_call : g_ring) + bias;
     }
     src_s[j] = row;
   }
@@ -213,10 +212,15 @@ __device__ void compress_token(const CompressSide& c, const BatchDev& bt, int t,
 
   // this token's raw (x, gate) into the ring (no window position read below is
   // this slot: ring capacity >= window - 1 + tokens per sequence)
-  const int slot_r = P % c.ring_cap;
-  uint32_t* rx = reinterpret_cast<uint32_t*>(c.ring_x + (int64_t(b) * c.ring_cap + slot_r) * c.dim);
-  if (own) rx[p] = xv;
-  if (p == 0) c.ring_gate[int64_t(b) * c.ring_cap + slot_r] = gt;
+  {
+    uint8_t* rrow;
+    float* rgate;
+    ring_slot(c.ring, b, P % c.ring.cap, &rrow, &rgate, p == 0 ? status : nullptr);
+    if (rrow) {
+      if (own) reinterpret_cast<uint32_t*>(rrow)[p] = xv;
+      if (p == 0) *rgate = gt;
+    }
+  }
   if (!emit) return;
 
   // ---- window weights: softmax over the valid positions ----
@@ -293,7 +297,7 @@ __device__ void compress_token(const CompressSide& c, const BatchDev& bt, int t,
   }
 }
 
-__device__ void window_token(const WindowSide& w, int t, int b, int P) {
+__device__ void window_token(const WindowSide& w, int t, int b, int P, int32_t* status) {
   __shared__ float red[32];
   const int p = threadIdx.x;
   const bool own = p < (w.dim >> 1);
@@ -311,10 +315,11 @@ __device__ void window_token(const WindowSide& w, int t, int b, int P) {
       v1 = x0 * sn + x1 * cs;
     }
   }
-  const int64_t slot = int64_t(b) * w.ring_cap + P % w.ring_cap;
-  uint8_t* row = w.ring + slot * kv_row_bytes(w.format, w.dim);
-  store_kv_row(w.format, w.dim, p, own, v0, v1, row,
-               w.format == V4A_KV_FP8_TOKEN ? w.ring_scale + slot : nullptr, red);
+  uint8_t* row;
+  float* scale;
+  ring_slot(w.ring, b, P % w.ring.cap, &row, &scale, p == 0 ? status : nullptr);
+  if (!row) return;                          // uniform over the CTA
+  store_kv_row(w.format, w.dim, p, own, v0, v1, row, scale, red);
 }
 
 __global__ void compress_insert_kernel(BatchDev bt, CompressSide mainc, CompressSide ixc,
@@ -335,16 +340,14 @@ __global__ void compress_insert_kernel(BatchDev bt, CompressSide mainc, Compress
   if (!ok && threadIdx.x == 0 && role == 0) report(status, V4A_DEV_BAD_BATCH);
   if (role == 0 && mainc.active) compress_token(mainc, bt, t, b, P, ok, status);
   if (role == 1 && ixc.active) compress_token(ixc, bt, t, b, P, ok, status);
-  if (role == 2 && win.active && ok) window_token(win, t, b, P);
+  if (role == 2 && win.active && ok) window_token(win, t, b, P, status);
 }
 
 static int fill_side(const v4a_compressor* c, bool indexer, CompressSide* s, int max_new) {
   *s = CompressSide{};
   if (!c) return V4A_OK;
   const v4a_cache& k = c->cache;
-  if (!k.pool || !k.block_table || !c->x || !c->gate || !c->bias || !c->gamma || !c->ring_x ||
-      !c->ring_gate)
-    return V4A_ERR_INVALID_ARG;
+  if (!k.pool || !k.block_table || !c->x || !c->gate || !c->bias || !c->gamma) return V4A_ERR_INVALID_ARG;
   if (k.ratio != 4 && k.ratio != 128) return V4A_ERR_INVALID_ARG;
   if (indexer && k.ratio != 4) return V4A_ERR_UNSUPPORTED;
   if (k.dim <= 0 || k.dim % 64 || k.dim > 1024) return V4A_ERR_UNSUPPORTED;
@@ -373,8 +376,7 @@ static int fill_side(const v4a_compressor* c, bool indexer, CompressSide* s, int
   s->block_bytes = indexer ? ix_block_bytes(k.format, k.dim) : kv_block_bytes(k.format, k.ratio, k.dim);
   s->bt = k.block_table; s->max_blocks = k.max_blocks;
   s->x = c->x; s->gate = c->gate; s->bias = c->bias; s->gamma = c->gamma;
-  s->ring_x = c->ring_x; s->ring_gate = c->ring_gate; s->ring_cap = c->ring_cap;
-  return V4A_OK;
+  return ring_dev_fill(&s->ring, c->ring_x, c->ring_gate, c->ring_cap, 2 * k.dim, true, c->ring_pages);
 }
 
 int compress_insert(const v4a_compress_args* a, cudaStream_t stream) {
@@ -390,11 +392,10 @@ int compress_insert(const v4a_compress_args* a, cudaStream_t stream) {
   WindowSide ws{};
   if (a->window) {
     const v4a_window& w = *a->window;
-    if (!w.k || !w.ring || w.ring_cap <= 0) return V4A_ERR_INVALID_ARG;
+    if (!w.k || w.ring_cap <= 0) return V4A_ERR_INVALID_ARG;
     if (w.dim <= 0 || w.dim % 64 || w.dim > 1024) return V4A_ERR_UNSUPPORTED;
     if (w.rope_dims < 0 || w.rope_dims > w.dim || w.rope_dims % 2) return V4A_ERR_INVALID_ARG;
     if (w.format != V4A_KV_BF16 && w.format != V4A_KV_FP8_TOKEN) return V4A_ERR_INVALID_ARG;
-    if (w.format == V4A_KV_FP8_TOKEN && !w.ring_scale) return V4A_ERR_INVALID_ARG;
     if (w.window_len < 1) return V4A_ERR_INVALID_ARG;
     // a query's window [P - window_len + 1, P] must still be in the ring after
     // the call has written its max_new_per_seq positions
@@ -402,8 +403,10 @@ int compress_insert(const v4a_compress_args* a, cudaStream_t stream) {
     if (w.rope_dims > 128) return V4A_ERR_UNSUPPORTED;
     ws.rope = make_rope_freq(w.rope_dims, w.rope_theta);
     ws.active = 1; ws.dim = w.dim; ws.rope_dims = w.rope_dims; ws.format = w.format;
-    ws.theta = w.rope_theta; ws.k = w.k; ws.ring = static_cast<uint8_t*>(w.ring);
-    ws.ring_scale = w.ring_scale; ws.ring_cap = w.ring_cap;
+    ws.theta = w.rope_theta; ws.k = w.k;
+    rc = ring_dev_fill(&ws.ring, w.ring, w.ring_scale, w.ring_cap, int(kv_row_bytes(w.format, w.dim)),
+                       w.format == V4A_KV_FP8_TOKEN, w.ring_pages);
+    if (rc) return rc;
   }
   if (B.num_tokens == 0 || (!mc.active && !ic.active && !ws.active)) return V4A_OK;
   int maxdim = 64;

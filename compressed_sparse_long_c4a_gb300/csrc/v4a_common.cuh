@@ -181,6 +181,74 @@ __device__ __forceinline__ float block_reduce(float v, float* red) {
   return r;
 }
 
+// A ring (compressor state or sliding-window keys) as the kernels address it:
+// a per-sequence buffer ([B][cap][row] plus an optional [B][cap] fp32 side
+// array), or slots in pages of a shared pool (table != nullptr; the page
+// holds [slots][row] then [slots] fp32).
+struct RingDev {
+  uint8_t* rows;          // dense rows, or the page pool
+  float* side;            // dense side array (nullptr: none); unused when paged
+  const int32_t* table;   // [B][cap / slots] page ids, or nullptr
+  int64_t num_pages, page_bytes;
+  int cap, slots, row_bytes, has_side;
+};
+
+// Addresses of slot s (0 <= s < cap) of sequence b.  A page id out of range
+// reports V4A_DEV_BAD_BLOCK and gives null addresses.
+__device__ __forceinline__ void ring_slot(const RingDev& r, int b, int s, uint8_t** row, float** side,
+                                          int32_t* status) {
+  if (!r.table) {
+    const int64_t i = int64_t(b) * r.cap + s;
+    *row = r.rows + i * r.row_bytes;
+    *side = r.has_side ? r.side + i : nullptr;
+    return;
+  }
+  const int q = s / r.slots, j = s - q * r.slots;
+  const int32_t pg = r.table[int64_t(b) * (r.cap / r.slots) + q];
+  if (pg < 0 || pg >= r.num_pages) {
+    report(status, V4A_DEV_BAD_BLOCK);
+    *row = nullptr;
+    *side = nullptr;
+    return;
+  }
+  uint8_t* base = r.rows + int64_t(pg) * r.page_bytes;
+  *row = base + int64_t(j) * r.row_bytes;
+  *side = r.has_side ? reinterpret_cast<float*>(base + int64_t(r.slots) * r.row_bytes) + j : nullptr;
+}
+
+// Fills a RingDev from a dense buffer pair or a v4a_ring_pages descriptor;
+// V4A_OK or V4A_ERR_INVALID_ARG.
+inline int ring_dev_fill(RingDev* r, void* rows, float* side, int cap, int row_bytes, bool has_side,
+                         const v4a_ring_pages* pg) {
+  *r = RingDev{};
+  r->cap = cap;
+  r->row_bytes = row_bytes;
+  r->has_side = has_side ? 1 : 0;
+  if (cap <= 0) return V4A_ERR_INVALID_ARG;
+  if (!pg) {
+    if (!rows || (has_side && !side)) return V4A_ERR_INVALID_ARG;
+    r->rows = static_cast<uint8_t*>(rows);
+    r->side = side;
+    return V4A_OK;
+  }
+  if (!pg->pool || !pg->table || pg->num_pages <= 0 || pg->slots <= 0 || cap % pg->slots) return V4A_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(pg->pool) & 15) || (pg->page_bytes & 15)) return V4A_ERR_INVALID_ARG;
+  if (pg->page_bytes < int64_t(pg->slots) * (row_bytes + (has_side ? 4 : 0))) return V4A_ERR_INVALID_ARG;
+  r->rows = static_cast<uint8_t*>(pg->pool);
+  r->table = pg->table;
+  r->num_pages = pg->num_pages;
+  r->page_bytes = pg->page_bytes;
+  r->slots = pg->slots;
+  return V4A_OK;
+}
+
+// The window ring of an attention call (dense or paged).
+inline int attn_window_ring(const v4a_attn_args* a, RingDev* r) {
+  return ring_dev_fill(r, const_cast<void*>(a->window), const_cast<float*>(a->window_scale), a->window_cap,
+                       int(kv_row_bytes(a->window_format, a->kv.dim)), a->window_format == V4A_KV_FP8_TOKEN,
+                       a->window_pages);
+}
+
 // Order-preserving map of a float to uint32 (larger float -> larger key).
 __device__ __forceinline__ uint32_t float_key(float f) {
   uint32_t u = __float_as_uint(f);

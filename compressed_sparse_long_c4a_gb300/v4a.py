@@ -17,7 +17,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libv4a.so")
 
 V4A_OK = 0
-ERRORS = {1: "invalid argument", 2: "unsupported", 3: "ring too small", 4: "workspace", 5: "cuda"}
+ERRORS = {1: "invalid argument", 2: "unsupported", 3: "ring too small", 4: "workspace", 5: "cuda",
+          6: "out of pages"}
 DEV_BAD_BLOCK, DEV_BAD_BATCH, DEV_BAD_INDEX = 1, 2, 4
 KV_BF16, KV_FP8_TOKEN = 0, 1
 IX_BF16, IX_FP8_B128, IX_FP4_B32, IX_FP4_MX32 = 0, 1, 2, 3
@@ -38,15 +39,21 @@ class Cache(C.Structure):
                 ("num_blocks", C.c_int64), ("block_table", _p), ("max_blocks", C.c_int32)]
 
 
+class RingPages(C.Structure):
+    _fields_ = [("pool", _p), ("num_pages", C.c_int64), ("page_bytes", C.c_int64), ("table", _p),
+                ("slots", C.c_int32)]
+
+
 class Compressor(C.Structure):
     _fields_ = [("cache", Cache), ("x", _p), ("gate", _p), ("bias", _p), ("gamma", _p),
-                ("eps", C.c_float), ("ring_x", _p), ("ring_gate", _p), ("ring_cap", C.c_int32)]
+                ("eps", C.c_float), ("ring_x", _p), ("ring_gate", _p), ("ring_cap", C.c_int32),
+                ("ring_pages", C.POINTER(RingPages))]
 
 
 class Window(C.Structure):
     _fields_ = [("k", _p), ("dim", C.c_int32), ("rope_dims", C.c_int32), ("rope_theta", C.c_float),
                 ("format", C.c_int32), ("ring", _p), ("ring_scale", _p), ("ring_cap", C.c_int32),
-                ("window_len", C.c_int32)]
+                ("window_len", C.c_int32), ("ring_pages", C.POINTER(RingPages))]
 
 
 class CompressArgs(C.Structure):
@@ -64,7 +71,8 @@ class AttnArgs(C.Structure):
     _fields_ = [("batch", Batch), ("kv", Cache), ("idx", _p), ("k", C.c_int32), ("window", _p),
                 ("window_scale", _p), ("window_cap", C.c_int32), ("window_format", C.c_int32),
                 ("window_len", C.c_int32), ("num_heads", C.c_int32), ("q", _p),
-                ("softmax_scale", C.c_float), ("out", _p), ("lse", _p), ("status", _p)]
+                ("softmax_scale", C.c_float), ("out", _p), ("lse", _p), ("status", _p),
+                ("window_pages", C.POINTER(RingPages))]
 
 
 class OutputArgs(C.Structure):
@@ -129,11 +137,29 @@ def _check(where: str, rc: int):
 
 
 @dataclass
+class PagedViews:
+    """Where a layer's caches and rings live when they are pages of shared
+    bucket pools (pages.py): per cache (pool, pages in it, device table,
+    table columns); per ring its v4a_ring_pages struct and capacity."""
+    kv: tuple
+    ix: tuple | None
+    ring_main: RingPages | None
+    main_cap: int
+    ring_ix: RingPages | None
+    ix_cap: int
+    ring_swa: RingPages
+    swa_cap: int
+
+
+@dataclass
 class DeviceLayer:
-    """One layer's caches, rings, block table and the step inputs on the GPU."""
+    """One layer's caches, rings, block table and the step inputs on the GPU
+    (caches and rings in the layer's own tensors, or in shared page pools
+    when `paged` is set)."""
     spec: object
     t: dict            # name -> CUDA tensor
     status: torch.Tensor
+    paged: PagedViews | None = None
 
     @classmethod
     def from_case(cls, case, device="cuda") -> "DeviceLayer":
@@ -157,32 +183,50 @@ class DeviceLayer:
 
     def kv_cache(self) -> Cache:
         s = self.spec
+        if self.paged:
+            pool, n, table, cols = self.paged.kv
+            return Cache(s.ratio, s.dim, s.rope_dims, s.theta, s.kv_fmt, _ptr(pool), n, _ptr(table), cols)
         return Cache(s.ratio, s.dim, s.rope_dims, s.theta, s.kv_fmt, _ptr(self.t["kv_pool"]),
                      s.num_blocks, _ptr(self.t["block_table"]), s.max_blocks)
 
     def ix_cache(self) -> Cache:
         s = self.spec
+        if self.paged:
+            pool, n, table, cols = self.paged.ix
+            return Cache(4, s.ix_dim, s.ix_rope_dims, s.theta, s.ix_fmt, _ptr(pool), n, _ptr(table), cols)
         return Cache(4, s.ix_dim, s.ix_rope_dims, s.theta, s.ix_fmt, _ptr(self.t["ix_pool"]),
                      s.num_blocks, _ptr(self.t["block_table"]), s.max_blocks)
 
     def compress_args(self, parts=("main", "indexer", "window")):
         """Arguments of v4a_compress_insert for the named parts (the others
         NULL: the call skips them)."""
-        s, t = self.spec, self.t
+        s, t, pg = self.spec, self.t, self.paged
         keep = []
         main = ix = win = None
         if "main" in parts:
-            main = Compressor(self.kv_cache(), _ptr(t["x"]), _ptr(t["gate"]), _ptr(t["bias"]),
-                              _ptr(t["gamma"]), 1e-6, _ptr(t["ring_x"]), _ptr(t["ring_gate"]), s.ring_cap)
+            if pg:
+                main = Compressor(self.kv_cache(), _ptr(t["x"]), _ptr(t["gate"]), _ptr(t["bias"]),
+                                  _ptr(t["gamma"]), 1e-6, None, None, pg.main_cap, C.pointer(pg.ring_main))
+            else:
+                main = Compressor(self.kv_cache(), _ptr(t["x"]), _ptr(t["gate"]), _ptr(t["bias"]),
+                                  _ptr(t["gamma"]), 1e-6, _ptr(t["ring_x"]), _ptr(t["ring_gate"]), s.ring_cap)
             keep.append(main)
         if s.ix_heads and "indexer" in parts:
-            ix = Compressor(self.ix_cache(), _ptr(t["x_i"]), _ptr(t["gate_i"]), _ptr(t["bias_i"]),
-                            _ptr(t["gamma_i"]), 1e-6, _ptr(t["ring_x_i"]), _ptr(t["ring_gate_i"]),
-                            s.ix_ring_cap)
+            if pg:
+                ix = Compressor(self.ix_cache(), _ptr(t["x_i"]), _ptr(t["gate_i"]), _ptr(t["bias_i"]),
+                                _ptr(t["gamma_i"]), 1e-6, None, None, pg.ix_cap, C.pointer(pg.ring_ix))
+            else:
+                ix = Compressor(self.ix_cache(), _ptr(t["x_i"]), _ptr(t["gate_i"]), _ptr(t["bias_i"]),
+                                _ptr(t["gamma_i"]), 1e-6, _ptr(t["ring_x_i"]), _ptr(t["ring_gate_i"]),
+                                s.ix_ring_cap)
             keep.append(ix)
         if "window" in parts:
-            win = Window(_ptr(t["k_swa"]), s.dim, s.rope_dims, s.theta, s.swa_fmt, _ptr(t["swa_ring"]),
-                         _ptr(t.get("swa_scale")), s.swa_cap, s.swa)
+            if pg:
+                win = Window(_ptr(t["k_swa"]), s.dim, s.rope_dims, s.theta, s.swa_fmt, None, None, pg.swa_cap,
+                             s.swa, C.pointer(pg.ring_swa))
+            else:
+                win = Window(_ptr(t["k_swa"]), s.dim, s.rope_dims, s.theta, s.swa_fmt, _ptr(t["swa_ring"]),
+                             _ptr(t.get("swa_scale")), s.swa_cap, s.swa)
             keep.append(win)
         a = CompressArgs(self.batch(), C.pointer(main) if main else None, C.pointer(ix) if ix else None,
                          C.pointer(win) if win else None, _ptr(self.status))
@@ -200,6 +244,11 @@ class DeviceLayer:
             idx, k = t["window_only_idx"], 0
         else:
             k = s.topk if idx is not None else 0
+        if self.paged:
+            pg = self.paged
+            return AttnArgs(self.batch(), self.kv_cache(), _ptr(idx), k, None, None, pg.swa_cap, s.swa_fmt,
+                            s.swa, s.heads, _ptr(t["q"]), 1.0 / math.sqrt(s.dim), _ptr(out), _ptr(lse),
+                            _ptr(self.status), C.pointer(pg.ring_swa))
         return AttnArgs(self.batch(), self.kv_cache(), _ptr(idx), k,
                         _ptr(t["swa_ring"]), _ptr(t.get("swa_scale")), s.swa_cap, s.swa_fmt, s.swa,
                         s.heads, _ptr(t["q"]), 1.0 / math.sqrt(s.dim), _ptr(out), _ptr(lse),

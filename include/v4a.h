@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define V4A_ABI_VERSION 2
+#define V4A_ABI_VERSION 3
 
 #if defined(__GNUC__)
 #define V4A_API __attribute__((visibility("default")))
@@ -54,6 +54,7 @@ extern "C" {
 #define V4A_ERR_RING_TOO_SMALL 3  /* ring capacity < window - 1 + max_new_per_seq */
 #define V4A_ERR_WORKSPACE      4  /* workspace missing or smaller than *_workspace_size */
 #define V4A_ERR_CUDA           5  /* a kernel launch failed */
+#define V4A_ERR_OUT_OF_PAGES   6  /* page allocator (v4a_pages.h): a bucket has too few free pages */
 
 /* ---- device status bits (OR-ed into *status when status != NULL) ---------- */
 #define V4A_DEV_BAD_BLOCK  1  /* a needed block-table entry is < 0 or >= num_blocks */
@@ -129,6 +130,26 @@ typedef struct {
 } v4a_cache;
 
 /*
+ * A ring kept in pages of a shared pool instead of a per-sequence buffer
+ * (vLLM page, Method details, "compressor state as a sliding window": the
+ * rolling compressor residual, like the sliding-window keys, is registered as
+ * sliding-window KV and lives in the same page pools as the compressed
+ * caches).  Slot s (0 <= s < ring_cap) of sequence b lives in page
+ * table[b][s / slots] at index s % slots.  Inside a page the rows come first
+ * ([slots][row bytes]: the bf16 x of a compressor ring, the key row of a
+ * window ring), then one fp32 per slot (the compressor's gate, the fp8
+ * window's scale; absent for a bf16 window).  A page id outside
+ * [0, num_pages) sets V4A_DEV_BAD_BLOCK and the slot is skipped.
+ */
+typedef struct {
+  void* pool;                  /* page pool base; 16-byte aligned */
+  int64_t num_pages;
+  int64_t page_bytes;          /* page stride: a multiple of 16, >= slots * (row bytes + 4) */
+  const int32_t* table;        /* [num_seqs][ring_cap / slots] page ids */
+  int32_t slots;               /* slots per page; ring_cap must be a multiple of it */
+} v4a_ring_pages;
+
+/*
  * One compressor (the main KV compressor or the indexer's own).  For token t
  * at position P with (P+1) % ratio == 0 it emits entry i = (P+1)/ratio - 1 over
  * the native positions [4i-4, 4i+3] (c4a; positions < 0 take no weight) or
@@ -148,6 +169,8 @@ typedef struct {
   uint16_t* ring_x;            /* [num_seqs][ring_cap][cache.dim] bf16 */
   float* ring_gate;            /* [num_seqs][ring_cap] */
   int32_t ring_cap;            /* >= window - 1 + max_new_per_seq (window 8 or 128) */
+  const v4a_ring_pages* ring_pages; /* host pointer or NULL.  Non-NULL: the ring lives in
+                                       these pages and ring_x / ring_gate are not read */
 } v4a_compressor;
 
 /* Uncompressed sliding-window keys: k[t] rotated at P, encoded, stored at
@@ -161,6 +184,8 @@ typedef struct {
   float* ring_scale;           /* [num_seqs][ring_cap] (fp8 only) */
   int32_t ring_cap;            /* >= window_len - 1 + max_new_per_seq, else V4A_ERR_RING_TOO_SMALL */
   int32_t window_len;          /* the sliding window the ring serves (128); >= 1 */
+  const v4a_ring_pages* ring_pages; /* host pointer or NULL.  Non-NULL: the ring lives in
+                                       these pages and ring / ring_scale are not read */
 } v4a_window;
 
 typedef struct {
@@ -276,6 +301,8 @@ typedef struct {
   uint16_t* out;               /* [T][H][kv.dim] bf16 */
   float* lse;                  /* [T][H] or NULL */
   int32_t* status;
+  const v4a_ring_pages* window_pages; /* host pointer or NULL.  Non-NULL: the window ring
+                                         lives in these pages (window / window_scale unread) */
 } v4a_attn_args;
 
 /* Bytes of device workspace v4a_sparse_attn needs: the per-chunk results of

@@ -22,13 +22,16 @@ def lib():
 
 
 def test_exports_every_declared_symbol(lib):
-    hdr = open(os.path.join(ROOT, "include", "v4a.h")).read()
-    names = re.findall(r"V4A_API\s+[\w\s\*]+?\b(v4a_\w+)\s*\(", hdr)
-    assert len(names) >= 8
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            hdr = open(os.path.join(ROOT, "include", h)).read()
+            names += re.findall(r"V4A_API\s+[\w\s\*]+?\b(v4a_\w+)\s*\(", hdr)
+    assert len(names) >= 18 and "v4a_pages_create" in names
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.v4a_abi_version() == 2
-    for code in range(6):
+    assert lib.v4a_abi_version() == 3
+    for code in range(7):
         assert lib.v4a_status_string(code).decode() != "unknown status"
 
 
@@ -177,3 +180,36 @@ def test_attention_workspace_covers_one_launch_of_a_long_batch(lib):
                       d.swa, d.heads, 0x40, 0.04, 0x50, None, None)
     dchunks = -(-(d.topk + d.swa) // 64)
     assert lib.v4a_attn_workspace_size(C.byref(ad)) >= d.tokens * dchunks * d.heads * (d.dim * 2 + 8)
+
+
+def test_host_validation_of_paged_rings(lib):
+    """A ring kept in pages must name a 16-byte aligned pool and page stride,
+    a capacity that is a whole number of pages and pages large enough for
+    their slots (row + fp32); an empty batch checks them without launching."""
+    spec = I.c4a_decode_1m()
+    L = _FakeLayer(spec)
+    b0 = L.batch()
+    b0.num_tokens = 0
+    cap = 32 * 4                                   # >= window - 1 + new for the c4a compressor
+    row = 2 * spec.dim + 4
+
+    def run(pool=0x10000, page_bytes=32 * row, slots=32, cap=cap, table=0x9000):
+        rp = v4a.RingPages(pool, 1000, page_bytes, table, slots)
+        comp = v4a.Compressor(L.kv_cache(), 0x10, 0x20, 0x30, 0x40, 1e-6, None, None, cap, C.pointer(rp))
+        a = v4a.CompressArgs(b0, C.pointer(comp), None, None, None)
+        return lib.v4a_compress_insert(C.byref(a), None)
+
+    assert 32 * row % 16 == 0
+    assert run() == 0
+    assert run(page_bytes=32 * row - 16) == 1      # too small for 32 slots
+    assert run(page_bytes=32 * row + 8) == 1       # stride not a multiple of 16
+    assert run(pool=0x10008) == 1                  # pool not 16-byte aligned
+    assert run(cap=cap + 1) == 1                   # capacity not a whole number of pages
+    assert run(table=None) == 1
+    # the window ring: fp8 rows carry an fp32 scale, bf16 rows none
+    for fmt, rb in ((I.KV_FP8_TOKEN, spec.dim + 4), (I.KV_BF16, 2 * spec.dim)):
+        for pb, want in ((64 * rb + (-64 * rb) % 16, 0), (64 * rb - 16, 1)):
+            rp = v4a.RingPages(0x10000, 100, pb, 0x9000, 64)
+            win = v4a.Window(0x70, spec.dim, 64, 1e4, fmt, None, None, 128 * 2, 128, C.pointer(rp))
+            a = v4a.CompressArgs(b0, None, None, C.pointer(win), None)
+            assert lib.v4a_compress_insert(C.byref(a), None) == want, (fmt, pb)

@@ -76,3 +76,76 @@ def test_c128a_fp8_layer_matches_oracle():
                   "c128a fp8")
     assert np.allclose(step.lse.cpu().numpy(), np.stack([att[t][1] for t in range(s.tokens)]), atol=1e-3,
                        rtol=1e-4)
+
+
+def _pages_of(stack, name, li):
+    dev, host, info = stack._table(name, li)
+    bk = stack.alloc.bucket(info.bucket)
+    return stack.pools[info.bucket].view(-1, bk.page_bytes), host
+
+
+def test_paged_stack_equals_dense_stack():
+    """Caches and rings of every layer as pages of the allocator's three
+    bucket pools, replayed from one CUDA graph: the same output bytes and
+    selections as the stack with per-layer buffers, and every cache block
+    (the step's new entries included) holds the same bytes in its page."""
+    cases = S.shared_context_cases()
+    kinds = ["c128a", "c4a", "swa", "c4a", "c128a"]
+    dense = S.AttentionStack(kinds, cases)
+    paged = S.AttentionStack(kinds, cases, paged=True)
+    assert len(paged.pools) == 3
+    assert [paged.alloc.info(paged.slot[n]).bucket for n in ("c4a.kv", "c4a.swa", "c4a.state", "c128a.state",
+                                                             "c128a.swa", "swa.swa")] == [0] * 6
+    assert [paged.alloc.info(paged.slot[n]).bucket for n in ("c4a.ix", "c4a.ix_state", "c128a.kv")] == [1, 1, 2]
+    dense.run()
+    stream = torch.cuda.Stream()
+    g = paged.capture(stream)
+    g.replay()
+    torch.cuda.synchronize()
+    assert dense.status() == 0 and paged.status() == 0
+    seen = {}
+    for k, ld, lp, sd, sp in zip(kinds, dense.layers, paged.layers, dense.steps, paged.steps):
+        li = seen.get(k, 0)
+        seen[k] = li + 1
+        assert torch.equal(sd.out.cpu(), sp.out.cpu()), k
+        if sd.out_scale is not None:
+            assert torch.equal(sd.out_scale.cpu(), sp.out_scale.cpu()), k
+        if sd.idx is not None:
+            assert torch.equal(sd.idx.cpu(), sp.idx.cpu()), k
+        if k == "swa":
+            continue
+        bt = cases[k].block_table.numpy()
+        mask = bt >= 0
+        for pool_key, name in (("kv_pool", f"{k}.kv"), ("ix_pool", f"{k}.ix")):
+            if pool_key not in ld.t:
+                continue
+            pages, host = _pages_of(paged, name, li)
+            dpool = ld.t[pool_key].view(-1, pages.shape[1])
+            src = torch.from_numpy(bt[mask].astype(np.int64)).cuda()
+            dst = torch.from_numpy(host[mask].astype(np.int64)).cuda()
+            assert torch.equal(dpool[src].cpu(), pages[dst].cpu()), name
+
+
+def test_paged_layers_match_oracle():
+    """A c128a layer and a window-only layer read their caches and windows
+    from pages (compress, then attention with per-call outputs) and agree
+    with the oracle's chain on the same case."""
+    from compressed_sparse_long_c4a_gb300 import v4a
+    cases = S.shared_context_cases()
+    st = S.AttentionStack(["c4a", "c128a", "swa"], cases, paged=True)
+    for li, kind in ((1, "c128a"), (2, "swa")):
+        case = cases[kind]
+        s = case.spec
+        L = st.layers[li]
+        step = v4a.Step(L, fused_out=False)
+        step.run()
+        torch.cuda.synchronize()
+        assert int(L.status.item()) == 0, kind
+        main, ix, swa = OB.oracle_compress(case)
+        kv, ixp, ring, rsc = OB.oracle_state_after_compress(case, main, ix, swa)
+        sel = {t: np.zeros(0, np.int64) for t in range(s.tokens)} if kind == "swa" else None
+        att = OB.oracle_attention(case, kv, ring, rsc, sel)
+        U.check_close(step.o.float().cpu().numpy(), np.stack([att[t][0] for t in range(s.tokens)]), U.FP8_TOL,
+                      f"paged {kind}")
+        assert np.allclose(step.lse.cpu().numpy(), np.stack([att[t][1] for t in range(s.tokens)]), atol=1e-3,
+                           rtol=1e-4)

@@ -40,3 +40,52 @@ def test_oracle_window_only_attention_is_softmax_over_the_window():
         lse = np.log(p.sum(axis=1)) + z.max(axis=1)
         assert np.allclose(att[t][0], o, rtol=1e-12, atol=1e-12)
         assert np.allclose(att[t][1], lse, rtol=1e-12, atol=1e-12)
+
+
+def test_paged_stack_places_every_slot_the_kernels_read():
+    """The paged stack built on the CPU (no kernel runs): every cache block
+    of the synthetic cases is in the page its table names, and every ring
+    position a step reads (the compressor windows and the attention window)
+    is at page table[b][s // slots], index s % slots, s = p % ring_cap, with
+    its fp32 after the page's rows (the v4a_ring_pages layout)."""
+    cases = S.shared_context_cases()
+    kinds = ["c4a", "c128a", "swa", "c4a"]
+    st = S.AttentionStack(kinds, cases, device="cpu", paged=True)
+    assert len(st.pools) == 3
+    seen = {}
+    for k, L in zip(kinds, st.layers):
+        li = seen.get(k, 0)
+        seen[k] = li + 1
+        case = cases[k]
+        s = case.spec
+        bt = case.block_table.numpy()
+        caches = [] if k == "swa" else [(f"{k}.kv", case.kv_pool)] + ([("c4a.ix", case.ix_pool)] if k == "c4a" else [])
+        for name, dense in caches:
+            dev, host, info = st._table(name, li)
+            pb = st.alloc.bucket(info.bucket).page_bytes
+            pages = st.pools[info.bucket].view(-1, pb)
+            for b in range(s.batch):
+                for lb in np.nonzero(bt[b] >= 0)[0]:
+                    assert torch.equal(pages[host[b, lb]], dense.view(-1, pb)[bt[b, lb]]), (name, b, lb)
+            assert torch.equal(dev, torch.from_numpy(host))
+        rings = [(f"{k}.swa", case.swa_ring, case.swa_scale if case.swa_scale.numel() else None, s.swa - 1)]
+        if k != "swa":
+            rings.append((f"{k}.state", case.ring_x, case.ring_gate, s.window - 1))
+        if k == "c4a":
+            rings.append(("c4a.ix_state", case.ring_x_i, case.ring_gate_i, 7))
+        for name, rows, side, back in rings:
+            dev, host, info = st._table(name, li)
+            pb = st.alloc.bucket(info.bucket).page_bytes
+            pool = st.pools[info.bucket]
+            cap = rows.shape[1]
+            rb = rows[0, 0].numel() * rows.element_size()
+            rows8 = rows.contiguous().view(torch.uint8).view(s.batch, cap, rb)
+            for b in range(s.batch):
+                for p in range(max(0, s.cached[b] - back), s.cached[b]):
+                    sp = p % info.ring_cap
+                    page, j = int(host[b, sp // info.slots]), sp % info.slots
+                    base = page * pb
+                    assert torch.equal(pool[base + j * rb: base + (j + 1) * rb], rows8[b, p % cap]), (name, b, p)
+                    if side is not None:
+                        got = pool[base + info.slots * rb + 4 * j: base + info.slots * rb + 4 * j + 4]
+                        assert torch.equal(got, side[b, p % cap].reshape(1).view(torch.uint8)), (name, b, p)
