@@ -28,7 +28,7 @@ import numpy as np
 
 from . import formats as F
 from . import geometry as G
-from .compressor import compressed_entry, rope
+from .compressor import compressed_entry, rms_norm, rope, RMS_EPS
 from .indexer import index_scores, topk_set
 from .attention import shared_kv_attention, inverse_rope, quant_fp8_per_token
 
@@ -83,6 +83,21 @@ def window_keys(seq_ids, positions, k_bits, rope_dims, theta) -> dict:
     """Rotated window keys of this call's tokens: {(seq, position): vector}."""
     return {(int(b), int(p)): rope(F.bf16_decode(k_bits[t]), int(p), rope_dims, theta)
             for t, (b, p) in enumerate(zip(seq_ids, positions))}
+
+def query_prep(q_bits, positions, gamma, rope_dims, theta, eps=RMS_EPS) -> np.ndarray:
+    """The queries' elementwise work before attention ("DeepSeek V4 in vLLM",
+    Method details, fusion (3): the Q norm, horizontally fused with the window
+    keys' RoPE + insert).  Reading: each (token, head) row of the bf16 query
+    is RMS-normalised over the head's dims with the shared weight gamma, then
+    rotated at the token's position like every key (last rope_dims dims,
+    interleaved pairs), so that q . k depends on the relative position only.
+    q_bits: [T][H][D] bf16 bits -> float64 [T][H][D]."""
+    q = F.bf16_decode(q_bits)
+    out = np.empty_like(q)
+    for t in range(q.shape[0]):
+        for h in range(q.shape[1]):
+            out[t, h] = rope(rms_norm(q[t, h], gamma, eps), int(positions[t]), rope_dims, theta)
+    return out
 
 # --------------------------------------------------------------------------
 # Encoding into the oracle's own copy of the caches

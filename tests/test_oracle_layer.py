@@ -174,3 +174,51 @@ def test_window_keys_translation_invariance_through_the_layer_chain(monkeypatch)
         assert np.allclose(_window_chain(delta), base, atol=1e-10)
     monkeypatch.setattr(L, "rope", lambda v, pos, rope_dims, theta, inverse=False: v)
     assert not np.allclose(_window_chain(768), _window_chain(0), atol=1e-3)
+
+
+# --------------------------------------------------------------------------
+# The queries' elementwise work (fusion (3): Q norm, then the query rotated
+# at its position like every key)
+# --------------------------------------------------------------------------
+
+def test_query_prep_hand_worked_example():
+    """D = 4, one head at position 0 (no rotation), eps 0: q = (1, 2, 2, 4) has
+    mean square 25/4, so the normalised row is (0.4, 0.8, 0.8, 1.6); times
+    gamma (1, 0.5, 2, 1) it is (0.4, 0.4, 1.6, 1.6)."""
+    from oracle import layer as LY
+    q = F.bf16_encode(np.array([[[1.0, 2.0, 2.0, 4.0]]]))
+    out = LY.query_prep(q, np.array([0]), np.array([1.0, 0.5, 2.0, 1.0]), 2, 10000.0, eps=0.0)
+    assert np.allclose(out[0, 0], [0.4, 0.4, 1.6, 1.6], rtol=0, atol=1e-15)
+
+
+def test_query_prep_normalises_each_head_on_its_own():
+    """gamma = 1, eps = 0: every (token, head) row has RMS 1 after the norm and
+    the rotation (which keeps lengths), whatever the heads' magnitudes."""
+    from oracle import layer as LY
+    rng = np.random.default_rng(3)
+    D, H = 64, 5
+    q = rng.standard_normal((2, H, D)) * np.array([1e-3, 1.0, 30.0, 7.0, 0.2])[None, :, None]
+    out = LY.query_prep(F.bf16_encode(q), np.array([17, 900]), np.ones(D), 32, 10000.0, eps=0.0)
+    rms = np.sqrt(np.mean(out ** 2, axis=-1))
+    assert np.allclose(rms, 1.0, rtol=1e-12)
+
+
+def test_query_prep_scores_depend_on_relative_position_only():
+    """With a gamma that differs inside each rotary pair, q . k of a prepared
+    query at m and a key rotated at n is unchanged when m and n move
+    together, and changes when only m moves (a query left unrotated, rotated
+    the wrong way or rotated before the norm fails this)."""
+    from oracle import layer as LY
+    from oracle import compressor as CO
+    rng = np.random.default_rng(5)
+    D, R = 128, 64
+    gamma = 1.0 + 0.3 * rng.standard_normal(D)
+    q = F.bf16_encode(rng.standard_normal((1, 1, D)))
+    k = rng.standard_normal(D)
+
+    def score(m, n):
+        return float(LY.query_prep(q, np.array([m]), gamma, R, 10000.0)[0, 0] @ CO.rope(k, n, R, 10000.0))
+
+    base = score(1000, 37)
+    assert abs(score(1000 + 4321, 37 + 4321) - base) < 1e-9 * (1 + abs(base))
+    assert abs(score(1000 + 4321, 37) - base) > 1e-3
