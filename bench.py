@@ -16,8 +16,9 @@ dominant kernel (the indexer scan) against the measured HBM copy bandwidth.
 
 `variants` holds the same measurement for the indexer format with
 power-of-two block scales (the block-scaled tensor-core scan) and, for the
-default workload, for the same layer at 128k context; `model_stack` times the
-model's whole attention stack (30 c4a + 31 c128a layers) as one graph.
+default workload, for the same layer at 128k context and with the queries'
+RMSNorm + RoPE inside the step; `model_stack` times the model's whole
+attention stack (30 c4a + 31 c128a layers) as one graph.
 
 --gpus N outside a launcher starts N ranks through torch.distributed.run (one
 replica of the step per GPU: the path shards by sequence, no collective).
@@ -168,13 +169,14 @@ def oracle_token(case, t, frac=1.0):
         q_i=None if c.q_i is None else c.q_i[t:t + 1],
         q_i_scale=None if c.q_i_scale is None else c.q_i_scale[t:t + 1],
         w_i=None if c.w_i is None else c.w_i[t:t + 1],
+        q_raw=None if c.q_raw is None else c.q_raw[t:t + 1],
         spec=dataclasses.replace(c.spec, new=1))
     main, ix, swa = OB.oracle_compress(sub)
     kv, ixp, ring, rsc = OB.oracle_state_after_compress(sub, main, ix, swa)
     idx = None
     if sub.spec.ix_heads:
         idx, _ = OB.oracle_index(sub, ixp)
-    att = OB.oracle_attention(sub, kv, ring, rsc, idx)
+    att = OB.oracle_attention(sub, kv, ring, rsc, idx, q_bits=OB.step_q_bits(sub))
     o = np.stack([att[0][0]])
     from oracle import formats as F
     OB.oracle_output(sub, F.bf16_encode(o))
@@ -527,8 +529,10 @@ def main():
     # the same layer with the indexer's per-32 scales restricted to powers of
     # two (the block-scaled tensor-core scan): a second configuration of the
     # same workload, reported beside the headline, not instead of it
-    # and the same layer at 128k context (the low end of the decode target's range)
-    variants = [f"{spec.name}_mx"] + (["c4a_decode_b4_128k"] if spec.name == "c4a_decode_b4_1m" else [])
+    # and the same layer at 128k context (the low end of the decode target's
+    # range) and with the queries normalised and rotated inside the step
+    variants = [f"{spec.name}_mx"] + (["c4a_decode_b4_128k", "c4a_decode_b4_1m_qprep"]
+                                      if spec.name == "c4a_decode_b4_1m" else [])
     for variant in variants:
         if args.no_variants or variant not in I.WORKLOADS:
             continue

@@ -186,18 +186,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_chunk_tc(const AtcArgs a,
     s.abort_flag = 0;
     tc::mbar_fence_init();
     if (a.tma_out) tc::prefetch_tmap(&omap);
+    tc::prefetch_tmap(&qmap);
+  }
+  __syncwarp();   // tcgen05.alloc is warp-collective: reconverge warp 0 after the init above
+  if (warp == 0) tc::tmem_alloc(&s.tmem_base, D < 64 ? 64 : D);
+  // everything above overlaps the previous kernel; the queries (which the
+  // compressor call may have just normalised and rotated), the selected
+  // indices, the caches and the window ring are read only after it has
+  // completed
+  pdl_wait();
+  if (tid == 0) {
     // Q: 128 rows from this query's first head (rows past the last head are
     // the next query's or zero-filled; their outputs are never stored), one
-    // 64-column swizzled box per K sub-tile
+    // 64-column swizzled box per K sub-tile; waited for before the first MMA
     tc::mbar_arrive_expect_tx(&s.bar_q, uint32_t(nsub * kRows * 128));
     for (int sub = 0; sub < nsub; ++sub)
       tc::tma_load_2d(Qs + sub * (kRows * 128), &qmap, sub * 64, t * a.H, &s.bar_q);
   }
-  __syncwarp();   // tcgen05.alloc is warp-collective: reconverge warp 0 after the init above
-  if (warp == 0) tc::tmem_alloc(&s.tmem_base, D < 64 ? 64 : D);
-  // everything above overlaps the previous kernel; the selected indices, the
-  // caches and the window ring are read only after it has completed
-  pdl_wait();
 
   // ---- key slots of this chunk (sources; the scales are loaded with the rows) ----
   if (tid < kKeys) {

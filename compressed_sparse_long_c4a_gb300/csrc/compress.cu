@@ -8,11 +8,18 @@
 // key RoPE + insert), Appendix "exact position ranges and causality" (windows
 // [4i-4, 4i+3] / [128i, 128i+127], RoPE once at the last native position).
 //
-// Grid: (T tokens, 3 roles).  Role 0 = main compressor, 1 = indexer
-// compressor, 2 = window key.  Each CTA owns one token; thread p owns the
-// element pair (2p, 2p+1) of the row, which is also one RoPE pair.  A CTA of
-// a compressor role always writes its token into the ring; if the token ends
-// a window (position P with (P+1) % ratio == 0) it also builds the entry.
+// Grid: (T tokens, 2 + head groups).  Role 0 = main compressor, 1 = indexer
+// compressor: each CTA owns one token; thread p owns the element pair
+// (2p, 2p+1) of the row, which is also one RoPE pair.  A CTA of a compressor
+// role always writes its token into the ring; if the token ends a window
+// (position P with (P+1) % ratio == 0) it also builds the entry.  Role 2 is
+// the window key (RoPE + encode + insert, thread p owning pair p as above).
+// Roles >= 3 are the queries' side of the pages' horizontal fusion (3), with
+// static warp roles: warp w of query group g normalises and rotates head
+// g * warps + w of the token, with no communication between warps.  (The
+// pages give the window key one warp as well; here it keeps a CTA of its
+// own: with one warp per key the kernels after this launch ran 8 us slower
+// per 1M-context decode step, measured, cause not found.)
 // Window positions that belong to this call are read from the call's inputs,
 // older ones from the ring; ring capacity >= window - 1 + tokens per sequence
 // guarantees no ring slot written by this call is one of those older slots.
@@ -44,6 +51,15 @@ struct WindowSide {
   float theta;
   const uint16_t* k;
   RingDev ring;      // rows: the encoded key; side: the fp8 scale
+};
+
+struct QuerySide {
+  RopeFreq rope;
+  int active, H, dim, rope_dims;
+  float eps;
+  const uint16_t* q_in;
+  uint16_t* q_out;
+  const float* gamma;
 };
 
 struct BatchDev {
@@ -297,6 +313,49 @@ __device__ void compress_token(const CompressSide& c, const BatchDev& bt, int t,
   }
 }
 
+// ---- fusion (3), the queries: one warp per query head ----
+// Lane l holds the element pairs l, l + 32, ... (pairs never straddle lanes,
+// so the rotation stays in the lane); dim % 64 == 0 and dim <= 1024.
+constexpr int kWarpPairsMax = 16;
+
+__device__ void query_head(const QuerySide& q, int t, int P, int h, int lane) {
+  const int per = q.dim >> 6;                 // pairs per lane
+  const int64_t row = (int64_t(t) * q.H + h) * q.dim;
+  const uint32_t* in = reinterpret_cast<const uint32_t*>(q.q_in + row);
+  const float2* g2 = reinterpret_cast<const float2*>(q.gamma);
+  float v0[kWarpPairsMax], v1[kWarpPairsMax];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < kWarpPairsMax; ++i) {
+    if (i < per) {
+      const uint32_t v = in[lane + 32 * i];
+      v0[i] = bf16_to_f32(uint16_t(v & 0xffffu));
+      v1[i] = bf16_to_f32(uint16_t(v >> 16));
+      ss = fmaf(v0[i], v0[i], fmaf(v1[i], v1[i], ss));
+    }
+  }
+  ss = warp_sum(ss);
+  const float r = 1.f / sqrtf(ss / float(q.dim) + q.eps);
+  const int first = q.dim - q.rope_dims;
+  uint32_t* out = reinterpret_cast<uint32_t*>(q.q_out + row);
+#pragma unroll
+  for (int i = 0; i < kWarpPairsMax; ++i) {
+    if (i < per) {
+      const int j = lane + 32 * i;
+      const float2 g = g2[j];
+      float x0 = v0[i] * r * g.x, x1 = v1[i] * r * g.y;
+      if (2 * j >= first) {
+        float cs, sn;
+        rope_cos_sin(P, q.rope.inv[(2 * j - first) >> 1], &cs, &sn);
+        const float a0 = x0, a1 = x1;
+        x0 = a0 * cs - a1 * sn;
+        x1 = a0 * sn + a1 * cs;
+      }
+      out[j] = uint32_t(f32_to_bf16(x0)) | (uint32_t(f32_to_bf16(x1)) << 16);
+    }
+  }
+}
+
 __device__ void window_token(const WindowSide& w, int t, int b, int P, int32_t* status) {
   __shared__ float red[32];
   const int p = threadIdx.x;
@@ -323,7 +382,7 @@ __device__ void window_token(const WindowSide& w, int t, int b, int P, int32_t* 
 }
 
 __global__ void compress_insert_kernel(BatchDev bt, CompressSide mainc, CompressSide ixc,
-                                       WindowSide win, int32_t* status) {
+                                       WindowSide win, QuerySide qs, int32_t* status) {
   pdl_trigger();   // the next kernel may be scheduled now (it waits for this one in-kernel)
   const int t = blockIdx.x;
   const int role = blockIdx.y;
@@ -341,6 +400,11 @@ __global__ void compress_insert_kernel(BatchDev bt, CompressSide mainc, Compress
   if (role == 0 && mainc.active) compress_token(mainc, bt, t, b, P, ok, status);
   if (role == 1 && ixc.active) compress_token(ixc, bt, t, b, P, ok, status);
   if (role == 2 && win.active && ok) window_token(win, t, b, P, status);
+  if (role >= 3 && qs.active) {
+    // static warp roles: warp w of query group g takes head g * warps + w
+    const int h = (role - 3) * int(blockDim.x >> 5) + int(threadIdx.x >> 5);
+    if (h < qs.H) query_head(qs, t, P, h, threadIdx.x & 31);
+  }
 }
 
 static int fill_side(const v4a_compressor* c, bool indexer, CompressSide* s, int max_new) {
@@ -408,17 +472,32 @@ int compress_insert(const v4a_compress_args* a, cudaStream_t stream) {
                        w.format == V4A_KV_FP8_TOKEN, w.ring_pages);
     if (rc) return rc;
   }
-  if (B.num_tokens == 0 || (!mc.active && !ic.active && !ws.active)) return V4A_OK;
+  QuerySide qs{};
+  if (a->query) {
+    const v4a_query& q = *a->query;
+    if (!q.q_in || !q.q_out || !q.gamma || q.num_heads < 1) return V4A_ERR_INVALID_ARG;
+    if (q.dim <= 0 || q.dim % 64 || q.dim > 1024) return V4A_ERR_UNSUPPORTED;
+    if (q.rope_dims < 0 || q.rope_dims > q.dim || q.rope_dims % 2 || !(q.eps >= 0.f)) return V4A_ERR_INVALID_ARG;
+    if (q.rope_dims > 128) return V4A_ERR_UNSUPPORTED;
+    qs.rope = make_rope_freq(q.rope_dims, q.rope_theta);
+    qs.active = 1; qs.H = q.num_heads; qs.dim = q.dim; qs.rope_dims = q.rope_dims; qs.eps = q.eps;
+    qs.q_in = q.q_in; qs.q_out = q.q_out; qs.gamma = q.gamma;
+  }
+  if (B.num_tokens == 0 || (!mc.active && !ic.active && !ws.active && !qs.active)) return V4A_OK;
   int maxdim = 64;
   if (mc.active) maxdim = max(maxdim, mc.dim);
   if (ic.active) maxdim = max(maxdim, ic.dim);
-  if (ws.active) maxdim = max(maxdim, ws.dim);
   int threads = ((maxdim / 2) + 31) / 32 * 32;
   // one thread per window position as well (128 for c128a compressors)
   if ((mc.active && mc.ratio == 128) || (ic.active && ic.ratio == 128)) threads = max(threads, 128);
+  if (ws.active) threads = max(threads, ((ws.dim / 2) + 31) / 32 * 32);
+  // query heads: one warp each, in groups of 8 warps (or more) per CTA
+  if (qs.active) threads = max(threads, 256);
+  threads = max(threads, 64);
+  const int groups = qs.active ? (qs.H + threads / 32 - 1) / (threads / 32) : 0;
   BatchDev bd{B.num_tokens, B.num_seqs, B.max_new_per_seq, B.seq_ids, B.positions};
-  dim3 grid(B.num_tokens, 3);
-  compress_insert_kernel<<<grid, max(threads, 64), 0, stream>>>(bd, mc, ic, ws, a->status);
+  dim3 grid(B.num_tokens, 3 + groups);
+  compress_insert_kernel<<<grid, threads, 0, stream>>>(bd, mc, ic, ws, qs, a->status);
   return cudaGetLastError() == cudaSuccess ? V4A_OK : V4A_ERR_CUDA;
 }
 

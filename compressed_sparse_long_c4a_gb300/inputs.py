@@ -65,6 +65,7 @@ class LayerSpec:
     out_fmt: int = OUT_BF16
     spare_blocks: int = 3      # unused physical blocks in the pool
     window_only: bool = False  # pure sliding-window layer: attention over the window alone
+    q_prep: bool = False       # the step normalises and rotates the raw queries (fusion (3))
 
     @property
     def entries_per_block(self) -> int:
@@ -186,7 +187,7 @@ class Case:
     k_swa: torch.Tensor            # [T][D] bf16 (pre-RoPE window key)
     swa_ring: torch.Tensor         # [B][Rs][D] bf16 or uint8
     swa_scale: torch.Tensor        # [B][Rs] fp32 (fp8 window only; else empty)
-    q: torch.Tensor                # [T][H][D] bf16 (already rotated)
+    q: torch.Tensor                # [T][H][D] bf16 (already rotated; the step's output when q_prep)
     ix_pool: torch.Tensor | None = None
     x_i: torch.Tensor | None = None
     gate_i: torch.Tensor | None = None
@@ -198,6 +199,8 @@ class Case:
     q_i_scale: torch.Tensor | None = None  # [T][HI] fp32 (fp8 query)
     w_i: torch.Tensor | None = None        # [T][HI] fp32
     o_in: torch.Tensor | None = None       # [T][H][D] bf16 (input of the output stage)
+    q_raw: torch.Tensor | None = None      # [T][H][D] bf16 query before norm + RoPE (q_prep)
+    gamma_q: torch.Tensor | None = None    # [D] fp32 query RMSNorm weight (q_prep)
 
 
 def make_case(spec: LayerSpec, seed: int = 0) -> Case:
@@ -278,6 +281,9 @@ def make_case(spec: LayerSpec, seed: int = 0) -> Case:
             case.q_i = _fp8_codes((T, HI, dI), seed, 28)
             case.q_i_scale = _scales(T * HI, seed, 29, 100.0).view(T, HI)
         case.w_i = _rand((T, HI), seed, 30)
+    if s.q_prep:
+        case.q_raw = _bf16(_randn((T, s.heads, D), seed, 31, std=2.0))
+        case.gamma_q = _randn((D,), seed, 32, std=0.1, mean=1.0)
     return case
 
 
@@ -329,8 +335,9 @@ def c4a_prefill_4x4k() -> LayerSpec:
 
 def c4a_decode_1m() -> LayerSpec:
     """c4a decode at 1M context, batch 4, fp8 attention cache, fp4 indexer,
-    fp8 output.  m = 1,048,575 emits entry 262,143 (the last slot of a block),
-    so each query sees 262,144 entries."""
+    fp8 output (the queries arrive normalised and rotated).  m = 1,048,575
+    emits entry 262,143 (the last slot of a block), so each query sees
+    262,144 entries."""
     return LayerSpec(name="c4a_decode_b4_1m", ratio=4, batch=4, heads=128, dim=512,
                      cached=(1_048_575,) * 4, kv_fmt=KV_FP8_TOKEN, swa_fmt=KV_FP8_TOKEN,
                      ix_heads=64, ix_dim=128, ix_fmt=IX_FP4_B32, ix_q_fmt=Q_FP8_HEAD,
@@ -349,6 +356,12 @@ def c4a_decode_1m_mx() -> LayerSpec:
     powers of two (the OCP MX rule; same bytes per entry), which the tensor
     cores apply inside a block-scaled MMA."""
     return dataclasses.replace(c4a_decode_1m(), name="c4a_decode_b4_1m_mx", ix_fmt=IX_FP4_MX32)
+
+
+def c4a_decode_1m_qprep() -> LayerSpec:
+    """c4a_decode_b4_1m with the queries' RMSNorm + RoPE inside the step
+    (the query side of the horizontal fusion with the window-key insert)."""
+    return dataclasses.replace(c4a_decode_1m(), name="c4a_decode_b4_1m_qprep", q_prep=True)
 
 
 def c4a_decode_128k() -> LayerSpec:
@@ -386,6 +399,7 @@ WORKLOADS = {
     "c4a_decode_b4_128k": c4a_decode_128k,
     "c128a_decode_b4_1m": c128a_decode_1m,
     "c4a_decode_b4_1m_dsv4": c4a_decode_1m_dsv4,
+    "c4a_decode_b4_1m_qprep": c4a_decode_1m_qprep,
 }
 
 

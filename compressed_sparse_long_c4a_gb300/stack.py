@@ -36,7 +36,7 @@ from . import v4a
 
 # step inputs a layer keeps in its own tensors when its caches and rings are paged
 _STEP_INPUTS = ("seq_ids", "positions", "x", "gate", "bias", "gamma", "k_swa", "q", "x_i", "gate_i",
-                "bias_i", "gamma_i", "q_i", "q_i_scale", "w_i", "o_in", "window_only_idx")
+                "bias_i", "gamma_i", "q_i", "q_i_scale", "w_i", "o_in", "window_only_idx", "q_raw", "gamma_q")
 
 
 def deepseek_v4_mix(n_c4a: int = 30, n_c128a: int = 31, n_swa: int = 0) -> list:
@@ -247,9 +247,10 @@ def decode_1m_cases(seed: int = 0, c4a_case=None) -> dict:
 
 def shared_context_cases(seed: int = 0) -> dict:
     """Small cases of the three kinds with one context per sequence (the
-    paged stack's rule): sequence 0 at position 12,031 ends a c128a window
-    and a c4a window, sequence 1 at 10,003 a c4a window only."""
-    ctx = dict(batch=2, cached=(128 * 94 - 1, 4 * 2500 + 3))
+    paged stack's rule), the queries normalised and rotated inside the step:
+    sequence 0 at position 12,031 ends a c128a window and a c4a window,
+    sequence 1 at 10,003 a c4a window only."""
+    ctx = dict(batch=2, cached=(128 * 94 - 1, 4 * 2500 + 3), q_prep=True)
     c4a = dataclasses.replace(I.c4a_decode_1m(), name="paged_c4a_small", **ctx)
     c128a = dataclasses.replace(I.c128a_decode_1m(), name="paged_c128a_small", **ctx)
     swa = dataclasses.replace(I.swa_decode_1m(), name="paged_swa_small", **ctx)

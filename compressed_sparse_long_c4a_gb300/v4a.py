@@ -56,9 +56,14 @@ class Window(C.Structure):
                 ("window_len", C.c_int32), ("ring_pages", C.POINTER(RingPages))]
 
 
+class Query(C.Structure):
+    _fields_ = [("q_in", _p), ("q_out", _p), ("gamma", _p), ("eps", C.c_float), ("num_heads", C.c_int32),
+                ("dim", C.c_int32), ("rope_dims", C.c_int32), ("rope_theta", C.c_float)]
+
+
 class CompressArgs(C.Structure):
     _fields_ = [("batch", Batch), ("main", C.POINTER(Compressor)), ("indexer", C.POINTER(Compressor)),
-                ("window", C.POINTER(Window)), ("status", _p)]
+                ("window", C.POINTER(Window)), ("status", _p), ("query", C.POINTER(Query))]
 
 
 class IndexArgs(C.Structure):
@@ -167,7 +172,7 @@ class DeviceLayer:
         for f in ("seq_ids", "positions", "block_table", "kv_pool", "x", "gate", "bias", "gamma",
                   "ring_x", "ring_gate", "k_swa", "swa_ring", "swa_scale", "q", "ix_pool", "x_i",
                   "gate_i", "bias_i", "gamma_i", "ring_x_i", "ring_gate_i", "q_i", "q_i_scale",
-                  "w_i", "o_in"):
+                  "w_i", "o_in", "q_raw", "gamma_q"):
             v = getattr(case, f)
             if v is not None and v.numel() > 0:
                 t[f] = v.to(device).contiguous()
@@ -197,12 +202,13 @@ class DeviceLayer:
         return Cache(4, s.ix_dim, s.ix_rope_dims, s.theta, s.ix_fmt, _ptr(self.t["ix_pool"]),
                      s.num_blocks, _ptr(self.t["block_table"]), s.max_blocks)
 
-    def compress_args(self, parts=("main", "indexer", "window")):
+    def compress_args(self, parts=("main", "indexer", "window", "query")):
         """Arguments of v4a_compress_insert for the named parts (the others
-        NULL: the call skips them)."""
+        NULL: the call skips them).  "query" (layers with q_prep) normalises
+        and rotates q_raw into q, the attention's query."""
         s, t, pg = self.spec, self.t, self.paged
         keep = []
-        main = ix = win = None
+        main = ix = win = qry = None
         if "main" in parts:
             if pg:
                 main = Compressor(self.kv_cache(), _ptr(t["x"]), _ptr(t["gate"]), _ptr(t["bias"]),
@@ -228,8 +234,12 @@ class DeviceLayer:
                 win = Window(_ptr(t["k_swa"]), s.dim, s.rope_dims, s.theta, s.swa_fmt, _ptr(t["swa_ring"]),
                              _ptr(t.get("swa_scale")), s.swa_cap, s.swa)
             keep.append(win)
+        if s.q_prep and "query" in parts:
+            qry = Query(_ptr(t["q_raw"]), _ptr(t["q"]), _ptr(t["gamma_q"]), 1e-6, s.heads, s.dim, s.rope_dims,
+                        s.theta)
+            keep.append(qry)
         a = CompressArgs(self.batch(), C.pointer(main) if main else None, C.pointer(ix) if ix else None,
-                         C.pointer(win) if win else None, _ptr(self.status))
+                         C.pointer(win) if win else None, _ptr(self.status), C.pointer(qry) if qry else None)
         return a, keep
 
     def index_args(self, out_idx: torch.Tensor) -> IndexArgs:
@@ -264,7 +274,7 @@ class DeviceLayer:
 # --------------------------------------------------------------------------
 
 
-def compress_insert(layer: DeviceLayer, stream=None, parts=("main", "indexer", "window")):
+def compress_insert(layer: DeviceLayer, stream=None, parts=("main", "indexer", "window", "query")):
     a, keep = layer.compress_args(parts)
     _check("v4a_compress_insert", lib().v4a_compress_insert(C.byref(a), _stream(stream)))
 
@@ -420,7 +430,7 @@ class Step:
         (with `overlap`, the compressor's parts split over two streams)."""
         L = self.layer
         if L.spec.window_only:
-            compress_insert(L, stream, parts=("window",))   # a pure sliding-window layer has no compressor
+            compress_insert(L, stream, parts=("window", "query"))   # a pure sliding-window layer has no compressor
         elif self.overlap == "serial":
             compress_insert(L, stream)
             if L.spec.ix_heads:
@@ -435,7 +445,7 @@ class Step:
                 index_scores(L, self.idx, self.ws_index, cur)
                 fork.record(cur)
             self.side.wait_event(fork)
-            compress_insert(L, self.side, parts=("main", "window"))
+            compress_insert(L, self.side, parts=("main", "window", "query"))
             joined.record(self.side)
             if self.overlap == "select":
                 index_select(L, self.idx, self.ws_index, cur)

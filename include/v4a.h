@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define V4A_ABI_VERSION 3
+#define V4A_ABI_VERSION 4
 
 #if defined(__GNUC__)
 #define V4A_API __attribute__((visibility("default")))
@@ -188,20 +188,42 @@ typedef struct {
                                        these pages and ring / ring_scale are not read */
 } v4a_window;
 
+/*
+ * The queries' elementwise work before attention (vLLM page, Method details,
+ * fusion (3): the Q norm, fused horizontally with the window keys' RoPE +
+ * insert, one warp per query head or key head).  For token t at position P
+ * and head h:  q_out[t][h] = RoPE_P(q_in[t][h] / sqrt(mean(q_in[t][h]^2) + eps)
+ * * gamma), the rotation on the last rope_dims dims (interleaved pairs) as for
+ * the keys.  q_out is what v4a_sparse_attn takes as its already rotated q.
+ */
+typedef struct {
+  const uint16_t* q_in;        /* [T][H][dim] bf16 */
+  uint16_t* q_out;             /* [T][H][dim] bf16; may equal q_in (in place) */
+  const float* gamma;          /* [dim] RMSNorm weight, shared by the heads */
+  float eps;                   /* RMSNorm epsilon (1e-6) */
+  int32_t num_heads;           /* H >= 1 */
+  int32_t dim;                 /* a multiple of 64, <= 1024 */
+  int32_t rope_dims;           /* even, <= min(dim, 128) */
+  float rope_theta;
+} v4a_query;
+
 typedef struct {
   v4a_batch batch;
   const v4a_compressor* main;     /* host pointer; may be NULL */
   const v4a_compressor* indexer;  /* host pointer; may be NULL (c128a layers) */
   const v4a_window* window;       /* host pointer; may be NULL */
   int32_t* status;                /* optional device word */
+  const v4a_query* query;         /* host pointer; may be NULL */
 } v4a_compress_args;
 
 /*
  * Fused compressor + RMSNorm + RoPE + cache insert for the main and indexer
- * caches, and RoPE + insert of the window keys (vLLM page, Method details,
- * fusions (1) and (3); appendix "exact position ranges and causality").
- * One launch.  Returns V4A_ERR_RING_TOO_SMALL when a ring cannot hold the
- * call's tokens without overwriting positions a window still reads.
+ * caches, and the queries' norm + RoPE beside the window keys' RoPE + insert
+ * (vLLM page, Method details, fusions (1) and (3); appendix "exact position
+ * ranges and causality").  One launch: one CTA per token for each
+ * compressor, and warps that each take one query head or one window key.
+ * Returns V4A_ERR_RING_TOO_SMALL when a ring cannot hold the call's tokens
+ * without overwriting positions a window still reads.
  */
 V4A_API int v4a_compress_insert(const v4a_compress_args* args, void* stream);
 

@@ -93,9 +93,26 @@ def oracle_index(case, ix_pool, rows=None):
                         s.ix_dim, s.topk, rows=rows)
 
 
-def oracle_attention(case, kv_pool, swa_ring, swa_scale, idx, rows=None):
+def oracle_query(case):
+    """The oracle's prepared queries (norm + RoPE, fusion (3)) in float64."""
     s = case.spec
-    return L.attention(case.seq_ids.numpy(), case.positions.numpy(), u16(case.q), idx,
+    return L.query_prep(u16(case.q_raw), case.positions.numpy(), f64(case.gamma_q), s.rope_dims, s.theta)
+
+
+def step_q_bits(case):
+    """The bf16 query a whole step's attention reads: the oracle's prepared
+    query rounded to bf16 when the step prepares it, else the case's q."""
+    if case.spec.q_prep:
+        return F.bf16_encode(oracle_query(case))
+    return u16(case.q)
+
+
+def oracle_attention(case, kv_pool, swa_ring, swa_scale, idx, rows=None, q_bits=None):
+    """Attention of the case's queries (q_bits: the bf16 query to use instead
+    of case.q, e.g. the step's prepared query)."""
+    s = case.spec
+    q = u16(case.q) if q_bits is None else q_bits
+    return L.attention(case.seq_ids.numpy(), case.positions.numpy(), q, idx,
                        kv_pool, s.kv_block_bytes, case.block_table.numpy(), s.kv_fmt, s.ratio,
                        s.dim, swa_ring, swa_scale, s.swa_fmt, s.swa, 1.0 / math.sqrt(s.dim),
                        rows=rows)

@@ -30,7 +30,7 @@ def test_exports_every_declared_symbol(lib):
     assert len(names) >= 18 and "v4a_pages_create" in names
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.v4a_abi_version() == 3
+    assert lib.v4a_abi_version() == 4
     for code in range(7):
         assert lib.v4a_status_string(code).decode() != "unknown status"
 
@@ -213,3 +213,25 @@ def test_host_validation_of_paged_rings(lib):
             win = v4a.Window(0x70, spec.dim, 64, 1e4, fmt, None, None, 128 * 2, 128, C.pointer(rp))
             a = v4a.CompressArgs(b0, None, None, C.pointer(win), None)
             assert lib.v4a_compress_insert(C.byref(a), None) == want, (fmt, pb)
+
+
+def test_host_validation_of_query_part(lib):
+    """The queries' norm + RoPE part: pointers, a dim that is a multiple of 64
+    up to 1024, even rope dims up to 128; checked with an empty batch."""
+    spec = I.c4a_decode_1m()
+    L = _FakeLayer(spec)
+    b0 = L.batch()
+    b0.num_tokens = 0
+
+    def run(q_in=0x100, q_out=0x200, gamma=0x300, heads=128, dim=512, rope=64, eps=1e-6):
+        q = v4a.Query(q_in, q_out, gamma, eps, heads, dim, rope, 1e4)
+        a = v4a.CompressArgs(b0, None, None, None, None, C.pointer(q))
+        return lib.v4a_compress_insert(C.byref(a), None)
+
+    assert run() == 0
+    assert run(q_out=0x100) == 0            # in place
+    assert run(q_in=None) == 1 and run(q_out=None) == 1 and run(gamma=None) == 1
+    assert run(heads=0) == 1
+    assert run(dim=96) == 2 and run(dim=2048) == 2
+    assert run(rope=63) == 1 and run(rope=600) == 1 and run(rope=256) == 2
+    assert run(eps=-1.0) == 1

@@ -40,7 +40,9 @@ def _small_workloads():
                                cached=(4 * 10000 + 3, 39001, 256 * 90 + 255))
     s5d = dataclasses.replace(I.c4a_decode_1m(), name="c4a_decode_small_fp4ix_dsv4kv", batch=3,
                               kv_fmt=I.KV_FP8_DSV4, cached=(4 * 10000 + 3, 39001, 256 * 90 + 255))
-    return [I.c4a_decode_1k(), s2, s3, s4, s5, s5mx, s5d]
+    s5q = dataclasses.replace(I.c4a_decode_1m_qprep(), name="c4a_decode_small_qprep", batch=3,
+                              cached=(4 * 10000 + 3, 39001, 256 * 90 + 255))
+    return [I.c4a_decode_1k(), s2, s3, s4, s5, s5mx, s5d, s5q]
 
 
 SMALL = {s.name: s for s in _small_workloads()}
@@ -104,6 +106,13 @@ def test_compress_insert(name):
     v4a.compress_insert(L)
     torch.cuda.synchronize()
     assert int(L.status.item()) == 0
+    if s.q_prep:
+        # the queries' norm + RoPE, fused with the window keys (fusion (3))
+        qref = OB.oracle_query(case)
+        qgpu = L.t["q"].cpu()
+        for t in range(s.tokens):
+            for h in range(s.heads):
+                U.check_bf16_row(OB.u16(qgpu[t, h]), qref[t, h], f"{name} q t={t} h={h}")
     main, ix, swa = r.oracle_compress()
     bt = case.block_table.numpy()
     kv_in, kv_out = OB.u8(case.kv_pool), L.t["kv_pool"].cpu().numpy()
@@ -279,6 +288,13 @@ def test_end_to_end(name):
     torch.cuda.synchronize()
     assert int(L.status.item()) == 0
     rows = r.rows()
+    if s.q_prep:
+        # the queries' norm + RoPE (fusion (3)): bf16 within 1 ulp of the oracle
+        qref = OB.oracle_query(case)
+        qgpu = L.t["q"].cpu()
+        for t in rows[:64]:
+            for h in range(s.heads):
+                U.check_bf16_row(OB.u16(qgpu[t, h]), qref[t, h], f"{name} q t={t} h={h}")
     main, ix, swa = r.oracle_compress()
     kv, ixp, ring, rsc = OB.oracle_state_after_compress(case, main, ix, swa)
     idx = None
@@ -295,7 +311,8 @@ def test_end_to_end(name):
     # more than the attention tolerance (observed: one swap at 2e-8 of the k-th
     # score in 1,536 prefill rows), so the rest of the chain is compared on the
     # GPU's own set.
-    att = OB.oracle_attention(case, kv, ring, rsc, idx if gsel is None else gsel, rows=rows)
+    att = OB.oracle_attention(case, kv, ring, rsc, idx if gsel is None else gsel, rows=rows,
+                              q_bits=OB.step_q_bits(case))
     o_ref = np.stack([att[t][0] for t in rows])
     tol = U.BF16_TOL if s.kv_fmt == F.KV_BF16 else U.FP8_TOL
     U.check_close(step.o.float().cpu().numpy()[rows], o_ref, tol, name)
@@ -322,7 +339,8 @@ def test_end_to_end(name):
 FUSED_EXPECTED = {"c4a_decode_b4_1m", "c4a_decode_b4_1m_mx", "c4a_decode_b4_128k", "c128a_decode_b4_1m",
                   "c4a_decode_b32_32k_64k",
                   "c128a_decode_b64_64k_128k", "c4a_decode_small_fp8ix", "c4a_decode_small_fp4ix_fp8kv",
-                  "c4a_decode_small_mx4ix_fp8kv", "c4a_decode_small_fp4ix_dsv4kv", "c4a_decode_b4_1m_dsv4"}
+                  "c4a_decode_small_mx4ix_fp8kv", "c4a_decode_small_fp4ix_dsv4kv", "c4a_decode_b4_1m_dsv4",
+                  "c4a_decode_small_qprep", "c4a_decode_b4_1m_qprep"}
 
 
 @pytest.mark.parametrize("name", [_marks(n) for n in ALL])
@@ -348,7 +366,7 @@ def test_fused_output_equals_two_calls(name):
 
 
 OVERLAP_CASES = ["c4a_decode_small_fp4ix_fp8kv", "c4a_decode_small_mx4ix_fp8kv", "c4a_decode_small_fp8ix",
-                 "c4a_prefill_small"]
+                 "c4a_prefill_small", "c4a_decode_small_qprep"]
 
 
 @pytest.mark.parametrize("mode", ["start", "select"])
@@ -386,3 +404,34 @@ def test_overlap_modes_equal_serial(name, mode):
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(split_g.out.cpu(), ref.out.cpu())
+
+
+@pytest.mark.parametrize("heads,dim,rope,inplace", [(5, 128, 64, False), (128, 512, 64, True), (33, 1024, 128, False),
+                                                    (1, 64, 0, False), (9, 256, 32, True)])
+def test_query_norm_rope(heads, dim, rope, inplace):
+    """The query part of v4a_compress_insert alone (one warp per head; head
+    counts that leave a head group partly empty; no rotation; in place)
+    against the oracle: every element within 1 bf16 ulp."""
+    import ctypes as C
+    from compressed_sparse_long_c4a_gb300 import v4a
+    T = 7
+    g = torch.Generator().manual_seed(heads * 1000 + dim)
+    q_in = (torch.randn((T, heads, dim), generator=g) * 3).to(torch.bfloat16)
+    gamma = 1 + 0.2 * torch.randn((dim,), generator=g)
+    pos = torch.tensor([0, 1, 127, 4095, 65536, 1_048_575, 777_777], dtype=torch.int32)
+    dq_in, dgam, dpos = q_in.cuda(), gamma.cuda(), pos.cuda()
+    dq_out = dq_in if inplace else torch.empty_like(dq_in)
+    sid = torch.arange(T, dtype=torch.int32).cuda()
+    status = torch.zeros(1, dtype=torch.int32).cuda()
+    qs = v4a.Query(dq_in.data_ptr(), dq_out.data_ptr(), dgam.data_ptr(), 1e-6, heads, dim, rope, 10000.0)
+    a = v4a.CompressArgs(v4a.Batch(T, sid.data_ptr(), dpos.data_ptr(), T, 1), None, None, None,
+                         status.data_ptr(), C.pointer(qs))
+    assert v4a.lib().v4a_compress_insert(C.byref(a), None) == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    from oracle import layer as LY
+    ref = LY.query_prep(OB.u16(q_in), pos.numpy(), gamma.double().numpy(), rope, 10000.0)
+    got = dq_out.cpu()
+    for t in range(T):
+        for h in range(heads):
+            U.check_bf16_row(OB.u16(got[t, h]), ref[t, h], f"t={t} h={h}")

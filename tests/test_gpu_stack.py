@@ -24,7 +24,8 @@ def test_window_only_attention_matches_oracle():
     # the oracle's chain on its own window insert, attention over no compressed entry
     main, ix, swa = OB.oracle_compress(case)
     kv, ixp, ring, rsc = OB.oracle_state_after_compress(case, main, ix, swa)
-    att = OB.oracle_attention(case, kv, ring, rsc, {t: np.zeros(0, np.int64) for t in range(s.tokens)})
+    att = OB.oracle_attention(case, kv, ring, rsc, {t: np.zeros(0, np.int64) for t in range(s.tokens)},
+                              q_bits=OB.step_q_bits(case))
     U.check_close(step.o.float().cpu().numpy(), np.stack([att[t][0] for t in range(s.tokens)]), U.FP8_TOL,
                   "window only")
     lse_ref = np.stack([att[t][1] for t in range(s.tokens)])
@@ -71,7 +72,7 @@ def test_c128a_fp8_layer_matches_oracle():
     assert int(L.status.item()) == 0
     main, ix, swa = OB.oracle_compress(case)
     kv, ixp, ring, rsc = OB.oracle_state_after_compress(case, main, ix, swa)
-    att = OB.oracle_attention(case, kv, ring, rsc, None)
+    att = OB.oracle_attention(case, kv, ring, rsc, None, q_bits=OB.step_q_bits(case))
     U.check_close(step.o.float().cpu().numpy(), np.stack([att[t][0] for t in range(s.tokens)]), U.FP8_TOL,
                   "c128a fp8")
     assert np.allclose(step.lse.cpu().numpy(), np.stack([att[t][1] for t in range(s.tokens)]), atol=1e-3,
@@ -144,7 +145,7 @@ def test_paged_layers_match_oracle():
         main, ix, swa = OB.oracle_compress(case)
         kv, ixp, ring, rsc = OB.oracle_state_after_compress(case, main, ix, swa)
         sel = {t: np.zeros(0, np.int64) for t in range(s.tokens)} if kind == "swa" else None
-        att = OB.oracle_attention(case, kv, ring, rsc, sel)
+        att = OB.oracle_attention(case, kv, ring, rsc, sel, q_bits=OB.step_q_bits(case))
         U.check_close(step.o.float().cpu().numpy(), np.stack([att[t][0] for t in range(s.tokens)]), U.FP8_TOL,
                       f"paged {kind}")
         assert np.allclose(step.lse.cpu().numpy(), np.stack([att[t][1] for t in range(s.tokens)]), atol=1e-3,
