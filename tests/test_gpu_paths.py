@@ -5,7 +5,8 @@ oracle, through the C ABI:
   count the tensor-core scans do not take) on rows long enough for the
   multi-CTA top-k (histogram kernel, filter, final);
 * the long-row top-k after each tensor-core scan (fp8, fp4, MX fp4 keys);
-* the CUDA-core attention (head dim 64; 256 heads).
+* the CUDA-core attention (head dim 64; 256 heads);
+* the window ring read from pages of a pool, on both attention paths.
 
 Scores must agree entry by entry within 1e-5 of the query's score scale; the
 top-k sets may differ only by swaps within 1e-5 of the k-th score; attention
@@ -111,3 +112,66 @@ def test_cuda_core_attention(name):
     U.check_close(o, np.stack([ref[t][0] for t in range(spec.tokens)]), U.BF16_TOL, name)
     assert np.allclose(step.lse.cpu().numpy(), np.stack([ref[t][1] for t in range(spec.tokens)]),
                        atol=1e-3, rtol=1e-4)
+
+
+def _paged_window(case, spec, slots, seed):
+    """The case's window ring as slots in pages of one pool under a shuffled
+    page table (the v4a_ring_pages layout: [slots][row] then [slots] fp32)."""
+    B, cap, D = spec.batch, spec.swa_cap, spec.dim
+    fp8 = spec.swa_fmt == I.KV_FP8_TOKEN
+    rb = D if fp8 else 2 * D
+    pb = -(-slots * (rb + (4 if fp8 else 0)) // 16) * 16
+    per = cap // slots
+    assert per * slots == cap
+    g = torch.Generator().manual_seed(seed)
+    npages = B * per + 3
+    table = torch.randperm(npages, generator=g)[:B * per].to(torch.int32).view(B, per)
+    pool = torch.zeros(npages * pb, dtype=torch.uint8)
+    rows = case.swa_ring.contiguous().view(torch.uint8).view(B, cap, rb)
+    for b in range(B):
+        for s in range(cap):
+            base = int(table[b, s // slots]) * pb
+            j = s % slots
+            pool[base + j * rb: base + (j + 1) * rb] = rows[b, s]
+            if fp8:
+                pool[base + slots * rb + 4 * j: base + slots * rb + 4 * j + 4] = \
+                    case.swa_scale[b, s].reshape(1).view(torch.uint8)
+    return pool.cuda(), table.cuda(), npages, pb
+
+
+PAGED_WINDOW = {
+    "simt_attn_d64": (ATTN["simt_attn_d64"], 32),
+    "simt_attn_h256": (ATTN["simt_attn_h256"], 64),
+    "tc_fp8_window": (dataclasses.replace(I.c4a_decode_1m(), name="tc_fp8_window", batch=2,
+                                          cached=(4 * 3000 + 3, 9001)), 16),
+    "tc_bf16_window": (dataclasses.replace(I.c4a_decode_1k(), name="tc_bf16_window", batch=3,
+                                           cached=(1024, 3001, 700)), 128),
+}
+
+
+@pytest.mark.parametrize("name", list(PAGED_WINDOW))
+def test_paged_window_equals_dense_window(name):
+    """Attention over every visible entry with the window read from pages of
+    a pool (shuffled page table) writes the same output and lse bytes as
+    with the per-sequence ring: CUDA-core path (head dim 64, 256 heads) and
+    tensor-core path (fp8 and bf16 windows)."""
+    import ctypes as C
+    v4a = _v4a()
+    spec, slots = PAGED_WINDOW[name]
+    case = I.make_case(spec, seed=5)
+    L = v4a.DeviceLayer.from_case(case)
+    T, H, D = spec.tokens, spec.heads, spec.dim
+    ws = torch.empty(max(v4a.attn_workspace_bytes(L, False), 256), dtype=torch.uint8, device="cuda")
+    o1 = torch.empty((T, H, D), dtype=torch.bfloat16, device="cuda")
+    l1 = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    o2, l2 = torch.empty_like(o1), torch.empty_like(l1)
+    v4a.sparse_attn(L, None, o1, l1, ws)
+    pool, table, npages, pb = _paged_window(case, spec, slots, seed=11)
+    rp = v4a.RingPages(pool.data_ptr(), npages, pb, table.data_ptr(), slots)
+    a = L.attn_args(None, o2, l2)
+    a.window, a.window_scale, a.window_pages = None, None, C.pointer(rp)
+    rc = v4a.lib().v4a_sparse_attn(C.byref(a), ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert int(L.status.item()) == 0
+    assert torch.equal(o1.cpu(), o2.cpu()) and torch.equal(l1.cpu(), l2.cpu())
