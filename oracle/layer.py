@@ -99,6 +99,24 @@ def query_prep(q_bits, positions, gamma, rope_dims, theta, eps=RMS_EPS) -> np.nd
             out[t, h] = rope(rms_norm(q[t, h], gamma, eps), int(positions[t]), rope_dims, theta)
     return out
 
+def index_query_prep(q_bits, positions, w, w_mult, rope_dims, theta):
+    """The indexer query's preparation ("DeepSeek V4 in vLLM", Method details:
+    the reused DeepSeek-V3.2 fusion of Q RoPE, quantisation and the weight
+    multiplication).  Reading: each (token, head) row of the bf16 indexer
+    query is rotated at the token's position on its last rope_dims dims, then
+    encoded as e4m3 with one scale per (token, head), amax / 448 (the scan's
+    fp8 query format); the head weights are multiplied by the constant
+    w_mult.  -> (codes uint8 [T][H][D], scales float64 [T][H], weights
+    float64 [T][H])."""
+    q = F.bf16_decode(q_bits)
+    T, H, D = q.shape
+    codes = np.empty((T, H, D), np.uint8)
+    scales = np.empty((T, H), np.float64)
+    for t in range(T):
+        for h in range(H):
+            codes[t, h], scales[t, h] = F.fp8_token_encode(rope(q[t, h], int(positions[t]), rope_dims, theta))
+    return codes, scales, np.asarray(w, np.float64) * float(w_mult)
+
 # --------------------------------------------------------------------------
 # Encoding into the oracle's own copy of the caches
 # --------------------------------------------------------------------------

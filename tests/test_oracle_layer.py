@@ -222,3 +222,43 @@ def test_query_prep_scores_depend_on_relative_position_only():
     base = score(1000, 37)
     assert abs(score(1000 + 4321, 37 + 4321) - base) < 1e-9 * (1 + abs(base))
     assert abs(score(1000 + 4321, 37) - base) > 1e-3
+
+
+# --------------------------------------------------------------------------
+# The indexer query's preparation (RoPE, per-head fp8, weight multiply)
+# --------------------------------------------------------------------------
+
+def test_index_query_prep_hand_worked_example():
+    """Position 0 (no rotation): q = (1, 2, 2, 4) has amax 4, so the scale is
+    4/448 and the codes are e4m3 of (112, 224, 224, 448), all exact; the
+    weights are multiplied by w_mult."""
+    from oracle import layer as LY
+    q = F.bf16_encode(np.array([[[1.0, 2.0, 2.0, 4.0]]]))
+    codes, sc, w = LY.index_query_prep(q, np.array([0]), np.array([[0.75]]), 0.125, 2, 10000.0)
+    assert sc[0, 0] == np.float32(4.0 / 448.0)
+    assert list(F.e4m3_decode(codes[0, 0])) == [112.0, 224.0, 224.0, 448.0]
+    assert w[0, 0] == 0.75 * 0.125
+
+
+def test_index_query_prep_rotates_forward_per_head():
+    """Decoding the codes and rotating back by the token's position gives the
+    bf16 query within one e4m3 step of the row (the two errors of a pair
+    mix); a rotation the wrong way, at the wrong position or on the wrong
+    dims fails.  Each head has its own scale, amax / 448 of its rotated row."""
+    from oracle import layer as LY
+    from oracle import compressor as CO
+    rng = np.random.default_rng(9)
+    T, H, D, R = 3, 4, 128, 64
+    q = rng.standard_normal((T, H, D)) * np.array([0.01, 1.0, 5.0, 80.0])[None, :, None]
+    qb = F.bf16_encode(q)
+    pos = np.array([5, 1000, 777_777])
+    codes, sc, _ = LY.index_query_prep(qb, pos, np.ones((T, H)), 1.0, R, 10000.0)
+    qd = F.bf16_decode(qb)
+    for t in range(T):
+        for h in range(H):
+            rot = CO.rope(qd[t, h], int(pos[t]), R, 10000.0)
+            assert sc[t, h] == np.float32(np.max(np.abs(rot)) / 448.0)
+            back = CO.rope(F.e4m3_decode(codes[t, h]) * sc[t, h], int(pos[t]), R, 10000.0, inverse=True)
+            step = F.e4m3_ulp(rot / sc[t, h]) * sc[t, h]
+            assert np.all(np.abs(back - qd[t, h]) <= np.max(step) + 1e-12)
+    assert len(set(np.round(sc[0], 12))) == H
