@@ -170,12 +170,14 @@ def oracle_token(case, t, frac=1.0):
         q_i_scale=None if c.q_i_scale is None else c.q_i_scale[t:t + 1],
         w_i=None if c.w_i is None else c.w_i[t:t + 1],
         q_raw=None if c.q_raw is None else c.q_raw[t:t + 1],
+        q_i_raw=None if c.q_i_raw is None else c.q_i_raw[t:t + 1],
+        w_i_raw=None if c.w_i_raw is None else c.w_i_raw[t:t + 1],
         spec=dataclasses.replace(c.spec, new=1))
     main, ix, swa = OB.oracle_compress(sub)
     kv, ixp, ring, rsc = OB.oracle_state_after_compress(sub, main, ix, swa)
     idx = None
     if sub.spec.ix_heads:
-        idx, _ = OB.oracle_index(sub, ixp)
+        idx, _ = OB.oracle_index(sub, ixp, query=OB.step_index_query(sub))
     att = OB.oracle_attention(sub, kv, ring, rsc, idx, q_bits=OB.step_q_bits(sub))
     o = np.stack([att[0][0]])
     from oracle import formats as F

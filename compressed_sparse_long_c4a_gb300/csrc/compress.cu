@@ -15,8 +15,9 @@
 // (position P with (P+1) % ratio == 0) it also builds the entry.  Role 2 is
 // the window key (RoPE + encode + insert, thread p owning pair p as above).
 // Roles >= 3 are the queries' side of the pages' horizontal fusion (3), with
-// static warp roles: warp w of query group g normalises and rotates head
-// g * warps + w of the token, with no communication between warps.  (The
+// static warp roles: warp w of group g takes item g * warps + w of the
+// token, a query head (RMSNorm + RoPE) or an indexer-query head (RoPE +
+// per-head fp8 + head weight), with no communication between warps.  (The
 // pages give the window key one warp as well; here it keeps a CTA of its
 // own: with one warp per key the kernels after this launch ran 8 us slower
 // per 1M-context decode step, measured, cause not found.)
@@ -60,6 +61,17 @@ struct QuerySide {
   const uint16_t* q_in;
   uint16_t* q_out;
   const float* gamma;
+};
+
+struct IndexQuerySide {
+  RopeFreq rope;
+  int active, H, dim, rope_dims;
+  float w_mult;
+  const uint16_t* q_in;
+  uint8_t* q_out;
+  float* q_scale;
+  const float* w_in;
+  float* w_out;
 };
 
 struct BatchDev {
@@ -356,6 +368,47 @@ __device__ void query_head(const QuerySide& q, int t, int P, int h, int lane) {
   }
 }
 
+// The indexer query: rotate, then e4m3 with one scale per head (amax / 448),
+// and the head weight times w_mult; one warp per head, pairs as above.
+__device__ void index_query_head(const IndexQuerySide& q, int t, int P, int h, int lane) {
+  const int per = q.dim >> 6;
+  const int64_t row = (int64_t(t) * q.H + h) * q.dim;
+  const uint32_t* in = reinterpret_cast<const uint32_t*>(q.q_in + row);
+  const int first = q.dim - q.rope_dims;
+  float v0[kWarpPairsMax], v1[kWarpPairsMax];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < kWarpPairsMax; ++i) {
+    if (i < per) {
+      const int j = lane + 32 * i;
+      const uint32_t v = in[j];
+      float x0 = bf16_to_f32(uint16_t(v & 0xffffu)), x1 = bf16_to_f32(uint16_t(v >> 16));
+      if (2 * j >= first) {
+        float cs, sn;
+        rope_cos_sin(P, q.rope.inv[(2 * j - first) >> 1], &cs, &sn);
+        const float a0 = x0, a1 = x1;
+        x0 = a0 * cs - a1 * sn;
+        x1 = a0 * sn + a1 * cs;
+      }
+      v0[i] = x0;
+      v1[i] = x1;
+      amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
+    }
+  }
+  amax = warp_max(amax);
+  const float s = amax > 0.f ? amax / 448.f : 1.f;
+  uint16_t* out = reinterpret_cast<uint16_t*>(q.q_out + row);
+#pragma unroll
+  for (int i = 0; i < kWarpPairsMax; ++i)
+    if (i < per)
+      out[lane + 32 * i] = uint16_t(f32_to_e4m3(v0[i] / s)) | (uint16_t(f32_to_e4m3(v1[i] / s)) << 8);
+  if (lane == 0) {
+    const int64_t th = int64_t(t) * q.H + h;
+    q.q_scale[th] = s;
+    q.w_out[th] = q.w_in[th] * q.w_mult;
+  }
+}
+
 __device__ void window_token(const WindowSide& w, int t, int b, int P, int32_t* status) {
   __shared__ float red[32];
   const int p = threadIdx.x;
@@ -382,7 +435,7 @@ __device__ void window_token(const WindowSide& w, int t, int b, int P, int32_t* 
 }
 
 __global__ void compress_insert_kernel(BatchDev bt, CompressSide mainc, CompressSide ixc,
-                                       WindowSide win, QuerySide qs, int32_t* status) {
+                                       WindowSide win, QuerySide qs, IndexQuerySide iq, int32_t* status) {
   pdl_trigger();   // the next kernel may be scheduled now (it waits for this one in-kernel)
   const int t = blockIdx.x;
   const int role = blockIdx.y;
@@ -400,10 +453,13 @@ __global__ void compress_insert_kernel(BatchDev bt, CompressSide mainc, Compress
   if (role == 0 && mainc.active) compress_token(mainc, bt, t, b, P, ok, status);
   if (role == 1 && ixc.active) compress_token(ixc, bt, t, b, P, ok, status);
   if (role == 2 && win.active && ok) window_token(win, t, b, P, status);
-  if (role >= 3 && qs.active) {
-    // static warp roles: warp w of query group g takes head g * warps + w
-    const int h = (role - 3) * int(blockDim.x >> 5) + int(threadIdx.x >> 5);
-    if (h < qs.H) query_head(qs, t, P, h, threadIdx.x & 31);
+  if (role >= 3) {
+    // static warp roles: warp w of group g takes item g * warps + w, the
+    // query heads first, then the indexer query's heads
+    const int item = (role - 3) * int(blockDim.x >> 5) + int(threadIdx.x >> 5);
+    const int nq = qs.active ? qs.H : 0, ni = iq.active ? iq.H : 0;
+    if (item < nq) query_head(qs, t, P, item, threadIdx.x & 31);
+    else if (item < nq + ni) index_query_head(iq, t, P, item - nq, threadIdx.x & 31);
   }
 }
 
@@ -483,7 +539,18 @@ int compress_insert(const v4a_compress_args* a, cudaStream_t stream) {
     qs.active = 1; qs.H = q.num_heads; qs.dim = q.dim; qs.rope_dims = q.rope_dims; qs.eps = q.eps;
     qs.q_in = q.q_in; qs.q_out = q.q_out; qs.gamma = q.gamma;
   }
-  if (B.num_tokens == 0 || (!mc.active && !ic.active && !ws.active && !qs.active)) return V4A_OK;
+  IndexQuerySide iq{};
+  if (a->index_query) {
+    const v4a_index_query& q = *a->index_query;
+    if (!q.q_in || !q.q_out || !q.q_scale || !q.w_in || !q.w_out || q.num_heads < 1) return V4A_ERR_INVALID_ARG;
+    if (q.dim <= 0 || q.dim % 64 || q.dim > 1024) return V4A_ERR_UNSUPPORTED;
+    if (q.rope_dims < 0 || q.rope_dims > q.dim || q.rope_dims % 2) return V4A_ERR_INVALID_ARG;
+    if (q.rope_dims > 128) return V4A_ERR_UNSUPPORTED;
+    iq.rope = make_rope_freq(q.rope_dims, q.rope_theta);
+    iq.active = 1; iq.H = q.num_heads; iq.dim = q.dim; iq.rope_dims = q.rope_dims; iq.w_mult = q.w_mult;
+    iq.q_in = q.q_in; iq.q_out = q.q_out; iq.q_scale = q.q_scale; iq.w_in = q.w_in; iq.w_out = q.w_out;
+  }
+  if (B.num_tokens == 0 || (!mc.active && !ic.active && !ws.active && !qs.active && !iq.active)) return V4A_OK;
   int maxdim = 64;
   if (mc.active) maxdim = max(maxdim, mc.dim);
   if (ic.active) maxdim = max(maxdim, ic.dim);
@@ -491,13 +558,15 @@ int compress_insert(const v4a_compress_args* a, cudaStream_t stream) {
   // one thread per window position as well (128 for c128a compressors)
   if ((mc.active && mc.ratio == 128) || (ic.active && ic.ratio == 128)) threads = max(threads, 128);
   if (ws.active) threads = max(threads, ((ws.dim / 2) + 31) / 32 * 32);
-  // query heads: one warp each, in groups of 8 warps (or more) per CTA
-  if (qs.active) threads = max(threads, 256);
+  // query and indexer-query heads: one warp each, in groups of 8 warps (or
+  // more) per CTA
+  const int items = (qs.active ? qs.H : 0) + (iq.active ? iq.H : 0);
+  if (items > 0) threads = max(threads, 256);
   threads = max(threads, 64);
-  const int groups = qs.active ? (qs.H + threads / 32 - 1) / (threads / 32) : 0;
+  const int groups = (items + threads / 32 - 1) / (threads / 32);
   BatchDev bd{B.num_tokens, B.num_seqs, B.max_new_per_seq, B.seq_ids, B.positions};
   dim3 grid(B.num_tokens, 3 + groups);
-  compress_insert_kernel<<<grid, threads, 0, stream>>>(bd, mc, ic, ws, qs, a->status);
+  compress_insert_kernel<<<grid, threads, 0, stream>>>(bd, mc, ic, ws, qs, iq, a->status);
   return cudaGetLastError() == cudaSuccess ? V4A_OK : V4A_ERR_CUDA;
 }
 

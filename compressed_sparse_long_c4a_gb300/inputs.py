@@ -66,6 +66,7 @@ class LayerSpec:
     spare_blocks: int = 3      # unused physical blocks in the pool
     window_only: bool = False  # pure sliding-window layer: attention over the window alone
     q_prep: bool = False       # the step normalises and rotates the raw queries (fusion (3))
+    ix_q_prep: bool = False    # the step rotates + encodes the raw indexer query (fp8 query only)
 
     @property
     def entries_per_block(self) -> int:
@@ -74,6 +75,11 @@ class LayerSpec:
     @property
     def ix_rope_dims(self) -> int:
         return self.ix_dim // 2
+
+    @property
+    def ix_w_mult(self) -> float:
+        """Constant of the indexer weights' multiplication: 1/sqrt(H_I * d_I)."""
+        return float((self.ix_heads * self.ix_dim) ** -0.5) if self.ix_heads else 1.0
 
     @property
     def window(self) -> int:
@@ -201,6 +207,8 @@ class Case:
     o_in: torch.Tensor | None = None       # [T][H][D] bf16 (input of the output stage)
     q_raw: torch.Tensor | None = None      # [T][H][D] bf16 query before norm + RoPE (q_prep)
     gamma_q: torch.Tensor | None = None    # [D] fp32 query RMSNorm weight (q_prep)
+    q_i_raw: torch.Tensor | None = None    # [T][HI][dI] bf16 indexer query before RoPE + fp8 (ix_q_prep)
+    w_i_raw: torch.Tensor | None = None    # [T][HI] fp32 head weights before the multiplication (ix_q_prep)
 
 
 def make_case(spec: LayerSpec, seed: int = 0) -> Case:
@@ -284,6 +292,10 @@ def make_case(spec: LayerSpec, seed: int = 0) -> Case:
     if s.q_prep:
         case.q_raw = _bf16(_randn((T, s.heads, D), seed, 31, std=2.0))
         case.gamma_q = _randn((D,), seed, 32, std=0.1, mean=1.0)
+    if s.ix_q_prep:
+        assert s.ix_heads and s.ix_q_fmt == Q_FP8_HEAD
+        case.q_i_raw = _bf16(_randn((T, s.ix_heads, s.ix_dim), seed, 33))
+        case.w_i_raw = _rand((T, s.ix_heads), seed, 34)
     return case
 
 
@@ -362,6 +374,12 @@ def c4a_decode_1m_qprep() -> LayerSpec:
     """c4a_decode_b4_1m with the queries' RMSNorm + RoPE inside the step
     (the query side of the horizontal fusion with the window-key insert)."""
     return dataclasses.replace(c4a_decode_1m(), name="c4a_decode_b4_1m_qprep", q_prep=True)
+
+
+def c4a_decode_1m_ixprep() -> LayerSpec:
+    """c4a_decode_b4_1m with the indexer query's RoPE + per-head fp8 + weight
+    multiplication inside the step."""
+    return dataclasses.replace(c4a_decode_1m(), name="c4a_decode_b4_1m_ixprep", ix_q_prep=True)
 
 
 def c4a_decode_128k() -> LayerSpec:

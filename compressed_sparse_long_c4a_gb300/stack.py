@@ -36,7 +36,7 @@ from . import v4a
 
 # step inputs a layer keeps in its own tensors when its caches and rings are paged
 _STEP_INPUTS = ("seq_ids", "positions", "x", "gate", "bias", "gamma", "k_swa", "q", "x_i", "gate_i",
-                "bias_i", "gamma_i", "q_i", "q_i_scale", "w_i", "o_in", "window_only_idx", "q_raw", "gamma_q")
+                "bias_i", "gamma_i", "q_i", "q_i_scale", "w_i", "o_in", "window_only_idx", "q_raw", "gamma_q", "q_i_raw", "w_i_raw")
 
 
 def deepseek_v4_mix(n_c4a: int = 30, n_c128a: int = 31, n_swa: int = 0) -> list:

@@ -61,9 +61,15 @@ class Query(C.Structure):
                 ("dim", C.c_int32), ("rope_dims", C.c_int32), ("rope_theta", C.c_float)]
 
 
+class IndexQuery(C.Structure):
+    _fields_ = [("q_in", _p), ("q_out", _p), ("q_scale", _p), ("w_in", _p), ("w_out", _p), ("w_mult", C.c_float),
+                ("num_heads", C.c_int32), ("dim", C.c_int32), ("rope_dims", C.c_int32), ("rope_theta", C.c_float)]
+
+
 class CompressArgs(C.Structure):
     _fields_ = [("batch", Batch), ("main", C.POINTER(Compressor)), ("indexer", C.POINTER(Compressor)),
-                ("window", C.POINTER(Window)), ("status", _p), ("query", C.POINTER(Query))]
+                ("window", C.POINTER(Window)), ("status", _p), ("query", C.POINTER(Query)),
+                ("index_query", C.POINTER(IndexQuery))]
 
 
 class IndexArgs(C.Structure):
@@ -172,7 +178,7 @@ class DeviceLayer:
         for f in ("seq_ids", "positions", "block_table", "kv_pool", "x", "gate", "bias", "gamma",
                   "ring_x", "ring_gate", "k_swa", "swa_ring", "swa_scale", "q", "ix_pool", "x_i",
                   "gate_i", "bias_i", "gamma_i", "ring_x_i", "ring_gate_i", "q_i", "q_i_scale",
-                  "w_i", "o_in", "q_raw", "gamma_q"):
+                  "w_i", "o_in", "q_raw", "gamma_q", "q_i_raw", "w_i_raw"):
             v = getattr(case, f)
             if v is not None and v.numel() > 0:
                 t[f] = v.to(device).contiguous()
@@ -202,13 +208,15 @@ class DeviceLayer:
         return Cache(4, s.ix_dim, s.ix_rope_dims, s.theta, s.ix_fmt, _ptr(self.t["ix_pool"]),
                      s.num_blocks, _ptr(self.t["block_table"]), s.max_blocks)
 
-    def compress_args(self, parts=("main", "indexer", "window", "query")):
+    def compress_args(self, parts=("main", "indexer", "window", "query", "index_query")):
         """Arguments of v4a_compress_insert for the named parts (the others
         NULL: the call skips them).  "query" (layers with q_prep) normalises
-        and rotates q_raw into q, the attention's query."""
+        and rotates q_raw into q, the attention's query; "index_query"
+        (layers with ix_q_prep) rotates and encodes q_i_raw into q_i and
+        q_i_scale and scales w_i_raw into w_i, the indexer's inputs."""
         s, t, pg = self.spec, self.t, self.paged
         keep = []
-        main = ix = win = qry = None
+        main = ix = win = qry = ixq = None
         if "main" in parts:
             if pg:
                 main = Compressor(self.kv_cache(), _ptr(t["x"]), _ptr(t["gate"]), _ptr(t["bias"]),
@@ -238,8 +246,13 @@ class DeviceLayer:
             qry = Query(_ptr(t["q_raw"]), _ptr(t["q"]), _ptr(t["gamma_q"]), 1e-6, s.heads, s.dim, s.rope_dims,
                         s.theta)
             keep.append(qry)
+        if s.ix_q_prep and "index_query" in parts:
+            ixq = IndexQuery(_ptr(t["q_i_raw"]), _ptr(t["q_i"]), _ptr(t["q_i_scale"]), _ptr(t["w_i_raw"]),
+                             _ptr(t["w_i"]), s.ix_w_mult, s.ix_heads, s.ix_dim, s.ix_rope_dims, s.theta)
+            keep.append(ixq)
         a = CompressArgs(self.batch(), C.pointer(main) if main else None, C.pointer(ix) if ix else None,
-                         C.pointer(win) if win else None, _ptr(self.status), C.pointer(qry) if qry else None)
+                         C.pointer(win) if win else None, _ptr(self.status), C.pointer(qry) if qry else None,
+                         C.pointer(ixq) if ixq else None)
         return a, keep
 
     def index_args(self, out_idx: torch.Tensor) -> IndexArgs:
@@ -274,7 +287,7 @@ class DeviceLayer:
 # --------------------------------------------------------------------------
 
 
-def compress_insert(layer: DeviceLayer, stream=None, parts=("main", "indexer", "window", "query")):
+def compress_insert(layer: DeviceLayer, stream=None, parts=("main", "indexer", "window", "query", "index_query")):
     a, keep = layer.compress_args(parts)
     _check("v4a_compress_insert", lib().v4a_compress_insert(C.byref(a), _stream(stream)))
 
@@ -440,7 +453,7 @@ class Step:
             fork = torch.cuda.Event()
             joined = torch.cuda.Event()
             fork.record(cur)
-            compress_insert(L, cur, parts=("indexer",))
+            compress_insert(L, cur, parts=("indexer", "index_query"))
             if self.overlap == "select":
                 index_scores(L, self.idx, self.ws_index, cur)
                 fork.record(cur)

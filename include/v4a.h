@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define V4A_ABI_VERSION 4
+#define V4A_ABI_VERSION 5
 
 #if defined(__GNUC__)
 #define V4A_API __attribute__((visibility("default")))
@@ -207,6 +207,29 @@ typedef struct {
   float rope_theta;
 } v4a_query;
 
+/*
+ * The indexer query's preparation (vLLM page, Method details: the reused
+ * DeepSeek-V3.2 fusion of Q RoPE, quantisation and the weight
+ * multiplication), one warp per indexer head.  For token t at position P
+ * and head h: v = RoPE_P(q_in[t][h]) on the last rope_dims dims (interleaved
+ * pairs), q_scale[t][h] = amax|v| / 448 (1 when 0), q_out[t][h] =
+ * e4m3(v / q_scale[t][h]), w_out[t][h] = w_in[t][h] * w_mult.  The outputs
+ * are the V4A_Q_FP8_HEAD query, its scales and the head weights that
+ * v4a_index_topk takes.
+ */
+typedef struct {
+  const uint16_t* q_in;        /* [T][H_I][dim] bf16 */
+  uint8_t* q_out;              /* [T][H_I][dim] e4m3 */
+  float* q_scale;              /* [T][H_I] */
+  const float* w_in;           /* [T][H_I] */
+  float* w_out;                /* [T][H_I]; may equal w_in */
+  float w_mult;
+  int32_t num_heads;           /* H_I >= 1 */
+  int32_t dim;                 /* a multiple of 64, <= 1024 */
+  int32_t rope_dims;           /* even, <= min(dim, 128) */
+  float rope_theta;
+} v4a_index_query;
+
 typedef struct {
   v4a_batch batch;
   const v4a_compressor* main;     /* host pointer; may be NULL */
@@ -214,14 +237,16 @@ typedef struct {
   const v4a_window* window;       /* host pointer; may be NULL */
   int32_t* status;                /* optional device word */
   const v4a_query* query;         /* host pointer; may be NULL */
+  const v4a_index_query* index_query; /* host pointer; may be NULL */
 } v4a_compress_args;
 
 /*
  * Fused compressor + RMSNorm + RoPE + cache insert for the main and indexer
  * caches, and the queries' norm + RoPE beside the window keys' RoPE + insert
  * (vLLM page, Method details, fusions (1) and (3); appendix "exact position
- * ranges and causality").  One launch: one CTA per token for each
- * compressor, and warps that each take one query head or one window key.
+ * ranges and causality"), and the indexer query's RoPE + fp8 + weights.
+ * One launch: one CTA per token for each compressor and for the window key,
+ * then warps that each take one query head or one indexer-query head.
  * Returns V4A_ERR_RING_TOO_SMALL when a ring cannot hold the call's tokens
  * without overwriting positions a window still reads.
  */

@@ -84,11 +84,25 @@ def oracle_state_after_compress(case, main, ix, swa):
     return kv, ixp, ring, rsc
 
 
-def oracle_index(case, ix_pool, rows=None):
+def step_index_query(case):
+    """The indexer query, its scales and head weights a whole step's scan
+    reads: the oracle's own preparation (RoPE + per-head fp8 + weights) when
+    the step prepares them, else the case's inputs."""
     s = case.spec
-    return L.index_topk(case.seq_ids.numpy(), case.positions.numpy(),
-                        u16(case.q_i) if s.ix_q_fmt == 0 else u8(case.q_i),
-                        f64(case.q_i_scale), f64(case.w_i), s.ix_q_fmt == 1,
+    if s.ix_q_prep:
+        return L.index_query_prep(u16(case.q_i_raw), case.positions.numpy(), f64(case.w_i_raw), s.ix_w_mult,
+                                  s.ix_rope_dims, s.theta)
+    return (u16(case.q_i) if s.ix_q_fmt == 0 else u8(case.q_i)), f64(case.q_i_scale), f64(case.w_i)
+
+
+def oracle_index(case, ix_pool, rows=None, query=None):
+    """Indexer scores and top-k of the case's queries (query: a (q, q_scale,
+    weights) triple to use instead of the case's inputs)."""
+    s = case.spec
+    if query is None:
+        query = ((u16(case.q_i) if s.ix_q_fmt == 0 else u8(case.q_i)), f64(case.q_i_scale), f64(case.w_i))
+    q, qs, w = query
+    return L.index_topk(case.seq_ids.numpy(), case.positions.numpy(), q, qs, w, s.ix_q_fmt == 1,
                         ix_pool, s.ix_block_bytes, case.block_table.numpy(), s.ix_fmt,
                         s.ix_dim, s.topk, rows=rows)
 

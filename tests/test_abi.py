@@ -30,7 +30,7 @@ def test_exports_every_declared_symbol(lib):
     assert len(names) >= 18 and "v4a_pages_create" in names
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.v4a_abi_version() == 4
+    assert lib.v4a_abi_version() == 5
     for code in range(7):
         assert lib.v4a_status_string(code).decode() != "unknown status"
 
@@ -235,3 +235,24 @@ def test_host_validation_of_query_part(lib):
     assert run(dim=96) == 2 and run(dim=2048) == 2
     assert run(rope=63) == 1 and run(rope=600) == 1 and run(rope=256) == 2
     assert run(eps=-1.0) == 1
+
+
+def test_host_validation_of_index_query_part(lib):
+    """The indexer query's RoPE + fp8 + weights part: every pointer, a dim
+    that is a multiple of 64 up to 1024, even rope dims up to 128."""
+    spec = I.c4a_decode_1m()
+    L = _FakeLayer(spec)
+    b0 = L.batch()
+    b0.num_tokens = 0
+
+    def run(q_in=0x100, q_out=0x200, q_scale=0x300, w_in=0x400, w_out=0x500, heads=64, dim=128, rope=64):
+        q = v4a.IndexQuery(q_in, q_out, q_scale, w_in, w_out, 0.5, heads, dim, rope, 1e4)
+        a = v4a.CompressArgs(b0, None, None, None, None, None, C.pointer(q))
+        return lib.v4a_compress_insert(C.byref(a), None)
+
+    assert run() == 0 and run(w_out=0x400) == 0        # weights in place
+    for k in ("q_in", "q_out", "q_scale", "w_in", "w_out"):
+        assert run(**{k: None}) == 1, k
+    assert run(heads=0) == 1
+    assert run(dim=96) == 2 and run(dim=2048) == 2
+    assert run(rope=63) == 1 and run(rope=256) == 1 and run(dim=512, rope=256) == 2

