@@ -9,7 +9,9 @@
  * logical block size, compressor state as a sliding window, kernel fusions)
  * and Appendix (inverse RoPE, exact position ranges and causality, values of
  * k, why the short window).  Byte layouts of the fp8 indexer entry follow the
- * SGLang KV-pool article, section "DSA".
+ * SGLang KV-pool article, section "DSA", and the DeepSeek-V4 584-byte cache
+ * row its section "DeepSeek-V4".  The host page allocator (page-size
+ * buckets) is declared in v4a_pages.h.
  *
  * General rules for every entry point:
  *  - All pointers inside the argument structs are DEVICE pointers unless a
@@ -166,8 +168,8 @@ typedef struct {
   const float* bias;           /* [8] (c4a) or [128] (c128a) */
   const float* gamma;          /* [cache.dim] */
   float eps;                   /* RMSNorm epsilon (1e-6) */
-  uint16_t* ring_x;            /* [num_seqs][ring_cap][cache.dim] bf16 */
-  float* ring_gate;            /* [num_seqs][ring_cap] */
+  uint16_t* ring_x;            /* [num_seqs][ring_cap][cache.dim] bf16 (NULL with ring_pages) */
+  float* ring_gate;            /* [num_seqs][ring_cap] (NULL with ring_pages) */
   int32_t ring_cap;            /* >= window - 1 + max_new_per_seq (window 8 or 128) */
   const v4a_ring_pages* ring_pages; /* host pointer or NULL.  Non-NULL: the ring lives in
                                        these pages and ring_x / ring_gate are not read */
@@ -180,8 +182,8 @@ typedef struct {
   int32_t dim, rope_dims;
   float rope_theta;
   int32_t format;              /* V4A_KV_BF16 or V4A_KV_FP8_TOKEN */
-  void* ring;                  /* [num_seqs][ring_cap][dim] bf16 or e4m3 */
-  float* ring_scale;           /* [num_seqs][ring_cap] (fp8 only) */
+  void* ring;                  /* [num_seqs][ring_cap][dim] bf16 or e4m3 (NULL with ring_pages) */
+  float* ring_scale;           /* [num_seqs][ring_cap] (fp8 only; NULL with ring_pages) */
   int32_t ring_cap;            /* >= window_len - 1 + max_new_per_seq, else V4A_ERR_RING_TOO_SMALL */
   int32_t window_len;          /* the sliding window the ring serves (128); >= 1 */
   const v4a_ring_pages* ring_pages; /* host pointer or NULL.  Non-NULL: the ring lives in
@@ -337,8 +339,8 @@ typedef struct {
   v4a_cache kv;                /* main compressed cache */
   const int32_t* idx;          /* [T][k] or NULL */
   int32_t k;                   /* 1..65536 with idx; 0 with a non-NULL idx: window only */
-  const void* window;          /* [num_seqs][window_cap][kv.dim] */
-  const float* window_scale;   /* [num_seqs][window_cap] (fp8 window only) */
+  const void* window;          /* [num_seqs][window_cap][row bytes]; unread with window_pages */
+  const float* window_scale;   /* [num_seqs][window_cap] (fp8 window only); unread with window_pages */
   int32_t window_cap;          /* >= window_len - 1 + max_new_per_seq, else V4A_ERR_RING_TOO_SMALL */
   int32_t window_format;       /* V4A_KV_* */
   int32_t window_len;          /* 128 */
