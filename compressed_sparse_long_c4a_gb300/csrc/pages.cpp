@@ -11,6 +11,7 @@
 #include <algorithm>
 #include <climits>
 #include <cstdint>
+#include <memory>
 #include <new>
 #include <vector>
 
@@ -45,12 +46,10 @@ struct v4a_pages {
   }
 };
 
-extern "C" {
+namespace {
 
-V4A_API int v4a_pages_create(const v4a_pages_kind* kinds, int32_t num_kinds, int32_t max_seqs,
-                             int32_t max_blocks, int64_t budget_bytes, v4a_pages** out) {
-  if (!out) return V4A_ERR_INVALID_ARG;
-  *out = nullptr;
+int create(const v4a_pages_kind* kinds, int32_t num_kinds, int32_t max_seqs, int32_t max_blocks,
+           int64_t budget_bytes, v4a_pages** out) {
   if (!kinds || num_kinds < 1 || max_seqs < 1 || max_blocks < 1 || budget_bytes < 0) return V4A_ERR_INVALID_ARG;
 
   // the buckets: the distinct page sizes of the compressed caches, largest first
@@ -71,7 +70,7 @@ V4A_API int v4a_pages_create(const v4a_pages_kind* kinds, int32_t num_kinds, int
   std::sort(sizes.begin(), sizes.end(), [](int64_t a, int64_t b) { return a > b; });
   sizes.erase(std::unique(sizes.begin(), sizes.end()), sizes.end());
 
-  v4a_pages* p = new (std::nothrow) v4a_pages;
+  std::unique_ptr<v4a_pages> p(new (std::nothrow) v4a_pages);
   if (!p) return V4A_ERR_INVALID_ARG;
   p->max_seqs = max_seqs;
   p->max_blocks = max_blocks;
@@ -108,37 +107,49 @@ V4A_API int v4a_pages_create(const v4a_pages_kind* kinds, int32_t num_kinds, int
     if (offset > kMaxTableEntries) rc = V4A_ERR_INVALID_ARG;
     p->kinds.push_back(K);
   }
-  if (rc) { delete p; return rc; }
+  if (rc) return rc;
 
   // pool sizes: the rings of max_seqs sequences, then as many logical blocks
   // (one page per BLOCK kind and layer each) as the rest of the budget holds
   int64_t ring_bytes = 0, block_bytes = 0;
   for (const auto& B : p->buckets) {
-    if (B.ring_pages > 0 && int64_t(max_seqs) * B.ring_pages > INT32_MAX) { delete p; return V4A_ERR_INVALID_ARG; }
+    if (B.ring_pages > 0 && int64_t(max_seqs) * B.ring_pages > INT32_MAX) return V4A_ERR_INVALID_ARG;
     ring_bytes += int64_t(max_seqs) * B.ring_pages * B.page_bytes;
     block_bytes += B.block_pages * B.page_bytes;
   }
-  if (ring_bytes > budget_bytes) { delete p; return V4A_ERR_OUT_OF_PAGES; }
+  if (ring_bytes > budget_bytes) return V4A_ERR_OUT_OF_PAGES;
   int64_t nblk = (budget_bytes - ring_bytes) / block_bytes;
   nblk = std::min<int64_t>(nblk, int64_t(max_seqs) * max_blocks);
   for (const auto& B : p->buckets)
     if (B.block_pages > 0)
       nblk = std::min<int64_t>(nblk, (INT32_MAX - int64_t(max_seqs) * B.ring_pages) / B.block_pages);
-  if (nblk < 1) { delete p; return V4A_ERR_OUT_OF_PAGES; }
+  if (nblk < 1) return V4A_ERR_OUT_OF_PAGES;
+  for (auto& B : p->buckets) {
+    B.num_pages = int64_t(max_seqs) * B.ring_pages + nblk * B.block_pages;
+    B.free.resize(size_t(B.num_pages));
+    for (int64_t j = 0; j < B.num_pages; ++j) B.free[size_t(j)] = int32_t(B.num_pages - 1 - j);
+  }
+  p->tables.assign(size_t(offset), -1);
+  p->blocks.assign(size_t(max_seqs), -1);
+  *out = p.release();
+  return V4A_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+// No exception leaves the C ABI: an allocation failure while planning is
+// reported as V4A_ERR_INVALID_ARG with nothing created.
+V4A_API int v4a_pages_create(const v4a_pages_kind* kinds, int32_t num_kinds, int32_t max_seqs,
+                             int32_t max_blocks, int64_t budget_bytes, v4a_pages** out) {
+  if (!out) return V4A_ERR_INVALID_ARG;
+  *out = nullptr;
   try {
-    for (auto& B : p->buckets) {
-      B.num_pages = int64_t(max_seqs) * B.ring_pages + nblk * B.block_pages;
-      B.free.resize(size_t(B.num_pages));
-      for (int64_t j = 0; j < B.num_pages; ++j) B.free[size_t(j)] = int32_t(B.num_pages - 1 - j);
-    }
-    p->tables.assign(size_t(offset), -1);
-    p->blocks.assign(size_t(max_seqs), -1);
+    return create(kinds, num_kinds, max_seqs, max_blocks, budget_bytes, out);
   } catch (...) {
-    delete p;
     return V4A_ERR_INVALID_ARG;
   }
-  *out = p;
-  return V4A_OK;
 }
 
 V4A_API void v4a_pages_destroy(v4a_pages* p) { delete p; }

@@ -89,3 +89,20 @@ def test_paged_stack_places_every_slot_the_kernels_read():
                     if side is not None:
                         got = pool[base + info.slots * rb + 4 * j: base + info.slots * rb + 4 * j + 4]
                         assert torch.equal(got, side[b, p % cap].reshape(1).view(torch.uint8)), (name, b, p)
+
+
+def test_paged_stack_rejects_what_the_allocator_cannot_plan():
+    """One context per sequence in every layer (a logical block reserves the
+    same 256 positions everywhere), and at least one compressed cache to
+    size the pages; a c128a-only stack's one bucket (1,032-byte pages) cannot
+    hold rings, whose pages need 16-byte strides."""
+    import pytest
+    cases = S.shared_context_cases()
+    mixed = dict(cases, c128a=S.shrink_cases()["c128a"])          # another context
+    with pytest.raises(ValueError):
+        S.AttentionStack(["c4a", "c128a"], mixed, device="cpu", paged=True)
+    with pytest.raises(ValueError):
+        S.AttentionStack(["swa"], cases, device="cpu", paged=True)
+    from compressed_sparse_long_c4a_gb300 import v4a
+    with pytest.raises(v4a.V4AError):
+        S.AttentionStack(["c128a"], cases, device="cpu", paged=True)
