@@ -146,7 +146,8 @@ typedef struct {
 typedef struct {
   void* pool;                  /* page pool base; 16-byte aligned */
   int64_t num_pages;
-  int64_t page_bytes;          /* page stride: a multiple of 16, >= slots * (row bytes + 4) */
+  int64_t page_bytes;          /* page stride: a multiple of 16, >= slots * row bytes, plus
+                                  slots * 4 when the ring keeps an fp32 per slot */
   const int32_t* table;        /* [num_seqs][ring_cap / slots] page ids */
   int32_t slots;               /* slots per page; ring_cap must be a multiple of it */
 } v4a_ring_pages;
