@@ -463,11 +463,17 @@ __global__ void compress_insert_kernel(BatchDev bt, CompressSide mainc, Compress
   }
 }
 
+// True when pointer p is a multiple of `bytes` (the width of the loads and
+// stores the kernel makes through it).
+static bool aligned(const void* p, uintptr_t bytes) { return (reinterpret_cast<uintptr_t>(p) & (bytes - 1)) == 0; }
+
 static int fill_side(const v4a_compressor* c, bool indexer, CompressSide* s, int max_new) {
   *s = CompressSide{};
   if (!c) return V4A_OK;
   const v4a_cache& k = c->cache;
   if (!k.pool || !k.block_table || !c->x || !c->gate || !c->bias || !c->gamma) return V4A_ERR_INVALID_ARG;
+  // bf16 rows are read and written as element pairs
+  if (!aligned(c->x, 4) || (!c->ring_pages && c->ring_x && !aligned(c->ring_x, 4))) return V4A_ERR_INVALID_ARG;
   if (k.ratio != 4 && k.ratio != 128) return V4A_ERR_INVALID_ARG;
   if (indexer && k.ratio != 4) return V4A_ERR_UNSUPPORTED;
   if (k.dim <= 0 || k.dim % 64 || k.dim > 1024) return V4A_ERR_UNSUPPORTED;
@@ -512,7 +518,7 @@ int compress_insert(const v4a_compress_args* a, cudaStream_t stream) {
   WindowSide ws{};
   if (a->window) {
     const v4a_window& w = *a->window;
-    if (!w.k || w.ring_cap <= 0) return V4A_ERR_INVALID_ARG;
+    if (!w.k || w.ring_cap <= 0 || !aligned(w.k, 4)) return V4A_ERR_INVALID_ARG;
     if (w.dim <= 0 || w.dim % 64 || w.dim > 1024) return V4A_ERR_UNSUPPORTED;
     if (w.rope_dims < 0 || w.rope_dims > w.dim || w.rope_dims % 2) return V4A_ERR_INVALID_ARG;
     if (w.format != V4A_KV_BF16 && w.format != V4A_KV_FP8_TOKEN) return V4A_ERR_INVALID_ARG;
@@ -532,6 +538,7 @@ int compress_insert(const v4a_compress_args* a, cudaStream_t stream) {
   if (a->query) {
     const v4a_query& q = *a->query;
     if (!q.q_in || !q.q_out || !q.gamma || q.num_heads < 1) return V4A_ERR_INVALID_ARG;
+    if (!aligned(q.q_in, 4) || !aligned(q.q_out, 4) || !aligned(q.gamma, 8)) return V4A_ERR_INVALID_ARG;
     if (q.dim <= 0 || q.dim % 64 || q.dim > 1024) return V4A_ERR_UNSUPPORTED;
     if (q.rope_dims < 0 || q.rope_dims > q.dim || q.rope_dims % 2 || !(q.eps >= 0.f)) return V4A_ERR_INVALID_ARG;
     if (q.rope_dims > 128) return V4A_ERR_UNSUPPORTED;
@@ -543,6 +550,9 @@ int compress_insert(const v4a_compress_args* a, cudaStream_t stream) {
   if (a->index_query) {
     const v4a_index_query& q = *a->index_query;
     if (!q.q_in || !q.q_out || !q.q_scale || !q.w_in || !q.w_out || q.num_heads < 1) return V4A_ERR_INVALID_ARG;
+    if (!aligned(q.q_in, 4) || !aligned(q.q_out, 2) || !aligned(q.q_scale, 4) || !aligned(q.w_in, 4) ||
+        !aligned(q.w_out, 4))
+      return V4A_ERR_INVALID_ARG;
     if (q.dim <= 0 || q.dim % 64 || q.dim > 1024) return V4A_ERR_UNSUPPORTED;
     if (q.rope_dims < 0 || q.rope_dims > q.dim || q.rope_dims % 2) return V4A_ERR_INVALID_ARG;
     if (q.rope_dims > 128) return V4A_ERR_UNSUPPORTED;

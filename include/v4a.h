@@ -30,6 +30,13 @@
  *    No kernel traps and no kernel waits on another.
  *  - bf16 tensors are passed as uint16_t bit patterns; fp8 is OCP e4m3fn,
  *    fp4 is OCP e2m1 (element 2j in the low nibble of byte j).
+ *  - Rows are read and written in element pairs: bf16 row pointers must be
+ *    4-byte aligned, e4m3 rows written by the compressor launch 2-byte
+ *    aligned, fp32 pairs (the query norm's gamma) 8-byte aligned; pools,
+ *    rings and tables should start on 16 bytes (the tensor-core paths need
+ *    it and take another path or return V4A_ERR_UNSUPPORTED otherwise).
+ *    v4a_compress_insert returns V4A_ERR_INVALID_ARG for a misaligned input
+ *    or output row pointer.
  */
 #ifndef V4A_H
 #define V4A_H

@@ -256,3 +256,28 @@ def test_host_validation_of_index_query_part(lib):
     assert run(heads=0) == 1
     assert run(dim=96) == 2 and run(dim=2048) == 2
     assert run(rope=63) == 1 and run(rope=256) == 1 and run(dim=512, rope=256) == 2
+
+
+def test_misaligned_rows_are_refused_before_launch(lib):
+    """Row pointers the compressor launch reads or writes in pairs must be
+    aligned to the pair's width; a misaligned one is an invalid argument
+    (checked on the host with an empty batch, so nothing launches)."""
+    spec = I.c4a_decode_1m()
+    L = _FakeLayer(spec)
+    b0 = L.batch()
+    b0.num_tokens = 0
+    comp = v4a.Compressor(L.kv_cache(), 0x12, 0x20, 0x30, 0x40, 1e-6, 0x50, 0x60, 32)   # x on 2 bytes
+    assert lib.v4a_compress_insert(C.byref(v4a.CompressArgs(b0, C.pointer(comp), None, None, None)), None) == 1
+    comp.x = 0x10
+    assert lib.v4a_compress_insert(C.byref(v4a.CompressArgs(b0, C.pointer(comp), None, None, None)), None) == 0
+    win = v4a.Window(0x72, spec.dim, 64, 1e4, 0, 0x80, None, 128, 128)                  # k on 2 bytes
+    assert lib.v4a_compress_insert(C.byref(v4a.CompressArgs(b0, None, None, C.pointer(win), None)), None) == 1
+    q = v4a.Query(0x100, 0x200, 0x304, 1e-6, 128, 512, 64, 1e4)                         # gamma on 4 bytes
+    assert lib.v4a_compress_insert(C.byref(v4a.CompressArgs(b0, None, None, None, None, C.pointer(q))), None) == 1
+    q.gamma = 0x308
+    assert lib.v4a_compress_insert(C.byref(v4a.CompressArgs(b0, None, None, None, None, C.pointer(q))), None) == 0
+    iq = v4a.IndexQuery(0x100, 0x201, 0x300, 0x400, 0x500, 0.5, 64, 128, 64, 1e4)        # codes on 1 byte
+    a = v4a.CompressArgs(b0, None, None, None, None, None, C.pointer(iq))
+    assert lib.v4a_compress_insert(C.byref(a), None) == 1
+    iq.q_out = 0x202
+    assert lib.v4a_compress_insert(C.byref(a), None) == 0
