@@ -223,6 +223,10 @@ static int validate(const v4a_attn_args* a, bool need_out = true) {
   if (!a->batch.seq_ids || !a->batch.positions || !a->q || (need_out && !a->out) || !a->kv.pool ||
       !a->kv.block_table)
     return V4A_ERR_INVALID_ARG;
+  // key rows are read as 4-byte words (cache rows start on 4 bytes within a block)
+  if ((reinterpret_cast<uintptr_t>(a->kv.pool) & 3) ||
+      (!a->window_pages && (reinterpret_cast<uintptr_t>(a->window) & 3)))
+    return V4A_ERR_INVALID_ARG;
   RingDev wr;
   return attn_window_ring(a, &wr);
 }

@@ -281,3 +281,18 @@ def test_misaligned_rows_are_refused_before_launch(lib):
     assert lib.v4a_compress_insert(C.byref(a), None) == 1
     iq.q_out = 0x202
     assert lib.v4a_compress_insert(C.byref(a), None) == 0
+
+
+def test_attention_refuses_misaligned_key_rows(lib):
+    """Cache and window rows are read as 4-byte words: a pool or window that
+    does not start on 4 bytes is an invalid argument, refused before any
+    launch."""
+    spec = I.c4a_decode_1k()
+    L = _FakeLayer(spec)
+    kv = L.kv_cache()
+    kv.pool = 0x3002
+    a = v4a.AttnArgs(L.batch(), kv, 0x9000, spec.topk, 0x7000, None, spec.swa_cap, spec.swa_fmt, spec.swa,
+                     spec.heads, 0xA000, 0.1, 0xB000, None, None)
+    assert lib.v4a_sparse_attn(C.byref(a), 0xC000, 1 << 30, None) == 1
+    a.kv.pool, a.window = 0x3000, 0x7002
+    assert lib.v4a_sparse_attn(C.byref(a), 0xC000, 1 << 30, None) == 1
